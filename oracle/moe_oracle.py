@@ -1,0 +1,477 @@
+"""fp64 CPU oracle of the fine-grained Mixture-of-Experts layer, forward and backward.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, the package smoke check and the benchmark's CPU
+baseline leg may import this module. The product path never calls it and shares no code
+with it.
+
+What the layer computes (the method as the source pages state it):
+
+* "The whole stack, in the open" (Apex-3), section "What's inside", row "Fine-grained MoE":
+  a sigmoid router picks the top experts, a per-expert bias balances the load without a
+  loss term, and the experts run as grouped GEMMs.
+* KempnerForge README, section "Features" (Mixture-of-Experts bullet) and "AI / NeuroAI use
+  cases" (sparse architecture research): softmax top-k and DeepSeek-V3 sigmoid routers,
+  shared experts, fine-grained experts and router z-loss.
+* "How to train a large-scale Mixture-of-Experts model from scratch" (the handbook summary),
+  section 2.5 "First training of MoE": the router chooses 8 of 64 experts for each token,
+  tokens are sent to the chosen experts and the experts' outputs are returned; a SwiGLU
+  expert without bias has three weight matrices; the router logits are computed in fp32
+  (``--moe-router-dtype fp32``).
+
+The pages print no formula for the router, the gates, the bias rule, the z-loss or SwiGLU.
+The readings taken where they are silent are the workload definitions:
+
+* sigmoid router: s = sigmoid(l), choose the top k of s + b, lower expert index first on
+  exact ties; gates = chosen s renormalised to sum 1; b receives no gradient;
+* softmax router: p = softmax(l) over all experts, choose the top k of l (same order as p),
+  gates = chosen p without renormalisation; z-loss = coef * mean_t(logsumexp(l_t)^2);
+* SwiGLU expert: h = silu(x W_g^T) * (x W_u^T), y = h W_d^T;
+* shared expert: the same SwiGLU on every token, added with weight 1;
+* combine: out_t = sum_i g_ti * y_ti + y_shared_t;
+* bias update: b_e <- b_e + gamma * sign(T*k/E - c_e) in fp32, after backward.
+
+Everything is fp64 numpy; bf16 and fp32 inputs convert to fp64 exactly. Matrix products use
+numpy's matmul as a library step. Rows are processed per expert in the order of the
+definition; there is no blocking or fusion.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+SIGMOID = "sigmoid"
+SOFTMAX = "softmax"
+
+
+# ---------------------------------------------------------------------------------------
+# conversions
+
+def to64(t) -> np.ndarray:
+    """Exact fp64 copy of a host tensor or array (bf16 and fp32 are subsets of fp64)."""
+    if hasattr(t, "detach"):
+        t = t.detach().cpu().float().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z * sigmoid(z)
+
+
+# ---------------------------------------------------------------------------------------
+# router (forward)
+
+def router_logits(x: np.ndarray, W_r: np.ndarray) -> np.ndarray:
+    """l[t, e] = sum_j x[t, j] * W_r[e, j] (router logits, fp32 router per section 2.5)."""
+    return x @ W_r.T
+
+
+def _top_k_desc(score: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest scores per row, largest first, lower index first on ties."""
+    T, E = score.shape
+    index = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((index, -score), axis=-1)  # primary key: -score, then index
+    return order[:, :k]
+
+
+def route_sigmoid(logits: np.ndarray, b: np.ndarray, k: int) -> dict:
+    """Sigmoid router with selection bias (Apex-3 "Fine-grained MoE"; DeepSeek-V3 sigmoid
+    routing in KempnerForge "Features").
+
+    The bias only steers which experts are chosen; gates are the chosen sigmoid scores
+    renormalised to sum 1."""
+    s = sigmoid(logits)
+    v = s + b[None, :]
+    idx = _top_k_desc(v, k)
+    s_sel = np.take_along_axis(s, idx, axis=1)
+    gate = s_sel / s_sel.sum(axis=1, keepdims=True)
+    return {"idx": idx, "gate": gate, "score": s_sel, "select_value": v}
+
+
+def route_softmax(logits: np.ndarray, k: int, z_coef: float) -> dict:
+    """Softmax top-k router with router z-loss (KempnerForge "Features").
+
+    p = softmax over all experts; the k largest logits are chosen (the same order as p);
+    gates are the chosen p, not renormalised; z = z_coef * mean_t(lse_t^2)."""
+    m = logits.max(axis=1, keepdims=True)
+    ex = np.exp(logits - m)
+    denom = ex.sum(axis=1, keepdims=True)
+    p = ex / denom
+    lse = (m + np.log(denom))[:, 0]
+    idx = _top_k_desc(logits, k)
+    gate = np.take_along_axis(p, idx, axis=1)
+    z = z_coef * float(np.mean(lse * lse))
+    return {"idx": idx, "gate": gate, "score": gate.copy(), "p": p, "lse": lse, "z_loss": z,
+            "select_value": logits}
+
+
+def route(logits: np.ndarray, mode: str, k: int, b: np.ndarray | None = None,
+          z_coef: float = 0.0) -> dict:
+    if mode == SIGMOID:
+        r = route_sigmoid(logits, b, k)
+    elif mode == SOFTMAX:
+        r = route_softmax(logits, k, z_coef)
+    else:
+        raise ValueError(mode)
+    r["logits"] = logits
+    return r
+
+
+def near_tie_tokens(select_value: np.ndarray, k: int, gap: float = 1e-6) -> np.ndarray:
+    """Tokens whose sorted top-(k+1) selection values have an adjacent gap below ``gap``.
+
+    On such tokens an fp32 and an fp64 evaluation of the selection value may order the
+    experts differently; they are reported and left out of bit-exact index checks."""
+    E = select_value.shape[1]
+    kk = min(k + 1, E)
+    srt = -np.sort(-select_value, axis=1)[:, :kk]
+    if kk < 2:
+        return np.zeros(select_value.shape[0], dtype=bool)
+    return (np.abs(np.diff(srt, axis=1)) < gap).any(axis=1)
+
+
+def select_brute_force(v_row: np.ndarray, k: int) -> tuple:
+    """Chosen expert set of one token by enumerating every k-subset: the set with the
+    largest total selection value; among equal totals, the lexicographically smallest
+    sorted index tuple. Returns the indices ordered by descending value, lower index
+    first on ties. Only for tiny E."""
+    E = v_row.shape[0]
+    best, best_sum = None, -math.inf
+    for comb in itertools.combinations(range(E), k):
+        tot = float(sum(v_row[list(comb)]))
+        if tot > best_sum:
+            best, best_sum = comb, tot
+    return tuple(sorted(best, key=lambda e: (-v_row[e], e)))
+
+
+# ---------------------------------------------------------------------------------------
+# dispatch (token permutation)
+
+def dispatch(idx: np.ndarray, E: int) -> dict:
+    """Send every (token, slot) to its expert: per-expert counts, exclusive-scan offsets,
+    and rows ordered by (expert, token), which is unique because a token's k experts are
+    distinct (section 2.5: tokens must be sent to the selected experts)."""
+    T, k = idx.shape
+    counts = np.bincount(idx.reshape(-1), minlength=E).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    tok = np.repeat(np.arange(T), k)
+    slot = np.tile(np.arange(k), T)
+    e_flat = idx.reshape(-1)
+    order = np.lexsort((tok, e_flat))  # primary key expert, then token
+    perm_token = tok[order]
+    perm_slot = slot[order]
+    slot_to_row = np.empty((T, k), dtype=np.int64)
+    slot_to_row[perm_token, perm_slot] = np.arange(T * k)
+    return {"counts": counts, "offsets": offsets, "perm_token": perm_token,
+            "perm_slot": perm_slot, "slot_to_row": slot_to_row}
+
+
+# ---------------------------------------------------------------------------------------
+# experts and combine
+
+def swiglu_expert(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray):
+    """One bias-free SwiGLU expert (three weight matrices, section 2.5):
+    a = x W_g^T, u = x W_u^T, h = silu(a) * u, y = h W_d^T."""
+    a = rows @ W_g.T
+    u = rows @ W_u.T
+    h = silu(a) * u
+    y = h @ W_d.T
+    return a, u, h, y
+
+
+def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d) -> dict:
+    """Each expert applied to its own contiguous segment of the permuted rows."""
+    N = x_perm.shape[0]
+    f = W_g.shape[1]
+    d_out = W_d.shape[1]
+    A = np.zeros((N, f)); U = np.zeros((N, f)); H = np.zeros((N, f)); Y = np.zeros((N, d_out))
+    for e in range(W_g.shape[0]):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            A[lo:hi], U[lo:hi], H[lo:hi], Y[lo:hi] = swiglu_expert(x_perm[lo:hi], W_g[e], W_u[e], W_d[e])
+    return {"A": A, "U": U, "H": H, "Y_perm": Y}
+
+
+def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
+            Y_shared: np.ndarray | None) -> np.ndarray:
+    """out_t = sum over slots of gate * expert output, plus the shared expert's output
+    (section 2.5: each expert's output is returned to the token)."""
+    T, k = gate.shape
+    out = np.zeros((T, Y_perm.shape[1]))
+    for i in range(k):
+        out += gate[:, i:i + 1] * Y_perm[slot_to_row[:, i]]
+    if Y_shared is not None:
+        out += Y_shared
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# whole layer, forward
+
+def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
+                  logits: np.ndarray | None = None, idx: np.ndarray | None = None) -> dict:
+    """Full forward of the layer from fp64 copies of the inputs.
+
+    ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
+    that index checks compare selections made from identical logits). ``idx`` replaces
+    the chosen experts (used so value checks do not cascade from a near-tie)."""
+    x = inp["x"]
+    E = inp["W_r"].shape[0]
+    if logits is None:
+        logits = router_logits(x, inp["W_r"])
+    r = route(logits, mode, k, inp.get("b"), z_coef)
+    if idx is not None:
+        r = _regate(r, logits, idx, mode, inp.get("b"), z_coef)
+    disp = dispatch(r["idx"], E)
+    x_perm = x[disp["perm_token"]]
+    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"])
+    shared = None
+    if "Ws_g" in inp:
+        shared = swiglu_expert(x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])
+    out = combine(ex["Y_perm"], r["gate"], disp["slot_to_row"], None if shared is None else shared[3])
+    res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
+           "z_coef": z_coef}
+    if shared is not None:
+        res["shared"] = dict(zip("AUHY", shared))
+    return res
+
+
+def _regate(r: dict, logits, idx, mode, b, z_coef) -> dict:
+    """Gates and scores for a given choice of experts (replay of a selection)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    r = dict(r)
+    r["idx"] = idx
+    if mode == SIGMOID:
+        s = sigmoid(logits)
+        s_sel = np.take_along_axis(s, idx, axis=1)
+        r["score"] = s_sel
+        r["gate"] = s_sel / s_sel.sum(axis=1, keepdims=True)
+    else:
+        r["gate"] = np.take_along_axis(r["p"], idx, axis=1)
+        r["score"] = r["gate"].copy()
+    return r
+
+
+def layer_forward_dense_masked(inp: dict, mode: str, k: int, z_coef: float = 0.0) -> np.ndarray:
+    """Brute-force forward: every expert on every token, then out = sum_e m[t, e] y_e(x_t)
+    with m the gate of a chosen expert and 0 elsewhere. No permutation at all; an
+    independent path to the same definition."""
+    x = inp["x"]
+    logits = router_logits(x, inp["W_r"])
+    r = route(logits, mode, k, inp.get("b"), z_coef)
+    T = x.shape[0]
+    E = inp["W_r"].shape[0]
+    m = np.zeros((T, E))
+    for i in range(k):
+        m[np.arange(T), r["idx"][:, i]] = r["gate"][:, i]
+    out = np.zeros_like(x)
+    for e in range(E):
+        _, _, _, y = swiglu_expert(x, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e])
+        out += m[:, e:e + 1] * y
+    if "Ws_g" in inp:
+        out += swiglu_expert(x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])[3]
+    return out
+
+
+def loss(fwd: dict, dY: np.ndarray) -> float:
+    """Scalar whose gradient the backward computes: <out, dY> plus the z-loss (weight 1)."""
+    L = float(np.sum(fwd["out"] * dY))
+    if fwd["mode"] == SOFTMAX:
+        L += fwd["z_loss"]
+    return L
+
+
+# ---------------------------------------------------------------------------------------
+# backward
+
+def swiglu_backward(dh: np.ndarray, a: np.ndarray, u: np.ndarray):
+    """d/da and d/du of h = silu(a) * u."""
+    sa = sigmoid(a)
+    da = dh * u * sa * (1.0 + a * (1.0 - sa))
+    du = dh * silu(a)
+    return da, du
+
+
+def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndarray,
+                    mode: str, z_coef: float, T_norm: int | None = None) -> dict:
+    """Gradient of the loss with respect to the router logits, W_r and x, given the
+    gradient with respect to the gates. No gradient flows through the choice of experts
+    or into the bias. ``T_norm`` is the token count of the z-loss mean (default: the rows
+    given)."""
+    idx, gate = route_res["idx"], route_res["gate"]
+    T, k = idx.shape
+    if T_norm is None:
+        T_norm = T
+    E = W_r.shape[0]
+    dl = np.zeros((T, E))
+    rows = np.arange(T)
+    if mode == SIGMOID:
+        s = route_res["score"]
+        S = s.sum(axis=1, keepdims=True)
+        gdg = (gate * dg).sum(axis=1, keepdims=True)
+        ds = (dg - gdg) / S
+        for i in range(k):
+            dl[rows, idx[:, i]] += ds[:, i] * s[:, i] * (1.0 - s[:, i])
+    else:
+        p, lse = route_res["p"], route_res["lse"]
+        pdg = (gate * dg).sum(axis=1, keepdims=True)
+        sel = np.zeros((T, E))
+        for i in range(k):
+            sel[rows, idx[:, i]] = dg[:, i]
+        dl = p * (sel - pdg) + (2.0 * z_coef / T_norm) * lse[:, None] * p
+    return {"dlogits": dl, "dW_r": dl.T @ x, "dx_r": dl @ W_r}
+
+
+def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
+    """Gradients of ``loss`` with respect to x, every weight and the router."""
+    idx, gate, s2r = fwd["idx"], fwd["gate"], fwd["slot_to_row"]
+    T, k = idx.shape
+    E = inp["W_r"].shape[0]
+    offs = fwd["offsets"]
+    tok = fwd["perm_token"]
+    slot = fwd["perm_slot"]
+    # combine backward
+    dY_perm = gate[tok, slot][:, None] * dY[tok]
+    dg = np.zeros((T, k))
+    for i in range(k):
+        dg[:, i] = np.sum(dY * fwd["Y_perm"][s2r[:, i]], axis=1)
+    # experts backward
+    N, d = fwd["X_perm"].shape
+    f = inp["W_g"].shape[1]
+    dX_perm = np.zeros((N, d))
+    dW_g = np.zeros_like(inp["W_g"]); dW_u = np.zeros_like(inp["W_u"]); dW_d = np.zeros_like(inp["W_d"])
+    dA = np.zeros((N, f)); dU = np.zeros((N, f))
+    for e in range(E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo:
+            continue
+        dH = dY_perm[lo:hi] @ inp["W_d"][e]
+        dA[lo:hi], dU[lo:hi] = swiglu_backward(dH, fwd["A"][lo:hi], fwd["U"][lo:hi])
+        dW_d[e] = dY_perm[lo:hi].T @ fwd["H"][lo:hi]
+        dW_g[e] = dA[lo:hi].T @ fwd["X_perm"][lo:hi]
+        dW_u[e] = dU[lo:hi].T @ fwd["X_perm"][lo:hi]
+        dX_perm[lo:hi] = dA[lo:hi] @ inp["W_g"][e] + dU[lo:hi] @ inp["W_u"][e]
+    dx = np.zeros((T, d))
+    for i in range(k):
+        dx += dX_perm[s2r[:, i]]
+    res = {"dY_perm": dY_perm, "dg": dg, "dA": dA, "dU": dU, "dX_perm": dX_perm,
+           "dW_g": dW_g, "dW_u": dW_u, "dW_d": dW_d}
+    if "shared" in fwd:
+        sh = fwd["shared"]
+        dHs = dY @ inp["Ws_d"]
+        dAs, dUs = swiglu_backward(dHs, sh["A"], sh["U"])
+        res["dWs_d"] = dY.T @ sh["H"]
+        res["dWs_g"] = dAs.T @ inp["x"]
+        res["dWs_u"] = dUs.T @ inp["x"]
+        res["dx_shared"] = dAs @ inp["Ws_g"] + dUs @ inp["Ws_u"]
+        dx += res["dx_shared"]
+    rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"])
+    res.update(rb)
+    dx += rb["dx_r"]
+    res["dx"] = dx
+    return res
+
+
+# ---------------------------------------------------------------------------------------
+# aux-loss-free bias update
+
+def bias_update(counts: np.ndarray, b: np.ndarray, T: int, k: int, gamma: float) -> np.ndarray:
+    """b_e <- b_e + gamma * sign(mean load - c_e), evaluated in fp32 with one rounding.
+
+    Under-loaded experts get a larger bias and so are chosen more often; the bias never
+    enters a loss (Apex-3 "Fine-grained MoE": the bias balances the load without a loss
+    term). mean load = T*k/E."""
+    E = b.shape[0]
+    mean = np.float64(T) * k / E
+    sgn = np.sign(mean - counts.astype(np.float64)).astype(np.float32)
+    return (np.asarray(b, dtype=np.float32) + np.float32(gamma) * sgn).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------------------
+# sampled evaluation for workloads too large to run whole on the CPU
+
+def token_forward(inp: dict, t: int, experts, gates) -> np.ndarray:
+    """out_t for one token given its chosen experts and gates."""
+    x_t = inp["x"][t:t + 1]
+    out = np.zeros((1, inp["x"].shape[1]))
+    for e, g in zip(experts, gates):
+        out += g * swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e])[3]
+    if "Ws_g" in inp:
+        out += swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])[3]
+    return out[0]
+
+
+def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, k: int,
+                   dY_t: np.ndarray, z_coef: float, T: int) -> dict:
+    """Gradient rows of one token: dx_t, dg_t and the router logit gradient for it.
+
+    A token's dx depends only on its own routing, experts and upstream gradient, so it can
+    be evaluated alone. ``T`` is the batch size that normalises the z-loss mean."""
+    x_t = inp["x"][t:t + 1]
+    lg = logits_t[None, :]
+    r = route(lg, mode, k, inp.get("b"), z_coef)
+    r = _regate(r, lg, np.asarray([experts]), mode, inp.get("b"), z_coef)
+    gate = r["gate"][0]
+    dx = np.zeros((1, x_t.shape[1]))
+    dg = np.zeros((1, k))
+    for i, e in enumerate(experts):
+        a, u, h, y = swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e])
+        dg[0, i] = float(np.sum(dY_t * y[0]))
+        dH = (gate[i] * dY_t[None, :]) @ inp["W_d"][e]
+        dA, dU = swiglu_backward(dH, a, u)
+        dx += dA @ inp["W_g"][e] + dU @ inp["W_u"][e]
+    if "Ws_g" in inp:
+        a, u, h, y = swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])
+        dA, dU = swiglu_backward(dY_t[None, :] @ inp["Ws_d"], a, u)
+        dx += dA @ inp["Ws_g"] + dU @ inp["Ws_u"]
+    rb = router_backward(dg, r, x_t, inp["W_r"], mode, z_coef, T_norm=T)
+    dx += rb["dx_r"]
+    return {"dx": dx[0], "dg": dg[0], "dlogits": rb["dlogits"][0]}
+
+
+def expert_weight_grad_entries(inp: dict, e: int, tokens: np.ndarray, slots_gate: np.ndarray,
+                               dY: np.ndarray, entries_d, entries_gu) -> dict:
+    """Chosen entries of dW_d[e], dW_g[e] and dW_u[e].
+
+    ``tokens`` are the tokens routed to expert e in ascending order and ``slots_gate`` their
+    gates for e. ``entries_d`` lists (i, j) of dW_d[e][i, j] = sum_p dY_perm[p, i] h[p, j];
+    ``entries_gu`` lists (j, i) of dW_g[e][j, i] = sum_p dA[p, j] x_perm[p, i] (and dW_u)."""
+    X = inp["x"][tokens]
+    dYp = slots_gate[:, None] * dY[tokens]
+    Wg, Wu, Wd = inp["W_g"][e], inp["W_u"][e], inp["W_d"][e]
+    res = {"dW_d": [], "dW_g": [], "dW_u": []}
+    for (i, j) in entries_d:
+        a = X @ Wg[j]
+        u = X @ Wu[j]
+        h = silu(a) * u
+        res["dW_d"].append(float(np.sum(dYp[:, i] * h)))
+    for (j, i) in entries_gu:
+        a = X @ Wg[j]
+        u = X @ Wu[j]
+        dh = dYp @ Wd[:, j]
+        da, du = swiglu_backward(dh, a, u)
+        res["dW_g"].append(float(np.sum(da * X[:, i])))
+        res["dW_u"].append(float(np.sum(du * X[:, i])))
+    return res
+
+
+def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu) -> dict:
+    """Chosen entries of the shared expert's weight gradients (every token, weight 1)."""
+    X = inp["x"]
+    Wg, Wu, Wd = inp["Ws_g"], inp["Ws_u"], inp["Ws_d"]
+    res = {"dWs_d": [], "dWs_g": [], "dWs_u": []}
+    for (i, j) in entries_d:
+        h = silu(X @ Wg[j]) * (X @ Wu[j])
+        res["dWs_d"].append(float(np.sum(dY[:, i] * h)))
+    for (j, i) in entries_gu:
+        a = X @ Wg[j]
+        u = X @ Wu[j]
+        da, du = swiglu_backward(dY @ Wd[:, j], a, u)
+        res["dWs_g"].append(float(np.sum(da * X[:, i])))
+        res["dWs_u"].append(float(np.sum(du * X[:, i])))
+    return res

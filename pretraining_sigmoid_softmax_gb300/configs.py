@@ -1,0 +1,71 @@
+"""The five synthetic MoE-layer workloads, as shapes and switches only.
+
+Each workload is one fine-grained Mixture-of-Experts layer of a decoder LLM training step
+(the "Fine-grained MoE" row of "The whole stack, in the open", section "What's inside": a
+sigmoid router picks the top experts, a per-expert bias balances the load without a loss
+term, and experts run as grouped GEMMs). The softmax top-k router with router z-loss is the
+KempnerForge README's other router ("Features", Mixture-of-Experts bullet).
+
+Nothing here computes any part of the layer.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+
+@dataclass(frozen=True)
+class MoEConfig:
+    name: str
+    T: int            # tokens in the step (batch x sequence)
+    d: int            # d_model
+    E: int            # routed experts
+    k: int            # experts chosen per token
+    f: int            # routed expert SwiGLU width (d_ff)
+    f_shared: int     # always-on shared expert width, 0 = no shared expert
+    mode: str         # "sigmoid" (bias-steered selection, renormalised gates) or "softmax"
+    seed: int
+    backward: bool    # forward + backward when true, forward only otherwise
+    bias_update: bool # aux-loss-free bias update after backward
+    gamma: float = 0.001   # bias update step
+    z_coef: float = 0.0    # router z-loss coefficient (softmax mode)
+    zipf: bool = False     # skewed expert popularity with a block of never-chosen experts
+
+    @property
+    def N(self) -> int:
+        """Routed rows: every token is sent to k experts."""
+        return self.T * self.k
+
+    @property
+    def mode_id(self) -> int:
+        return 0 if self.mode == "sigmoid" else 1
+
+    def gemm_flops(self) -> float:
+        """Algorithmic grouped-GEMM FLOPs of one step (routed + shared).
+
+        A SwiGLU expert has three bias-free d x f matrices, so one row costs 3 GEMVs of
+        2*d*f FLOPs forward; backward is twice the forward (data and weight gradients)."""
+        fwd = 6.0 * self.N * self.d * self.f + 6.0 * self.T * self.d * self.f_shared
+        return fwd * (3.0 if self.backward else 1.0)
+
+    def with_(self, **kw) -> "MoEConfig":
+        return replace(self, **kw)
+
+
+# Tiny forward-only parity workload.
+C0 = MoEConfig("tiny_fwd_T512_d256_E8_k2_f128", T=512, d=256, E=8, k=2, f=128, f_shared=0,
+               mode="sigmoid", seed=0, backward=False, bias_update=False)
+# Fine-grained sigmoid-routed layer with one shared expert and the bias update.
+C1 = MoEConfig("finegrained_T8192_d1024_E64_k8_f256_shared512", T=8192, d=1024, E=64, k=8,
+               f=256, f_shared=512, mode="sigmoid", seed=1, backward=True, bias_update=True)
+# Softmax top-k without renormalisation, router z-loss 1e-3.
+C2 = MoEConfig("softmax_zloss_T16384_d2048_E32_k4_f1024", T=16384, d=2048, E=32, k=4, f=1024,
+               f_shared=0, mode="softmax", seed=2, backward=True, bias_update=False,
+               z_coef=1e-3)
+# Skewed expert load: ragged and empty grouped-GEMM segments.
+C3 = MoEConfig("skewed_T32768_d2048_E128_k8_f768", T=32768, d=2048, E=128, k=8, f=768,
+               f_shared=0, mode="sigmoid", seed=3, backward=True, bias_update=False, zipf=True)
+# Large fine-grained layer with a shared expert and the bias update.
+C4 = MoEConfig("large_T65536_d4096_E64_k8_f1536_shared3072", T=65536, d=4096, E=64, k=8,
+               f=1536, f_shared=3072, mode="sigmoid", seed=4, backward=True, bias_update=True)
+
+CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4}

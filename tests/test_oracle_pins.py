@@ -1,0 +1,309 @@
+"""The fp64 oracle pinned to facts outside itself: brute force on tiny inputs, closed forms
+worked by hand, invariants of the method, finite differences and the pages' own
+parameter arithmetic. CPU only."""
+import json
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from pretraining_sigmoid_softmax_gb300.configs import MoEConfig
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as fh:
+        return json.load(fh)
+
+
+def _tiny_inputs(rng, T, d, E, f, fs=0, b_scale=0.05):
+    inp = {
+        "x": rng.standard_normal((T, d)),
+        "W_r": rng.standard_normal((E, d)) / math.sqrt(d),
+        "b": rng.uniform(-b_scale, b_scale, E),
+        "W_g": rng.standard_normal((E, f, d)) / math.sqrt(d),
+        "W_u": rng.standard_normal((E, f, d)) / math.sqrt(d),
+        "W_d": rng.standard_normal((E, d, f)) / math.sqrt(f),
+    }
+    if fs:
+        inp["Ws_g"] = rng.standard_normal((fs, d)) / math.sqrt(d)
+        inp["Ws_u"] = rng.standard_normal((fs, d)) / math.sqrt(d)
+        inp["Ws_d"] = rng.standard_normal((d, fs)) / math.sqrt(fs)
+    return inp
+
+
+# ----------------------------------------------------------------------------- selection
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 8])
+def test_selection_matches_subset_enumeration_with_exact_ties(k):
+    """Dyadic logits (exact sums) with many exact ties: the softmax router's choice equals
+    the k-subset of largest total, lexicographically smallest among equal totals."""
+    rng = np.random.default_rng(10 + k)
+    E = 8
+    logits = rng.integers(-3, 4, size=(64, E)).astype(np.float64) / 4.0
+    r = O.route_softmax(logits, k, 0.0)
+    for t in range(64):
+        assert tuple(r["idx"][t]) == O.select_brute_force(logits[t], k)
+
+
+@pytest.mark.parametrize("k", [1, 2, 4])
+def test_sigmoid_selection_uses_bias_and_breaks_ties_low(k):
+    """Zero logits make every sigmoid score exactly 0.5, so the dyadic bias alone decides
+    (with exact ties); the chosen set is the subset enumeration's."""
+    rng = np.random.default_rng(20 + k)
+    E = 8
+    logits = np.zeros((32, E))
+    for t in range(32):
+        b = rng.integers(-2, 3, size=E).astype(np.float64) / 64.0
+        r = O.route_sigmoid(logits[t:t + 1], b, k)
+        assert tuple(r["idx"][0]) == O.select_brute_force(0.5 + b, k)
+        np.testing.assert_allclose(r["gate"][0], np.full(k, 1.0 / k), rtol=0, atol=1e-15)
+
+
+def test_sigmoid_selection_random_against_enumeration():
+    rng = np.random.default_rng(3)
+    E, k = 8, 3
+    logits = rng.standard_normal((64, E))
+    b = rng.uniform(-0.05, 0.05, E)
+    r = O.route_sigmoid(logits, b, k)
+    v = 1.0 / (1.0 + np.exp(-logits)) + b
+    for t in range(64):
+        assert tuple(r["idx"][t]) == O.select_brute_force(v[t], k)
+
+
+def test_bias_steers_selection_but_not_gates():
+    """A large bias forces an expert in; its gate is still its own renormalised score."""
+    logits = np.array([[2.0, 1.0, 0.0, -1.0]])
+    b = np.array([0.0, 0.0, 0.0, 10.0])
+    r = O.route_sigmoid(logits, b, 2)
+    assert list(r["idx"][0]) == [3, 0]
+    s = [1 / (1 + math.exp(1.0)), 1 / (1 + math.exp(-2.0))]
+    np.testing.assert_allclose(r["gate"][0], [s[0] / (s[0] + s[1]), s[1] / (s[0] + s[1])], rtol=1e-15)
+
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_all_equal_logits(mode):
+    E, k = 8, 3
+    logits = np.full((5, E), 0.7)
+    r = O.route(logits, mode, k, np.zeros(E), 0.0)
+    assert (r["idx"] == np.arange(k)).all()
+    want = 1.0 / k if mode == "sigmoid" else 1.0 / E
+    np.testing.assert_allclose(r["gate"], want, rtol=1e-15)
+
+
+def test_z_loss_closed_form_at_zero_logits():
+    g = _gold("closed_forms.json")["z_loss_uniform"]
+    r = O.route_softmax(np.zeros((7, g["E"])), 2, g["coef"])
+    assert r["z_loss"] == pytest.approx(g["z"], rel=1e-14)
+    np.testing.assert_allclose(r["lse"], math.log(g["E"]), rtol=1e-15)
+
+
+def test_softmax_gates_are_unrenormalised_probabilities():
+    rng = np.random.default_rng(4)
+    logits = rng.standard_normal((16, 6))
+    r = O.route_softmax(logits, 2, 0.0)
+    np.testing.assert_allclose(r["p"].sum(1), 1.0, rtol=1e-14)
+    assert (r["gate"].sum(1) < 1.0).all()
+    # the chosen probabilities are the two largest probabilities
+    top2 = -np.sort(-r["p"], axis=1)[:, :2]
+    np.testing.assert_allclose(r["gate"], top2, rtol=0, atol=0)
+
+
+def test_k_equals_E_chooses_everything():
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((9, 5))
+    r = O.route_sigmoid(logits, np.zeros(5), 5)
+    assert (np.sort(r["idx"], 1) == np.arange(5)).all()
+    s = 1 / (1 + np.exp(-logits))
+    np.testing.assert_allclose(np.sort(r["gate"], 1), np.sort(s / s.sum(1, keepdims=True), 1), rtol=1e-14)
+
+
+def test_near_tie_detector():
+    v = np.array([[0.9, 0.9 + 5e-7, 0.1, 0.0], [0.9, 0.8, 0.7, 0.6]])
+    assert list(O.near_tie_tokens(v, 2)) == [True, False]
+
+
+# ------------------------------------------------------------------------------ dispatch
+
+def test_dispatch_invariants_and_round_trip():
+    rng = np.random.default_rng(6)
+    T, E, k, d = 200, 13, 4, 7
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    D = O.dispatch(idx, E)
+    assert D["counts"].sum() == T * k
+    assert (np.diff(D["offsets"]) >= 0).all() and D["offsets"][-1] == T * k
+    # rows sorted by (expert, token), strictly
+    e_of_row = idx[D["perm_token"], D["perm_slot"]]
+    key = e_of_row * T + D["perm_token"]
+    assert (np.diff(key) > 0).all()
+    for e in range(E):
+        assert (e_of_row[D["offsets"][e]:D["offsets"][e + 1]] == e).all()
+    # slot_to_row is a bijection onto the rows
+    assert sorted(D["slot_to_row"].reshape(-1).tolist()) == list(range(T * k))
+    x = rng.standard_normal((T, d))
+    x_perm = x[D["perm_token"]]
+    for i in range(k):
+        assert (x_perm[D["slot_to_row"][:, i]] == x).all()
+
+
+def test_dispatch_empty_experts():
+    idx = np.array([[0, 3], [3, 0], [0, 3]])
+    D = O.dispatch(idx, 5)
+    assert D["counts"].tolist() == [3, 0, 0, 3, 0]
+    assert D["offsets"].tolist() == [0, 3, 3, 3, 6, 6]
+    assert D["perm_token"].tolist() == [0, 1, 2, 0, 1, 2]
+
+
+# ------------------------------------------------------------------- experts and combine
+
+def test_swiglu_scalar_closed_form():
+    g = _gold("closed_forms.json")["swiglu_scalar"]
+    a, u, h, y = O.swiglu_expert(np.array([[g["x"]]]), np.array([[g["w_gate"]]]),
+                                 np.array([[g["w_up"]]]), np.array([[g["w_down"]]]))
+    assert a[0, 0] == g["a"] and u[0, 0] == g["u"]
+    assert h[0, 0] == pytest.approx(g["h"], rel=1e-15)
+    assert y[0, 0] == pytest.approx(g["y"], rel=1e-15)
+
+
+@pytest.mark.parametrize("mode,fs", [("sigmoid", 0), ("sigmoid", 6), ("softmax", 0)])
+def test_permuted_layer_equals_dense_masked_brute_force(mode, fs):
+    rng = np.random.default_rng(7)
+    inp = _tiny_inputs(rng, T=40, d=12, E=6, f=5, fs=fs)
+    fwd = O.layer_forward(inp, mode, 3, 1e-3)
+    ref = O.layer_forward_dense_masked(inp, mode, 3, 1e-3)
+    np.testing.assert_allclose(fwd["out"], ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_single_expert_top1_is_the_dense_ffn(mode):
+    """One expert with top-1 routing is the dense SwiGLU FFN it replaces, and the router
+    weight gets exactly zero gradient (handbook summary, section 2.5)."""
+    rng = np.random.default_rng(8)
+    inp = _tiny_inputs(rng, T=11, d=6, E=1, f=4)
+    fwd = O.layer_forward(inp, mode, 1, 0.0)
+    assert (fwd["gate"] == 1.0).all()
+    dense = O.swiglu_expert(inp["x"], inp["W_g"][0], inp["W_u"][0], inp["W_d"][0])[3]
+    np.testing.assert_array_equal(fwd["out"], dense)
+    dY = rng.standard_normal(fwd["out"].shape)
+    bwd = O.layer_backward(inp, fwd, dY)
+    assert (bwd["dW_r"] == 0.0).all()
+    assert (bwd["dlogits"] == 0.0).all()
+
+
+def test_gemm_flop_accounting_reproduces_the_pages_parameter_counts():
+    """A SwiGLU expert holds 3*d*f parameters, so the eight chosen experts equal the
+    dense layer they replace and the printed model totals follow."""
+    g = _gold("param_counts.json")
+    d, f, E, k, L = g["hidden"], g["expert_width"], g["experts"], g["top_k"], g["layers"]
+    cfg = MoEConfig("pin", T=1, d=d, E=E, k=k, f=f, f_shared=0, mode="sigmoid", seed=0,
+                    backward=False, bias_update=False)
+    per_expert = cfg.gemm_flops() / (2.0 * cfg.N)  # FLOPs per routed row / 2 = params per expert
+    assert per_expert == 3 * d * f == 6_291_456
+    assert k * per_expert == 3 * d * g["dense_ffn_width"]
+    router = E * d
+    dense_total = g["dense_total_params_printed_B"] * 1e9
+    moe_total = dense_total + L * (E * per_expert - 3 * d * g["dense_ffn_width"] + router)
+    moe_active = dense_total + L * router
+    assert round(moe_total / 1e9, 2) == g["moe_total_params_printed_B"]
+    assert round(moe_active / 1e9, 3) == g["moe_active_params_printed_B"]
+    assert L * 1 * d == g["zero_grad_params_single_expert_printed"] - 2
+
+
+# ---------------------------------------------------------------------------- bias update
+
+def test_bias_update_worked_example():
+    g = _gold("closed_forms.json")["bias_update_example"]
+    nb = O.bias_update(np.array(g["counts"]), np.array(g["b_before"], np.float32), g["T"], g["k"], g["gamma"])
+    got = [hex(struct.unpack("<I", struct.pack("<f", float(v)))[0]) for v in nb]
+    assert got == g["b_after_fp32_hex"]
+
+
+def test_bias_update_invariants():
+    rng = np.random.default_rng(9)
+    E, T, k = 16, 100, 4
+    b = rng.uniform(-0.05, 0.05, E).astype(np.float32)
+    counts = rng.multinomial(T * k, np.ones(E) / E)
+    nb = O.bias_update(counts, b, T, k, 0.001)
+    mean = T * k / E
+    delta = nb.astype(np.float64) - b
+    for e in range(E):
+        if counts[e] == mean:
+            assert delta[e] == 0
+        else:
+            assert np.sign(delta[e]) == np.sign(mean - counts[e])
+            assert abs(abs(delta[e]) - 0.001) < 1e-8
+    balanced = O.bias_update(np.full(E, T * k // E), b, T, k, 0.001)
+    np.testing.assert_array_equal(balanced, b)
+
+
+# ----------------------------------------------------------------------- finite differences
+
+def _fd_case(mode, seed):
+    """Tiny inputs whose selections sit at least 1e-3 away from a tie."""
+    rng = np.random.default_rng(seed)
+    while True:
+        inp = _tiny_inputs(rng, T=6, d=5, E=5, f=3, fs=2)
+        lg = O.router_logits(inp["x"], inp["W_r"])
+        r = O.route(lg, mode, 2, inp["b"], 0.1)
+        if not O.near_tie_tokens(r["select_value"], 2, gap=1e-3).any():
+            return inp, rng
+
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_backward_matches_central_finite_differences(mode):
+    inp, rng = _fd_case(mode, 11 if mode == "sigmoid" else 12)
+    z = 0.1 if mode == "softmax" else 0.0
+    dY = rng.standard_normal((6, 5))
+    fwd = O.layer_forward(inp, mode, 2, z)
+    bwd = O.layer_backward(inp, fwd, dY)
+    names = {"x": "dx", "W_r": "dW_r", "W_g": "dW_g", "W_u": "dW_u", "W_d": "dW_d",
+             "Ws_g": "dWs_g", "Ws_u": "dWs_u", "Ws_d": "dWs_d"}
+    h = 1e-6
+    for p, gname in names.items():
+        arr = inp[p]
+        num = np.zeros_like(arr)
+        for ix in np.ndindex(arr.shape):
+            old = arr[ix]
+            arr[ix] = old + h
+            lp = O.loss(O.layer_forward(inp, mode, 2, z), dY)
+            arr[ix] = old - h
+            lm = O.loss(O.layer_forward(inp, mode, 2, z), dY)
+            arr[ix] = old
+            num[ix] = (lp - lm) / (2 * h)
+        ana = bwd[gname]
+        scale = max(1.0, np.abs(num).max())
+        assert np.abs(ana - num).max() / scale < 1e-6, p
+
+
+def test_sampled_rows_equal_full_layer():
+    """The per-token and per-entry evaluations used at large sizes agree with the whole
+    layer."""
+    rng = np.random.default_rng(13)
+    for mode, z in (("sigmoid", 0.0), ("softmax", 0.05)):
+        inp = _tiny_inputs(rng, T=30, d=8, E=5, f=4, fs=3 if mode == "sigmoid" else 0)
+        dY = rng.standard_normal((30, 8))
+        fwd = O.layer_forward(inp, mode, 2, z)
+        bwd = O.layer_backward(inp, fwd, dY)
+        for t in (0, 7, 29):
+            o = O.token_forward(inp, t, fwd["idx"][t], fwd["gate"][t])
+            np.testing.assert_allclose(o, fwd["out"][t], rtol=1e-12, atol=1e-12)
+            tb = O.token_backward(inp, t, fwd["logits"][t], fwd["idx"][t], mode, 2, dY[t], z, 30)
+            np.testing.assert_allclose(tb["dx"], bwd["dx"][t], rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(tb["dg"], bwd["dg"][t], rtol=1e-12, atol=1e-12)
+        for e in range(5):
+            rows = np.arange(fwd["offsets"][e], fwd["offsets"][e + 1])
+            toks = fwd["perm_token"][rows]
+            gates = fwd["gate"][toks, fwd["perm_slot"][rows]]
+            ent = O.expert_weight_grad_entries(inp, e, toks, gates, dY, [(0, 1), (7, 3)], [(2, 5), (0, 0)])
+            np.testing.assert_allclose(ent["dW_d"], [bwd["dW_d"][e][0, 1], bwd["dW_d"][e][7, 3]], rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(ent["dW_g"], [bwd["dW_g"][e][2, 5], bwd["dW_g"][e][0, 0]], rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(ent["dW_u"], [bwd["dW_u"][e][2, 5], bwd["dW_u"][e][0, 0]], rtol=1e-11, atol=1e-13)
+        if mode == "sigmoid":
+            ent = O.shared_weight_grad_entries(inp, dY, [(1, 2)], [(0, 3)])
+            np.testing.assert_allclose(ent["dWs_d"], [bwd["dWs_d"][1, 2]], rtol=1e-11)
+            np.testing.assert_allclose(ent["dWs_g"], [bwd["dWs_g"][0, 3]], rtol=1e-11)
+            np.testing.assert_allclose(ent["dWs_u"], [bwd["dWs_u"][0, 3]], rtol=1e-11)
