@@ -33,6 +33,18 @@ The readings taken where they are silent are the workload definitions:
 Everything is fp64 numpy; bf16 and fp32 inputs convert to fp64 exactly. Matrix products use
 numpy's matmul as a library step. Rows are processed per expert in the order of the
 definition; there is no blocking or fusion.
+
+Storage precision. The workloads state "bf16 weights and activations, fp32 accumulate" (and
+bf16 outputs and gradients). Every function that produces a tensor the layer hands from one
+step to the next takes ``rnd``: ``None`` keeps the exact fp64 value (the plain definition);
+``bf16_round`` rounds that stored tensor to bf16 (round to nearest even) at the point it is
+materialised, computing it first from unrounded operands:
+a, u and h of an expert (h from the unrounded a and u), the expert output y, the shared
+expert's a, u, h, y, the layer output, the scaled upstream gradient g * dY of each routed
+row, the SwiGLU input gradients da and du (from the stored a and u), each expert's input
+gradient, the weight gradients, the shared expert's input gradient and the layer's input
+gradient. Router quantities (logits, gates, logit gradients, dW_r) stay fp32-or-better and
+are never rounded to bf16.
 """
 from __future__ import annotations
 
@@ -53,6 +65,22 @@ def to64(t) -> np.ndarray:
     if hasattr(t, "detach"):
         t = t.detach().cpu().float().numpy()
     return np.asarray(t, dtype=np.float64)
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round to the nearest bf16 value (8 significant bits), ties to even.
+
+    x = m * 2**e with 0.5 <= |m| < 1, so x * 2**(8 - e) has 8 integer bits; rint rounds
+    half to even. Below the smallest normal bf16 (2**-126) the spacing stays 2**-133, as for
+    bf16 subnormals. Zero stays zero; overflow to infinity is not modelled."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    return np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)
+
+
+def _r(rnd, x):
+    return x if rnd is None else rnd(x)
 
 
 def sigmoid(z: np.ndarray) -> np.ndarray:
@@ -174,17 +202,18 @@ def dispatch(idx: np.ndarray, E: int) -> dict:
 # ---------------------------------------------------------------------------------------
 # experts and combine
 
-def swiglu_expert(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray):
+def swiglu_expert(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
+                  rnd=None):
     """One bias-free SwiGLU expert (three weight matrices, section 2.5):
-    a = x W_g^T, u = x W_u^T, h = silu(a) * u, y = h W_d^T."""
+    a = x W_g^T, u = x W_u^T, h = silu(a) * u, y = h W_d^T. Returns the stored a, u, h, y."""
     a = rows @ W_g.T
     u = rows @ W_u.T
-    h = silu(a) * u
-    y = h @ W_d.T
-    return a, u, h, y
+    h = _r(rnd, silu(a) * u)
+    y = _r(rnd, h @ W_d.T)
+    return _r(rnd, a), _r(rnd, u), h, y
 
 
-def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d) -> dict:
+def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d, rnd=None) -> dict:
     """Each expert applied to its own contiguous segment of the permuted rows."""
     N = x_perm.shape[0]
     f = W_g.shape[1]
@@ -193,12 +222,13 @@ def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d) -> d
     for e in range(W_g.shape[0]):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi > lo:
-            A[lo:hi], U[lo:hi], H[lo:hi], Y[lo:hi] = swiglu_expert(x_perm[lo:hi], W_g[e], W_u[e], W_d[e])
+            A[lo:hi], U[lo:hi], H[lo:hi], Y[lo:hi] = swiglu_expert(x_perm[lo:hi], W_g[e], W_u[e],
+                                                                   W_d[e], rnd)
     return {"A": A, "U": U, "H": H, "Y_perm": Y}
 
 
 def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
-            Y_shared: np.ndarray | None) -> np.ndarray:
+            Y_shared: np.ndarray | None, rnd=None) -> np.ndarray:
     """out_t = sum over slots of gate * expert output, plus the shared expert's output
     (section 2.5: each expert's output is returned to the token)."""
     T, k = gate.shape
@@ -207,14 +237,15 @@ def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
         out += gate[:, i:i + 1] * Y_perm[slot_to_row[:, i]]
     if Y_shared is not None:
         out += Y_shared
-    return out
+    return _r(rnd, out)
 
 
 # ---------------------------------------------------------------------------------------
 # whole layer, forward
 
 def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
-                  logits: np.ndarray | None = None, idx: np.ndarray | None = None) -> dict:
+                  logits: np.ndarray | None = None, idx: np.ndarray | None = None,
+                  rnd=None) -> dict:
     """Full forward of the layer from fp64 copies of the inputs.
 
     ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
@@ -229,13 +260,14 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
         r = _regate(r, logits, idx, mode, inp.get("b"), z_coef)
     disp = dispatch(r["idx"], E)
     x_perm = x[disp["perm_token"]]
-    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"])
+    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"], rnd)
     shared = None
     if "Ws_g" in inp:
-        shared = swiglu_expert(x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])
-    out = combine(ex["Y_perm"], r["gate"], disp["slot_to_row"], None if shared is None else shared[3])
+        shared = swiglu_expert(x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)
+    out = combine(ex["Y_perm"], r["gate"], disp["slot_to_row"],
+                  None if shared is None else shared[3], rnd)
     res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
-           "z_coef": z_coef}
+           "z_coef": z_coef, "rnd": rnd}
     if shared is not None:
         res["shared"] = dict(zip("AUHY", shared))
     return res
@@ -328,7 +360,9 @@ def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndar
 
 
 def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
-    """Gradients of ``loss`` with respect to x, every weight and the router."""
+    """Gradients of ``loss`` with respect to x, every weight and the router (stored in the
+    precision the forward used)."""
+    rnd = fwd.get("rnd")
     idx, gate, s2r = fwd["idx"], fwd["gate"], fwd["slot_to_row"]
     T, k = idx.shape
     E = inp["W_r"].shape[0]
@@ -336,7 +370,7 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
     tok = fwd["perm_token"]
     slot = fwd["perm_slot"]
     # combine backward
-    dY_perm = gate[tok, slot][:, None] * dY[tok]
+    dY_perm = _r(rnd, gate[tok, slot][:, None] * dY[tok])
     dg = np.zeros((T, k))
     for i in range(k):
         dg[:, i] = np.sum(dY * fwd["Y_perm"][s2r[:, i]], axis=1)
@@ -351,11 +385,12 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
         if hi == lo:
             continue
         dH = dY_perm[lo:hi] @ inp["W_d"][e]
-        dA[lo:hi], dU[lo:hi] = swiglu_backward(dH, fwd["A"][lo:hi], fwd["U"][lo:hi])
-        dW_d[e] = dY_perm[lo:hi].T @ fwd["H"][lo:hi]
-        dW_g[e] = dA[lo:hi].T @ fwd["X_perm"][lo:hi]
-        dW_u[e] = dU[lo:hi].T @ fwd["X_perm"][lo:hi]
-        dX_perm[lo:hi] = dA[lo:hi] @ inp["W_g"][e] + dU[lo:hi] @ inp["W_u"][e]
+        da, du = swiglu_backward(dH, fwd["A"][lo:hi], fwd["U"][lo:hi])
+        dA[lo:hi], dU[lo:hi] = _r(rnd, da), _r(rnd, du)
+        dW_d[e] = _r(rnd, dY_perm[lo:hi].T @ fwd["H"][lo:hi])
+        dW_g[e] = _r(rnd, dA[lo:hi].T @ fwd["X_perm"][lo:hi])
+        dW_u[e] = _r(rnd, dU[lo:hi].T @ fwd["X_perm"][lo:hi])
+        dX_perm[lo:hi] = _r(rnd, dA[lo:hi] @ inp["W_g"][e] + dU[lo:hi] @ inp["W_u"][e])
     dx = np.zeros((T, d))
     for i in range(k):
         dx += dX_perm[s2r[:, i]]
@@ -365,15 +400,16 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
         sh = fwd["shared"]
         dHs = dY @ inp["Ws_d"]
         dAs, dUs = swiglu_backward(dHs, sh["A"], sh["U"])
-        res["dWs_d"] = dY.T @ sh["H"]
-        res["dWs_g"] = dAs.T @ inp["x"]
-        res["dWs_u"] = dUs.T @ inp["x"]
-        res["dx_shared"] = dAs @ inp["Ws_g"] + dUs @ inp["Ws_u"]
+        dAs, dUs = _r(rnd, dAs), _r(rnd, dUs)
+        res["dWs_d"] = _r(rnd, dY.T @ sh["H"])
+        res["dWs_g"] = _r(rnd, dAs.T @ inp["x"])
+        res["dWs_u"] = _r(rnd, dUs.T @ inp["x"])
+        res["dx_shared"] = _r(rnd, dAs @ inp["Ws_g"] + dUs @ inp["Ws_u"])
         dx += res["dx_shared"]
     rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"])
     res.update(rb)
     dx += rb["dx_r"]
-    res["dx"] = dx
+    res["dx"] = _r(rnd, dx)
     return res
 
 
@@ -395,19 +431,19 @@ def bias_update(counts: np.ndarray, b: np.ndarray, T: int, k: int, gamma: float)
 # ---------------------------------------------------------------------------------------
 # sampled evaluation for workloads too large to run whole on the CPU
 
-def token_forward(inp: dict, t: int, experts, gates) -> np.ndarray:
+def token_forward(inp: dict, t: int, experts, gates, rnd=None) -> np.ndarray:
     """out_t for one token given its chosen experts and gates."""
     x_t = inp["x"][t:t + 1]
     out = np.zeros((1, inp["x"].shape[1]))
     for e, g in zip(experts, gates):
-        out += g * swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e])[3]
+        out += g * swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)[3]
     if "Ws_g" in inp:
-        out += swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])[3]
-    return out[0]
+        out += swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)[3]
+    return _r(rnd, out[0])
 
 
 def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, k: int,
-                   dY_t: np.ndarray, z_coef: float, T: int) -> dict:
+                   dY_t: np.ndarray, z_coef: float, T: int, rnd=None) -> dict:
     """Gradient rows of one token: dx_t, dg_t and the router logit gradient for it.
 
     A token's dx depends only on its own routing, experts and upstream gradient, so it can
@@ -420,58 +456,60 @@ def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, 
     dx = np.zeros((1, x_t.shape[1]))
     dg = np.zeros((1, k))
     for i, e in enumerate(experts):
-        a, u, h, y = swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e])
+        a, u, h, y = swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)
         dg[0, i] = float(np.sum(dY_t * y[0]))
-        dH = (gate[i] * dY_t[None, :]) @ inp["W_d"][e]
+        dH = _r(rnd, gate[i] * dY_t[None, :]) @ inp["W_d"][e]
         dA, dU = swiglu_backward(dH, a, u)
-        dx += dA @ inp["W_g"][e] + dU @ inp["W_u"][e]
+        dA, dU = _r(rnd, dA), _r(rnd, dU)
+        dx += _r(rnd, dA @ inp["W_g"][e] + dU @ inp["W_u"][e])
     if "Ws_g" in inp:
-        a, u, h, y = swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"])
+        a, u, h, y = swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)
         dA, dU = swiglu_backward(dY_t[None, :] @ inp["Ws_d"], a, u)
-        dx += dA @ inp["Ws_g"] + dU @ inp["Ws_u"]
+        dA, dU = _r(rnd, dA), _r(rnd, dU)
+        dx += _r(rnd, dA @ inp["Ws_g"] + dU @ inp["Ws_u"])
     rb = router_backward(dg, r, x_t, inp["W_r"], mode, z_coef, T_norm=T)
     dx += rb["dx_r"]
-    return {"dx": dx[0], "dg": dg[0], "dlogits": rb["dlogits"][0]}
+    return {"dx": _r(rnd, dx[0]), "dg": dg[0], "dlogits": rb["dlogits"][0]}
 
 
 def expert_weight_grad_entries(inp: dict, e: int, tokens: np.ndarray, slots_gate: np.ndarray,
-                               dY: np.ndarray, entries_d, entries_gu) -> dict:
+                               dY: np.ndarray, entries_d, entries_gu, rnd=None) -> dict:
     """Chosen entries of dW_d[e], dW_g[e] and dW_u[e].
 
     ``tokens`` are the tokens routed to expert e in ascending order and ``slots_gate`` their
     gates for e. ``entries_d`` lists (i, j) of dW_d[e][i, j] = sum_p dY_perm[p, i] h[p, j];
     ``entries_gu`` lists (j, i) of dW_g[e][j, i] = sum_p dA[p, j] x_perm[p, i] (and dW_u)."""
     X = inp["x"][tokens]
-    dYp = slots_gate[:, None] * dY[tokens]
+    dYp = _r(rnd, slots_gate[:, None] * dY[tokens])
     Wg, Wu, Wd = inp["W_g"][e], inp["W_u"][e], inp["W_d"][e]
     res = {"dW_d": [], "dW_g": [], "dW_u": []}
     for (i, j) in entries_d:
         a = X @ Wg[j]
         u = X @ Wu[j]
-        h = silu(a) * u
-        res["dW_d"].append(float(np.sum(dYp[:, i] * h)))
+        h = _r(rnd, silu(a) * u)
+        res["dW_d"].append(float(_r(rnd, np.sum(dYp[:, i] * h))))
     for (j, i) in entries_gu:
-        a = X @ Wg[j]
-        u = X @ Wu[j]
+        a = _r(rnd, X @ Wg[j])
+        u = _r(rnd, X @ Wu[j])
         dh = dYp @ Wd[:, j]
         da, du = swiglu_backward(dh, a, u)
-        res["dW_g"].append(float(np.sum(da * X[:, i])))
-        res["dW_u"].append(float(np.sum(du * X[:, i])))
+        res["dW_g"].append(float(_r(rnd, np.sum(_r(rnd, da) * X[:, i]))))
+        res["dW_u"].append(float(_r(rnd, np.sum(_r(rnd, du) * X[:, i]))))
     return res
 
 
-def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu) -> dict:
+def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu, rnd=None) -> dict:
     """Chosen entries of the shared expert's weight gradients (every token, weight 1)."""
     X = inp["x"]
     Wg, Wu, Wd = inp["Ws_g"], inp["Ws_u"], inp["Ws_d"]
     res = {"dWs_d": [], "dWs_g": [], "dWs_u": []}
     for (i, j) in entries_d:
-        h = silu(X @ Wg[j]) * (X @ Wu[j])
-        res["dWs_d"].append(float(np.sum(dY[:, i] * h)))
+        h = _r(rnd, silu(X @ Wg[j]) * (X @ Wu[j]))
+        res["dWs_d"].append(float(_r(rnd, np.sum(dY[:, i] * h))))
     for (j, i) in entries_gu:
-        a = X @ Wg[j]
-        u = X @ Wu[j]
+        a = _r(rnd, X @ Wg[j])
+        u = _r(rnd, X @ Wu[j])
         da, du = swiglu_backward(dY @ Wd[:, j], a, u)
-        res["dWs_g"].append(float(np.sum(da * X[:, i])))
-        res["dWs_u"].append(float(np.sum(du * X[:, i])))
+        res["dWs_g"].append(float(_r(rnd, np.sum(_r(rnd, da) * X[:, i]))))
+        res["dWs_u"].append(float(_r(rnd, np.sum(_r(rnd, du) * X[:, i]))))
     return res

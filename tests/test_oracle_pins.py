@@ -307,3 +307,61 @@ def test_sampled_rows_equal_full_layer():
             np.testing.assert_allclose(ent["dWs_d"], [bwd["dWs_d"][1, 2]], rtol=1e-11)
             np.testing.assert_allclose(ent["dWs_g"], [bwd["dWs_g"][0, 3]], rtol=1e-11)
             np.testing.assert_allclose(ent["dWs_u"], [bwd["dWs_u"][0, 3]], rtol=1e-11)
+
+
+# ----------------------------------------------------------------- bf16 storage precision
+
+def test_bf16_round_matches_library_conversion_including_ties():
+    """Round-to-nearest-even to 8 significant bits equals torch's fp32 -> bf16 conversion
+    (a library routine) on random values and on exact halfway cases."""
+    import torch
+    rng = np.random.default_rng(14)
+    scale = (10.0 ** rng.integers(-40, 30, 20000)).astype(np.float32)  # includes subnormals
+    vals = (rng.standard_normal(20000) * scale).astype(np.float32)
+    bits = vals.view(np.uint32)
+    ties = ((bits & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)  # exact halfway
+    allv = np.concatenate([vals, ties, np.float32([0.0, -0.0, 1.0, 1.00390625, 1.01171875])])
+    want = torch.from_numpy(allv).to(torch.bfloat16).float().numpy().astype(np.float64)
+    got = O.bf16_round(allv.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_mode_sampled_rows_equal_full_layer():
+    rng = np.random.default_rng(15)
+    for mode, z in (("sigmoid", 0.0), ("softmax", 0.05)):
+        inp = _tiny_inputs(rng, T=24, d=8, E=5, f=4, fs=3 if mode == "sigmoid" else 0)
+        dY = O.bf16_round(rng.standard_normal((24, 8)))
+        fwd = O.layer_forward(inp, mode, 2, z, rnd=O.bf16_round)
+        bwd = O.layer_backward(inp, fwd, dY)
+        for t in (0, 5, 23):
+            o = O.token_forward(inp, t, fwd["idx"][t], fwd["gate"][t], rnd=O.bf16_round)
+            np.testing.assert_allclose(o, fwd["out"][t], rtol=1e-12, atol=1e-12)
+            tb = O.token_backward(inp, t, fwd["logits"][t], fwd["idx"][t], mode, 2, dY[t], z, 24,
+                                  rnd=O.bf16_round)
+            np.testing.assert_allclose(tb["dx"], bwd["dx"][t], rtol=1e-11, atol=1e-12)
+        for e in range(5):
+            rows = np.arange(fwd["offsets"][e], fwd["offsets"][e + 1])
+            toks = fwd["perm_token"][rows]
+            gates = fwd["gate"][toks, fwd["perm_slot"][rows]]
+            ent = O.expert_weight_grad_entries(inp, e, toks, gates, dY, [(3, 1)], [(2, 5)],
+                                               rnd=O.bf16_round)
+            np.testing.assert_allclose(ent["dW_d"], [bwd["dW_d"][e][3, 1]], rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(ent["dW_g"], [bwd["dW_g"][e][2, 5]], rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(ent["dW_u"], [bwd["dW_u"][e][2, 5]], rtol=1e-11, atol=1e-13)
+
+
+def test_bf16_mode_stays_close_to_the_exact_definition():
+    """Storing activations in bf16 moves the layer by about the bf16 unit roundoff."""
+    rng = np.random.default_rng(16)
+    inp = _tiny_inputs(rng, T=64, d=32, E=6, f=16, fs=8)
+    dY = O.bf16_round(rng.standard_normal((64, 32)))
+    f64 = O.layer_forward(inp, "sigmoid", 2)
+    b16 = O.layer_forward(inp, "sigmoid", 2, rnd=O.bf16_round)
+    np.testing.assert_allclose(b16["out"], f64["out"], rtol=2e-2, atol=2e-2)
+    g64 = O.layer_backward(inp, f64, dY)
+    g16 = O.layer_backward(inp, b16, dY)
+    for name in ("dx", "dW_g", "dW_d", "dWs_u", "dW_r"):
+        np.testing.assert_allclose(g16[name], g64[name], rtol=3e-2, atol=3e-2)
+    # the stored tensors are bf16 values
+    for name in ("A", "U", "H", "Y_perm", "out"):
+        np.testing.assert_array_equal(O.bf16_round(b16[name]), b16[name])
