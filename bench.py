@@ -1,0 +1,310 @@
+"""Benchmark of the MoE layer step (forward + backward + bias update) on GB300.
+
+Default workload: the large fine-grained layer (T=65536 = 16 x 4096 tokens, d_model 4096,
+64 experts, top-8, expert d_ff 1536, one shared expert of d_ff 3072, sigmoid router with
+bias and bias update), synthetic inputs. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C4] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica on its own batch (no collective on the data
+path: the layer step does not exchange data); `value` is the tokens of all ranks divided
+by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--config", default="C4")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=128)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            pk = json.load(fh)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(cfg):
+    return {"workload": cfg.name, "T": cfg.T, "d_model": cfg.d, "experts": cfg.E, "top_k": cfg.k,
+            "d_ff": cfg.f, "shared_d_ff": cfg.f_shared, "router": cfg.mode,
+            "bias_update": cfg.bias_update, "pass": "fwd+bwd" if cfg.backward else "fwd",
+            "l2": "inputs larger than L2 (x alone is %.0f MiB; permuted rows %.1f GiB)"
+                  % (cfg.T * cfg.d * 2 / 2**20, cfg.N * cfg.d * 2 / 2**30),
+            "parallelism": "replicas"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
+    """The fp64 oracle (forward + backward + bias update) on the first T_s tokens of the
+    workload, all experts; returns (tokens/s, threads, seconds per step)."""
+    from oracle import moe_oracle as O
+    sub = dict(inp)
+    sub["x"] = inp["x"][:T_s]
+    sub["dY"] = inp["dY"][:T_s]
+    i64 = {k: O.to64(v) for k, v in sub.items() if k != "dY"}
+    dY = O.to64(sub["dY"])
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef)
+        if cfg.backward:
+            O.layer_backward(i64, fwd, dY)
+        if cfg.bias_update:
+            O.bias_update(fwd["counts"], i64["b"].astype("float32"), T_s, cfg.k, cfg.gamma)
+        times.append(time.perf_counter() - t0)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return T_s / statistics.median(times), cores, times
+
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from pretraining_sigmoid_softmax_gb300.inputs import make_inputs
+    inp = make_inputs(cfg)
+    T_s = max(8, min(args.cpu_sample_tokens // 4, cfg.T))
+    rate, cores, times = cpu_oracle_rate(cfg, inp, T_s, steps=args.warmup + args.steps)
+    timed = times[args.warmup:] or times
+    ms = 1e3 * sum(timed) / len(timed)
+    value = T_s / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(cfg),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {T_s} tokens of the workload per step, all "
+                                       f"{cfg.E} experts, fp64 forward+backward+bias update"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    from pretraining_sigmoid_softmax_gb300.configs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import torch
+    import torch.distributed as dist
+    from pretraining_sigmoid_softmax_gb300 import build, ops
+    from pretraining_sigmoid_softmax_gb300.inputs import make_inputs
+    from pretraining_sigmoid_softmax_gb300.layer import MoEPlan, MoEShape
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if local == 0:
+        build.build_library()
+    if world > 1:
+        dist.barrier()
+
+    inp = make_inputs(cfg)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    plan = MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)
+    b_work = dev["b"].clone()
+    stream = torch.cuda.current_stream()
+
+    def step(x, dY):
+        plan.forward(x, dev["W_r"], b_work, dev["W_g"], dev["W_u"], dev["W_d"], dev.get("Ws_g"),
+                     dev.get("Ws_u"), dev.get("Ws_d"))
+        if cfg.backward:
+            plan.backward(dY)
+            if cfg.bias_update:
+                plan.bias_update(b_work, cfg.gamma)
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step(dev["x"], dev.get("dY"))
+    ops.moe_clear_device_status()
+    sync_all()
+
+    # ---------------------------------------------------------------- device-resident timing
+    plan.gemm_events = []
+    sampler = ClockSampler(gpu_id_for(local))
+    sync_all()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(dev["x"], dev.get("dY"))
+    t_end.record(stream)
+    sync_all()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    gemm_ms = sum(a.elapsed_time(b) for a, b in plan.gemm_events)
+    plan.gemm_events = None
+    code, site = ops.moe_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} ({ops.status_string(code)}) at site {site}")
+    t = torch.tensor([ms_total, gemm_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total, gemm_ms = float(t[0]), float(t[1])
+    ms_step = ms_total / args.steps
+    value = world * cfg.T / (ms_step / 1e3)
+
+    # ------------------------------------------------------------ end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = inp["x"].pin_memory()
+        hdy = inp["dY"].pin_memory() if cfg.backward else None
+        hout = torch.empty_like(inp["x"]).pin_memory()
+        hdx = torch.empty_like(inp["x"]).pin_memory() if cfg.backward else None
+        xd = torch.empty_like(dev["x"])
+        dyd = torch.empty_like(dev["dY"]) if cfg.backward else None
+
+        def e2e_step():
+            xd.copy_(hx, non_blocking=True)
+            if cfg.backward:
+                dyd.copy_(hdy, non_blocking=True)
+            step(xd, dyd)
+            hout.copy_(plan.out, non_blocking=True)
+            if cfg.backward:
+                hdx.copy_(plan.dx, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        sync_all()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        sync_all()
+        te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        ms_e2e = float(te[0]) / args.steps
+        nbytes = cfg.T * cfg.d * 2
+        e2e = {"value": world * cfg.T / (ms_e2e / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": nbytes * (2 if cfg.backward else 1),
+               "d2h_bytes_per_step": nbytes * (2 if cfg.backward else 1),
+               "ms_per_step": ms_e2e}
+
+    # ------------------------------------------------------------------------- report
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+    pk, kind = peaks()
+    gemm_flops = cfg.gemm_flops()
+    gemm_tflops = gemm_flops / (gemm_ms / args.steps / 1e3) / 1e12
+    peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_desc(cfg),
+            "gemm_tflops": gemm_tflops, "gemm_frac_of_peak": gemm_tflops / peak_t,
+            "gemm_ms_per_step": gemm_ms / args.steps,
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (all GEMM launches)",
+                         "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": gemm_tflops / peak_t, "peak_kind": f"{kind} bf16 sustained",
+                         "traffic": None},
+            "gpu_launches": plan.launches_per_step(cfg.backward, cfg.bias_update) * args.steps,
+            "clocks": clocks, "e2e": e2e}
+    if world == 1 and not args.no_cpu_baseline:
+        T_s = min(args.cpu_sample_tokens, cfg.T)
+        rate, cores, _ = cpu_oracle_rate(cfg, inp, T_s)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"first {T_s} tokens of the workload, all {cfg.E} "
+                                          f"experts, fp64 forward+backward+bias update"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

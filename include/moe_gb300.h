@@ -1,0 +1,247 @@
+/*
+ * moe_gb300.h - C ABI of the GB300 (sm_103a) fine-grained Mixture-of-Experts layer.
+ *
+ * The layer (forward and backward of one decoder MoE layer on one GPU):
+ *   route    : router logits l = x W_r^T in fp32, top-k expert choice, gates;
+ *   permute  : every token copied to the rows of its k experts, grouped by expert;
+ *   experts  : SwiGLU experts h = silu(x W_g^T) * (x W_u^T), y = h W_d^T as grouped GEMMs;
+ *   combine  : out_t = sum_i g_ti y_ti (+ shared expert output);
+ *   bias     : aux-loss-free per-expert bias update after backward.
+ * Sources: "The whole stack, in the open" (Apex-3), "What's inside", row "Fine-grained MoE"
+ * (sigmoid router, per-expert bias balancing the load without a loss term, grouped GEMM
+ * experts); KempnerForge README, "Features" (softmax top-k and DeepSeek-V3 sigmoid routers,
+ * shared experts, router z-loss); "How to train a large-scale Mixture-of-Experts model from
+ * scratch", section 2.5 "First training of MoE" (top-8 of 64 experts, tokens sent to the
+ * chosen experts and outputs returned, bias-free SwiGLU experts, fp32 router logits).
+ *
+ * Conventions for every entry point
+ *   - Every pointer is caller-owned DEVICE memory unless stated otherwise; the library
+ *     never allocates or frees memory. Scratch space is the caller's `ws` buffer of at
+ *     least moe_workspace_bytes() bytes (256-byte aligned).
+ *   - Row-major layouts. bf16 tensors are passed as `moe_bf16*` (IEEE bfloat16 bits).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream);
+ *     no call synchronises. The return value reports host-side argument checks and
+ *     launch errors only. Problems found on the device (an expert index out of range,
+ *     a bounded wait that ran out) are recorded in a per-device status word read with
+ *     moe_device_status().
+ *   - Results are deterministic: no floating-point atomics, every reduction has a fixed
+ *     order, so two runs on the same inputs give identical bits.
+ *   - Shape limits: 1 <= k <= min(E, 32), E <= 256, d % 128 == 0, f % 128 == 0,
+ *     T >= 1. Violations return MOE_ERR_UNSUPPORTED; null or inconsistent arguments
+ *     MOE_ERR_INVALID_ARG.
+ *
+ * Permuted ("expert-major") layout
+ *   Rows routed to expert e are stored contiguously, in ascending token order, starting
+ *   at row_offsets[e]. Each expert's segment is padded with zero rows to a multiple of
+ *   MOE_ROW_ALIGN (128) rows so that every 128-row tile of the grouped GEMMs belongs to
+ *   a single expert. row_offsets[e+1] - row_offsets[e] = round_up(counts[e], 128).
+ *   Buffers in this layout have moe_padded_rows(T, k, E) rows of capacity; rows past
+ *   row_offsets[E] are never read or written.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;               /* IEEE bfloat16 bit pattern */
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
+
+#define MOE_ROW_ALIGN 128
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,  /* shape outside the limits above, or not an sm_103 device */
+    MOE_ERR_WORKSPACE = 3,    /* ws_bytes smaller than moe_workspace_bytes() */
+    MOE_ERR_LAUNCH = 4,       /* a CUDA launch or runtime call failed */
+    MOE_ERR_BAD_INDEX = 5,    /* device: an expert index outside [0, E) or a layout overflow */
+    MOE_ERR_TIMEOUT = 6       /* device: a bounded wait inside a kernel ran out */
+};
+
+enum moe_router_mode {
+    MOE_MODE_SIGMOID = 0, /* sigmoid scores, top-k of score + bias, gates renormalised */
+    MOE_MODE_SOFTMAX = 1  /* softmax over all experts, top-k of logits, gates not renormalised */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int moe_version(void);
+
+/* Row capacity of a buffer in the permuted layout: round_up(T*k + E*127, 128). */
+int64_t moe_padded_rows(int64_t T, int k, int E);
+
+/* Bytes of scratch any one entry point needs for these sizes (the maximum over all). */
+size_t moe_workspace_bytes(int64_t T, int d, int E, int k);
+
+/*
+ * Device status word of the current device, written by kernels that detect a problem.
+ * Synchronises `stream`, stores the first recorded code (MOE_OK if none) in *code and
+ * the site that recorded it in *site (may be NULL). Returns MOE_OK or MOE_ERR_LAUNCH.
+ */
+int moe_device_status(moe_stream_t stream, int* code, int* site);
+/* Clears the device status word (enqueued on `stream`). */
+int moe_clear_device_status(moe_stream_t stream);
+
+/*
+ * Upper limit, in nanoseconds, of every bounded wait inside the grouped-GEMM kernels
+ * (default 2e9). A wait that runs out records MOE_ERR_TIMEOUT and the kernel returns
+ * after releasing its tensor memory.
+ */
+void moe_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * moe_route - router forward (R1).
+ * Definition: l[t,e] = sum_j x[t,j] * W_r[e,j] in fp32, each sum in a fixed order.
+ *   MOE_MODE_SIGMOID: s = 1/(1+exp(-l)); choose the k largest s[e] + b[e] (lower e first
+ *     on equal values); topk_score = chosen s; topk_gate = chosen s / sum of chosen s.
+ *   MOE_MODE_SOFTMAX: p = softmax(l) over all E; choose the k largest l (lower e first);
+ *     topk_gate = topk_score = chosen p (no renormalisation); lse[t] = logsumexp(l[t]);
+ *     z_loss[0] = z_coef * mean_t(lse[t]^2).
+ * Source: Apex-3 "Fine-grained MoE" row (sigmoid router with selection bias, no loss
+ * term); KempnerForge "Features" (softmax top-k router, router z-loss); section 2.5 of
+ * the handbook summary (router logits in fp32).
+ * In : x [T,d] bf16; W_r [E,d] fp32; b [E] fp32 (sigmoid mode; ignored and may be NULL
+ *      in softmax mode).
+ * Out: logits [T,E] fp32 (may be NULL in sigmoid mode; required in softmax mode, where
+ *      the backward needs it); topk_idx [T,k] int32, slots in descending selection value;
+ *      topk_gate [T,k] fp32; topk_score [T,k] fp32; lse [T] fp32 and z_loss [1] fp32
+ *      (softmax mode only, required there).
+ */
+int moe_route(const moe_bf16* x, const float* W_r, const float* b, int64_t T, int d, int E,
+              int k, int mode, float z_coef, float* logits, int32_t* topk_idx,
+              float* topk_gate, float* topk_score, float* lse, float* z_loss, void* ws,
+              size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_permute - token dispatch (R2): counts, offsets and a stable expert-major copy of x.
+ * Definition: counts[e] = number of (t,i) with topk_idx[t,i] == e; offsets = exclusive
+ * scan of counts (offsets[E] = T*k); rows of expert e hold the tokens that chose e in
+ * ascending token order. Source: section 2.5 of the handbook summary (tokens must be
+ * sent to the chosen experts).
+ * In : topk_idx [T,k] int32 (each row k distinct experts in [0,E)); x [T,d] bf16.
+ * Out: counts [E] int32; offsets [E+1] int64 (unpadded); row_offsets [E+1] int64 (padded
+ *      layout, multiples of 128); perm_token [moe_padded_rows] int32 (token of each row,
+ *      -1 for padding rows); slot_to_row [T,k] int32 (row of slot (t,i));
+ *      X_perm [moe_padded_rows, d] bf16 (x rows in the permuted layout, padding rows 0).
+ * An out-of-range index records MOE_ERR_BAD_INDEX; that slot is dropped.
+ */
+int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, int E, int k,
+                int32_t* counts, int64_t* offsets, int64_t* row_offsets, int32_t* perm_token,
+                int32_t* slot_to_row, moe_bf16* X_perm, void* ws, size_t ws_bytes,
+                moe_stream_t stream);
+
+/*
+ * moe_expert_fwd - SwiGLU experts as grouped GEMMs (G1 + G2), on tcgen05 tensor cores.
+ * Definition, for each row p of expert e: a = X[p] W_g[e]^T, u = X[p] W_u[e]^T,
+ * h = silu(a) * u, y = h W_d[e]^T; fp32 accumulation, bf16 results.
+ * Source: Apex-3 "Fine-grained MoE" (experts run as grouped GEMMs); section 2.5 of the
+ * handbook summary (bias-free SwiGLU expert, three weight matrices).
+ * In : X [rows,d] bf16; row_offsets [E+1] int64 device array in the padded layout, or
+ *      NULL for one dense expert over all `rows` rows (E must be 1; used for the shared
+ *      expert with X = x, rows = T); W_g, W_u [E,f,d] bf16; W_d [E,d,f] bf16.
+ * Out: A, U, H [rows,f] bf16 (saved for backward); Y [rows,d] bf16.
+ * `rows` is the row capacity of X/A/U/H/Y; rows past it are never touched.
+ */
+int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int E, int64_t rows, int d,
+                   int f, const moe_bf16* W_g, const moe_bf16* W_u, const moe_bf16* W_d,
+                   moe_bf16* A, moe_bf16* U, moe_bf16* H, moe_bf16* Y, void* ws,
+                   size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine - gate-weighted sum of the expert outputs (C1).
+ * Definition: out[t] = sum_{i<k} topk_gate[t,i] * Y_perm[slot_to_row[t,i]] + Y_shared[t],
+ * summed in fp32 in slot order, shared term last, one bf16 rounding. Source: section 2.5
+ * of the handbook summary (each expert's output is returned to its token); KempnerForge
+ * "Features" (shared experts).
+ * In : Y_perm [padded rows, d] bf16; topk_gate [T,k] fp32; slot_to_row [T,k] int32;
+ *      Y_shared [T,d] bf16 or NULL.  Out: out [T,d] bf16.
+ */
+int moe_combine(const moe_bf16* Y_perm, const float* topk_gate, const int32_t* slot_to_row,
+                const moe_bf16* Y_shared, int64_t T, int d, int k, moe_bf16* out,
+                moe_stream_t stream);
+
+/*
+ * moe_bias_update - aux-loss-free load balancing (U1), applied once per step after
+ * backward with the step's counts. Definition: b[e] = fp32(b[e] + gamma * sign(T*k/E -
+ * counts[e])), sign(0) = 0, the sign taken exactly in integers. Source: Apex-3 "Fine-grained
+ * MoE" (a per-expert bias balances the load without a loss term) and the training command
+ * on that page (router bias rate 1e-3).
+ * In : counts [E] int32.  In/out: b [E] fp32.
+ */
+int moe_bias_update(const int32_t* counts, int E, int64_t T, int k, float gamma, float* b,
+                    moe_stream_t stream);
+
+/*
+ * moe_combine_bwd - backward of moe_combine (B1).
+ * Definition: dY_perm[slot_to_row[t,i]] = bf16(topk_gate[t,i] * dY[t]);
+ * dg[t,i] = sum_j dY[t,j] * Y_perm[slot_to_row[t,i], j] (fp32, fixed order).
+ * In : dY [T,d] bf16; Y_perm; topk_gate; slot_to_row; row_offsets [E+1] and perm_token
+ *      (to zero the padding rows of dY_perm).
+ * Out: dY_perm [padded rows, d] bf16 (padding rows 0); dg [T,k] fp32.
+ */
+int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm, const float* topk_gate,
+                    const int32_t* slot_to_row, const int64_t* row_offsets,
+                    const int32_t* perm_token, int64_t T, int d, int E, int k,
+                    moe_bf16* dY_perm, float* dg, moe_stream_t stream);
+
+/*
+ * moe_expert_bwd - backward of moe_expert_fwd (B2-B5) on tcgen05 tensor cores.
+ * Definition, per row p of expert e, with dy = dY[p]:
+ *   dh = dy W_d[e]; da = dh * u * s(a) * (1 + a (1 - s(a))); du = dh * silu(a);
+ *   dX[p] = da W_g[e] + du W_u[e];
+ *   dW_d[e] = sum_p dy^T h;  dW_g[e] = sum_p da^T X[p];  dW_u[e] = sum_p du^T X[p].
+ * fp32 accumulation; bf16 results. An expert with no rows gets zero weight gradients.
+ * In : dY, X [rows, d] bf16; A, U, H [rows, f] bf16 (from moe_expert_fwd); row_offsets as
+ *      in moe_expert_fwd (NULL = one dense expert over `rows` rows); W_g, W_u, W_d.
+ *      Padding rows of dY and X must be zero (moe_permute and moe_combine_bwd do this).
+ * Out: dX [rows, d] bf16; dA, dU [rows, f] bf16 (the SwiGLU input gradients, kept as
+ *      operands of the weight-gradient GEMMs); dW_g, dW_u [E,f,d] bf16; dW_d [E,d,f] bf16.
+ */
+int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
+                   const moe_bf16* U, const moe_bf16* H, const int64_t* row_offsets, int E,
+                   int64_t rows, int d, int f, const moe_bf16* W_g, const moe_bf16* W_u,
+                   const moe_bf16* W_d, moe_bf16* dX, moe_bf16* dA, moe_bf16* dU,
+                   moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, void* ws, size_t ws_bytes,
+                   moe_stream_t stream);
+
+/*
+ * moe_route_bwd - router backward (R1b). No gradient reaches the bias or the choice.
+ * Definition: MOE_MODE_SIGMOID: S = sum_i topk_score[t,i]; ds_i = (dg_i - sum_j g_j dg_j)/S;
+ *   dlogits[t, idx_i] = ds_i * s_i * (1 - s_i), other experts 0.
+ *   MOE_MODE_SOFTMAX: p = exp(l - lse); dlogits[t,e] = p_e * (dg[slot of e, or 0] -
+ *   sum_i g_i dg_i) + (2 z_coef / T) * lse[t] * p_e (z-loss with weight 1).
+ *   dW_r = dlogits^T x (fp32, fixed-order split reduction over tokens).
+ * In : dg [T,k] fp32; x [T,d] bf16; topk_idx, topk_gate, topk_score [T,k]; logits [T,E]
+ *      and lse [T] (softmax mode; may be NULL in sigmoid mode).
+ * Out: dlogits [T,E] fp32 (consumed by moe_permute_bwd for the router's dx term);
+ *      dW_r [E,d] fp32.
+ */
+int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* topk_idx,
+                  const float* topk_gate, const float* topk_score, const float* logits,
+                  const float* lse, int64_t T, int d, int E, int k, int mode, float z_coef,
+                  float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_permute_bwd - input gradient of the layer (B6).
+ * Definition: dx[t] = sum_{i<k} dX_perm[slot_to_row[t,i]] + dx_shared[t]
+ *                     + sum_e dlogits[t,e] * W_r[e]  (fp32 in that order, one bf16 rounding).
+ * In : dX_perm [padded rows, d] bf16; slot_to_row [T,k]; dx_shared [T,d] bf16 or NULL;
+ *      dlogits [T,E] fp32 and W_r [E,d] fp32, or both NULL.
+ * Out: dx [T,d] bf16.
+ */
+int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_row,
+                    const moe_bf16* dx_shared, const float* dlogits, const float* W_r,
+                    int64_t T, int d, int E, int k, moe_bf16* dx, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -329,6 +329,20 @@ def swiglu_backward(dh: np.ndarray, a: np.ndarray, u: np.ndarray):
     return da, du
 
 
+def expert_backward(dy: np.ndarray, x: np.ndarray, a: np.ndarray, u: np.ndarray,
+                    h: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
+                    rnd=None) -> dict:
+    """Backward of one SwiGLU expert over its rows, given the upstream gradient of its
+    output and the stored a, u, h of the forward:
+    dh = dy W_d, (da, du) from the SwiGLU derivative, dx = da W_g + du W_u,
+    dW_d = dy^T h, dW_g = da^T x, dW_u = du^T x."""
+    dh = dy @ W_d
+    da, du = swiglu_backward(dh, a, u)
+    da, du = _r(rnd, da), _r(rnd, du)
+    return {"dA": da, "dU": du, "dX": _r(rnd, da @ W_g + du @ W_u),
+            "dW_d": _r(rnd, dy.T @ h), "dW_g": _r(rnd, da.T @ x), "dW_u": _r(rnd, du.T @ x)}
+
+
 def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndarray,
                     mode: str, z_coef: float, T_norm: int | None = None) -> dict:
     """Gradient of the loss with respect to the router logits, W_r and x, given the
@@ -369,11 +383,7 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
     offs = fwd["offsets"]
     tok = fwd["perm_token"]
     slot = fwd["perm_slot"]
-    # combine backward
-    dY_perm = _r(rnd, gate[tok, slot][:, None] * dY[tok])
-    dg = np.zeros((T, k))
-    for i in range(k):
-        dg[:, i] = np.sum(dY * fwd["Y_perm"][s2r[:, i]], axis=1)
+    dY_perm, dg = combine_backward(dY, fwd["Y_perm"], gate, s2r, tok, slot, rnd)
     # experts backward
     N, d = fwd["X_perm"].shape
     f = inp["W_g"].shape[1]
@@ -384,33 +394,49 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
         lo, hi = int(offs[e]), int(offs[e + 1])
         if hi == lo:
             continue
-        dH = dY_perm[lo:hi] @ inp["W_d"][e]
-        da, du = swiglu_backward(dH, fwd["A"][lo:hi], fwd["U"][lo:hi])
-        dA[lo:hi], dU[lo:hi] = _r(rnd, da), _r(rnd, du)
-        dW_d[e] = _r(rnd, dY_perm[lo:hi].T @ fwd["H"][lo:hi])
-        dW_g[e] = _r(rnd, dA[lo:hi].T @ fwd["X_perm"][lo:hi])
-        dW_u[e] = _r(rnd, dU[lo:hi].T @ fwd["X_perm"][lo:hi])
-        dX_perm[lo:hi] = _r(rnd, dA[lo:hi] @ inp["W_g"][e] + dU[lo:hi] @ inp["W_u"][e])
-    dx = np.zeros((T, d))
-    for i in range(k):
-        dx += dX_perm[s2r[:, i]]
+        g = expert_backward(dY_perm[lo:hi], fwd["X_perm"][lo:hi], fwd["A"][lo:hi],
+                            fwd["U"][lo:hi], fwd["H"][lo:hi], inp["W_g"][e], inp["W_u"][e],
+                            inp["W_d"][e], rnd)
+        dX_perm[lo:hi], dA[lo:hi], dU[lo:hi] = g["dX"], g["dA"], g["dU"]
+        dW_g[e], dW_u[e], dW_d[e] = g["dW_g"], g["dW_u"], g["dW_d"]
     res = {"dY_perm": dY_perm, "dg": dg, "dA": dA, "dU": dU, "dX_perm": dX_perm,
            "dW_g": dW_g, "dW_u": dW_u, "dW_d": dW_d}
     if "shared" in fwd:
         sh = fwd["shared"]
-        dHs = dY @ inp["Ws_d"]
-        dAs, dUs = swiglu_backward(dHs, sh["A"], sh["U"])
-        dAs, dUs = _r(rnd, dAs), _r(rnd, dUs)
-        res["dWs_d"] = _r(rnd, dY.T @ sh["H"])
-        res["dWs_g"] = _r(rnd, dAs.T @ inp["x"])
-        res["dWs_u"] = _r(rnd, dUs.T @ inp["x"])
-        res["dx_shared"] = _r(rnd, dAs @ inp["Ws_g"] + dUs @ inp["Ws_u"])
-        dx += res["dx_shared"]
+        g = expert_backward(dY, inp["x"], sh["A"], sh["U"], sh["H"], inp["Ws_g"], inp["Ws_u"],
+                            inp["Ws_d"], rnd)
+        res["dWs_d"], res["dWs_g"], res["dWs_u"] = g["dW_d"], g["dW_g"], g["dW_u"]
+        res["dx_shared"] = g["dX"]
     rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"])
     res.update(rb)
-    dx += rb["dx_r"]
-    res["dx"] = _r(rnd, dx)
+    res["dx"] = input_gradient(dX_perm, s2r, res.get("dx_shared"), rb["dx_r"], rnd)
     return res
+
+
+def combine_backward(dY, Y_perm, gate, slot_to_row, perm_token, perm_slot, rnd=None):
+    """Backward of the combine: each routed row receives its gate times the token's
+    upstream gradient; the gate gradient is the inner product of the upstream gradient
+    with that row's expert output."""
+    T, k = gate.shape
+    dY_perm = _r(rnd, gate[perm_token, perm_slot][:, None] * dY[perm_token])
+    dg = np.zeros((T, k))
+    for i in range(k):
+        dg[:, i] = np.sum(dY * Y_perm[slot_to_row[:, i]], axis=1)
+    return dY_perm, dg
+
+
+def input_gradient(dX_perm, slot_to_row, dx_shared, dx_router, rnd=None):
+    """dx_t = sum over the token's slots of its rows' input gradients, plus the shared
+    expert's and the router's input gradients."""
+    T, k = slot_to_row.shape
+    dx = np.zeros((T, dX_perm.shape[1]))
+    for i in range(k):
+        dx += dX_perm[slot_to_row[:, i]]
+    if dx_shared is not None:
+        dx += dx_shared
+    if dx_router is not None:
+        dx += dx_router
+    return _r(rnd, dx)
 
 
 # ---------------------------------------------------------------------------------------

@@ -1,0 +1,715 @@
+// SwiGLU experts as grouped GEMMs on the sm_100-family tensor cores (tcgen05, TMEM, TMA).
+//
+// "The whole stack, in the open" (Apex-3), "What's inside", row "Fine-grained MoE": the
+// experts run as grouped GEMMs. Handbook summary, section 2.5: a bias-free SwiGLU expert
+// has three weight matrices (gate, up, down).
+//
+// One persistent kernel template serves every GEMM of the layer:
+//   G1  [a|u] = X W_g^T, X W_u^T      two accumulators, SwiGLU in the epilogue (A, U, H out)
+//   G2  Y = H W_d^T
+//   B2  dH = dY W_d, SwiGLU backward in the epilogue (dA, dU out)
+//   B4  dX = dA W_g + dU W_u          K split over two operand pairs
+//   B3  dW_d[e] = dY_e^T H_e           weight gradients: K runs over expert e's rows
+//   B5  dW_g[e] = dA_e^T X_e, dW_u[e] = dU_e^T X_e
+// Row tiles are 128 rows of the expert-major layout, whose segments are padded to 128
+// rows, so every tile belongs to one expert and is found from row_offsets on the device
+// (no host synchronisation). Roles per CTA (256 threads, one CTA per SM):
+//   warp 0  TMA producer (one thread): operand tiles into a ring of shared-memory stages;
+//   warp 1  MMA issuer (one thread): tcgen05.mma 128 x N x 16 steps into a TMEM accumulator;
+//   warp 2  allocates / frees tensor memory (two accumulators, double-buffered);
+//   warps 4-7 epilogue: tcgen05.ld of TMEM lanes 0-127 (one output row per thread), the
+//            fused elementwise step, bf16 stores.
+// Operand tiles use the 128-byte swizzle. K-major tiles are TMA boxes of 64 K-elements x
+// rows; MN-major tiles are boxes of 64 MN-elements x 64 k-rows. Every wait on an mbarrier
+// is bounded in time; a wait that runs out records MOE_ERR_TIMEOUT, stops every role of
+// the CTA and the kernel frees its tensor memory before returning.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "sizes.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 256;
+constexpr int kSmemBudget = 200 * 1024;
+
+enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
+
+template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr bool A_MN = A_MN_;
+    static constexpr bool B_MN = B_MN_;
+    static constexpr bool DUAL = DUAL_;      // two B operands -> two accumulators (G1)
+    static constexpr int EPI = EPI_;
+    static constexpr bool TWO_K = TWO_K_;    // K = [K0 from (a0,b0)] ++ [K1 from (a1,b1)]
+    static constexpr bool WGRAD = WGRAD_;    // M = weight rows, K = expert's token rows
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2 * (DUAL ? 2 : 1);
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (kSmemBudget / STAGE_BYTES) > 6 ? 6 : (kSmemBudget / STAGE_BYTES);
+    static constexpr int ACC_COLS = DUAL ? 2 * BN : BN;
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulator buffers
+    static constexpr uint32_t IDESC = idesc_bf16_m128(BN, A_MN, B_MN);
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory columns");
+    static_assert(BN % 64 == 0 && BN <= 256, "tile width");
+    static constexpr size_t SMEM_BYTES =
+        1024 + (size_t)STAGES * STAGE_BYTES + 1024 /* barriers etc. */ +
+        sizeof(int64_t) * (kMaxExperts + 1) + sizeof(int32_t) * kMaxExperts;
+};
+
+struct Params {
+    const int64_t* row_offsets;  // padded expert segments, or null = one dense expert
+    const int32_t* expert_order; // weight gradients: experts in descending row count
+    int64_t rows;                // extent of the token dimension
+    int E;
+    int N;      // output columns
+    int K0;     // token-major: reduction length of operand pair 0
+    int K1;     // token-major: reduction length of operand pair 1 (TWO_K)
+    int M_out;  // weight gradients: rows of each expert's output
+    int nprob;  // weight gradients: (a0,out0) and, if 2, (a1,out1)
+    int kb_per_expert;  // B operand rows per expert (MN-major weights: K extent per expert)
+    __nv_bfloat16* out0;
+    __nv_bfloat16* out1;
+    __nv_bfloat16* out2;
+    const __nv_bfloat16* in0;  // SwiGLU backward: saved a
+    const __nv_bfloat16* in1;  // SwiGLU backward: saved u
+    int ld_out;
+    int* status;
+    uint64_t wait_limit_ns;
+};
+
+struct TileInfo {
+    int e;       // expert
+    int p;       // weight-gradient problem (0 or 1)
+    int64_t m0;  // token-major: first row; weight gradients: first output row
+    int n0;      // first output column
+    int64_t k_lo;  // weight gradients: first token row of the expert
+    int k_iters;   // 64-wide K blocks
+};
+
+struct SmemLayout {
+    uint8_t* a;        // STAGES x A tile
+    uint8_t* b;        // STAGES x B tile(s)
+    uint64_t* full;    // STAGES
+    uint64_t* empty;   // STAGES
+    uint64_t* tfull;   // 2
+    uint64_t* tempty;  // 2
+    uint32_t* tmem_slot;
+    int* abort_flag;
+    int64_t* offs;     // E + 1
+    int32_t* order;    // E
+};
+
+template <class C>
+__device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
+    SmemLayout s;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.a = base;
+    s.b = base + (size_t)C::STAGES * C::A_BYTES;
+    uint8_t* misc = base + (size_t)C::STAGES * C::STAGE_BYTES;
+    s.full = reinterpret_cast<uint64_t*>(misc);
+    s.empty = s.full + C::STAGES;
+    s.tfull = s.empty + C::STAGES;
+    s.tempty = s.tfull + 2;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.tempty + 2);
+    s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
+    s.offs = reinterpret_cast<int64_t*>(misc + 512);
+    s.order = reinterpret_cast<int32_t*>(s.offs + kMaxExperts + 1);
+    return s;
+}
+
+__device__ __forceinline__ int64_t cdiv_dev(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <class C>
+__device__ __forceinline__ int64_t total_tiles(const Params& P, const SmemLayout& S) {
+    const int n_tiles = P.N / C::BN;
+    if constexpr (C::WGRAD) {
+        return (int64_t)P.E * P.nprob * (P.M_out / BM) * n_tiles;
+    } else {
+        const int64_t mt = P.row_offsets ? S.offs[P.E] / BM : cdiv_dev(P.rows, BM);
+        return mt * n_tiles;
+    }
+}
+
+template <class C>
+__device__ __forceinline__ TileInfo decode(int64_t tile, const Params& P, const SmemLayout& S) {
+    TileInfo ti;
+    const int n_tiles = P.N / C::BN;
+    if constexpr (C::WGRAD) {
+        const int m_tiles = P.M_out / BM;
+        const int64_t per_e = (int64_t)P.nprob * m_tiles * n_tiles;
+        const int oi = (int)(tile / per_e);
+        int64_t rem = tile % per_e;
+        ti.e = S.order[oi];
+        ti.p = (int)(rem / (m_tiles * n_tiles));
+        rem %= (m_tiles * n_tiles);
+        ti.m0 = (rem / n_tiles) * BM;
+        ti.n0 = (int)(rem % n_tiles) * C::BN;
+        int64_t lo = 0, hi = P.rows;
+        if (P.row_offsets) {
+            lo = S.offs[ti.e];
+            hi = S.offs[ti.e + 1];
+        }
+        ti.k_lo = lo;
+        ti.k_iters = (int)cdiv_dev(hi - lo, BK);
+    } else {
+        const int64_t mt = tile / n_tiles;
+        ti.n0 = (int)(tile % n_tiles) * C::BN;
+        ti.m0 = mt * BM;
+        ti.p = 0;
+        ti.k_lo = 0;
+        int e = 0;
+        if (P.row_offsets) {  // last expert whose segment starts at or before m0
+            int lo = 0, hi = P.E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (S.offs[mid] <= ti.m0) lo = mid;
+                else hi = mid - 1;
+            }
+            e = lo;  // among equal offsets (empty experts) the last one owns the rows
+        }
+        ti.e = e;
+        ti.k_iters = (P.K0 + (C::TWO_K ? P.K1 : 0)) / BK;
+    }
+    return ti;
+}
+
+// Loads of K block `kb` of a tile into stage buffers.
+template <class C>
+__device__ __forceinline__ void issue_loads(const TileInfo& ti, int kb, uint32_t a_dst,
+                                            uint32_t b_dst, uint32_t bar, const Params& P,
+                                            const CUtensorMap* ma0, const CUtensorMap* ma1,
+                                            const CUtensorMap* mb0, const CUtensorMap* mb1) {
+    if constexpr (C::WGRAD) {
+        const int32_t krow = (int32_t)(ti.k_lo + (int64_t)kb * BK);
+        const CUtensorMap* ma = ti.p == 0 ? ma0 : ma1;
+        // A: MN-major, two 64-wide boxes along M
+        tma_load_2d(a_dst, ma, bar, (int32_t)ti.m0, krow);
+        tma_load_2d(a_dst + 8192, ma, bar, (int32_t)ti.m0 + 64, krow);
+#pragma unroll
+        for (int j = 0; j < C::BN / 64; ++j)
+            tma_load_2d(b_dst + j * 8192, mb0, bar, ti.n0 + 64 * j, krow);
+    } else {
+        int kk = kb * BK;
+        const CUtensorMap* ma = ma0;
+        const CUtensorMap* mb = mb0;
+        int kper = P.kb_per_expert;
+        if (C::TWO_K && kk >= P.K0) {
+            kk -= P.K0;
+            ma = ma1;
+            mb = mb1;
+        }
+        tma_load_2d(a_dst, ma, bar, kk, (int32_t)ti.m0);
+        if constexpr (C::B_MN) {
+            const int32_t brow = ti.e * kper + kk;
+#pragma unroll
+            for (int j = 0; j < C::BN / 64; ++j)
+                tma_load_2d(b_dst + j * 8192, mb, bar, ti.n0 + 64 * j, brow);
+        } else {
+            const int32_t brow = ti.e * P.N + ti.n0;
+            tma_load_2d(b_dst, C::DUAL ? mb0 : mb, bar, kk, brow);
+            if constexpr (C::DUAL) tma_load_2d(b_dst + C::BN * 128, mb1, bar, kk, brow);
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 pack_chunk8(const float* v) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+
+template <class C>
+__device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc, int row_in_tile,
+                                              const Params& P) {
+    if constexpr (C::WGRAD) {
+        const int64_t row = ti.m0 + row_in_tile;
+        __nv_bfloat16* out = (ti.p == 0 ? P.out0 : P.out1) +
+                             ((int64_t)ti.e * P.M_out + row) * P.N + ti.n0;
+        for (int c = 0; c < C::BN; c += 32) {
+            float v[32];
+            if (ti.k_iters > 0) {
+                uint32_t r[32];
+                tmem_ld32(t_acc + c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = pack_chunk8(v + 8 * q);
+        }
+    } else {
+        const int64_t row = ti.m0 + row_in_tile;
+        const bool ok = row < P.rows;
+        const int64_t base = row * (int64_t)P.ld_out + ti.n0;
+        for (int c = 0; c < C::BN; c += 32) {
+            if constexpr (C::EPI == kEpiSwigluFwd) {
+                uint32_t g[32], u[32];
+                tmem_ld32(t_acc + c, g);
+                tmem_ld32(t_acc + C::BN + c, u);
+                tmem_ld_wait();
+                if (ok) {
+                    float av[32], uv[32], hv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        av[j] = __uint_as_float(g[j]);
+                        uv[j] = __uint_as_float(u[j]);
+                        hv[j] = av[j] / (1.0f + __expf(-av[j])) * uv[j];
+                    }
+                    uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
+                    uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
+                    uint4* dh = reinterpret_cast<uint4*>(P.out2 + base + c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        da[q] = pack_chunk8(av + 8 * q);
+                        du[q] = pack_chunk8(uv + 8 * q);
+                        dh[q] = pack_chunk8(hv + 8 * q);
+                    }
+                }
+            } else if constexpr (C::EPI == kEpiSwigluBwd) {
+                uint32_t r[32];
+                tmem_ld32(t_acc + c, r);
+                tmem_ld_wait();
+                if (ok) {
+                    const uint4* pa = reinterpret_cast<const uint4*>(P.in0 + base + c);
+                    const uint4* pu = reinterpret_cast<const uint4*>(P.in1 + base + c);
+                    float dav[32], duv[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 a4 = pa[q], u4 = pu[q];
+                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) {
+                            const float a = (h & 1) ? bf16_hi(aw[h >> 1]) : bf16_lo(aw[h >> 1]);
+                            const float u = (h & 1) ? bf16_hi(uw[h >> 1]) : bf16_lo(uw[h >> 1]);
+                            const float dh = __uint_as_float(r[8 * q + h]);
+                            const float sa = 1.0f / (1.0f + __expf(-a));
+                            dav[8 * q + h] = dh * u * sa * (1.0f + a * (1.0f - sa));
+                            duv[8 * q + h] = dh * a * sa;
+                        }
+                    }
+                    uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
+                    uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        da[q] = pack_chunk8(dav + 8 * q);
+                        du[q] = pack_chunk8(duv + 8 * q);
+                    }
+                }
+            } else {
+                uint32_t r[32];
+                tmem_ld32(t_acc + c, r);
+                tmem_ld_wait();
+                if (ok) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    uint4* dst = reinterpret_cast<uint4*>(P.out0 + base + c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = pack_chunk8(v + 8 * q);
+                }
+            }
+        }
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap ma0,
+                        const __grid_constant__ CUtensorMap ma1,
+                        const __grid_constant__ CUtensorMap mb0,
+                        const __grid_constant__ CUtensorMap mb1, const Params P) {
+    extern __shared__ uint8_t gg_smem_raw[];
+    const SmemLayout S = carve<C>(gg_smem_raw);
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);
+            mbar_init(smem_u32(&S.empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&S.tfull[b]), 1);
+            mbar_init(smem_u32(&S.tempty[b]), 4);
+        }
+        *S.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (P.row_offsets)
+        for (int i = tid; i <= P.E; i += kThreads) S.offs[i] = P.row_offsets[i];
+    if (C::WGRAD)
+        for (int i = tid; i < P.E; i += kThreads) S.order[i] = P.expert_order ? P.expert_order[i] : i;
+    if (warp == 2) {
+        tmem_alloc(smem_u32(S.tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *S.tmem_slot;
+    volatile int* abort_flag = S.abort_flag;
+
+    bool layout_ok = true;
+    if (!C::WGRAD && P.row_offsets && S.offs[P.E] > P.rows) layout_ok = false;
+    if (C::WGRAD && P.row_offsets && S.offs[P.E] > P.rows) layout_ok = false;
+    if (!layout_ok && tid == 0) record_error(P.status, MOE_ERR_BAD_INDEX, 20);
+    const int64_t ntiles = layout_ok ? total_tiles<C>(P, S) : 0;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer
+        tma_prefetch_desc(&ma0);
+        tma_prefetch_desc(&mb0);
+        if (C::TWO_K || C::WGRAD) tma_prefetch_desc(&ma1);
+        if (C::TWO_K || C::DUAL) tma_prefetch_desc(&mb1);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const TileInfo ti = decode<C>(tile, P, S);
+            bool ok = true;
+            for (int kb = 0; kb < ti.k_iters; ++kb) {
+                if (!mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1u, abort_flag, P.status,
+                                       P.wait_limit_ns, 30)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = smem_u32(&S.full[stage]);
+                mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                issue_loads<C>(ti, kb, smem_u32(S.a + (size_t)stage * C::A_BYTES),
+                               smem_u32(S.b + (size_t)stage * C::B_BYTES), full, P, &ma0, &ma1,
+                               &mb0, &mb1);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+            const TileInfo ti = decode<C>(tile, P, S);
+            const int buf = local & 1;
+            const uint32_t use = (local >> 1) & 1;
+            if (!mbar_wait_bounded(smem_u32(&S.tempty[buf]), use ^ 1u, abort_flag, P.status,
+                                   P.wait_limit_ns, 31))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS;
+            bool ok = true;
+            for (int kb = 0; kb < ti.k_iters; ++kb) {
+                if (!mbar_wait_bounded(smem_u32(&S.full[stage]), phase, abort_flag, P.status,
+                                       P.wait_limit_ns, 32)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_s = smem_u32(S.a + (size_t)stage * C::A_BYTES);
+                const uint32_t b_s = smem_u32(S.b + (size_t)stage * C::B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t adesc = C::A_MN ? sdesc_sw128(a_s + kk * 2048, 8192, 1024)
+                                                   : sdesc_sw128(a_s + kk * 32, 16, 1024);
+                    const uint64_t bdesc = C::B_MN ? sdesc_sw128(b_s + kk * 2048, 8192, 1024)
+                                                   : sdesc_sw128(b_s + kk * 32, 16, 1024);
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    umma_bf16(d_tmem, adesc, bdesc, C::IDESC, acc);
+                    if constexpr (C::DUAL) {
+                        const uint64_t b1desc = sdesc_sw128(b_s + C::BN * 128 + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem + C::BN, adesc, b1desc, C::IDESC, acc);
+                    }
+                }
+                umma_commit(smem_u32(&S.empty[stage]));
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(smem_u32(&S.tfull[buf]));
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
+        const int row_in_tile = 32 * q + lane;
+        int local = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+            const TileInfo ti = decode<C>(tile, P, S);
+            const int buf = local & 1;
+            const uint32_t ph = (local >> 1) & 1;
+            bool ok = mbar_wait_bounded(smem_u32(&S.tfull[buf]), ph, abort_flag, P.status,
+                                        P.wait_limit_ns, 33);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t_acc = tmem_base + buf * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
+            epilogue_tile<C>(ti, t_acc, row_in_tile, P);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.tempty[buf]));
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+    if (*abort_flag) {  // let copies still in flight land before the CTA exits
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+    }
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Experts in descending padded row count (ties: lower index), for the weight-gradient
+// tile order: the longest reductions are scheduled first.
+__global__ void expert_order_kernel(const int64_t* __restrict__ row_offsets, int E,
+                                    int32_t* __restrict__ order) {
+    const int e = threadIdx.x;
+    if (e >= E) return;
+    const int64_t ce = row_offsets[e + 1] - row_offsets[e];
+    int rank = 0;
+    for (int j = 0; j < E; ++j) {
+        const int64_t cj = row_offsets[j + 1] - row_offsets[j];
+        if (cj > ce || (cj == ce && j < e)) ++rank;
+    }
+    order[rank] = e;
+}
+
+// ---------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] matrix, 128-byte swizzled boxes.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+    auto enc = get_encoder();
+    if (!enc || !base) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <class C>
+int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+           const CUtensorMap& b1, const Params& P, int64_t max_tiles, cudaStream_t st) {
+    static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM_BYTES) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    int64_t grid = sm_count();
+    if (max_tiles < grid) grid = max_tiles;
+    if (grid < 1) grid = 1;
+    grouped_gemm_kernel<C><<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, P);
+    return launch_status();
+}
+
+// Configurations of the layer's GEMMs.
+using CfgG1 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false>;
+template <int BN> using CfgStoreK = Cfg<BN, false, false, false, kEpiStore, false, false>;
+template <int BN> using CfgSwigluBwd = Cfg<BN, false, true, false, kEpiSwigluBwd, false, false>;
+template <int BN> using CfgDgrad2 = Cfg<BN, false, true, false, kEpiStore, true, false>;
+template <int BN> using CfgWgrad = Cfg<BN, true, true, false, kEpiStore, false, true>;
+
+Params base_params(const int64_t* row_offsets, int64_t rows, int E) {
+    Params P{};
+    P.row_offsets = row_offsets;
+    P.rows = rows;
+    P.E = E;
+    P.status = device_status_word();
+    P.wait_limit_ns = wait_limit_ns();
+    return P;
+}
+
+int64_t token_tiles_max(int64_t rows, int N, int BN) { return cdiv(rows, BM) * (N / BN); }
+
+bool gemm_shape_ok(int d, int f) { return d % 128 == 0 && f % 128 == 0 && d > 0 && f > 0; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int E, int64_t rows,
+                              int d, int f, const moe_bf16* W_g, const moe_bf16* W_u,
+                              const moe_bf16* W_d, moe_bf16* A, moe_bf16* U, moe_bf16* H,
+                              moe_bf16* Y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!X || !W_g || !W_u || !W_d || !A || !U || !H || !Y) return MOE_ERR_INVALID_ARG;
+    if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
+    const void* ptrs[8] = {X, W_g, W_u, W_d, A, U, H, Y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    if (!device_status_word()) return MOE_ERR_LAUNCH;
+    cudaStream_t st = (cudaStream_t)stream;
+    CUtensorMap mx, mwg, mwu, mh, mwd;
+    if (!make_map(&mx, X, d, rows, 64, 128) || !make_map(&mwg, W_g, d, (uint64_t)E * f, 64, 128) ||
+        !make_map(&mwu, W_u, d, (uint64_t)E * f, 64, 128) || !make_map(&mh, H, f, rows, 64, 128))
+        return MOE_ERR_LAUNCH;
+    // G1: a, u, h
+    Params P = base_params(row_offsets, rows, E);
+    P.N = f;
+    P.K0 = d;
+    P.out0 = reinterpret_cast<__nv_bfloat16*>(A);
+    P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
+    P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
+    P.ld_out = f;
+    int rc = launch<CfgG1>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st);
+    if (rc != MOE_OK) return rc;
+    // G2: y = h W_d^T
+    Params Q = base_params(row_offsets, rows, E);
+    Q.N = d;
+    Q.K0 = f;
+    Q.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
+    Q.ld_out = d;
+    if (d % 256 == 0) {
+        if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 256)) return MOE_ERR_LAUNCH;
+        rc = launch<CfgStoreK<256>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st);
+    } else {
+        if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
+        rc = launch<CfgStoreK<128>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st);
+    }
+    return rc;
+}
+
+extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
+                              const moe_bf16* U, const moe_bf16* H, const int64_t* row_offsets,
+                              int E, int64_t rows, int d, int f, const moe_bf16* W_g,
+                              const moe_bf16* W_u, const moe_bf16* W_d, moe_bf16* dX,
+                              moe_bf16* dA, moe_bf16* dU, moe_bf16* dW_g, moe_bf16* dW_u,
+                              moe_bf16* dW_d, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!dY || !X || !A || !U || !H || !W_g || !W_u || !W_d || !dX || !dA || !dU || !dW_g ||
+        !dW_u || !dW_d)
+        return MOE_ERR_INVALID_ARG;
+    if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
+    const void* ptrs[14] = {dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    if (!device_status_word()) return MOE_ERR_LAUNCH;
+    WsCarver wc(ws, ws_bytes);
+    int32_t* order = wc.take<int32_t>(E + 1);
+    if (row_offsets && (!ws || !wc.ok())) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const __nv_bfloat16* Ab = reinterpret_cast<const __nv_bfloat16*>(A);
+    const __nv_bfloat16* Ub = reinterpret_cast<const __nv_bfloat16*>(U);
+    int rc;
+
+    // B2: dH = dY W_d (W_d[e] is [d, f]: K = d rows, N = f contiguous), SwiGLU backward
+    {
+        CUtensorMap mdy, mwd;
+        if (!make_map(&mdy, dY, d, rows, 64, 128) || !make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 64))
+            return MOE_ERR_LAUNCH;
+        Params P = base_params(row_offsets, rows, E);
+        P.N = f;
+        P.K0 = d;
+        P.kb_per_expert = d;
+        P.out0 = reinterpret_cast<__nv_bfloat16*>(dA);
+        P.out1 = reinterpret_cast<__nv_bfloat16*>(dU);
+        P.in0 = Ab;
+        P.in1 = Ub;
+        P.ld_out = f;
+        if (f % 256 == 0)
+            rc = launch<CfgSwigluBwd<256>>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 256), st);
+        else
+            rc = launch<CfgSwigluBwd<128>>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 128), st);
+        if (rc != MOE_OK) return rc;
+    }
+    // B4: dX = dA W_g + dU W_u (W_g[e] is [f, d]: K = f rows, N = d contiguous)
+    {
+        CUtensorMap mda, mdu, mwg, mwu;
+        if (!make_map(&mda, dA, f, rows, 64, 128) || !make_map(&mdu, dU, f, rows, 64, 128) ||
+            !make_map(&mwg, W_g, d, (uint64_t)E * f, 64, 64) ||
+            !make_map(&mwu, W_u, d, (uint64_t)E * f, 64, 64))
+            return MOE_ERR_LAUNCH;
+        Params P = base_params(row_offsets, rows, E);
+        P.N = d;
+        P.K0 = f;
+        P.K1 = f;
+        P.kb_per_expert = f;
+        P.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
+        P.ld_out = d;
+        if (d % 256 == 0)
+            rc = launch<CfgDgrad2<256>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 256), st);
+        else
+            rc = launch<CfgDgrad2<128>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 128), st);
+        if (rc != MOE_OK) return rc;
+    }
+    if (row_offsets) {
+        expert_order_kernel<<<1, kMaxExperts, 0, st>>>(row_offsets, E, order);
+        if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
+    }
+    const int32_t* order_ptr = row_offsets ? order : nullptr;
+    // B3: dW_d[e] = dY_e^T H_e  (M = d, N = f, K = the expert's rows)
+    {
+        CUtensorMap mdy, mh;
+        if (!make_map(&mdy, dY, d, rows, 64, 64) || !make_map(&mh, H, f, rows, 64, 64))
+            return MOE_ERR_LAUNCH;
+        Params P = base_params(row_offsets, rows, E);
+        P.expert_order = order_ptr;
+        P.N = f;
+        P.M_out = d;
+        P.nprob = 1;
+        P.out0 = reinterpret_cast<__nv_bfloat16*>(dW_d);
+        if (f % 256 == 0)
+            rc = launch<CfgWgrad<256>>(mdy, mdy, mh, mh, P, (int64_t)E * (d / BM) * (f / 256), st);
+        else
+            rc = launch<CfgWgrad<128>>(mdy, mdy, mh, mh, P, (int64_t)E * (d / BM) * (f / 128), st);
+        if (rc != MOE_OK) return rc;
+    }
+    // B5: dW_g[e] = dA_e^T X_e, dW_u[e] = dU_e^T X_e  (M = f, N = d)
+    {
+        CUtensorMap mda, mdu, mxx;
+        if (!make_map(&mda, dA, f, rows, 64, 64) || !make_map(&mdu, dU, f, rows, 64, 64) ||
+            !make_map(&mxx, X, d, rows, 64, 64))
+            return MOE_ERR_LAUNCH;
+        Params P = base_params(row_offsets, rows, E);
+        P.expert_order = order_ptr;
+        P.N = d;
+        P.M_out = f;
+        P.nprob = 2;
+        P.out0 = reinterpret_cast<__nv_bfloat16*>(dW_g);
+        P.out1 = reinterpret_cast<__nv_bfloat16*>(dW_u);
+        if (d % 256 == 0)
+            rc = launch<CfgWgrad<256>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 256), st);
+        else
+            rc = launch<CfgWgrad<128>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 128), st);
+    }
+    return rc;
+}

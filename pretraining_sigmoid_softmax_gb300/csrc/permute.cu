@@ -1,0 +1,496 @@
+// Token dispatch (histogram, scan, stable expert-major permutation, 16-byte row copies),
+// the gate-weighted combine, their backward passes and the aux-loss-free bias update.
+//
+// Dispatch and combine: handbook summary ("How to train a large-scale Mixture-of-Experts
+// model from scratch"), section 2.5: tokens must be sent to the chosen experts and each
+// expert's output returned. Bias update: "The whole stack, in the open" (Apex-3), "What's
+// inside", row "Fine-grained MoE": a per-expert bias balances the load without a loss term.
+//
+// These steps move bytes: every row copy is a warp-wide run of 16-byte vectors so each
+// memory instruction touches whole 512-byte spans. Counting uses integer atomics in shared
+// memory only (order-independent); every floating-point sum has a fixed order.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "sizes.h"
+
+namespace moe {
+namespace {
+
+constexpr int kHistThreads = 256;
+constexpr int kScatterThreads = kHistTokensPerCta;  // one token per thread
+constexpr int kWarpsPerCta = 8;                     // warp-per-token kernels
+
+// Expert of slot (t, i), or -1 when the index is out of range or repeats an earlier slot
+// of the same token (both are input errors; the slot is dropped).
+__device__ __forceinline__ int valid_expert(const int32_t* __restrict__ idx, int64_t t, int k,
+                                            int i, int E) {
+    const int e = idx[t * k + i];
+    if (e < 0 || e >= E) return -1;
+    for (int j = 0; j < i; ++j)
+        if (idx[t * k + j] == e) return -1;
+    return e;
+}
+
+__global__ void __launch_bounds__(kHistThreads) hist_kernel(const int32_t* __restrict__ idx,
+                                                            int64_t T, int E, int k,
+                                                            int32_t* __restrict__ block_counts,
+                                                            int* status) {
+    __shared__ int cnt[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += kHistThreads) cnt[e] = 0;
+    __syncthreads();
+    const int64_t t0 = (int64_t)blockIdx.x * kHistTokensPerCta;
+    for (int q = threadIdx.x; q < kHistTokensPerCta; q += kHistThreads) {
+        const int64_t t = t0 + q;
+        if (t >= T) break;
+        for (int i = 0; i < k; ++i) {
+            const int e = valid_expert(idx, t, k, i, E);
+            if (e >= 0) atomicAdd(&cnt[e], 1);
+            else record_error(status, MOE_ERR_BAD_INDEX, 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kHistThreads)
+        block_counts[(int64_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// One CTA: per-expert running sums over the chunks (block bases), counts, the unpadded
+// offsets and the 128-row padded segment offsets.
+__global__ void __launch_bounds__(kMaxExperts) scan_kernel(
+    const int32_t* __restrict__ block_counts, int64_t nblocks, int E,
+    int32_t* __restrict__ block_base, int32_t* __restrict__ counts, int64_t* __restrict__ offsets,
+    int64_t* __restrict__ row_offsets) {
+    __shared__ int32_t c_sh[kMaxExperts];
+    const int e = threadIdx.x;
+    if (e < E) {
+        int32_t run = 0;
+        int64_t b = 0;
+        for (; b + 4 <= nblocks; b += 4) {  // four independent loads in flight
+            const int32_t v0 = block_counts[(b + 0) * E + e];
+            const int32_t v1 = block_counts[(b + 1) * E + e];
+            const int32_t v2 = block_counts[(b + 2) * E + e];
+            const int32_t v3 = block_counts[(b + 3) * E + e];
+            block_base[(b + 0) * E + e] = run;
+            block_base[(b + 1) * E + e] = run + v0;
+            block_base[(b + 2) * E + e] = run + v0 + v1;
+            block_base[(b + 3) * E + e] = run + v0 + v1 + v2;
+            run += v0 + v1 + v2 + v3;
+        }
+        for (; b < nblocks; ++b) {
+            const int32_t v = block_counts[b * E + e];
+            block_base[b * E + e] = run;
+            run += v;
+        }
+        counts[e] = run;
+        c_sh[e] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t o = 0, ro = 0;
+        for (int j = 0; j < E; ++j) {
+            offsets[j] = o;
+            row_offsets[j] = ro;
+            o += c_sh[j];
+            ro += (c_sh[j] + MOE_ROW_ALIGN - 1) / MOE_ROW_ALIGN * MOE_ROW_ALIGN;
+        }
+        offsets[E] = o;
+        row_offsets[E] = ro;
+    }
+}
+
+// Padding rows of each expert segment: perm_token = -1 and (optionally) a zero row.
+__global__ void __launch_bounds__(256) pad_rows_kernel(const int64_t* __restrict__ row_offsets,
+                                                       const int32_t* __restrict__ counts,
+                                                       int d, int32_t* __restrict__ perm_token,
+                                                       __nv_bfloat16* __restrict__ buf) {
+    const int e = blockIdx.x;
+    const int64_t lo = row_offsets[e] + counts[e], hi = row_offsets[e + 1];
+    const int vec_per_row = d / 8;
+    for (int64_t i = threadIdx.x; i < (hi - lo) * vec_per_row; i += blockDim.x) {
+        const int64_t r = lo + i / vec_per_row;
+        const int c = (int)(i % vec_per_row);
+        reinterpret_cast<uint4*>(buf + r * d)[c] = make_uint4(0, 0, 0, 0);
+        if (c == 0 && perm_token) perm_token[r] = -1;
+    }
+}
+
+// Zero the padding rows of each segment, found as the trailing rows with perm_token < 0.
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int64_t* __restrict__ row_offsets,
+                                                            const int32_t* __restrict__ perm_token,
+                                                            int d, __nv_bfloat16* __restrict__ buf) {
+    const int e = blockIdx.x;
+    const int64_t hi = row_offsets[e + 1];
+    int64_t lo = row_offsets[e];
+    if (hi - lo > MOE_ROW_ALIGN - 1) lo = hi - (MOE_ROW_ALIGN - 1);
+    const int vec_per_row = d / 8;
+    for (int64_t i = threadIdx.x; i < (hi - lo) * vec_per_row; i += blockDim.x) {
+        const int64_t r = lo + i / vec_per_row;
+        if (perm_token[r] < 0)
+            reinterpret_cast<uint4*>(buf + r * d)[i % vec_per_row] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Stable ranks: within a chunk of 1024 tokens, warp w owns tokens [32 w, 32 w + 32).
+// Row of (t, i) = row_offsets[e] + chunk base of e + warp base of e + rank within warp.
+__global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
+    const int32_t* __restrict__ idx, int64_t T, int E, int k,
+    const int32_t* __restrict__ block_base, const int64_t* __restrict__ row_offsets,
+    int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_to_row) {
+    extern __shared__ int32_t sc_smem[];
+    int32_t* wcnt = sc_smem;                                                       // [32][E]
+    uint32_t* wmask = reinterpret_cast<uint32_t*>(sc_smem + 32 * E);              // [32][E]
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    for (int i = tid; i < 32 * E; i += kScatterThreads) {
+        wcnt[i] = 0;
+        wmask[i] = 0u;
+    }
+    __syncthreads();
+    const int64_t t = (int64_t)blockIdx.x * kHistTokensPerCta + tid;
+    const bool live = t < T;
+    if (live)
+        for (int i = 0; i < k; ++i) {
+            const int e = valid_expert(idx, t, k, i, E);
+            if (e >= 0) {
+                atomicAdd(&wcnt[warp * E + e], 1);
+                atomicOr(&wmask[warp * E + e], 1u << lane);
+            }
+        }
+    __syncthreads();
+    if (tid < E) {  // exclusive scan over warps, per expert
+        int32_t run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int32_t c = wcnt[w * E + tid];
+            wcnt[w * E + tid] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    if (!live) return;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int i = 0; i < k; ++i) {
+        const int e = valid_expert(idx, t, k, i, E);
+        int32_t row = -1;
+        if (e >= 0) {
+            const int rank = __popc(wmask[warp * E + e] & lt_mask);
+            row = (int32_t)(row_offsets[e] + block_base[(int64_t)blockIdx.x * E + e] +
+                            wcnt[warp * E + e] + rank);
+            perm_token[row] = (int32_t)t;
+        }
+        slot_to_row[t * k + i] = row;
+    }
+}
+
+// Copy x[t] to the k rows of token t: one warp per token, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ x,
+                                                     const int32_t* __restrict__ slot_to_row,
+                                                     int64_t T, int d, int k,
+                                                     __nv_bfloat16* __restrict__ X_perm) {
+    const int lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
+    if (t >= T) return;
+    int32_t my_row = -1;
+    if (lane < k) my_row = slot_to_row[t * k + lane];
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+    const int nvec = d / 8;
+    for (int c0 = 0; c0 < nvec; c0 += 32) {  // warp-uniform trip count
+        const int c = c0 + lane;
+        const bool in = c < nvec;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (in) v = src[c];
+        for (int i = 0; i < k; ++i) {
+            const int32_t row = __shfl_sync(0xffffffffu, my_row, i);
+            if (in && row >= 0) reinterpret_cast<uint4*>(X_perm + (int64_t)row * d)[c] = v;
+        }
+    }
+}
+
+__device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4 v, float g) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = fmaf(g, bf16_lo(w[q]), acc[2 * q]);
+        acc[2 * q + 1] = fmaf(g, bf16_hi(w[q]), acc[2 * q + 1]);
+    }
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += bf16_lo(w[q]);
+        acc[2 * q + 1] += bf16_hi(w[q]);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
+    return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                      pack_bf16x2(a[6], a[7]));
+}
+
+// out[t] = sum_i g[t,i] * Y_perm[row(t,i)] (+ Y_shared[t]); fp32, slot order, shared last.
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ Y_perm,
+                                                      const float* __restrict__ gate,
+                                                      const int32_t* __restrict__ slot_to_row,
+                                                      const __nv_bfloat16* __restrict__ Y_sh,
+                                                      int64_t T, int d, int k,
+                                                      __nv_bfloat16* __restrict__ out) {
+    const int lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
+    if (t >= T) return;
+    int32_t my_row = -1;
+    float my_g = 0.f;
+    if (lane < k) {
+        my_row = slot_to_row[t * k + lane];
+        my_g = gate[t * k + lane];
+    }
+    const int nvec = d / 8;
+    for (int c0 = 0; c0 < nvec; c0 += 32) {  // warp-uniform trip count
+        const int c = c0 + lane;
+        const bool in = c < nvec;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < k; ++i) {
+            const int32_t row = __shfl_sync(0xffffffffu, my_row, i);
+            const float g = __shfl_sync(0xffffffffu, my_g, i);
+            if (in && row >= 0)
+                acc_bf16x8(acc, reinterpret_cast<const uint4*>(Y_perm + (int64_t)row * d)[c], g);
+        }
+        if (!in) continue;
+        if (Y_sh) add_bf16x8(acc, reinterpret_cast<const uint4*>(Y_sh + t * d)[c]);
+        reinterpret_cast<uint4*>(out + t * d)[c] = pack8(acc);
+    }
+}
+
+// dY_perm[row(t,i)] = bf16(g[t,i] * dY[t]); dg[t,i] = <dY[t], Y_perm[row(t,i)]>.
+template <int KMAX>
+__global__ void __launch_bounds__(256) combine_bwd_kernel(
+    const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ Y_perm,
+    const float* __restrict__ gate, const int32_t* __restrict__ slot_to_row, int64_t T, int d,
+    int k, __nv_bfloat16* __restrict__ dY_perm, float* __restrict__ dg) {
+    const int lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
+    if (t >= T) return;
+    int32_t my_row = -1;
+    float my_g = 0.f;
+    if (lane < k) {
+        my_row = slot_to_row[t * k + lane];
+        my_g = gate[t * k + lane];
+    }
+    float dot[KMAX];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) dot[i] = 0.f;
+    const int nvec = d / 8;
+    for (int c0 = 0; c0 < nvec; c0 += 32) {  // warp-uniform trip count
+        const int c = c0 + lane;
+        const bool in = c < nvec;
+        uint4 dv = make_uint4(0, 0, 0, 0);
+        if (in) dv = reinterpret_cast<const uint4*>(dY + t * d)[c];
+        const uint32_t w[4] = {dv.x, dv.y, dv.z, dv.w};
+        float dyf[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            dyf[2 * q] = bf16_lo(w[q]);
+            dyf[2 * q + 1] = bf16_hi(w[q]);
+        }
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+            if (i < k) {
+                const int32_t row = __shfl_sync(0xffffffffu, my_row, i);
+                const float g = __shfl_sync(0xffffffffu, my_g, i);
+                if (in && row >= 0) {
+                    const uint4 yv = reinterpret_cast<const uint4*>(Y_perm + (int64_t)row * d)[c];
+                    const uint32_t y[4] = {yv.x, yv.y, yv.z, yv.w};
+                    float s = dot[i];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        s = fmaf(dyf[2 * q], bf16_lo(y[q]), s);
+                        s = fmaf(dyf[2 * q + 1], bf16_hi(y[q]), s);
+                    }
+                    dot[i] = s;
+                    float o[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o[q] = g * dyf[q];
+                    reinterpret_cast<uint4*>(dY_perm + (int64_t)row * d)[c] = pack8(o);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
+        if (i < k) {
+            float s = dot[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) dg[t * k + i] = s;
+        }
+    }
+}
+
+// dx[t] = sum_i dX_perm[row(t,i)] + dx_shared[t] + sum_e dlogits[t,e] W_r[e].
+__global__ void __launch_bounds__(256) permute_bwd_kernel(
+    const __nv_bfloat16* __restrict__ dX_perm, const int32_t* __restrict__ slot_to_row,
+    const __nv_bfloat16* __restrict__ dx_sh, const float* __restrict__ dlogits,
+    const float* __restrict__ W_r, int64_t T, int d, int E, int k,
+    __nv_bfloat16* __restrict__ dx) {
+    const int lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
+    if (t >= T) return;
+    int32_t my_row = -1;
+    if (lane < k) my_row = slot_to_row[t * k + lane];
+    const int nvec = d / 8;
+    int32_t rows[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rows[i] = __shfl_sync(0xffffffffu, my_row, i);
+    for (int c = lane; c < nvec; c += 32) {  // no warp collectives inside
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i < k && rows[i] >= 0)
+                add_bf16x8(acc, reinterpret_cast<const uint4*>(dX_perm + (int64_t)rows[i] * d)[c]);
+        }
+        if (dx_sh) add_bf16x8(acc, reinterpret_cast<const uint4*>(dx_sh + t * d)[c]);
+        if (dlogits) {
+            for (int e = 0; e < E; ++e) {
+                const float g = dlogits[t * E + e];  // same address across the warp
+                if (g != 0.f) {
+                    const float4* w = reinterpret_cast<const float4*>(W_r + (int64_t)e * d + c * 8);
+                    const float4 a = w[0], b = w[1];
+                    acc[0] = fmaf(g, a.x, acc[0]);
+                    acc[1] = fmaf(g, a.y, acc[1]);
+                    acc[2] = fmaf(g, a.z, acc[2]);
+                    acc[3] = fmaf(g, a.w, acc[3]);
+                    acc[4] = fmaf(g, b.x, acc[4]);
+                    acc[5] = fmaf(g, b.y, acc[5]);
+                    acc[6] = fmaf(g, b.z, acc[6]);
+                    acc[7] = fmaf(g, b.w, acc[7]);
+                }
+            }
+        }
+        reinterpret_cast<uint4*>(dx + t * d)[c] = pack8(acc);
+    }
+}
+
+__global__ void bias_update_kernel(const int32_t* __restrict__ counts, int E, int64_t T, int k,
+                                   float gamma, float* __restrict__ b) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    // sign(T*k/E - c) == sign(T*k - E*c), exact in integers
+    const int64_t diff = T * (int64_t)k - (int64_t)E * counts[e];
+    const float sgn = diff > 0 ? 1.f : (diff < 0 ? -1.f : 0.f);
+    b[e] = b[e] + gamma * sgn;
+}
+
+inline unsigned warp_grid(int64_t T) { return (unsigned)cdiv(T, kWarpsPerCta); }
+
+bool shape_ok(int64_t T, int d, int E, int k) {
+    return T > 0 && d > 0 && E > 0 && k > 0;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, int E,
+                           int k, int32_t* counts, int64_t* offsets, int64_t* row_offsets,
+                           int32_t* perm_token, int32_t* slot_to_row, moe_bf16* X_perm,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!topk_idx || !x || !counts || !offsets || !row_offsets || !perm_token || !slot_to_row ||
+        !X_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(X_perm)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    int* status = device_status_word();
+    if (!status) return MOE_ERR_LAUNCH;
+    const int64_t nb = hist_blocks(T);
+    WsCarver wc(ws, ws_bytes);
+    int32_t* bcounts = wc.take<int32_t>(nb * E);
+    int32_t* bbase = wc.take<int32_t>(nb * E);
+    if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    hist_kernel<<<(unsigned)nb, kHistThreads, 0, st>>>(topk_idx, T, E, k, bcounts, status);
+    scan_kernel<<<1, kMaxExperts, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
+    pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, counts, d, perm_token,
+                                       reinterpret_cast<__nv_bfloat16*>(X_perm));
+    const size_t sc_smem = sizeof(int32_t) * 64 * E;
+    if (cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sc_smem) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    scatter_kernel<<<(unsigned)nb, kScatterThreads, sc_smem, st>>>(topk_idx, T, E, k, bbase,
+                                                                   row_offsets, perm_token,
+                                                                   slot_to_row);
+    gather_kernel<<<warp_grid(T), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x),
+                                                slot_to_row, T, d, k,
+                                                reinterpret_cast<__nv_bfloat16*>(X_perm));
+    return launch_status();
+}
+
+extern "C" int moe_combine(const moe_bf16* Y_perm, const float* topk_gate,
+                           const int32_t* slot_to_row, const moe_bf16* Y_shared, int64_t T,
+                           int d, int k, moe_bf16* out, moe_stream_t stream) {
+    if (!Y_perm || !topk_gate || !slot_to_row || !out) return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(T, d, 1, k)) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(Y_perm) || !aligned16(out) || (Y_shared && !aligned16(Y_shared)))
+        return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    combine_kernel<<<warp_grid(T), 256, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(Y_perm), topk_gate, slot_to_row,
+        reinterpret_cast<const __nv_bfloat16*>(Y_shared), T, d, k,
+        reinterpret_cast<__nv_bfloat16*>(out));
+    return launch_status();
+}
+
+extern "C" int moe_bias_update(const int32_t* counts, int E, int64_t T, int k, float gamma,
+                               float* b, moe_stream_t stream) {
+    if (!counts || !b || E <= 0 || T <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    bias_update_kernel<<<(unsigned)cdiv(E, 256), 256, 0, (cudaStream_t)stream>>>(counts, E, T, k,
+                                                                                gamma, b);
+    return launch_status();
+}
+
+extern "C" int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm,
+                               const float* topk_gate, const int32_t* slot_to_row,
+                               const int64_t* row_offsets, const int32_t* perm_token,
+                               int64_t T, int d, int E, int k, moe_bf16* dY_perm, float* dg,
+                               moe_stream_t stream) {
+    if (!dY || !Y_perm || !topk_gate || !slot_to_row || !row_offsets || !perm_token ||
+        !dY_perm || !dg)
+        return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(dY) || !aligned16(Y_perm) || !aligned16(dY_perm)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const __nv_bfloat16* dYb = reinterpret_cast<const __nv_bfloat16*>(dY);
+    const __nv_bfloat16* Yb = reinterpret_cast<const __nv_bfloat16*>(Y_perm);
+    __nv_bfloat16* dYp = reinterpret_cast<__nv_bfloat16*>(dY_perm);
+    if (k <= 2) combine_bwd_kernel<2><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
+    else if (k <= 4) combine_bwd_kernel<4><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
+    else if (k <= 8) combine_bwd_kernel<8><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
+    else if (k <= 16) combine_bwd_kernel<16><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
+    else combine_bwd_kernel<32><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
+    zero_pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    return launch_status();
+}
+
+extern "C" int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_row,
+                               const moe_bf16* dx_shared, const float* dlogits,
+                               const float* W_r, int64_t T, int d, int E, int k, moe_bf16* dx,
+                               moe_stream_t stream) {
+    if (!dX_perm || !slot_to_row || !dx) return MOE_ERR_INVALID_ARG;
+    if ((dlogits == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(dX_perm) || !aligned16(dx) || (dx_shared && !aligned16(dx_shared)) ||
+        (W_r && !aligned16(W_r)))
+        return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    permute_bwd_kernel<<<warp_grid(T), 256, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(dX_perm), slot_to_row,
+        reinterpret_cast<const __nv_bfloat16*>(dx_shared), dlogits, W_r, T, d, E, k,
+        reinterpret_cast<__nv_bfloat16*>(dx));
+    return launch_status();
+}

@@ -1,0 +1,244 @@
+"""The MoE layer step on one GPU, as a sequence of C-ABI calls on one stream.
+
+Forward (route -> permute -> routed experts -> shared expert -> combine) and backward
+(combine backward -> routed experts backward -> shared expert backward -> router backward
+-> input gradient), then the aux-loss-free bias update. Every step runs in the library's
+CUDA kernels; this module only owns the device buffers (allocated once per shape) and the
+call order.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import ops
+
+
+@dataclass
+class MoEShape:
+    T: int
+    d: int
+    E: int
+    k: int
+    f: int
+    f_shared: int = 0
+    mode: int = ops.MODE_SIGMOID
+    z_coef: float = 0.0
+
+    @classmethod
+    def from_config(cls, cfg) -> "MoEShape":
+        return cls(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_shared, cfg.mode_id, cfg.z_coef)
+
+
+def _empty(shape, dtype, dev):
+    return torch.empty(shape, dtype=dtype, device=dev)
+
+
+class MoEPlan:
+    """Device buffers of one layer shape and the forward / backward call sequences."""
+
+    def __init__(self, shape: MoEShape, device="cuda", backward: bool = True):
+        s = self.s = shape
+        dev = torch.device(device)
+        bf, f32, i32, i64 = torch.bfloat16, torch.float32, torch.int32, torch.int64
+        T, d, E, k, f, fs = s.T, s.d, s.E, s.k, s.f, s.f_shared
+        R = ops.moe_padded_rows(T, k, E)
+        self.R = R
+        self.ws = _empty((ops.moe_workspace_bytes(T, d, E, k),), torch.uint8, dev)
+        self.logits = _empty((T, E), f32, dev)
+        self.topk_idx = _empty((T, k), i32, dev)
+        self.topk_gate = _empty((T, k), f32, dev)
+        self.topk_score = _empty((T, k), f32, dev)
+        self.lse = _empty((T,), f32, dev)
+        self.z_loss = torch.zeros((1,), dtype=f32, device=dev)
+        self.counts = _empty((E,), i32, dev)
+        self.offsets = _empty((E + 1,), i64, dev)
+        self.row_offsets = _empty((E + 1,), i64, dev)
+        self.perm_token = _empty((R,), i32, dev)
+        self.slot_to_row = _empty((T, k), i32, dev)
+        self.X_perm = _empty((R, d), bf, dev)
+        self.A = _empty((R, f), bf, dev)
+        self.U = _empty((R, f), bf, dev)
+        self.H = _empty((R, f), bf, dev)
+        self.Y_perm = _empty((R, d), bf, dev)
+        self.out = _empty((T, d), bf, dev)
+        if fs:
+            self.As = _empty((T, fs), bf, dev)
+            self.Us = _empty((T, fs), bf, dev)
+            self.Hs = _empty((T, fs), bf, dev)
+            self.Ys = _empty((T, d), bf, dev)
+        self.has_backward = backward
+        if backward:
+            self.dY_perm = _empty((R, d), bf, dev)
+            self.dg = _empty((T, k), f32, dev)
+            self.dA = _empty((R, f), bf, dev)
+            self.dU = _empty((R, f), bf, dev)
+            self.dX_perm = _empty((R, d), bf, dev)
+            self.dW_g = _empty((E, f, d), bf, dev)
+            self.dW_u = _empty((E, f, d), bf, dev)
+            self.dW_d = _empty((E, d, f), bf, dev)
+            self.dlogits = _empty((T, E), f32, dev)
+            self.dW_r = _empty((E, d), f32, dev)
+            self.dx = _empty((T, d), bf, dev)
+            if fs:
+                self.dAs = _empty((T, fs), bf, dev)
+                self.dUs = _empty((T, fs), bf, dev)
+                self.dxs = _empty((T, d), bf, dev)
+                self.dWs_g = _empty((fs, d), bf, dev)
+                self.dWs_u = _empty((fs, d), bf, dev)
+                self.dWs_d = _empty((d, fs), bf, dev)
+
+    # Optional list that receives (start, end) CUDA event pairs around every grouped-GEMM
+    # entry point call, recorded on the launching stream (used to time the GEMMs inside a
+    # step without adding synchronisation).
+    gemm_events = None
+
+    def _gemm(self, fn, *args, stream=None):
+        if self.gemm_events is None:
+            fn(*args, stream)
+            return
+        st = stream if stream is not None else torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn(*args, stream)
+        b.record(st)
+        self.gemm_events.append((a, b))
+
+    def launches_per_step(self, backward=True, bias_update=False) -> int:
+        """Kernel launches of one step through this plan (what the entry points enqueue)."""
+        s = self.s
+        n = 1 + (1 if s.mode == ops.MODE_SOFTMAX else 0)   # route (+ z-loss reduction)
+        n += 5                                              # permute
+        n += 2 + (2 if s.f_shared else 0)                   # expert forward (G1, G2)
+        n += 1                                              # combine
+        if backward:
+            n += 2                                          # combine backward + padding rows
+            n += 5 + (4 if s.f_shared else 0)               # expert backward (+ expert order)
+            n += 3                                          # router backward
+            n += 1                                          # input gradient
+        if bias_update:
+            n += 1
+        return n
+
+    # ------------------------------------------------------------------ forward
+    def forward(self, x, W_r, b, W_g, W_u, W_d, Ws_g=None, Ws_u=None, Ws_d=None, stream=None):
+        s = self.s
+        self.x = x
+        self.W = (W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d)
+        softmax = s.mode == ops.MODE_SOFTMAX
+        ops.moe_route(x, W_r, None if softmax else b, s.k, s.mode, s.z_coef, self.logits,
+                      self.topk_idx, self.topk_gate, self.topk_score,
+                      self.lse if softmax else None, self.z_loss if softmax else None, self.ws,
+                      stream)
+        ops.moe_permute(self.topk_idx, x, s.E, self.counts, self.offsets, self.row_offsets,
+                        self.perm_token, self.slot_to_row, self.X_perm, self.ws, stream)
+        self._gemm(ops.moe_expert_fwd, self.X_perm, self.row_offsets, W_g, W_u, W_d, self.A,
+                   self.U, self.H, self.Y_perm, self.ws, stream=stream)
+        ys = None
+        if s.f_shared:
+            self._gemm(ops.moe_expert_fwd, x, None, Ws_g[None], Ws_u[None], Ws_d[None], self.As,
+                       self.Us, self.Hs, self.Ys, self.ws, stream=stream)
+            ys = self.Ys
+        ops.moe_combine(self.Y_perm, self.topk_gate, self.slot_to_row, ys, self.out, stream)
+        return self.out
+
+    # ----------------------------------------------------------------- backward
+    def backward(self, dY, stream=None):
+        s = self.s
+        x = self.x
+        W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d = self.W
+        softmax = s.mode == ops.MODE_SOFTMAX
+        ops.moe_combine_bwd(dY, self.Y_perm, self.topk_gate, self.slot_to_row, self.row_offsets,
+                            self.perm_token, self.dY_perm, self.dg, stream)
+        self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
+                   self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU, self.dW_g,
+                   self.dW_u, self.dW_d, self.ws, stream=stream)
+        dxs = None
+        if s.f_shared:
+            self._gemm(ops.moe_expert_bwd, dY, x, self.As, self.Us, self.Hs, None, Ws_g[None],
+                       Ws_u[None], Ws_d[None], self.dxs, self.dAs, self.dUs, self.dWs_g[None],
+                       self.dWs_u[None], self.dWs_d[None], self.ws, stream=stream)
+            dxs = self.dxs
+        ops.moe_route_bwd(self.dg, x, self.topk_idx, self.topk_gate, self.topk_score,
+                          self.logits if softmax else None, self.lse if softmax else None, s.E,
+                          s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream)
+        ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx, stream)
+        return self.dx
+
+    def bias_update(self, b, gamma, stream=None):
+        ops.moe_bias_update(self.counts, self.s.T, self.s.k, gamma, b, stream)
+
+    def grads(self) -> dict:
+        g = {"dx": self.dx, "dW_r": self.dW_r, "dW_g": self.dW_g, "dW_u": self.dW_u,
+             "dW_d": self.dW_d}
+        if self.s.f_shared:
+            g.update(dWs_g=self.dWs_g, dWs_u=self.dWs_u, dWs_d=self.dWs_d)
+        return g
+
+
+class _MoEFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, plan):
+        ctx.plan = plan
+        out = plan.forward(x.contiguous(), W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d)
+        return out.clone()
+
+    @staticmethod
+    def backward(ctx, dY):
+        plan = ctx.plan
+        plan.backward(dY.contiguous())
+        g = plan.grads()
+        shared = plan.s.f_shared > 0
+        return (g["dx"].clone(), g["dW_r"].clone(), None, g["dW_g"].clone(), g["dW_u"].clone(),
+                g["dW_d"].clone(), g["dWs_g"].clone() if shared else None,
+                g["dWs_u"].clone() if shared else None, g["dWs_d"].clone() if shared else None,
+                None)
+
+
+class MoELayer(torch.nn.Module):
+    """Fine-grained MoE layer module (bf16 experts, fp32 router and bias) on one GPU.
+
+    ``forward(x)`` with x [T, d] bf16; gradients flow to x and every weight; the bias is a
+    buffer updated by ``update_bias()`` after backward (it gets no gradient)."""
+
+    def __init__(self, d, E, k, f, f_shared=0, mode="sigmoid", z_coef=0.0, gamma=1e-3,
+                 device="cuda"):
+        super().__init__()
+        self.d, self.E, self.k, self.f, self.f_shared = d, E, k, f, f_shared
+        self.mode = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
+        self.z_coef, self.gamma = z_coef, gamma
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.W_r = torch.nn.Parameter(torch.randn(E, d, device=device) * d ** -0.5)
+        self.register_buffer("b", torch.zeros(E, device=device))
+        self.W_g = torch.nn.Parameter((torch.randn(E, f, d, device=device) * d ** -0.5).to(**bf))
+        self.W_u = torch.nn.Parameter((torch.randn(E, f, d, device=device) * d ** -0.5).to(**bf))
+        self.W_d = torch.nn.Parameter((torch.randn(E, d, f, device=device) * f ** -0.5).to(**bf))
+        if f_shared:
+            self.Ws_g = torch.nn.Parameter((torch.randn(f_shared, d, device=device) * d ** -0.5).to(**bf))
+            self.Ws_u = torch.nn.Parameter((torch.randn(f_shared, d, device=device) * d ** -0.5).to(**bf))
+            self.Ws_d = torch.nn.Parameter((torch.randn(d, f_shared, device=device) * f_shared ** -0.5).to(**bf))
+        else:
+            self.Ws_g = self.Ws_u = self.Ws_d = None
+        self._plans = {}
+        self._last_plan = None
+
+    def _plan(self, T):
+        if T not in self._plans:
+            self._plans[T] = MoEPlan(MoEShape(T, self.d, self.E, self.k, self.f, self.f_shared,
+                                              self.mode, self.z_coef), self.W_g.device)
+        return self._plans[T]
+
+    def forward(self, x):
+        plan = self._plan(x.shape[0])
+        self._last_plan = plan
+        return _MoEFunction.apply(x, self.W_r, self.b, self.W_g, self.W_u, self.W_d, self.Ws_g,
+                                  self.Ws_u, self.Ws_d, plan)
+
+    @torch.no_grad()
+    def update_bias(self):
+        if self.mode == ops.MODE_SIGMOID and self._last_plan is not None:
+            self._last_plan.bias_update(self.b, self.gamma)
+
+    def z_loss(self):
+        return None if self._last_plan is None else self._last_plan.z_loss

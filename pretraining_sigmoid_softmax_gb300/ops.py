@@ -1,0 +1,159 @@
+"""Thin Python binding of the C ABI: one function per entry point, same names, arguments
+are torch tensors (device memory) that are turned into raw pointers and sizes. No step of
+the layer is computed here."""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+MODE_SIGMOID = 0
+MODE_SOFTMAX = 1
+ROW_ALIGN = 128
+
+
+class MoEError(RuntimeError):
+    pass
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        msg = _lib.load().moe_status_string(rc).decode()
+        raise MoEError(f"{name} failed: {msg} (status {rc})")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise MoEError("tensors passed to the MoE library must be contiguous")
+
+
+def status_string(rc: int) -> str:
+    return _lib.load().moe_status_string(rc).decode()
+
+
+def moe_version() -> int:
+    return _lib.load().moe_version()
+
+
+def moe_padded_rows(T: int, k: int, E: int) -> int:
+    return _lib.load().moe_padded_rows(T, k, E)
+
+
+def moe_workspace_bytes(T: int, d: int, E: int, k: int) -> int:
+    return _lib.load().moe_workspace_bytes(T, d, E, k)
+
+
+def moe_device_status(stream=None) -> tuple[int, int]:
+    code, site = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.load().moe_device_status(_stream(stream), ctypes.byref(code), ctypes.byref(site)),
+           "moe_device_status")
+    return code.value, site.value
+
+
+def moe_clear_device_status(stream=None):
+    _check(_lib.load().moe_clear_device_status(_stream(stream)), "moe_clear_device_status")
+
+
+def moe_set_wait_limit_ns(ns: int):
+    _lib.load().moe_set_wait_limit_ns(int(ns))
+
+
+def moe_route(x, W_r, b, k, mode, z_coef, logits, topk_idx, topk_gate, topk_score, lse, z_loss,
+              ws, stream=None):
+    T, d = x.shape
+    E = W_r.shape[0]
+    _contig(x, W_r, b, logits, topk_idx, topk_gate, topk_score, lse, z_loss, ws)
+    _check(_lib.load().moe_route(_p(x), _p(W_r), _p(b), T, d, E, k, mode, float(z_coef),
+                                 _p(logits), _p(topk_idx), _p(topk_gate), _p(topk_score), _p(lse),
+                                 _p(z_loss), _p(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def moe_permute(topk_idx, x, E, counts, offsets, row_offsets, perm_token, slot_to_row, X_perm,
+                ws, stream=None):
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    _contig(topk_idx, x, counts, offsets, row_offsets, perm_token, slot_to_row, X_perm, ws)
+    _check(_lib.load().moe_permute(_p(topk_idx), _p(x), T, d, E, k, _p(counts), _p(offsets),
+                                   _p(row_offsets), _p(perm_token), _p(slot_to_row), _p(X_perm),
+                                   _p(ws), ws.numel(), _stream(stream)), "moe_permute")
+
+
+def moe_expert_fwd(X, row_offsets, W_g, W_u, W_d, A, U, H, Y, ws, stream=None):
+    rows, d = X.shape
+    E, f, _ = W_g.shape
+    _contig(X, W_g, W_u, W_d, A, U, H, Y, ws)
+    _check(_lib.load().moe_expert_fwd(_p(X), _p(row_offsets), E, rows, d, f, _p(W_g), _p(W_u),
+                                      _p(W_d), _p(A), _p(U), _p(H), _p(Y), _p(ws),
+                                      0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_expert_fwd")
+
+
+def moe_combine(Y_perm, topk_gate, slot_to_row, Y_shared, out, stream=None):
+    T, k = topk_gate.shape
+    d = Y_perm.shape[1]
+    _contig(Y_perm, topk_gate, slot_to_row, Y_shared, out)
+    _check(_lib.load().moe_combine(_p(Y_perm), _p(topk_gate), _p(slot_to_row), _p(Y_shared), T, d,
+                                   k, _p(out), _stream(stream)), "moe_combine")
+
+
+def moe_bias_update(counts, T, k, gamma, b, stream=None):
+    E = counts.shape[0]
+    _contig(counts, b)
+    _check(_lib.load().moe_bias_update(_p(counts), E, T, k, float(gamma), _p(b), _stream(stream)),
+           "moe_bias_update")
+
+
+def moe_combine_bwd(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm, dg,
+                    stream=None):
+    T, k = topk_gate.shape
+    d = dY.shape[1]
+    E = row_offsets.shape[0] - 1
+    _contig(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm, dg)
+    _check(_lib.load().moe_combine_bwd(_p(dY), _p(Y_perm), _p(topk_gate), _p(slot_to_row),
+                                       _p(row_offsets), _p(perm_token), T, d, E, k, _p(dY_perm),
+                                       _p(dg), _stream(stream)), "moe_combine_bwd")
+
+
+def moe_expert_bwd(dY, X, A, U, H, row_offsets, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws,
+                   stream=None):
+    rows, d = X.shape
+    E, f, _ = W_g.shape
+    _contig(dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws)
+    _check(_lib.load().moe_expert_bwd(_p(dY), _p(X), _p(A), _p(U), _p(H), _p(row_offsets), E, rows,
+                                      d, f, _p(W_g), _p(W_u), _p(W_d), _p(dX), _p(dA), _p(dU),
+                                      _p(dW_g), _p(dW_u), _p(dW_d), _p(ws),
+                                      0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_expert_bwd")
+
+
+def moe_route_bwd(dg, x, topk_idx, topk_gate, topk_score, logits, lse, E, mode, z_coef, dlogits,
+                  dW_r, ws, stream=None):
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    _contig(dg, x, topk_idx, topk_gate, topk_score, logits, lse, dlogits, dW_r, ws)
+    _check(_lib.load().moe_route_bwd(_p(dg), _p(x), _p(topk_idx), _p(topk_gate), _p(topk_score),
+                                     _p(logits), _p(lse), T, d, E, k, mode, float(z_coef),
+                                     _p(dlogits), _p(dW_r), _p(ws), ws.numel(), _stream(stream)),
+           "moe_route_bwd")
+
+
+def moe_permute_bwd(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx, stream=None):
+    T, k = slot_to_row.shape
+    d = dx.shape[1]
+    E = 0 if W_r is None else W_r.shape[0]
+    _contig(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx)
+    _check(_lib.load().moe_permute_bwd(_p(dX_perm), _p(slot_to_row), _p(dx_shared), _p(dlogits),
+                                       _p(W_r), T, d, max(E, 1), k, _p(dx), _stream(stream)),
+           "moe_permute_bwd")

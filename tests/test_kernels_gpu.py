@@ -1,0 +1,332 @@
+"""Per-kernel parity of the CUDA path against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from pretraining_sigmoid_softmax_gb300 import ops
+
+from gpu_common import (assert_close, dev, gpu_rows, h64, padded_offsets, randn_bf16,
+                        require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    require_gpu()
+
+
+def _ws(T, d, E, k):
+    return torch.empty(ops.moe_workspace_bytes(T, d, E, k), dtype=torch.uint8, device="cuda")
+
+
+def _route(x, W_r, b, k, mode, z):
+    T, d = x.shape
+    E = W_r.shape[0]
+    out = dict(logits=torch.empty(T, E, device="cuda"),
+               idx=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+               gate=torch.empty(T, k, device="cuda"), score=torch.empty(T, k, device="cuda"),
+               lse=torch.empty(T, device="cuda"), z=torch.zeros(1, device="cuda"))
+    softmax = mode == ops.MODE_SOFTMAX
+    ops.moe_route(dev(x), dev(W_r), None if softmax else dev(b), k, mode, z, out["logits"],
+                  out["idx"], out["gate"], out["score"], out["lse"] if softmax else None,
+                  out["z"] if softmax else None, _ws(T, d, E, k))
+    torch.cuda.synchronize()
+    return out
+
+
+# ------------------------------------------------------------------------------- router
+
+ROUTE_CASES = [
+    (512, 256, 8, 2, "sigmoid"),
+    (1000, 384, 64, 8, "sigmoid"),
+    (777, 256, 32, 4, "softmax"),
+    (300, 128, 128, 8, "sigmoid"),
+    (129, 256, 256, 32, "softmax"),
+    (64, 128, 1, 1, "sigmoid"),
+    (200, 128, 5, 5, "softmax"),
+    (65, 128, 200, 3, "sigmoid"),
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,mode", ROUTE_CASES)
+def test_route_matches_oracle(T, d, E, k, mode):
+    g = torch.Generator().manual_seed(T * 7 + E)
+    x = randn_bf16((T, d), g)
+    W_r = torch.randn(E, d, generator=g) * d ** -0.5
+    b = torch.rand(E, generator=g) * 0.1 - 0.05
+    m = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
+    z = 1e-3
+    r = _route(x, W_r, b, k, m, z)
+    x64, W64, b64 = h64(x), h64(W_r), h64(b)
+    l64 = O.router_logits(x64, W64)
+    lg = h64(r["logits"])
+    # fp32 dot product error bound (Higham): gamma_d * sum |x_j w_j|
+    u = 2.0 ** -24
+    gamma = d * u / (1 - d * u)
+    bound = gamma * (np.abs(x64) @ np.abs(W64).T)
+    assert (np.abs(lg - l64) <= bound).all(), "router logits outside the fp32 error bound"
+    # replay the choice on the GPU's own fp32 logits
+    ref = O.route(lg, mode, k, b64, z)
+    near = O.near_tie_tokens(ref["select_value"], k) if mode == "sigmoid" else np.zeros(T, bool)
+    idx = r["idx"].cpu().numpy()
+    assert (idx[~near] == ref["idx"][~near]).all(), "expert choice differs from the oracle"
+    assert near.mean() < 0.01
+    keep = ~near
+    np.testing.assert_allclose(h64(r["gate"])[keep], ref["gate"][keep], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(h64(r["score"])[keep], ref["score"][keep], rtol=1e-5, atol=1e-6)
+    for t in range(T):  # k distinct experts per token
+        assert len(set(idx[t].tolist())) == k
+    if mode == "softmax":
+        np.testing.assert_allclose(h64(r["lse"]), ref["lse"], rtol=1e-5, atol=1e-5)
+        assert float(r["z"][0]) == pytest.approx(ref["z_loss"], rel=1e-4)
+
+
+def test_route_is_bitwise_repeatable():
+    g = torch.Generator().manual_seed(5)
+    x = randn_bf16((2000, 512), g)
+    W_r = torch.randn(64, 512, generator=g) * 512 ** -0.5
+    b = torch.rand(64, generator=g) * 0.1 - 0.05
+    r1 = _route(x, W_r, b, 8, ops.MODE_SIGMOID, 0.0)
+    r2 = _route(x, W_r, b, 8, ops.MODE_SIGMOID, 0.0)
+    for key in ("logits", "idx", "gate"):
+        assert torch.equal(r1[key], r2[key])
+
+
+# ------------------------------------------------------------------------------ permute
+
+def _random_choice(T, E, k, gen, skew=False):
+    w = torch.ones(E)
+    if skew:
+        w = torch.tensor([1.0 / (i + 1) ** 1.2 for i in range(E)])
+        w[E // 2:E // 2 + max(1, E // 8)] = 0.0  # a block of empty experts
+    idx = torch.stack([torch.multinomial(w, k, replacement=False, generator=gen) for _ in range(T)])
+    return idx.to(torch.int32)
+
+
+def _permute(idx, x, E):
+    T, k = idx.shape
+    d = x.shape[1]
+    R = ops.moe_padded_rows(T, k, E)
+    out = dict(counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+               offsets=torch.empty(E + 1, dtype=torch.int64, device="cuda"),
+               row_offsets=torch.empty(E + 1, dtype=torch.int64, device="cuda"),
+               perm_token=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
+               slot_to_row=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+               X_perm=torch.full((R, d), float("nan"), dtype=torch.bfloat16, device="cuda"))
+    ops.moe_permute(dev(idx), dev(x), E, out["counts"], out["offsets"], out["row_offsets"],
+                    out["perm_token"], out["slot_to_row"], out["X_perm"], _ws(T, d, E, k))
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("T,d,E,k,skew", [(1000, 128, 8, 2, False), (3000, 256, 64, 8, True),
+                                          (2049, 128, 256, 32, False), (5, 128, 16, 4, True),
+                                          (1, 128, 1, 1, False)])
+def test_permute_is_bit_exact(T, d, E, k, skew):
+    g = torch.Generator().manual_seed(T + E)
+    idx = _random_choice(T, E, k, g, skew)
+    x = randn_bf16((T, d), g)
+    r = _permute(idx, x, E)
+    D = O.dispatch(idx.numpy().astype(np.int64), E)
+    counts = r["counts"].cpu().numpy()
+    assert (counts == D["counts"]).all()
+    assert (r["offsets"].cpu().numpy() == D["offsets"]).all()
+    ro = r["row_offsets"].cpu().numpy()
+    assert (ro == padded_offsets(D["counts"])).all()
+    rows = gpu_rows(D["offsets"], ro)
+    pt = r["perm_token"].cpu().numpy()
+    assert (pt[rows] == D["perm_token"]).all()
+    s2r = r["slot_to_row"].cpu().numpy()
+    assert (s2r == rows[D["slot_to_row"]]).all()
+    Xp = r["X_perm"].float().cpu()
+    assert torch.equal(Xp[torch.from_numpy(rows)], x.float()[torch.from_numpy(D["perm_token"])])
+    pad = np.setdiff1d(np.arange(int(ro[-1])), rows)
+    assert (pt[pad] == -1).all()
+    assert (Xp[torch.from_numpy(pad)] == 0).all()
+
+
+def test_permute_reports_bad_index_without_touching_other_rows():
+    ops.moe_clear_device_status()
+    idx = torch.tensor([[0, 1], [1, 9], [2, 2]], dtype=torch.int32)  # 9 out of range, 2 repeated
+    x = randn_bf16((3, 128), torch.Generator().manual_seed(1))
+    r = _permute(idx, x, 4)
+    code, site = ops.moe_device_status()
+    assert code == 5
+    s2r = r["slot_to_row"].cpu().numpy()
+    assert s2r[1, 1] == -1 and s2r[2, 1] == -1
+    assert r["counts"].cpu().tolist() == [1, 2, 1, 0]
+    ops.moe_clear_device_status()
+    assert ops.moe_device_status()[0] == 0
+
+
+# --------------------------------------------------------------------- expert GEMMs
+
+def _expert_buffers(rows, d, f, E):
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    return {k: torch.full(s, float("nan"), **bf) for k, s in
+            dict(A=(rows, f), U=(rows, f), H=(rows, f), Y=(rows, d), dX=(rows, d), dA=(rows, f),
+                 dU=(rows, f), dW_g=(E, f, d), dW_u=(E, f, d), dW_d=(E, d, f)).items()}
+
+
+def _run_experts(X, dY, row_offsets, W_g, W_u, W_d):
+    rows, d = X.shape
+    E, f, _ = W_g.shape
+    B = _expert_buffers(rows, d, f, E)
+    ws = _ws(rows, d, E, 1)
+    ro = None if row_offsets is None else dev(torch.from_numpy(row_offsets))
+    ops.moe_expert_fwd(dev(X), ro, dev(W_g), dev(W_u), dev(W_d), B["A"], B["U"], B["H"], B["Y"], ws)
+    ops.moe_expert_bwd(dev(dY), dev(X), B["A"], B["U"], B["H"], ro, dev(W_g), dev(W_u), dev(W_d),
+                       B["dX"], B["dA"], B["dU"], B["dW_g"], B["dW_u"], B["dW_d"], ws)
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    return B
+
+
+def _weights(E, d, f, g):
+    return (randn_bf16((E, f, d), g, d ** -0.5), randn_bf16((E, f, d), g, d ** -0.5),
+            randn_bf16((E, d, f), g, f ** -0.5))
+
+
+def _check_expert(B, e, lo, hi, X, dY, W_g, W_u, W_d, tag):
+    rnd = O.bf16_round
+    x = h64(X[lo:hi])
+    a, u, h, y = O.swiglu_expert(x, h64(W_g[e]), h64(W_u[e]), h64(W_d[e]), rnd)
+    assert_close(B["A"][lo:hi], a, f"{tag} A")
+    assert_close(B["U"][lo:hi], u, f"{tag} U")
+    assert_close(B["H"][lo:hi], h, f"{tag} H")
+    assert_close(B["Y"][lo:hi], y, f"{tag} Y")
+    gr = O.expert_backward(h64(dY[lo:hi]), x, a, u, h, h64(W_g[e]), h64(W_u[e]), h64(W_d[e]), rnd)
+    assert_close(B["dA"][lo:hi], gr["dA"], f"{tag} dA")
+    assert_close(B["dU"][lo:hi], gr["dU"], f"{tag} dU")
+    assert_close(B["dX"][lo:hi], gr["dX"], f"{tag} dX")
+    assert_close(B["dW_d"][e], gr["dW_d"], f"{tag} dW_d")
+    assert_close(B["dW_g"][e], gr["dW_g"], f"{tag} dW_g")
+    assert_close(B["dW_u"][e], gr["dW_u"], f"{tag} dW_u")
+
+
+@pytest.mark.parametrize("rows,d,f", [(200, 256, 128), (128, 384, 256), (77, 128, 128),
+                                      (640, 512, 384)])
+def test_dense_expert_gemms(rows, d, f):
+    """One expert over all rows (the shared-expert path): ragged M tail, both tile widths."""
+    g = torch.Generator().manual_seed(rows + d + f)
+    X = randn_bf16((rows, d), g)
+    dY = randn_bf16((rows, d), g)
+    W_g, W_u, W_d = _weights(1, d, f, g)
+    B = _run_experts(X, dY, None, W_g, W_u, W_d)
+    _check_expert(B, 0, 0, rows, X, dY, W_g, W_u, W_d, "dense")
+
+
+@pytest.mark.parametrize("counts,d,f", [([130, 0, 5, 256, 1], 256, 128),
+                                        ([0, 300, 0], 256, 256),
+                                        ([128, 129, 127, 0, 0, 1], 384, 128)])
+def test_routed_expert_gemms(counts, d, f):
+    """Padded expert segments with empty experts and 1-row / 127 / 128 / 129-row segments."""
+    E = len(counts)
+    g = torch.Generator().manual_seed(sum(counts) + d)
+    ro = padded_offsets(counts)
+    rows = int(ro[-1]) + 128  # capacity beyond the last segment is never touched
+    X = torch.zeros(rows, d, dtype=torch.bfloat16)
+    dY = torch.zeros(rows, d, dtype=torch.bfloat16)
+    for e in range(E):
+        X[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g)
+        dY[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g, 0.25)
+    W_g, W_u, W_d = _weights(E, d, f, g)
+    B = _run_experts(X, dY, ro, W_g, W_u, W_d)
+    for e in range(E):
+        lo, c = int(ro[e]), counts[e]
+        if c == 0:
+            for name in ("dW_g", "dW_u", "dW_d"):
+                assert (B[name][e].float() == 0).all(), f"empty expert {e} {name}"
+            continue
+        _check_expert(B, e, lo, lo + c, X, dY, W_g, W_u, W_d, f"expert {e}")
+        # padding rows stay zero through every GEMM
+        for name in ("A", "U", "H", "Y", "dA", "dU", "dX"):
+            assert (B[name][lo + c:int(ro[e + 1])].float() == 0).all(), f"{name} padding {e}"
+
+
+# ------------------------------------------------------------- combine and backward
+
+def test_combine_and_backward_kernels():
+    g = torch.Generator().manual_seed(21)
+    T, d, E, k = 700, 256, 16, 4
+    idx = _random_choice(T, E, k, g, skew=True)
+    x = randn_bf16((T, d), g)
+    P = _permute(idx, x, E)
+    D = O.dispatch(idx.numpy().astype(np.int64), E)
+    ro = P["row_offsets"].cpu().numpy()
+    rows = gpu_rows(D["offsets"], ro)
+    R = P["X_perm"].shape[0]
+    Y_perm = torch.zeros(R, d, dtype=torch.bfloat16)
+    Y_perm[torch.from_numpy(rows)] = randn_bf16((T * k, d), g)
+    gate = torch.rand(T, k, generator=g)
+    Ys = randn_bf16((T, d), g)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    ops.moe_combine(dev(Y_perm), dev(gate), P["slot_to_row"], dev(Ys), out)
+    Yp64 = h64(Y_perm)[rows]
+    ref = O.combine(Yp64, h64(gate), D["slot_to_row"], h64(Ys), O.bf16_round)
+    assert_close(out, ref, "combine")
+    # combine backward
+    dY = randn_bf16((T, d), g)
+    dY_perm = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dg = torch.empty(T, k, device="cuda")
+    ops.moe_combine_bwd(dev(dY), dev(Y_perm), dev(gate), P["slot_to_row"], P["row_offsets"],
+                        P["perm_token"], dY_perm, dg)
+    rdYp, rdg = O.combine_backward(h64(dY), Yp64, h64(gate), D["slot_to_row"], D["perm_token"],
+                                   D["perm_slot"], O.bf16_round)
+    assert_close(dY_perm[torch.from_numpy(rows).cuda()], rdYp, "dY_perm")
+    assert_close(dg, rdg, "dg", atol=1e-4, rtol=1e-4)
+    pad = torch.from_numpy(np.setdiff1d(np.arange(int(ro[-1])), rows)).cuda()
+    assert (dY_perm[pad].float() == 0).all()
+    # input gradient with shared and router terms
+    dX_perm = torch.zeros(R, d, dtype=torch.bfloat16)
+    dX_perm[torch.from_numpy(rows)] = randn_bf16((T * k, d), g)
+    dxs = randn_bf16((T, d), g)
+    W_r = torch.randn(E, d, generator=g) * d ** -0.5
+    dl = torch.randn(T, E, generator=g) * (torch.rand(T, E, generator=g) < 0.3)
+    dx = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    ops.moe_permute_bwd(dev(dX_perm), P["slot_to_row"], dev(dxs), dev(dl), dev(W_r), dx)
+    ref = O.input_gradient(h64(dX_perm)[rows], D["slot_to_row"], h64(dxs), h64(dl) @ h64(W_r),
+                           O.bf16_round)
+    assert_close(dx, ref, "dx")
+
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_router_backward(mode):
+    g = torch.Generator().manual_seed(31)
+    T, d, E, k = 3000, 256, 32, 4
+    x = randn_bf16((T, d), g)
+    W_r = torch.randn(E, d, generator=g) * d ** -0.5
+    b = torch.rand(E, generator=g) * 0.1 - 0.05
+    m = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
+    z = 0.01
+    r = _route(x, W_r, b, k, m, z)
+    dg = torch.randn(T, k, generator=g)
+    dl = torch.empty(T, E, device="cuda")
+    dW_r = torch.empty(E, d, device="cuda")
+    ops.moe_route_bwd(dev(dg), dev(x), r["idx"], r["gate"], r["score"],
+                      r["logits"] if mode == "softmax" else None,
+                      r["lse"] if mode == "softmax" else None, E, m, z, dl, dW_r, _ws(T, d, E, k))
+    torch.cuda.synchronize()
+    lg = h64(r["logits"])
+    ref = O.route(lg, mode, k, h64(b), z)
+    ref = O._regate(ref, lg, r["idx"].cpu().numpy(), mode, h64(b), z)
+    rb = O.router_backward(h64(dg), ref, h64(x), h64(W_r), mode, z)
+    assert_close(dl, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
+    assert_close(dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3)
+
+
+def test_bias_update_is_bit_exact():
+    g = torch.Generator().manual_seed(41)
+    E, T, k = 64, 4096, 8
+    counts = torch.multinomial(torch.ones(E), T * k, replacement=True, generator=g).bincount(minlength=E)
+    counts[3] = T * k // E  # exactly balanced expert: no change
+    counts = counts.to(torch.int32)
+    b = torch.rand(E, generator=g) * 0.1 - 0.05
+    bd = dev(b)
+    ops.moe_bias_update(dev(counts), T, k, 0.001, bd)
+    ref = O.bias_update(counts.numpy(), b.numpy(), T, k, 0.001)
+    assert np.array_equal(bd.cpu().numpy().view(np.uint32), ref.view(np.uint32))

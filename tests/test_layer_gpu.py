@@ -1,0 +1,244 @@
+"""Whole-layer parity (forward, backward, bias update) of the CUDA path against the fp64
+oracle on the five workloads and on small ragged shapes, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from pretraining_sigmoid_softmax_gb300 import ops
+from pretraining_sigmoid_softmax_gb300.configs import CONFIGS, MoEConfig
+from pretraining_sigmoid_softmax_gb300.inputs import make_inputs, make_upstream_gate_grad
+from pretraining_sigmoid_softmax_gb300.layer import MoEPlan, MoEShape
+
+from gpu_common import assert_close, gpu_rows, h64, padded_offsets, require_gpu
+
+pytestmark = pytest.mark.gpu
+RND = O.bf16_round
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    require_gpu()
+
+
+class Lazy:
+    """fp64 view of a host tensor converted slice by slice (whole-weight fp64 copies of the
+    large workloads would need tens of GB)."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, key):
+        return O.to64(self.t[key])
+
+
+WEIGHTS = ("W_g", "W_u", "W_d", "Ws_g", "Ws_u", "Ws_d")
+
+
+def run_gpu(cfg: MoEConfig, inp: dict):
+    plan = MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)
+    d = {k: v.cuda() for k, v in inp.items()}
+    ops.moe_clear_device_status()
+    plan.forward(d["x"], d["W_r"], d["b"], d["W_g"], d["W_u"], d["W_d"], d.get("Ws_g"),
+                 d.get("Ws_u"), d.get("Ws_d"))
+    b_new = None
+    if cfg.backward:
+        plan.backward(d["dY"])
+        if cfg.bias_update:
+            b_new = d["b"].clone()
+            plan.bias_update(b_new, cfg.gamma)
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    return plan, b_new
+
+
+def check_routing(cfg, inp, plan):
+    """Bit-exact choice against the oracle replayed on the GPU's fp32 logits; returns the
+    GPU choice and logits (fp64)."""
+    lg = h64(plan.logits)
+    b64 = h64(inp["b"])
+    ref = O.route(lg, cfg.mode, cfg.k, b64, cfg.z_coef)
+    near = (O.near_tie_tokens(ref["select_value"], cfg.k) if cfg.mode == "sigmoid"
+            else np.zeros(cfg.T, bool))
+    idx = plan.topk_idx.cpu().numpy().astype(np.int64)
+    assert (idx[~near] == ref["idx"][~near]).all(), "expert choice differs from the oracle"
+    assert near.mean() < 0.01, f"near-tie tokens {near.sum()}"
+    # dispatch of the GPU's choice: counts, offsets and permutation bit-exact
+    D = O.dispatch(idx, cfg.E)
+    assert (plan.counts.cpu().numpy() == D["counts"]).all()
+    assert (plan.offsets.cpu().numpy() == D["offsets"]).all()
+    ro = plan.row_offsets.cpu().numpy()
+    assert (ro == padded_offsets(D["counts"])).all()
+    rows = gpu_rows(D["offsets"], ro)
+    assert (plan.perm_token.cpu().numpy()[rows] == D["perm_token"]).all()
+    assert (plan.slot_to_row.cpu().numpy() == rows[D["slot_to_row"]]).all()
+    return idx, lg, D, rows, int(near.sum())
+
+
+def full_parity(cfg, inp):
+    plan, b_new = run_gpu(cfg, inp)
+    idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
+    i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
+    fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND)
+    assert_close(plan.topk_gate, fwd["gate"], "gates", atol=1e-6, rtol=1e-5)
+    assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], fwd["X_perm"], "X_perm", 0, 0)
+    assert_close(plan.out, fwd["out"], "out")
+    if cfg.mode == "softmax":
+        assert float(plan.z_loss[0]) == pytest.approx(fwd["z_loss"], rel=1e-4)
+    if not cfg.backward:
+        return
+    bwd = O.layer_backward(i64, fwd, O.to64(inp["dY"]))
+    assert_close(plan.dx, bwd["dx"], "dx")
+    for name in ("dW_g", "dW_u", "dW_d"):
+        assert_close(getattr(plan, name), bwd[name], name)
+    assert_close(plan.dW_r, bwd["dW_r"], "dW_r")
+    if cfg.f_shared:
+        for name in ("dWs_g", "dWs_u", "dWs_d"):
+            assert_close(getattr(plan, name), bwd[name], name)
+    if cfg.bias_update:
+        ref = O.bias_update(D["counts"], inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
+        assert np.array_equal(b_new.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+SMALL = [
+    MoEConfig("ragged_sigmoid_shared", T=300, d=256, E=6, k=3, f=128, f_shared=128,
+              mode="sigmoid", seed=11, backward=True, bias_update=True),
+    MoEConfig("ragged_softmax", T=1000, d=384, E=16, k=4, f=256, f_shared=0, mode="softmax",
+              seed=12, backward=True, bias_update=False, z_coef=1e-3),
+    MoEConfig("one_expert_top1", T=200, d=128, E=1, k=1, f=128, f_shared=0, mode="sigmoid",
+              seed=13, backward=True, bias_update=True),
+    MoEConfig("k_equals_E", T=130, d=128, E=4, k=4, f=128, f_shared=128, mode="softmax",
+              seed=14, backward=True, bias_update=False, z_coef=1e-2),
+    MoEConfig("skewed_small", T=2048, d=256, E=32, k=4, f=128, f_shared=0, mode="sigmoid",
+              seed=15, backward=True, bias_update=False, zipf=True),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_small_layers_full_parity(cfg):
+    full_parity(cfg, make_inputs(cfg))
+
+
+def test_single_expert_router_gets_zero_gradient():
+    """One expert with top-1: the gate is 1 and the router weight gradient is exactly 0."""
+    cfg = SMALL[2]
+    plan, _ = run_gpu(cfg, make_inputs(cfg))
+    assert (plan.topk_gate == 1).all()
+    assert (plan.dW_r == 0).all()
+
+
+@pytest.mark.parametrize("name", ["C0", "C1"])
+def test_workload_full_parity(name):
+    cfg = CONFIGS[name]
+    full_parity(cfg, make_inputs(cfg))
+
+
+def test_layer_is_bitwise_repeatable():
+    cfg = CONFIGS["C1"]
+    inp = make_inputs(cfg)
+    p1, _ = run_gpu(cfg, inp)
+    r1 = {k: v.clone() for k, v in p1.grads().items()}
+    o1 = p1.out.clone()
+    p2, _ = run_gpu(cfg, inp)
+    assert torch.equal(o1, p2.out)
+    for k, v in p2.grads().items():
+        assert torch.equal(r1[k], v), k
+
+
+@pytest.mark.parametrize("name", ["C2", "C3", "C4"])
+def test_workload_sampled_parity(name):
+    """Full-size workloads in the benchmark's launch configuration: routing, counts and
+    permutation in full; out and dx on sampled tokens; weight-gradient entries of sampled
+    experts (every empty expert must have exactly zero weight gradients)."""
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg)
+    plan, b_new = run_gpu(cfg, inp)
+    idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
+    lazy = {k: (Lazy(v) if k in WEIGHTS or k == "x" else O.to64(v)) for k, v in inp.items()
+            if k != "dY"}
+    rng = np.random.default_rng(cfg.seed)
+    toks = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, 14, replace=False)]))
+    ref = O.route(lg, cfg.mode, cfg.k, O.to64(inp["b"]), cfg.z_coef)
+    ref = O._regate(ref, lg, idx, cfg.mode, O.to64(inp["b"]), cfg.z_coef)
+    out = plan.out[torch.from_numpy(toks).cuda()]
+    dx = plan.dx[torch.from_numpy(toks).cuda()]
+    for j, t in enumerate(toks):
+        o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND)
+        assert_close(out[j], o, f"out[{t}]")
+        tb = O.token_backward(lazy, int(t), lg[t], idx[t], cfg.mode, cfg.k,
+                              O.to64(inp["dY"][t]), cfg.z_coef, cfg.T, rnd=RND)
+        assert_close(dx[j], tb["dx"], f"dx[{t}]")
+    counts = D["counts"]
+    live = np.nonzero(counts)[0]
+    picks = {int(live[np.argmax(counts[live])]), int(live[np.argmin(counts[live])]),
+             int(rng.choice(live))}
+    dY64 = Lazy(inp["dY"])
+    for e in sorted(picks):
+        lo, hi = int(D["offsets"][e]), int(D["offsets"][e + 1])
+        tok_e = D["perm_token"][lo:hi]
+        gates = ref["gate"][tok_e, D["perm_slot"][lo:hi]]
+        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f))) for _ in range(3)]
+        eg = [(int(rng.integers(cfg.f)), int(rng.integers(cfg.d))) for _ in range(3)]
+        want = O.expert_weight_grad_entries(
+            {"x": O.to64(inp["x"][torch.from_numpy(tok_e)]), "W_g": lazy["W_g"],
+             "W_u": lazy["W_u"], "W_d": lazy["W_d"]},
+            e, np.arange(hi - lo), gates, O.to64(inp["dY"][torch.from_numpy(tok_e)]), ed, eg,
+            rnd=RND)
+        got_d = [float(plan.dW_d[e, i, j]) for (i, j) in ed]
+        got_g = [float(plan.dW_g[e, j, i]) for (j, i) in eg]
+        got_u = [float(plan.dW_u[e, j, i]) for (j, i) in eg]
+        assert_close(np.array(got_d), want["dW_d"], f"dW_d[{e}]")
+        assert_close(np.array(got_g), want["dW_g"], f"dW_g[{e}]")
+        assert_close(np.array(got_u), want["dW_u"], f"dW_u[{e}]")
+    for e in np.nonzero(counts == 0)[0]:
+        for name in ("dW_g", "dW_u", "dW_d"):
+            assert (getattr(plan, name)[int(e)] == 0).all()
+    if cfg.zipf:
+        assert (counts == 0).sum() >= 10
+    if cfg.f_shared:
+        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f_shared))) for _ in range(2)]
+        eg = [(int(rng.integers(cfg.f_shared)), int(rng.integers(cfg.d))) for _ in range(2)]
+        want = O.shared_weight_grad_entries({"x": O.to64(inp["x"]), "Ws_g": lazy["Ws_g"][:],
+                                             "Ws_u": lazy["Ws_u"][:], "Ws_d": lazy["Ws_d"][:]},
+                                            O.to64(inp["dY"]), ed, eg, rnd=RND)
+        assert_close(np.array([float(plan.dWs_d[i, j]) for (i, j) in ed]), want["dWs_d"], "dWs_d")
+        assert_close(np.array([float(plan.dWs_g[j, i]) for (j, i) in eg]), want["dWs_g"], "dWs_g")
+        assert_close(np.array([float(plan.dWs_u[j, i]) for (j, i) in eg]), want["dWs_u"], "dWs_u")
+    if cfg.bias_update:
+        refb = O.bias_update(counts, inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
+        assert np.array_equal(b_new.cpu().numpy().view(np.uint32), refb.view(np.uint32))
+    del dY64
+
+
+def test_router_backward_at_full_size():
+    """Router backward of the largest workload with a synthetic gate gradient."""
+    cfg = CONFIGS["C4"]
+    g = torch.Generator().manual_seed(cfg.seed)
+    x = (torch.randn(cfg.T, cfg.d, generator=g)).to(torch.bfloat16)
+    W_r = torch.randn(cfg.E, cfg.d, generator=g) * cfg.d ** -0.5
+    b = torch.rand(cfg.E, generator=g) * 0.1 - 0.05
+    T, d, E, k = cfg.T, cfg.d, cfg.E, cfg.k
+    f32 = dict(device="cuda", dtype=torch.float32)
+    logits, gate, score = torch.empty(T, E, **f32), torch.empty(T, k, **f32), torch.empty(T, k, **f32)
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    dl, dW_r = torch.empty(T, E, **f32), torch.empty(E, d, **f32)
+    ws = torch.empty(ops.moe_workspace_bytes(T, d, E, k), dtype=torch.uint8, device="cuda")
+    xd, Wd = x.cuda(), W_r.cuda()
+    ops.moe_route(xd, Wd, b.cuda(), k, ops.MODE_SIGMOID, 0.0, logits, idx, gate, score, None,
+                  None, ws)
+    dg = make_upstream_gate_grad(T, k, cfg.seed)
+    ops.moe_route_bwd(dg.cuda(), xd, idx, gate, score, None, None, E, ops.MODE_SIGMOID, 0.0, dl,
+                      dW_r, ws)
+    torch.cuda.synchronize()
+
+    class _P:
+        pass
+    plan = _P()
+    plan.logits, plan.topk_idx, plan.dlogits, plan.dW_r = logits, idx, dl, dW_r
+    lg = h64(plan.logits)
+    ref = O.route(lg, "sigmoid", cfg.k, O.to64(b))
+    ref = O._regate(ref, lg, plan.topk_idx.cpu().numpy(), "sigmoid", O.to64(b), 0.0)
+    rb = O.router_backward(O.to64(dg), ref, O.to64(x), O.to64(W_r), "sigmoid", 0.0)
+    assert_close(plan.dlogits, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
+    assert_close(plan.dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3)

@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares; the
+host-only entry points and argument checks work without a GPU."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+from pretraining_sigmoid_softmax_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not installed")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return _lib.load()
+
+
+def test_header_declares_the_layer_entry_points():
+    names = header_functions()
+    for must in ("moe_route", "moe_permute", "moe_expert_fwd", "moe_combine", "moe_bias_update",
+                 "moe_expert_bwd", "moe_combine_bwd", "moe_route_bwd", "moe_permute_bwd"):
+        assert must in names
+    assert set(names) == set(_lib.PROTOTYPES), "binding prototypes differ from the header"
+
+
+@needs_nvcc
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+@needs_nvcc
+def test_host_only_entry_points(lib):
+    assert lib.moe_version() >= 100
+    assert lib.moe_status_string(0) == b"ok"
+    assert lib.moe_status_string(6) == b"bounded device wait ran out"
+    # capacity of the padded layout: round_up(T*k + E*127, 128)
+    assert lib.moe_padded_rows(512, 2, 8) == 2048
+    assert lib.moe_padded_rows(65536, 8, 64) == 532480
+    assert lib.moe_padded_rows(1, 1, 1) == 128
+    assert lib.moe_workspace_bytes(65536, 4096, 64, 8) >= 32 * 64 * 4096 * 4
+    assert lib.moe_workspace_bytes(0, 1, 1, 1) == 0
+
+
+@needs_nvcc
+def test_argument_checks_return_before_any_device_work(lib):
+    # null pointers are rejected on the host
+    rc = lib.moe_route(None, None, None, 16, 128, 8, 2, 0, 0.0, None, None, None, None, None,
+                       None, None, 0, None)
+    assert rc == 1
+    rc = lib.moe_permute(None, None, 16, 128, 8, 2, None, None, None, None, None, None, None, 0, None)
+    assert rc == 1
+    rc = lib.moe_expert_fwd(None, None, 1, 16, 128, 128, None, None, None, None, None, None, None,
+                            None, 0, None)
+    assert rc == 1
+    rc = lib.moe_bias_update(None, 8, 16, 2, 0.001, None, None)
+    assert rc == 1
+    code = ctypes.c_int(0)
+    assert lib.moe_device_status(None, None, None) == 1
