@@ -8,8 +8,8 @@ import torch
 from oracle import moe_oracle as O
 from pretraining_sigmoid_softmax_gb300 import ops
 
-from gpu_common import (assert_close, dev, gpu_rows, h64, padded_offsets, randn_bf16,
-                        require_gpu)
+from gpu_common import (assert_close, assert_gemm_exact, dev, gpu_rows, h64, padded_offsets,
+                        randn_bf16, require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -181,6 +181,17 @@ def _run_experts(X, dY, row_offsets, W_g, W_u, W_d):
     ops.moe_expert_fwd(dev(X), ro, dev(W_g), dev(W_u), dev(W_d), B["A"], B["U"], B["H"], B["Y"], ws)
     ops.moe_expert_bwd(dev(dY), dev(X), B["A"], B["U"], B["H"], ro, dev(W_g), dev(W_u), dev(W_d),
                        B["dX"], B["dA"], B["dU"], B["dW_g"], B["dW_u"], B["dW_d"], ws)
+    # the backward again with caller-made saved activations (padding rows zero), so that
+    # the weight-gradient GEMM can be checked on operands that are all test inputs
+    g = torch.Generator().manual_seed(rows + 99)
+    live = (X.float().abs().sum(1, keepdim=True) > 0).to(torch.bfloat16)
+    B["Hin"] = randn_bf16((rows, f), g) * live
+    B2 = _expert_buffers(rows, d, f, E)
+    ops.moe_expert_bwd(dev(dY), dev(X), dev(randn_bf16((rows, f), g) * live),
+                       dev(randn_bf16((rows, f), g) * live), dev(B["Hin"]), ro, dev(W_g),
+                       dev(W_u), dev(W_d), B2["dX"], B2["dA"], B2["dU"], B2["dW_g"], B2["dW_u"],
+                       B2["dW_d"], ws)
+    B["dW_d_in"] = B2["dW_d"]
     torch.cuda.synchronize()
     assert ops.moe_device_status()[0] == 0
     return B
@@ -203,9 +214,13 @@ def _check_expert(B, e, lo, hi, X, dY, W_g, W_u, W_d, tag):
     assert_close(B["dA"][lo:hi], gr["dA"], f"{tag} dA")
     assert_close(B["dU"][lo:hi], gr["dU"], f"{tag} dU")
     assert_close(B["dX"][lo:hi], gr["dX"], f"{tag} dX")
-    assert_close(B["dW_d"][e], gr["dW_d"], f"{tag} dW_d")
-    assert_close(B["dW_g"][e], gr["dW_g"], f"{tag} dW_g")
-    assert_close(B["dW_u"][e], gr["dW_u"], f"{tag} dW_u")
+    assert_close(B["dW_d"][e], gr["dW_d"], f"{tag} dW_d", reduction=True)
+    assert_close(B["dW_g"][e], gr["dW_g"], f"{tag} dW_g", reduction=True)
+    assert_close(B["dW_u"][e], gr["dW_u"], f"{tag} dW_u", reduction=True)
+    # tensor-core results of the caller's own operands: within half a bf16 ulp + fp32 bound
+    assert_gemm_exact(B["A"][lo:hi], x, h64(W_g[e]).T, f"{tag} A exact")
+    assert_gemm_exact(B["U"][lo:hi], x, h64(W_u[e]).T, f"{tag} U exact")
+    assert_gemm_exact(B["dW_d_in"][e], h64(dY[lo:hi]).T, h64(B["Hin"][lo:hi]), f"{tag} dW_d exact")
 
 
 @pytest.mark.parametrize("rows,d,f", [(200, 256, 128), (128, 384, 256), (77, 128, 128),
@@ -278,7 +293,7 @@ def test_combine_and_backward_kernels():
     rdYp, rdg = O.combine_backward(h64(dY), Yp64, h64(gate), D["slot_to_row"], D["perm_token"],
                                    D["perm_slot"], O.bf16_round)
     assert_close(dY_perm[torch.from_numpy(rows).cuda()], rdYp, "dY_perm")
-    assert_close(dg, rdg, "dg", atol=1e-4, rtol=1e-4)
+    assert_close(dg, rdg, "dg", atol=1e-4, rtol=1e-4, reduction=True)
     pad = torch.from_numpy(np.setdiff1d(np.arange(int(ro[-1])), rows)).cuda()
     assert (dY_perm[pad].float() == 0).all()
     # input gradient with shared and router terms
@@ -316,7 +331,7 @@ def test_router_backward(mode):
     ref = O._regate(ref, lg, r["idx"].cpu().numpy(), mode, h64(b), z)
     rb = O.router_backward(h64(dg), ref, h64(x), h64(W_r), mode, z)
     assert_close(dl, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
-    assert_close(dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3)
+    assert_close(dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)
 
 
 def test_bias_update_is_bit_exact():

@@ -33,7 +33,7 @@ class Lazy:
         return O.to64(self.t[key])
 
 
-WEIGHTS = ("W_g", "W_u", "W_d", "Ws_g", "Ws_u", "Ws_d")
+WEIGHTS = ("W_g", "W_u", "W_d")  # converted to fp64 slice by slice
 
 
 def run_gpu(cfg: MoEConfig, inp: dict):
@@ -91,11 +91,11 @@ def full_parity(cfg, inp):
     bwd = O.layer_backward(i64, fwd, O.to64(inp["dY"]))
     assert_close(plan.dx, bwd["dx"], "dx")
     for name in ("dW_g", "dW_u", "dW_d"):
-        assert_close(getattr(plan, name), bwd[name], name)
-    assert_close(plan.dW_r, bwd["dW_r"], "dW_r")
+        assert_close(getattr(plan, name), bwd[name], name, reduction=True)
+    assert_close(plan.dW_r, bwd["dW_r"], "dW_r", reduction=True)
     if cfg.f_shared:
         for name in ("dWs_g", "dWs_u", "dWs_d"):
-            assert_close(getattr(plan, name), bwd[name], name)
+            assert_close(getattr(plan, name), bwd[name], name, reduction=True)
     if cfg.bias_update:
         ref = O.bias_update(D["counts"], inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), ref.view(np.uint32))
@@ -178,8 +178,8 @@ def test_workload_sampled_parity(name):
         lo, hi = int(D["offsets"][e]), int(D["offsets"][e + 1])
         tok_e = D["perm_token"][lo:hi]
         gates = ref["gate"][tok_e, D["perm_slot"][lo:hi]]
-        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f))) for _ in range(3)]
-        eg = [(int(rng.integers(cfg.f)), int(rng.integers(cfg.d))) for _ in range(3)]
+        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f))) for _ in range(8)]
+        eg = [(int(rng.integers(cfg.f)), int(rng.integers(cfg.d))) for _ in range(8)]
         want = O.expert_weight_grad_entries(
             {"x": O.to64(inp["x"][torch.from_numpy(tok_e)]), "W_g": lazy["W_g"],
              "W_u": lazy["W_u"], "W_d": lazy["W_d"]},
@@ -188,23 +188,26 @@ def test_workload_sampled_parity(name):
         got_d = [float(plan.dW_d[e, i, j]) for (i, j) in ed]
         got_g = [float(plan.dW_g[e, j, i]) for (j, i) in eg]
         got_u = [float(plan.dW_u[e, j, i]) for (j, i) in eg]
-        assert_close(np.array(got_d), want["dW_d"], f"dW_d[{e}]")
-        assert_close(np.array(got_g), want["dW_g"], f"dW_g[{e}]")
-        assert_close(np.array(got_u), want["dW_u"], f"dW_u[{e}]")
+        assert_close(np.array(got_d), want["dW_d"], f"dW_d[{e}]", reduction=True)
+        assert_close(np.array(got_g), want["dW_g"], f"dW_g[{e}]", reduction=True)
+        assert_close(np.array(got_u), want["dW_u"], f"dW_u[{e}]", reduction=True)
     for e in np.nonzero(counts == 0)[0]:
         for name in ("dW_g", "dW_u", "dW_d"):
             assert (getattr(plan, name)[int(e)] == 0).all()
     if cfg.zipf:
         assert (counts == 0).sum() >= 10
     if cfg.f_shared:
-        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f_shared))) for _ in range(2)]
-        eg = [(int(rng.integers(cfg.f_shared)), int(rng.integers(cfg.d))) for _ in range(2)]
-        want = O.shared_weight_grad_entries({"x": O.to64(inp["x"]), "Ws_g": lazy["Ws_g"][:],
-                                             "Ws_u": lazy["Ws_u"][:], "Ws_d": lazy["Ws_d"][:]},
+        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f_shared))) for _ in range(6)]
+        eg = [(int(rng.integers(cfg.f_shared)), int(rng.integers(cfg.d))) for _ in range(6)]
+        want = O.shared_weight_grad_entries({"x": O.to64(inp["x"]), "Ws_g": lazy["Ws_g"],
+                                             "Ws_u": lazy["Ws_u"], "Ws_d": lazy["Ws_d"]},
                                             O.to64(inp["dY"]), ed, eg, rnd=RND)
-        assert_close(np.array([float(plan.dWs_d[i, j]) for (i, j) in ed]), want["dWs_d"], "dWs_d")
-        assert_close(np.array([float(plan.dWs_g[j, i]) for (j, i) in eg]), want["dWs_g"], "dWs_g")
-        assert_close(np.array([float(plan.dWs_u[j, i]) for (j, i) in eg]), want["dWs_u"], "dWs_u")
+        assert_close(np.array([float(plan.dWs_d[i, j]) for (i, j) in ed]), want["dWs_d"], "dWs_d",
+                     reduction=True)
+        assert_close(np.array([float(plan.dWs_g[j, i]) for (j, i) in eg]), want["dWs_g"], "dWs_g",
+                     reduction=True)
+        assert_close(np.array([float(plan.dWs_u[j, i]) for (j, i) in eg]), want["dWs_u"], "dWs_u",
+                     reduction=True)
     if cfg.bias_update:
         refb = O.bias_update(counts, inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), refb.view(np.uint32))
@@ -241,4 +244,4 @@ def test_router_backward_at_full_size():
     ref = O._regate(ref, lg, plan.topk_idx.cpu().numpy(), "sigmoid", O.to64(b), 0.0)
     rb = O.router_backward(O.to64(dg), ref, O.to64(x), O.to64(W_r), "sigmoid", 0.0)
     assert_close(plan.dlogits, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
-    assert_close(plan.dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3)
+    assert_close(plan.dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)
