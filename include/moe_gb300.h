@@ -60,7 +60,8 @@ enum moe_status {
     MOE_ERR_WORKSPACE = 3,    /* ws_bytes smaller than moe_workspace_bytes() */
     MOE_ERR_LAUNCH = 4,       /* a CUDA launch or runtime call failed */
     MOE_ERR_BAD_INDEX = 5,    /* device: an expert index outside [0, E) or a layout overflow */
-    MOE_ERR_TIMEOUT = 6       /* device: a bounded wait inside a kernel ran out */
+    MOE_ERR_TIMEOUT = 6,      /* device: a bounded wait inside a kernel ran out */
+    MOE_ERR_TOO_LARGE = 7     /* sizes exceed a fixed, library-owned scratch array */
 };
 
 enum moe_router_mode {
@@ -136,6 +137,35 @@ int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, in
                 int32_t* counts, int64_t* offsets, int64_t* row_offsets, int32_t* perm_token,
                 int32_t* slot_to_row, moe_bf16* X_perm, void* ws, size_t ws_bytes,
                 moe_stream_t stream);
+
+/*
+ * moe_permute_noalloc - moe_permute for callers that cannot allocate device memory.
+ * The source pages have no counterpart to this entry point; it exists for the library's
+ * users. Some callers hold only the input and output buffers of the layer: a plug-in or
+ * fixed-signature callback that is handed tensors but no allocator, or a process whose
+ * device memory is owned entirely by another allocator. They cannot provide the `ws`
+ * scratch that moe_permute needs and cannot call cudaMalloc to make one.
+ * This variant takes the same arguments as moe_permute minus `ws`/`ws_bytes` and gives
+ * the same results. Its scratch (two ceil(T/1024) x E int32 tables of per-chunk expert
+ * counts) lives in a static device array of MOE_PERMUTE_NOALLOC_MAX_INTS int32 per table
+ * (2 MiB in total), which every GPU that loads the library holds until the process exits.
+ *   - Limit: ceil(T / 1024) * E <= MOE_PERMUTE_NOALLOC_MAX_INTS (T up to 4,194,304 tokens
+ *     with E = 64, 1,048,576 with E = 256); larger sizes return MOE_ERR_TOO_LARGE before
+ *     any device work.
+ *   - Allocation: none. It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - Set-up: the first call on each device (made with that device current) looks up the
+ *     device address of the static array once; make that first call before any stream
+ *     capture on that device.
+ *   - Sharing: all calls on a device use the same array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero: every entry is written before it is
+ *     read). Calls that overlap on the GPU (different streams, no ordering between them)
+ *     race on the array and give wrong results; order them on one stream.
+ */
+#define MOE_PERMUTE_NOALLOC_MAX_INTS 262144
+int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, int E,
+                        int k, int32_t* counts, int64_t* offsets, int64_t* row_offsets,
+                        int32_t* perm_token, int32_t* slot_to_row, moe_bf16* X_perm,
+                        moe_stream_t stream);
 
 /*
  * moe_expert_fwd - SwiGLU experts as grouped GEMMs (G1 + G2), on tcgen05 tensor cores.

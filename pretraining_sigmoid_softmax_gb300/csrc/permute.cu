@@ -11,6 +11,8 @@
 // memory only (order-independent); every floating-point sum has a fixed order.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "sizes.h"
 
@@ -492,5 +494,77 @@ extern "C" int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_r
         reinterpret_cast<const __nv_bfloat16*>(dX_perm), slot_to_row,
         reinterpret_cast<const __nv_bfloat16*>(dx_shared), dlogits, W_r, T, d, E, k,
         reinterpret_cast<__nv_bfloat16*>(dx));
+    return launch_status();
+}
+
+// ------------------------------------------------------------------------------------
+// moe_permute_noalloc: the same launches as moe_permute, with the two per-chunk count
+// tables in a library-owned static device array instead of the caller's workspace, for
+// callers that have no way to allocate device memory (see the header).
+
+namespace {
+
+constexpr int kNoallocMaxInts = MOE_PERMUTE_NOALLOC_MAX_INTS;
+constexpr int kNoallocMaxDevices = 64;
+
+// [0, kNoallocMaxInts): per-chunk counts; [kNoallocMaxInts, 2 kNoallocMaxInts): chunk bases.
+static __device__ __align__(256) int32_t g_permute_scratch[2 * kNoallocMaxInts];
+
+int32_t* g_permute_scratch_ptr[kNoallocMaxDevices] = {nullptr};
+std::mutex g_permute_scratch_mu;
+
+// Device address of g_permute_scratch on the current device, looked up once per device.
+// In host code the symbol name is only a host-side handle, so the address must come from
+// the runtime before a kernel can be given it.
+int32_t* permute_scratch_on_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_permute_scratch_mu);
+    if (!g_permute_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
+            return nullptr;
+        g_permute_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    return g_permute_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d,
+                                   int E, int k, int32_t* counts, int64_t* offsets,
+                                   int64_t* row_offsets, int32_t* perm_token,
+                                   int32_t* slot_to_row, moe_bf16* X_perm,
+                                   moe_stream_t stream) {
+    if (!topk_idx || !x || !counts || !offsets || !row_offsets || !perm_token || !slot_to_row ||
+        !X_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(X_perm)) return MOE_ERR_INVALID_ARG;
+    const int64_t nb = hist_blocks(T);
+    if (nb * E > kNoallocMaxInts) return MOE_ERR_TOO_LARGE;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    int* status = device_status_word();
+    if (!status) return MOE_ERR_LAUNCH;
+    int32_t* scratch = permute_scratch_on_current_device();
+    if (!scratch) return MOE_ERR_LAUNCH;
+    int32_t* bcounts = scratch;
+    int32_t* bbase = scratch + kNoallocMaxInts;
+    cudaStream_t st = (cudaStream_t)stream;
+    hist_kernel<<<(unsigned)nb, kHistThreads, 0, st>>>(topk_idx, T, E, k, bcounts, status);
+    scan_kernel<<<1, kMaxExperts, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
+    pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, counts, d, perm_token,
+                                       reinterpret_cast<__nv_bfloat16*>(X_perm));
+    const size_t sc_smem = sizeof(int32_t) * 64 * E;
+    if (cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sc_smem) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    scatter_kernel<<<(unsigned)nb, kScatterThreads, sc_smem, st>>>(topk_idx, T, E, k, bbase,
+                                                                   row_offsets, perm_token,
+                                                                   slot_to_row);
+    gather_kernel<<<warp_grid(T), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x),
+                                                slot_to_row, T, d, k,
+                                                reinterpret_cast<__nv_bfloat16*>(X_perm));
     return launch_status();
 }

@@ -82,6 +82,7 @@ const char* moe_status_string(int status) {
         case MOE_ERR_LAUNCH: return "CUDA launch or runtime error";
         case MOE_ERR_BAD_INDEX: return "expert index out of range or layout overflow";
         case MOE_ERR_TIMEOUT: return "bounded device wait ran out";
+        case MOE_ERR_TOO_LARGE: return "sizes exceed the library's fixed scratch array";
         default: return "unknown status";
     }
 }

@@ -90,6 +90,19 @@ def moe_permute(topk_idx, x, E, counts, offsets, row_offsets, perm_token, slot_t
                                    _p(ws), ws.numel(), _stream(stream)), "moe_permute")
 
 
+def moe_permute_noalloc(topk_idx, x, E, counts, offsets, row_offsets, perm_token, slot_to_row,
+                        X_perm, stream=None):
+    """moe_permute without a workspace argument: its scratch is a fixed, library-owned
+    device array, for callers that cannot allocate device memory."""
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    _contig(topk_idx, x, counts, offsets, row_offsets, perm_token, slot_to_row, X_perm)
+    _check(_lib.load().moe_permute_noalloc(_p(topk_idx), _p(x), T, d, E, k, _p(counts),
+                                           _p(offsets), _p(row_offsets), _p(perm_token),
+                                           _p(slot_to_row), _p(X_perm), _stream(stream)),
+           "moe_permute_noalloc")
+
+
 def moe_expert_fwd(X, row_offsets, W_g, W_u, W_d, A, U, H, Y, ws, stream=None):
     rows, d = X.shape
     E, f, _ = W_g.shape
