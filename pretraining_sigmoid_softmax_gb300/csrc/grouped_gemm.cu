@@ -57,9 +57,11 @@ struct Cfg {
     static constexpr int STAGES = (kSmemBudget / STAGE_BYTES) > 6 ? 6 : (kSmemBudget / STAGE_BYTES);
     static constexpr int ACC_COLS = DUAL ? 2 * BN : BN;
     static constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulator buffers
-    static constexpr uint32_t IDESC = idesc_bf16_m128(BN, A_MN, B_MN);
+    // DUAL: the W_g and W_u boxes sit back to back in shared memory as one 2*BN-row B tile,
+    // so a single N = 2*BN instruction fills gate columns [0, BN) and up columns [BN, 2BN).
+    static constexpr uint32_t IDESC = idesc_bf16_m128(DUAL ? 2 * BN : BN, A_MN, B_MN);
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory columns");
-    static_assert(BN % 64 == 0 && BN <= 256, "tile width");
+    static_assert(BN % 64 == 0 && (DUAL ? 2 * BN : BN) <= 256, "tile width");
     static constexpr size_t SMEM_BYTES =
         1024 + (size_t)STAGES * STAGE_BYTES + 1024 /* barriers etc. */ +
         sizeof(int64_t) * (kMaxExperts + 1) + sizeof(int32_t) * kMaxExperts;
@@ -226,9 +228,25 @@ __device__ __forceinline__ uint4 pack_chunk8(const float* v) {
                       pack_bf16x2(v[6], v[7]));
 }
 
+// Saved a and u (32 bf16 each) of one 32-column chunk of this thread's row.
+struct AuChunk {
+    uint4 a[4];
+    uint4 u[4];
+};
+
+__device__ __forceinline__ void load_au(AuChunk& c, const Params& P, int64_t off) {
+    const uint4* pa = reinterpret_cast<const uint4*>(P.in0 + off);
+    const uint4* pu = reinterpret_cast<const uint4*>(P.in1 + off);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        c.a[q] = __ldg(pa + q);
+        c.u[q] = __ldg(pu + q);
+    }
+}
+
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc, int row_in_tile,
-                                              const Params& P) {
+                                              const Params& P, AuChunk& pre) {
     if constexpr (C::WGRAD) {
         const int64_t row = ti.m0 + row_in_tile;
         __nv_bfloat16* out = (ti.p == 0 ? P.out0 : P.out1) +
@@ -278,18 +296,24 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
                     }
                 }
             } else if constexpr (C::EPI == kEpiSwigluBwd) {
+                // saved a, u of this chunk were loaded one chunk ahead (chunk 0 before the
+                // accumulator wait); start the next chunk's loads before using these
+                uint4 ca[4], cu[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    ca[q] = pre.a[q];
+                    cu[q] = pre.u[q];
+                }
                 uint32_t r[32];
                 tmem_ld32(t_acc + c, r);
+                if (ok && c + 32 < C::BN) load_au(pre, P, base + c + 32);
                 tmem_ld_wait();
                 if (ok) {
-                    const uint4* pa = reinterpret_cast<const uint4*>(P.in0 + base + c);
-                    const uint4* pu = reinterpret_cast<const uint4*>(P.in1 + base + c);
                     float dav[32], duv[32];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint4 a4 = pa[q], u4 = pu[q];
-                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
-                        const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+                        const uint32_t aw[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
+                        const uint32_t uw[4] = {cu[q].x, cu[q].y, cu[q].z, cu[q].w};
 #pragma unroll
                         for (int h = 0; h < 8; ++h) {
                             const float a = (h & 1) ? bf16_hi(aw[h >> 1]) : bf16_lo(aw[h >> 1]);
@@ -428,10 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    : sdesc_sw128(b_s + kk * 32, 16, 1024);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     umma_bf16(d_tmem, adesc, bdesc, C::IDESC, acc);
-                    if constexpr (C::DUAL) {
-                        const uint64_t b1desc = sdesc_sw128(b_s + C::BN * 128 + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem + C::BN, adesc, b1desc, C::IDESC, acc);
-                    }
                 }
                 umma_commit(smem_u32(&S.empty[stage]));
                 if (++stage == C::STAGES) {
@@ -451,13 +471,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileInfo ti = decode<C>(tile, P, S);
             const int buf = local & 1;
             const uint32_t ph = (local >> 1) & 1;
+            AuChunk pre;
+            if constexpr (C::EPI == kEpiSwigluBwd) {  // first chunk's a, u before the wait
+                const int64_t row = ti.m0 + row_in_tile;
+                if (row < P.rows) load_au(pre, P, row * (int64_t)P.ld_out + ti.n0);
+            }
             bool ok = mbar_wait_bounded(smem_u32(&S.tfull[buf]), ph, abort_flag, P.status,
                                         P.wait_limit_ns, 33);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_acc = tmem_base + buf * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
-            epilogue_tile<C>(ti, t_acc, row_in_tile, P);
+            epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&S.tempty[buf]));

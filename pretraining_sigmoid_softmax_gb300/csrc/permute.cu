@@ -327,45 +327,62 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     }
 }
 
-// dx[t] = sum_i dX_perm[row(t,i)] + dx_shared[t] + sum_e dlogits[t,e] W_r[e].
+// dx[t] = sum_i dX_perm[slot_to_row[t,i]] + dx_shared[t] + sum_e dlogits[t,e] W_r[e].
+// One warp per token. The token's nonzero router terms (k in sigmoid mode, E in softmax
+// mode) are listed once, in expert order, in the warp's shared-memory slice; the row loop
+// then touches only those rows of W_r.
+template <int KMAX>
 __global__ void __launch_bounds__(256) permute_bwd_kernel(
     const __nv_bfloat16* __restrict__ dX_perm, const int32_t* __restrict__ slot_to_row,
     const __nv_bfloat16* __restrict__ dx_sh, const float* __restrict__ dlogits,
     const float* __restrict__ W_r, int64_t T, int d, int E, int k,
     __nv_bfloat16* __restrict__ dx) {
-    const int lane = threadIdx.x % 32;
-    const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
-    if (t >= T) return;
+    __shared__ int s_e[kWarpsPerCta][kMaxExperts];
+    __shared__ float s_g[kWarpsPerCta][kMaxExperts];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + warp;
+    if (t >= T) return;  // whole warp
     int32_t my_row = -1;
     if (lane < k) my_row = slot_to_row[t * k + lane];
-    const int nvec = d / 8;
-    int32_t rows[32];
+    int32_t rows[KMAX];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) rows[i] = __shfl_sync(0xffffffffu, my_row, i);
+    for (int i = 0; i < KMAX; ++i) rows[i] = __shfl_sync(0xffffffffu, my_row, i);
+    int n = 0;
+    if (dlogits) {
+        for (int e0 = 0; e0 < E; e0 += 32) {  // warp-uniform trip count
+            const int e = e0 + lane;
+            const float g = e < E ? dlogits[t * E + e] : 0.f;
+            const unsigned m = __ballot_sync(0xffffffffu, g != 0.f);
+            if (g != 0.f) {
+                const int pos = n + __popc(m & ((1u << lane) - 1u));
+                s_e[warp][pos] = e;
+                s_g[warp][pos] = g;
+            }
+            n += __popc(m);
+        }
+        __syncwarp();
+    }
+    const int nvec = d / 8;
     for (int c = lane; c < nvec; c += 32) {  // no warp collectives inside
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < KMAX; ++i) {
             if (i < k && rows[i] >= 0)
                 add_bf16x8(acc, reinterpret_cast<const uint4*>(dX_perm + (int64_t)rows[i] * d)[c]);
         }
         if (dx_sh) add_bf16x8(acc, reinterpret_cast<const uint4*>(dx_sh + t * d)[c]);
-        if (dlogits) {
-            for (int e = 0; e < E; ++e) {
-                const float g = dlogits[t * E + e];  // same address across the warp
-                if (g != 0.f) {
-                    const float4* w = reinterpret_cast<const float4*>(W_r + (int64_t)e * d + c * 8);
-                    const float4 a = w[0], b = w[1];
-                    acc[0] = fmaf(g, a.x, acc[0]);
-                    acc[1] = fmaf(g, a.y, acc[1]);
-                    acc[2] = fmaf(g, a.z, acc[2]);
-                    acc[3] = fmaf(g, a.w, acc[3]);
-                    acc[4] = fmaf(g, b.x, acc[4]);
-                    acc[5] = fmaf(g, b.y, acc[5]);
-                    acc[6] = fmaf(g, b.z, acc[6]);
-                    acc[7] = fmaf(g, b.w, acc[7]);
-                }
-            }
+        for (int j = 0; j < n; ++j) {
+            const float g = s_g[warp][j];
+            const float4* w = reinterpret_cast<const float4*>(W_r + (int64_t)s_e[warp][j] * d + c * 8);
+            const float4 a = __ldg(w), b = __ldg(w + 1);
+            acc[0] = fmaf(g, a.x, acc[0]);
+            acc[1] = fmaf(g, a.y, acc[1]);
+            acc[2] = fmaf(g, a.z, acc[2]);
+            acc[3] = fmaf(g, a.w, acc[3]);
+            acc[4] = fmaf(g, b.x, acc[4]);
+            acc[5] = fmaf(g, b.y, acc[5]);
+            acc[6] = fmaf(g, b.z, acc[6]);
+            acc[7] = fmaf(g, b.w, acc[7]);
         }
         reinterpret_cast<uint4*>(dx + t * d)[c] = pack8(acc);
     }
@@ -490,10 +507,16 @@ extern "C" int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_r
         (W_r && !aligned16(W_r)))
         return MOE_ERR_INVALID_ARG;
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
-    permute_bwd_kernel<<<warp_grid(T), 256, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(dX_perm), slot_to_row,
-        reinterpret_cast<const __nv_bfloat16*>(dx_shared), dlogits, W_r, T, d, E, k,
-        reinterpret_cast<__nv_bfloat16*>(dx));
+    cudaStream_t st = (cudaStream_t)stream;
+    const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(dX_perm);
+    const __nv_bfloat16* sh = reinterpret_cast<const __nv_bfloat16*>(dx_shared);
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(dx);
+    const unsigned grid = warp_grid(T);
+    if (k <= 2) permute_bwd_kernel<2><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
+    else if (k <= 4) permute_bwd_kernel<4><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
+    else if (k <= 8) permute_bwd_kernel<8><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
+    else if (k <= 16) permute_bwd_kernel<16><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
+    else permute_bwd_kernel<32><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
     return launch_status();
 }
 
