@@ -129,7 +129,8 @@ def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
         if cfg.backward:
             O.layer_backward(i64, fwd, dY)
         if cfg.bias_update:
-            O.bias_update(fwd["counts"], i64["b"].astype("float32"), T_s, cfg.k, cfg.gamma)
+            rule = O.bias_update_proportional if cfg.bias_rule == "proportional" else O.bias_update
+            rule(fwd["counts"], i64["b"].astype("float32"), T_s, cfg.k, cfg.gamma)
         times.append(time.perf_counter() - t0)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return T_s / statistics.median(times), cores, times
@@ -195,7 +196,7 @@ def main():
         if cfg.backward:
             plan.backward(dY)
             if cfg.bias_update:
-                plan.bias_update(b_work, cfg.gamma)
+                plan.bias_update(b_work, cfg.gamma, cfg.bias_rule)
 
     def sync_all():
         torch.cuda.synchronize()

@@ -209,6 +209,18 @@ int moe_bias_update(const int32_t* counts, int E, int64_t T, int k, float gamma,
                     moe_stream_t stream);
 
 /*
+ * moe_bias_update_proportional - the proportional variant of the bias update, named by the
+ * Apex-3 benchmark and training commands ("router_bias_update=proportional", rates 0.01 and
+ * 1e-3) on "The whole stack, in the open", "Run it yourself". The page prints no formula;
+ * reading: the step is proportional to the relative load deviation,
+ *   b[e] = fp32(b[e] + fp32(gamma * r_e)),  r_e = fp32((T*k - E*counts[e]) / (T*k)),
+ * with the ratio formed exactly from integers in fp64 and each fp32 operation rounded once.
+ * In : counts [E] int32.  In/out: b [E] fp32.
+ */
+int moe_bias_update_proportional(const int32_t* counts, int E, int64_t T, int k, float gamma,
+                                 float* b, moe_stream_t stream);
+
+/*
  * moe_combine_bwd - backward of moe_combine (B1).
  * Definition: dY_perm[slot_to_row[t,i]] = bf16(topk_gate[t,i] * dY[t]);
  * dg[t,i] = sum_j dY[t,j] * Y_perm[slot_to_row[t,i], j] (fp32, fixed order).

@@ -454,6 +454,21 @@ def bias_update(counts: np.ndarray, b: np.ndarray, T: int, k: int, gamma: float)
     return (np.asarray(b, dtype=np.float32) + np.float32(gamma) * sgn).astype(np.float32)
 
 
+def bias_update_proportional(counts: np.ndarray, b: np.ndarray, T: int, k: int,
+                             gamma: float) -> np.ndarray:
+    """Proportional variant (the Apex-3 commands' router_bias_update=proportional, whose
+    formula the page does not print). Reading: the step is proportional to the relative
+    load deviation, b_e <- b_e + gamma * (mean - c_e) / mean with mean = T*k/E.
+
+    Evaluated as: r_e = (T*k - E*c_e) / (T*k) exactly in fp64 (integers), rounded once to
+    fp32; then fp32(gamma * r_e) and fp32(b_e + that), each one fp32 rounding."""
+    E = b.shape[0]
+    N = np.float64(T) * k
+    r = ((N - np.float64(E) * counts.astype(np.float64)) / N).astype(np.float32)
+    step = (np.float32(gamma) * r).astype(np.float32)
+    return (np.asarray(b, dtype=np.float32) + step).astype(np.float32)
+
+
 # ---------------------------------------------------------------------------------------
 # sampled evaluation for workloads too large to run whole on the CPU
 

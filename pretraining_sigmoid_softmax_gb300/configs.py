@@ -29,6 +29,7 @@ class MoEConfig:
     gamma: float = 0.001   # bias update step
     z_coef: float = 0.0    # router z-loss coefficient (softmax mode)
     zipf: bool = False     # skewed expert popularity with a block of never-chosen experts
+    bias_rule: str = "sign"  # "sign": b += gamma sign(mean - c); "proportional": gamma (mean - c)/mean
 
     @property
     def N(self) -> int:
@@ -68,4 +69,11 @@ C3 = MoEConfig("skewed_T32768_d2048_E128_k8_f768", T=32768, d=2048, E=128, k=8, 
 C4 = MoEConfig("large_T65536_d4096_E64_k8_f1536_shared3072", T=65536, d=4096, E=64, k=8,
                f=1536, f_shared=3072, mode="sigmoid", seed=4, backward=True, bias_update=True)
 
-CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4}
+# The Apex-3 step-10 benchmark's layer ("The whole stack, in the open", "Run it yourself":
+# 64 experts, expert width 1280, top-4, router bias rate 0.01 with the proportional update,
+# micro-batch 6 x 8192 tokens). d_model is not printed there; 2048 is a reading.
+C5 = MoEConfig("apex3_T49152_d2048_E64_k4_f1280_proportional", T=49152, d=2048, E=64, k=4,
+               f=1280, f_shared=0, mode="sigmoid", seed=5, backward=True, bias_update=True,
+               gamma=0.01, bias_rule="proportional")
+
+CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5}

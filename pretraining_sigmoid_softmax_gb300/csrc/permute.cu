@@ -398,6 +398,19 @@ __global__ void bias_update_kernel(const int32_t* __restrict__ counts, int E, in
     b[e] = b[e] + gamma * sgn;
 }
 
+// Proportional variant: b[e] += gamma * (T*k - E*c) / (T*k). The ratio is formed in fp64
+// from exact integers and rounded once to fp32; the product and the sum are single fp32
+// roundings (no fused multiply-add).
+__global__ void bias_update_proportional_kernel(const int32_t* __restrict__ counts, int E,
+                                                int64_t T, int k, float gamma,
+                                                float* __restrict__ b) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const double n = (double)T * (double)k;
+    const float r = (float)((n - (double)E * (double)counts[e]) / n);
+    b[e] = __fadd_rn(b[e], __fmul_rn(gamma, r));
+}
+
 inline unsigned warp_grid(int64_t T) { return (unsigned)cdiv(T, kWarpsPerCta); }
 
 bool shape_ok(int64_t T, int d, int E, int k) {
@@ -467,6 +480,15 @@ extern "C" int moe_bias_update(const int32_t* counts, int E, int64_t T, int k, f
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     bias_update_kernel<<<(unsigned)cdiv(E, 256), 256, 0, (cudaStream_t)stream>>>(counts, E, T, k,
                                                                                 gamma, b);
+    return launch_status();
+}
+
+extern "C" int moe_bias_update_proportional(const int32_t* counts, int E, int64_t T, int k,
+                                            float gamma, float* b, moe_stream_t stream) {
+    if (!counts || !b || E <= 0 || T <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    bias_update_proportional_kernel<<<(unsigned)cdiv(E, 256), 256, 0, (cudaStream_t)stream>>>(
+        counts, E, T, k, gamma, b);
     return launch_status();
 }
 

@@ -18,7 +18,6 @@
 namespace moe {
 namespace {
 
-constexpr int kTM = kRouteTokensPerCta;  // tokens per CTA (64)
 constexpr int kKC = 32;                  // d-chunk per smem stage
 constexpr int kThreads = 256;
 
@@ -29,80 +28,129 @@ __device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
 
 __device__ __forceinline__ float sigmoid_f(float l) { return 1.0f / (1.0f + expf(-l)); }
 
-// EJ = experts per thread column (E padded to 16 * EJ).
-template <int EJ>
+// Logit tile of TM tokens x EP (padded) experts per CTA, 256 threads; each thread owns
+// TTOK tokens x EJ experts and sums over d sequentially (fixed order). The next 32-wide
+// d-chunk is prefetched into registers while the current one is multiplied from shared
+// memory.
+template <int EP, int TM, int TTOK, int EJ>
 __global__ void __launch_bounds__(kThreads) route_fwd_kernel(
     const __nv_bfloat16* __restrict__ x, const float* __restrict__ W_r,
     const float* __restrict__ bias, int64_t T, int d, int E, int k, int mode,
     float* __restrict__ logits, int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
     float* __restrict__ topk_score, float* __restrict__ lse_out, double* __restrict__ z_part) {
-    constexpr int EP = 16 * EJ;  // padded expert count of this instantiation
+    constexpr int TXN = EP / EJ;  // thread columns
+    static_assert((TM / TTOK) * TXN == kThreads, "thread tiling");
+    static_assert(TTOK % 4 == 0 && (EJ % 4 == 0 || EJ == 2), "vector widths");
+    constexpr int XV = TM * (kKC / 8);  // uint4 (8 bf16) per x chunk
+    constexpr int WV = EP * (kKC / 4);  // float4 per W chunk
+    constexpr int XL = (XV + kThreads - 1) / kThreads;
+    constexpr int WL = (WV + kThreads - 1) / kThreads;
     // dynamic smem: the staging tiles (xs, wsm) and later the logit tile (lg) share space
     extern __shared__ __align__(16) unsigned char route_smem[];
-    float(*xs)[kTM] = reinterpret_cast<float(*)[kTM]>(route_smem);
-    float(*wsm)[EP] = reinterpret_cast<float(*)[EP]>(route_smem + sizeof(float) * kKC * kTM);
+    float(*xs)[TM] = reinterpret_cast<float(*)[TM]>(route_smem);
+    float(*wsm)[EP] = reinterpret_cast<float(*)[EP]>(route_smem + sizeof(float) * kKC * TM);
     float(*lg)[EP + 1] = reinterpret_cast<float(*)[EP + 1]>(route_smem);
     __shared__ double zw[kThreads / 32];
 
     const int tid = threadIdx.x;
-    const int ty = tid / 16, tx = tid % 16;
-    const int64_t t0 = (int64_t)blockIdx.x * kTM;
+    const int ty = tid / TXN, tx = tid % TXN;
+    const int64_t t0 = (int64_t)blockIdx.x * TM;
 
-    float acc[4][EJ];
+    float acc[TTOK][EJ];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TTOK; ++i)
 #pragma unroll
         for (int j = 0; j < EJ; ++j) acc[i][j] = 0.f;
 
-    for (int k0 = 0; k0 < d; k0 += kKC) {
-        // x chunk: 64 tokens x 32 columns of bf16, 8 columns (16 bytes) per thread
-        {
-            const int tok = tid / 4, part = tid % 4;
-            const int64_t t = t0 + tok;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < T) v = *reinterpret_cast<const uint4*>(x + t * d + k0 + part * 8);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 xr[XL];
+    float4 wr[WL];
+    auto fetch = [&](int k0) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                xs[part * 8 + 2 * q][tok] = bf16_lo(w[q]);
-                xs[part * 8 + 2 * q + 1][tok] = bf16_hi(w[q]);
-            }
+        for (int q = 0; q < XL; ++q) {
+            const int i = tid + q * kThreads;
+            const int tok = i / (kKC / 8), part = i % (kKC / 8);
+            xr[q] = make_uint4(0, 0, 0, 0);
+            if (i < XV && t0 + tok < T)
+                xr[q] = __ldg(reinterpret_cast<const uint4*>(x + (t0 + tok) * d + k0 + part * 8));
         }
-        // W_r chunk: EP experts x 32 columns of fp32
-        for (int i = tid; i < EP * (kKC / 4); i += kThreads) {
+#pragma unroll
+        for (int q = 0; q < WL; ++q) {
+            const int i = tid + q * kThreads;
             const int e = i / (kKC / 4), part = i % (kKC / 4);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < E) v = *reinterpret_cast<const float4*>(W_r + (int64_t)e * d + k0 + part * 4);
-            wsm[part * 4 + 0][e] = v.x;
-            wsm[part * 4 + 1][e] = v.y;
-            wsm[part * 4 + 2][e] = v.z;
-            wsm[part * 4 + 3][e] = v.w;
+            wr[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < WV && e < E)
+                wr[q] = __ldg(reinterpret_cast<const float4*>(W_r + (int64_t)e * d + k0 + part * 4));
         }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < kKC; ++kk) {
-            const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
-            float wv[EJ];
+    };
+    fetch(0);
+    for (int k0 = 0; k0 < d; k0 += kKC) {
+        __syncthreads();  // the previous chunk's readers are done
 #pragma unroll
-            for (int j = 0; j < EJ; ++j) wv[j] = wsm[kk][tx * EJ + j];
+        for (int q = 0; q < XL; ++q) {
+            const int i = tid + q * kThreads;
+            if (i < XV) {
+                const int tok = i / (kKC / 8), part = i % (kKC / 8);
+                const uint32_t w[4] = {xr[q].x, xr[q].y, xr[q].z, xr[q].w};
 #pragma unroll
-            for (int j = 0; j < EJ; ++j) {
-                acc[0][j] = fmaf(xv.x, wv[j], acc[0][j]);
-                acc[1][j] = fmaf(xv.y, wv[j], acc[1][j]);
-                acc[2][j] = fmaf(xv.z, wv[j], acc[2][j]);
-                acc[3][j] = fmaf(xv.w, wv[j], acc[3][j]);
+                for (int h = 0; h < 4; ++h) {
+                    xs[part * 8 + 2 * h][tok] = bf16_lo(w[h]);
+                    xs[part * 8 + 2 * h + 1][tok] = bf16_hi(w[h]);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < WL; ++q) {
+            const int i = tid + q * kThreads;
+            if (i < WV) {
+                const int e = i / (kKC / 4), part = i % (kKC / 4);
+                wsm[part * 4 + 0][e] = wr[q].x;
+                wsm[part * 4 + 1][e] = wr[q].y;
+                wsm[part * 4 + 2][e] = wr[q].z;
+                wsm[part * 4 + 3][e] = wr[q].w;
             }
         }
         __syncthreads();
+        if (k0 + kKC < d) fetch(k0 + kKC);  // in flight while this chunk is multiplied
+#pragma unroll 4
+        for (int kk = 0; kk < kKC; ++kk) {
+            float xv[TTOK], wv[EJ];
+#pragma unroll
+            for (int i = 0; i < TTOK; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(&xs[kk][ty * TTOK + i]);
+                xv[i] = v.x;
+                xv[i + 1] = v.y;
+                xv[i + 2] = v.z;
+                xv[i + 3] = v.w;
+            }
+            if constexpr (EJ == 2) {
+                const float2 v = *reinterpret_cast<const float2*>(&wsm[kk][tx * EJ]);
+                wv[0] = v.x;
+                wv[1] = v.y;
+            } else {
+#pragma unroll
+                for (int j = 0; j < EJ; j += 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(&wsm[kk][tx * EJ + j]);
+                    wv[j] = v.x;
+                    wv[j + 1] = v.y;
+                    wv[j + 2] = v.z;
+                    wv[j + 3] = v.w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < TTOK; ++i)
+#pragma unroll
+                for (int j = 0; j < EJ; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        }
     }
+    __syncthreads();  // staging tiles are dead; reuse the space for the logit tile
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TTOK; ++i)
 #pragma unroll
-        for (int j = 0; j < EJ; ++j) lg[ty * 4 + i][tx * EJ + j] = acc[i][j];
+        for (int j = 0; j < EJ; ++j) lg[ty * TTOK + i][tx * EJ + j] = acc[i][j];
     __syncthreads();
 
     if (logits) {
-        for (int i = tid; i < kTM * E; i += kThreads) {
+        for (int i = tid; i < TM * E; i += kThreads) {
             const int r = i / E, e = i % E;
             if (t0 + r < T) logits[(t0 + r) * E + e] = lg[r][e];
         }
@@ -112,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) route_fwd_kernel(
     const int warp = tid / 32, lane = tid % 32;
     constexpr int VJ = (EP + 31) / 32;
     double zsum = 0.0;
-    for (int r = warp; r < kTM; r += kThreads / 32) {
+    for (int r = warp; r < TM; r += kThreads / 32) {
         const int64_t t = t0 + r;
         if (t >= T) break;
         float val[VJ];
@@ -263,7 +311,8 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
 }
 
 // dW_r partial sums: part[s][e][j] = sum over tokens of split s of dlogits[t][e] * x[t][j].
-// CTA tile: 64 experts x 128 columns; 256 threads, each 8 experts x 4 columns.
+// CTA tile: 64 experts x 128 columns; 256 threads, each 8 experts x 4 columns, summing over
+// the split's tokens in order. The next 32-token chunk is prefetched into registers.
 constexpr int kBwTE = 64, kBwTJ = 128, kBwTK = 32;
 
 __global__ void __launch_bounds__(256) route_bwd_dwr_kernel(
@@ -282,39 +331,60 @@ __global__ void __launch_bounds__(256) route_bwd_dwr_kernel(
     for (int a = 0; a < 8; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-    for (int64_t tc = tbeg; tc < tend; tc += kBwTK) {
-        // x chunk: 32 tokens x 128 columns bf16 = 32 x 16 uint4
-        for (int i = tid; i < kBwTK * (kBwTJ / 8); i += 256) {
-            const int r = i / (kBwTJ / 8), c = i % (kBwTJ / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (tc + r < tend) v = *reinterpret_cast<const uint4*>(x + (tc + r) * d + j0 + c * 8);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // per chunk: x 32 x 128 bf16 = 512 uint4, dlogits 32 x 64 fp32 = 2048 floats
+    uint4 xr[2];
+    float dr[8];
+    auto fetch = [&](int64_t tc) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                xs[r][c * 8 + 2 * q] = bf16_lo(w[q]);
-                xs[r][c * 8 + 2 * q + 1] = bf16_hi(w[q]);
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + q * 256;
+            const int r = i / (kBwTJ / 8), c = i % (kBwTJ / 8);
+            xr[q] = make_uint4(0, 0, 0, 0);
+            if (tc + r < tend) xr[q] = __ldg(reinterpret_cast<const uint4*>(x + (tc + r) * d + j0 + c * 8));
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = tid + q * 256;
+            const int r = i / kBwTE, e = i % kBwTE;
+            dr[q] = 0.f;
+            if (tc + r < tend && e0 + e < E) dr[q] = __ldg(dlogits + (tc + r) * E + e0 + e);
+        }
+    };
+    fetch(tbeg);
+    for (int64_t tc = tbeg; tc < tend; tc += kBwTK) {
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + q * 256;
+            const int r = i / (kBwTJ / 8), c = i % (kBwTJ / 8);
+            const uint32_t w[4] = {xr[q].x, xr[q].y, xr[q].z, xr[q].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                xs[r][c * 8 + 2 * h] = bf16_lo(w[h]);
+                xs[r][c * 8 + 2 * h + 1] = bf16_hi(w[h]);
             }
         }
-        for (int i = tid; i < kBwTK * kBwTE; i += 256) {
-            const int r = i / kBwTE, e = i % kBwTE;
-            float v = 0.f;
-            if (tc + r < tend && e0 + e < E) v = dlogits[(tc + r) * E + e0 + e];
-            ds[r][e] = v;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = tid + q * 256;
+            ds[i / kBwTE][i % kBwTE] = dr[q];
         }
         __syncthreads();
+        if (tc + kBwTK < tend) fetch(tc + kBwTK);
 #pragma unroll 4
         for (int r = 0; r < kBwTK; ++r) {
             const float4 xv = *reinterpret_cast<const float4*>(&xs[r][tx * 4]);
+            const float4 d0 = *reinterpret_cast<const float4*>(&ds[r][ty * 8]);
+            const float4 d1 = *reinterpret_cast<const float4*>(&ds[r][ty * 8 + 4]);
+            const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
             for (int a = 0; a < 8; ++a) {
-                const float dv = ds[r][ty * 8 + a];
-                acc[a][0] = fmaf(dv, xv.x, acc[a][0]);
-                acc[a][1] = fmaf(dv, xv.y, acc[a][1]);
-                acc[a][2] = fmaf(dv, xv.z, acc[a][2]);
-                acc[a][3] = fmaf(dv, xv.w, acc[a][3]);
+                acc[a][0] = fmaf(dv[a], xv.x, acc[a][0]);
+                acc[a][1] = fmaf(dv[a], xv.y, acc[a][1]);
+                acc[a][2] = fmaf(dv[a], xv.z, acc[a][2]);
+                acc[a][3] = fmaf(dv[a], xv.w, acc[a][3]);
             }
         }
-        __syncthreads();
     }
     float* out = part + (size_t)blockIdx.z * E * d;
 #pragma unroll
@@ -335,21 +405,22 @@ __global__ void route_bwd_reduce_kernel(const float* __restrict__ part, int64_t 
     dW_r[i] = s;
 }
 
-template <int EJ>
+template <int EP, int TM, int TTOK, int EJ>
 int launch_route_fwd(const moe_bf16* x, const float* W_r, const float* b, int64_t T, int d,
                      int E, int k, int mode, float* logits, int32_t* idx, float* gate,
-                     float* score, float* lse, double* zp, cudaStream_t st) {
-    const int64_t nb = route_blocks(T);
-    constexpr int EP = 16 * EJ;
-    const size_t stage = sizeof(float) * kKC * (kTM + EP);
-    const size_t tile = sizeof(float) * kTM * (EP + 1);
+                     float* score, float* lse, double* zp, int64_t* nblocks, cudaStream_t st) {
+    const int64_t nb = cdiv(T, TM);
+    *nblocks = nb;
+    const size_t stage = sizeof(float) * kKC * (TM + EP);
+    const size_t tile = sizeof(float) * TM * (EP + 1);
     const size_t smem = stage > tile ? stage : tile;
-    if (cudaFuncSetAttribute(route_fwd_kernel<EJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    auto kern = route_fwd_kernel<EP, TM, TTOK, EJ>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
         return MOE_ERR_LAUNCH;
-    route_fwd_kernel<EJ><<<(unsigned)nb, kThreads, smem, st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(x), W_r, b, T, d, E, k, mode, logits, idx, gate,
-        score, lse, zp);
+    kern<<<(unsigned)nb, kThreads, smem, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), W_r, b,
+                                               T, d, E, k, mode, logits, idx, gate, score, lse,
+                                               zp);
     return launch_status();
 }
 
@@ -375,14 +446,17 @@ extern "C" int moe_route(const moe_bf16* x, const float* W_r, const float* b, in
     if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     int rc;
-    if (E <= 16) rc = launch_route_fwd<1>(x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, st);
-    else if (E <= 32) rc = launch_route_fwd<2>(x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, st);
-    else if (E <= 64) rc = launch_route_fwd<4>(x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, st);
-    else if (E <= 128) rc = launch_route_fwd<8>(x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, st);
-    else rc = launch_route_fwd<16>(x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, st);
+    int64_t nb = 0;
+#define MOE_ROUTE_ARGS x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, &nb, st
+    if (E <= 16) rc = launch_route_fwd<16, 128, 4, 2>(MOE_ROUTE_ARGS);
+    else if (E <= 32) rc = launch_route_fwd<32, 128, 4, 4>(MOE_ROUTE_ARGS);
+    else if (E <= 64) rc = launch_route_fwd<64, 128, 8, 4>(MOE_ROUTE_ARGS);
+    else if (E <= 128) rc = launch_route_fwd<128, 128, 8, 8>(MOE_ROUTE_ARGS);
+    else rc = launch_route_fwd<256, 64, 8, 8>(MOE_ROUTE_ARGS);
+#undef MOE_ROUTE_ARGS
     if (rc != MOE_OK) return rc;
     if (mode == MOE_MODE_SOFTMAX) {
-        z_finalize_kernel<<<1, 32, 0, st>>>(zp, route_blocks(T), T, z_coef, z_loss);
+        z_finalize_kernel<<<1, 32, 0, st>>>(zp, nb, T, z_coef, z_loss);
         rc = launch_status();
     }
     return rc;

@@ -166,8 +166,11 @@ class MoEPlan:
         ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx, stream)
         return self.dx
 
-    def bias_update(self, b, gamma, stream=None):
-        ops.moe_bias_update(self.counts, self.s.T, self.s.k, gamma, b, stream)
+    def bias_update(self, b, gamma, rule="sign", stream=None):
+        if rule == "proportional":
+            ops.moe_bias_update_proportional(self.counts, self.s.T, self.s.k, gamma, b, stream)
+        else:
+            ops.moe_bias_update(self.counts, self.s.T, self.s.k, gamma, b, stream)
 
     def grads(self) -> dict:
         g = {"dx": self.dx, "dW_r": self.dW_r, "dW_g": self.dW_g, "dW_u": self.dW_u,

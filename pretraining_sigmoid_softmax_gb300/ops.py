@@ -128,6 +128,14 @@ def moe_bias_update(counts, T, k, gamma, b, stream=None):
            "moe_bias_update")
 
 
+def moe_bias_update_proportional(counts, T, k, gamma, b, stream=None):
+    E = counts.shape[0]
+    _contig(counts, b)
+    _check(_lib.load().moe_bias_update_proportional(_p(counts), E, T, k, float(gamma), _p(b),
+                                                    _stream(stream)),
+           "moe_bias_update_proportional")
+
+
 def moe_combine_bwd(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm, dg,
                     stream=None):
     T, k = topk_gate.shape

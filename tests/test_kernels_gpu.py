@@ -345,3 +345,16 @@ def test_bias_update_is_bit_exact():
     ops.moe_bias_update(dev(counts), T, k, 0.001, bd)
     ref = O.bias_update(counts.numpy(), b.numpy(), T, k, 0.001)
     assert np.array_equal(bd.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_proportional_bias_update_is_bit_exact():
+    g = torch.Generator().manual_seed(43)
+    E, T, k = 64, 49152, 4
+    counts = torch.multinomial(torch.ones(E), T * k, replacement=True, generator=g).bincount(minlength=E)
+    counts[5] = T * k // E
+    counts = counts.to(torch.int32)
+    b = torch.rand(E, generator=g) * 0.1 - 0.05
+    bd = dev(b)
+    ops.moe_bias_update_proportional(dev(counts), T, k, 0.01, bd)
+    ref = O.bias_update_proportional(counts.numpy(), b.numpy(), T, k, 0.01)
+    assert np.array_equal(bd.cpu().numpy().view(np.uint32), ref.view(np.uint32))

@@ -36,6 +36,10 @@ class Lazy:
 WEIGHTS = ("W_g", "W_u", "W_d")  # converted to fp64 slice by slice
 
 
+def oracle_bias(cfg):
+    return O.bias_update_proportional if cfg.bias_rule == "proportional" else O.bias_update
+
+
 def run_gpu(cfg: MoEConfig, inp: dict):
     plan = MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)
     d = {k: v.cuda() for k, v in inp.items()}
@@ -47,7 +51,7 @@ def run_gpu(cfg: MoEConfig, inp: dict):
         plan.backward(d["dY"])
         if cfg.bias_update:
             b_new = d["b"].clone()
-            plan.bias_update(b_new, cfg.gamma)
+            plan.bias_update(b_new, cfg.gamma, cfg.bias_rule)
     torch.cuda.synchronize()
     assert ops.moe_device_status()[0] == 0
     return plan, b_new
@@ -97,7 +101,7 @@ def full_parity(cfg, inp):
         for name in ("dWs_g", "dWs_u", "dWs_d"):
             assert_close(getattr(plan, name), bwd[name], name, reduction=True)
     if cfg.bias_update:
-        ref = O.bias_update(D["counts"], inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
+        ref = oracle_bias(cfg)(D["counts"], inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
@@ -146,7 +150,7 @@ def test_layer_is_bitwise_repeatable():
         assert torch.equal(r1[k], v), k
 
 
-@pytest.mark.parametrize("name", ["C2", "C3", "C4"])
+@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5"])
 def test_workload_sampled_parity(name):
     """Full-size workloads in the benchmark's launch configuration: routing, counts and
     permutation in full; out and dx on sampled tokens; weight-gradient entries of sampled
@@ -209,7 +213,7 @@ def test_workload_sampled_parity(name):
         assert_close(np.array([float(plan.dWs_u[j, i]) for (j, i) in eg]), want["dWs_u"], "dWs_u",
                      reduction=True)
     if cfg.bias_update:
-        refb = O.bias_update(counts, inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
+        refb = oracle_bias(cfg)(counts, inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), refb.view(np.uint32))
     del dY64
 

@@ -365,3 +365,23 @@ def test_bf16_mode_stays_close_to_the_exact_definition():
     # the stored tensors are bf16 values
     for name in ("A", "U", "H", "Y_perm", "out"):
         np.testing.assert_array_equal(O.bf16_round(b16[name]), b16[name])
+
+
+def test_proportional_bias_update_invariants():
+    """Reading of the proportional rule: the step is gamma times the relative deviation of
+    the load from the mean, toward the mean; a balanced expert does not move."""
+    rng = np.random.default_rng(17)
+    E, T, k, gamma = 64, 49152, 4, 0.01
+    b = rng.uniform(-0.05, 0.05, E).astype(np.float32)
+    counts = rng.multinomial(T * k, np.ones(E) / E)
+    counts[7] = T * k // E
+    nb = O.bias_update_proportional(counts, b, T, k, gamma)
+    mean = T * k / E
+    exact_step = gamma * (mean - counts) / mean
+    delta = nb.astype(np.float64) - b.astype(np.float64)
+    assert delta[7] == 0.0
+    # one fp32 rounding of the ratio, the product and the sum: within a few fp32 ulps of b
+    ulp32 = np.spacing((np.abs(b) + np.abs(exact_step)).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(delta - exact_step) <= 4 * ulp32)
+    moved = counts != mean
+    assert np.all(np.sign(delta[moved]) == np.sign(mean - counts[moved]))
