@@ -19,6 +19,12 @@
 //   warp 2  allocates / frees tensor memory (two accumulators, double-buffered);
 //   warps 4-7 epilogue: tcgen05.ld of TMEM lanes 0-127 (one output row per thread), the
 //            fused elementwise step, bf16 stores.
+// Pair mode (a cluster of two CTAs on two SMs): the leading CTA issues
+// tcgen05.mma.cta_group::2 over a 256-row tile; each CTA stages its own 128 rows of A and
+// half of the tile's B columns, so per SM the shared-memory operand traffic and the TMA
+// bytes per FLOP drop by a third compared with a 128 x 256 tile on one SM. Both CTAs' TMA
+// loads complete on the leader's "full" barriers, the leader's commits arrive on both
+// CTAs' barriers (multicast), and both epilogues release the accumulator to the leader.
 // Operand tiles use the 128-byte swizzle. K-major tiles are TMA boxes of 64 K-elements x
 // rows; MN-major tiles are boxes of 64 MN-elements x 64 k-rows. Every wait on an mbarrier
 // is bounded in time; a wait that runs out records MOE_ERR_TIMEOUT, stops every role of
@@ -42,29 +48,36 @@ constexpr int kSmemBudget = 200 * 1024;
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
 
-template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_>
+template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
+          bool PAIR_ = false>
 struct Cfg {
-    static constexpr int BN = BN_;
+    static constexpr int BN = BN_;           // output columns per tile (per B matrix if DUAL)
     static constexpr bool A_MN = A_MN_;
     static constexpr bool B_MN = B_MN_;
-    static constexpr bool DUAL = DUAL_;      // two B operands -> two accumulators (G1)
+    static constexpr bool DUAL = DUAL_;      // two B operands -> gate and up accumulators (G1)
     static constexpr int EPI = EPI_;
     static constexpr bool TWO_K = TWO_K_;    // K = [K0 from (a0,b0)] ++ [K1 from (a1,b1)]
     static constexpr bool WGRAD = WGRAD_;    // M = weight rows, K = expert's token rows
+    static constexpr bool PAIR = PAIR_;      // CTA pair: 256-row tiles, B split between CTAs
+    static constexpr int MMA_N = DUAL ? 2 * BN : BN;         // accumulator columns per row
+    static constexpr int BROWS = PAIR ? MMA_N / 2 : MMA_N;   // B rows staged by this CTA
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;        // rows of one (pair) tile
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2 * (DUAL ? 2 : 1);
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int B_BYTES = BROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // this CTA's bytes per K block
     static constexpr int STAGES = (kSmemBudget / STAGE_BYTES) > 6 ? 6 : (kSmemBudget / STAGE_BYTES);
-    static constexpr int ACC_COLS = DUAL ? 2 * BN : BN;
+    static constexpr int ACC_COLS = MMA_N;
     static constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulator buffers
-    // DUAL: the W_g and W_u boxes sit back to back in shared memory as one 2*BN-row B tile,
-    // so a single N = 2*BN instruction fills gate columns [0, BN) and up columns [BN, 2BN).
-    static constexpr uint32_t IDESC = idesc_bf16_m128(DUAL ? 2 * BN : BN, A_MN, B_MN);
+    // DUAL: the W_g and W_u boxes form one 2*BN-row B tile (on one CTA, back to back; in a
+    // pair, W_g on the leader and W_u on the peer), so one instruction fills gate columns
+    // [0, BN) and up columns [BN, 2BN).
+    static constexpr uint32_t IDESC = idesc_bf16(MMA_N, TILE_M, A_MN, B_MN);
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory columns");
-    static_assert(BN % 64 == 0 && (DUAL ? 2 * BN : BN) <= 256, "tile width");
-    static constexpr size_t SMEM_BYTES =
-        1024 + (size_t)STAGES * STAGE_BYTES + 1024 /* barriers etc. */ +
-        sizeof(int64_t) * (kMaxExperts + 1) + sizeof(int32_t) * kMaxExperts;
+    static_assert(BN % 64 == 0 && MMA_N <= 256 && BROWS % 64 == 0, "tile width");
+    static constexpr size_t MISC_BYTES = 512 + sizeof(int64_t) * (kMaxExperts + 1) +
+                                         sizeof(int32_t) * kMaxExperts +
+                                         sizeof(int32_t) * (kMaxExperts + 1);
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + MISC_BYTES;
 };
 
 struct Params {
@@ -95,6 +108,7 @@ struct TileInfo {
     int n0;      // first output column
     int64_t k_lo;  // weight gradients: first token row of the expert
     int k_iters;   // 64-wide K blocks
+    int64_t row_end;  // token-major: rows at or past this are not stored
 };
 
 struct SmemLayout {
@@ -108,6 +122,7 @@ struct SmemLayout {
     int* abort_flag;
     int64_t* offs;     // E + 1
     int32_t* order;    // E
+    int32_t* ptp;      // E + 1: exclusive prefix of pair tiles per expert (pair, token-major)
 };
 
 template <class C>
@@ -125,6 +140,7 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
     s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
     s.offs = reinterpret_cast<int64_t*>(misc + 512);
     s.order = reinterpret_cast<int32_t*>(s.offs + kMaxExperts + 1);
+    s.ptp = s.order + kMaxExperts;
     return s;
 }
 
@@ -134,26 +150,45 @@ template <class C>
 __device__ __forceinline__ int64_t total_tiles(const Params& P, const SmemLayout& S) {
     const int n_tiles = P.N / C::BN;
     if constexpr (C::WGRAD) {
-        return (int64_t)P.E * P.nprob * (P.M_out / BM) * n_tiles;
+        return (int64_t)P.E * P.nprob * (P.M_out / C::TILE_M) * n_tiles;
     } else {
-        const int64_t mt = P.row_offsets ? S.offs[P.E] / BM : cdiv_dev(P.rows, BM);
+        int64_t mt;
+        if (!P.row_offsets) mt = cdiv_dev(P.rows, C::TILE_M);
+        else if (C::PAIR) mt = S.ptp[P.E];
+        else mt = S.offs[P.E] / BM;
         return mt * n_tiles;
     }
 }
 
+// Last expert e in [0, E) with key[e] <= v (key non-decreasing). Among equal keys (empty
+// experts) the last one is the expert that owns the rows.
+template <class K>
+__device__ __forceinline__ int last_le(const K* key, int E, int64_t v) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)key[mid] <= v) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Tile `tile` as seen by CTA `rank` of its pair (rank 0 outside pair mode).
 template <class C>
-__device__ __forceinline__ TileInfo decode(int64_t tile, const Params& P, const SmemLayout& S) {
+__device__ __forceinline__ TileInfo decode(int64_t tile, const Params& P, const SmemLayout& S,
+                                           uint32_t rank) {
     TileInfo ti;
     const int n_tiles = P.N / C::BN;
+    const int64_t half = C::PAIR ? (int64_t)rank * BM : 0;
     if constexpr (C::WGRAD) {
-        const int m_tiles = P.M_out / BM;
+        const int m_tiles = P.M_out / C::TILE_M;
         const int64_t per_e = (int64_t)P.nprob * m_tiles * n_tiles;
         const int oi = (int)(tile / per_e);
         int64_t rem = tile % per_e;
         ti.e = S.order[oi];
         ti.p = (int)(rem / (m_tiles * n_tiles));
         rem %= (m_tiles * n_tiles);
-        ti.m0 = (rem / n_tiles) * BM;
+        ti.m0 = (rem / n_tiles) * C::TILE_M + half;
         ti.n0 = (int)(rem % n_tiles) * C::BN;
         int64_t lo = 0, hi = P.rows;
         if (P.row_offsets) {
@@ -162,43 +197,57 @@ __device__ __forceinline__ TileInfo decode(int64_t tile, const Params& P, const 
         }
         ti.k_lo = lo;
         ti.k_iters = (int)cdiv_dev(hi - lo, BK);
+        ti.row_end = P.M_out;
     } else {
         const int64_t mt = tile / n_tiles;
         ti.n0 = (int)(tile % n_tiles) * C::BN;
-        ti.m0 = mt * BM;
         ti.p = 0;
         ti.k_lo = 0;
-        int e = 0;
-        if (P.row_offsets) {  // last expert whose segment starts at or before m0
-            int lo = 0, hi = P.E - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (S.offs[mid] <= ti.m0) lo = mid;
-                else hi = mid - 1;
-            }
-            e = lo;  // among equal offsets (empty experts) the last one owns the rows
+        ti.e = 0;
+        if (!P.row_offsets) {
+            ti.m0 = mt * C::TILE_M + half;
+            ti.row_end = P.rows;
+        } else if constexpr (C::PAIR) {
+            // pair tiles of expert e cover its padded segment 256 rows at a time; the
+            // second half of a segment's last pair tile may lie past the segment
+            ti.e = last_le(S.ptp, P.E, mt);
+            ti.m0 = S.offs[ti.e] + (mt - S.ptp[ti.e]) * C::TILE_M + half;
+            ti.row_end = S.offs[ti.e + 1];
+        } else {
+            ti.m0 = mt * BM;
+            ti.e = last_le(S.offs, P.E, ti.m0);
+            ti.row_end = S.offs[ti.e + 1];
         }
-        ti.e = e;
         ti.k_iters = (P.K0 + (C::TWO_K ? P.K1 : 0)) / BK;
     }
     return ti;
 }
 
-// Loads of K block `kb` of a tile into stage buffers.
+template <class C>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                         int32_t c0, int32_t c1) {
+    if constexpr (C::PAIR) tma_load_2d_pair(dst, map, bar, c0, c1);
+    else tma_load_2d(dst, map, bar, c0, c1);
+}
+
+// Loads of K block `kb` of a tile into this CTA's stage buffers; `bar` is the barrier the
+// copies complete on (in pair mode the leader's, as a shared::cluster address).
 template <class C>
 __device__ __forceinline__ void issue_loads(const TileInfo& ti, int kb, uint32_t a_dst,
                                             uint32_t b_dst, uint32_t bar, const Params& P,
                                             const CUtensorMap* ma0, const CUtensorMap* ma1,
-                                            const CUtensorMap* mb0, const CUtensorMap* mb1) {
+                                            const CUtensorMap* mb0, const CUtensorMap* mb1,
+                                            uint32_t rank) {
+    const int32_t bhalf = C::PAIR ? (int32_t)rank * C::BROWS : 0;  // this CTA's B columns
     if constexpr (C::WGRAD) {
         const int32_t krow = (int32_t)(ti.k_lo + (int64_t)kb * BK);
         const CUtensorMap* ma = ti.p == 0 ? ma0 : ma1;
         // A: MN-major, two 64-wide boxes along M
-        tma_load_2d(a_dst, ma, bar, (int32_t)ti.m0, krow);
-        tma_load_2d(a_dst + 8192, ma, bar, (int32_t)ti.m0 + 64, krow);
+        tma_load<C>(a_dst, ma, bar, (int32_t)ti.m0, krow);
+        tma_load<C>(a_dst + 8192, ma, bar, (int32_t)ti.m0 + 64, krow);
 #pragma unroll
-        for (int j = 0; j < C::BN / 64; ++j)
-            tma_load_2d(b_dst + j * 8192, mb0, bar, ti.n0 + 64 * j, krow);
+        for (int j = 0; j < C::BROWS / 64; ++j)
+            tma_load<C>(b_dst + j * 8192, mb0, bar, ti.n0 + bhalf + 64 * j, krow);
     } else {
         int kk = kb * BK;
         const CUtensorMap* ma = ma0;
@@ -209,16 +258,22 @@ __device__ __forceinline__ void issue_loads(const TileInfo& ti, int kb, uint32_t
             ma = ma1;
             mb = mb1;
         }
-        tma_load_2d(a_dst, ma, bar, kk, (int32_t)ti.m0);
+        tma_load<C>(a_dst, ma, bar, kk, (int32_t)ti.m0);
         if constexpr (C::B_MN) {
             const int32_t brow = ti.e * kper + kk;
 #pragma unroll
-            for (int j = 0; j < C::BN / 64; ++j)
-                tma_load_2d(b_dst + j * 8192, mb, bar, ti.n0 + 64 * j, brow);
-        } else {
+            for (int j = 0; j < C::BROWS / 64; ++j)
+                tma_load<C>(b_dst + j * 8192, mb, bar, ti.n0 + bhalf + 64 * j, brow);
+        } else if constexpr (C::DUAL) {
             const int32_t brow = ti.e * P.N + ti.n0;
-            tma_load_2d(b_dst, C::DUAL ? mb0 : mb, bar, kk, brow);
-            if constexpr (C::DUAL) tma_load_2d(b_dst + C::BN * 128, mb1, bar, kk, brow);
+            if constexpr (C::PAIR) {
+                tma_load<C>(b_dst, rank == 0 ? mb0 : mb1, bar, kk, brow);
+            } else {
+                tma_load<C>(b_dst, mb0, bar, kk, brow);
+                tma_load<C>(b_dst + C::BN * 128, mb1, bar, kk, brow);
+            }
+        } else {
+            tma_load<C>(b_dst, mb, bar, kk, ti.e * P.N + ti.n0 + bhalf);
         }
     }
 }
@@ -269,7 +324,7 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
         }
     } else {
         const int64_t row = ti.m0 + row_in_tile;
-        const bool ok = row < P.rows;
+        const bool ok = row < ti.row_end;
         const int64_t base = row * (int64_t)P.ld_out + ti.n0;
         for (int c = 0; c < C::BN; c += 32) {
             if constexpr (C::EPI == kEpiSwigluFwd) {
@@ -358,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t gg_smem_raw[];
     const SmemLayout S = carve<C>(gg_smem_raw);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const uint32_t rank = C::PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    // tiles are dealt to CTAs (or to pairs, whose two CTAs take the same tile)
+    const int64_t first_tile = C::PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const int64_t tile_step = C::PAIR ? gridDim.x / 2 : gridDim.x;
 
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -366,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&S.tfull[b]), 1);
-            mbar_init(smem_u32(&S.tempty[b]), 4);
+            mbar_init(smem_u32(&S.tempty[b]), C::PAIR ? 8 : 4);
         }
         *S.abort_flag = 0;
         fence_mbar_init();
@@ -376,18 +436,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C::WGRAD)
         for (int i = tid; i < P.E; i += kThreads) S.order[i] = P.expert_order ? P.expert_order[i] : i;
     if (warp == 2) {
-        tmem_alloc(smem_u32(S.tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (C::PAIR) {
+            tmem_alloc_pair(smem_u32(S.tmem_slot), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(S.tmem_slot), C::TMEM_COLS);
+            tmem_relinquish();
+        }
+    }
+    if constexpr (C::PAIR && !C::WGRAD) {
+        // pair tiles per expert = ceil(128-row tiles / 2); exclusive prefix in S.ptp
+        __syncthreads();
+        if (P.row_offsets) {
+            int v = 0;
+            if (tid < P.E) v = (int)(((S.offs[tid + 1] - S.offs[tid]) / BM + 1) / 2);
+            S.ptp[tid + 1] = v;  // tid < 256 = kMaxExperts
+            if (tid == 0) S.ptp[0] = 0;
+            __syncthreads();
+            for (int off = 1; off < kThreads; off <<= 1) {  // inclusive scan of S.ptp[1..256]
+                int add = 0;
+                if (tid >= off) add = S.ptp[tid + 1 - off];
+                __syncthreads();
+                S.ptp[tid + 1] += add;
+                __syncthreads();
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (C::PAIR) cluster_sync();  // the peer's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_slot;
     volatile int* abort_flag = S.abort_flag;
 
     bool layout_ok = true;
-    if (!C::WGRAD && P.row_offsets && S.offs[P.E] > P.rows) layout_ok = false;
-    if (C::WGRAD && P.row_offsets && S.offs[P.E] > P.rows) layout_ok = false;
+    if (P.row_offsets && S.offs[P.E] > P.rows) layout_ok = false;
     if (!layout_ok && tid == 0) record_error(P.status, MOE_ERR_BAD_INDEX, 20);
     const int64_t ntiles = layout_ok ? total_tiles<C>(P, S) : 0;
 
@@ -399,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (C::TWO_K || C::DUAL) tma_prefetch_desc(&mb1);
         int stage = 0;
         uint32_t phase = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            const TileInfo ti = decode<C>(tile, P, S);
+        for (int64_t tile = first_tile; tile < ntiles; tile += tile_step) {
+            const TileInfo ti = decode<C>(tile, P, S, rank);
             bool ok = true;
             for (int kb = 0; kb < ti.k_iters; ++kb) {
                 if (!mbar_wait_bounded(smem_u32(&S.empty[stage]), phase ^ 1u, abort_flag, P.status,
@@ -409,10 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t full = smem_u32(&S.full[stage]);
-                mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                uint32_t bar = full;
+                if constexpr (C::PAIR) {
+                    bar = mapa_shared(full, 0);  // both CTAs' copies complete on the leader's
+                    if (leader) mbar_arrive_expect_tx(full, 2 * C::STAGE_BYTES);
+                } else {
+                    mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                }
                 issue_loads<C>(ti, kb, smem_u32(S.a + (size_t)stage * C::A_BYTES),
-                               smem_u32(S.b + (size_t)stage * C::B_BYTES), full, P, &ma0, &ma1,
-                               &mb0, &mb1);
+                               smem_u32(S.b + (size_t)stage * C::B_BYTES), bar, P, &ma0, &ma1,
+                               &mb0, &mb1, rank);
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -420,13 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------------ MMA issuer
         int stage = 0;
         uint32_t phase = 0;
         int local = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-            const TileInfo ti = decode<C>(tile, P, S);
+        for (int64_t tile = first_tile; tile < ntiles; tile += tile_step, ++local) {
+            const TileInfo ti = decode<C>(tile, P, S, rank);
             const int buf = local & 1;
             const uint32_t use = (local >> 1) & 1;
             if (!mbar_wait_bounded(smem_u32(&S.tempty[buf]), use ^ 1u, abort_flag, P.status,
@@ -451,30 +540,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bdesc = C::B_MN ? sdesc_sw128(b_s + kk * 2048, 8192, 1024)
                                                    : sdesc_sw128(b_s + kk * 32, 16, 1024);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                    umma_bf16(d_tmem, adesc, bdesc, C::IDESC, acc);
+                    if constexpr (C::PAIR) umma_bf16_pair(d_tmem, adesc, bdesc, C::IDESC, acc);
+                    else umma_bf16(d_tmem, adesc, bdesc, C::IDESC, acc);
                 }
-                umma_commit(smem_u32(&S.empty[stage]));
+                if constexpr (C::PAIR) umma_commit_pair(smem_u32(&S.empty[stage]), 0x3);
+                else umma_commit(smem_u32(&S.empty[stage]));
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            umma_commit(smem_u32(&S.tfull[buf]));
+            if constexpr (C::PAIR) umma_commit_pair(smem_u32(&S.tfull[buf]), 0x3);
+            else umma_commit(smem_u32(&S.tfull[buf]));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         const int row_in_tile = 32 * q + lane;
         int local = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-            const TileInfo ti = decode<C>(tile, P, S);
+        for (int64_t tile = first_tile; tile < ntiles; tile += tile_step, ++local) {
+            const TileInfo ti = decode<C>(tile, P, S, rank);
             const int buf = local & 1;
             const uint32_t ph = (local >> 1) & 1;
             AuChunk pre;
             if constexpr (C::EPI == kEpiSwigluBwd) {  // first chunk's a, u before the wait
                 const int64_t row = ti.m0 + row_in_tile;
-                if (row < P.rows) load_au(pre, P, row * (int64_t)P.ld_out + ti.n0);
+                if (row < ti.row_end) load_au(pre, P, row * (int64_t)P.ld_out + ti.n0);
             }
             bool ok = mbar_wait_bounded(smem_u32(&S.tfull[buf]), ph, abort_flag, P.status,
                                         P.wait_limit_ns, 33);
@@ -485,11 +577,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.tempty[buf]));
+            if (lane == 0) {
+                if constexpr (C::PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+                else mbar_arrive(smem_u32(&S.tempty[buf]));
+            }
         }
     }
     __syncwarp();
     __syncthreads();
+    if constexpr (C::PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
     if (*abort_flag) {  // let copies still in flight land before the CTA exits
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 200000ull) {
@@ -497,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (C::PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -551,22 +648,52 @@ template <class C>
 int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
            const CUtensorMap& b1, const Params& P, int64_t max_tiles, cudaStream_t st) {
     static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = grouped_gemm_kernel<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM_BYTES) != cudaSuccess)
         return MOE_ERR_LAUNCH;
-    int64_t grid = sm_count();
-    if (max_tiles < grid) grid = max_tiles;
-    if (grid < 1) grid = 1;
-    grouped_gemm_kernel<C><<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, P);
-    return launch_status();
+    if constexpr (C::PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2));
+        int clusters = 0;  // pairs that fit on the GPU at once (one CTA per SM)
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+            clusters = sm_count() / 2;
+        int64_t pairs = clusters;
+        if (max_tiles < pairs) pairs = max_tiles;
+        if (pairs < 1) pairs = 1;
+        cfg.gridDim = dim3(2 * (unsigned)pairs);
+        if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, P) != cudaSuccess) return MOE_ERR_LAUNCH;
+        return launch_status();
+    } else {
+        int64_t grid = sm_count();
+        if (max_tiles < grid) grid = max_tiles;
+        if (grid < 1) grid = 1;
+        kern<<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, P);
+        return launch_status();
+    }
 }
 
-// Configurations of the layer's GEMMs.
+// Configurations of the layer's GEMMs (P: CTA-pair versions).
 using CfgG1 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false>;
+using CfgG1P = Cfg<128, false, false, true, kEpiSwigluFwd, false, false, true>;
 template <int BN> using CfgStoreK = Cfg<BN, false, false, false, kEpiStore, false, false>;
+using CfgStoreKP = Cfg<256, false, false, false, kEpiStore, false, false, true>;
 template <int BN> using CfgSwigluBwd = Cfg<BN, false, true, false, kEpiSwigluBwd, false, false>;
+using CfgSwigluBwdP = Cfg<256, false, true, false, kEpiSwigluBwd, false, false, true>;
 template <int BN> using CfgDgrad2 = Cfg<BN, false, true, false, kEpiStore, true, false>;
+using CfgDgrad2P = Cfg<256, false, true, false, kEpiStore, true, false, true>;
 template <int BN> using CfgWgrad = Cfg<BN, true, true, false, kEpiStore, false, true>;
+using CfgWgradP = Cfg<256, true, true, false, kEpiStore, false, true, true>;
 
 Params base_params(const int64_t* row_offsets, int64_t rows, int E) {
     Params P{};
@@ -614,7 +741,7 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
     P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
     P.ld_out = f;
-    int rc = launch<CfgG1>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st);
+    int rc = launch<CfgG1P>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st);
     if (rc != MOE_OK) return rc;
     // G2: y = h W_d^T
     Params Q = base_params(row_offsets, rows, E);
@@ -622,9 +749,9 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     Q.K0 = f;
     Q.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
     Q.ld_out = d;
-    if (d % 256 == 0) {
-        if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 256)) return MOE_ERR_LAUNCH;
-        rc = launch<CfgStoreK<256>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st);
+    if (d % 256 == 0) {  // CTA pair: each CTA stages 128 of the tile's 256 W_d rows
+        if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
+        rc = launch<CfgStoreKP>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st);
     } else {
         if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
         rc = launch<CfgStoreK<128>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st);
@@ -671,7 +798,7 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.in1 = Ub;
         P.ld_out = f;
         if (f % 256 == 0)
-            rc = launch<CfgSwigluBwd<256>>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 256), st);
+            rc = launch<CfgSwigluBwdP>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 256), st);
         else
             rc = launch<CfgSwigluBwd<128>>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 128), st);
         if (rc != MOE_OK) return rc;
@@ -691,7 +818,7 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
         P.ld_out = d;
         if (d % 256 == 0)
-            rc = launch<CfgDgrad2<256>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 256), st);
+            rc = launch<CfgDgrad2P>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 256), st);
         else
             rc = launch<CfgDgrad2<128>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 128), st);
         if (rc != MOE_OK) return rc;
@@ -712,7 +839,9 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.M_out = d;
         P.nprob = 1;
         P.out0 = reinterpret_cast<__nv_bfloat16*>(dW_d);
-        if (f % 256 == 0)
+        if (d % 256 == 0 && f % 256 == 0)
+            rc = launch<CfgWgradP>(mdy, mdy, mh, mh, P, (int64_t)E * (d / 256) * (f / 256), st);
+        else if (f % 256 == 0)
             rc = launch<CfgWgrad<256>>(mdy, mdy, mh, mh, P, (int64_t)E * (d / BM) * (f / 256), st);
         else
             rc = launch<CfgWgrad<128>>(mdy, mdy, mh, mh, P, (int64_t)E * (d / BM) * (f / 128), st);
@@ -731,7 +860,9 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.nprob = 2;
         P.out0 = reinterpret_cast<__nv_bfloat16*>(dW_g);
         P.out1 = reinterpret_cast<__nv_bfloat16*>(dW_u);
-        if (d % 256 == 0)
+        if (d % 256 == 0 && f % 256 == 0)
+            rc = launch<CfgWgradP>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / 256) * (d / 256), st);
+        else if (d % 256 == 0)
             rc = launch<CfgWgrad<256>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 256), st);
         else
             rc = launch<CfgWgrad<128>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 128), st);

@@ -224,7 +224,7 @@ def _check_expert(B, e, lo, hi, X, dY, W_g, W_u, W_d, tag):
 
 
 @pytest.mark.parametrize("rows,d,f", [(200, 256, 128), (128, 384, 256), (77, 128, 128),
-                                      (640, 512, 384)])
+                                      (640, 512, 384), (1000, 512, 512)])
 def test_dense_expert_gemms(rows, d, f):
     """One expert over all rows (the shared-expert path): ragged M tail, both tile widths."""
     g = torch.Generator().manual_seed(rows + d + f)
@@ -237,7 +237,8 @@ def test_dense_expert_gemms(rows, d, f):
 
 @pytest.mark.parametrize("counts,d,f", [([130, 0, 5, 256, 1], 256, 128),
                                         ([0, 300, 0], 256, 256),
-                                        ([128, 129, 127, 0, 0, 1], 384, 128)])
+                                        ([128, 129, 127, 0, 0, 1], 384, 128),
+                                        ([300, 0, 129, 1, 513, 256], 512, 256)])
 def test_routed_expert_gemms(counts, d, f):
     """Padded expert segments with empty experts and 1-row / 127 / 128 / 129-row segments."""
     E = len(counts)
