@@ -25,6 +25,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 peak"
+# DRAM bytes (read + write) of one step's grouped-GEMM launches from an ncu capture of the
+# current kernels (profiles/grouped_gemm_dram_C4_large.md); workloads without a capture
+# report null.
+MEASURED_GEMM_TRAFFIC = {"C4": 115.11e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -236,29 +240,66 @@ def main():
     # ------------------------------------------------------------ end to end, host buffers
     e2e = None
     if not args.no_e2e:
+        # Pipelined like a training loop: step i+1's inputs are uploaded on a copy stream
+        # while step i computes, and step i's out/dx are read back while step i+1 computes.
+        # Two sets of activation buffers (plans) alternate so a readback never races the
+        # next step's writes. Every step's copies are inside the timed region.
+        plans = [plan, MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)]
         hx = inp["x"].pin_memory()
         hdy = inp["dY"].pin_memory() if cfg.backward else None
-        hout = torch.empty_like(inp["x"]).pin_memory()
-        hdx = torch.empty_like(inp["x"]).pin_memory() if cfg.backward else None
-        xd = torch.empty_like(dev["x"])
-        dyd = torch.empty_like(dev["dY"]) if cfg.backward else None
+        hout = [torch.empty_like(inp["x"]).pin_memory() for _ in range(2)]
+        hdx = [torch.empty_like(inp["x"]).pin_memory() for _ in range(2)] if cfg.backward else None
+        xd = [torch.empty_like(dev["x"]) for _ in range(2)]
+        dyd = [torch.empty_like(dev["dY"]) for _ in range(2)] if cfg.backward else None
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        read_back = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]  # inputs of a slot consumed
 
-        def e2e_step():
-            xd.copy_(hx, non_blocking=True)
-            if cfg.backward:
-                dyd.copy_(hdy, non_blocking=True)
-            step(xd, dyd)
-            hout.copy_(plan.out, non_blocking=True)
-            if cfg.backward:
-                hdx.copy_(plan.dx, non_blocking=True)
+        def upload(i):
+            j = i % 2
+            up.wait_event(freed[j])
+            with torch.cuda.stream(up):
+                xd[j].copy_(hx, non_blocking=True)
+                if cfg.backward:
+                    dyd[j].copy_(hdy, non_blocking=True)
+                uploaded[j].record(up)
 
-        for _ in range(2):
-            e2e_step()
+        def run_steps(n):
+            for j in range(2):  # nothing pending on either slot
+                freed[j].record(stream)
+                read_back[j].record(stream)
+            upload(0)
+            for i in range(n):
+                j = i % 2
+                if i + 1 < n:
+                    upload(i + 1)
+                stream.wait_event(uploaded[j])
+                stream.wait_event(read_back[j])  # slot j's previous outputs are on the host
+                p = plans[j]
+                p.forward(xd[j], dev["W_r"], b_work, dev["W_g"], dev["W_u"], dev["W_d"],
+                          dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"))
+                if cfg.backward:
+                    p.backward(dyd[j])
+                    if cfg.bias_update:
+                        p.bias_update(b_work, cfg.gamma, cfg.bias_rule)
+                freed[j].record(stream)
+                computed[j].record(stream)
+                down.wait_event(computed[j])
+                with torch.cuda.stream(down):
+                    hout[j].copy_(p.out, non_blocking=True)
+                    if cfg.backward:
+                        hdx[j].copy_(p.dx, non_blocking=True)
+                    read_back[j].record(down)
+            stream.wait_event(read_back[0])
+            stream.wait_event(read_back[1])
+
+        run_steps(2)
         sync_all()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        run_steps(args.steps)
         b.record(stream)
         sync_all()
         te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device="cuda")
@@ -269,7 +310,9 @@ def main():
         e2e = {"value": world * cfg.T / (ms_e2e / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": nbytes * (2 if cfg.backward else 1),
                "d2h_bytes_per_step": nbytes * (2 if cfg.backward else 1),
-               "ms_per_step": ms_e2e}
+               "ms_per_step": ms_e2e,
+               "note": "pinned host buffers; uploads and readbacks overlap adjacent steps"}
+        del plans
 
     # ------------------------------------------------------------------------- report
     if rank != 0:
@@ -290,7 +333,8 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (all GEMM launches)",
                          "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
                          "frac": gemm_tflops / peak_t, "peak_kind": f"{kind} bf16 sustained",
-                         "traffic": None},
+                         "traffic": MEASURED_GEMM_TRAFFIC.get(args.config),
+                         "traffic_unit": "bytes per step (all grouped-GEMM launches)"},
             "gpu_launches": plan.launches_per_step(cfg.backward, cfg.bias_update) * args.steps,
             "clocks": clocks, "e2e": e2e}
     if world == 1 and not args.no_cpu_baseline:
