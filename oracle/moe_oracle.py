@@ -245,7 +245,7 @@ def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
 
 def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                   logits: np.ndarray | None = None, idx: np.ndarray | None = None,
-                  rnd=None) -> dict:
+                  rnd=None, aux: tuple | None = None) -> dict:
     """Full forward of the layer from fp64 copies of the inputs.
 
     ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
@@ -267,7 +267,10 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
     out = combine(ex["Y_perm"], r["gate"], disp["slot_to_row"],
                   None if shared is None else shared[3], rnd)
     res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
-           "z_coef": z_coef, "rnd": rnd}
+           "z_coef": z_coef, "rnd": rnd, "aux": aux}
+    if aux is not None:  # (seq_len, switch_coef, seq_coef)
+        a = aux_losses(logits, r["idx"], mode, *aux)
+        res["aux_switch"], res["aux_seq"] = a["switch"], a["seq"]
     if shared is not None:
         res["shared"] = dict(zip("AUHY", shared))
     return res
@@ -311,10 +314,13 @@ def layer_forward_dense_masked(inp: dict, mode: str, k: int, z_coef: float = 0.0
 
 
 def loss(fwd: dict, dY: np.ndarray) -> float:
-    """Scalar whose gradient the backward computes: <out, dY> plus the z-loss (weight 1)."""
+    """Scalar whose gradient the backward computes: <out, dY> plus the z-loss and the
+    balancing losses when present (weight 1 each)."""
     L = float(np.sum(fwd["out"] * dY))
     if fwd["mode"] == SOFTMAX:
         L += fwd["z_loss"]
+    if fwd.get("aux") is not None:
+        L += fwd["aux_switch"] + fwd["aux_seq"]
     return L
 
 
@@ -344,7 +350,8 @@ def expert_backward(dy: np.ndarray, x: np.ndarray, a: np.ndarray, u: np.ndarray,
 
 
 def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndarray,
-                    mode: str, z_coef: float, T_norm: int | None = None) -> dict:
+                    mode: str, z_coef: float, T_norm: int | None = None,
+                    dl_extra: np.ndarray | None = None) -> dict:
     """Gradient of the loss with respect to the router logits, W_r and x, given the
     gradient with respect to the gates. No gradient flows through the choice of experts
     or into the bias. ``T_norm`` is the token count of the z-loss mean (default: the rows
@@ -370,6 +377,8 @@ def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndar
         for i in range(k):
             sel[rows, idx[:, i]] = dg[:, i]
         dl = p * (sel - pdg) + (2.0 * z_coef / T_norm) * lse[:, None] * p
+    if dl_extra is not None:
+        dl = dl + dl_extra
     return {"dlogits": dl, "dW_r": dl.T @ x, "dx_r": dl @ W_r}
 
 
@@ -407,7 +416,11 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
                             inp["Ws_d"], rnd)
         res["dWs_d"], res["dWs_g"], res["dWs_u"] = g["dW_d"], g["dW_g"], g["dW_u"]
         res["dx_shared"] = g["dX"]
-    rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"])
+    dl_aux = None
+    if fwd.get("aux") is not None:
+        dl_aux = aux_losses_backward(fwd["logits"], idx, fwd["mode"], *fwd["aux"])
+    rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"],
+                         dl_extra=dl_aux)
     res.update(rb)
     res["dx"] = input_gradient(dX_perm, s2r, res.get("dx_shared"), rb["dx_r"], rnd)
     return res
@@ -437,6 +450,68 @@ def input_gradient(dX_perm, slot_to_row, dx_shared, dx_router, rnd=None):
     if dx_router is not None:
         dx += dx_router
     return _r(rnd, dx)
+
+
+# ---------------------------------------------------------------------------------------
+# load-balancing auxiliary losses
+
+def router_probs(logits: np.ndarray, mode: str) -> np.ndarray:
+    """Per-token probability vector over all experts used by the balancing losses: the
+    softmax in softmax mode; the sigmoid scores normalised to sum 1 in sigmoid mode."""
+    if mode == SOFTMAX:
+        m = logits.max(axis=1, keepdims=True)
+        ex = np.exp(logits - m)
+        return ex / ex.sum(axis=1, keepdims=True)
+    s = sigmoid(logits)
+    return s / s.sum(axis=1, keepdims=True)
+
+
+def aux_losses(logits: np.ndarray, idx: np.ndarray, mode: str, seq_len: int,
+               switch_coef: float, seq_coef: float) -> dict:
+    """Load-balancing losses (handbook summary, section 2.5: --moe-router-load-balancing-type
+    aux_loss with coefficient 1e-3, recorded as exactly 1 for a one-expert model; Apex-3
+    training command: seq_aux_alpha=1e-3; KempnerForge roadmap: sequence aux loss).
+
+    Readings (no formula on the pages):
+      switch = switch_coef * E * sum_e f_e P_e, f_e = c_e / (T k), P_e = mean_t pi[t, e];
+      seq    = seq_coef * mean over sequences s of sum_e f[s,e] P[s,e],
+               f[s,e] = E c[s,e] / (k L), P[s,e] = mean over the sequence of pi[t, e],
+    with pi the per-token probabilities of ``router_probs`` and c the chosen-expert counts.
+    Both equal their coefficient times 1 for E = 1, k = 1."""
+    T, E = logits.shape
+    k = idx.shape[1]
+    pi = router_probs(logits, mode)
+    onehot = np.zeros((T, E))
+    for i in range(k):
+        onehot[np.arange(T), idx[:, i]] = 1.0
+    f = onehot.sum(axis=0) / (T * k)
+    P = pi.mean(axis=0)
+    switch_unscaled = E * float(np.sum(f * P))
+    B = T // seq_len
+    fs = E * onehot.reshape(B, seq_len, E).sum(axis=1) / (k * seq_len)
+    Ps = pi.reshape(B, seq_len, E).mean(axis=1)
+    seq_unscaled = float(np.mean(np.sum(fs * Ps, axis=1)))
+    return {"switch": switch_coef * switch_unscaled, "seq": seq_coef * seq_unscaled,
+            "switch_unscaled": switch_unscaled, "seq_unscaled": seq_unscaled,
+            "f": f, "f_seq": fs, "pi": pi}
+
+
+def aux_losses_backward(logits: np.ndarray, idx: np.ndarray, mode: str, seq_len: int,
+                        switch_coef: float, seq_coef: float) -> np.ndarray:
+    """Gradient of switch + seq with respect to the logits (the counts f are piecewise
+    constant and receive none)."""
+    T, E = logits.shape
+    a = aux_losses(logits, idx, mode, seq_len, switch_coef, seq_coef)
+    B = T // seq_len
+    g = switch_coef * E * a["f"][None, :] / T + \
+        (seq_coef / B) * np.repeat(a["f_seq"], seq_len, axis=0) / seq_len
+    pi = a["pi"]
+    gpi = np.sum(g * pi, axis=1, keepdims=True)
+    if mode == SOFTMAX:
+        return pi * (g - gpi)
+    s = sigmoid(logits)
+    S = s.sum(axis=1, keepdims=True)
+    return (g - gpi) / S * s * (1.0 - s)
 
 
 # ---------------------------------------------------------------------------------------

@@ -253,12 +253,13 @@ def _fd_case(mode, seed):
             return inp, rng
 
 
-@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
-def test_backward_matches_central_finite_differences(mode):
+@pytest.mark.parametrize("mode,aux", [("sigmoid", None), ("softmax", None),
+                                      ("sigmoid", (3, 0.2, 0.3)), ("softmax", (2, 0.4, 0.1))])
+def test_backward_matches_central_finite_differences(mode, aux):
     inp, rng = _fd_case(mode, 11 if mode == "sigmoid" else 12)
     z = 0.1 if mode == "softmax" else 0.0
     dY = rng.standard_normal((6, 5))
-    fwd = O.layer_forward(inp, mode, 2, z)
+    fwd = O.layer_forward(inp, mode, 2, z, aux=aux)
     bwd = O.layer_backward(inp, fwd, dY)
     names = {"x": "dx", "W_r": "dW_r", "W_g": "dW_g", "W_u": "dW_u", "W_d": "dW_d",
              "Ws_g": "dWs_g", "Ws_u": "dWs_u", "Ws_d": "dWs_d"}
@@ -269,9 +270,9 @@ def test_backward_matches_central_finite_differences(mode):
         for ix in np.ndindex(arr.shape):
             old = arr[ix]
             arr[ix] = old + h
-            lp = O.loss(O.layer_forward(inp, mode, 2, z), dY)
+            lp = O.loss(O.layer_forward(inp, mode, 2, z, aux=aux), dY)
             arr[ix] = old - h
-            lm = O.loss(O.layer_forward(inp, mode, 2, z), dY)
+            lm = O.loss(O.layer_forward(inp, mode, 2, z, aux=aux), dY)
             arr[ix] = old
             num[ix] = (lp - lm) / (2 * h)
         ana = bwd[gname]
@@ -385,3 +386,48 @@ def test_proportional_bias_update_invariants():
     assert np.all(np.abs(delta - exact_step) <= 4 * ulp32)
     moved = counts != mean
     assert np.all(np.sign(delta[moved]) == np.sign(mean - counts[moved]))
+
+
+# ------------------------------------------------------------------- balancing losses
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_aux_losses_are_exactly_one_for_a_single_expert(mode):
+    """Handbook summary, section 2.5: the one-expert MoE recorded a load-balance loss of
+    exactly 1 (before its coefficient)."""
+    rng = np.random.default_rng(18)
+    logits = rng.standard_normal((64, 1))
+    a = O.aux_losses(logits, np.zeros((64, 1), dtype=np.int64), mode, 16, 1e-3, 1e-3)
+    assert a["switch_unscaled"] == 1.0 and a["seq_unscaled"] == 1.0
+    assert a["switch"] == pytest.approx(1e-3) and a["seq"] == pytest.approx(1e-3)
+    assert (O.aux_losses_backward(logits, np.zeros((64, 1), dtype=np.int64), mode, 16, 1e-3, 1e-3) == 0).all()
+
+
+def test_aux_losses_balanced_closed_form():
+    """Uniform probabilities and perfectly balanced choices: f_e = 1/E and P_e = 1/E, so the
+    unscaled losses are E * E * (1/E)(1/E) = 1."""
+    E, k, T = 8, 2, 32
+    logits = np.zeros((T, E))
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    for mode in ("sigmoid", "softmax"):
+        a = O.aux_losses(logits, idx, mode, 8, 1.0, 1.0)
+        assert a["switch_unscaled"] == pytest.approx(1.0, abs=1e-15)
+        assert a["seq_unscaled"] == pytest.approx(1.0, abs=1e-15)
+
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_aux_losses_gradient_matches_finite_differences(mode):
+    rng = np.random.default_rng(19)
+    T, E, k, L = 12, 5, 2, 4
+    logits = rng.standard_normal((T, E))
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    coef = (0.3, 0.7)
+    ana = O.aux_losses_backward(logits, idx, mode, L, *coef)
+    h = 1e-6
+    num = np.zeros_like(logits)
+    for ix in np.ndindex(logits.shape):
+        lp = logits.copy(); lp[ix] += h
+        lm = logits.copy(); lm[ix] -= h
+        ap = O.aux_losses(lp, idx, mode, L, *coef)
+        am = O.aux_losses(lm, idx, mode, L, *coef)
+        num[ix] = ((ap["switch"] + ap["seq"]) - (am["switch"] + am["seq"])) / (2 * h)
+    np.testing.assert_allclose(ana, num, rtol=1e-6, atol=1e-9)
