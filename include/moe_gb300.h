@@ -261,14 +261,47 @@ int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
  *   sum_i g_i dg_i) + (2 z_coef / T) * lse[t] * p_e (z-loss with weight 1).
  *   dW_r = dlogits^T x (fp32, fixed-order split reduction over tokens).
  * In : dg [T,k] fp32; x [T,d] bf16; topk_idx, topk_gate, topk_score [T,k]; logits [T,E]
- *      and lse [T] (softmax mode; may be NULL in sigmoid mode).
+ *      and lse [T] (softmax mode; may be NULL in sigmoid mode); dlogits_extra [T,E] fp32 or
+ *      NULL: a further logit gradient (the balancing losses') added before dW_r is formed.
  * Out: dlogits [T,E] fp32 (consumed by moe_permute_bwd for the router's dx term);
  *      dW_r [E,d] fp32.
  */
 int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* topk_idx,
                   const float* topk_gate, const float* topk_score, const float* logits,
-                  const float* lse, int64_t T, int d, int E, int k, int mode, float z_coef,
-                  float* dlogits, float* dW_r, void* ws, size_t ws_bytes, moe_stream_t stream);
+                  const float* lse, const float* dlogits_extra, int64_t T, int d, int E, int k,
+                  int mode, float z_coef, float* dlogits, float* dW_r, void* ws,
+                  size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_aux_loss - load-balancing losses of the router (forward).
+ * The pages name two such losses without printing their formulas: Megatron's "aux_loss"
+ * with coefficient 1e-3, recorded as exactly 1 for a one-expert model (handbook summary,
+ * section 2.5), and the sequence-wise loss "seq_aux_alpha=1e-3" of the Apex-3 training
+ * command ("The whole stack, in the open", "Run it yourself"; KempnerForge roadmap,
+ * "sequence aux loss"). Reading, with pi[t,e] the per-token probabilities over all experts
+ * (softmax of the logits in MOE_MODE_SOFTMAX; sigmoid scores normalised to sum 1 in
+ * MOE_MODE_SIGMOID) and c the chosen-expert counts:
+ *   aux_loss[0] = switch_coef * E * sum_e f_e P_e,  f_e = c_e / (T k),  P_e = mean_t pi[t,e];
+ *   aux_loss[1] = seq_coef * mean over the T/seq_len sequences s of sum_e f[s,e] P[s,e],
+ *                 f[s,e] = E c[s,e] / (k seq_len),  P[s,e] = mean over s of pi[t,e].
+ * In : logits [T,E] fp32 (from moe_route); topk_idx [T,k]. T % seq_len == 0.
+ * Out: aux_loss [2] fp32; aux_f [E + (T/seq_len) E] fp32 (f_e then f[s,e], consumed by
+ *      moe_aux_loss_bwd). Sums are in a fixed order (fp64 for the final reductions).
+ */
+int moe_aux_loss(const float* logits, const int32_t* topk_idx, int64_t T, int E, int k,
+                 int mode, int64_t seq_len, float switch_coef, float seq_coef, float* aux_loss,
+                 float* aux_f, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_aux_loss_bwd - gradient of aux_loss[0] + aux_loss[1] with respect to the logits (the
+ * counts get none). With g_e = switch_coef E f_e / T + seq_coef f[s,e] / (T/seq_len * seq_len):
+ * softmax mode pi (g - <g, pi>); sigmoid mode (g - <g, pi>) / S * s (1 - s), S = sum of s.
+ * In : logits [T,E]; aux_f from moe_aux_loss.  Out: dlogits_aux [T,E] fp32, to be passed to
+ * moe_route_bwd as dlogits_extra so that it reaches dW_r and the input gradient.
+ */
+int moe_aux_loss_bwd(const float* logits, const float* aux_f, int64_t T, int E, int mode,
+                     int64_t seq_len, float switch_coef, float seq_coef, float* dlogits_aux,
+                     moe_stream_t stream);
 
 /*
  * moe_permute_bwd - input gradient of the layer (B6).

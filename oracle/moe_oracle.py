@@ -559,11 +559,14 @@ def token_forward(inp: dict, t: int, experts, gates, rnd=None) -> np.ndarray:
 
 
 def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, k: int,
-                   dY_t: np.ndarray, z_coef: float, T: int, rnd=None) -> dict:
+                   dY_t: np.ndarray, z_coef: float, T: int, rnd=None,
+                   dl_extra_t: np.ndarray | None = None) -> dict:
     """Gradient rows of one token: dx_t, dg_t and the router logit gradient for it.
 
     A token's dx depends only on its own routing, experts and upstream gradient, so it can
-    be evaluated alone. ``T`` is the batch size that normalises the z-loss mean."""
+    be evaluated alone. ``T`` is the batch size that normalises the z-loss mean.
+    ``dl_extra_t`` adds a logit gradient row for the token (the balancing losses', which
+    depend on batch-wide counts)."""
     x_t = inp["x"][t:t + 1]
     lg = logits_t[None, :]
     r = route(lg, mode, k, inp.get("b"), z_coef)
@@ -583,7 +586,8 @@ def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, 
         dA, dU = swiglu_backward(dY_t[None, :] @ inp["Ws_d"], a, u)
         dA, dU = _r(rnd, dA), _r(rnd, dU)
         dx += _r(rnd, dA @ inp["Ws_g"] + dU @ inp["Ws_u"])
-    rb = router_backward(dg, r, x_t, inp["W_r"], mode, z_coef, T_norm=T)
+    rb = router_backward(dg, r, x_t, inp["W_r"], mode, z_coef, T_norm=T,
+                         dl_extra=None if dl_extra_t is None else dl_extra_t[None, :])
     dx += rb["dx_r"]
     return {"dx": _r(rnd, dx[0]), "dg": dg[0], "dlogits": rb["dlogits"][0]}
 

@@ -30,6 +30,13 @@ class MoEConfig:
     z_coef: float = 0.0    # router z-loss coefficient (softmax mode)
     zipf: bool = False     # skewed expert popularity with a block of never-chosen experts
     bias_rule: str = "sign"  # "sign": b += gamma sign(mean - c); "proportional": gamma (mean - c)/mean
+    aux_switch: float = 0.0  # Switch-style load-balancing loss coefficient (0 = off)
+    aux_seq: float = 0.0     # sequence-wise load-balancing loss coefficient (0 = off)
+    seq_len: int = 0         # tokens per sequence for the sequence-wise loss
+
+    @property
+    def has_aux(self) -> bool:
+        return self.aux_switch != 0.0 or self.aux_seq != 0.0
 
     @property
     def N(self) -> int:
@@ -76,4 +83,10 @@ C5 = MoEConfig("apex3_T49152_d2048_E64_k4_f1280_proportional", T=49152, d=2048, 
                f=1280, f_shared=0, mode="sigmoid", seed=5, backward=True, bias_update=True,
                gamma=0.01, bias_rule="proportional")
 
-CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5}
+# The large layer with the load-balancing losses the pages name: Megatron's aux_loss with
+# coefficient 1e-3 (handbook summary, section 2.5) and the sequence-wise loss with
+# seq_aux_alpha = 1e-3 (Apex-3 training command), over its 16 sequences of 4096 tokens.
+C6 = C4.with_(name="large_T65536_d4096_E64_k8_f1536_shared3072_auxlosses", aux_switch=1e-3,
+              aux_seq=1e-3, seq_len=4096)
+
+CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5, "C6": C6}

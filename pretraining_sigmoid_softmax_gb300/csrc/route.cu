@@ -259,8 +259,9 @@ __global__ void z_finalize_kernel(const double* __restrict__ z_part, int64_t nbl
 __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
     const float* __restrict__ dg, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ topk_gate, const float* __restrict__ topk_score,
-    const float* __restrict__ logits, const float* __restrict__ lse, int64_t T, int E, int k,
-    int mode, float z_scale, float* __restrict__ dlogits) {
+    const float* __restrict__ logits, const float* __restrict__ lse,
+    const float* __restrict__ extra, int64_t T, int E, int k, int mode, float z_scale,
+    float* __restrict__ dlogits) {
     const int lane = threadIdx.x % 32;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (t >= T) return;
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
                 const float vi = __shfl_sync(0xffffffffu, v, i);
                 if (ei == e) out = vi;
             }
-            if (e < E) dlogits[t * E + e] = out;
+            if (e < E) dlogits[t * E + e] = extra ? out + extra[t * E + e] : out;
         }
     } else {
         const float l_se = lse[t];
@@ -304,7 +305,8 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
             }
             if (e < E) {
                 const float p = expf(logits[t * E + e] - l_se);
-                dlogits[t * E + e] = p * (sel - gdg) + z_scale * l_se * p;
+                const float v = p * (sel - gdg) + z_scale * l_se * p;
+                dlogits[t * E + e] = extra ? v + extra[t * E + e] : v;
             }
         }
     }
@@ -405,6 +407,140 @@ __global__ void route_bwd_reduce_kernel(const float* __restrict__ part, int64_t 
     dW_r[i] = s;
 }
 
+// ------------------------------------------------------------------ balancing losses
+// Per-token probabilities pi over all experts: softmax of the logits, or the sigmoid
+// scores normalised to sum 1. Per (sequence, chunk of kAuxChunk tokens): column sums of pi
+// and chosen-expert counts, one thread per expert summing its tokens in order.
+constexpr int kAuxChunk = 256;
+
+__global__ void __launch_bounds__(kThreads) aux_partial_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ topk_idx, int64_t seq_len,
+    int E, int k, int mode, float* __restrict__ Ppart, int32_t* __restrict__ Cpart) {
+    __shared__ float nrm_a[kAuxChunk];  // softmax: max; sigmoid: sum of scores
+    __shared__ float nrm_b[kAuxChunk];  // softmax: sum of exp(l - max)
+    const int64_t s = blockIdx.x, c = blockIdx.y;
+    const int64_t t0 = s * seq_len + c * kAuxChunk;
+    const int64_t n = min((int64_t)kAuxChunk, seq_len - c * kAuxChunk);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int r = warp; r < n; r += kThreads / 32) {
+        const float* lg = logits + (t0 + r) * E;
+        float a = (mode == MOE_MODE_SOFTMAX) ? -INFINITY : 0.f, b = 0.f;
+        if (mode == MOE_MODE_SOFTMAX) {
+            for (int e = lane; e < E; e += 32) a = fmaxf(a, lg[e]);
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            for (int e = lane; e < E; e += 32) b += expf(lg[e] - a);
+            for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+        } else {
+            for (int e = lane; e < E; e += 32) a += sigmoid_f(lg[e]);
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        }
+        if (lane == 0) {
+            nrm_a[r] = a;
+            nrm_b[r] = b;
+        }
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    if (e >= E) return;
+    float P = 0.f;
+    int32_t cnt = 0;
+    for (int r = 0; r < n; ++r) {
+        const float l = logits[(t0 + r) * E + e];
+        P += (mode == MOE_MODE_SOFTMAX) ? expf(l - nrm_a[r]) / nrm_b[r] : sigmoid_f(l) / nrm_a[r];
+        const int32_t* id = topk_idx + (t0 + r) * k;
+        for (int i = 0; i < k; ++i) cnt += (id[i] == e);
+    }
+    const int64_t slot = (s * gridDim.y + c) * E + e;
+    Ppart[slot] = P;
+    Cpart[slot] = cnt;
+}
+
+// One CTA: f and P per expert and per sequence, the two losses, and the f values the
+// backward needs (aux_f[e] = f_e, aux_f[E + s E + e] = f[s,e]).
+__global__ void __launch_bounds__(kThreads) aux_final_kernel(
+    const float* __restrict__ Ppart, const int32_t* __restrict__ Cpart, int64_t B, int64_t C,
+    int64_t seq_len, int E, int k, float switch_coef, float seq_coef, float* __restrict__ aux_f,
+    float* __restrict__ aux_loss) {
+    __shared__ double sw[kThreads], sq[kThreads];
+    const int e = threadIdx.x;
+    double sw_e = 0.0, sq_e = 0.0;
+    if (e < E) {
+        const double T = (double)B * (double)seq_len;
+        double Psum = 0.0, csum = 0.0;
+        for (int64_t s = 0; s < B; ++s) {
+            double Ps = 0.0, cs = 0.0;
+            for (int64_t c = 0; c < C; ++c) {
+                Ps += Ppart[(s * C + c) * E + e];
+                cs += Cpart[(s * C + c) * E + e];
+            }
+            const double fs = (double)E * cs / ((double)k * (double)seq_len);
+            aux_f[E + s * E + e] = (float)fs;
+            sq_e += fs * (Ps / (double)seq_len);
+            Psum += Ps;
+            csum += cs;
+        }
+        const double f = csum / (T * (double)k);
+        aux_f[e] = (float)f;
+        sw_e = f * (Psum / T);
+    }
+    sw[e] = sw_e;
+    sq[e] = sq_e;
+    __syncthreads();
+    if (e == 0) {
+        double a = 0.0, b = 0.0;
+        for (int j = 0; j < E; ++j) {
+            a += sw[j];
+            b += sq[j];
+        }
+        aux_loss[0] = (float)((double)switch_coef * (double)E * a);
+        aux_loss[1] = (float)((double)seq_coef * b / (double)B);
+    }
+}
+
+// Gradient of the two losses with respect to the logits, one warp per token:
+// g_e = switch_coef E f_e / T + seq_coef f[s,e] / (B L); softmax: pi (g - <g, pi>);
+// sigmoid: (g - <g, pi>) / S * s (1 - s).
+__global__ void __launch_bounds__(256) aux_bwd_kernel(
+    const float* __restrict__ logits, const float* __restrict__ aux_f, int64_t T, int E,
+    int64_t seq_len, int mode, float switch_coef, float seq_coef, float* __restrict__ dl) {
+    const int lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (t >= T) return;  // whole warp
+    const int64_t B = T / seq_len, s = t / seq_len;
+    const float* lg = logits + t * E;
+    float a = (mode == MOE_MODE_SOFTMAX) ? -INFINITY : 0.f, b = 0.f;
+    if (mode == MOE_MODE_SOFTMAX) {
+        for (int e = lane; e < E; e += 32) a = fmaxf(a, lg[e]);
+        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        for (int e = lane; e < E; e += 32) b += expf(lg[e] - a);
+        for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+    } else {
+        for (int e = lane; e < E; e += 32) a += sigmoid_f(lg[e]);
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    }
+    const float c_sw = switch_coef * (float)E / (float)T;
+    const float c_sq = seq_coef / ((float)B * (float)seq_len);
+    float gpi = 0.f;
+    for (int e = lane; e < E; e += 32) {
+        const float l = lg[e];
+        const float pi = (mode == MOE_MODE_SOFTMAX) ? expf(l - a) / b : sigmoid_f(l) / a;
+        gpi += (c_sw * aux_f[e] + c_sq * aux_f[E + s * E + e]) * pi;
+    }
+    for (int o = 16; o > 0; o >>= 1) gpi += __shfl_xor_sync(0xffffffffu, gpi, o);
+    for (int e = lane; e < E; e += 32) {
+        const float l = lg[e];
+        const float g = c_sw * aux_f[e] + c_sq * aux_f[E + s * E + e];
+        float v;
+        if (mode == MOE_MODE_SOFTMAX) {
+            v = expf(l - a) / b * (g - gpi);
+        } else {
+            const float sg = sigmoid_f(l);
+            v = (g - gpi) / a * sg * (1.f - sg);
+        }
+        dl[t * E + e] = v;
+    }
+}
+
 template <int EP, int TM, int TTOK, int EJ>
 int launch_route_fwd(const moe_bf16* x, const float* W_r, const float* b, int64_t T, int d,
                      int E, int k, int mode, float* logits, int32_t* idx, float* gate,
@@ -464,9 +600,10 @@ extern "C" int moe_route(const moe_bf16* x, const float* W_r, const float* b, in
 
 extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* topk_idx,
                              const float* topk_gate, const float* topk_score,
-                             const float* logits, const float* lse, int64_t T, int d, int E,
-                             int k, int mode, float z_coef, float* dlogits, float* dW_r,
-                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+                             const float* logits, const float* lse, const float* dlogits_extra,
+                             int64_t T, int d, int E, int k, int mode, float z_coef,
+                             float* dlogits, float* dW_r, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
     if (!dg || !x || !topk_idx || !topk_gate || !topk_score || !dlogits || !dW_r)
         return MOE_ERR_INVALID_ARG;
     if (T <= 0 || d <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
@@ -482,7 +619,8 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
     cudaStream_t st = (cudaStream_t)stream;
     const float z_scale = 2.0f * z_coef / (float)T;
     route_bwd_dlogits_kernel<<<(unsigned)cdiv(T, 8), 256, 0, st>>>(
-        dg, topk_idx, topk_gate, topk_score, logits, lse, T, E, k, mode, z_scale, dlogits);
+        dg, topk_idx, topk_gate, topk_score, logits, lse, dlogits_extra, T, E, k, mode, z_scale,
+        dlogits);
     if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
     dim3 grid(d / kBwTJ, (unsigned)cdiv(E, kBwTE), (unsigned)nsplit);
     route_bwd_dwr_kernel<<<grid, 256, 0, st>>>(dlogits, reinterpret_cast<const __nv_bfloat16*>(x),
@@ -490,5 +628,40 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
     if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
     const int64_t n = (int64_t)E * d;
     route_bwd_reduce_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(part, nsplit, n, dW_r);
+    return launch_status();
+}
+
+extern "C" int moe_aux_loss(const float* logits, const int32_t* topk_idx, int64_t T, int E, int k,
+                            int mode, int64_t seq_len, float switch_coef, float seq_coef,
+                            float* aux_loss, float* aux_f, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+    if (!logits || !topk_idx || !aux_loss || !aux_f) return MOE_ERR_INVALID_ARG;
+    if (T <= 0 || E <= 0 || k <= 0 || seq_len <= 0 || T % seq_len != 0) return MOE_ERR_INVALID_ARG;
+    if (mode != MOE_MODE_SIGMOID && mode != MOE_MODE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > E || k > 32) return MOE_ERR_UNSUPPORTED;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    const int64_t B = T / seq_len, C = cdiv(seq_len, kAuxChunk);
+    WsCarver wc(ws, ws_bytes);
+    float* Ppart = wc.take<float>((size_t)B * C * E);
+    int32_t* Cpart = wc.take<int32_t>((size_t)B * C * E);
+    if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    aux_partial_kernel<<<dim3((unsigned)B, (unsigned)C), kThreads, 0, st>>>(
+        logits, topk_idx, seq_len, E, k, mode, Ppart, Cpart);
+    aux_final_kernel<<<1, kThreads, 0, st>>>(Ppart, Cpart, B, C, seq_len, E, k, switch_coef,
+                                              seq_coef, aux_f, aux_loss);
+    return launch_status();
+}
+
+extern "C" int moe_aux_loss_bwd(const float* logits, const float* aux_f, int64_t T, int E, int mode,
+                                int64_t seq_len, float switch_coef, float seq_coef,
+                                float* dlogits_aux, moe_stream_t stream) {
+    if (!logits || !aux_f || !dlogits_aux) return MOE_ERR_INVALID_ARG;
+    if (T <= 0 || E <= 0 || seq_len <= 0 || T % seq_len != 0) return MOE_ERR_INVALID_ARG;
+    if (mode != MOE_MODE_SIGMOID && mode != MOE_MODE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    aux_bwd_kernel<<<(unsigned)cdiv(T, 8), 256, 0, (cudaStream_t)stream>>>(
+        logits, aux_f, T, E, seq_len, mode, switch_coef, seq_coef, dlogits_aux);
     return launch_status();
 }

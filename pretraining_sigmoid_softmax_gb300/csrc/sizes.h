@@ -28,6 +28,11 @@ inline size_t ws_route_bwd(int64_t T, int d, int E) {
     return round256(sizeof(float) * route_bwd_splits(T) * (size_t)E * d);
 }
 inline size_t ws_expert(int E) { return round256(sizeof(int32_t) * (E + 1)) * 2; }
+// Balancing losses: partial sums per (sequence, 256-token chunk); there are at most T such
+// chunks (one-token sequences), each holding E floats and E counts.
+inline size_t ws_aux(int64_t T, int E) {
+    return 2 * round256(sizeof(float) * (size_t)T * E);
+}
 
 inline size_t ws_total(int64_t T, int d, int E, int k) {
     (void)k;
@@ -35,6 +40,7 @@ inline size_t ws_total(int64_t T, int d, int E, int k) {
     if (ws_permute(T, E) > m) m = ws_permute(T, E);
     if (ws_route_bwd(T, d, E) > m) m = ws_route_bwd(T, d, E);
     if (ws_expert(E) > m) m = ws_expert(E);
+    if (ws_aux(T, E) > m) m = ws_aux(T, E);
     return m + 256;
 }
 

@@ -25,10 +25,18 @@ class MoEShape:
     f_shared: int = 0
     mode: int = ops.MODE_SIGMOID
     z_coef: float = 0.0
+    aux_switch: float = 0.0
+    aux_seq: float = 0.0
+    seq_len: int = 0
+
+    @property
+    def has_aux(self) -> bool:
+        return self.aux_switch != 0.0 or self.aux_seq != 0.0
 
     @classmethod
     def from_config(cls, cfg) -> "MoEShape":
-        return cls(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_shared, cfg.mode_id, cfg.z_coef)
+        return cls(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_shared, cfg.mode_id, cfg.z_coef,
+                   cfg.aux_switch, cfg.aux_seq, cfg.seq_len or cfg.T)
 
 
 def _empty(shape, dtype, dev):
@@ -68,8 +76,13 @@ class MoEPlan:
             self.Us = _empty((T, fs), bf, dev)
             self.Hs = _empty((T, fs), bf, dev)
             self.Ys = _empty((T, d), bf, dev)
+        if s.has_aux:
+            self.aux_loss = torch.zeros((2,), dtype=f32, device=dev)
+            self.aux_f = _empty((E + (T // s.seq_len) * E,), f32, dev)
         self.has_backward = backward
         if backward:
+            if s.has_aux:
+                self.dlogits_aux = _empty((T, E), f32, dev)
             self.dY_perm = _empty((R, d), bf, dev)
             self.dg = _empty((T, k), f32, dev)
             self.dA = _empty((R, f), bf, dev)
@@ -109,6 +122,8 @@ class MoEPlan:
         """Kernel launches of one step through this plan (what the entry points enqueue)."""
         s = self.s
         n = 1 + (1 if s.mode == ops.MODE_SOFTMAX else 0)   # route (+ z-loss reduction)
+        if s.has_aux:
+            n += 2 + (1 if backward else 0)                 # balancing losses (+ gradient)
         n += 5                                              # permute
         n += 2 + (2 if s.f_shared else 0)                   # expert forward (G1, G2)
         n += 1                                              # combine
@@ -131,6 +146,9 @@ class MoEPlan:
                       self.topk_idx, self.topk_gate, self.topk_score,
                       self.lse if softmax else None, self.z_loss if softmax else None, self.ws,
                       stream)
+        if s.has_aux:
+            ops.moe_aux_loss(self.logits, self.topk_idx, s.mode, s.seq_len, s.aux_switch,
+                             s.aux_seq, self.aux_loss, self.aux_f, self.ws, stream)
         ops.moe_permute(self.topk_idx, x, s.E, self.counts, self.offsets, self.row_offsets,
                         self.perm_token, self.slot_to_row, self.X_perm, self.ws, stream)
         self._gemm(ops.moe_expert_fwd, self.X_perm, self.row_offsets, W_g, W_u, W_d, self.A,
@@ -160,9 +178,15 @@ class MoEPlan:
                        Ws_u[None], Ws_d[None], self.dxs, self.dAs, self.dUs, self.dWs_g[None],
                        self.dWs_u[None], self.dWs_d[None], self.ws, stream=stream)
             dxs = self.dxs
+        extra = None
+        if s.has_aux:
+            ops.moe_aux_loss_bwd(self.logits, self.aux_f, s.mode, s.seq_len, s.aux_switch,
+                                 s.aux_seq, self.dlogits_aux, stream)
+            extra = self.dlogits_aux
         ops.moe_route_bwd(self.dg, x, self.topk_idx, self.topk_gate, self.topk_score,
                           self.logits if softmax else None, self.lse if softmax else None, s.E,
-                          s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream)
+                          s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream,
+                          dlogits_extra=extra)
         ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx, stream)
         return self.dx
 

@@ -160,14 +160,34 @@ def moe_expert_bwd(dY, X, A, U, H, row_offsets, W_g, W_u, W_d, dX, dA, dU, dW_g,
 
 
 def moe_route_bwd(dg, x, topk_idx, topk_gate, topk_score, logits, lse, E, mode, z_coef, dlogits,
-                  dW_r, ws, stream=None):
+                  dW_r, ws, stream=None, dlogits_extra=None):
     T, k = topk_idx.shape
     d = x.shape[1]
-    _contig(dg, x, topk_idx, topk_gate, topk_score, logits, lse, dlogits, dW_r, ws)
+    _contig(dg, x, topk_idx, topk_gate, topk_score, logits, lse, dlogits, dW_r, ws, dlogits_extra)
     _check(_lib.load().moe_route_bwd(_p(dg), _p(x), _p(topk_idx), _p(topk_gate), _p(topk_score),
-                                     _p(logits), _p(lse), T, d, E, k, mode, float(z_coef),
-                                     _p(dlogits), _p(dW_r), _p(ws), ws.numel(), _stream(stream)),
+                                     _p(logits), _p(lse), _p(dlogits_extra), T, d, E, k, mode,
+                                     float(z_coef), _p(dlogits), _p(dW_r), _p(ws), ws.numel(),
+                                     _stream(stream)),
            "moe_route_bwd")
+
+
+def moe_aux_loss(logits, topk_idx, mode, seq_len, switch_coef, seq_coef, aux_loss, aux_f, ws,
+                 stream=None):
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    _contig(logits, topk_idx, aux_loss, aux_f, ws)
+    _check(_lib.load().moe_aux_loss(_p(logits), _p(topk_idx), T, E, k, mode, seq_len,
+                                    float(switch_coef), float(seq_coef), _p(aux_loss), _p(aux_f),
+                                    _p(ws), ws.numel(), _stream(stream)), "moe_aux_loss")
+
+
+def moe_aux_loss_bwd(logits, aux_f, mode, seq_len, switch_coef, seq_coef, dlogits_aux,
+                     stream=None):
+    T, E = logits.shape
+    _contig(logits, aux_f, dlogits_aux)
+    _check(_lib.load().moe_aux_loss_bwd(_p(logits), _p(aux_f), T, E, mode, seq_len,
+                                        float(switch_coef), float(seq_coef), _p(dlogits_aux),
+                                        _stream(stream)), "moe_aux_loss_bwd")
 
 
 def moe_permute_bwd(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx, stream=None):

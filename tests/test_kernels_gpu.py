@@ -359,3 +359,48 @@ def test_proportional_bias_update_is_bit_exact():
     ops.moe_bias_update_proportional(dev(counts), T, k, 0.01, bd)
     ref = O.bias_update_proportional(counts.numpy(), b.numpy(), T, k, 0.01)
     assert np.array_equal(bd.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode,T,E,k,L", [("sigmoid", 4096, 64, 8, 1024), ("softmax", 3000, 32, 4, 1000),
+                                         ("sigmoid", 512, 1, 1, 256), ("softmax", 777, 200, 3, 777)])
+def test_balancing_losses_match_oracle(mode, T, E, k, L):
+    g = torch.Generator().manual_seed(T + E)
+    logits = torch.randn(T, E, generator=g) * 2
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    m = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
+    sw, sq = 1e-3, 2e-3
+    aux = torch.zeros(2, device="cuda")
+    f = torch.empty(E + (T // L) * E, device="cuda")
+    dl = torch.empty(T, E, device="cuda")
+    ops.moe_aux_loss(dev(logits), dev(idx), m, L, sw, sq, aux, f, _ws(T, 128, E, k))
+    ops.moe_aux_loss_bwd(dev(logits), f, m, L, sw, sq, dl)
+    torch.cuda.synchronize()
+    ref = O.aux_losses(h64(logits), idx.numpy().astype(np.int64), mode, L, sw, sq)
+    assert float(aux[0]) == pytest.approx(ref["switch"], rel=1e-5)
+    assert float(aux[1]) == pytest.approx(ref["seq"], rel=1e-5)
+    np.testing.assert_allclose(h64(f[:E]), ref["f"], rtol=1e-6)
+    rdl = O.aux_losses_backward(h64(logits), idx.numpy().astype(np.int64), mode, L, sw, sq)
+    scale = np.abs(rdl).max()
+    assert_close(dl, rdl, "dlogits_aux", atol=1e-5 * scale, rtol=1e-4)
+
+
+def test_router_backward_adds_the_extra_logit_gradient():
+    g = torch.Generator().manual_seed(33)
+    T, d, E, k = 2000, 256, 32, 4
+    x = randn_bf16((T, d), g)
+    W_r = torch.randn(E, d, generator=g) * d ** -0.5
+    b = torch.rand(E, generator=g) * 0.1 - 0.05
+    r = _route(x, W_r, b, k, ops.MODE_SIGMOID, 0.0)
+    dg = torch.randn(T, k, generator=g)
+    extra = torch.randn(T, E, generator=g) * 1e-3
+    dl = torch.empty(T, E, device="cuda")
+    dW_r = torch.empty(E, d, device="cuda")
+    ops.moe_route_bwd(dev(dg), dev(x), r["idx"], r["gate"], r["score"], None, None, E,
+                      ops.MODE_SIGMOID, 0.0, dl, dW_r, _ws(T, d, E, k), dlogits_extra=dev(extra))
+    torch.cuda.synchronize()
+    lg = h64(r["logits"])
+    ref = O.route(lg, "sigmoid", k, h64(b))
+    ref = O._regate(ref, lg, r["idx"].cpu().numpy(), "sigmoid", h64(b), 0.0)
+    rb = O.router_backward(h64(dg), ref, h64(x), h64(W_r), "sigmoid", 0.0, dl_extra=h64(extra))
+    assert_close(dl, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
+    assert_close(dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)

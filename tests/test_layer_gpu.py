@@ -84,8 +84,12 @@ def full_parity(cfg, inp):
     plan, b_new = run_gpu(cfg, inp)
     idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
     i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
-    fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND)
+    aux = (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
+    fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND, aux=aux)
     assert_close(plan.topk_gate, fwd["gate"], "gates", atol=1e-6, rtol=1e-5)
+    if aux is not None:
+        assert float(plan.aux_loss[0]) == pytest.approx(fwd["aux_switch"], rel=1e-5)
+        assert float(plan.aux_loss[1]) == pytest.approx(fwd["aux_seq"], rel=1e-5)
     assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], fwd["X_perm"], "X_perm", 0, 0)
     assert_close(plan.out, fwd["out"], "out")
     if cfg.mode == "softmax":
@@ -116,6 +120,12 @@ SMALL = [
               seed=14, backward=True, bias_update=False, z_coef=1e-2),
     MoEConfig("skewed_small", T=2048, d=256, E=32, k=4, f=128, f_shared=0, mode="sigmoid",
               seed=15, backward=True, bias_update=False, zipf=True),
+    MoEConfig("aux_losses_sigmoid", T=1024, d=256, E=16, k=4, f=256, f_shared=128,
+              mode="sigmoid", seed=16, backward=True, bias_update=True, aux_switch=1e-2,
+              aux_seq=2e-2, seq_len=256),
+    MoEConfig("aux_losses_softmax", T=768, d=256, E=8, k=2, f=128, f_shared=0, mode="softmax",
+              seed=17, backward=True, bias_update=False, z_coef=1e-3, aux_switch=1e-2,
+              aux_seq=1e-2, seq_len=384),
 ]
 
 
@@ -150,7 +160,7 @@ def test_layer_is_bitwise_repeatable():
         assert torch.equal(r1[k], v), k
 
 
-@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5"])
+@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5", "C6"])
 def test_workload_sampled_parity(name):
     """Full-size workloads in the benchmark's launch configuration: routing, counts and
     permutation in full; out and dx on sampled tokens; weight-gradient entries of sampled
@@ -167,11 +177,18 @@ def test_workload_sampled_parity(name):
     ref = O._regate(ref, lg, idx, cfg.mode, O.to64(inp["b"]), cfg.z_coef)
     out = plan.out[torch.from_numpy(toks).cuda()]
     dx = plan.dx[torch.from_numpy(toks).cuda()]
+    dl_aux = None
+    if cfg.has_aux:  # batch-wide losses: compared in full, their gradient feeds dx
+        a = O.aux_losses(lg, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
+        assert float(plan.aux_loss[0]) == pytest.approx(a["switch"], rel=1e-5)
+        assert float(plan.aux_loss[1]) == pytest.approx(a["seq"], rel=1e-5)
+        dl_aux = O.aux_losses_backward(lg, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
     for j, t in enumerate(toks):
         o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND)
         assert_close(out[j], o, f"out[{t}]")
         tb = O.token_backward(lazy, int(t), lg[t], idx[t], cfg.mode, cfg.k,
-                              O.to64(inp["dY"][t]), cfg.z_coef, cfg.T, rnd=RND)
+                              O.to64(inp["dY"][t]), cfg.z_coef, cfg.T, rnd=RND,
+                              dl_extra_t=None if dl_aux is None else dl_aux[t])
         assert_close(dx[j], tb["dx"], f"dx[{t}]")
     counts = D["counts"]
     live = np.nonzero(counts)[0]
