@@ -196,6 +196,33 @@ class MoEPlan:
         else:
             ops.moe_bias_update(self.counts, self.s.T, self.s.k, gamma, b, stream)
 
+    def capture_step(self, x, weights: dict, dY=None, b=None, gamma=0.0, rule="sign",
+                     bias_update=False, warmup=1):
+        """Record one whole step (forward, backward when dY is given, bias update) into a
+        CUDA graph over this plan's fixed buffers; ``graph.replay()`` then re-runs it with
+        one launch from the host. Inputs are read from the same device tensors at replay
+        time, so callers refresh them in place. The warm-up runs load every kernel first."""
+        W = (weights["W_r"], b, weights["W_g"], weights["W_u"], weights["W_d"],
+             weights.get("Ws_g"), weights.get("Ws_u"), weights.get("Ws_d"))
+
+        def step():
+            self.forward(x, *W)
+            if dY is not None:
+                self.backward(dY)
+                if bias_update:
+                    self.bias_update(b, gamma, rule)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                step()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        return graph
+
     def grads(self) -> dict:
         g = {"dx": self.dx, "dW_r": self.dW_r, "dW_g": self.dW_g, "dW_u": self.dW_u,
              "dW_d": self.dW_d}

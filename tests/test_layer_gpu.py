@@ -266,3 +266,24 @@ def test_router_backward_at_full_size():
     rb = O.router_backward(O.to64(dg), ref, O.to64(x), O.to64(W_r), "sigmoid", 0.0)
     assert_close(plan.dlogits, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
     assert_close(plan.dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)
+
+
+def test_cuda_graph_replay_matches_eager_step():
+    """A whole step captured as one CUDA graph and replayed gives the eager step's bits."""
+    cfg = CONFIGS["C1"]
+    inp = make_inputs(cfg)
+    p_eager, b_eager = run_gpu(cfg, inp)
+    d = {k: v.cuda() for k, v in inp.items()}
+    plan = MoEPlan(MoEShape.from_config(cfg), "cuda", backward=True)
+    b = d["b"].clone()
+    weights = {k: d[k] for k in ("W_r", "W_g", "W_u", "W_d", "Ws_g", "Ws_u", "Ws_d")}
+    graph = plan.capture_step(d["x"], weights, d["dY"], b, cfg.gamma, cfg.bias_rule, True,
+                              warmup=1)
+    b.copy_(d["b"])  # capture ran one warm-up step that moved the bias
+    graph.replay()
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    assert torch.equal(plan.out, p_eager.out)
+    for k, v in plan.grads().items():
+        assert torch.equal(v, p_eager.grads()[k]), k
+    assert torch.equal(b, b_eager)
