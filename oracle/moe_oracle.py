@@ -83,6 +83,39 @@ def _r(rnd, x):
     return x if rnd is None else rnd(x)
 
 
+# ---------------------------------------------------------------------------------------
+# FP8 (E4M3) rowwise quantisation of GEMM operands
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (4 significant bits, ties to even), saturating at
+    +-448. Below the smallest normal (2**-6) the spacing stays 2**-9 (subnormals)."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e, -5)
+    q = np.ldexp(np.rint(np.ldexp(x, 4 - e)), e - 4)
+    return np.clip(q, -E4M3_MAX, E4M3_MAX)
+
+
+def quantize_rows_fp8(X: np.ndarray):
+    """Rowwise FP8 quantisation (the Apex-3 stack's fp8_rowwise precision): per row,
+    scale = fp32(amax / 448) (1 for an all-zero row), q = E4M3(fp32(x / scale)).
+    Returns (q, scale); q * scale[:, None] is the dequantised operand. The divisions are
+    IEEE fp32 divisions, as the GPU evaluates them."""
+    X32 = np.asarray(X, dtype=np.float32)
+    amax = np.abs(X32).max(axis=1)
+    scale = np.where(amax > 0, (amax / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0))
+    y = (X32 / scale[:, None]).astype(np.float32)
+    return e4m3_round(y), scale.astype(np.float64)
+
+
+def fp8_dequant_rows(X: np.ndarray) -> np.ndarray:
+    q, sc = quantize_rows_fp8(X)
+    return q * sc[:, None]
+
+
 def sigmoid(z: np.ndarray) -> np.ndarray:
     return 1.0 / (1.0 + np.exp(-z))
 
@@ -202,6 +235,20 @@ def dispatch(idx: np.ndarray, E: int) -> dict:
 # ---------------------------------------------------------------------------------------
 # experts and combine
 
+def swiglu_expert_fp8(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
+                      rnd=None):
+    """The SwiGLU expert with FP8 rowwise GEMM operands (row scales for the activations,
+    per-output-channel scales for the weights, fp32-exact accumulation): x and the rows of
+    W_g, W_u, W_d are quantised; h is stored (rnd) and then quantised per row for the down
+    projection."""
+    xq = fp8_dequant_rows(rows)
+    a = xq @ fp8_dequant_rows(W_g).T
+    u = xq @ fp8_dequant_rows(W_u).T
+    h = _r(rnd, silu(a) * u)
+    y = _r(rnd, fp8_dequant_rows(h) @ fp8_dequant_rows(W_d).T)
+    return _r(rnd, a), _r(rnd, u), h, y
+
+
 def swiglu_expert(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
                   rnd=None):
     """One bias-free SwiGLU expert (three weight matrices, section 2.5):
@@ -213,8 +260,10 @@ def swiglu_expert(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.nd
     return _r(rnd, a), _r(rnd, u), h, y
 
 
-def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d, rnd=None) -> dict:
+def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d, rnd=None,
+                    fp8: bool = False) -> dict:
     """Each expert applied to its own contiguous segment of the permuted rows."""
+    expert = swiglu_expert_fp8 if fp8 else swiglu_expert
     N = x_perm.shape[0]
     f = W_g.shape[1]
     d_out = W_d.shape[1]
@@ -222,8 +271,8 @@ def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d, rnd=
     for e in range(W_g.shape[0]):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi > lo:
-            A[lo:hi], U[lo:hi], H[lo:hi], Y[lo:hi] = swiglu_expert(x_perm[lo:hi], W_g[e], W_u[e],
-                                                                   W_d[e], rnd)
+            A[lo:hi], U[lo:hi], H[lo:hi], Y[lo:hi] = expert(x_perm[lo:hi], W_g[e], W_u[e],
+                                                            W_d[e], rnd)
     return {"A": A, "U": U, "H": H, "Y_perm": Y}
 
 
@@ -245,7 +294,7 @@ def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
 
 def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                   logits: np.ndarray | None = None, idx: np.ndarray | None = None,
-                  rnd=None, aux: tuple | None = None) -> dict:
+                  rnd=None, aux: tuple | None = None, fp8: bool = False) -> dict:
     """Full forward of the layer from fp64 copies of the inputs.
 
     ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
@@ -260,10 +309,11 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
         r = _regate(r, logits, idx, mode, inp.get("b"), z_coef)
     disp = dispatch(r["idx"], E)
     x_perm = x[disp["perm_token"]]
-    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"], rnd)
+    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"], rnd, fp8)
     shared = None
     if "Ws_g" in inp:
-        shared = swiglu_expert(x, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)
+        shared = (swiglu_expert_fp8 if fp8 else swiglu_expert)(x, inp["Ws_g"], inp["Ws_u"],
+                                                               inp["Ws_d"], rnd)
     out = combine(ex["Y_perm"], r["gate"], disp["slot_to_row"],
                   None if shared is None else shared[3], rnd)
     res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
@@ -547,14 +597,15 @@ def bias_update_proportional(counts: np.ndarray, b: np.ndarray, T: int, k: int,
 # ---------------------------------------------------------------------------------------
 # sampled evaluation for workloads too large to run whole on the CPU
 
-def token_forward(inp: dict, t: int, experts, gates, rnd=None) -> np.ndarray:
+def token_forward(inp: dict, t: int, experts, gates, rnd=None, fp8: bool = False) -> np.ndarray:
     """out_t for one token given its chosen experts and gates."""
+    expert = swiglu_expert_fp8 if fp8 else swiglu_expert
     x_t = inp["x"][t:t + 1]
     out = np.zeros((1, inp["x"].shape[1]))
     for e, g in zip(experts, gates):
-        out += g * swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)[3]
+        out += g * expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)[3]
     if "Ws_g" in inp:
-        out += swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)[3]
+        out += expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)[3]
     return _r(rnd, out[0])
 
 

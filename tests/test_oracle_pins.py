@@ -431,3 +431,48 @@ def test_aux_losses_gradient_matches_finite_differences(mode):
         am = O.aux_losses(lm, idx, mode, L, *coef)
         num[ix] = ((ap["switch"] + ap["seq"]) - (am["switch"] + am["seq"])) / (2 * h)
     np.testing.assert_allclose(ana, num, rtol=1e-6, atol=1e-9)
+
+
+# -------------------------------------------------------------------- FP8 quantisation
+
+def test_e4m3_round_matches_library_conversion():
+    """Round to nearest even on 4 significant bits with E4M3 subnormals equals torch's
+    float8_e4m3fn conversion (a library routine) over the finite range."""
+    import torch
+    rng = np.random.default_rng(21)
+    scale = (2.0 ** rng.integers(-12, 9, 20000)).astype(np.float32)
+    vals = (rng.uniform(-1, 1, 20000).astype(np.float32) * scale)
+    vals = vals[np.abs(vals) <= 464.0]
+    halfway = np.array([0.5625, 1.0625, 1.1875, 3.25 + 0.125, 2.0 ** -9 * 1.5, 440.0, 464.0 - 1e-3],
+                       dtype=np.float32)  # exact midpoints and near-max values
+    allv = np.concatenate([vals, halfway, -halfway, np.float32([0.0])])
+    want = torch.from_numpy(allv).to(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(O.e4m3_round(allv.astype(np.float64)), want)
+
+
+def test_rowwise_fp8_quantisation_invariants():
+    rng = np.random.default_rng(22)
+    X = O.bf16_round(rng.standard_normal((50, 64)) * rng.uniform(0.01, 100, (50, 1)))
+    X[3] = 0.0
+    q, sc = O.quantize_rows_fp8(X)
+    assert np.all(np.abs(q) <= 448.0)
+    amax_pos = np.argmax(np.abs(X), axis=1)
+    live = np.abs(X).max(axis=1) > 0
+    assert np.all(np.abs(q[np.arange(50), amax_pos])[live] == 448.0)  # the row maximum maps to 448
+    assert np.all(q[3] == 0.0) and sc[3] == 1.0
+    assert np.all(O.e4m3_round(q) == q)  # every code is an E4M3 value
+    deq = q * sc[:, None]
+    rel = np.abs(deq - X) / np.maximum(np.abs(X), 1e-30)
+    assert np.all((rel <= 2.0 ** -4 + 1e-12) | (np.abs(X) < 2.0 ** -6 * sc[:, None]))
+
+
+def test_fp8_expert_stays_close_to_bf16_expert():
+    """FP8 operands (3 mantissa bits, about 2% RMS rounding each) move an expert's output
+    by several percent through the two GEMMs and the SwiGLU."""
+    rng = np.random.default_rng(23)
+    x = O.bf16_round(rng.standard_normal((64, 128)))
+    Wg, Wu = (O.bf16_round(rng.standard_normal((96, 128)) / np.sqrt(128)) for _ in range(2))
+    Wd = O.bf16_round(rng.standard_normal((128, 96)) / np.sqrt(96))
+    y16 = O.swiglu_expert(x, Wg, Wu, Wd)[3]
+    y8 = O.swiglu_expert_fp8(x, Wg, Wu, Wd)[3]
+    assert np.linalg.norm(y8 - y16) / np.linalg.norm(y16) < 0.10  # measured 0.062
