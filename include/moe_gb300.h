@@ -185,6 +185,35 @@ int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int E, int64_t
                    size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_quantize_rows_fp8 - rowwise FP8 (E4M3) quantisation of a GEMM operand, the Apex-3
+ * stack's "fp8_rowwise" precision ("The whole stack, in the open", "Run it yourself":
+ * --precision fp8_rowwise; KempnerForge "Features": FP8 via E4M3). Reading: per row,
+ * scale[r] = fp32(amax_r / 448) (1 for an all-zero row), Q[r,c] = E4M3(fp32(X[r,c] /
+ * scale[r])), round to nearest even, saturating at +-448; both divisions IEEE fp32.
+ * In : X [rows, cols] bf16; rows_limit: device int64 or NULL; only rows below
+ *      min(rows, *rows_limit) are written (pass row_offsets + E for the padded layout).
+ * Out: Q [rows, cols] E4M3 codes (bytes); scale [rows] fp32. cols % 128 == 0.
+ */
+int moe_quantize_rows_fp8(const moe_bf16* X, const int64_t* rows_limit, int64_t rows, int cols,
+                          uint8_t* Q, float* scale, moe_stream_t stream);
+
+/*
+ * moe_expert_fwd_fp8 - moe_expert_fwd with E4M3 GEMM operands (tcgen05 kind::f8f6f4, fp32
+ * accumulation). Each product is dequantised in the epilogue by its A-row scale and its
+ * B-row (output-channel) scale; a, u, h, y are bf16 as in moe_expert_fwd. h is quantised
+ * per row (into Hq, sH) before the down projection.
+ * In : Xq [rows, d] codes and sX [rows] (moe_quantize_rows_fp8 of the expert-major rows);
+ *      Wgq, Wuq [E f, d] codes with sWg, sWu [E f]; Wdq [E d, f] codes with sWd [E d]
+ *      (moe_quantize_rows_fp8 of the weights viewed as [E f, d] and [E d, f]).
+ * Out: A, U, H [rows, f] bf16; Hq [rows, f] codes and sH [rows]; Y [rows, d] bf16.
+ */
+int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int64_t* row_offsets, int E,
+                       int64_t rows, int d, int f, const uint8_t* Wgq, const float* sWg,
+                       const uint8_t* Wuq, const float* sWu, const uint8_t* Wdq,
+                       const float* sWd, moe_bf16* A, moe_bf16* U, moe_bf16* H, uint8_t* Hq,
+                       float* sH, moe_bf16* Y, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_combine - gate-weighted sum of the expert outputs (C1).
  * Definition: out[t] = sum_{i<k} topk_gate[t,i] * Y_perm[slot_to_row[t,i]] + Y_shared[t],
  * summed in fp32 in slot order, shared term last, one bf16 rounding. Source: section 2.5

@@ -611,7 +611,7 @@ def token_forward(inp: dict, t: int, experts, gates, rnd=None, fp8: bool = False
 
 def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, k: int,
                    dY_t: np.ndarray, z_coef: float, T: int, rnd=None,
-                   dl_extra_t: np.ndarray | None = None) -> dict:
+                   dl_extra_t: np.ndarray | None = None, fp8: bool = False) -> dict:
     """Gradient rows of one token: dx_t, dg_t and the router logit gradient for it.
 
     A token's dx depends only on its own routing, experts and upstream gradient, so it can
@@ -625,15 +625,16 @@ def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, 
     gate = r["gate"][0]
     dx = np.zeros((1, x_t.shape[1]))
     dg = np.zeros((1, k))
+    expert = swiglu_expert_fp8 if fp8 else swiglu_expert
     for i, e in enumerate(experts):
-        a, u, h, y = swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)
+        a, u, h, y = expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)
         dg[0, i] = float(np.sum(dY_t * y[0]))
         dH = _r(rnd, gate[i] * dY_t[None, :]) @ inp["W_d"][e]
         dA, dU = swiglu_backward(dH, a, u)
         dA, dU = _r(rnd, dA), _r(rnd, dU)
         dx += _r(rnd, dA @ inp["W_g"][e] + dU @ inp["W_u"][e])
     if "Ws_g" in inp:
-        a, u, h, y = swiglu_expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)
+        a, u, h, y = expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)
         dA, dU = swiglu_backward(dY_t[None, :] @ inp["Ws_d"], a, u)
         dA, dU = _r(rnd, dA), _r(rnd, dU)
         dx += _r(rnd, dA @ inp["Ws_g"] + dU @ inp["Ws_u"])
@@ -643,8 +644,17 @@ def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, 
     return {"dx": _r(rnd, dx[0]), "dg": dg[0], "dlogits": rb["dlogits"][0]}
 
 
+def _gemm_operands(X, Wg, Wu, fp8):
+    """The operands the gate/up products see: the bf16 values, or their E4M3 rowwise
+    dequantisations when fp8."""
+    if fp8:
+        return fp8_dequant_rows(X), fp8_dequant_rows(Wg), fp8_dequant_rows(Wu)
+    return X, Wg, Wu
+
+
 def expert_weight_grad_entries(inp: dict, e: int, tokens: np.ndarray, slots_gate: np.ndarray,
-                               dY: np.ndarray, entries_d, entries_gu, rnd=None) -> dict:
+                               dY: np.ndarray, entries_d, entries_gu, rnd=None,
+                               fp8: bool = False) -> dict:
     """Chosen entries of dW_d[e], dW_g[e] and dW_u[e].
 
     ``tokens`` are the tokens routed to expert e in ascending order and ``slots_gate`` their
@@ -654,14 +664,13 @@ def expert_weight_grad_entries(inp: dict, e: int, tokens: np.ndarray, slots_gate
     dYp = _r(rnd, slots_gate[:, None] * dY[tokens])
     Wg, Wu, Wd = inp["W_g"][e], inp["W_u"][e], inp["W_d"][e]
     res = {"dW_d": [], "dW_g": [], "dW_u": []}
+    Xo, Wgo, Wuo = _gemm_operands(X, Wg, Wu, fp8)
     for (i, j) in entries_d:
-        a = X @ Wg[j]
-        u = X @ Wu[j]
+        a, u = Xo @ Wgo[j], Xo @ Wuo[j]
         h = _r(rnd, silu(a) * u)
         res["dW_d"].append(float(_r(rnd, np.sum(dYp[:, i] * h))))
     for (j, i) in entries_gu:
-        a = _r(rnd, X @ Wg[j])
-        u = _r(rnd, X @ Wu[j])
+        a, u = _r(rnd, Xo @ Wgo[j]), _r(rnd, Xo @ Wuo[j])
         dh = dYp @ Wd[:, j]
         da, du = swiglu_backward(dh, a, u)
         res["dW_g"].append(float(_r(rnd, np.sum(_r(rnd, da) * X[:, i]))))
@@ -669,17 +678,19 @@ def expert_weight_grad_entries(inp: dict, e: int, tokens: np.ndarray, slots_gate
     return res
 
 
-def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu, rnd=None) -> dict:
+def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu, rnd=None,
+                               fp8: bool = False) -> dict:
     """Chosen entries of the shared expert's weight gradients (every token, weight 1)."""
     X = inp["x"]
     Wg, Wu, Wd = inp["Ws_g"], inp["Ws_u"], inp["Ws_d"]
     res = {"dWs_d": [], "dWs_g": [], "dWs_u": []}
+    Xo, Wgo, Wuo = _gemm_operands(X, Wg, Wu, fp8)
     for (i, j) in entries_d:
-        h = _r(rnd, silu(X @ Wg[j]) * (X @ Wu[j]))
+        a, u = Xo @ Wgo[j], Xo @ Wuo[j]
+        h = _r(rnd, silu(a) * u)
         res["dWs_d"].append(float(_r(rnd, np.sum(dY[:, i] * h))))
     for (j, i) in entries_gu:
-        a = _r(rnd, X @ Wg[j])
-        u = _r(rnd, X @ Wu[j])
+        a, u = _r(rnd, Xo @ Wgo[j]), _r(rnd, Xo @ Wuo[j])
         da, du = swiglu_backward(dY @ Wd[:, j], a, u)
         res["dWs_g"].append(float(_r(rnd, np.sum(_r(rnd, da) * X[:, i]))))
         res["dWs_u"].append(float(_r(rnd, np.sum(_r(rnd, du) * X[:, i]))))

@@ -33,6 +33,7 @@ class MoEConfig:
     aux_switch: float = 0.0  # Switch-style load-balancing loss coefficient (0 = off)
     aux_seq: float = 0.0     # sequence-wise load-balancing loss coefficient (0 = off)
     seq_len: int = 0         # tokens per sequence for the sequence-wise loss
+    precision: str = "bf16"  # expert forward GEMM operands: "bf16" or "fp8" (E4M3 rowwise)
 
     @property
     def has_aux(self) -> bool:
@@ -89,4 +90,8 @@ C5 = MoEConfig("apex3_T49152_d2048_E64_k4_f1280_proportional", T=49152, d=2048, 
 C6 = C4.with_(name="large_T65536_d4096_E64_k8_f1536_shared3072_auxlosses", aux_switch=1e-3,
               aux_seq=1e-3, seq_len=4096)
 
-CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5, "C6": C6}
+# The large layer with the experts' forward GEMMs on E4M3 rowwise-scaled operands (the Apex-3
+# stack's fp8_rowwise precision); the backward stays bf16.
+C7 = C4.with_(name="large_T65536_d4096_E64_k8_f1536_shared3072_fp8fwd", precision="fp8")
+
+CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5, "C6": C6, "C7": C7}

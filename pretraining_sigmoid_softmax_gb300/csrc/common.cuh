@@ -22,6 +22,10 @@ int sm_count();
 // True when the current device is an sm_103 part (the only target of this library).
 bool device_supported();
 
+// Rowwise E4M3 quantisation of rows [0, min(rows, *limit)) of X (limit may be null); see fp8.cu.
+int launch_quantize_rows_fp8(const __nv_bfloat16* X, const int64_t* limit, int64_t rows, int cols,
+                             uint8_t* Q, float* S, cudaStream_t st);
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
@@ -171,6 +175,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T for one 128 x N x 32 E4M3 step, fp32 accumulate.
+__device__ __forceinline__ void umma_fp8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
@@ -211,13 +226,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return desc;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, M = 128 (one CTA) or 256 (a
-// CTA pair).
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, uint32_t m, bool a_mn_major,
-                                                  bool b_mn_major) {
+// Instruction descriptor with fp32 D, M = 128 (one CTA) or 256 (a CTA pair). kind::f16 with
+// bf16 A/B (format 1), or kind::f8f6f4 with E4M3 A/B (format 0).
+__host__ __device__ constexpr uint32_t idesc_mma(uint32_t n, uint32_t m, bool a_mn_major,
+                                                 bool b_mn_major, bool fp8 = false) {
     return (1u << 4)                       // D format fp32
-           | (1u << 7)                     // A format bf16
-           | (1u << 10)                    // B format bf16
+           | ((fp8 ? 0u : 1u) << 7)        // A format: bf16 (kind::f16) or E4M3 (kind::f8f6f4)
+           | ((fp8 ? 0u : 1u) << 10)       // B format
            | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((n >> 3) << 17)                // N / 8
            | ((m >> 4) << 24);             // M / 16
@@ -285,6 +300,17 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The 256 x N x 32 E4M3 step of a CTA pair (operands split as for umma_bf16_pair).
+__device__ __forceinline__ void umma_fp8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

@@ -42,15 +42,18 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
+constexpr int BK = 64;        // bf16 K elements per stage (128 bytes per row)
+constexpr int BK_FP8 = 128;   // E4M3 K elements per stage (also 128 bytes per row)
 constexpr int kThreads = 256;
 constexpr int kSmemBudget = 200 * 1024;
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
 
 template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
-          bool PAIR_ = false>
+          bool PAIR_ = false, bool FP8_ = false>
 struct Cfg {
+    static constexpr bool FP8 = FP8_;        // E4M3 operands with row / column scales
+    static constexpr int KB = FP8 ? BK_FP8 : BK;  // K elements per stage
     static constexpr int BN = BN_;           // output columns per tile (per B matrix if DUAL)
     static constexpr bool A_MN = A_MN_;
     static constexpr bool B_MN = B_MN_;
@@ -62,8 +65,8 @@ struct Cfg {
     static constexpr int MMA_N = DUAL ? 2 * BN : BN;         // accumulator columns per row
     static constexpr int BROWS = PAIR ? MMA_N / 2 : MMA_N;   // B rows staged by this CTA
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;        // rows of one (pair) tile
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BROWS * BK * 2;
+    static constexpr int A_BYTES = BM * 128;     // 128-byte rows in either type
+    static constexpr int B_BYTES = BROWS * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // this CTA's bytes per K block
     static constexpr int STAGES = (kSmemBudget / STAGE_BYTES) > 6 ? 6 : (kSmemBudget / STAGE_BYTES);
     static constexpr int ACC_COLS = MMA_N;
@@ -71,7 +74,8 @@ struct Cfg {
     // DUAL: the W_g and W_u boxes form one 2*BN-row B tile (on one CTA, back to back; in a
     // pair, W_g on the leader and W_u on the peer), so one instruction fills gate columns
     // [0, BN) and up columns [BN, 2BN).
-    static constexpr uint32_t IDESC = idesc_bf16(MMA_N, TILE_M, A_MN, B_MN);
+    static constexpr uint32_t IDESC = idesc_mma(MMA_N, TILE_M, A_MN, B_MN, FP8);
+    static_assert(!FP8 || (!A_MN && !B_MN && !WGRAD && !TWO_K), "FP8: forward K-major GEMMs");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "tensor memory columns");
     static_assert(BN % 64 == 0 && MMA_N <= 256 && BROWS % 64 == 0, "tile width");
     static constexpr size_t MISC_BYTES = 512 + sizeof(int64_t) * (kMaxExperts + 1) +
@@ -96,6 +100,9 @@ struct Params {
     __nv_bfloat16* out2;
     const __nv_bfloat16* in0;  // SwiGLU backward: saved a
     const __nv_bfloat16* in1;  // SwiGLU backward: saved u
+    const float* sa;           // FP8: scale of each A row (indexed by the global row)
+    const float* sb0;          // FP8: scale of each B row (output channel), first B operand
+    const float* sb1;          // FP8: second B operand (W_u of G1)
     int ld_out;
     int* status;
     uint64_t wait_limit_ns;
@@ -218,7 +225,7 @@ __device__ __forceinline__ TileInfo decode(int64_t tile, const Params& P, const 
             ti.e = last_le(S.offs, P.E, ti.m0);
             ti.row_end = S.offs[ti.e + 1];
         }
-        ti.k_iters = (P.K0 + (C::TWO_K ? P.K1 : 0)) / BK;
+        ti.k_iters = (P.K0 + (C::TWO_K ? P.K1 : 0)) / C::KB;
     }
     return ti;
 }
@@ -249,7 +256,7 @@ __device__ __forceinline__ void issue_loads(const TileInfo& ti, int kb, uint32_t
         for (int j = 0; j < C::BROWS / 64; ++j)
             tma_load<C>(b_dst + j * 8192, mb0, bar, ti.n0 + bhalf + 64 * j, krow);
     } else {
-        int kk = kb * BK;
+        int kk = kb * C::KB;
         const CUtensorMap* ma = ma0;
         const CUtensorMap* mb = mb0;
         int kper = P.kb_per_expert;
@@ -281,6 +288,35 @@ __device__ __forceinline__ void issue_loads(const TileInfo& ti, int kb, uint32_t
 __device__ __forceinline__ uint4 pack_chunk8(const float* v) {
     return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                       pack_bf16x2(v[6], v[7]));
+}
+
+// FP8 dequantisation of a 32-column accumulator chunk: value * scale(A row) * scale(B row
+// of each output column). With dual=true, `a` takes the first B operand's column scales
+// and `b` the second's (G1: gate and up); otherwise only `a` is scaled.
+__device__ __forceinline__ void fp8_scale(float* a, float* b, const Params& P, int64_t row,
+                                          const TileInfo& ti, int c, bool dual = true) {
+    const float sr = __ldg(P.sa + row);
+    const int64_t col0 = (int64_t)ti.e * P.N + ti.n0 + c;
+    const float4* s0 = reinterpret_cast<const float4*>(P.sb0 + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 v = __ldg(s0 + q);
+        a[4 * q] *= sr * v.x;
+        a[4 * q + 1] *= sr * v.y;
+        a[4 * q + 2] *= sr * v.z;
+        a[4 * q + 3] *= sr * v.w;
+    }
+    if (dual) {
+        const float4* s1 = reinterpret_cast<const float4*>(P.sb1 + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = __ldg(s1 + q);
+            b[4 * q] *= sr * v.x;
+            b[4 * q + 1] *= sr * v.y;
+            b[4 * q + 2] *= sr * v.z;
+            b[4 * q + 3] *= sr * v.w;
+        }
+    }
 }
 
 // Saved a and u (32 bf16 each) of one 32-column chunk of this thread's row.
@@ -338,8 +374,10 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
                     for (int j = 0; j < 32; ++j) {
                         av[j] = __uint_as_float(g[j]);
                         uv[j] = __uint_as_float(u[j]);
-                        hv[j] = av[j] / (1.0f + __expf(-av[j])) * uv[j];
                     }
+                    if constexpr (C::FP8) fp8_scale(av, uv, P, row, ti, c);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) hv[j] = av[j] / (1.0f + __expf(-av[j])) * uv[j];
                     uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
                     uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
                     uint4* dh = reinterpret_cast<uint4*>(P.out2 + base + c);
@@ -395,6 +433,7 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if constexpr (C::FP8) fp8_scale(v, v, P, row, ti, c, /*dual=*/false);
                     uint4* dst = reinterpret_cast<uint4*>(P.out0 + base + c);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) dst[q] = pack_chunk8(v + 8 * q);
@@ -534,13 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a_s = smem_u32(S.a + (size_t)stage * C::A_BYTES);
                 const uint32_t b_s = smem_u32(S.b + (size_t)stage * C::B_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
+                for (int kk = 0; kk < 4; ++kk) {  // 4 instructions of 32 bytes of K
                     const uint64_t adesc = C::A_MN ? sdesc_sw128(a_s + kk * 2048, 8192, 1024)
                                                    : sdesc_sw128(a_s + kk * 32, 16, 1024);
                     const uint64_t bdesc = C::B_MN ? sdesc_sw128(b_s + kk * 2048, 8192, 1024)
                                                    : sdesc_sw128(b_s + kk * 32, 16, 1024);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (C::PAIR) umma_bf16_pair(d_tmem, adesc, bdesc, C::IDESC, acc);
+                    if constexpr (C::PAIR && C::FP8) umma_fp8_pair(d_tmem, adesc, bdesc, C::IDESC, acc);
+                    else if constexpr (C::PAIR) umma_bf16_pair(d_tmem, adesc, bdesc, C::IDESC, acc);
+                    else if constexpr (C::FP8) umma_fp8(d_tmem, adesc, bdesc, C::IDESC, acc);
                     else umma_bf16(d_tmem, adesc, bdesc, C::IDESC, acc);
                 }
                 if constexpr (C::PAIR) umma_commit_pair(smem_u32(&S.empty[stage]), 0x3);
@@ -629,19 +670,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] matrix, 128-byte swizzled boxes.
+// 2-D map over a row-major [outer, inner] matrix of bf16 (or of bytes, for E4M3 codes),
+// 128-byte swizzled boxes.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, bool bytes = false) {
     auto enc = get_encoder();
     if (!enc || !base) return false;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
+    cuuint64_t strides[1] = {inner * (bytes ? 1 : 2)};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <class C>
@@ -694,6 +736,10 @@ template <int BN> using CfgDgrad2 = Cfg<BN, false, true, false, kEpiStore, true,
 using CfgDgrad2P = Cfg<256, false, true, false, kEpiStore, true, false, true>;
 template <int BN> using CfgWgrad = Cfg<BN, true, true, false, kEpiStore, false, true>;
 using CfgWgradP = Cfg<256, true, true, false, kEpiStore, false, true, true>;
+// E4M3 forward GEMMs (rowwise scales)
+using CfgG1P8 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false, true, true>;
+using CfgStoreKP8 = Cfg<256, false, false, false, kEpiStore, false, false, true, true>;
+using CfgStoreK8 = Cfg<128, false, false, false, kEpiStore, false, false, false, true>;
 
 Params base_params(const int64_t* row_offsets, int64_t rows, int E) {
     Params P{};
@@ -867,5 +913,63 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         else
             rc = launch<CfgWgrad<128>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 128), st);
     }
+    return rc;
+}
+
+extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int64_t* row_offsets,
+                                  int E, int64_t rows, int d, int f, const uint8_t* Wgq,
+                                  const float* sWg, const uint8_t* Wuq, const float* sWu,
+                                  const uint8_t* Wdq, const float* sWd, moe_bf16* A, moe_bf16* U,
+                                  moe_bf16* H, uint8_t* Hq, float* sH, moe_bf16* Y, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!Xq || !sX || !Wgq || !sWg || !Wuq || !sWu || !Wdq || !sWd || !A || !U || !H || !Hq ||
+        !sH || !Y)
+        return MOE_ERR_INVALID_ARG;
+    if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
+    const void* ptrs[9] = {Xq, Wgq, Wuq, Wdq, A, U, H, Hq, Y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    if (!device_status_word()) return MOE_ERR_LAUNCH;
+    cudaStream_t st = (cudaStream_t)stream;
+    CUtensorMap mx, mwg, mwu, mh, mwd;
+    if (!make_map(&mx, Xq, d, rows, 128, 128, true) ||
+        !make_map(&mwg, Wgq, d, (uint64_t)E * f, 128, 128, true) ||
+        !make_map(&mwu, Wuq, d, (uint64_t)E * f, 128, 128, true) ||
+        !make_map(&mh, Hq, f, rows, 128, 128, true) ||
+        !make_map(&mwd, Wdq, f, (uint64_t)E * d, 128, 128, true))
+        return MOE_ERR_LAUNCH;
+    // G1 on E4M3 codes: a, u, h
+    Params P = base_params(row_offsets, rows, E);
+    P.N = f;
+    P.K0 = d;
+    P.out0 = reinterpret_cast<__nv_bfloat16*>(A);
+    P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
+    P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
+    P.ld_out = f;
+    P.sa = sX;
+    P.sb0 = sWg;
+    P.sb1 = sWu;
+    int rc = launch<CfgG1P8>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st);
+    if (rc != MOE_OK) return rc;
+    // h rows -> E4M3 codes for the down projection
+    rc = launch_quantize_rows_fp8(reinterpret_cast<const __nv_bfloat16*>(H),
+                                  row_offsets ? row_offsets + E : nullptr, rows, f, Hq, sH, st);
+    if (rc != MOE_OK) return rc;
+    // G2 on E4M3 codes: y
+    Params Q = base_params(row_offsets, rows, E);
+    Q.N = d;
+    Q.K0 = f;
+    Q.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
+    Q.ld_out = d;
+    Q.sa = sH;
+    Q.sb0 = sWd;
+    if (d % 256 == 0)
+        rc = launch<CfgStoreKP8>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st);
+    else
+        rc = launch<CfgStoreK8>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st);
     return rc;
 }

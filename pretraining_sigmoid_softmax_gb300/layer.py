@@ -28,6 +28,7 @@ class MoEShape:
     aux_switch: float = 0.0
     aux_seq: float = 0.0
     seq_len: int = 0
+    fp8: bool = False
 
     @property
     def has_aux(self) -> bool:
@@ -36,7 +37,7 @@ class MoEShape:
     @classmethod
     def from_config(cls, cfg) -> "MoEShape":
         return cls(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_shared, cfg.mode_id, cfg.z_coef,
-                   cfg.aux_switch, cfg.aux_seq, cfg.seq_len or cfg.T)
+                   cfg.aux_switch, cfg.aux_seq, cfg.seq_len or cfg.T, cfg.precision == "fp8")
 
 
 def _empty(shape, dtype, dev):
@@ -76,6 +77,19 @@ class MoEPlan:
             self.Us = _empty((T, fs), bf, dev)
             self.Hs = _empty((T, fs), bf, dev)
             self.Ys = _empty((T, d), bf, dev)
+        if s.fp8:  # E4M3 codes and fp32 scales of every forward GEMM operand
+            u8 = torch.uint8
+            self.X8, self.sX = _empty((R, d), u8, dev), _empty((R,), f32, dev)
+            self.H8, self.sH = _empty((R, f), u8, dev), _empty((R,), f32, dev)
+            self.Wg8, self.sWg = _empty((E, f, d), u8, dev), _empty((E * f,), f32, dev)
+            self.Wu8, self.sWu = _empty((E, f, d), u8, dev), _empty((E * f,), f32, dev)
+            self.Wd8, self.sWd = _empty((E, d, f), u8, dev), _empty((E * d,), f32, dev)
+            if fs:
+                self.x8, self.sx = _empty((T, d), u8, dev), _empty((T,), f32, dev)
+                self.Hs8, self.sHs = _empty((T, fs), u8, dev), _empty((T,), f32, dev)
+                self.Wsg8, self.sWsg = _empty((1, fs, d), u8, dev), _empty((fs,), f32, dev)
+                self.Wsu8, self.sWsu = _empty((1, fs, d), u8, dev), _empty((fs,), f32, dev)
+                self.Wsd8, self.sWsd = _empty((1, d, fs), u8, dev), _empty((d,), f32, dev)
         if s.has_aux:
             self.aux_loss = torch.zeros((2,), dtype=f32, device=dev)
             self.aux_f = _empty((E + (T // s.seq_len) * E,), f32, dev)
@@ -125,7 +139,10 @@ class MoEPlan:
         if s.has_aux:
             n += 2 + (1 if backward else 0)                 # balancing losses (+ gradient)
         n += 5                                              # permute
-        n += 2 + (2 if s.f_shared else 0)                   # expert forward (G1, G2)
+        if s.fp8:  # quantise X, W_g, W_u, W_d; G1, quantise H, G2 (shared: the same)
+            n += 7 + (7 if s.f_shared else 0)
+        else:
+            n += 2 + (2 if s.f_shared else 0)               # expert forward (G1, G2)
         n += 1                                              # combine
         if backward:
             n += 2                                          # combine backward + padding rows
@@ -151,13 +168,32 @@ class MoEPlan:
                              s.aux_seq, self.aux_loss, self.aux_f, self.ws, stream)
         ops.moe_permute(self.topk_idx, x, s.E, self.counts, self.offsets, self.row_offsets,
                         self.perm_token, self.slot_to_row, self.X_perm, self.ws, stream)
-        self._gemm(ops.moe_expert_fwd, self.X_perm, self.row_offsets, W_g, W_u, W_d, self.A,
-                   self.U, self.H, self.Y_perm, self.ws, stream=stream)
         ys = None
-        if s.f_shared:
-            self._gemm(ops.moe_expert_fwd, x, None, Ws_g[None], Ws_u[None], Ws_d[None], self.As,
-                       self.Us, self.Hs, self.Ys, self.ws, stream=stream)
-            ys = self.Ys
+        if s.fp8:
+            q = ops.moe_quantize_rows_fp8
+            q(W_g, None, self.Wg8, self.sWg, stream)
+            q(W_u, None, self.Wu8, self.sWu, stream)
+            q(W_d, None, self.Wd8, self.sWd, stream)
+            q(self.X_perm, self.row_offsets[s.E:], self.X8, self.sX, stream)
+            self._gemm(ops.moe_expert_fwd_fp8, self.X8, self.sX, self.row_offsets, self.Wg8,
+                       self.sWg, self.Wu8, self.sWu, self.Wd8, self.sWd, self.A, self.U, self.H,
+                       self.H8, self.sH, self.Y_perm, self.ws, stream=stream)
+            if s.f_shared:
+                q(Ws_g, None, self.Wsg8, self.sWsg, stream)
+                q(Ws_u, None, self.Wsu8, self.sWsu, stream)
+                q(Ws_d, None, self.Wsd8, self.sWsd, stream)
+                q(x, None, self.x8, self.sx, stream)
+                self._gemm(ops.moe_expert_fwd_fp8, self.x8, self.sx, None, self.Wsg8, self.sWsg,
+                           self.Wsu8, self.sWsu, self.Wsd8, self.sWsd, self.As, self.Us, self.Hs,
+                           self.Hs8, self.sHs, self.Ys, self.ws, stream=stream)
+                ys = self.Ys
+        else:
+            self._gemm(ops.moe_expert_fwd, self.X_perm, self.row_offsets, W_g, W_u, W_d, self.A,
+                       self.U, self.H, self.Y_perm, self.ws, stream=stream)
+            if s.f_shared:
+                self._gemm(ops.moe_expert_fwd, x, None, Ws_g[None], Ws_u[None], Ws_d[None],
+                           self.As, self.Us, self.Hs, self.Ys, self.ws, stream=stream)
+                ys = self.Ys
         ops.moe_combine(self.Y_perm, self.topk_gate, self.slot_to_row, ys, self.out, stream)
         return self.out
 

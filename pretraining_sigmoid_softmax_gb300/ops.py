@@ -113,6 +113,27 @@ def moe_expert_fwd(X, row_offsets, W_g, W_u, W_d, A, U, H, Y, ws, stream=None):
            "moe_expert_fwd")
 
 
+def moe_quantize_rows_fp8(X, rows_limit, Q, scale, stream=None):
+    """Rowwise E4M3 codes (uint8) and fp32 scales of a [rows, cols] bf16 matrix."""
+    X2 = X.reshape(-1, X.shape[-1])
+    rows, cols = X2.shape
+    _contig(X, Q, scale)
+    _check(_lib.load().moe_quantize_rows_fp8(_p(X), _p(rows_limit), rows, cols, _p(Q), _p(scale),
+                                             _stream(stream)), "moe_quantize_rows_fp8")
+
+
+def moe_expert_fwd_fp8(Xq, sX, row_offsets, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y,
+                       ws, stream=None):
+    rows, d = Xq.shape
+    E, f, _ = Wgq.shape
+    _contig(Xq, sX, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y)
+    _check(_lib.load().moe_expert_fwd_fp8(_p(Xq), _p(sX), _p(row_offsets), E, rows, d, f,
+                                          _p(Wgq), _p(sWg), _p(Wuq), _p(sWu), _p(Wdq), _p(sWd),
+                                          _p(A), _p(U), _p(H), _p(Hq), _p(sH), _p(Y), _p(ws),
+                                          0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_expert_fwd_fp8")
+
+
 def moe_combine(Y_perm, topk_gate, slot_to_row, Y_shared, out, stream=None):
     T, k = topk_gate.shape
     d = Y_perm.shape[1]

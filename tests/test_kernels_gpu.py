@@ -404,3 +404,80 @@ def test_router_backward_adds_the_extra_logit_gradient():
     rb = O.router_backward(h64(dg), ref, h64(x), h64(W_r), "sigmoid", 0.0, dl_extra=h64(extra))
     assert_close(dl, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
     assert_close(dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)
+
+
+# ------------------------------------------------------------------------------- FP8
+
+def _e4m3_values(codes_u8):
+    return h64(codes_u8.cpu().view(torch.float8_e4m3fn).float())
+
+
+def test_fp8_rowwise_quantisation_is_bit_exact():
+    g = torch.Generator().manual_seed(51)
+    X = randn_bf16((300, 512), g) * torch.rand(300, 1, generator=g).mul(50).to(torch.bfloat16)
+    X[7] = 0
+    Q = torch.empty(300, 512, dtype=torch.uint8, device="cuda")
+    S = torch.empty(300, device="cuda")
+    lim = torch.tensor([250], dtype=torch.int64, device="cuda")  # rows past 250 untouched
+    Q.fill_(0x7F)
+    ops.moe_quantize_rows_fp8(dev(X), lim, Q, S)
+    torch.cuda.synchronize()
+    q_ref, s_ref = O.quantize_rows_fp8(h64(X))
+    assert np.array_equal(S[:250].cpu().numpy().view(np.uint32), s_ref[:250].astype(np.float32).view(np.uint32))
+    assert np.array_equal(_e4m3_values(Q[:250]), q_ref[:250])
+    assert (Q[250:] == 0x7F).all()
+
+
+def _quantize(t):
+    rows = t.reshape(-1, t.shape[-1])
+    Q = torch.empty(rows.shape, dtype=torch.uint8, device="cuda")
+    S = torch.empty(rows.shape[0], device="cuda")
+    ops.moe_quantize_rows_fp8(dev(rows), None, Q, S)
+    return Q.view(t.shape), S
+
+
+@pytest.mark.parametrize("counts,d,f", [(None, 512, 256), ([300, 0, 129, 1, 513], 512, 256),
+                                        ([130, 5, 0], 384, 128)])
+def test_fp8_expert_forward_matches_oracle(counts, d, f):
+    g = torch.Generator().manual_seed(61 + d)
+    if counts is None:
+        rows, E, ro, segs = 700, 1, None, [(0, 700)]
+        X = randn_bf16((rows, d), g)
+    else:
+        E = len(counts)
+        ro = padded_offsets(counts)
+        rows = int(ro[-1]) + 128
+        X = torch.zeros(rows, d, dtype=torch.bfloat16)
+        segs = []
+        for e in range(E):
+            X[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g)
+            segs.append((int(ro[e]), int(ro[e]) + counts[e]))
+    W_g, W_u, W_d = _weights(E, d, f, g)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    A, U, H = (torch.full((rows, f), float("nan"), **bf) for _ in range(3))
+    Y = torch.full((rows, d), float("nan"), **bf)
+    Hq = torch.empty(rows, f, dtype=torch.uint8, device="cuda")
+    sH = torch.empty(rows, device="cuda")
+    ro_d = None if ro is None else dev(torch.from_numpy(ro))
+    Xq = torch.empty(rows, d, dtype=torch.uint8, device="cuda")
+    sX = torch.empty(rows, device="cuda")
+    ops.moe_quantize_rows_fp8(dev(X), None if ro_d is None else ro_d[E:], Xq, sX)
+    Wgq, sWg = _quantize(W_g)
+    Wuq, sWu = _quantize(W_u)
+    Wdq, sWd = _quantize(W_d)
+    ops.moe_expert_fwd_fp8(Xq, sX, ro_d, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y,
+                           _ws(rows, d, E, 1))
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    for e, (lo, hi) in enumerate(segs):
+        if hi == lo:
+            continue
+        a, u, h, y = O.swiglu_expert_fp8(h64(X[lo:hi]), h64(W_g[e]), h64(W_u[e]), h64(W_d[e]),
+                                         O.bf16_round)
+        assert_close(A[lo:hi], a, f"fp8 A e{e}")
+        assert_close(U[lo:hi], u, f"fp8 U e{e}")
+        assert_close(H[lo:hi], h, f"fp8 H e{e}")
+        assert_close(Y[lo:hi], y, f"fp8 Y e{e}")
+        # tensor-core result of the oracle's own E4M3 operands, dequantised in the epilogue
+        xq = O.fp8_dequant_rows(h64(X[lo:hi]))
+        assert_gemm_exact(A[lo:hi], xq, O.fp8_dequant_rows(h64(W_g[e])).T, f"fp8 A exact e{e}")

@@ -85,7 +85,8 @@ def full_parity(cfg, inp):
     idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
     i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
     aux = (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
-    fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND, aux=aux)
+    fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND, aux=aux,
+                          fp8=cfg.precision == "fp8")
     assert_close(plan.topk_gate, fwd["gate"], "gates", atol=1e-6, rtol=1e-5)
     if aux is not None:
         assert float(plan.aux_loss[0]) == pytest.approx(fwd["aux_switch"], rel=1e-5)
@@ -126,6 +127,8 @@ SMALL = [
     MoEConfig("aux_losses_softmax", T=768, d=256, E=8, k=2, f=128, f_shared=0, mode="softmax",
               seed=17, backward=True, bias_update=False, z_coef=1e-3, aux_switch=1e-2,
               aux_seq=1e-2, seq_len=384),
+    MoEConfig("fp8_forward_shared", T=1024, d=512, E=8, k=2, f=256, f_shared=256,
+              mode="sigmoid", seed=18, backward=True, bias_update=True, precision="fp8"),
 ]
 
 
@@ -160,7 +163,7 @@ def test_layer_is_bitwise_repeatable():
         assert torch.equal(r1[k], v), k
 
 
-@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5", "C6"])
+@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5", "C6", "C7"])
 def test_workload_sampled_parity(name):
     """Full-size workloads in the benchmark's launch configuration: routing, counts and
     permutation in full; out and dx on sampled tokens; weight-gradient entries of sampled
@@ -183,12 +186,13 @@ def test_workload_sampled_parity(name):
         assert float(plan.aux_loss[0]) == pytest.approx(a["switch"], rel=1e-5)
         assert float(plan.aux_loss[1]) == pytest.approx(a["seq"], rel=1e-5)
         dl_aux = O.aux_losses_backward(lg, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
+    fp8 = cfg.precision == "fp8"
     for j, t in enumerate(toks):
-        o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND)
+        o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND, fp8=fp8)
         assert_close(out[j], o, f"out[{t}]")
         tb = O.token_backward(lazy, int(t), lg[t], idx[t], cfg.mode, cfg.k,
                               O.to64(inp["dY"][t]), cfg.z_coef, cfg.T, rnd=RND,
-                              dl_extra_t=None if dl_aux is None else dl_aux[t])
+                              dl_extra_t=None if dl_aux is None else dl_aux[t], fp8=fp8)
         assert_close(dx[j], tb["dx"], f"dx[{t}]")
     counts = D["counts"]
     live = np.nonzero(counts)[0]
@@ -205,7 +209,7 @@ def test_workload_sampled_parity(name):
             {"x": O.to64(inp["x"][torch.from_numpy(tok_e)]), "W_g": lazy["W_g"],
              "W_u": lazy["W_u"], "W_d": lazy["W_d"]},
             e, np.arange(hi - lo), gates, O.to64(inp["dY"][torch.from_numpy(tok_e)]), ed, eg,
-            rnd=RND)
+            rnd=RND, fp8=fp8)
         got_d = [float(plan.dW_d[e, i, j]) for (i, j) in ed]
         got_g = [float(plan.dW_g[e, j, i]) for (j, i) in eg]
         got_u = [float(plan.dW_u[e, j, i]) for (j, i) in eg]
@@ -222,7 +226,7 @@ def test_workload_sampled_parity(name):
         eg = [(int(rng.integers(cfg.f_shared)), int(rng.integers(cfg.d))) for _ in range(6)]
         want = O.shared_weight_grad_entries({"x": O.to64(inp["x"]), "Ws_g": lazy["Ws_g"],
                                              "Ws_u": lazy["Ws_u"], "Ws_d": lazy["Ws_d"]},
-                                            O.to64(inp["dY"]), ed, eg, rnd=RND)
+                                            O.to64(inp["dY"]), ed, eg, rnd=RND, fp8=fp8)
         assert_close(np.array([float(plan.dWs_d[i, j]) for (i, j) in ed]), want["dWs_d"], "dWs_d",
                      reduction=True)
         assert_close(np.array([float(plan.dWs_g[j, i]) for (j, i) in eg]), want["dWs_g"], "dWs_g",
