@@ -18,7 +18,7 @@ LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 BUILD_DIR = os.path.join(HERE, "_build")
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
-SOURCES = ["status.cu", "route.cu", "permute.cu", "grouped_gemm.cu", "fp8.cu"]
+SOURCES = ["status.cu", "route.cu", "route_tc.cu", "permute.cu", "grouped_gemm.cu", "fp8.cu"]
 
 
 def nvcc_path() -> str:

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "sizes.h"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -756,6 +757,12 @@ int64_t token_tiles_max(int64_t rows, int N, int BN) { return cdiv(rows, BM) * (
 bool gemm_shape_ok(int d, int f) { return d % 128 == 0 && f % 128 == 0 && d > 0 && f > 0; }
 
 }  // namespace
+
+bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                       uint32_t box_inner, uint32_t box_outer) {
+    return make_map(m, base, inner, outer, box_inner, box_outer);
+}
+
 }  // namespace moe
 
 using namespace moe;

@@ -6,13 +6,14 @@
 // with no loss term. KempnerForge README, "Features": softmax top-k router and router
 // z-loss. Handbook summary, section 2.5: router logits in fp32.
 //
-// The logits are an fp32 SIMT contraction over d (the router has E <= 256 outputs per
-// token, too narrow for a tensor-core tile to pay, and fp32 is the stated router dtype).
-// Every output is one thread's sequential sum over d, so results are bitwise repeatable.
+// Routers of up to 128 experts run their two contractions (logits, W_r gradient) on the
+// tensor cores (route_tc.cu). Wider routers use the fp32 SIMT kernels here: every output is
+// one thread's sequential sum, so results are bitwise repeatable on either path.
 #include <cuda_runtime.h>
 #include <math.h>
 
 #include "common.cuh"
+#include "router.cuh"
 #include "sizes.h"
 
 namespace moe {
@@ -21,12 +22,11 @@ namespace {
 constexpr int kKC = 32;                  // d-chunk per smem stage
 constexpr int kThreads = 256;
 
-// Ordering used for the choice: larger value first, lower expert index on equal values.
 __device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
-    return v1 > v2 || (v1 == v2 && e1 < e2);
+    return route_better(v1, e1, v2, e2);
 }
 
-__device__ __forceinline__ float sigmoid_f(float l) { return 1.0f / (1.0f + expf(-l)); }
+__device__ __forceinline__ float sigmoid_f(float l) { return route_sigmoid(l); }
 
 // Logit tile of TM tokens x EP (padded) experts per CTA, 256 threads; each thread owns
 // TTOK tokens x EJ experts and sums over d sequentially (fixed order). The next 32-wide
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
     const float* __restrict__ topk_gate, const float* __restrict__ topk_score,
     const float* __restrict__ logits, const float* __restrict__ lse,
     const float* __restrict__ extra, int64_t T, int E, int k, int mode, float z_scale,
-    float* __restrict__ dlogits) {
+    float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dl3, int np) {
     const int lane = threadIdx.x % 32;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (t >= T) return;
@@ -280,23 +280,21 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
         S += __shfl_sync(0xffffffffu, my_s, i);
         gdg += __shfl_sync(0xffffffffu, my_g * my_dg, i);
     }
-    if (mode == MOE_MODE_SIGMOID) {
-        const float ds = (my_dg - gdg) / S;
-        const float v = ds * my_s * (1.f - my_s);
-        for (int e0 = 0; e0 < E; e0 += 32) {  // warp-uniform trip count
-            const int e = e0 + lane;
-            float out = 0.f;
+    // with dl3, the row is also written as three bf16 pieces [3][T][np] (zero past E)
+    const int ecount = dl3 ? np : E;
+    const float ds = (my_dg - gdg) / S;
+    const float vs = ds * my_s * (1.f - my_s);
+    const float l_se = mode == MOE_MODE_SIGMOID ? 0.f : lse[t];
+    for (int e0 = 0; e0 < ecount; e0 += 32) {  // warp-uniform trip count
+        const int e = e0 + lane;
+        float out = 0.f;
+        if (mode == MOE_MODE_SIGMOID) {
             for (int i = 0; i < k; ++i) {
                 const int ei = __shfl_sync(0xffffffffu, my_e, i);
-                const float vi = __shfl_sync(0xffffffffu, v, i);
+                const float vi = __shfl_sync(0xffffffffu, vs, i);
                 if (ei == e) out = vi;
             }
-            if (e < E) dlogits[t * E + e] = extra ? out + extra[t * E + e] : out;
-        }
-    } else {
-        const float l_se = lse[t];
-        for (int e0 = 0; e0 < E; e0 += 32) {
-            const int e = e0 + lane;
+        } else {
             float sel = 0.f;
             for (int i = 0; i < k; ++i) {
                 const int ei = __shfl_sync(0xffffffffu, my_e, i);
@@ -305,9 +303,20 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
             }
             if (e < E) {
                 const float p = expf(logits[t * E + e] - l_se);
-                const float v = p * (sel - gdg) + z_scale * l_se * p;
-                dlogits[t * E + e] = extra ? v + extra[t * E + e] : v;
+                out = p * (sel - gdg) + z_scale * l_se * p;
             }
+        }
+        if (e < E) {
+            if (extra) out += extra[t * E + e];
+            dlogits[t * E + e] = out;
+        }
+        if (dl3) {
+            __nv_bfloat16 p0, p1, p2;
+            split3_bf16(e < E ? out : 0.f, p0, p1, p2);
+            const int64_t i = t * np + e;
+            dl3[i] = p0;
+            dl3[T * np + i] = p1;
+            dl3[2 * T * np + i] = p2;
         }
     }
 }
@@ -578,18 +587,23 @@ extern "C" int moe_route(const moe_bf16* x, const float* W_r, const float* b, in
     if (!aligned16(x) || !aligned16(W_r)) return MOE_ERR_INVALID_ARG;
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     WsCarver wc(ws, ws_bytes);
-    double* zp = wc.take<double>(route_blocks(T));
+    const int epad = route_tc_epad(E);
+    int64_t nzp = route_blocks(T);
+    if (4 * route_tc_tiles(T) > nzp) nzp = 4 * route_tc_tiles(T);
+    double* zp = wc.take<double>(nzp);
+    __nv_bfloat16* w3 = epad ? wc.take<__nv_bfloat16>((size_t)3 * epad * d) : nullptr;
     if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     int rc;
     int64_t nb = 0;
-#define MOE_ROUTE_ARGS x, W_r, b, T, d, E, k, mode, logits, topk_idx, topk_gate, topk_score, lse, zp, &nb, st
-    if (E <= 16) rc = launch_route_fwd<16, 128, 4, 2>(MOE_ROUTE_ARGS);
-    else if (E <= 32) rc = launch_route_fwd<32, 128, 4, 4>(MOE_ROUTE_ARGS);
-    else if (E <= 64) rc = launch_route_fwd<64, 128, 8, 4>(MOE_ROUTE_ARGS);
-    else if (E <= 128) rc = launch_route_fwd<128, 128, 8, 8>(MOE_ROUTE_ARGS);
-    else rc = launch_route_fwd<256, 64, 8, 8>(MOE_ROUTE_ARGS);
-#undef MOE_ROUTE_ARGS
+    if (epad) {
+        rc = launch_route_logits_tc(reinterpret_cast<const __nv_bfloat16*>(x), W_r, b, T, d, E, k,
+                                    mode, logits, topk_idx, topk_gate, topk_score, lse, zp, &nb,
+                                    w3, st);
+    } else {
+        rc = launch_route_fwd<256, 64, 8, 8>(x, W_r, b, T, d, E, k, mode, logits, topk_idx,
+                                             topk_gate, topk_score, lse, zp, &nb, st);
+    }
     if (rc != MOE_OK) return rc;
     if (mode == MOE_MODE_SOFTMAX) {
         z_finalize_kernel<<<1, 32, 0, st>>>(zp, nb, T, z_coef, z_loss);
@@ -613,19 +627,34 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
     if (!aligned16(x) || !aligned16(dW_r)) return MOE_ERR_INVALID_ARG;
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     WsCarver wc(ws, ws_bytes);
-    const int64_t nsplit = route_bwd_splits(T);
+    const int np = route_tc_np(E);
+    int64_t nsplit = route_bwd_splits(T);
+    if (np && route_tc_splits_max(T) > nsplit) nsplit = route_tc_splits_max(T);
     float* part = wc.take<float>((size_t)nsplit * E * d);
+    __nv_bfloat16* dl3 = nullptr;
+    if (np) {  // three pieces, each [T, np], each in its own 256-byte aligned region
+        dl3 = wc.take<__nv_bfloat16>((size_t)T * np);
+        __nv_bfloat16* p1 = wc.take<__nv_bfloat16>((size_t)T * np);
+        __nv_bfloat16* p2 = wc.take<__nv_bfloat16>((size_t)T * np);
+        if (p1 != dl3 + (size_t)T * np || p2 != p1 + (size_t)T * np) return MOE_ERR_WORKSPACE;
+    }
     if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     const float z_scale = 2.0f * z_coef / (float)T;
     route_bwd_dlogits_kernel<<<(unsigned)cdiv(T, 8), 256, 0, st>>>(
         dg, topk_idx, topk_gate, topk_score, logits, lse, dlogits_extra, T, E, k, mode, z_scale,
-        dlogits);
+        dlogits, dl3, np);
     if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
-    dim3 grid(d / kBwTJ, (unsigned)cdiv(E, kBwTE), (unsigned)nsplit);
-    route_bwd_dwr_kernel<<<grid, 256, 0, st>>>(dlogits, reinterpret_cast<const __nv_bfloat16*>(x),
-                                               T, d, E, part);
-    if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
+    if (np) {
+        int rc = launch_route_dwr_tc(reinterpret_cast<const __nv_bfloat16*>(x), dl3, T, d, E,
+                                     part, &nsplit, st);
+        if (rc != MOE_OK) return rc;
+    } else {
+        dim3 grid(d / kBwTJ, (unsigned)cdiv(E, kBwTE), (unsigned)nsplit);
+        route_bwd_dwr_kernel<<<grid, 256, 0, st>>>(
+            dlogits, reinterpret_cast<const __nv_bfloat16*>(x), T, d, E, part);
+        if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
+    }
     const int64_t n = (int64_t)E * d;
     route_bwd_reduce_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(part, nsplit, n, dW_r);
     return launch_status();

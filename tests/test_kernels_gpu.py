@@ -310,10 +310,13 @@ def test_combine_and_backward_kernels():
     assert_close(dx, ref, "dx")
 
 
-@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
-def test_router_backward(mode):
-    g = torch.Generator().manual_seed(31)
-    T, d, E, k = 3000, 256, 32, 4
+# E <= 128 runs the tensor-core W_r-gradient kernel (64- and 128-wide expert tiles, ragged
+# token splits); E = 200 the SIMT kernel.
+@pytest.mark.parametrize("mode,T,d,E,k", [("sigmoid", 3000, 256, 32, 4), ("softmax", 3000, 256, 32, 4),
+                                          ("sigmoid", 4100, 512, 64, 8), ("softmax", 1000, 384, 128, 8),
+                                          ("sigmoid", 333, 128, 200, 3), ("softmax", 70, 128, 8, 2)])
+def test_router_backward(mode, T, d, E, k):
+    g = torch.Generator().manual_seed(31 + T + E)
     x = randn_bf16((T, d), g)
     W_r = torch.randn(E, d, generator=g) * d ** -0.5
     b = torch.rand(E, generator=g) * 0.1 - 0.05
