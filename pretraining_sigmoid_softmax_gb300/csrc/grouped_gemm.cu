@@ -13,12 +13,15 @@
 //   B5  dW_g[e] = dA_e^T X_e, dW_u[e] = dU_e^T X_e
 // Row tiles are 128 rows of the expert-major layout, whose segments are padded to 128
 // rows, so every tile belongs to one expert and is found from row_offsets on the device
-// (no host synchronisation). Roles per CTA (256 threads, one CTA per SM):
+// (no host synchronisation). Roles per CTA (384 threads, one CTA per SM):
 //   warp 0  TMA producer (one thread): operand tiles into a ring of shared-memory stages;
 //   warp 1  MMA issuer (one thread): tcgen05.mma 128 x N x 16 steps into a TMEM accumulator;
 //   warp 2  allocates / frees tensor memory (two accumulators, double-buffered);
-//   warps 4-7 epilogue: tcgen05.ld of TMEM lanes 0-127 (one output row per thread), the
-//            fused elementwise step, bf16 stores.
+//   warps 4-11 epilogue: tcgen05.ld of TMEM lanes 0-127 (one output row per thread; warps w
+//            and w + 4 share a lane quadrant and take one half of the columns each), the
+//            fused elementwise step, bf16 stores. Two warps per quadrant double the loads
+//            and stores in flight, which the epilogues that read saved activations need to
+//            keep pace with the tensor cores.
 // Pair mode (a cluster of two CTAs on two SMs): the leading CTA issues
 // tcgen05.mma.cta_group::2 over a 256-row tile; each CTA stages its own 128 rows of A and
 // half of the tile's B columns, so per SM the shared-memory operand traffic and the TMA
@@ -45,7 +48,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;        // bf16 K elements per stage (128 bytes per row)
 constexpr int BK_FP8 = 128;   // E4M3 K elements per stage (also 128 bytes per row)
-constexpr int kThreads = 256;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each taking half the columns
+constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 200 * 1024;
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
@@ -336,14 +340,15 @@ __device__ __forceinline__ void load_au(AuChunk& c, const Params& P, int64_t off
     }
 }
 
+// Columns [c_lo, c_hi) of this thread's row of the tile.
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc, int row_in_tile,
-                                              const Params& P, AuChunk& pre) {
+                                              const Params& P, AuChunk& pre, int c_lo, int c_hi) {
     if constexpr (C::WGRAD) {
         const int64_t row = ti.m0 + row_in_tile;
         __nv_bfloat16* out = (ti.p == 0 ? P.out0 : P.out1) +
                              ((int64_t)ti.e * P.M_out + row) * P.N + ti.n0;
-        for (int c = 0; c < C::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
             float v[32];
             if (ti.k_iters > 0) {
                 uint32_t r[32];
@@ -363,7 +368,7 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
         const int64_t row = ti.m0 + row_in_tile;
         const bool ok = row < ti.row_end;
         const int64_t base = row * (int64_t)P.ld_out + ti.n0;
-        for (int c = 0; c < C::BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
             if constexpr (C::EPI == kEpiSwigluFwd) {
                 uint32_t g[32], u[32];
                 tmem_ld32(t_acc + c, g);
@@ -400,7 +405,7 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
                 }
                 uint32_t r[32];
                 tmem_ld32(t_acc + c, r);
-                if (ok && c + 32 < C::BN) load_au(pre, P, base + c + 32);
+                if (ok && c + 32 < c_hi) load_au(pre, P, base + c + 32);
                 tmem_ld_wait();
                 if (ok) {
                     float dav[32], duv[32];
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&S.tfull[b]), 1);
-            mbar_init(smem_u32(&S.tempty[b]), C::PAIR ? 8 : 4);
+            mbar_init(smem_u32(&S.tempty[b]), C::PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         *S.abort_flag = 0;
         fence_mbar_init();
@@ -490,14 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (P.row_offsets) {
             int v = 0;
             if (tid < P.E) v = (int)(((S.offs[tid + 1] - S.offs[tid]) / BM + 1) / 2);
-            S.ptp[tid + 1] = v;  // tid < 256 = kMaxExperts
+            if (tid < kMaxExperts) S.ptp[tid + 1] = v;
             if (tid == 0) S.ptp[0] = 0;
             __syncthreads();
-            for (int off = 1; off < kThreads; off <<= 1) {  // inclusive scan of S.ptp[1..256]
+            for (int off = 1; off < kMaxExperts; off <<= 1) {  // inclusive scan of S.ptp[1..256]
                 int add = 0;
-                if (tid >= off) add = S.ptp[tid + 1 - off];
+                if (tid >= off && tid < kMaxExperts) add = S.ptp[tid + 1 - off];
                 __syncthreads();
-                S.ptp[tid + 1] += add;
+                if (tid < kMaxExperts) S.ptp[tid + 1] += add;
                 __syncthreads();
             }
         }
@@ -598,8 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
-        const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
+        const int q = warp % 4;  // TMEM lanes 32q .. 32q+31 (a warp's rank in its warpgroup)
         const int row_in_tile = 32 * q + lane;
+        constexpr int kCols = C::BN / (kEpiWarps / 4);  // columns per epilogue warp
+        static_assert(kCols % 32 == 0, "epilogue column split");
+        const int c_lo = ((warp - 4) / 4) * kCols;
         int local = 0;
         for (int64_t tile = first_tile; tile < ntiles; tile += tile_step, ++local) {
             const TileInfo ti = decode<C>(tile, P, S, rank);
@@ -608,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             AuChunk pre;
             if constexpr (C::EPI == kEpiSwigluBwd) {  // first chunk's a, u before the wait
                 const int64_t row = ti.m0 + row_in_tile;
-                if (row < ti.row_end) load_au(pre, P, row * (int64_t)P.ld_out + ti.n0);
+                if (row < ti.row_end) load_au(pre, P, row * (int64_t)P.ld_out + ti.n0 + c_lo);
             }
             bool ok = mbar_wait_bounded(smem_u32(&S.tfull[buf]), ph, abort_flag, P.status,
                                         P.wait_limit_ns, 33);
@@ -616,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_acc = tmem_base + buf * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
-            epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre);
+            epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre, c_lo, c_lo + kCols);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
