@@ -53,6 +53,12 @@ constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 200 * 1024;
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
+// SwiGLU backward: each epilogue warp stages the saved a and u of its 32 rows by TMA, kAuCols
+// columns per chunk, kAuBufs chunks deep; the ring of operand stages gets what is left of
+// kSmemBudgetAu.
+constexpr int kAuCols = 16;
+constexpr int kAuBufs = 3;
+constexpr int kSmemBudgetAu = 220 * 1024;
 
 template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
           bool PAIR_ = false, bool FP8_ = false>
@@ -73,7 +79,11 @@ struct Cfg {
     static constexpr int A_BYTES = BM * 128;     // 128-byte rows in either type
     static constexpr int B_BYTES = BROWS * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // this CTA's bytes per K block
-    static constexpr int STAGES = (kSmemBudget / STAGE_BYTES) > 6 ? 6 : (kSmemBudget / STAGE_BYTES);
+    static constexpr bool AU = EPI == kEpiSwigluBwd;
+    static constexpr int AU_BUF_BYTES = 2 * 32 * kAuCols * 2;  // a and u: 32 rows x kAuCols
+    static constexpr int AU_BYTES = AU ? kEpiWarps * kAuBufs * AU_BUF_BYTES : 0;
+    static constexpr int BUDGET = (AU ? kSmemBudgetAu : kSmemBudget) - AU_BYTES;
+    static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 6 ? 6 : (BUDGET / STAGE_BYTES);
     static constexpr int ACC_COLS = MMA_N;
     static constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulator buffers
     // DUAL: the W_g and W_u boxes form one 2*BN-row B tile (on one CTA, back to back; in a
@@ -86,7 +96,8 @@ struct Cfg {
     static constexpr size_t MISC_BYTES = 512 + sizeof(int64_t) * (kMaxExperts + 1) +
                                          sizeof(int32_t) * kMaxExperts +
                                          sizeof(int32_t) * (kMaxExperts + 1);
-    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + MISC_BYTES;
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + AU_BYTES + MISC_BYTES;
+    static_assert((2 * STAGES + 4 + kEpiWarps * kAuBufs) * 8 + 8 <= 512, "barrier block");
 };
 
 struct Params {
@@ -135,6 +146,8 @@ struct SmemLayout {
     int64_t* offs;     // E + 1
     int32_t* order;    // E
     int32_t* ptp;      // E + 1: exclusive prefix of pair tiles per expert (pair, token-major)
+    uint8_t* au;       // SwiGLU backward: kEpiWarps x kAuBufs staged (a | u) chunks
+    uint64_t* au_full; // kEpiWarps x kAuBufs
 };
 
 template <class C>
@@ -143,12 +156,14 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
     s.b = base + (size_t)C::STAGES * C::A_BYTES;
-    uint8_t* misc = base + (size_t)C::STAGES * C::STAGE_BYTES;
+    s.au = base + (size_t)C::STAGES * C::STAGE_BYTES;  // 1024-aligned: stage sizes are
+    uint8_t* misc = s.au + C::AU_BYTES;
     s.full = reinterpret_cast<uint64_t*>(misc);
     s.empty = s.full + C::STAGES;
     s.tfull = s.empty + C::STAGES;
     s.tempty = s.tfull + 2;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.tempty + 2);
+    s.au_full = s.tempty + 2;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.au_full + (C::AU ? kEpiWarps * kAuBufs : 0));
     s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
     s.offs = reinterpret_cast<int64_t*>(misc + 512);
     s.order = reinterpret_cast<int32_t*>(s.offs + kMaxExperts + 1);
@@ -449,6 +464,98 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
     }
 }
 
+// ------------------------------------------------- SwiGLU backward with staged a and u
+// Each epilogue warp owns 32 rows x (BN / 2) columns of the tile and walks them in chunks of
+// kAuCols. The chunk's saved a and u arrive by TMA (boxes of kAuCols x 32 rows, swizzled
+// so that the row-per-lane reads below hit distinct banks) into one of the warp's kAuBufs
+// buffers; lane 0 issues the copy of chunk n + kAuBufs once the warp is done with chunk n,
+// and a tile's first chunks before its accumulator is ready.
+
+// Byte offset of 16-byte piece j of row r in a staged (a or u) chunk.
+__device__ __forceinline__ int au_offset(int r, int j) {
+    if constexpr (kAuCols == 32) return r * 64 + ((j ^ ((r >> 1) & 3)) << 4);  // 64-byte swizzle
+    else if constexpr (kAuCols == 16) return r * 32 + ((j ^ ((r >> 2) & 1)) << 4);  // 32-byte
+    else return r * 16;                                                            // unswizzled
+}
+
+template <class C>
+__device__ __forceinline__ void au_issue(const SmemLayout& S, const CUtensorMap* ma,
+                                         const CUtensorMap* mu, int slot, uint32_t n, int64_t row0,
+                                         int col) {
+    const int b = (int)(n % kAuBufs);
+    const uint32_t dst = smem_u32(S.au + ((size_t)slot * kAuBufs + b) * C::AU_BUF_BYTES);
+    const uint32_t bar = smem_u32(&S.au_full[slot * kAuBufs + b]);
+    mbar_arrive_expect_tx(bar, C::AU_BUF_BYTES);
+    tma_load_2d(dst, ma, bar, col, (int32_t)row0);
+    tma_load_2d(dst + C::AU_BUF_BYTES / 2, mu, bar, col, (int32_t)row0);
+}
+
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_ld32(taddr, r);
+    else if constexpr (W == 16) tmem_ld16(taddr, r);
+    else tmem_ld8(taddr, r);
+}
+
+// One tile of this warp's columns [c_lo, c_lo + ncols). `n` counts the warp's chunks over the
+// kernel's life (it picks buffer and phase). Returns false when a wait failed (uniform
+// across the warp).
+template <class C>
+__device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const TileInfo& ti,
+                                                  uint32_t t_acc, int q, int lane, int slot,
+                                                  int c_lo, int ncols, const Params& P,
+                                                  const CUtensorMap* ma, const CUtensorMap* mu,
+                                                  uint32_t& n, volatile int* abort_flag) {
+    const int nch = ncols / kAuCols;
+    const int64_t row0 = ti.m0 + 32 * q;
+    const int64_t row = row0 + lane;
+    const bool ok_row = row < ti.row_end;
+    const int64_t base = row * (int64_t)P.ld_out + ti.n0;
+    for (int i = 0; i < nch; ++i, ++n) {
+        const int c = c_lo + i * kAuCols;
+        const int b = (int)(n % kAuBufs);
+        uint32_t acc[kAuCols];
+        tmem_ld_cols<kAuCols>(t_acc + c, acc);
+        bool ok = mbar_wait_bounded(smem_u32(&S.au_full[slot * kAuBufs + b]), (n / kAuBufs) & 1u,
+                                    abort_flag, P.status, P.wait_limit_ns, 34);
+        tmem_ld_wait();
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        if (ok_row) {
+            const uint8_t* abuf = S.au + ((size_t)slot * kAuBufs + b) * C::AU_BUF_BYTES;
+            const uint8_t* ubuf = abuf + C::AU_BUF_BYTES / 2;
+            float dav[kAuCols], duv[kAuCols];
+#pragma unroll
+            for (int j = 0; j < kAuCols / 8; ++j) {
+                const uint4 a4 = *reinterpret_cast<const uint4*>(abuf + au_offset(lane, j));
+                const uint4 u4 = *reinterpret_cast<const uint4*>(ubuf + au_offset(lane, j));
+                const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const float a = (h & 1) ? bf16_hi(aw[h >> 1]) : bf16_lo(aw[h >> 1]);
+                    const float u = (h & 1) ? bf16_hi(uw[h >> 1]) : bf16_lo(uw[h >> 1]);
+                    const float dh = __uint_as_float(acc[8 * j + h]);
+                    const float sa = 1.0f / (1.0f + __expf(-a));
+                    dav[8 * j + h] = dh * u * sa * (1.0f + a * (1.0f - sa));
+                    duv[8 * j + h] = dh * a * sa;
+                }
+            }
+            uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
+            uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
+#pragma unroll
+            for (int j = 0; j < kAuCols / 8; ++j) {
+                da[j] = pack_chunk8(dav + 8 * j);
+                du[j] = pack_chunk8(duv + 8 * j);
+            }
+        }
+        __syncwarp();  // every lane is done with buffer b
+        if (lane == 0 && i + kAuBufs < nch)
+            au_issue<C>(S, ma, mu, slot, n + kAuBufs, row0, ti.n0 + c + kAuBufs * kAuCols);
+    }
+    return true;
+}
+
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap ma0,
@@ -473,6 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&S.tfull[b]), 1);
             mbar_init(smem_u32(&S.tempty[b]), C::PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
+        if constexpr (C::AU)
+            for (int b = 0; b < kEpiWarps * kAuBufs; ++b) mbar_init(smem_u32(&S.au_full[b]), 1);
         *S.abort_flag = 0;
         fence_mbar_init();
     }
@@ -608,15 +717,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kCols = C::BN / (kEpiWarps / 4);  // columns per epilogue warp
         static_assert(kCols % 32 == 0, "epilogue column split");
         const int c_lo = ((warp - 4) / 4) * kCols;
+        const int slot = warp - 4;
+        uint32_t n_au = 0;  // staged a/u chunks consumed by this warp
         int local = 0;
         for (int64_t tile = first_tile; tile < ntiles; tile += tile_step, ++local) {
             const TileInfo ti = decode<C>(tile, P, S, rank);
             const int buf = local & 1;
             const uint32_t ph = (local >> 1) & 1;
             AuChunk pre;
-            if constexpr (C::EPI == kEpiSwigluBwd) {  // first chunk's a, u before the wait
-                const int64_t row = ti.m0 + row_in_tile;
-                if (row < ti.row_end) load_au(pre, P, row * (int64_t)P.ld_out + ti.n0 + c_lo);
+            if constexpr (C::AU) {  // this tile's first a/u chunks while the MMA runs
+                if (lane == 0)
+                    for (int i = 0; i < kAuBufs && i < kCols / kAuCols; ++i)
+                        au_issue<C>(S, &ma1, &mb1, slot, n_au + i, ti.m0 + 32 * q,
+                                    ti.n0 + c_lo + i * kAuCols);
             }
             bool ok = mbar_wait_bounded(smem_u32(&S.tfull[buf]), ph, abort_flag, P.status,
                                         P.wait_limit_ns, 33);
@@ -624,7 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_acc = tmem_base + buf * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
-            epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre, c_lo, c_lo + kCols);
+            if constexpr (C::AU) {
+                if (!swiglu_bwd_staged<C>(S, ti, t_acc, q, lane, slot, c_lo, kCols, P, &ma1, &mb1,
+                                          n_au, abort_flag))
+                    break;
+            } else {
+                epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre, c_lo, c_lo + kCols);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -682,7 +801,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 // 2-D map over a row-major [outer, inner] matrix of bf16 (or of bytes, for E4M3 codes),
 // 128-byte swizzled boxes.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer, bool bytes = false) {
+              uint32_t box_inner, uint32_t box_outer, bool bytes = false,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = get_encoder();
     if (!enc || !base) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -691,7 +811,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
     cuuint32_t es[2] = {1, 1};
     return enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -844,10 +964,16 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
     const __nv_bfloat16* Ub = reinterpret_cast<const __nv_bfloat16*>(U);
     int rc;
 
-    // B2: dH = dY W_d (W_d[e] is [d, f]: K = d rows, N = f contiguous), SwiGLU backward
+    // B2: dH = dY W_d (W_d[e] is [d, f]: K = d rows, N = f contiguous), SwiGLU backward; the
+    // saved a and u are staged by TMA (their maps ride in the second A and B slots)
     {
-        CUtensorMap mdy, mwd;
-        if (!make_map(&mdy, dY, d, rows, 64, 128) || !make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 64))
+        constexpr CUtensorMapSwizzle kAuSwz = kAuCols == 32   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : kAuCols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                              : CU_TENSOR_MAP_SWIZZLE_NONE;
+        CUtensorMap mdy, mwd, msa, msu;
+        if (!make_map(&mdy, dY, d, rows, 64, 128) || !make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 64) ||
+            !make_map(&msa, A, f, rows, kAuCols, 32, false, kAuSwz) ||
+            !make_map(&msu, U, f, rows, kAuCols, 32, false, kAuSwz))
             return MOE_ERR_LAUNCH;
         Params P = base_params(row_offsets, rows, E);
         P.N = f;
@@ -859,9 +985,9 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.in1 = Ub;
         P.ld_out = f;
         if (f % 256 == 0)
-            rc = launch<CfgSwigluBwdP>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 256), st);
+            rc = launch<CfgSwigluBwdP>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st);
         else
-            rc = launch<CfgSwigluBwd<128>>(mdy, mdy, mwd, mwd, P, token_tiles_max(rows, f, 128), st);
+            rc = launch<CfgSwigluBwd<128>>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 128), st);
         if (rc != MOE_OK) return rc;
     }
     // B4: dX = dA W_g + dU W_u (W_g[e] is [f, d]: K = f rows, N = d contiguous)
