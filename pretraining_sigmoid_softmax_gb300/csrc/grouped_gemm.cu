@@ -339,26 +339,11 @@ __device__ __forceinline__ void fp8_scale(float* a, float* b, const Params& P, i
     }
 }
 
-// Saved a and u (32 bf16 each) of one 32-column chunk of this thread's row.
-struct AuChunk {
-    uint4 a[4];
-    uint4 u[4];
-};
-
-__device__ __forceinline__ void load_au(AuChunk& c, const Params& P, int64_t off) {
-    const uint4* pa = reinterpret_cast<const uint4*>(P.in0 + off);
-    const uint4* pu = reinterpret_cast<const uint4*>(P.in1 + off);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        c.a[q] = __ldg(pa + q);
-        c.u[q] = __ldg(pu + q);
-    }
-}
-
-// Columns [c_lo, c_hi) of this thread's row of the tile.
+// Columns [c_lo, c_hi) of this thread's row of the tile (every epilogue except the SwiGLU
+// backward, which runs swiglu_bwd_staged).
 template <class C>
 __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc, int row_in_tile,
-                                              const Params& P, AuChunk& pre, int c_lo, int c_hi) {
+                                              const Params& P, int c_lo, int c_hi) {
     if constexpr (C::WGRAD) {
         const int64_t row = ti.m0 + row_in_tile;
         __nv_bfloat16* out = (ti.p == 0 ? P.out0 : P.out1) +
@@ -407,43 +392,6 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc
                         da[q] = pack_chunk8(av + 8 * q);
                         du[q] = pack_chunk8(uv + 8 * q);
                         dh[q] = pack_chunk8(hv + 8 * q);
-                    }
-                }
-            } else if constexpr (C::EPI == kEpiSwigluBwd) {
-                // saved a, u of this chunk were loaded one chunk ahead (chunk 0 before the
-                // accumulator wait); start the next chunk's loads before using these
-                uint4 ca[4], cu[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    ca[q] = pre.a[q];
-                    cu[q] = pre.u[q];
-                }
-                uint32_t r[32];
-                tmem_ld32(t_acc + c, r);
-                if (ok && c + 32 < c_hi) load_au(pre, P, base + c + 32);
-                tmem_ld_wait();
-                if (ok) {
-                    float dav[32], duv[32];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t aw[4] = {ca[q].x, ca[q].y, ca[q].z, ca[q].w};
-                        const uint32_t uw[4] = {cu[q].x, cu[q].y, cu[q].z, cu[q].w};
-#pragma unroll
-                        for (int h = 0; h < 8; ++h) {
-                            const float a = (h & 1) ? bf16_hi(aw[h >> 1]) : bf16_lo(aw[h >> 1]);
-                            const float u = (h & 1) ? bf16_hi(uw[h >> 1]) : bf16_lo(uw[h >> 1]);
-                            const float dh = __uint_as_float(r[8 * q + h]);
-                            const float sa = 1.0f / (1.0f + __expf(-a));
-                            dav[8 * q + h] = dh * u * sa * (1.0f + a * (1.0f - sa));
-                            duv[8 * q + h] = dh * a * sa;
-                        }
-                    }
-                    uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
-                    uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        da[q] = pack_chunk8(dav + 8 * q);
-                        du[q] = pack_chunk8(duv + 8 * q);
                     }
                 }
             } else {
@@ -724,7 +672,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileInfo ti = decode<C>(tile, P, S, rank);
             const int buf = local & 1;
             const uint32_t ph = (local >> 1) & 1;
-            AuChunk pre;
             if constexpr (C::AU) {  // this tile's first a/u chunks while the MMA runs
                 if (lane == 0)
                     for (int i = 0; i < kAuBufs && i < kCols / kAuCols; ++i)
@@ -742,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           n_au, abort_flag))
                     break;
             } else {
-                epilogue_tile<C>(ti, t_acc, row_in_tile, P, pre, c_lo, c_lo + kCols);
+                epilogue_tile<C>(ti, t_acc, row_in_tile, P, c_lo, c_lo + kCols);
             }
             tc_fence_before();
             __syncwarp();
