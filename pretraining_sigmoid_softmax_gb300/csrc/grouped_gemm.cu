@@ -19,9 +19,10 @@
 //   warp 2  allocates / frees tensor memory (two accumulators, double-buffered);
 //   warps 4-11 epilogue: tcgen05.ld of TMEM lanes 0-127 (one output row per thread; warps w
 //            and w + 4 share a lane quadrant and take one half of the columns each), the
-//            fused elementwise step, bf16 stores. Two warps per quadrant double the loads
-//            and stores in flight, which the epilogues that read saved activations need to
-//            keep pace with the tensor cores.
+//            fused elementwise step, bf16 outputs. Token-major outputs (G1, G2, B4) are
+//            packed into swizzled shared-memory boxes and written by TMA stores; B2 reads
+//            its saved a and u through TMA-staged boxes; weight gradients store per thread.
+//            Two warps per quadrant double the loads and stores in flight.
 // Pair mode (a cluster of two CTAs on two SMs): the leading CTA issues
 // tcgen05.mma.cta_group::2 over a 256-row tile; each CTA stages its own 128 rows of A and
 // half of the tile's B columns, so per SM the shared-memory operand traffic and the TMA
@@ -59,6 +60,9 @@ enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
 constexpr int kAuCols = 16;
 constexpr int kAuBufs = 3;
 constexpr int kSmemBudgetAu = 220 * 1024;
+// Token-major epilogues other than the SwiGLU backward stage their outputs in shared memory,
+// 16 columns x 32 rows per warp and output, two buffers deep, and write them with TMA stores.
+constexpr int kOutCols = 16;
 
 template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
           bool PAIR_ = false, bool FP8_ = false>
@@ -82,7 +86,11 @@ struct Cfg {
     static constexpr bool AU = EPI == kEpiSwigluBwd;
     static constexpr int AU_BUF_BYTES = 2 * 32 * kAuCols * 2;  // a and u: 32 rows x kAuCols
     static constexpr int AU_BYTES = AU ? kEpiWarps * kAuBufs * AU_BUF_BYTES : 0;
-    static constexpr int BUDGET = (AU ? kSmemBudgetAu : kSmemBudget) - AU_BYTES;
+    static constexpr bool TS = !WGRAD && EPI != kEpiSwigluBwd;  // TMA-store epilogue
+    static constexpr int NOUT = EPI == kEpiSwigluFwd ? 3 : 1;
+    static constexpr int OUT_BUF_BYTES = NOUT * 32 * kOutCols * 2;  // one chunk, every output
+    static constexpr int OUT_BYTES = TS ? kEpiWarps * 2 * OUT_BUF_BYTES : 0;
+    static constexpr int BUDGET = (AU || TS ? kSmemBudgetAu : kSmemBudget) - AU_BYTES - OUT_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 6 ? 6 : (BUDGET / STAGE_BYTES);
     static constexpr int ACC_COLS = MMA_N;
     static constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulator buffers
@@ -96,7 +104,8 @@ struct Cfg {
     static constexpr size_t MISC_BYTES = 512 + sizeof(int64_t) * (kMaxExperts + 1) +
                                          sizeof(int32_t) * kMaxExperts +
                                          sizeof(int32_t) * (kMaxExperts + 1);
-    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + AU_BYTES + MISC_BYTES;
+    static constexpr size_t SMEM_BYTES =
+        1024 + (size_t)STAGES * STAGE_BYTES + AU_BYTES + OUT_BYTES + MISC_BYTES;
     static_assert((2 * STAGES + 4 + kEpiWarps * kAuBufs) * 8 + 8 <= 512, "barrier block");
 };
 
@@ -148,6 +157,7 @@ struct SmemLayout {
     int32_t* ptp;      // E + 1: exclusive prefix of pair tiles per expert (pair, token-major)
     uint8_t* au;       // SwiGLU backward: kEpiWarps x kAuBufs staged (a | u) chunks
     uint64_t* au_full; // kEpiWarps x kAuBufs
+    uint8_t* ob;       // TMA-store epilogues: kEpiWarps x 2 staged output chunks
 };
 
 template <class C>
@@ -157,7 +167,8 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
     s.a = base;
     s.b = base + (size_t)C::STAGES * C::A_BYTES;
     s.au = base + (size_t)C::STAGES * C::STAGE_BYTES;  // 1024-aligned: stage sizes are
-    uint8_t* misc = s.au + C::AU_BYTES;
+    s.ob = s.au + C::AU_BYTES;  // 1024-aligned: the a/u buffers are whole KB
+    uint8_t* misc = s.ob + C::OUT_BYTES;
     s.full = reinterpret_cast<uint64_t*>(misc);
     s.empty = s.full + C::STAGES;
     s.tfull = s.empty + C::STAGES;
@@ -313,13 +324,14 @@ __device__ __forceinline__ uint4 pack_chunk8(const float* v) {
 // FP8 dequantisation of a 32-column accumulator chunk: value * scale(A row) * scale(B row
 // of each output column). With dual=true, `a` takes the first B operand's column scales
 // and `b` the second's (G1: gate and up); otherwise only `a` is scaled.
+template <int W = 32>
 __device__ __forceinline__ void fp8_scale(float* a, float* b, const Params& P, int64_t row,
                                           const TileInfo& ti, int c, bool dual = true) {
     const float sr = __ldg(P.sa + row);
     const int64_t col0 = (int64_t)ti.e * P.N + ti.n0 + c;
     const float4* s0 = reinterpret_cast<const float4*>(P.sb0 + col0);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < W / 4; ++q) {
         const float4 v = __ldg(s0 + q);
         a[4 * q] *= sr * v.x;
         a[4 * q + 1] *= sr * v.y;
@@ -329,7 +341,7 @@ __device__ __forceinline__ void fp8_scale(float* a, float* b, const Params& P, i
     if (dual) {
         const float4* s1 = reinterpret_cast<const float4*>(P.sb1 + col0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < W / 4; ++q) {
             const float4 v = __ldg(s1 + q);
             b[4 * q] *= sr * v.x;
             b[4 * q + 1] *= sr * v.y;
@@ -339,75 +351,97 @@ __device__ __forceinline__ void fp8_scale(float* a, float* b, const Params& P, i
     }
 }
 
-// Columns [c_lo, c_hi) of this thread's row of the tile (every epilogue except the SwiGLU
-// backward, which runs swiglu_bwd_staged).
+// Weight-gradient epilogue: columns [c_lo, c_hi) of this thread's output row (a weight row;
+// always inside the output, as M_out and N are whole tiles). An expert with no rows gives
+// zeros.
 template <class C>
-__device__ __forceinline__ void epilogue_tile(const TileInfo& ti, uint32_t t_acc, int row_in_tile,
-                                              const Params& P, int c_lo, int c_hi) {
-    if constexpr (C::WGRAD) {
-        const int64_t row = ti.m0 + row_in_tile;
-        __nv_bfloat16* out = (ti.p == 0 ? P.out0 : P.out1) +
-                             ((int64_t)ti.e * P.M_out + row) * P.N + ti.n0;
-        for (int c = c_lo; c < c_hi; c += 32) {
-            float v[32];
-            if (ti.k_iters > 0) {
-                uint32_t r[32];
-                tmem_ld32(t_acc + c, r);
-                tmem_ld_wait();
+__device__ __forceinline__ void epilogue_wgrad(const TileInfo& ti, uint32_t t_acc, int row_in_tile,
+                                               const Params& P, int c_lo, int c_hi) {
+    static_assert(C::WGRAD, "weight-gradient tiles only");
+    const int64_t row = ti.m0 + row_in_tile;
+    __nv_bfloat16* out = (ti.p == 0 ? P.out0 : P.out1) + ((int64_t)ti.e * P.M_out + row) * P.N + ti.n0;
+    for (int c = c_lo; c < c_hi; c += 32) {
+        float v[32];
+        if (ti.k_iters > 0) {
+            uint32_t r[32];
+            tmem_ld32(t_acc + c, r);
+            tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-            } else {
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = pack_chunk8(v + 8 * q);
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
-    } else {
-        const int64_t row = ti.m0 + row_in_tile;
-        const bool ok = row < ti.row_end;
-        const int64_t base = row * (int64_t)P.ld_out + ti.n0;
-        for (int c = c_lo; c < c_hi; c += 32) {
-            if constexpr (C::EPI == kEpiSwigluFwd) {
-                uint32_t g[32], u[32];
-                tmem_ld32(t_acc + c, g);
-                tmem_ld32(t_acc + C::BN + c, u);
-                tmem_ld_wait();
-                if (ok) {
-                    float av[32], uv[32], hv[32];
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        av[j] = __uint_as_float(g[j]);
-                        uv[j] = __uint_as_float(u[j]);
-                    }
-                    if constexpr (C::FP8) fp8_scale(av, uv, P, row, ti, c);
+        for (int q = 0; q < 4; ++q) dst[q] = pack_chunk8(v + 8 * q);
+    }
+}
+
+// ------------------------------------------------------- epilogues with TMA stores
+// Each epilogue warp owns 32 rows x (BN / 2) columns of the tile and walks them in chunks of
+// kOutCols. Per chunk its lanes pack their rows of every output into a shared-memory buffer
+// laid out as the 32-byte-swizzled TMA box (kOutCols x 32 rows), and lane 0 stores the boxes;
+// a buffer is rewritten only after the store that read it two chunks earlier is done.
+// A 128-row half of a pair tile that lies past the expert's segment stores nothing (such a
+// half is wholly inside or wholly outside, as segments are padded to 128 rows); rows past
+// the end of the output tensor are clipped by the stores themselves.
+
+// Byte offset of 16-byte piece j of row r in a 32-byte-swizzled box of 32-byte rows.
+__device__ __forceinline__ int sw32_offset(int r, int j) { return r * 32 + ((j ^ ((r >> 2) & 1)) << 4); }
+
+template <class C>
+__device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const TileInfo& ti,
+                                                   uint32_t t_acc, int q, int lane, int slot,
+                                                   int c_lo, int ncols, const Params& P,
+                                                   const CUtensorMap* mo0, const CUtensorMap* mo1,
+                                                   const CUtensorMap* mo2, uint32_t& n) {
+    static_assert(kOutCols == 16, "chunk layout");
+    if (ti.m0 >= ti.row_end) return;  // warp-uniform: the whole half is past the segment
+    const int64_t row0 = ti.m0 + 32 * q;
+    // rows past row_end (the tail of an unpadded layout) are clipped by the store; their FP8
+    // row scale is read from the last row instead
+    const int64_t row = row0 + lane < ti.row_end ? row0 + lane : ti.row_end - 1;
+    for (int i = 0; i < ncols / kOutCols; ++i, ++n) {
+        const int c = c_lo + i * kOutCols;
+        float v[C::NOUT][kOutCols];
+        if constexpr (C::EPI == kEpiSwigluFwd) {
+            uint32_t g[kOutCols], u[kOutCols];
+            tmem_ld16(t_acc + c, g);
+            tmem_ld16(t_acc + C::BN + c, u);
+            tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) hv[j] = av[j] / (1.0f + __expf(-av[j])) * uv[j];
-                    uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
-                    uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
-                    uint4* dh = reinterpret_cast<uint4*>(P.out2 + base + c);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        da[q] = pack_chunk8(av + 8 * q);
-                        du[q] = pack_chunk8(uv + 8 * q);
-                        dh[q] = pack_chunk8(hv + 8 * q);
-                    }
-                }
-            } else {
-                uint32_t r[32];
-                tmem_ld32(t_acc + c, r);
-                tmem_ld_wait();
-                if (ok) {
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    if constexpr (C::FP8) fp8_scale(v, v, P, row, ti, c, /*dual=*/false);
-                    uint4* dst = reinterpret_cast<uint4*>(P.out0 + base + c);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = pack_chunk8(v + 8 * q);
-                }
+            for (int j = 0; j < kOutCols; ++j) {
+                v[0][j] = __uint_as_float(g[j]);
+                v[1][j] = __uint_as_float(u[j]);
             }
+            if constexpr (C::FP8) fp8_scale<kOutCols>(v[0], v[1], P, row, ti, c);
+#pragma unroll
+            for (int j = 0; j < kOutCols; ++j) v[2][j] = v[0][j] / (1.0f + __expf(-v[0][j])) * v[1][j];
+        } else {
+            uint32_t r[kOutCols];
+            tmem_ld16(t_acc + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < kOutCols; ++j) v[0][j] = __uint_as_float(r[j]);
+            if constexpr (C::FP8) fp8_scale<kOutCols>(v[0], v[0], P, row, ti, c, /*dual=*/false);
+        }
+        uint8_t* buf = S.ob + ((size_t)slot * 2 + (n & 1)) * C::OUT_BUF_BYTES;
+        if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+        __syncwarp();
+#pragma unroll
+        for (int o = 0; o < C::NOUT; ++o)
+#pragma unroll
+            for (int j = 0; j < kOutCols / 8; ++j)
+                *reinterpret_cast<uint4*>(buf + o * 1024 + sw32_offset(lane, j)) = pack_chunk8(v[o] + 8 * j);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const CUtensorMap* mo[3] = {mo0, mo1, mo2};
+#pragma unroll
+            for (int o = 0; o < C::NOUT; ++o)
+                tma_store_2d(mo[o], smem_u32(buf + o * 1024), ti.n0 + c, (int32_t)row0);
+            bulk_commit();
         }
     }
 }
@@ -509,7 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap ma0,
                         const __grid_constant__ CUtensorMap ma1,
                         const __grid_constant__ CUtensorMap mb0,
-                        const __grid_constant__ CUtensorMap mb1, const Params P) {
+                        const __grid_constant__ CUtensorMap mb1,
+                        const __grid_constant__ CUtensorMap mo0,
+                        const __grid_constant__ CUtensorMap mo1,
+                        const __grid_constant__ CUtensorMap mo2, const Params P) {
     extern __shared__ uint8_t gg_smem_raw[];
     const SmemLayout S = carve<C>(gg_smem_raw);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -688,8 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!swiglu_bwd_staged<C>(S, ti, t_acc, q, lane, slot, c_lo, kCols, P, &ma1, &mb1,
                                           n_au, abort_flag))
                     break;
+            } else if constexpr (C::TS) {
+                epilogue_tma_store<C>(S, ti, t_acc, q, lane, slot, c_lo, kCols, P, &mo0, &mo1, &mo2,
+                                      n_au);
             } else {
-                epilogue_tile<C>(ti, t_acc, row_in_tile, P, c_lo, c_lo + kCols);
+                epilogue_wgrad<C>(ti, t_acc, row_in_tile, P, c_lo, c_lo + kCols);
             }
             tc_fence_before();
             __syncwarp();
@@ -697,6 +737,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (C::PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[buf]), 0));
                 else mbar_arrive(smem_u32(&S.tempty[buf]));
             }
+        }
+        if constexpr (C::TS) {
+            if (lane == 0) bulk_wait<0>();  // this warp's stores are complete
         }
     }
     __syncwarp();
@@ -762,10 +805,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps for the TMA-store epilogue: boxes of kOutCols x 32 rows over [rows, ld] bf16.
+bool out_maps(CUtensorMap (&mo)[3], const void* o0, const void* o1, const void* o2, uint64_t ld,
+              uint64_t rows) {
+    const void* o[3] = {o0, o1 ? o1 : o0, o2 ? o2 : o0};
+    for (int i = 0; i < 3; ++i)
+        if (!make_map(&mo[i], o[i], ld, rows, kOutCols, 32, false, CU_TENSOR_MAP_SWIZZLE_32B))
+            return false;
+    return true;
+}
+
+// `mo` (TMA-store configurations only): the output maps from out_maps.
 template <class C>
 int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-           const CUtensorMap& b1, const Params& P, int64_t max_tiles, cudaStream_t st) {
+           const CUtensorMap& b1, const Params& P, int64_t max_tiles, cudaStream_t st,
+           const CUtensorMap* mo = nullptr) {
     static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
+    if (C::TS && !mo) return MOE_ERR_LAUNCH;
+    const CUtensorMap& o0 = mo ? mo[0] : a0;
+    const CUtensorMap& o1 = mo ? mo[1] : a0;
+    const CUtensorMap& o2 = mo ? mo[2] : a0;
     auto kern = grouped_gemm_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM_BYTES) != cudaSuccess)
@@ -790,13 +849,14 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
         if (max_tiles < pairs) pairs = max_tiles;
         if (pairs < 1) pairs = 1;
         cfg.gridDim = dim3(2 * (unsigned)pairs);
-        if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, P) != cudaSuccess) return MOE_ERR_LAUNCH;
+        if (cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, o0, o1, o2, P) != cudaSuccess)
+            return MOE_ERR_LAUNCH;
         return launch_status();
     } else {
         int64_t grid = sm_count();
         if (max_tiles < grid) grid = max_tiles;
         if (grid < 1) grid = 1;
-        kern<<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, P);
+        kern<<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, o0, o1, o2, P);
         return launch_status();
     }
 }
@@ -869,7 +929,10 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
     P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
     P.ld_out = f;
-    int rc = launch<CfgG1P>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st);
+    CUtensorMap moa[3], moy[3];
+    if (!out_maps(moa, A, U, H, f, rows) || !out_maps(moy, Y, nullptr, nullptr, d, rows))
+        return MOE_ERR_LAUNCH;
+    int rc = launch<CfgG1P>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st, moa);
     if (rc != MOE_OK) return rc;
     // G2: y = h W_d^T
     Params Q = base_params(row_offsets, rows, E);
@@ -879,10 +942,10 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     Q.ld_out = d;
     if (d % 256 == 0) {  // CTA pair: each CTA stages 128 of the tile's 256 W_d rows
         if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
-        rc = launch<CfgStoreKP>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st);
+        rc = launch<CfgStoreKP>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st, moy);
     } else {
         if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
-        rc = launch<CfgStoreK<128>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st);
+        rc = launch<CfgStoreK<128>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st, moy);
     }
     return rc;
 }
@@ -951,10 +1014,12 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.kb_per_expert = f;
         P.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
         P.ld_out = d;
+        CUtensorMap mox[3];
+        if (!out_maps(mox, dX, nullptr, nullptr, d, rows)) return MOE_ERR_LAUNCH;
         if (d % 256 == 0)
-            rc = launch<CfgDgrad2P>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 256), st);
+            rc = launch<CfgDgrad2P>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 256), st, mox);
         else
-            rc = launch<CfgDgrad2<128>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 128), st);
+            rc = launch<CfgDgrad2<128>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 128), st, mox);
         if (rc != MOE_OK) return rc;
     }
     if (row_offsets) {
@@ -1041,7 +1106,10 @@ extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int6
     P.sa = sX;
     P.sb0 = sWg;
     P.sb1 = sWu;
-    int rc = launch<CfgG1P8>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st);
+    CUtensorMap moa[3], moy[3];
+    if (!out_maps(moa, A, U, H, f, rows) || !out_maps(moy, Y, nullptr, nullptr, d, rows))
+        return MOE_ERR_LAUNCH;
+    int rc = launch<CfgG1P8>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st, moa);
     if (rc != MOE_OK) return rc;
     // h rows -> E4M3 codes for the down projection
     rc = launch_quantize_rows_fp8(reinterpret_cast<const __nv_bfloat16*>(H),
@@ -1056,8 +1124,8 @@ extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int6
     Q.sa = sH;
     Q.sb0 = sWd;
     if (d % 256 == 0)
-        rc = launch<CfgStoreKP8>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st);
+        rc = launch<CfgStoreKP8>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st, moy);
     else
-        rc = launch<CfgStoreK8>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st);
+        rc = launch<CfgStoreK8>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st, moy);
     return rc;
 }
