@@ -177,12 +177,16 @@ int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, int64_t T, i
  *      NULL for one dense expert over all `rows` rows (E must be 1; used for the shared
  *      expert with X = x, rows = T); W_g, W_u [E,f,d] bf16; W_d [E,d,f] bf16.
  * Out: A, U, H [rows,f] bf16 (saved for backward); Y [rows,d] bf16.
+ * row_gate [rows] fp32 or NULL: with it the row's gate is folded into the expert, h is
+ *      written as row_gate[p] * silu(a) * u (one bf16 rounding) and y is therefore the gated
+ *      output; a and u are not scaled. The down projection is linear, so this gives the
+ *      combine's g * y without a second pass (moe_row_gates builds row_gate).
  * `rows` is the row capacity of X/A/U/H/Y; rows past it are never touched.
  */
 int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int E, int64_t rows, int d,
                    int f, const moe_bf16* W_g, const moe_bf16* W_u, const moe_bf16* W_d,
-                   moe_bf16* A, moe_bf16* U, moe_bf16* H, moe_bf16* Y, void* ws,
-                   size_t ws_bytes, moe_stream_t stream);
+                   moe_bf16* A, moe_bf16* U, moe_bf16* H, moe_bf16* Y, const float* row_gate,
+                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_quantize_rows_fp8 - rowwise FP8 (E4M3) quantisation of a GEMM operand, the Apex-3
@@ -206,12 +210,14 @@ int moe_quantize_rows_fp8(const moe_bf16* X, const int64_t* rows_limit, int64_t 
  *      Wgq, Wuq [E f, d] codes with sWg, sWu [E f]; Wdq [E d, f] codes with sWd [E d]
  *      (moe_quantize_rows_fp8 of the weights viewed as [E f, d] and [E d, f]).
  * Out: A, U, H [rows, f] bf16; Hq [rows, f] codes and sH [rows]; Y [rows, d] bf16.
+ * row_gate: as in moe_expert_fwd (h, and so Hq and y, carry the row's gate).
  */
 int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int64_t* row_offsets, int E,
                        int64_t rows, int d, int f, const uint8_t* Wgq, const float* sWg,
                        const uint8_t* Wuq, const float* sWu, const uint8_t* Wdq,
                        const float* sWd, moe_bf16* A, moe_bf16* U, moe_bf16* H, uint8_t* Hq,
-                       float* sH, moe_bf16* Y, void* ws, size_t ws_bytes, moe_stream_t stream);
+                       float* sH, moe_bf16* Y, const float* row_gate, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /*
  * moe_combine - gate-weighted sum of the expert outputs (C1).
@@ -219,8 +225,9 @@ int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int64_t* row_of
  * summed in fp32 in slot order, shared term last, one bf16 rounding. Source: section 2.5
  * of the handbook summary (each expert's output is returned to its token); KempnerForge
  * "Features" (shared experts).
- * In : Y_perm [padded rows, d] bf16; topk_gate [T,k] fp32; slot_to_row [T,k] int32;
- *      Y_shared [T,d] bf16 or NULL.  Out: out [T,d] bf16.
+ * In : Y_perm [padded rows, d] bf16; topk_gate [T,k] fp32, or NULL when the rows already
+ *      carry their gates (moe_expert_fwd with row_gate): then every weight is 1;
+ *      slot_to_row [T,k] int32; Y_shared [T,d] bf16 or NULL.  Out: out [T,d] bf16.
  */
 int moe_combine(const moe_bf16* Y_perm, const float* topk_gate, const int32_t* slot_to_row,
                 const moe_bf16* Y_shared, int64_t T, int d, int k, moe_bf16* out,
@@ -256,6 +263,9 @@ int moe_bias_update_proportional(const int32_t* counts, int E, int64_t T, int k,
  * In : dY [T,d] bf16; Y_perm; topk_gate; slot_to_row; row_offsets [E+1] and perm_token
  *      (to zero the padding rows of dY_perm).
  * Out: dY_perm [padded rows, d] bf16 (padding rows 0); dg [T,k] fp32.
+ * Gate folded into the experts: topk_gate NULL makes dY_perm plain copies of dY[t] (the
+ * gradient of the gated rows); Y_perm and dg both NULL skip the gate gradient, which
+ * moe_expert_bwd and moe_gate_grad then form.
  */
 int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm, const float* topk_gate,
                     const int32_t* slot_to_row, const int64_t* row_offsets,
@@ -274,13 +284,39 @@ int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm, const float* top
  *      Padding rows of dY and X must be zero (moe_permute and moe_combine_bwd do this).
  * Out: dX [rows, d] bf16; dA, dU [rows, f] bf16 (the SwiGLU input gradients, kept as
  *      operands of the weight-gradient GEMMs); dW_g, dW_u [E,f,d] bf16; dW_d [E,d,f] bf16.
+ * Gate folded into the experts (row_gate and gate_part both given, else both NULL): dY is
+ *      the gradient of the gated rows (moe_combine_bwd without gates), H is the gated h of
+ *      moe_expert_fwd, and with r = dy W_d[e]: dh = row_gate[p] * r (so dW_d = sum dy^T H
+ *      needs no change) and gate_part[p, j] = sum over columns 64j .. 64j+63 of
+ *      r * silu(a) * u, in column order (h recomputed in fp32 from a and u): the gate's
+ *      gradient in f/64 partial sums. gate_part is [rows, f/64] fp32.
  */
 int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
                    const moe_bf16* U, const moe_bf16* H, const int64_t* row_offsets, int E,
                    int64_t rows, int d, int f, const moe_bf16* W_g, const moe_bf16* W_u,
                    const moe_bf16* W_d, moe_bf16* dX, moe_bf16* dA, moe_bf16* dU,
-                   moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, void* ws, size_t ws_bytes,
-                   moe_stream_t stream);
+                   moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, const float* row_gate,
+                   float* gate_part, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_row_gates - each slot's gate at its row of the expert-major layout, for folding the
+ * gate into the experts (the combine's weights, moved before the down projection: section
+ * 2.5 of the handbook summary weights each expert's output by its gate).
+ * Definition: row_gate[slot_to_row[t,i]] = topk_gate[t,i]; every other row (padding) 0.
+ * In : topk_gate [T,k] fp32; slot_to_row [T,k] int32 (from moe_permute); rows = the layout's
+ *      row capacity (moe_padded_rows).  Out: row_gate [rows] fp32.
+ */
+int moe_row_gates(const float* topk_gate, const int32_t* slot_to_row, int64_t T, int k,
+                  int64_t rows, float* row_gate, moe_stream_t stream);
+
+/*
+ * moe_gate_grad - the gate gradient from moe_expert_bwd's partial sums.
+ * Definition: dg[t,i] = sum_{j < f/64} gate_part[slot_to_row[t,i], j], in order of j; equal
+ * to sum_j dY[t,j] y[t,i,j] (the combine's gate gradient) since y = h W_d^T.
+ * In : gate_part [rows, f/64] fp32; slot_to_row [T,k].  Out: dg [T,k] fp32. f % 64 == 0.
+ */
+int moe_gate_grad(const float* gate_part, const int32_t* slot_to_row, int64_t T, int k, int f,
+                  float* dg, moe_stream_t stream);
 
 /*
  * moe_route_bwd - router backward (R1b). No gradient reaches the bias or the choice.

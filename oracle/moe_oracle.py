@@ -250,19 +250,28 @@ def swiglu_expert_fp8(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: n
 
 
 def swiglu_expert(rows: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
-                  rnd=None):
+                  rnd=None, row_gate: np.ndarray | None = None):
     """One bias-free SwiGLU expert (three weight matrices, section 2.5):
-    a = x W_g^T, u = x W_u^T, h = silu(a) * u, y = h W_d^T. Returns the stored a, u, h, y."""
+    a = x W_g^T, u = x W_u^T, h = silu(a) * u, y = h W_d^T. Returns the stored a, u, h, y.
+
+    ``row_gate`` (one value per row) moves the combine's gate weight before the down
+    projection: h is stored as g * silu(a) * u, so y is the gated output g * (h W_d^T). In
+    exact arithmetic this is the same product (W_d is linear); with ``rnd`` it models a
+    layout that stores the gated h."""
     a = rows @ W_g.T
     u = rows @ W_u.T
-    h = _r(rnd, silu(a) * u)
+    hv = silu(a) * u
+    if row_gate is not None:
+        hv = row_gate[:, None] * hv
+    h = _r(rnd, hv)
     y = _r(rnd, h @ W_d.T)
     return _r(rnd, a), _r(rnd, u), h, y
 
 
 def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d, rnd=None,
-                    fp8: bool = False) -> dict:
-    """Each expert applied to its own contiguous segment of the permuted rows."""
+                    fp8: bool = False, row_gate: np.ndarray | None = None) -> dict:
+    """Each expert applied to its own contiguous segment of the permuted rows (``row_gate``:
+    each row's gate folded into its expert, as in ``swiglu_expert``)."""
     expert = swiglu_expert_fp8 if fp8 else swiglu_expert
     N = x_perm.shape[0]
     f = W_g.shape[1]
@@ -271,8 +280,9 @@ def experts_forward(x_perm: np.ndarray, offsets: np.ndarray, W_g, W_u, W_d, rnd=
     for e in range(W_g.shape[0]):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi > lo:
+            kw = {} if row_gate is None else {"row_gate": row_gate[lo:hi]}
             A[lo:hi], U[lo:hi], H[lo:hi], Y[lo:hi] = expert(x_perm[lo:hi], W_g[e], W_u[e],
-                                                            W_d[e], rnd)
+                                                            W_d[e], rnd, **kw)
     return {"A": A, "U": U, "H": H, "Y_perm": Y}
 
 
@@ -294,12 +304,16 @@ def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
 
 def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                   logits: np.ndarray | None = None, idx: np.ndarray | None = None,
-                  rnd=None, aux: tuple | None = None, fp8: bool = False) -> dict:
+                  rnd=None, aux: tuple | None = None, fp8: bool = False,
+                  fold_gate: bool = False) -> dict:
     """Full forward of the layer from fp64 copies of the inputs.
 
     ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
     that index checks compare selections made from identical logits). ``idx`` replaces
-    the chosen experts (used so value checks do not cascade from a near-tie)."""
+    the chosen experts (used so value checks do not cascade from a near-tie).
+    ``fold_gate`` applies each slot's gate inside its expert (before the linear down
+    projection) and combines without weights: the same value in exact arithmetic, and with
+    ``rnd`` the rounding of a layout that stores the gated h and y."""
     x = inp["x"]
     E = inp["W_r"].shape[0]
     if logits is None:
@@ -309,15 +323,19 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
         r = _regate(r, logits, idx, mode, inp.get("b"), z_coef)
     disp = dispatch(r["idx"], E)
     x_perm = x[disp["perm_token"]]
-    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"], rnd, fp8)
+    if fold_gate and fp8:
+        raise ValueError("the FP8 expert model quantises the ungated h; fold_gate is bf16 only")
+    row_gate = r["gate"][disp["perm_token"], disp["perm_slot"]] if fold_gate else None
+    ex = experts_forward(x_perm, disp["offsets"], inp["W_g"], inp["W_u"], inp["W_d"], rnd, fp8,
+                         row_gate=row_gate)
     shared = None
     if "Ws_g" in inp:
         shared = (swiglu_expert_fp8 if fp8 else swiglu_expert)(x, inp["Ws_g"], inp["Ws_u"],
                                                                inp["Ws_d"], rnd)
-    out = combine(ex["Y_perm"], r["gate"], disp["slot_to_row"],
-                  None if shared is None else shared[3], rnd)
+    out = combine(ex["Y_perm"], np.ones_like(r["gate"]) if fold_gate else r["gate"],
+                  disp["slot_to_row"], None if shared is None else shared[3], rnd)
     res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
-           "z_coef": z_coef, "rnd": rnd, "aux": aux}
+           "z_coef": z_coef, "rnd": rnd, "aux": aux, "row_gate": row_gate}
     if aux is not None:  # (seq_len, switch_coef, seq_coef)
         a = aux_losses(logits, r["idx"], mode, *aux)
         res["aux_switch"], res["aux_seq"] = a["switch"], a["seq"]
@@ -387,16 +405,24 @@ def swiglu_backward(dh: np.ndarray, a: np.ndarray, u: np.ndarray):
 
 def expert_backward(dy: np.ndarray, x: np.ndarray, a: np.ndarray, u: np.ndarray,
                     h: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
-                    rnd=None) -> dict:
+                    rnd=None, row_gate: np.ndarray | None = None) -> dict:
     """Backward of one SwiGLU expert over its rows, given the upstream gradient of its
     output and the stored a, u, h of the forward:
     dh = dy W_d, (da, du) from the SwiGLU derivative, dx = da W_g + du W_u,
-    dW_d = dy^T h, dW_g = da^T x, dW_u = du^T x."""
-    dh = dy @ W_d
+    dW_d = dy^T h, dW_g = da^T x, dW_u = du^T x.
+
+    With ``row_gate`` (the gate folded into the expert, h stored gated): dy is the gradient
+    of the gated output, r = dy W_d, dh = g * r, dW_d = dy^T h (h already carries g), and
+    the gate's gradient per row is dg = sum_j r_j silu(a_j) u_j (returned as "dg_row")."""
+    r = dy @ W_d
+    dh = r if row_gate is None else row_gate[:, None] * r
     da, du = swiglu_backward(dh, a, u)
     da, du = _r(rnd, da), _r(rnd, du)
-    return {"dA": da, "dU": du, "dX": _r(rnd, da @ W_g + du @ W_u),
-            "dW_d": _r(rnd, dy.T @ h), "dW_g": _r(rnd, da.T @ x), "dW_u": _r(rnd, du.T @ x)}
+    res = {"dA": da, "dU": du, "dX": _r(rnd, da @ W_g + du @ W_u),
+           "dW_d": _r(rnd, dy.T @ h), "dW_g": _r(rnd, da.T @ x), "dW_u": _r(rnd, du.T @ x)}
+    if row_gate is not None:
+        res["dg_row"] = np.sum(r * silu(a) * u, axis=1)
+    return res
 
 
 def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndarray,
@@ -442,7 +468,11 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
     offs = fwd["offsets"]
     tok = fwd["perm_token"]
     slot = fwd["perm_slot"]
-    dY_perm, dg = combine_backward(dY, fwd["Y_perm"], gate, s2r, tok, slot, rnd)
+    row_gate = fwd.get("row_gate")
+    if row_gate is None:
+        dY_perm, dg = combine_backward(dY, fwd["Y_perm"], gate, s2r, tok, slot, rnd)
+    else:  # gate folded into the experts: rows get the token gradient itself
+        dY_perm, dg = dY[tok], np.zeros((T, k))
     # experts backward
     N, d = fwd["X_perm"].shape
     f = inp["W_g"].shape[1]
@@ -455,7 +485,10 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
             continue
         g = expert_backward(dY_perm[lo:hi], fwd["X_perm"][lo:hi], fwd["A"][lo:hi],
                             fwd["U"][lo:hi], fwd["H"][lo:hi], inp["W_g"][e], inp["W_u"][e],
-                            inp["W_d"][e], rnd)
+                            inp["W_d"][e], rnd,
+                            row_gate=None if row_gate is None else row_gate[lo:hi])
+        if row_gate is not None:
+            dg[tok[lo:hi], slot[lo:hi]] = g["dg_row"]
         dX_perm[lo:hi], dA[lo:hi], dU[lo:hi] = g["dX"], g["dA"], g["dU"]
         dW_g[e], dW_u[e], dW_d[e] = g["dW_g"], g["dW_u"], g["dW_d"]
     res = {"dY_perm": dY_perm, "dg": dg, "dA": dA, "dU": dU, "dX_perm": dX_perm,
@@ -597,13 +630,19 @@ def bias_update_proportional(counts: np.ndarray, b: np.ndarray, T: int, k: int,
 # ---------------------------------------------------------------------------------------
 # sampled evaluation for workloads too large to run whole on the CPU
 
-def token_forward(inp: dict, t: int, experts, gates, rnd=None, fp8: bool = False) -> np.ndarray:
-    """out_t for one token given its chosen experts and gates."""
+def token_forward(inp: dict, t: int, experts, gates, rnd=None, fp8: bool = False,
+                  fold_gate: bool = False) -> np.ndarray:
+    """out_t for one token given its chosen experts and gates (``fold_gate``: each gate
+    applied inside its expert, as in ``layer_forward``)."""
     expert = swiglu_expert_fp8 if fp8 else swiglu_expert
     x_t = inp["x"][t:t + 1]
     out = np.zeros((1, inp["x"].shape[1]))
     for e, g in zip(experts, gates):
-        out += g * expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)[3]
+        if fold_gate:
+            out += swiglu_expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd,
+                                 row_gate=np.array([g]))[3]
+        else:
+            out += g * expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)[3]
     if "Ws_g" in inp:
         out += expert(x_t, inp["Ws_g"], inp["Ws_u"], inp["Ws_d"], rnd)[3]
     return _r(rnd, out[0])
@@ -611,7 +650,8 @@ def token_forward(inp: dict, t: int, experts, gates, rnd=None, fp8: bool = False
 
 def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, k: int,
                    dY_t: np.ndarray, z_coef: float, T: int, rnd=None,
-                   dl_extra_t: np.ndarray | None = None, fp8: bool = False) -> dict:
+                   dl_extra_t: np.ndarray | None = None, fp8: bool = False,
+                   fold_gate: bool = False) -> dict:
     """Gradient rows of one token: dx_t, dg_t and the router logit gradient for it.
 
     A token's dx depends only on its own routing, experts and upstream gradient, so it can
@@ -628,8 +668,13 @@ def token_backward(inp: dict, t: int, logits_t: np.ndarray, experts, mode: str, 
     expert = swiglu_expert_fp8 if fp8 else swiglu_expert
     for i, e in enumerate(experts):
         a, u, h, y = expert(x_t, inp["W_g"][e], inp["W_u"][e], inp["W_d"][e], rnd)
-        dg[0, i] = float(np.sum(dY_t * y[0]))
-        dH = _r(rnd, gate[i] * dY_t[None, :]) @ inp["W_d"][e]
+        if fold_gate:  # dY_t itself reaches the gated expert; dg from r = dY_t W_d
+            rr = dY_t[None, :] @ inp["W_d"][e]
+            dg[0, i] = float(np.sum(rr * silu(a) * u))
+            dH = gate[i] * rr
+        else:
+            dg[0, i] = float(np.sum(dY_t * y[0]))
+            dH = _r(rnd, gate[i] * dY_t[None, :]) @ inp["W_d"][e]
         dA, dU = swiglu_backward(dH, a, u)
         dA, dU = _r(rnd, dA), _r(rnd, dU)
         dx += _r(rnd, dA @ inp["W_g"][e] + dU @ inp["W_u"][e])
@@ -654,24 +699,26 @@ def _gemm_operands(X, Wg, Wu, fp8):
 
 def expert_weight_grad_entries(inp: dict, e: int, tokens: np.ndarray, slots_gate: np.ndarray,
                                dY: np.ndarray, entries_d, entries_gu, rnd=None,
-                               fp8: bool = False) -> dict:
+                               fp8: bool = False, fold_gate: bool = False) -> dict:
     """Chosen entries of dW_d[e], dW_g[e] and dW_u[e].
 
     ``tokens`` are the tokens routed to expert e in ascending order and ``slots_gate`` their
     gates for e. ``entries_d`` lists (i, j) of dW_d[e][i, j] = sum_p dY_perm[p, i] h[p, j];
     ``entries_gu`` lists (j, i) of dW_g[e][j, i] = sum_p dA[p, j] x_perm[p, i] (and dW_u)."""
     X = inp["x"][tokens]
-    dYp = _r(rnd, slots_gate[:, None] * dY[tokens])
+    # fold_gate: the rows carry the token gradient itself and the gate sits in h and dh
+    g = slots_gate if fold_gate else np.ones(len(tokens))
+    dYp = dY[tokens] if fold_gate else _r(rnd, slots_gate[:, None] * dY[tokens])
     Wg, Wu, Wd = inp["W_g"][e], inp["W_u"][e], inp["W_d"][e]
     res = {"dW_d": [], "dW_g": [], "dW_u": []}
     Xo, Wgo, Wuo = _gemm_operands(X, Wg, Wu, fp8)
     for (i, j) in entries_d:
         a, u = Xo @ Wgo[j], Xo @ Wuo[j]
-        h = _r(rnd, silu(a) * u)
+        h = _r(rnd, g * silu(a) * u)
         res["dW_d"].append(float(_r(rnd, np.sum(dYp[:, i] * h))))
     for (j, i) in entries_gu:
         a, u = _r(rnd, Xo @ Wgo[j]), _r(rnd, Xo @ Wuo[j])
-        dh = dYp @ Wd[:, j]
+        dh = g * (dYp @ Wd[:, j])
         da, du = swiglu_backward(dh, a, u)
         res["dW_g"].append(float(_r(rnd, np.sum(_r(rnd, da) * X[:, i]))))
         res["dW_u"].append(float(_r(rnd, np.sum(_r(rnd, du) * X[:, i]))))

@@ -28,16 +28,19 @@ PROTOTYPES = {
     "moe_route": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
-    "moe_expert_fwd": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_fwd": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                            _P]),
     "moe_quantize_rows_fp8": (_I, [_P, _P, _I64, _I, _P, _P, _P]),
     "moe_expert_fwd_fp8": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                _P, _P, _P, _P, _SZ, _P]),
+                                _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I64, _I, _I, _P, _P]),
     "moe_bias_update": (_I, [_P, _I, _I64, _I, _F, _P, _P]),
     "moe_bias_update_proportional": (_I, [_P, _I, _I64, _I, _F, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P]),
     "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P,
-                            _P, _P, _P, _SZ, _P]),
+                            _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_row_gates": (_I, [_P, _P, _I64, _I, _I64, _P, _P]),
+    "moe_gate_grad": (_I, [_P, _P, _I64, _I, _I, _P, _P]),
     "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _F, _P, _P, _P,
                            _SZ, _P]),
     "moe_aux_loss": (_I, [_P, _P, _I64, _I, _I, _I, _I64, _F, _F, _P, _P, _P, _SZ, _P]),

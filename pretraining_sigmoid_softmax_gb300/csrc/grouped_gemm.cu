@@ -128,6 +128,8 @@ struct Params {
     const float* sa;           // FP8: scale of each A row (indexed by the global row)
     const float* sb0;          // FP8: scale of each B row (output channel), first B operand
     const float* sb1;          // FP8: second B operand (W_u of G1)
+    const float* row_scale;    // gate folded into the expert: G1 writes g*h, B2 forms g*dh
+    float* gate_part;          // B2 with row_scale: per row, (dy W_d) . h per 64 columns
     int ld_out;
     int* status;
     uint64_t wait_limit_ns;
@@ -416,8 +418,10 @@ __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const Ti
                 v[1][j] = __uint_as_float(u[j]);
             }
             if constexpr (C::FP8) fp8_scale<kOutCols>(v[0], v[1], P, row, ti, c);
+            const float rg = P.row_scale ? __ldg(P.row_scale + row) : 1.0f;
 #pragma unroll
-            for (int j = 0; j < kOutCols; ++j) v[2][j] = v[0][j] / (1.0f + __expf(-v[0][j])) * v[1][j];
+            for (int j = 0; j < kOutCols; ++j)
+                v[2][j] = v[0][j] / (1.0f + __expf(-v[0][j])) * v[1][j] * rg;
         } else {
             uint32_t r[kOutCols];
             tmem_ld16(t_acc + c, r);
@@ -493,6 +497,10 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
     const int64_t row = row0 + lane;
     const bool ok_row = row < ti.row_end;
     const int64_t base = row * (int64_t)P.ld_out + ti.n0;
+    // gate folded into the expert: dy is the ungated row gradient, dh = g (dy W_d), and the
+    // gate's gradient (dy W_d) . h is summed per 64-column group (h recomputed in fp32)
+    const float g = (P.row_scale && ok_row) ? __ldg(P.row_scale + row) : 1.0f;
+    float gpart = 0.f;
     for (int i = 0; i < nch; ++i, ++n) {
         const int c = c_lo + i * kAuCols;
         const int b = (int)(n % kAuBufs);
@@ -517,11 +525,18 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
                 for (int h = 0; h < 8; ++h) {
                     const float a = (h & 1) ? bf16_hi(aw[h >> 1]) : bf16_lo(aw[h >> 1]);
                     const float u = (h & 1) ? bf16_hi(uw[h >> 1]) : bf16_lo(uw[h >> 1]);
-                    const float dh = __uint_as_float(acc[8 * j + h]);
+                    const float acc_h = __uint_as_float(acc[8 * j + h]);
                     const float sa = 1.0f / (1.0f + __expf(-a));
+                    if (P.gate_part) gpart = fmaf(acc_h, a * sa * u, gpart);
+                    const float dh = acc_h * g;
                     dav[8 * j + h] = dh * u * sa * (1.0f + a * (1.0f - sa));
                     duv[8 * j + h] = dh * a * sa;
                 }
+            }
+            const int col = ti.n0 + c;
+            if (P.gate_part && (col + kAuCols) % 64 == 0) {  // last chunk of a 64-column group
+                P.gate_part[row * (int64_t)(P.ld_out / 64) + col / 64] = gpart;
+                gpart = 0.f;
             }
             uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
             uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
@@ -905,7 +920,8 @@ using namespace moe;
 extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int E, int64_t rows,
                               int d, int f, const moe_bf16* W_g, const moe_bf16* W_u,
                               const moe_bf16* W_d, moe_bf16* A, moe_bf16* U, moe_bf16* H,
-                              moe_bf16* Y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                              moe_bf16* Y, const float* row_gate, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
     (void)ws;
     (void)ws_bytes;
     if (!X || !W_g || !W_u || !W_d || !A || !U || !H || !Y) return MOE_ERR_INVALID_ARG;
@@ -929,6 +945,7 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
     P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
     P.ld_out = f;
+    P.row_scale = row_gate;
     CUtensorMap moa[3], moy[3];
     if (!out_maps(moa, A, U, H, f, rows) || !out_maps(moy, Y, nullptr, nullptr, d, rows))
         return MOE_ERR_LAUNCH;
@@ -955,10 +972,12 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
                               int E, int64_t rows, int d, int f, const moe_bf16* W_g,
                               const moe_bf16* W_u, const moe_bf16* W_d, moe_bf16* dX,
                               moe_bf16* dA, moe_bf16* dU, moe_bf16* dW_g, moe_bf16* dW_u,
-                              moe_bf16* dW_d, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                              moe_bf16* dW_d, const float* row_gate, float* gate_part, void* ws,
+                              size_t ws_bytes, moe_stream_t stream) {
     if (!dY || !X || !A || !U || !H || !W_g || !W_u || !W_d || !dX || !dA || !dU || !dW_g ||
         !dW_u || !dW_d)
         return MOE_ERR_INVALID_ARG;
+    if ((row_gate == nullptr) != (gate_part == nullptr)) return MOE_ERR_INVALID_ARG;
     if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
     const void* ptrs[14] = {dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d};
@@ -994,6 +1013,8 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.in0 = Ab;
         P.in1 = Ub;
         P.ld_out = f;
+        P.row_scale = row_gate;
+        P.gate_part = gate_part;
         if (f % 256 == 0)
             rc = launch<CfgSwigluBwdP>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st);
         else
@@ -1073,8 +1094,9 @@ extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int6
                                   int E, int64_t rows, int d, int f, const uint8_t* Wgq,
                                   const float* sWg, const uint8_t* Wuq, const float* sWu,
                                   const uint8_t* Wdq, const float* sWd, moe_bf16* A, moe_bf16* U,
-                                  moe_bf16* H, uint8_t* Hq, float* sH, moe_bf16* Y, void* ws,
-                                  size_t ws_bytes, moe_stream_t stream) {
+                                  moe_bf16* H, uint8_t* Hq, float* sH, moe_bf16* Y,
+                                  const float* row_gate, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
     (void)ws;
     (void)ws_bytes;
     if (!Xq || !sX || !Wgq || !sWg || !Wuq || !sWu || !Wdq || !sWd || !A || !U || !H || !Hq ||
@@ -1106,6 +1128,7 @@ extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int6
     P.sa = sX;
     P.sb0 = sWg;
     P.sb1 = sWu;
+    P.row_scale = row_gate;
     CUtensorMap moa[3], moy[3];
     if (!out_maps(moa, A, U, H, f, rows) || !out_maps(moy, Y, nullptr, nullptr, d, rows))
         return MOE_ERR_LAUNCH;

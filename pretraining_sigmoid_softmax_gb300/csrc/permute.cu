@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     float my_g = 0.f;
     if (lane < k) {
         my_row = slot_to_row[t * k + lane];
-        my_g = gate[t * k + lane];
+        my_g = gate ? gate[t * k + lane] : 1.0f;  // no gates: rows already carry them
     }
     const int nvec = d / 8;
     for (int c0 = 0; c0 < nvec; c0 += 32) {  // warp-uniform trip count
@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     }
 }
 
-// dY_perm[row(t,i)] = bf16(g[t,i] * dY[t]); dg[t,i] = <dY[t], Y_perm[row(t,i)]>.
+// dY_perm[row(t,i)] = bf16(g[t,i] * dY[t]); dg[t,i] = <dY[t], Y_perm[row(t,i)]>. Without
+// gates the rows are plain copies of dY[t]; without Y_perm no dg is formed.
 template <int KMAX>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ Y_perm,
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     float my_g = 0.f;
     if (lane < k) {
         my_row = slot_to_row[t * k + lane];
-        my_g = gate[t * k + lane];
+        my_g = gate ? gate[t * k + lane] : 1.0f;
     }
     float dot[KMAX];
 #pragma unroll
@@ -299,15 +300,17 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
                 const int32_t row = __shfl_sync(0xffffffffu, my_row, i);
                 const float g = __shfl_sync(0xffffffffu, my_g, i);
                 if (in && row >= 0) {
-                    const uint4 yv = reinterpret_cast<const uint4*>(Y_perm + (int64_t)row * d)[c];
-                    const uint32_t y[4] = {yv.x, yv.y, yv.z, yv.w};
-                    float s = dot[i];
+                    if (Y_perm) {
+                        const uint4 yv = reinterpret_cast<const uint4*>(Y_perm + (int64_t)row * d)[c];
+                        const uint32_t y[4] = {yv.x, yv.y, yv.z, yv.w};
+                        float s = dot[i];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        s = fmaf(dyf[2 * q], bf16_lo(y[q]), s);
-                        s = fmaf(dyf[2 * q + 1], bf16_hi(y[q]), s);
+                        for (int q = 0; q < 4; ++q) {
+                            s = fmaf(dyf[2 * q], bf16_lo(y[q]), s);
+                            s = fmaf(dyf[2 * q + 1], bf16_hi(y[q]), s);
+                        }
+                        dot[i] = s;
                     }
-                    dot[i] = s;
                     float o[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) o[q] = g * dyf[q];
@@ -316,6 +319,7 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
             }
         }
     }
+    if (!dg) return;
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
         if (i < k) {
@@ -325,6 +329,30 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
             if (lane == 0) dg[t * k + i] = s;
         }
     }
+}
+
+// row_gate[slot_to_row[s]] = gate[s] for every slot s (rows were zeroed first).
+__global__ void row_gates_kernel(const float* __restrict__ gate, const int32_t* __restrict__ slot_to_row,
+                                 int64_t n, int64_t rows, float* __restrict__ row_gate) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int32_t r = slot_to_row[i];
+    if (r >= 0 && r < rows) row_gate[r] = gate[i];
+}
+
+// dg[s] = sum_j part[slot_to_row[s], j], j = 0 .. nparts-1 in order.
+__global__ void gate_grad_kernel(const float* __restrict__ part, int nparts,
+                                 const int32_t* __restrict__ slot_to_row, int64_t n,
+                                 float* __restrict__ dg) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int32_t r = slot_to_row[i];
+    float s = 0.f;
+    if (r >= 0) {
+        const float* p = part + (int64_t)r * nparts;
+        for (int j = 0; j < nparts; ++j) s += p[j];
+    }
+    dg[i] = s;
 }
 
 // dx[t] = sum_i dX_perm[slot_to_row[t,i]] + dx_shared[t] + sum_e dlogits[t,e] W_r[e].
@@ -461,7 +489,7 @@ extern "C" int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T
 extern "C" int moe_combine(const moe_bf16* Y_perm, const float* topk_gate,
                            const int32_t* slot_to_row, const moe_bf16* Y_shared, int64_t T,
                            int d, int k, moe_bf16* out, moe_stream_t stream) {
-    if (!Y_perm || !topk_gate || !slot_to_row || !out) return MOE_ERR_INVALID_ARG;
+    if (!Y_perm || !slot_to_row || !out) return MOE_ERR_INVALID_ARG;
     if (!shape_ok(T, d, 1, k)) return MOE_ERR_INVALID_ARG;
     if (k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(Y_perm) || !aligned16(out) || (Y_shared && !aligned16(Y_shared)))
@@ -497,12 +525,13 @@ extern "C" int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm,
                                const int64_t* row_offsets, const int32_t* perm_token,
                                int64_t T, int d, int E, int k, moe_bf16* dY_perm, float* dg,
                                moe_stream_t stream) {
-    if (!dY || !Y_perm || !topk_gate || !slot_to_row || !row_offsets || !perm_token ||
-        !dY_perm || !dg)
+    if (!dY || !slot_to_row || !row_offsets || !perm_token || !dY_perm)
         return MOE_ERR_INVALID_ARG;
+    if ((Y_perm == nullptr) != (dg == nullptr)) return MOE_ERR_INVALID_ARG;
     if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
-    if (!aligned16(dY) || !aligned16(Y_perm) || !aligned16(dY_perm)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dY) || (Y_perm && !aligned16(Y_perm)) || !aligned16(dY_perm))
+        return MOE_ERR_INVALID_ARG;
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     const __nv_bfloat16* dYb = reinterpret_cast<const __nv_bfloat16*>(dY);
@@ -514,6 +543,29 @@ extern "C" int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm,
     else if (k <= 16) combine_bwd_kernel<16><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
     else combine_bwd_kernel<32><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
     zero_pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    return launch_status();
+}
+
+extern "C" int moe_row_gates(const float* topk_gate, const int32_t* slot_to_row, int64_t T, int k,
+                             int64_t rows, float* row_gate, moe_stream_t stream) {
+    if (!topk_gate || !slot_to_row || !row_gate || T <= 0 || k <= 0 || rows <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(row_gate, 0, sizeof(float) * rows, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+    const int64_t n = T * k;
+    row_gates_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(topk_gate, slot_to_row, n, rows, row_gate);
+    return launch_status();
+}
+
+extern "C" int moe_gate_grad(const float* gate_part, const int32_t* slot_to_row, int64_t T, int k,
+                             int f, float* dg, moe_stream_t stream) {
+    if (!gate_part || !slot_to_row || !dg || T <= 0 || k <= 0 || f <= 0 || f % 64 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    const int64_t n = T * k;
+    gate_grad_kernel<<<(unsigned)cdiv(n, 256), 256, 0, (cudaStream_t)stream>>>(gate_part, f / 64,
+                                                                              slot_to_row, n, dg);
     return launch_status();
 }
 

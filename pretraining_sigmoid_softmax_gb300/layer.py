@@ -71,6 +71,10 @@ class MoEPlan:
         self.U = _empty((R, f), bf, dev)
         self.H = _empty((R, f), bf, dev)
         self.Y_perm = _empty((R, d), bf, dev)
+        # bf16 experts take each row's gate inside (g * h before the linear down projection);
+        # the FP8 experts quantise the ungated h, so there the combine applies the gates
+        self.fold_gate = not s.fp8
+        self.row_gate = _empty((R,), f32, dev) if self.fold_gate else None
         self.out = _empty((T, d), bf, dev)
         if fs:
             self.As = _empty((T, fs), bf, dev)
@@ -99,6 +103,8 @@ class MoEPlan:
                 self.dlogits_aux = _empty((T, E), f32, dev)
             self.dY_perm = _empty((R, d), bf, dev)
             self.dg = _empty((T, k), f32, dev)
+            if self.fold_gate:  # gate-gradient partial sums of the expert backward
+                self.gate_part = _empty((R, f // 64), f32, dev)
             self.dA = _empty((R, f), bf, dev)
             self.dU = _empty((R, f), bf, dev)
             self.dX_perm = _empty((R, d), bf, dev)
@@ -121,24 +127,26 @@ class MoEPlan:
     # step without adding synchronisation).
     gemm_events = None
 
-    def _gemm(self, fn, *args, stream=None):
+    def _gemm(self, fn, *args, stream=None, **kw):
         if self.gemm_events is None:
-            fn(*args, stream)
+            fn(*args, stream, **kw)
             return
         st = stream if stream is not None else torch.cuda.current_stream()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
-        fn(*args, stream)
+        fn(*args, stream, **kw)
         b.record(st)
         self.gemm_events.append((a, b))
 
     def launches_per_step(self, backward=True, bias_update=False) -> int:
         """Kernel launches of one step through this plan (what the entry points enqueue)."""
         s = self.s
-        n = 1 + (1 if s.mode == ops.MODE_SOFTMAX else 0)   # route (+ z-loss reduction)
+        n = 1 + (1 if s.E <= 128 else 0)                   # route (W_r pieces + tensor-core
+        n += 1 if s.mode == ops.MODE_SOFTMAX else 0         # logits) (+ z-loss reduction)
         if s.has_aux:
             n += 2 + (1 if backward else 0)                 # balancing losses (+ gradient)
         n += 5                                              # permute
+        n += 1 if not s.fp8 else 0                          # row gates (folded gates)
         if s.fp8:  # quantise X, W_g, W_u, W_d; G1, quantise H, G2 (shared: the same)
             n += 7 + (7 if s.f_shared else 0)
         else:
@@ -146,6 +154,7 @@ class MoEPlan:
         n += 1                                              # combine
         if backward:
             n += 2                                          # combine backward + padding rows
+            n += 1 if not s.fp8 else 0                      # gate gradient from its partials
             n += 5 + (4 if s.f_shared else 0)               # expert backward (+ expert order)
             n += 3                                          # router backward
             n += 1                                          # input gradient
@@ -168,6 +177,10 @@ class MoEPlan:
                              s.aux_seq, self.aux_loss, self.aux_f, self.ws, stream)
         ops.moe_permute(self.topk_idx, x, s.E, self.counts, self.offsets, self.row_offsets,
                         self.perm_token, self.slot_to_row, self.X_perm, self.ws, stream)
+        # the combine's gate weights move before the (linear) down projection: the routed
+        # experts emit g * y directly, and the combine adds rows without weights
+        if self.fold_gate:
+            ops.moe_row_gates(self.topk_gate, self.slot_to_row, self.row_gate, stream)
         ys = None
         if s.fp8:
             q = ops.moe_quantize_rows_fp8
@@ -189,12 +202,13 @@ class MoEPlan:
                 ys = self.Ys
         else:
             self._gemm(ops.moe_expert_fwd, self.X_perm, self.row_offsets, W_g, W_u, W_d, self.A,
-                       self.U, self.H, self.Y_perm, self.ws, stream=stream)
+                       self.U, self.H, self.Y_perm, self.ws, stream=stream, row_gate=self.row_gate)
             if s.f_shared:
                 self._gemm(ops.moe_expert_fwd, x, None, Ws_g[None], Ws_u[None], Ws_d[None],
                            self.As, self.Us, self.Hs, self.Ys, self.ws, stream=stream)
                 ys = self.Ys
-        ops.moe_combine(self.Y_perm, self.topk_gate, self.slot_to_row, ys, self.out, stream)
+        ops.moe_combine(self.Y_perm, None if self.fold_gate else self.topk_gate, self.slot_to_row,
+                        ys, self.out, stream)
         return self.out
 
     # ----------------------------------------------------------------- backward
@@ -203,11 +217,22 @@ class MoEPlan:
         x = self.x
         W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d = self.W
         softmax = s.mode == ops.MODE_SOFTMAX
-        ops.moe_combine_bwd(dY, self.Y_perm, self.topk_gate, self.slot_to_row, self.row_offsets,
-                            self.perm_token, self.dY_perm, self.dg, stream)
-        self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
-                   self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU, self.dW_g,
-                   self.dW_u, self.dW_d, self.ws, stream=stream)
+        if self.fold_gate:
+            # gate folded into the experts: dY_perm holds plain copies of the token gradients,
+            # the expert backward applies each row's gate and sums the gate's gradient in parts
+            ops.moe_combine_bwd(dY, None, None, self.slot_to_row, self.row_offsets,
+                                self.perm_token, self.dY_perm, None, stream)
+            self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
+                       self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
+                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
+                       row_gate=self.row_gate, gate_part=self.gate_part)
+            ops.moe_gate_grad(self.gate_part, self.slot_to_row, s.f, self.dg, stream)
+        else:
+            ops.moe_combine_bwd(dY, self.Y_perm, self.topk_gate, self.slot_to_row,
+                                self.row_offsets, self.perm_token, self.dY_perm, self.dg, stream)
+            self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
+                       self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
+                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
         dxs = None
         if s.f_shared:
             self._gemm(ops.moe_expert_bwd, dY, x, self.As, self.Us, self.Hs, None, Ws_g[None],

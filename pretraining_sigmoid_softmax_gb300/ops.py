@@ -103,12 +103,13 @@ def moe_permute_noalloc(topk_idx, x, E, counts, offsets, row_offsets, perm_token
            "moe_permute_noalloc")
 
 
-def moe_expert_fwd(X, row_offsets, W_g, W_u, W_d, A, U, H, Y, ws, stream=None):
+def moe_expert_fwd(X, row_offsets, W_g, W_u, W_d, A, U, H, Y, ws, stream=None, row_gate=None):
+    """row_gate [rows] fp32 (from moe_row_gates) folds each row's gate into h and y."""
     rows, d = X.shape
     E, f, _ = W_g.shape
-    _contig(X, W_g, W_u, W_d, A, U, H, Y, ws)
+    _contig(X, W_g, W_u, W_d, A, U, H, Y, ws, row_gate)
     _check(_lib.load().moe_expert_fwd(_p(X), _p(row_offsets), E, rows, d, f, _p(W_g), _p(W_u),
-                                      _p(W_d), _p(A), _p(U), _p(H), _p(Y), _p(ws),
+                                      _p(W_d), _p(A), _p(U), _p(H), _p(Y), _p(row_gate), _p(ws),
                                       0 if ws is None else ws.numel(), _stream(stream)),
            "moe_expert_fwd")
 
@@ -123,19 +124,21 @@ def moe_quantize_rows_fp8(X, rows_limit, Q, scale, stream=None):
 
 
 def moe_expert_fwd_fp8(Xq, sX, row_offsets, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y,
-                       ws, stream=None):
+                       ws, stream=None, row_gate=None):
     rows, d = Xq.shape
     E, f, _ = Wgq.shape
-    _contig(Xq, sX, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y)
+    _contig(Xq, sX, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y, row_gate)
     _check(_lib.load().moe_expert_fwd_fp8(_p(Xq), _p(sX), _p(row_offsets), E, rows, d, f,
                                           _p(Wgq), _p(sWg), _p(Wuq), _p(sWu), _p(Wdq), _p(sWd),
-                                          _p(A), _p(U), _p(H), _p(Hq), _p(sH), _p(Y), _p(ws),
-                                          0 if ws is None else ws.numel(), _stream(stream)),
+                                          _p(A), _p(U), _p(H), _p(Hq), _p(sH), _p(Y),
+                                          _p(row_gate), _p(ws), 0 if ws is None else ws.numel(),
+                                          _stream(stream)),
            "moe_expert_fwd_fp8")
 
 
 def moe_combine(Y_perm, topk_gate, slot_to_row, Y_shared, out, stream=None):
-    T, k = topk_gate.shape
+    """topk_gate None: the rows of Y_perm already carry their gates."""
+    T, k = slot_to_row.shape
     d = Y_perm.shape[1]
     _contig(Y_perm, topk_gate, slot_to_row, Y_shared, out)
     _check(_lib.load().moe_combine(_p(Y_perm), _p(topk_gate), _p(slot_to_row), _p(Y_shared), T, d,
@@ -159,7 +162,8 @@ def moe_bias_update_proportional(counts, T, k, gamma, b, stream=None):
 
 def moe_combine_bwd(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm, dg,
                     stream=None):
-    T, k = topk_gate.shape
+    """topk_gate None: plain row copies; Y_perm and dg None: no gate gradient."""
+    T, k = slot_to_row.shape
     d = dY.shape[1]
     E = row_offsets.shape[0] - 1
     _contig(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm, dg)
@@ -169,15 +173,30 @@ def moe_combine_bwd(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token,
 
 
 def moe_expert_bwd(dY, X, A, U, H, row_offsets, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws,
-                   stream=None):
+                   stream=None, row_gate=None, gate_part=None):
+    """row_gate with gate_part [rows, f/64] fp32: the gate-folded backward (see the header)."""
     rows, d = X.shape
     E, f, _ = W_g.shape
-    _contig(dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws)
+    _contig(dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws, row_gate, gate_part)
     _check(_lib.load().moe_expert_bwd(_p(dY), _p(X), _p(A), _p(U), _p(H), _p(row_offsets), E, rows,
                                       d, f, _p(W_g), _p(W_u), _p(W_d), _p(dX), _p(dA), _p(dU),
-                                      _p(dW_g), _p(dW_u), _p(dW_d), _p(ws),
-                                      0 if ws is None else ws.numel(), _stream(stream)),
+                                      _p(dW_g), _p(dW_u), _p(dW_d), _p(row_gate), _p(gate_part),
+                                      _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "moe_expert_bwd")
+
+
+def moe_row_gates(topk_gate, slot_to_row, row_gate, stream=None):
+    T, k = topk_gate.shape
+    _contig(topk_gate, slot_to_row, row_gate)
+    _check(_lib.load().moe_row_gates(_p(topk_gate), _p(slot_to_row), T, k, row_gate.numel(),
+                                     _p(row_gate), _stream(stream)), "moe_row_gates")
+
+
+def moe_gate_grad(gate_part, slot_to_row, f, dg, stream=None):
+    T, k = slot_to_row.shape
+    _contig(gate_part, slot_to_row, dg)
+    _check(_lib.load().moe_gate_grad(_p(gate_part), _p(slot_to_row), T, k, f, _p(dg),
+                                     _stream(stream)), "moe_gate_grad")
 
 
 def moe_route_bwd(dg, x, topk_idx, topk_gate, topk_score, logits, lse, E, mode, z_coef, dlogits,

@@ -264,6 +264,93 @@ def test_routed_expert_gemms(counts, d, f):
             assert (B[name][lo + c:int(ro[e + 1])].float() == 0).all(), f"{name} padding {e}"
 
 
+# -------------------------------------------------- gate folded into the experts
+
+@pytest.mark.parametrize("counts,d,f", [([130, 0, 5, 256, 1], 256, 256), ([77, 300, 0], 384, 128)])
+def test_gate_folded_expert_path(counts, d, f):
+    """moe_expert_fwd / moe_expert_bwd with row gates: h and y carry the gate, dh = g (dy W_d),
+    and the gate-gradient partials sum to <dy, y> (the combine's gate gradient)."""
+    E = len(counts)
+    g = torch.Generator().manual_seed(sum(counts) + 7 * f)
+    ro = padded_offsets(counts)
+    rows = int(ro[-1]) + 128
+    X = torch.zeros(rows, d, dtype=torch.bfloat16)
+    dY = torch.zeros(rows, d, dtype=torch.bfloat16)
+    gate = torch.zeros(rows)
+    for e in range(E):
+        X[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g)
+        dY[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g, 0.25)
+        gate[ro[e]:ro[e] + counts[e]] = torch.rand(counts[e], generator=g) * 0.9 + 0.05
+    W_g, W_u, W_d = _weights(E, d, f, g)
+    B = _expert_buffers(rows, d, f, E)
+    ws = _ws(rows, d, E, 1)
+    rod = dev(torch.from_numpy(ro))
+    rg = dev(gate)
+    part = torch.full((rows, f // 64), float("nan"), device="cuda")
+    ops.moe_expert_fwd(dev(X), rod, dev(W_g), dev(W_u), dev(W_d), B["A"], B["U"], B["H"], B["Y"],
+                       ws, row_gate=rg)
+    ops.moe_expert_bwd(dev(dY), dev(X), B["A"], B["U"], B["H"], rod, dev(W_g), dev(W_u), dev(W_d),
+                       B["dX"], B["dA"], B["dU"], B["dW_g"], B["dW_u"], B["dW_d"], ws,
+                       row_gate=rg, gate_part=part)
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    rnd = O.bf16_round
+    for e in range(E):
+        lo, c = int(ro[e]), counts[e]
+        if c == 0:
+            for name in ("dW_g", "dW_u", "dW_d"):
+                assert (B[name][e].float() == 0).all()
+            continue
+        hi = lo + c
+        x, gv, dy = h64(X[lo:hi]), h64(gate[lo:hi])[:, None], h64(dY[lo:hi])
+        a, u, h, y = O.swiglu_expert(x, h64(W_g[e]), h64(W_u[e]), h64(W_d[e]), rnd)
+        assert_close(B["A"][lo:hi], a, f"expert {e} A")
+        a_acc, u_acc = x @ h64(W_g[e]).T, x @ h64(W_u[e]).T  # before their bf16 rounding
+        h_g = rnd(gv * O.silu(a_acc) * u_acc)  # the gated h, rounded where it is stored
+        assert_close(B["H"][lo:hi], h_g, f"expert {e} gated h")
+        assert_gemm_exact(B["Y"][lo:hi], h64(B["H"][lo:hi]), h64(W_d[e]).T, f"expert {e} gated y")
+        assert_close(B["Y"][lo:hi], gv * y, f"expert {e} gated y vs g y")
+        # upstream gradient g dy; dW_d = (g dy)^T (h_g / g) = dy^T h_g, the stored operand
+        gr = O.expert_backward(gv * dy, x, a, u, h_g / gv, h64(W_g[e]), h64(W_u[e]),
+                               h64(W_d[e]), rnd)
+        for name in ("dA", "dU", "dX"):
+            assert_close(B[name][lo:hi], gr[name], f"expert {e} {name}")
+        for name in ("dW_g", "dW_u", "dW_d"):
+            assert_close(B[name][e], gr[name], f"expert {e} {name}", reduction=True)
+        dg = part[lo:hi].double().sum(1).cpu().numpy()
+        # (dy W_d) . silu(a) u over the stored a, u (the kernel's own operands; the oracle's
+        # a, u can round to the neighbouring bf16 value): <dy, y> of the ungated y = h W_d^T
+        A_s, U_s = h64(B["A"][lo:hi]), h64(B["U"][lo:hi])
+        ref = ((dy @ h64(W_d[e])) * O.silu(A_s) * U_s).sum(1)
+        assert_close(dg, ref, f"expert {e} gate gradient", atol=1e-3, rtol=1e-3, reduction=True)
+        # padding rows of the segment stay zero
+        for name in ("A", "U", "H", "Y", "dA", "dU", "dX"):
+            assert (B[name][hi:int(ro[e + 1])].float() == 0).all(), f"{name} padding {e}"
+
+
+def test_row_gates_and_gate_gradient_are_bit_exact():
+    g = torch.Generator().manual_seed(61)
+    T, d, E, k, f = 900, 128, 12, 3, 384
+    idx = _random_choice(T, E, k, g, skew=True)
+    P = _permute(idx, randn_bf16((T, d), g), E)
+    R = P["X_perm"].shape[0]
+    gate = torch.rand(T, k, generator=g)
+    row_gate = torch.full((R,), float("nan"), device="cuda")
+    ops.moe_row_gates(dev(gate), P["slot_to_row"], row_gate)
+    s2r = P["slot_to_row"].cpu().numpy().reshape(-1)
+    want = np.zeros(R, np.float32)
+    want[s2r] = gate.numpy().reshape(-1)
+    assert np.array_equal(row_gate.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    part = torch.randn(R, f // 64, generator=g)
+    dg = torch.empty(T, k, device="cuda")
+    ops.moe_gate_grad(dev(part), P["slot_to_row"], f, dg)
+    acc = np.zeros(T * k, np.float32)
+    pn = part.numpy()[s2r]
+    for j in range(f // 64):  # fp32, in order of j
+        acc = (acc + pn[:, j]).astype(np.float32)
+    assert np.array_equal(dg.cpu().numpy().reshape(-1).view(np.uint32), acc.view(np.uint32))
+
+
 # ------------------------------------------------------------- combine and backward
 
 def test_combine_and_backward_kernels():
@@ -297,6 +384,17 @@ def test_combine_and_backward_kernels():
     assert_close(dg, rdg, "dg", atol=1e-4, rtol=1e-4, reduction=True)
     pad = torch.from_numpy(np.setdiff1d(np.arange(int(ro[-1])), rows)).cuda()
     assert (dY_perm[pad].float() == 0).all()
+    # rows that already carry their gates: unweighted sum; backward: plain row copies
+    out1 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    ops.moe_combine(dev(Y_perm), None, P["slot_to_row"], dev(Ys), out1)
+    assert_close(out1, O.combine(Yp64, np.ones((T, k)), D["slot_to_row"], h64(Ys), O.bf16_round),
+                 "combine without gates")
+    dY_copy = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ops.moe_combine_bwd(dev(dY), None, None, P["slot_to_row"], P["row_offsets"], P["perm_token"],
+                        dY_copy, None)
+    assert torch.equal(dY_copy[torch.from_numpy(rows).cuda()].cpu(),
+                       dY[torch.from_numpy(D["perm_token"])])
+    assert (dY_copy[pad].float() == 0).all()
     # input gradient with shared and router terms
     dX_perm = torch.zeros(R, d, dtype=torch.bfloat16)
     dX_perm[torch.from_numpy(rows)] = randn_bf16((T * k, d), g)

@@ -85,8 +85,10 @@ def full_parity(cfg, inp):
     idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
     i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
     aux = (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
+    # the bf16 layer folds each slot's gate into its expert (stored h and y carry the gate)
+    fp8 = cfg.precision == "fp8"
     fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND, aux=aux,
-                          fp8=cfg.precision == "fp8")
+                          fp8=fp8, fold_gate=not fp8)
     assert_close(plan.topk_gate, fwd["gate"], "gates", atol=1e-6, rtol=1e-5)
     if aux is not None:
         assert float(plan.aux_loss[0]) == pytest.approx(fwd["aux_switch"], rel=1e-5)
@@ -188,11 +190,13 @@ def test_workload_sampled_parity(name):
         dl_aux = O.aux_losses_backward(lg, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
     fp8 = cfg.precision == "fp8"
     for j, t in enumerate(toks):
-        o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND, fp8=fp8)
+        o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND, fp8=fp8,
+                            fold_gate=not fp8)
         assert_close(out[j], o, f"out[{t}]")
         tb = O.token_backward(lazy, int(t), lg[t], idx[t], cfg.mode, cfg.k,
                               O.to64(inp["dY"][t]), cfg.z_coef, cfg.T, rnd=RND,
-                              dl_extra_t=None if dl_aux is None else dl_aux[t], fp8=fp8)
+                              dl_extra_t=None if dl_aux is None else dl_aux[t], fp8=fp8,
+                              fold_gate=not fp8)
         assert_close(dx[j], tb["dx"], f"dx[{t}]")
     counts = D["counts"]
     live = np.nonzero(counts)[0]
@@ -209,7 +213,7 @@ def test_workload_sampled_parity(name):
             {"x": O.to64(inp["x"][torch.from_numpy(tok_e)]), "W_g": lazy["W_g"],
              "W_u": lazy["W_u"], "W_d": lazy["W_d"]},
             e, np.arange(hi - lo), gates, O.to64(inp["dY"][torch.from_numpy(tok_e)]), ed, eg,
-            rnd=RND, fp8=fp8)
+            rnd=RND, fp8=fp8, fold_gate=not fp8)
         got_d = [float(plan.dW_d[e, i, j]) for (i, j) in ed]
         got_g = [float(plan.dW_g[e, j, i]) for (j, i) in eg]
         got_u = [float(plan.dW_u[e, j, i]) for (j, i) in eg]

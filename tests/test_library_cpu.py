@@ -64,7 +64,7 @@ def test_argument_checks_return_before_any_device_work(lib):
     rc = lib.moe_permute(None, None, 16, 128, 8, 2, None, None, None, None, None, None, None, 0, None)
     assert rc == 1
     rc = lib.moe_expert_fwd(None, None, 1, 16, 128, 128, None, None, None, None, None, None, None,
-                            None, 0, None)
+                            None, None, 0, None)
     assert rc == 1
     rc = lib.moe_bias_update(None, 8, 16, 2, 0.001, None, None)
     assert rc == 1

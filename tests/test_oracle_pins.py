@@ -280,6 +280,43 @@ def test_backward_matches_central_finite_differences(mode, aux):
         assert np.abs(ana - num).max() / scale < 1e-6, p
 
 
+@pytest.mark.parametrize("mode,fs,aux", [("sigmoid", 0, None), ("sigmoid", 4, (5, 0.2, 0.3)),
+                                         ("softmax", 0, None)])
+def test_gate_folded_into_experts_is_the_same_layer(mode, fs, aux):
+    """Applying each slot's gate inside its expert (g * h before the linear down projection)
+    and combining without weights is the same layer in exact arithmetic: outputs, every
+    gradient and the gate gradient (sum_j (dy W_d)_j h_j) agree with the plain layer."""
+    rng = np.random.default_rng(31)
+    inp = _tiny_inputs(rng, T=30, d=8, E=5, f=6, fs=fs)
+    z = 0.05 if mode == "softmax" else 0.0
+    dY = rng.standard_normal((30, 8))
+    f0 = O.layer_forward(inp, mode, 2, z, aux=aux)
+    f1 = O.layer_forward(inp, mode, 2, z, aux=aux, fold_gate=True)
+    np.testing.assert_allclose(f1["out"], f0["out"], rtol=1e-12, atol=1e-13)
+    assert not np.allclose(f1["H"], f0["H"])  # the stored h really carries the gate
+    b0 = O.layer_backward(inp, f0, dY)
+    b1 = O.layer_backward(inp, f1, dY)
+    for name in ("dg", "dx", "dW_r", "dW_g", "dW_u", "dW_d", "dlogits"):
+        np.testing.assert_allclose(b1[name], b0[name], rtol=1e-11, atol=1e-12, err_msg=name)
+    # the per-token and per-entry forms used at large sizes, folded, give the same values
+    for t in (0, 17):
+        o = O.token_forward(inp, t, f1["idx"][t], f1["gate"][t], fold_gate=True)
+        np.testing.assert_allclose(o, f0["out"][t], rtol=1e-12, atol=1e-13)
+        if aux is None:
+            tb = O.token_backward(inp, t, f1["logits"][t], f1["idx"][t], mode, 2, dY[t], z, 30,
+                                  fold_gate=True)
+            np.testing.assert_allclose(tb["dx"], b0["dx"][t], rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(tb["dg"], b0["dg"][t], rtol=1e-11, atol=1e-12)
+    e = int(np.argmax(np.diff(f1["offsets"])))
+    rows = np.arange(f1["offsets"][e], f1["offsets"][e + 1])
+    tok, sl = f1["perm_token"][rows], f1["perm_slot"][rows]
+    ed, eg = [(1, 2), (7, 5)], [(3, 4), (0, 7)]
+    w0 = O.expert_weight_grad_entries(inp, e, tok, f1["gate"][tok, sl], dY, ed, eg)
+    w1 = O.expert_weight_grad_entries(inp, e, tok, f1["gate"][tok, sl], dY, ed, eg, fold_gate=True)
+    for name in ("dW_d", "dW_g", "dW_u"):
+        np.testing.assert_allclose(w1[name], w0[name], rtol=1e-11, atol=1e-13)
+
+
 def test_sampled_rows_equal_full_layer():
     """The per-token and per-entry evaluations used at large sizes agree with the whole
     layer."""
