@@ -10,18 +10,19 @@
 // fp32 through bf16 tensor cores. The fp32 operand (W_r forward, the logit gradient
 // backward) is split into three bf16 pieces that sum to it within 2^-24 relative (see
 // split3_bf16); the other operand (x) is bf16 already. Every product of two bf16 values is
-// exact in fp32, and the tensor core adds the three pieces' products into one fp32
-// accumulator, so the result is an fp32 contraction of the exact operands, as the router's
-// definition asks. The contraction is thin (E <= 128 outputs per token), so after the split
+// exact in fp32; the tensor core sums each piece's products in fp32 and the three partial
+// sums are added in fp32 (largest first), so the result is an fp32 contraction of the exact
+// operands, as the router's definition asks. The contraction is thin (E <= 128 outputs per token), so after the split
 // it is bound by reading x once from HBM rather than by arithmetic.
 //
 // Logits kernel: persistent, one CTA per SM, 128-token tiles. Warp 0 issues TMA loads of
-// the x tile (128 tokens x 64 of d) and of the three W_r pieces (epad experts x 64 of d)
-// into a ring of stages; warp 1 issues 3 x 4 tcgen05.mma (M = 128, N = epad, K = 16) per
-// stage into one of two TMEM accumulators; warps 4-7 each own 32 tokens (one TMEM lane per
-// token) and run the choice per thread, re-reading the token's logits from TMEM per pass:
-// k passes each pick the best expert not yet taken, in the order "larger value, then lower
-// index". The choice is therefore the same total order as the definition's.
+// the x tile (128 tokens x 64 of d) and of the three W_r pieces (epad experts x 64 of d,
+// back to back: a 3 epad-row operand) into a ring of stages; warp 1 issues one tcgen05.mma
+// (M = 128, N = 3 epad, K = 16; two of half the width when 3 epad > 256) per K step, which
+// leaves the three partial logits side by side in TMEM. Warps 4-7 each own 32 tokens (one
+// TMEM lane per token): a first pass adds the partials, writes the logits and parks logits
+// and selection values back in TMEM (tcgen05.st); then k passes each pick the best expert not
+// yet taken, in the order "larger value, then lower index" - the definition's total order.
 //
 // dW_r kernel: the transposed product dW_r^T[j][e] = sum_t x[t][j] dlogits[t][e], as
 // 128-column tiles of d (M) by np experts (N), K running over tokens. The token axis is
@@ -157,59 +158,80 @@ struct LogitCfg {
     static constexpr int B_BYTES = 3 * EPAD * 128;  // 3 pieces x EPAD experts x 64 bf16 of d
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (kTcSmemBudget / STAGE_BYTES) > 6 ? 6 : (kTcSmemBudget / STAGE_BYTES);
-    static constexpr int TMEM_COLS = 2 * EPAD;      // two accumulators
-    static constexpr uint32_t IDESC = idesc_mma(EPAD, 128, false, false);
+    // The three pieces sit back to back in a stage, a 3*EPAD-row B tile: one MMA of
+    // N = 3*EPAD per K step (two of half that when it exceeds 256) accumulates the three
+    // partial logits side by side in TMEM; the epilogue adds them.
+    static constexpr int NTOT = 3 * EPAD;
+    static constexpr int NMMA = NTOT <= 256 ? 1 : 2;
+    static constexpr int NPER = NTOT / NMMA;
+    static constexpr int NBUF = 2 * NTOT <= 512 ? 2 : 1;  // accumulators in flight
+    static constexpr int TMEM_COLS = NBUF * NTOT <= 256 ? 256 : 512;
+    static constexpr uint32_t IDESC = idesc_mma(NPER, 128, false, false);
     static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + kTcMisc + sizeof(float) * EPAD;
     static_assert(EPAD % 32 == 0 && EPAD >= 32 && EPAD <= 128, "expert tile");
     static_assert(STAGES >= 2, "pipeline depth");
 };
 
-// One token's choice from its logits in TMEM (32 columns per tcgen05.ld). Executed by all
-// 32 lanes of the warp together (tcgen05.ld is warp-collective); `live` masks the stores of
-// rows past the last token.
+// One token's choice from its three partial logits in TMEM (columns [0, EPAD), [EPAD,
+// 2 EPAD), [2 EPAD, 3 EPAD) of its lane). A first pass adds the partials, writes the logits,
+// and parks each logit and selection value (sigmoid + bias, or the logit) back in TMEM; the
+// k choice passes then read those. Executed by all 32 lanes of the warp together
+// (tcgen05.ld/st are warp-collective); `live` masks the stores of rows past the last token.
 template <int EPAD>
 __device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool live,
                                                  const LogitParams& P, const float* sbias) {
     constexpr int NCH = EPAD / 32;
     const int E = P.E, k = P.k;
     const bool sig = P.mode == MOE_MODE_SIGMOID;
-    uint32_t v[32];
+    const uint32_t t_l = t_acc;          // logits (over the first partial)
+    const uint32_t t_v = t_acc + EPAD;   // selection values (over the second)
     float mx = -INFINITY, sum = 0.f;
-    if (P.logits || !sig) {
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            tmem_ld32(t_acc + 32 * c, v);
-            tmem_ld_wait();
-            if (live && P.logits) {
-                float* row = P.logits + t * E;
-                if (P.vec_logits) {
+    for (int c = 0; c < NCH; ++c) {
+        uint32_t p0[32], p1[32], p2[32];
+        tmem_ld32(t_acc + 32 * c, p0);
+        tmem_ld32(t_acc + EPAD + 32 * c, p1);
+        tmem_ld32(t_acc + 2 * EPAD + 32 * c, p2);
+        tmem_ld_wait();
+        uint32_t lv[32], vv[32];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        if (32 * c + 4 * q < E)
-                            *reinterpret_cast<float4*>(row + 32 * c + 4 * q) =
-                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                } else {
+        for (int j = 0; j < 32; ++j) {
+            const int e = 32 * c + j;
+            const float l = (__uint_as_float(p0[j]) + __uint_as_float(p1[j])) + __uint_as_float(p2[j]);
+            float val = sig ? route_sigmoid(l) + sbias[e] : l;
+            if (val != val) val = -INFINITY;  // a NaN never wins
+            if (!sig && e < E) mx = fmaxf(mx, l);
+            lv[j] = __float_as_uint(l);
+            vv[j] = __float_as_uint(val);
+        }
+        if (live && P.logits) {
+            float* row = P.logits + t * E;
+            if (P.vec_logits) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (32 * c + j < E) row[32 * c + j] = __uint_as_float(v[j]);
-                }
-            }
-            if (!sig) {
+                for (int q = 0; q < 8; ++q)
+                    if (32 * c + 4 * q < E)
+                        *reinterpret_cast<float4*>(row + 32 * c + 4 * q) =
+                            make_float4(__uint_as_float(lv[4 * q]), __uint_as_float(lv[4 * q + 1]),
+                                        __uint_as_float(lv[4 * q + 2]), __uint_as_float(lv[4 * q + 3]));
+            } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (32 * c + j < E) mx = fmaxf(mx, __uint_as_float(v[j]));
+                    if (32 * c + j < E) row[32 * c + j] = __uint_as_float(lv[j]);
             }
         }
+        tmem_st32(t_l + 32 * c, lv);
+        tmem_st32(t_v + 32 * c, vv);
     }
-    if (!sig) {  // softmax statistics over all experts
+    tmem_st_wait();
+    if (!sig) {  // softmax normaliser over all experts
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            tmem_ld32(t_acc + 32 * c, v);
+            uint32_t lv[32];
+            tmem_ld32(t_l + 32 * c, lv);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (32 * c + j < E) sum += expf(__uint_as_float(v[j]) - mx);
+                if (32 * c + j < E) sum += expf(__uint_as_float(lv[j]) - mx);
         }
     }
     uint32_t taken[NCH];
@@ -224,20 +246,18 @@ __device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool
         int be = 0x7fffffff;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            tmem_ld32(t_acc + 32 * c, v);
+            uint32_t vv[32], lv[32];
+            tmem_ld32(t_v + 32 * c, vv);
+            tmem_ld32(t_l + 32 * c, lv);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int e = 32 * c + j;
-                if (e < E && !((taken[c] >> j) & 1u)) {
-                    const float l = __uint_as_float(v[j]);
-                    float val = sig ? route_sigmoid(l) + sbias[e] : l;
-                    if (val != val) val = -INFINITY;  // a NaN never wins
-                    if (route_better(val, e, bv, be)) {
-                        bv = val;
-                        be = e;
-                        bl = l;
-                    }
+                const float val = __uint_as_float(vv[j]);
+                if (e < E && !((taken[c] >> j) & 1u) && route_better(val, e, bv, be)) {
+                    bv = val;
+                    be = e;
+                    bl = __uint_as_float(lv[j]);
                 }
             }
         }
@@ -311,12 +331,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t phase = 0;
         int local = 0;
         for (int64_t tile = blockIdx.x; tile < P.ntiles; tile += gridDim.x, ++local) {
-            const int buf = local & 1;
-            if (!mbar_wait_bounded(smem_u32(&R.tempty[buf]), ((local >> 1) & 1) ^ 1u, abort_flag,
-                                   P.status, P.wait_limit_ns, 41))
+            const int buf = C::NBUF == 2 ? (local & 1) : 0;
+            const uint32_t use = C::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
+            if (!mbar_wait_bounded(smem_u32(&R.tempty[buf]), use ^ 1u, abort_flag, P.status,
+                                   P.wait_limit_ns, 41))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + buf * EPAD;
+            const uint32_t d_tmem = tmem_base + buf * C::NTOT;
             bool ok = true;
             for (int kb = 0; kb < kiters; ++kb) {
                 if (!mbar_wait_bounded(smem_u32(&R.full[stage]), phase, abort_flag, P.status,
@@ -331,9 +352,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int kk = 0; kk < 4; ++kk) {  // 4 steps of 16 K-elements (32 bytes)
                     const uint64_t adesc = sdesc_sw128(a_s + kk * 32, 16, 1024);
 #pragma unroll
-                    for (int p = 0; p < 3; ++p) {
-                        const uint64_t bdesc = sdesc_sw128(b_s + p * EPAD * 128 + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, adesc, bdesc, C::IDESC, (kb | kk | p) ? 1u : 0u);
+                    for (int m = 0; m < C::NMMA; ++m) {
+                        const uint64_t bdesc = sdesc_sw128(b_s + m * C::NPER * 128 + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem + m * C::NPER, adesc, bdesc, C::IDESC, (kb | kk) ? 1u : 0u);
                     }
                 }
                 umma_commit(smem_u32(&R.empty[stage]));
@@ -350,13 +371,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         int local = 0;
         for (int64_t tile = blockIdx.x; tile < P.ntiles; tile += gridDim.x, ++local) {
-            const int buf = local & 1;
-            bool ok = mbar_wait_bounded(smem_u32(&R.tfull[buf]), (local >> 1) & 1, abort_flag,
-                                        P.status, P.wait_limit_ns, 43);
+            const int buf = C::NBUF == 2 ? (local & 1) : 0;
+            const uint32_t use = C::NBUF == 2 ? ((local >> 1) & 1) : (local & 1);
+            bool ok = mbar_wait_bounded(smem_u32(&R.tfull[buf]), use, abort_flag, P.status,
+                                        P.wait_limit_ns, 43);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t t_acc = tmem_base + buf * EPAD + ((uint32_t)(32 * q) << 16);
+            const uint32_t t_acc = tmem_base + buf * C::NTOT + ((uint32_t)(32 * q) << 16);
             const int64_t t = tile * 128 + 32 * q + lane;
             double z = route_epilogue<EPAD>(t_acc, t, t < P.T, P, sbias);
             tc_fence_before();
