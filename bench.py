@@ -110,6 +110,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def slowest_rank(times_ms, world: int, device: str = "cuda"):
+    """Replicas: every rank times its own steps; the job's step time is the slowest rank's.
+    All-reduces (MAX) the list of timings over the default process group when world > 1
+    and returns them as floats, identical on every rank."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in times_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Weak scaling: each of `world` replicas processes its own batch of tokens per step; the
+    job's throughput is all ranks' tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def gpu_id_for(device_index: int) -> str:
     import torch
     try:
@@ -245,14 +263,11 @@ def main():
     code, site = ops.moe_device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} ({ops.status_string(code)}) at site {site}")
-    t = torch.tensor([ms_eager, gemm_ms, ms_graph if ms_graph is not None else 0.0],
-                     dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_eager, gemm_ms = float(t[0]), float(t[1])
-    ms_total = float(t[2]) if ms_graph is not None else ms_eager
+    ms_eager, gemm_ms, ms_g = slowest_rank(
+        [ms_eager, gemm_ms, ms_graph if ms_graph is not None else 0.0], world)
+    ms_total = ms_g if ms_graph is not None else ms_eager
     ms_step = ms_total / args.steps
-    value = world * cfg.T / (ms_step / 1e3)
+    value = job_tokens_per_s(world, cfg.T, ms_step)
 
     # ------------------------------------------------------------ end to end, host buffers
     e2e = None
@@ -319,12 +334,9 @@ def main():
         run_steps(args.steps)
         b.record(stream)
         sync_all()
-        te = torch.tensor([a.elapsed_time(b)], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        ms_e2e = float(te[0]) / args.steps
+        ms_e2e = slowest_rank([a.elapsed_time(b)], world)[0] / args.steps
         nbytes = cfg.T * cfg.d * 2
-        e2e = {"value": world * cfg.T / (ms_e2e / 1e3), "unit": "tokens/s",
+        e2e = {"value": job_tokens_per_s(world, cfg.T, ms_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": nbytes * (2 if cfg.backward else 1),
                "d2h_bytes_per_step": nbytes * (2 if cfg.backward else 1),
                "ms_per_step": ms_e2e,
