@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
     const float* __restrict__ topk_gate, const float* __restrict__ topk_score,
     const float* __restrict__ logits, const float* __restrict__ lse,
     const float* __restrict__ extra, int64_t T, int E, int k, int mode, float z_scale,
-    float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dl3, int np) {
+    float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dl3, int np, int64_t pstride) {
     const int lane = threadIdx.x % 32;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (t >= T) return;
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
         S += __shfl_sync(0xffffffffu, my_s, i);
         gdg += __shfl_sync(0xffffffffu, my_g * my_dg, i);
     }
-    // with dl3, the row is also written as three bf16 pieces [3][T][np] (zero past E)
+    // with dl3, the row is also written as three bf16 pieces, piece p at dl3 + p * pstride as
+    // a [T, np] matrix (zero past E)
     const int ecount = dl3 ? np : E;
     const float ds = (my_dg - gdg) / S;
     const float vs = ds * my_s * (1.f - my_s);
@@ -315,8 +316,8 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
             split3_bf16(e < E ? out : 0.f, p0, p1, p2);
             const int64_t i = t * np + e;
             dl3[i] = p0;
-            dl3[T * np + i] = p1;
-            dl3[2 * T * np + i] = p2;
+            dl3[pstride + i] = p1;
+            dl3[2 * pstride + i] = p2;
         }
     }
 }
@@ -632,22 +633,19 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
     if (np && route_tc_splits_max(T) > nsplit) nsplit = route_tc_splits_max(T);
     float* part = wc.take<float>((size_t)nsplit * E * d);
     __nv_bfloat16* dl3 = nullptr;
-    if (np) {  // three pieces, each [T, np], each in its own 256-byte aligned region
-        dl3 = wc.take<__nv_bfloat16>((size_t)T * np);
-        __nv_bfloat16* p1 = wc.take<__nv_bfloat16>((size_t)T * np);
-        __nv_bfloat16* p2 = wc.take<__nv_bfloat16>((size_t)T * np);
-        if (p1 != dl3 + (size_t)T * np || p2 != p1 + (size_t)T * np) return MOE_ERR_WORKSPACE;
-    }
+    // three pieces, each [T, np], each starting on a 256-byte boundary (pstride elements apart)
+    const int64_t pstride = (T * np + 127) / 128 * 128;
+    if (np) dl3 = wc.take<__nv_bfloat16>((size_t)3 * pstride);
     if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     const float z_scale = 2.0f * z_coef / (float)T;
     route_bwd_dlogits_kernel<<<(unsigned)cdiv(T, 8), 256, 0, st>>>(
         dg, topk_idx, topk_gate, topk_score, logits, lse, dlogits_extra, T, E, k, mode, z_scale,
-        dlogits, dl3, np);
+        dlogits, dl3, np, pstride);
     if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
     if (np) {
-        int rc = launch_route_dwr_tc(reinterpret_cast<const __nv_bfloat16*>(x), dl3, T, d, E,
-                                     part, &nsplit, st);
+        int rc = launch_route_dwr_tc(reinterpret_cast<const __nv_bfloat16*>(x), dl3, pstride, T,
+                                     d, E, part, &nsplit, st);
         if (rc != MOE_OK) return rc;
     } else {
         dim3 grid(d / kBwTJ, (unsigned)cdiv(E, kBwTE), (unsigned)nsplit);

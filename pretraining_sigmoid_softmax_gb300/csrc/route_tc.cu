@@ -623,8 +623,8 @@ int launch_route_logits_tc(const __nv_bfloat16* x, const float* W_r, const float
     return launch_logits<128>(mx, mw, P, st);
 }
 
-int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_t T, int d,
-                        int E, float* part, int64_t* nsplit, cudaStream_t st) {
+int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_t pstride,
+                        int64_t T, int d, int E, float* part, int64_t* nsplit, cudaStream_t st) {
     const int np = route_tc_np(E);
     if (!np || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
     DwrParams P{};
@@ -645,7 +645,7 @@ int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_
     CUtensorMap mx, ml[3];
     if (!make_tmap_bf16_2d(&mx, x, d, T, 64, 64)) return MOE_ERR_LAUNCH;
     for (int p = 0; p < 3; ++p)
-        if (!make_tmap_bf16_2d(&ml[p], dl3 + (size_t)p * T * np, np, T, 64, 64)) return MOE_ERR_LAUNCH;
+        if (!make_tmap_bf16_2d(&ml[p], dl3 + (size_t)p * pstride, np, T, 64, 64)) return MOE_ERR_LAUNCH;
     if (np == 64) return launch_dwr<64>(mx, ml, P, st);
     return launch_dwr<128>(mx, ml, P, st);
 }

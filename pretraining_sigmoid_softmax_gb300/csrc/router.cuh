@@ -38,9 +38,10 @@ int launch_route_logits_tc(const __nv_bfloat16* x, const float* W_r, const float
                            int64_t* nz, __nv_bfloat16* w3, cudaStream_t st);
 
 // Tensor-core W_r-gradient partial sums (E <= 128; route_tc.cu): part[s][e][j] over the
-// tokens of split s, from the three bf16 pieces of the logit gradient (each [T, np]).
-// *nsplit is set to the number of splits written.
-int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_t T, int d,
-                        int E, float* part, int64_t* nsplit, cudaStream_t st);
+// tokens of split s, from the three bf16 pieces of the logit gradient (piece p a [T, np]
+// matrix at dl3 + p * pstride, each 16-byte aligned). *nsplit is set to the number of splits
+// written.
+int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_t pstride,
+                        int64_t T, int d, int E, float* part, int64_t* nsplit, cudaStream_t st);
 
 }  // namespace moe

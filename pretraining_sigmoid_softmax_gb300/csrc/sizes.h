@@ -48,7 +48,8 @@ inline size_t ws_route_bwd(int64_t T, int d, int E) {
     int64_t s = route_bwd_splits(T);
     if (route_tc_np(E) && route_tc_splits_max(T) > s) s = route_tc_splits_max(T);
     const size_t part = round256(sizeof(float) * s * (size_t)E * d);
-    const size_t pieces = route_tc_np(E) ? 3 * round256((size_t)2 * T * route_tc_np(E)) : 0;
+    // 3 pieces of T * np bf16, each padded to a multiple of 128 elements (256 bytes)
+    const size_t pieces = route_tc_np(E) ? round256((size_t)3 * 2 * (((size_t)T * route_tc_np(E) + 127) / 128 * 128)) : 0;
     return part + pieces;
 }
 inline size_t ws_expert(int E) { return round256(sizeof(int32_t) * (E + 1)) * 2; }
