@@ -471,7 +471,10 @@ __device__ __forceinline__ void au_issue(const SmemLayout& S, const CUtensorMap*
     const int b = (int)(n % kAuBufs);
     const uint32_t dst = smem_u32(S.au + ((size_t)slot * kAuBufs + b) * C::AU_BUF_BYTES);
     const uint32_t bar = smem_u32(&S.au_full[slot * kAuBufs + b]);
-    mbar_arrive_expect_tx(bar, C::AU_BUF_BYTES);
+    // relaxed: the buffer's previous contents were read into registers and used before the
+    // warp synchronised, and the fill orders no earlier store of this thread; a releasing
+    // arrive would wait for the warp's dA/dU stores to drain (measured: B2 1.7% slower)
+    mbar_arrive_expect_tx_relaxed(bar, C::AU_BUF_BYTES);
     tma_load_2d(dst, ma, bar, col, (int32_t)row0);
     tma_load_2d(dst + C::AU_BUF_BYTES / 2, mu, bar, col, (int32_t)row0);
 }
