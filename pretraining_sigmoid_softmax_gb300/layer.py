@@ -47,7 +47,15 @@ def _empty(shape, dtype, dev):
 class MoEPlan:
     """Device buffers of one layer shape and the forward / backward call sequences."""
 
-    def __init__(self, shape: MoEShape, device="cuda", backward: bool = True):
+    # Shared-expert GEMM work per step (FLOPs, forward + backward) below which the shared
+    # expert runs on a side stream. Measured on GB300: the softmax-free small layer (T 8192,
+    # d 1024, shared 512: 0.08 TFLOP) 0.835 -> 0.746 ms per step with the overlap; the large
+    # layer (T 65536, d 4096, shared 3072: 14.8 TFLOP) 51.3 -> 52.7 ms, as it runs at the
+    # power cap, where concurrent kernels add interference and no energy budget.
+    OVERLAP_SHARED_MAX_FLOPS = 1e12
+
+    def __init__(self, shape: MoEShape, device="cuda", backward: bool = True,
+                 overlap_shared: bool | None = None):
         s = self.s = shape
         dev = torch.device(device)
         bf, f32, i32, i64 = torch.bfloat16, torch.float32, torch.int32, torch.int64
@@ -55,6 +63,15 @@ class MoEPlan:
         R = ops.moe_padded_rows(T, k, E)
         self.R = R
         self.ws = _empty((ops.moe_workspace_bytes(T, d, E, k),), torch.uint8, dev)
+        # The shared expert depends only on x (forward) and dY (backward): for small layers it
+        # runs on a side stream, so that its GEMMs overlap the routed path's short kernels
+        # (routing, permutation, the gradient gather, the router backward). Own scratch there.
+        if overlap_shared is None:
+            overlap_shared = 18.0 * T * d * fs < self.OVERLAP_SHARED_MAX_FLOPS
+        self.overlap = bool(fs) and overlap_shared
+        self.side = torch.cuda.Stream(dev) if self.overlap else None
+        self.ws_side = (_empty((ops.moe_workspace_bytes(T, d, 1, 1),), torch.uint8, dev)
+                        if self.overlap else self.ws)
         self.logits = _empty((T, E), f32, dev)
         self.topk_idx = _empty((T, k), i32, dev)
         self.topk_gate = _empty((T, k), f32, dev)
@@ -168,6 +185,10 @@ class MoEPlan:
         self.x = x
         self.W = (W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d)
         softmax = s.mode == ops.MODE_SOFTMAX
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if s.f_shared and self.overlap:  # fork: the shared expert on the side stream
+            self.side.wait_stream(main)
+            self._shared_forward(x, Ws_g, Ws_u, Ws_d, self.side)
         ops.moe_route(x, W_r, None if softmax else b, s.k, s.mode, s.z_coef, self.logits,
                       self.topk_idx, self.topk_gate, self.topk_score,
                       self.lse if softmax else None, self.z_loss if softmax else None, self.ws,
@@ -191,25 +212,33 @@ class MoEPlan:
             self._gemm(ops.moe_expert_fwd_fp8, self.X8, self.sX, self.row_offsets, self.Wg8,
                        self.sWg, self.Wu8, self.sWu, self.Wd8, self.sWd, self.A, self.U, self.H,
                        self.H8, self.sH, self.Y_perm, self.ws, stream=stream)
-            if s.f_shared:
-                q(Ws_g, None, self.Wsg8, self.sWsg, stream)
-                q(Ws_u, None, self.Wsu8, self.sWsu, stream)
-                q(Ws_d, None, self.Wsd8, self.sWsd, stream)
-                q(x, None, self.x8, self.sx, stream)
-                self._gemm(ops.moe_expert_fwd_fp8, self.x8, self.sx, None, self.Wsg8, self.sWsg,
-                           self.Wsu8, self.sWsu, self.Wsd8, self.sWsd, self.As, self.Us, self.Hs,
-                           self.Hs8, self.sHs, self.Ys, self.ws, stream=stream)
-                ys = self.Ys
         else:
             self._gemm(ops.moe_expert_fwd, self.X_perm, self.row_offsets, W_g, W_u, W_d, self.A,
                        self.U, self.H, self.Y_perm, self.ws, stream=stream, row_gate=self.row_gate)
-            if s.f_shared:
-                self._gemm(ops.moe_expert_fwd, x, None, Ws_g[None], Ws_u[None], Ws_d[None],
-                           self.As, self.Us, self.Hs, self.Ys, self.ws, stream=stream)
-                ys = self.Ys
+        if s.f_shared:
+            if self.overlap:  # join
+                main.wait_stream(self.side)
+            else:
+                self._shared_forward(x, Ws_g, Ws_u, Ws_d, stream)
+            ys = self.Ys
         ops.moe_combine(self.Y_perm, None if self.fold_gate else self.topk_gate, self.slot_to_row,
                         ys, self.out, stream)
         return self.out
+
+    def _shared_forward(self, x, Ws_g, Ws_u, Ws_d, side):
+        """The shared expert's forward on stream `side` (every token, weight 1)."""
+        if self.s.fp8:
+            q = ops.moe_quantize_rows_fp8
+            q(Ws_g, None, self.Wsg8, self.sWsg, side)
+            q(Ws_u, None, self.Wsu8, self.sWsu, side)
+            q(Ws_d, None, self.Wsd8, self.sWsd, side)
+            q(x, None, self.x8, self.sx, side)
+            self._gemm(ops.moe_expert_fwd_fp8, self.x8, self.sx, None, self.Wsg8, self.sWsg,
+                       self.Wsu8, self.sWsu, self.Wsd8, self.sWsd, self.As, self.Us, self.Hs,
+                       self.Hs8, self.sHs, self.Ys, self.ws_side, stream=side)
+        else:
+            self._gemm(ops.moe_expert_fwd, x, None, Ws_g[None], Ws_u[None], Ws_d[None],
+                       self.As, self.Us, self.Hs, self.Ys, self.ws_side, stream=side)
 
     # ----------------------------------------------------------------- backward
     def backward(self, dY, stream=None):
@@ -217,6 +246,10 @@ class MoEPlan:
         x = self.x
         W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d = self.W
         softmax = s.mode == ops.MODE_SOFTMAX
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if s.f_shared and self.overlap:  # fork: the shared expert's backward on the side stream
+            self.side.wait_stream(main)
+            self._shared_backward(dY, x, Ws_g, Ws_u, Ws_d, self.side)
         if self.fold_gate:
             # gate folded into the experts: dY_perm holds plain copies of the token gradients,
             # the expert backward applies each row's gate and sums the gate's gradient in parts
@@ -234,11 +267,6 @@ class MoEPlan:
                        self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
                        self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
         dxs = None
-        if s.f_shared:
-            self._gemm(ops.moe_expert_bwd, dY, x, self.As, self.Us, self.Hs, None, Ws_g[None],
-                       Ws_u[None], Ws_d[None], self.dxs, self.dAs, self.dUs, self.dWs_g[None],
-                       self.dWs_u[None], self.dWs_d[None], self.ws, stream=stream)
-            dxs = self.dxs
         extra = None
         if s.has_aux:
             ops.moe_aux_loss_bwd(self.logits, self.aux_f, s.mode, s.seq_len, s.aux_switch,
@@ -248,8 +276,19 @@ class MoEPlan:
                           self.logits if softmax else None, self.lse if softmax else None, s.E,
                           s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream,
                           dlogits_extra=extra)
+        if s.f_shared:
+            if self.overlap:  # join
+                main.wait_stream(self.side)
+            else:
+                self._shared_backward(dY, x, Ws_g, Ws_u, Ws_d, stream)
+            dxs = self.dxs
         ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx, stream)
         return self.dx
+
+    def _shared_backward(self, dY, x, Ws_g, Ws_u, Ws_d, st):
+        self._gemm(ops.moe_expert_bwd, dY, x, self.As, self.Us, self.Hs, None, Ws_g[None],
+                   Ws_u[None], Ws_d[None], self.dxs, self.dAs, self.dUs, self.dWs_g[None],
+                   self.dWs_u[None], self.dWs_d[None], self.ws_side, stream=st)
 
     def bias_update(self, b, gamma, rule="sign", stream=None):
         if rule == "proportional":
