@@ -369,16 +369,35 @@ int moe_aux_loss_bwd(const float* logits, const float* aux_f, int64_t T, int E, 
                      moe_stream_t stream);
 
 /*
+ * moe_router_dx - the router's term of the input gradient, dx_r = dlogits W_r, on the tensor
+ * cores, for dense logit gradients (the softmax router, or the balancing losses), where
+ * moe_permute_bwd's own row loop would read E rows of W_r per token.
+ * Definition: dx_r[t,j] = sum_e dlogits[t,e] W_r[e,j]. Both fp32 operands are split into bf16
+ * pieces (d0 + d1 + d2, w0 + w1 + w2, each piece the rounding of what the previous ones leave)
+ * and the products d0 w0 + d0 w1 + d1 w0 are accumulated in fp32; the dropped terms are below
+ * 3 * 2^-16 of each product. Source: section 2.5 of the handbook summary (router logits in
+ * fp32; the router's gradient reaches the input through x W_r^T).
+ * In : dlogits [T,E] fp32 (from moe_route_bwd); W_r [E,d] fp32. E <= 128, d % 128 == 0.
+ * Out: dx_r [T,d] fp32 (16-byte aligned). Scratch: ws (moe_workspace_bytes).
+ */
+int moe_router_dx(const float* dlogits, const float* W_r, int64_t T, int d, int E, float* dx_r,
+                  void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_permute_bwd - input gradient of the layer (B6).
- * Definition: dx[t] = sum_{i<k} dX_perm[slot_to_row[t,i]] + dx_shared[t]
- *                     + sum_e dlogits[t,e] * W_r[e]  (fp32 in that order, one bf16 rounding).
+ * Definition: dx[t] = sum_{i<k} dX_perm[slot_to_row[t,i]] + dx_shared[t] + r[t]
+ *                     (fp32 in that order, one bf16 rounding), with the router's term
+ *                     r[t] = sum_e dlogits[t,e] * W_r[e] (formed here, from the nonzero logit
+ *                     gradients of the token) or r = dx_router (formed by moe_router_dx).
  * In : dX_perm [padded rows, d] bf16; slot_to_row [T,k]; dx_shared [T,d] bf16 or NULL;
- *      dlogits [T,E] fp32 and W_r [E,d] fp32, or both NULL.
+ *      dlogits [T,E] fp32 and W_r [E,d] fp32, or both NULL; dx_router [T,d] fp32 or NULL
+ *      (not together with dlogits).
  * Out: dx [T,d] bf16.
  */
 int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_row,
                     const moe_bf16* dx_shared, const float* dlogits, const float* W_r,
-                    int64_t T, int d, int E, int k, moe_bf16* dx, moe_stream_t stream);
+                    const float* dx_router, int64_t T, int d, int E, int k, moe_bf16* dx,
+                    moe_stream_t stream);
 
 #ifdef __cplusplus
 }

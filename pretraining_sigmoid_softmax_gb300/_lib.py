@@ -45,7 +45,8 @@ PROTOTYPES = {
                            _SZ, _P]),
     "moe_aux_loss": (_I, [_P, _P, _I64, _I, _I, _I, _I64, _F, _F, _P, _P, _P, _SZ, _P]),
     "moe_aux_loss_bwd": (_I, [_P, _P, _I64, _I, _I, _I64, _F, _F, _P, _P]),
-    "moe_permute_bwd": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P]),
+    "moe_permute_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P]),
+    "moe_router_dx": (_I, [_P, _P, _I64, _I, _I, _P, _P, _SZ, _P]),
 }
 
 _lib = None

@@ -916,6 +916,19 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_
     return make_map(m, base, inner, outer, box_inner, box_outer);
 }
 
+bool make_tmap_f32_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer) {
+    auto enc = get_encoder();
+    if (!enc || !base) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace moe
 
 using namespace moe;

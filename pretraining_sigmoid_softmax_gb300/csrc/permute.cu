@@ -363,8 +363,8 @@ template <int KMAX>
 __global__ void __launch_bounds__(256) permute_bwd_kernel(
     const __nv_bfloat16* __restrict__ dX_perm, const int32_t* __restrict__ slot_to_row,
     const __nv_bfloat16* __restrict__ dx_sh, const float* __restrict__ dlogits,
-    const float* __restrict__ W_r, int64_t T, int d, int E, int k,
-    __nv_bfloat16* __restrict__ dx) {
+    const float* __restrict__ W_r, const float* __restrict__ dx_r, int64_t T, int d, int E,
+    int k, __nv_bfloat16* __restrict__ dx) {
     __shared__ int s_e[kWarpsPerCta][kMaxExperts];
     __shared__ float s_g[kWarpsPerCta][kMaxExperts];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -399,6 +399,18 @@ __global__ void __launch_bounds__(256) permute_bwd_kernel(
                 add_bf16x8(acc, reinterpret_cast<const uint4*>(dX_perm + (int64_t)rows[i] * d)[c]);
         }
         if (dx_sh) add_bf16x8(acc, reinterpret_cast<const uint4*>(dx_sh + t * d)[c]);
+        if (dx_r) {  // the router's term, formed beforehand (moe_router_dx)
+            const float4* r = reinterpret_cast<const float4*>(dx_r + t * d + c * 8);
+            const float4 a = r[0], b = r[1];
+            acc[0] += a.x;
+            acc[1] += a.y;
+            acc[2] += a.z;
+            acc[3] += a.w;
+            acc[4] += b.x;
+            acc[5] += b.y;
+            acc[6] += b.z;
+            acc[7] += b.w;
+        }
         for (int j = 0; j < n; ++j) {
             const float g = s_g[warp][j];
             const float4* w = reinterpret_cast<const float4*>(W_r + (int64_t)s_e[warp][j] * d + c * 8);
@@ -571,10 +583,12 @@ extern "C" int moe_gate_grad(const float* gate_part, const int32_t* slot_to_row,
 
 extern "C" int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_row,
                                const moe_bf16* dx_shared, const float* dlogits,
-                               const float* W_r, int64_t T, int d, int E, int k, moe_bf16* dx,
-                               moe_stream_t stream) {
+                               const float* W_r, const float* dx_router, int64_t T, int d, int E,
+                               int k, moe_bf16* dx, moe_stream_t stream) {
     if (!dX_perm || !slot_to_row || !dx) return MOE_ERR_INVALID_ARG;
     if ((dlogits == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (dx_router && dlogits) return MOE_ERR_INVALID_ARG;  // the router term once
+    if (dx_router && !aligned16(dx_router)) return MOE_ERR_INVALID_ARG;
     if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(dX_perm) || !aligned16(dx) || (dx_shared && !aligned16(dx_shared)) ||
@@ -586,11 +600,11 @@ extern "C" int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_r
     const __nv_bfloat16* sh = reinterpret_cast<const __nv_bfloat16*>(dx_shared);
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(dx);
     const unsigned grid = warp_grid(T);
-    if (k <= 2) permute_bwd_kernel<2><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
-    else if (k <= 4) permute_bwd_kernel<4><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
-    else if (k <= 8) permute_bwd_kernel<8><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
-    else if (k <= 16) permute_bwd_kernel<16><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
-    else permute_bwd_kernel<32><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, T, d, E, k, o);
+    if (k <= 2) permute_bwd_kernel<2><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else if (k <= 4) permute_bwd_kernel<4><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else if (k <= 8) permute_bwd_kernel<8><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else if (k <= 16) permute_bwd_kernel<16><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else permute_bwd_kernel<32><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
     return launch_status();
 }
 

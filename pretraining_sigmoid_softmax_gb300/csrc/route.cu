@@ -244,13 +244,21 @@ __global__ void __launch_bounds__(kThreads) route_fwd_kernel(
     }
 }
 
-__global__ void z_finalize_kernel(const double* __restrict__ z_part, int64_t nblocks, int64_t T,
-                                  float z_coef, float* __restrict__ z_loss) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) {
-        double s = 0.0;
-        for (int64_t i = 0; i < nblocks; ++i) s += z_part[i];
-        z_loss[0] = (float)((double)z_coef * s / (double)T);
+// One CTA of 256 threads: thread i sums partials i, i + 256, ... in order, then a fixed
+// tree over the threads (the same association on every run).
+__global__ void __launch_bounds__(256) z_finalize_kernel(const double* __restrict__ z_part,
+                                                         int64_t nblocks, int64_t T, float z_coef,
+                                                         float* __restrict__ z_loss) {
+    __shared__ double red[256];
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < nblocks; i += 256) s += z_part[i];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
     }
+    if (threadIdx.x == 0) z_loss[0] = (float)((double)z_coef * red[0] / (double)T);
 }
 
 // ---------------------------------------------------------------------------- backward
@@ -607,7 +615,7 @@ extern "C" int moe_route(const moe_bf16* x, const float* W_r, const float* b, in
     }
     if (rc != MOE_OK) return rc;
     if (mode == MOE_MODE_SOFTMAX) {
-        z_finalize_kernel<<<1, 32, 0, st>>>(zp, nb, T, z_coef, z_loss);
+        z_finalize_kernel<<<1, 256, 0, st>>>(zp, nb, T, z_coef, z_loss);
         rc = launch_status();
     }
     return rc;
@@ -656,6 +664,22 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
     const int64_t n = (int64_t)E * d;
     route_bwd_reduce_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(part, nsplit, n, dW_r);
     return launch_status();
+}
+
+extern "C" int moe_router_dx(const float* dlogits, const float* W_r, int64_t T, int d, int E,
+                             float* dx_r, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!dlogits || !W_r || !dx_r) return MOE_ERR_INVALID_ARG;
+    if (T <= 0 || d <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    const int np = route_tc_np(E);
+    if (!np || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(dx_r) || !aligned16(W_r)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    WsCarver wc(ws, ws_bytes);
+    const int64_t pstride = (T * np + 127) / 128 * 128;
+    __nv_bfloat16* dl2 = wc.take<__nv_bfloat16>((size_t)2 * pstride);
+    __nv_bfloat16* w3 = wc.take<__nv_bfloat16>((size_t)3 * np * d);
+    if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
+    return launch_router_dx_tc(dlogits, W_r, T, d, E, dl2, pstride, w3, dx_r, (cudaStream_t)stream);
 }
 
 extern "C" int moe_aux_loss(const float* logits, const int32_t* topk_idx, int64_t T, int E, int k,

@@ -64,6 +64,23 @@ __global__ void split3_rows_kernel(const float* __restrict__ src, int rows, int 
     }
 }
 
+// dst[p][t][e] for p = 0, 1, t < T, e < np: the first two bf16 pieces of src[t][e] (zero for
+// e >= E); piece p starts at dst + p * pstride.
+__global__ void split2_cols_kernel(const float* __restrict__ src, int64_t T, int E, int np,
+                                   int64_t pstride, __nv_bfloat16* __restrict__ dst) {
+    const int64_t n = T * np;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / np;
+        const int e = (int)(i % np);
+        const float v = e < E ? src[t * E + e] : 0.f;
+        __nv_bfloat16 p0, p1, p2;
+        split3_bf16(v, p0, p1, p2);
+        dst[i] = p0;
+        dst[pstride + i] = p1;
+    }
+}
+
 struct TcRing {
     uint8_t* a;
     uint8_t* b;
@@ -585,6 +602,181 @@ int launch_dwr(const CUtensorMap& mx, const CUtensorMap* ml, const DwrParams& P,
     return launch_status();
 }
 
+// ------------------------------------------------------------ router input gradient
+// dx_r[t][j] = sum_e dlogits[t][e] W_r[e][j] on the tensor cores, for dense logit gradients
+// (softmax router, balancing losses), where the input-gradient kernel's row loop over W_r
+// would read E rows of d fp32 from L2 per token. With the three-piece split d = d0 + d1 + d2
+// and w = w0 + w1 + w2, the product keeps d0 w0 + d0 w1 + d1 w0: the dropped terms are
+// below 3 * 2^-16 of each product, far under the bf16 rounding of the dx they feed. The
+// three kept terms are three K segments (np experts each) of one GEMM: M = 128 tokens,
+// N = BN columns of d, K = 3 np; A (the logit-gradient pieces, [T, np]) K-major, B (the W_r
+// pieces, [np, d]) MN-major. The fp32 result is staged per warp in 32 x 32 boxes (128-byte
+// swizzle) and written by TMA stores, which clip rows past T.
+
+struct RdxParams {
+    int64_t T;
+    int d, np;
+    int64_t ntiles;  // ceil(T / 128) * (d / BN)
+    int* status;
+    uint64_t wait_limit_ns;
+};
+
+template <int BN>
+struct RdxCfg {
+    static constexpr int A_BYTES = 128 * 128;          // 128 tokens x 64 experts, K-major
+    static constexpr int B_BYTES = (BN / 64) * 8192;   // 64 experts x BN columns, MN-major
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = 3;
+    static constexpr int TMEM_COLS = 2 * BN;           // two accumulators
+    static constexpr uint32_t IDESC = idesc_mma(BN, 128, false, true);
+    static constexpr int OUT_BUF = 32 * 128;           // 32 rows x 32 fp32
+    static constexpr size_t SMEM_BYTES =
+        1024 + (size_t)STAGES * STAGE_BYTES + kTcMisc + 1024 + 4 * 2 * OUT_BUF;
+    static_assert(BN == 128 || BN == 256, "column tile");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    router_dx_tc_kernel(const __grid_constant__ CUtensorMap ml0, const __grid_constant__ CUtensorMap ml1,
+                        const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mo,
+                        const RdxParams P) {
+    using C = RdxCfg<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const TcRing R = carve_ring<C::STAGES, C::A_BYTES, C::B_BYTES>(smem_raw);
+    uint8_t* ob = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(R.extra) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const uint32_t tmem_base = ring_setup<C::STAGES, C::TMEM_COLS>(R, tid, warp);
+    volatile int* abort_flag = R.abort_flag;
+    const int ntn = P.d / BN;
+    const int kb_seg = P.np / 64;    // k-blocks per segment
+    const int nkb = 3 * kb_seg;      // segments: (d0, w0), (d0, w1), (d1, w0)
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer
+        tma_prefetch_desc(&ml0);
+        tma_prefetch_desc(&ml1);
+        tma_prefetch_desc(&mw);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int64_t tile = blockIdx.x; tile < P.ntiles; tile += gridDim.x) {
+            const int32_t t0 = (int32_t)((tile / ntn) * 128), n0 = (int32_t)(tile % ntn) * BN;
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait_bounded(smem_u32(&R.empty[stage]), phase ^ 1u, abort_flag, P.status,
+                                       P.wait_limit_ns, 48)) {
+                    ok = false;
+                    break;
+                }
+                const int seg = kb / kb_seg, e0 = (kb % kb_seg) * 64;
+                const CUtensorMap* ma = seg == 2 ? &ml1 : &ml0;  // d1 in the third segment
+                const int32_t wrow = (seg == 1 ? P.np : 0) + e0;  // w1 in the second
+                const uint32_t bar = smem_u32(&R.full[stage]);
+                mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+                tma_load_2d(smem_u32(R.a + (size_t)stage * C::A_BYTES), ma, bar, e0, t0);
+                const uint32_t b_dst = smem_u32(R.b + (size_t)stage * C::B_BYTES);
+#pragma unroll
+                for (int g = 0; g < BN / 64; ++g) tma_load_2d(b_dst + g * 8192, &mw, bar, n0 + 64 * g, wrow);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        for (int64_t tile = blockIdx.x; tile < P.ntiles; tile += gridDim.x, ++local) {
+            const int buf = local & 1;
+            if (!mbar_wait_bounded(smem_u32(&R.tempty[buf]), ((local >> 1) & 1) ^ 1u, abort_flag,
+                                   P.status, P.wait_limit_ns, 49))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + buf * BN;
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait_bounded(smem_u32(&R.full[stage]), phase, abort_flag, P.status,
+                                       P.wait_limit_ns, 50)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_s = smem_u32(R.a + (size_t)stage * C::A_BYTES);
+                const uint32_t b_s = smem_u32(R.b + (size_t)stage * C::B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {  // 16 experts per step
+                    const uint64_t adesc = sdesc_sw128(a_s + kk * 32, 16, 1024);
+                    const uint64_t bdesc = sdesc_sw128(b_s + kk * 2048, 8192, 1024);
+                    umma_bf16(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&R.empty[stage]));
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(smem_u32(&R.tfull[buf]));
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp - 4;
+        int local = 0;
+        uint32_t n = 0;  // chunks staged by this warp (output buffer parity)
+        for (int64_t tile = blockIdx.x; tile < P.ntiles; tile += gridDim.x, ++local) {
+            const int buf = local & 1;
+            bool ok = mbar_wait_bounded(smem_u32(&R.tfull[buf]), (local >> 1) & 1, abort_flag,
+                                        P.status, P.wait_limit_ns, 51);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t_acc = tmem_base + buf * BN + ((uint32_t)(32 * q) << 16);
+            const int32_t row0 = (int32_t)((tile / ntn) * 128) + 32 * q;
+            const int32_t n0 = (int32_t)(tile % ntn) * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c, ++n) {
+                uint32_t v[32];
+                tmem_ld32(t_acc + 32 * c, v);
+                tmem_ld_wait();
+                uint8_t* ob_w = ob + ((size_t)q * 2 + (n & 1)) * C::OUT_BUF;
+                if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)  // 128-byte swizzle: piece j of row r at j ^ (r & 7)
+                    *reinterpret_cast<uint4*>(ob_w + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&mo, smem_u32(ob_w), n0 + 32 * c, row0);
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&R.tempty[buf]));
+        }
+        if (lane == 0) bulk_wait<0>();
+    }
+    ring_teardown<C::TMEM_COLS>(R, tmem_base, warp);
+}
+
+template <int BN>
+int launch_rdx(const CUtensorMap* ml, const CUtensorMap& mw, const CUtensorMap& mo,
+               const RdxParams& P, cudaStream_t st) {
+    using C = RdxCfg<BN>;
+    static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
+    auto kern = router_dx_tc_kernel<BN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES) !=
+        cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    const int64_t grid = P.ntiles < sm_count() ? P.ntiles : sm_count();
+    kern<<<(unsigned)grid, kTcThreads, C::SMEM_BYTES, st>>>(ml[0], ml[1], mw, mo, P);
+    return launch_status();
+}
+
 }  // namespace
 
 int launch_route_logits_tc(const __nv_bfloat16* x, const float* W_r, const float* b, int64_t T,
@@ -648,6 +840,40 @@ int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_
         if (!make_tmap_bf16_2d(&ml[p], dl3 + (size_t)p * pstride, np, T, 64, 64)) return MOE_ERR_LAUNCH;
     if (np == 64) return launch_dwr<64>(mx, ml, P, st);
     return launch_dwr<128>(mx, ml, P, st);
+}
+
+int launch_router_dx_tc(const float* dlogits, const float* W_r, int64_t T, int d, int E,
+                        __nv_bfloat16* dl2, int64_t pstride, __nv_bfloat16* w3, float* dx_r,
+                        cudaStream_t st) {
+    const int np = route_tc_np(E);
+    if (!np || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    {
+        const int64_t m = T * np;
+        const int blocks = (int)((m + 255) / 256 < 4096 ? (m + 255) / 256 : 4096);
+        split2_cols_kernel<<<blocks, 256, 0, st>>>(dlogits, T, E, np, pstride, dl2);
+        if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
+    }
+    const __nv_bfloat16* dl3 = dl2;
+    const int64_t n = (int64_t)np * d;
+    const int sblocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    split3_rows_kernel<<<sblocks, 256, 0, st>>>(W_r, E, d, np, w3);  // [3][np][d], zero past E
+    if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
+    const int BN = d % 256 == 0 ? 256 : 128;
+    CUtensorMap ml[2], mw, mo;
+    for (int p = 0; p < 2; ++p)
+        if (!make_tmap_bf16_2d(&ml[p], dl3 + (size_t)p * pstride, np, T, 64, 128)) return MOE_ERR_LAUNCH;
+    if (!make_tmap_bf16_2d(&mw, w3, d, 3 * (uint64_t)np, 64, 64) ||
+        !make_tmap_f32_2d(&mo, dx_r, d, T, 32, 32))
+        return MOE_ERR_LAUNCH;
+    RdxParams P{};
+    P.T = T;
+    P.d = d;
+    P.np = np;
+    P.ntiles = route_tc_tiles(T) * (d / BN);
+    P.status = device_status_word();
+    P.wait_limit_ns = wait_limit_ns();
+    if (BN == 256) return launch_rdx<256>(ml, mw, mo, P, st);
+    return launch_rdx<128>(ml, mw, mo, P, st);
 }
 
 }  // namespace moe

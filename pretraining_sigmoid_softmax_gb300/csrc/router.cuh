@@ -44,4 +44,11 @@ int launch_route_logits_tc(const __nv_bfloat16* x, const float* W_r, const float
 int launch_route_dwr_tc(const __nv_bfloat16* x, const __nv_bfloat16* dl3, int64_t pstride,
                         int64_t T, int d, int E, float* part, int64_t* nsplit, cudaStream_t st);
 
+// Router input-gradient term dx_r = dlogits W_r on the tensor cores (E <= 128; route_tc.cu).
+// Scratch: dl2, the first two bf16 pieces of dlogits ([T, np] each, pstride elements apart,
+// 16-byte aligned), and w3, the three pieces of W_r ([3][np][d]). dx_r [T, d] fp32.
+int launch_router_dx_tc(const float* dlogits, const float* W_r, int64_t T, int d, int E,
+                        __nv_bfloat16* dl2, int64_t pstride, __nv_bfloat16* w3, float* dx_r,
+                        cudaStream_t st);
+
 }  // namespace moe

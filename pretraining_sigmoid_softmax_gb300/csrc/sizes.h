@@ -59,6 +59,14 @@ inline size_t ws_aux(int64_t T, int E) {
     return 2 * round256(sizeof(float) * (size_t)T * E);
 }
 
+// Router input gradient (tensor cores): two bf16 pieces of the logit gradient and three of W_r.
+inline size_t ws_router_dx(int64_t T, int d, int E) {
+    const int np = route_tc_np(E);
+    if (!np) return 0;
+    const size_t pstride = ((size_t)T * np + 127) / 128 * 128;
+    return round256(2 * 2 * pstride) + round256((size_t)3 * np * d * 2);
+}
+
 inline size_t ws_total(int64_t T, int d, int E, int k) {
     (void)k;
     size_t m = ws_route(T, d, E);
@@ -66,6 +74,7 @@ inline size_t ws_total(int64_t T, int d, int E, int k) {
     if (ws_route_bwd(T, d, E) > m) m = ws_route_bwd(T, d, E);
     if (ws_expert(E) > m) m = ws_expert(E);
     if (ws_aux(T, E) > m) m = ws_aux(T, E);
+    if (ws_router_dx(T, d, E) > m) m = ws_router_dx(T, d, E);
     return m + 256;
 }
 

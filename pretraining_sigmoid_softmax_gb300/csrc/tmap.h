@@ -13,4 +13,8 @@ namespace moe {
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                        uint32_t box_inner, uint32_t box_outer);
 
+// The same over a row-major [outer, inner] fp32 matrix (box_inner * 4 <= 128).
+bool make_tmap_f32_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer);
+
 }  // namespace moe

@@ -129,6 +129,10 @@ class MoEPlan:
             self.dW_u = _empty((E, f, d), bf, dev)
             self.dW_d = _empty((E, d, f), bf, dev)
             self.dlogits = _empty((T, E), f32, dev)
+            # dense logit gradients (softmax router, balancing losses): the router's input-
+            # gradient term runs on the tensor cores instead of in the dx kernel's row loop
+            self.router_dx_tc = (s.mode == ops.MODE_SOFTMAX or s.has_aux) and E <= 128
+            self.dx_r = _empty((T, d), f32, dev) if self.router_dx_tc else None
             self.dW_r = _empty((E, d), f32, dev)
             self.dx = _empty((T, d), bf, dev)
             if fs:
@@ -174,6 +178,8 @@ class MoEPlan:
             n += 1 if not s.fp8 else 0                      # gate gradient from its partials
             n += 5 + (4 if s.f_shared else 0)               # expert backward (+ expert order)
             n += 3                                          # router backward
+            if (s.mode == ops.MODE_SOFTMAX or s.has_aux) and s.E <= 128:
+                n += 3                                      # router dx: two splits + GEMM
             n += 1                                          # input gradient
         if bias_update:
             n += 1
@@ -282,7 +288,13 @@ class MoEPlan:
             else:
                 self._shared_backward(dY, x, Ws_g, Ws_u, Ws_d, stream)
             dxs = self.dxs
-        ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx, stream)
+        if self.router_dx_tc:
+            ops.moe_router_dx(self.dlogits, W_r, self.dx_r, self.ws, stream)
+            ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, None, None, self.dx, stream,
+                                dx_router=self.dx_r)
+        else:
+            ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx,
+                                stream)
         return self.dx
 
     def _shared_backward(self, dY, x, Ws_g, Ws_u, Ws_d, st):

@@ -230,11 +230,23 @@ def moe_aux_loss_bwd(logits, aux_f, mode, seq_len, switch_coef, seq_coef, dlogit
                                         _stream(stream)), "moe_aux_loss_bwd")
 
 
-def moe_permute_bwd(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx, stream=None):
+def moe_permute_bwd(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx, stream=None,
+                    dx_router=None):
+    """dx_router [T, d] fp32 (from moe_router_dx) in place of (dlogits, W_r)."""
     T, k = slot_to_row.shape
     d = dx.shape[1]
     E = 0 if W_r is None else W_r.shape[0]
-    _contig(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx)
+    _contig(dX_perm, slot_to_row, dx_shared, dlogits, W_r, dx, dx_router)
     _check(_lib.load().moe_permute_bwd(_p(dX_perm), _p(slot_to_row), _p(dx_shared), _p(dlogits),
-                                       _p(W_r), T, d, max(E, 1), k, _p(dx), _stream(stream)),
+                                       _p(W_r), _p(dx_router), T, d, max(E, 1), k, _p(dx),
+                                       _stream(stream)),
            "moe_permute_bwd")
+
+
+def moe_router_dx(dlogits, W_r, dx_r, ws, stream=None):
+    """The router's input-gradient term dlogits W_r on the tensor cores (fp32 [T, d])."""
+    T, E = dlogits.shape
+    d = W_r.shape[1]
+    _contig(dlogits, W_r, dx_r, ws)
+    _check(_lib.load().moe_router_dx(_p(dlogits), _p(W_r), T, d, E, _p(dx_r), _p(ws), ws.numel(),
+                                     _stream(stream)), "moe_router_dx")

@@ -406,6 +406,34 @@ def test_combine_and_backward_kernels():
     ref = O.input_gradient(h64(dX_perm)[rows], D["slot_to_row"], h64(dxs), h64(dl) @ h64(W_r),
                            O.bf16_round)
     assert_close(dx, ref, "dx")
+    # the same with the router's term formed on the tensor cores first
+    dx_r = torch.empty(T, d, device="cuda")
+    ops.moe_router_dx(dev(dl), dev(W_r), dx_r, _ws(T, d, E, k))
+    dx2 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    ops.moe_permute_bwd(dev(dX_perm), P["slot_to_row"], dev(dxs), None, None, dx2, dx_router=dx_r)
+    assert_close(dx2, ref, "dx (router term from moe_router_dx)")
+
+
+# E = 8 and 100 (expert axis padded to 64 and 128), d = 256 and 384 (256- and 128-column
+# tiles), a ragged token count
+@pytest.mark.parametrize("T,d,E", [(1000, 256, 8), (777, 384, 100), (64, 128, 64)])
+def test_router_dx_is_the_fp32_product(T, d, E):
+    g = torch.Generator().manual_seed(T + d + E)
+    dl = torch.randn(T, E, generator=g) * 0.1
+    W_r = torch.randn(E, d, generator=g) * d ** -0.5
+    dx_r = torch.full((T, d), float("nan"), device="cuda")
+    ops.moe_router_dx(dev(dl), dev(W_r), dx_r, _ws(T, d, E, 2))
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    dl64, W64 = h64(dl), h64(W_r)
+    ref = dl64 @ W64
+    # kept pieces d0 w0 + d0 w1 + d1 w0: dropped terms below 3 * 2^-16 of each product, plus
+    # the fp32 accumulation of 3E products (Higham gamma_3E) and the pieces' own residue
+    scale = np.abs(dl64) @ np.abs(W64)
+    bound = (3 * 2.0 ** -16 + (3 * E + 8) * 2.0 ** -24) * scale
+    got = h64(dx_r)
+    assert np.isfinite(got).all()
+    assert (np.abs(got - ref) <= bound).all(), f"max excess {np.max(np.abs(got - ref) - bound):.3e}"
 
 
 # E <= 128 runs the tensor-core W_r-gradient kernel (64- and 128-wide expert tiles, ragged
