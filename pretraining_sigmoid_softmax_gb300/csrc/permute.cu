@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kMaxExperts) scan_kernel(
     }
 }
 
+// The padding kernels run kPadSplit CTAs per expert (grid E x kPadSplit), each taking a
+// strided share of the expert's padding rows.
+constexpr int kPadSplit = 16;
+
 // Padding rows of each expert segment: perm_token = -1 and (optionally) a zero row.
 __global__ void __launch_bounds__(256) pad_rows_kernel(const int64_t* __restrict__ row_offsets,
                                                        const int32_t* __restrict__ counts,
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(256) pad_rows_kernel(const int64_t* __restrict
     const int e = blockIdx.x;
     const int64_t lo = row_offsets[e] + counts[e], hi = row_offsets[e + 1];
     const int vec_per_row = d / 8;
-    for (int64_t i = threadIdx.x; i < (hi - lo) * vec_per_row; i += blockDim.x) {
+    for (int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
+         i += (int64_t)gridDim.y * blockDim.x) {
         const int64_t r = lo + i / vec_per_row;
         const int c = (int)(i % vec_per_row);
         reinterpret_cast<uint4*>(buf + r * d)[c] = make_uint4(0, 0, 0, 0);
@@ -125,7 +130,8 @@ __global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int64_t* __res
     int64_t lo = row_offsets[e];
     if (hi - lo > MOE_ROW_ALIGN - 1) lo = hi - (MOE_ROW_ALIGN - 1);
     const int vec_per_row = d / 8;
-    for (int64_t i = threadIdx.x; i < (hi - lo) * vec_per_row; i += blockDim.x) {
+    for (int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
+         i += (int64_t)gridDim.y * blockDim.x) {
         const int64_t r = lo + i / vec_per_row;
         if (perm_token[r] < 0)
             reinterpret_cast<uint4*>(buf + r * d)[i % vec_per_row] = make_uint4(0, 0, 0, 0);
@@ -359,7 +365,7 @@ __global__ void gate_grad_kernel(const float* __restrict__ part, int nparts,
 // One warp per token. The token's nonzero router terms (k in sigmoid mode, E in softmax
 // mode) are listed once, in expert order, in the warp's shared-memory slice; the row loop
 // then touches only those rows of W_r.
-template <int KMAX>
+template <int KMAX, bool DXR>
 __global__ void __launch_bounds__(256) permute_bwd_kernel(
     const __nv_bfloat16* __restrict__ dX_perm, const int32_t* __restrict__ slot_to_row,
     const __nv_bfloat16* __restrict__ dx_sh, const float* __restrict__ dlogits,
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(256) permute_bwd_kernel(
                 add_bf16x8(acc, reinterpret_cast<const uint4*>(dX_perm + (int64_t)rows[i] * d)[c]);
         }
         if (dx_sh) add_bf16x8(acc, reinterpret_cast<const uint4*>(dx_sh + t * d)[c]);
-        if (dx_r) {  // the router's term, formed beforehand (moe_router_dx)
+        if constexpr (DXR) {  // the router's term, formed beforehand (moe_router_dx)
             const float4* r = reinterpret_cast<const float4*>(dx_r + t * d + c * 8);
             const float4 a = r[0], b = r[1];
             acc[0] += a.x;
@@ -453,6 +459,18 @@ __global__ void bias_update_proportional_kernel(const int32_t* __restrict__ coun
 
 inline unsigned warp_grid(int64_t T) { return (unsigned)cdiv(T, kWarpsPerCta); }
 
+template <bool DXR>
+void launch_permute_bwd(unsigned grid, cudaStream_t st, const __nv_bfloat16* a,
+                        const int32_t* slot_to_row, const __nv_bfloat16* sh, const float* dlogits,
+                        const float* W_r, const float* dx_router, int64_t T, int d, int E, int k,
+                        __nv_bfloat16* o) {
+    if (k <= 2) permute_bwd_kernel<2, DXR><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else if (k <= 4) permute_bwd_kernel<4, DXR><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else if (k <= 8) permute_bwd_kernel<8, DXR><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else if (k <= 16) permute_bwd_kernel<16, DXR><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else permute_bwd_kernel<32, DXR><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+}
+
 bool shape_ok(int64_t T, int d, int E, int k) {
     return T > 0 && d > 0 && E > 0 && k > 0;
 }
@@ -483,7 +501,7 @@ extern "C" int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T
     cudaStream_t st = (cudaStream_t)stream;
     hist_kernel<<<(unsigned)nb, kHistThreads, 0, st>>>(topk_idx, T, E, k, bcounts, status);
     scan_kernel<<<1, kMaxExperts, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
-    pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, counts, d, perm_token,
+    pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, counts, d, perm_token,
                                        reinterpret_cast<__nv_bfloat16*>(X_perm));
     const size_t sc_smem = sizeof(int32_t) * 64 * E;
     if (cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -554,7 +572,7 @@ extern "C" int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm,
     else if (k <= 8) combine_bwd_kernel<8><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
     else if (k <= 16) combine_bwd_kernel<16><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
     else combine_bwd_kernel<32><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
-    zero_pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    zero_pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, perm_token, d, dYp);
     return launch_status();
 }
 
@@ -600,11 +618,10 @@ extern "C" int moe_permute_bwd(const moe_bf16* dX_perm, const int32_t* slot_to_r
     const __nv_bfloat16* sh = reinterpret_cast<const __nv_bfloat16*>(dx_shared);
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(dx);
     const unsigned grid = warp_grid(T);
-    if (k <= 2) permute_bwd_kernel<2><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
-    else if (k <= 4) permute_bwd_kernel<4><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
-    else if (k <= 8) permute_bwd_kernel<8><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
-    else if (k <= 16) permute_bwd_kernel<16><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
-    else permute_bwd_kernel<32><<<grid, 256, 0, st>>>(a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    if (dx_router)
+        launch_permute_bwd<true>(grid, st, a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
+    else
+        launch_permute_bwd<false>(grid, st, a, slot_to_row, sh, dlogits, W_r, dx_router, T, d, E, k, o);
     return launch_status();
 }
 
@@ -665,7 +682,7 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, i
     cudaStream_t st = (cudaStream_t)stream;
     hist_kernel<<<(unsigned)nb, kHistThreads, 0, st>>>(topk_idx, T, E, k, bcounts, status);
     scan_kernel<<<1, kMaxExperts, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
-    pad_rows_kernel<<<E, 256, 0, st>>>(row_offsets, counts, d, perm_token,
+    pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, counts, d, perm_token,
                                        reinterpret_cast<__nv_bfloat16*>(X_perm));
     const size_t sc_smem = sizeof(int32_t) * 64 * E;
     if (cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
