@@ -137,6 +137,16 @@ def gpu_id_for(device_index: int) -> str:
         return vis.split(",")[device_index] if vis else str(device_index)
 
 
+def oracle_pass_desc(cfg) -> str:
+    """What one oracle step computes for this workload (as bench.py times it)."""
+    parts = ["forward"]
+    if cfg.backward:
+        parts.append("backward")
+    if cfg.bias_update:
+        parts.append("bias update")
+    return "fp64 " + "+".join(parts)
+
+
 def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
     """The fp64 oracle (forward + backward + bias update) on the first T_s tokens of the
     workload, all experts; returns (tokens/s, threads, seconds per step)."""
@@ -176,7 +186,7 @@ def run_reference(args, cfg):
             "data": "synthetic", "config": workload_desc(cfg),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"first {T_s} tokens of the workload per step, all "
-                                       f"{cfg.E} experts, fp64 forward+backward+bias update"},
+                                       f"{cfg.E} experts, {oracle_pass_desc(cfg)}"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -384,7 +394,7 @@ def main():
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores,
                                 "kind": "oracle",
                                 "sample": f"first {T_s} tokens of the workload, all {cfg.E} "
-                                          f"experts, fp64 forward+backward+bias update"}
+                                          f"experts, {oracle_pass_desc(cfg)}"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
