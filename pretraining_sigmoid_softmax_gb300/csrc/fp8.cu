@@ -1,7 +1,12 @@
 // Rowwise FP8 (E4M3) quantisation of GEMM operands ("The whole stack, in the open" (Apex-3):
 // the benchmark and training run with --precision fp8_rowwise): per row, scale = amax / 448
-// and code = E4M3(x / scale), round to nearest even, saturating. Both divisions are IEEE
-// fp32 divisions so the codes are reproducible bit for bit.
+// and code = E4M3(x / scale), round to nearest even, saturating. Both quotients are the
+// correctly rounded fp32 quotients (IEEE division), so the codes are reproducible bit for
+// bit. Per element the quotient is formed without a division: with rs = RN(1 / scale) (the
+// correctly rounded reciprocal), q0 = RN(x rs), e = x - scale q0 (exact in one FMA) and
+// q = RN(q0 + e rs) is RN(x / scale) - Markstein's theorem for FMA division with a correctly
+// rounded reciprocal, valid while nothing under- or overflows; |x / scale| <= 448 here, and
+// quotients small enough to underflow quantise to zero whichever way they round.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -33,6 +38,12 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_fp8_kernel(
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         const float s = m > 0.f ? __fdiv_rn(m, 448.f) : 1.f;
+        const float rs = __frcp_rn(s);
+        auto quot = [s, rs](float x) {  // RN(x / s)
+            const float q0 = __fmul_rn(x, rs);
+            const float e = __fmaf_rn(-q0, s, x);
+            return __fmaf_rn(e, rs, q0);
+        };
         uint2* dst = reinterpret_cast<uint2*>(Q + r * cols);
         for (int c = lane; c < nvec; c += 32) {
             const uint4 v = src[c];
@@ -41,10 +52,10 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_fp8_kernel(
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const __nv_fp8x2_storage_t p0 = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(bf16_lo(w[2 * h]), s), __fdiv_rn(bf16_hi(w[2 * h]), s)),
+                    make_float2(quot(bf16_lo(w[2 * h])), quot(bf16_hi(w[2 * h]))),
                     __NV_SATFINITE, __NV_E4M3);
                 const __nv_fp8x2_storage_t p1 = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(bf16_lo(w[2 * h + 1]), s), __fdiv_rn(bf16_hi(w[2 * h + 1]), s)),
+                    make_float2(quot(bf16_lo(w[2 * h + 1])), quot(bf16_hi(w[2 * h + 1]))),
                     __NV_SATFINITE, __NV_E4M3);
                 packed[h] = (uint32_t)p0 | ((uint32_t)p1 << 16);
             }

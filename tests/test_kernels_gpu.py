@@ -557,6 +557,41 @@ def test_fp8_rowwise_quantisation_is_bit_exact():
     assert (Q[250:] == 0x7F).all()
 
 
+def test_fp8_quantisation_is_bit_exact_on_ties_and_extremes():
+    """Rows built so that x / scale lands exactly on E4M3 rounding midpoints (power-of-two
+    scales), rows spanning nine decades (most quotients round to zero or subnormal codes),
+    and rows at the saturation edge: the codes and scales must equal the oracle's IEEE
+    quotients bit for bit."""
+    g = torch.Generator().manual_seed(52)
+    cols = 256
+    rows = []
+    # midpoints between neighbouring E4M3 values in [2^-6, 448), signed, times 2^k
+    mids = []
+    for e in range(-6, 9):
+        for m in range(8):
+            lo = (1 + m / 8) * 2.0 ** e
+            mids.append(lo + 2.0 ** e / 16)
+    mids = torch.tensor([v for v in mids if v < 448.0])
+    for k in (-20, -3, 0, 5, 30):
+        v = mids[torch.randint(len(mids), (cols,), generator=g)]
+        v = v * torch.where(torch.rand(cols, generator=g) < 0.5, -1.0, 1.0)
+        v[0] = 448.0  # sets the row's amax, so scale = 2^k exactly
+        rows.append(v * 2.0 ** k)
+    for _ in range(40):  # nine decades in one row, random row maxima
+        mag = 10.0 ** (torch.rand(cols, generator=g) * 9 - 6)
+        rows.append(mag * torch.randn(cols, generator=g).sign())
+    rows.append(torch.full((cols,), 3.0))  # every element at the row maximum
+    X = torch.stack(rows).to(torch.bfloat16)
+    n = X.shape[0]
+    Q = torch.empty(n, cols, dtype=torch.uint8, device="cuda")
+    S = torch.empty(n, device="cuda")
+    ops.moe_quantize_rows_fp8(dev(X), None, Q, S)
+    torch.cuda.synchronize()
+    q_ref, s_ref = O.quantize_rows_fp8(h64(X))
+    assert np.array_equal(S.cpu().numpy().view(np.uint32), s_ref.astype(np.float32).view(np.uint32))
+    assert np.array_equal(_e4m3_values(Q), q_ref)
+
+
 def _quantize(t):
     rows = t.reshape(-1, t.shape[-1])
     Q = torch.empty(rows.shape, dtype=torch.uint8, device="cuda")
