@@ -30,6 +30,13 @@ The readings taken where they are silent are the workload definitions:
 * combine: out_t = sum_i g_ti * y_ti + y_shared_t;
 * bias update: b_e <- b_e + gamma * sign(T*k/E - c_e) in fp32, after backward.
 
+Pins (tests/test_oracle_pins.py) hold every function here to facts outside it: k-subset
+enumeration with exact ties, closed forms worked by hand (tests/golden), a dense masked
+brute force of the forward, central finite differences of the backward, torch's bf16 and
+E4M3 conversions, the bias rule's worked example and invariants, the balancing losses' value
+of exactly 1 for one expert. tests/test_pins_catch_mistakes.py plants mistakes here one at a
+time and checks that a pin fails for each. No function is parity unpinned.
+
 Everything is fp64 numpy; bf16 and fp32 inputs convert to fp64 exactly. Matrix products use
 numpy's matmul as a library step. Rows are processed per expert in the order of the
 definition; there is no blocking or fusion.

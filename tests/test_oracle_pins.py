@@ -36,6 +36,20 @@ def _tiny_inputs(rng, T, d, E, f, fs=0, b_scale=0.05):
     return inp
 
 
+# ------------------------------------------------------------------------- router logits
+
+def test_router_logits_of_basis_tokens_are_columns_of_the_router_weight():
+    """Token t = the t-th unit vector picks out column t of W_r: l[t, e] = W_r[e, t]. A square
+    shape (T = d = E) lets a transposed operand through the shapes, so the values catch it;
+    a scaled basis vector scales its logits exactly (dyadic values)."""
+    rng = np.random.default_rng(2)
+    n = 5
+    W_r = rng.integers(-8, 9, size=(n, n)) / 8.0
+    np.testing.assert_array_equal(O.router_logits(np.eye(n), W_r), W_r.T)
+    x = np.diag([1.0, -2.0, 0.5, 0.0, 4.0])
+    np.testing.assert_array_equal(O.router_logits(x, W_r), np.diag(x)[:, None] * W_r.T)
+
+
 # ----------------------------------------------------------------------------- selection
 
 @pytest.mark.parametrize("k", [1, 2, 3, 5, 8])
@@ -123,8 +137,13 @@ def test_k_equals_E_chooses_everything():
 
 
 def test_near_tie_detector():
-    v = np.array([[0.9, 0.9 + 5e-7, 0.1, 0.0], [0.9, 0.8, 0.7, 0.6]])
-    assert list(O.near_tie_tokens(v, 2)) == [True, False]
+    """k = 2: a near tie inside the top k, or between the k-th and the (k+1)-th value, puts
+    the choice in doubt; one below the (k+1)-th value does not."""
+    v = np.array([[0.9, 0.9 + 5e-7, 0.1, 0.0],
+                  [0.9, 0.8, 0.7, 0.6],
+                  [0.9, 0.5 + 5e-7, 0.5, 0.0],
+                  [0.9, 0.8, 0.7, 0.7 + 1e-9]])
+    assert list(O.near_tie_tokens(v, 2)) == [True, False, True, False]
 
 
 # ------------------------------------------------------------------------------ dispatch

@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, times, out):
 def test_slowest_rank_is_taken_on_every_rank():
     world = 2
     times = [[10.0, 3.0, 7.5], [9.0, 4.0, 8.25]]  # per rank: step, GEMM and graph timings
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), times, out), nprocs=world,
                            join=True, start_method="spawn")
