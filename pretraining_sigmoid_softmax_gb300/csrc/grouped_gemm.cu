@@ -19,7 +19,7 @@
 //   warp 2  allocates / frees tensor memory (two accumulators, double-buffered);
 //   warps 4-11 epilogue: tcgen05.ld of TMEM lanes 0-127 (one output row per thread; warps w
 //            and w + 4 share a lane quadrant and take one half of the columns each), the
-//            fused elementwise step, bf16 outputs. Token-major outputs (G1, G2, B4) are
+//            fused elementwise step, bf16 outputs. Token-major outputs (G1, G2, B2, B4) are
 //            packed into swizzled shared-memory boxes and written by TMA stores; B2 reads
 //            its saved a and u through TMA-staged boxes; weight gradients store per thread.
 //            Two warps per quadrant double the loads and stores in flight.
@@ -60,8 +60,8 @@ enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
 constexpr int kAuCols = 16;
 constexpr int kAuBufs = 3;
 constexpr int kSmemBudgetAu = 220 * 1024;
-// Token-major epilogues other than the SwiGLU backward stage their outputs in shared memory,
-// 16 columns x 32 rows per warp and output, two buffers deep, and write them with TMA stores.
+// Token-major epilogues stage their outputs in shared memory, 16 columns x 32 rows per warp
+// and output, two buffers deep, and write them with TMA stores.
 constexpr int kOutCols = 16;
 
 template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
@@ -86,8 +86,8 @@ struct Cfg {
     static constexpr bool AU = EPI == kEpiSwigluBwd;
     static constexpr int AU_BUF_BYTES = 2 * 32 * kAuCols * 2;  // a and u: 32 rows x kAuCols
     static constexpr int AU_BYTES = AU ? kEpiWarps * kAuBufs * AU_BUF_BYTES : 0;
-    static constexpr bool TS = !WGRAD && EPI != kEpiSwigluBwd;  // TMA-store epilogue
-    static constexpr int NOUT = EPI == kEpiSwigluFwd ? 3 : 1;
+    static constexpr bool TS = !WGRAD;  // token-major outputs leave by TMA stores
+    static constexpr int NOUT = EPI == kEpiSwigluFwd ? 3 : EPI == kEpiSwigluBwd ? 2 : 1;
     static constexpr int OUT_BUF_BYTES = NOUT * 32 * kOutCols * 2;  // one chunk, every output
     static constexpr int OUT_BYTES = TS ? kEpiWarps * 2 * OUT_BUF_BYTES : 0;
     static constexpr int BUDGET = (AU || TS ? kSmemBudgetAu : kSmemBudget) - AU_BYTES - OUT_BYTES;
@@ -494,12 +494,16 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
                                                   uint32_t t_acc, int q, int lane, int slot,
                                                   int c_lo, int ncols, const Params& P,
                                                   const CUtensorMap* ma, const CUtensorMap* mu,
+                                                  const CUtensorMap* mda, const CUtensorMap* mdu,
                                                   uint32_t& n, volatile int* abort_flag) {
+    static_assert(kAuCols == kOutCols, "one staged output chunk per a/u chunk");
     const int nch = ncols / kAuCols;
     const int64_t row0 = ti.m0 + 32 * q;
     const int64_t row = row0 + lane;
     const bool ok_row = row < ti.row_end;
-    const int64_t base = row * (int64_t)P.ld_out + ti.n0;
+    // padded segments are whole 128-row halves, so a warp's rows are all inside or all past
+    // the segment; rows past an unpadded layout's end are clipped by the store
+    const bool store = row0 < ti.row_end;
     // gate folded into the expert: dy is the ungated row gradient, dh = g (dy W_d), and the
     // gate's gradient (dy W_d) . h is summed per 64-column group (h recomputed in fp32)
     const float g = (P.row_scale && ok_row) ? __ldg(P.row_scale + row) : 1.0f;
@@ -514,10 +518,10 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
         tmem_ld_wait();
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) return false;
-        if (ok_row) {
+        float dav[kAuCols], duv[kAuCols];
+        if (store) {  // lanes past an unpadded layout's end see zero-filled a, u and acc
             const uint8_t* abuf = S.au + ((size_t)slot * kAuBufs + b) * C::AU_BUF_BYTES;
             const uint8_t* ubuf = abuf + C::AU_BUF_BYTES / 2;
-            float dav[kAuCols], duv[kAuCols];
 #pragma unroll
             for (int j = 0; j < kAuCols / 8; ++j) {
                 const uint4 a4 = *reinterpret_cast<const uint4*>(abuf + au_offset(lane, j));
@@ -538,20 +542,30 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
             }
             const int col = ti.n0 + c;
             if (P.gate_part && (col + kAuCols) % 64 == 0) {  // last chunk of a 64-column group
-                P.gate_part[row * (int64_t)(P.ld_out / 64) + col / 64] = gpart;
+                if (ok_row) P.gate_part[row * (int64_t)(P.ld_out / 64) + col / 64] = gpart;
                 gpart = 0.f;
             }
-            uint4* da = reinterpret_cast<uint4*>(P.out0 + base + c);
-            uint4* du = reinterpret_cast<uint4*>(P.out1 + base + c);
-#pragma unroll
-            for (int j = 0; j < kAuCols / 8; ++j) {
-                da[j] = pack_chunk8(dav + 8 * j);
-                du[j] = pack_chunk8(duv + 8 * j);
-            }
         }
-        __syncwarp();  // every lane is done with buffer b
+        __syncwarp();  // every lane is done with a/u buffer b
         if (lane == 0 && i + kAuBufs < nch)
             au_issue<C>(S, ma, mu, slot, n + kAuBufs, row0, ti.n0 + c + kAuBufs * kAuCols);
+        if (store) {
+            uint8_t* ob = S.ob + ((size_t)slot * 2 + (n & 1)) * C::OUT_BUF_BYTES;
+            if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kAuCols / 8; ++j) {
+                *reinterpret_cast<uint4*>(ob + sw32_offset(lane, j)) = pack_chunk8(dav + 8 * j);
+                *reinterpret_cast<uint4*>(ob + 1024 + sw32_offset(lane, j)) = pack_chunk8(duv + 8 * j);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(mda, smem_u32(ob), ti.n0 + c, (int32_t)row0);
+                tma_store_2d(mdu, smem_u32(ob + 1024), ti.n0 + c, (int32_t)row0);
+                bulk_commit();
+            }
+        }
     }
     return true;
 }
@@ -741,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t_acc = tmem_base + buf * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
             if constexpr (C::AU) {
                 if (!swiglu_bwd_staged<C>(S, ti, t_acc, q, lane, slot, c_lo, kCols, P, &ma1, &mb1,
-                                          n_au, abort_flag))
+                                          &mo0, &mo1, n_au, abort_flag))
                     break;
             } else if constexpr (C::TS) {
                 epilogue_tma_store<C>(S, ti, t_acc, q, lane, slot, c_lo, kCols, P, &mo0, &mo1, &mo2,
@@ -1031,10 +1045,13 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.ld_out = f;
         P.row_scale = row_gate;
         P.gate_part = gate_part;
+        CUtensorMap mod[3];
+        if (!out_maps(mod, dA, dU, nullptr, f, rows)) return MOE_ERR_LAUNCH;
         if (f % 256 == 0)
-            rc = launch<CfgSwigluBwdP>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st);
+            rc = launch<CfgSwigluBwdP>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st, mod);
         else
-            rc = launch<CfgSwigluBwd<128>>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 128), st);
+            rc = launch<CfgSwigluBwd<128>>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 128), st,
+                                           mod);
         if (rc != MOE_OK) return rc;
     }
     // B4: dX = dA W_g + dU W_u (W_g[e] is [f, d]: K = f rows, N = d contiguous)
