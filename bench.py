@@ -337,7 +337,7 @@ def main():
             stream.wait_event(read_back[0])
             stream.wait_event(read_back[1])
 
-        run_steps(2)
+        run_steps(max(4, args.warmup))  # the second buffer set warms up too
         sync_all()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)

@@ -202,6 +202,24 @@ int moe_quantize_rows_fp8(const moe_bf16* X, const int64_t* rows_limit, int64_t 
                           uint8_t* Q, float* scale, moe_stream_t stream);
 
 /*
+ * moe_permute_fp8 - the FP8 codes of the expert-major rows from the codes of the tokens.
+ * The rowwise codes and scale of a row depend on that row alone, and every expert-major
+ * row is a copy of its token's row x[t] (the dispatch of section 2.5 of the handbook
+ * summary). So quantising the T token rows once and copying them to the rows gives exactly
+ * moe_quantize_rows_fp8 of X_perm, bit for bit, with a k-fold smaller quantisation.
+ * In : xq [T, d] codes and sx [T] scales (moe_quantize_rows_fp8 of x); slot_to_row [T,k],
+ *      perm_token [rows] and row_offsets [E+1] from moe_permute (padding rows have
+ *      perm_token < 0).
+ * Out: Xq [rows, d] codes and sX [rows] scales, where rows = row_offsets[E]: the token's
+ *      codes and scale on each of its k rows; padding rows get zero codes and scale 1 (the
+ *      quantisation of a zero row). Slots with slot_to_row < 0 are skipped.
+ * d % 128 == 0, k <= min(E, 32), E <= 256; xq and Xq 16-byte aligned.
+ */
+int moe_permute_fp8(const uint8_t* xq, const float* sx, const int32_t* slot_to_row,
+                    const int32_t* perm_token, const int64_t* row_offsets, int64_t T, int d,
+                    int E, int k, uint8_t* Xq, float* sX, moe_stream_t stream);
+
+/*
  * moe_expert_fwd_fp8 - moe_expert_fwd with E4M3 GEMM operands (tcgen05 kind::f8f6f4, fp32
  * accumulation). Each product is dequantised in the epilogue by its A-row scale and its
  * B-row (output-channel) scale; a, u, h, y are bf16 as in moe_expert_fwd. h is quantised

@@ -31,6 +31,7 @@ PROTOTYPES = {
     "moe_expert_fwd": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                             _P]),
     "moe_quantize_rows_fp8": (_I, [_P, _P, _I64, _I, _P, _P, _P]),
+    "moe_permute_fp8": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P]),
     "moe_expert_fwd_fp8": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I64, _I, _I, _P, _P]),

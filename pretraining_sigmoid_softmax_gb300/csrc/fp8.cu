@@ -65,6 +65,60 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_fp8_kernel(
     }
 }
 
+// Rowwise codes are a function of the row alone, so the codes of a token's k expert-major
+// rows are its own codes: quantise the T token rows once and copy codes and scale to the
+// rows (one warp per token, 16-byte vectors), instead of quantising the k-fold larger
+// permuted bf16 rows.
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32) gather_fp8_kernel(
+    const uint8_t* __restrict__ xq, const float* __restrict__ sx,
+    const int32_t* __restrict__ slot_to_row, int64_t T, int d, int k, uint8_t* __restrict__ Xq,
+    float* __restrict__ sX) {
+    const int lane = threadIdx.x % 32;
+    const int64_t t = (int64_t)blockIdx.x * kGatherWarps + threadIdx.x / 32;
+    if (t >= T) return;
+    int32_t my_row = -1;
+    if (lane < k) my_row = slot_to_row[t * k + lane];
+    if (my_row >= 0) sX[my_row] = sx[t];
+    const uint4* src = reinterpret_cast<const uint4*>(xq + t * d);
+    const int nvec = d / 16;
+    for (int c0 = 0; c0 < nvec; c0 += 32) {  // warp-uniform trip count
+        const int c = c0 + lane;
+        const bool in = c < nvec;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (in) v = src[c];
+        for (int i = 0; i < k; ++i) {
+            const int32_t row = __shfl_sync(0xffffffffu, my_row, i);
+            if (in && row >= 0) reinterpret_cast<uint4*>(Xq + (int64_t)row * d)[c] = v;
+        }
+    }
+}
+
+// Padding rows of each segment (the trailing rows with perm_token < 0; at most
+// MOE_ROW_ALIGN - 1 per expert) get what quantising a zero row gives: zero codes, scale 1.
+constexpr int kPadSplitFp8 = 16;
+
+__global__ void __launch_bounds__(256) pad_rows_fp8_kernel(const int64_t* __restrict__ row_offsets,
+                                                           const int32_t* __restrict__ perm_token,
+                                                           int d, uint8_t* __restrict__ Xq,
+                                                           float* __restrict__ sX) {
+    const int e = blockIdx.x;
+    const int64_t hi = row_offsets[e + 1];
+    int64_t lo = row_offsets[e];
+    if (hi - lo > MOE_ROW_ALIGN - 1) lo = hi - (MOE_ROW_ALIGN - 1);
+    const int vec_per_row = d / 16;
+    for (int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
+         i += (int64_t)gridDim.y * blockDim.x) {
+        const int64_t r = lo + i / vec_per_row;
+        const int c = (int)(i % vec_per_row);
+        if (perm_token[r] < 0) {
+            reinterpret_cast<uint4*>(Xq + r * d)[c] = make_uint4(0, 0, 0, 0);
+            if (c == 0) sX[r] = 1.0f;
+        }
+    }
+}
+
 }  // namespace
 
 int launch_quantize_rows_fp8(const __nv_bfloat16* X, const int64_t* limit, int64_t rows, int cols,
@@ -90,4 +144,20 @@ extern "C" int moe_quantize_rows_fp8(const moe_bf16* X, const int64_t* rows_limi
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     return launch_quantize_rows_fp8(reinterpret_cast<const __nv_bfloat16*>(X), rows_limit, rows,
                                     cols, Q, scale, (cudaStream_t)stream);
+}
+
+extern "C" int moe_permute_fp8(const uint8_t* xq, const float* sx, const int32_t* slot_to_row,
+                               const int32_t* perm_token, const int64_t* row_offsets, int64_t T,
+                               int d, int E, int k, uint8_t* Xq, float* sX, moe_stream_t stream) {
+    if (!xq || !sx || !slot_to_row || !perm_token || !row_offsets || !Xq || !sX)
+        return MOE_ERR_INVALID_ARG;
+    if (T <= 0 || d <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(xq) || !aligned16(Xq)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    gather_fp8_kernel<<<(unsigned)cdiv(T, kGatherWarps), kGatherWarps * 32, 0, st>>>(
+        xq, sx, slot_to_row, T, d, k, Xq, sX);
+    pad_rows_fp8_kernel<<<dim3(E, kPadSplitFp8), 256, 0, st>>>(row_offsets, perm_token, d, Xq, sX);
+    return launch_status();
 }

@@ -105,8 +105,10 @@ class MoEPlan:
             self.Wg8, self.sWg = _empty((E, f, d), u8, dev), _empty((E * f,), f32, dev)
             self.Wu8, self.sWu = _empty((E, f, d), u8, dev), _empty((E * f,), f32, dev)
             self.Wd8, self.sWd = _empty((E, d, f), u8, dev), _empty((E * d,), f32, dev)
+            # codes of the token rows: copied to the expert-major rows, and the shared
+            # expert's operand
+            self.x8, self.sx = _empty((T, d), u8, dev), _empty((T,), f32, dev)
             if fs:
-                self.x8, self.sx = _empty((T, d), u8, dev), _empty((T,), f32, dev)
                 self.Hs8, self.sHs = _empty((T, fs), u8, dev), _empty((T,), f32, dev)
                 self.Wsg8, self.sWsg = _empty((1, fs, d), u8, dev), _empty((fs,), f32, dev)
                 self.Wsu8, self.sWsu = _empty((1, fs, d), u8, dev), _empty((fs,), f32, dev)
@@ -168,8 +170,8 @@ class MoEPlan:
             n += 2 + (1 if backward else 0)                 # balancing losses (+ gradient)
         n += 5                                              # permute
         n += 1 if not s.fp8 else 0                          # row gates (folded gates)
-        if s.fp8:  # quantise X, W_g, W_u, W_d; G1, quantise H, G2 (shared: the same)
-            n += 7 + (7 if s.f_shared else 0)
+        if s.fp8:  # quantise x, W_g, W_u, W_d; expert-major codes (2); G1, quantise H, G2
+            n += 9 + (6 if s.f_shared else 0)               # (shared: its weights, G1, H, G2)
         else:
             n += 2 + (2 if s.f_shared else 0)               # expert forward (G1, G2)
         n += 1                                              # combine
@@ -192,6 +194,8 @@ class MoEPlan:
         self.W = (W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d)
         softmax = s.mode == ops.MODE_SOFTMAX
         main = stream if stream is not None else torch.cuda.current_stream()
+        if s.fp8:  # before the fork: the routed rows and the shared expert both use them
+            ops.moe_quantize_rows_fp8(x, None, self.x8, self.sx, stream)
         if s.f_shared and self.overlap:  # fork: the shared expert on the side stream
             self.side.wait_stream(main)
             self._shared_forward(x, Ws_g, Ws_u, Ws_d, self.side)
@@ -214,7 +218,8 @@ class MoEPlan:
             q(W_g, None, self.Wg8, self.sWg, stream)
             q(W_u, None, self.Wu8, self.sWu, stream)
             q(W_d, None, self.Wd8, self.sWd, stream)
-            q(self.X_perm, self.row_offsets[s.E:], self.X8, self.sX, stream)
+            ops.moe_permute_fp8(self.x8, self.sx, self.slot_to_row, self.perm_token,
+                                self.row_offsets, self.X8, self.sX, stream)
             self._gemm(ops.moe_expert_fwd_fp8, self.X8, self.sX, self.row_offsets, self.Wg8,
                        self.sWg, self.Wu8, self.sWu, self.Wd8, self.sWd, self.A, self.U, self.H,
                        self.H8, self.sH, self.Y_perm, self.ws, stream=stream)
@@ -238,7 +243,6 @@ class MoEPlan:
             q(Ws_g, None, self.Wsg8, self.sWsg, side)
             q(Ws_u, None, self.Wsu8, self.sWsu, side)
             q(Ws_d, None, self.Wsd8, self.sWsd, side)
-            q(x, None, self.x8, self.sx, side)
             self._gemm(ops.moe_expert_fwd_fp8, self.x8, self.sx, None, self.Wsg8, self.sWsg,
                        self.Wsu8, self.sWsu, self.Wsd8, self.sWsd, self.As, self.Us, self.Hs,
                        self.Hs8, self.sHs, self.Ys, self.ws_side, stream=side)

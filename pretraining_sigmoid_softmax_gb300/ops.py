@@ -123,6 +123,17 @@ def moe_quantize_rows_fp8(X, rows_limit, Q, scale, stream=None):
                                              _stream(stream)), "moe_quantize_rows_fp8")
 
 
+def moe_permute_fp8(xq, sx, slot_to_row, perm_token, row_offsets, Xq, sX, stream=None):
+    """Codes and scales of the expert-major rows copied from those of the tokens."""
+    T, d = xq.shape
+    k = slot_to_row.shape[1]
+    E = row_offsets.numel() - 1
+    _contig(xq, sx, slot_to_row, perm_token, row_offsets, Xq, sX)
+    _check(_lib.load().moe_permute_fp8(_p(xq), _p(sx), _p(slot_to_row), _p(perm_token),
+                                       _p(row_offsets), T, d, E, k, _p(Xq), _p(sX),
+                                       _stream(stream)), "moe_permute_fp8")
+
+
 def moe_expert_fwd_fp8(Xq, sX, row_offsets, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, H, Hq, sH, Y,
                        ws, stream=None, row_gate=None):
     rows, d = Xq.shape

@@ -592,6 +592,34 @@ def test_fp8_quantisation_is_bit_exact_on_ties_and_extremes():
     assert np.array_equal(_e4m3_values(Q), q_ref)
 
 
+@pytest.mark.parametrize("T,d,E,k,skew", [(1000, 256, 8, 2, False), (777, 512, 16, 4, True),
+                                          (5, 128, 16, 4, True)])
+def test_fp8_permuted_codes_equal_quantised_permuted_rows(T, d, E, k, skew):
+    """Codes and scales copied from the token rows to the expert-major rows equal the
+    oracle's rowwise quantisation of the permuted bf16 rows bit for bit; padding rows are
+    zero codes with scale 1 (a zero row's quantisation), including skewed layouts with empty
+    experts."""
+    g = torch.Generator().manual_seed(T + 7 * E)
+    idx = _random_choice(T, E, k, g, skew)
+    x = randn_bf16((T, d), g) * torch.rand(T, 1, generator=g).mul(20).to(torch.bfloat16)
+    x[min(3, T - 1)] = 0  # a zero token row: scale 1 on each of its rows
+    r = _permute(idx, x, E)
+    xq = torch.empty(T, d, dtype=torch.uint8, device="cuda")
+    sx = torch.empty(T, device="cuda")
+    ops.moe_quantize_rows_fp8(dev(x), None, xq, sx)
+    R = r["X_perm"].shape[0]
+    Xq = torch.full((R, d), 0x7F, dtype=torch.uint8, device="cuda")
+    sX = torch.full((R,), -7.0, device="cuda")
+    ops.moe_permute_fp8(xq, sx, r["slot_to_row"], r["perm_token"], r["row_offsets"], Xq, sX)
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    n = int(r["row_offsets"][-1])
+    q_ref, s_ref = O.quantize_rows_fp8(h64(r["X_perm"][:n].cpu()))
+    assert np.array_equal(sX[:n].cpu().numpy().view(np.uint32), s_ref.astype(np.float32).view(np.uint32))
+    assert np.array_equal(_e4m3_values(Xq[:n]), q_ref)
+    assert (Xq[n:] == 0x7F).all() and (sX[n:] == -7.0).all()  # past the layout: untouched
+
+
 def _quantize(t):
     rows = t.reshape(-1, t.shape[-1])
     Q = torch.empty(rows.shape, dtype=torch.uint8, device="cuda")

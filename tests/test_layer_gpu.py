@@ -131,6 +131,9 @@ SMALL = [
               aux_seq=1e-2, seq_len=384),
     MoEConfig("fp8_forward_shared", T=1024, d=512, E=8, k=2, f=256, f_shared=256,
               mode="sigmoid", seed=18, backward=True, bias_update=True, precision="fp8"),
+    MoEConfig("fp8_forward_softmax_ragged", T=777, d=256, E=5, k=2, f=128, f_shared=0,
+              mode="softmax", seed=21, backward=True, bias_update=False, z_coef=1e-3,
+              precision="fp8"),
     # fewer tokens than one tile row block: 7-row tensors behind 32- and 128-row boxes
     MoEConfig("sub_tile_T7", T=7, d=128, E=4, k=2, f=128, f_shared=128, mode="sigmoid",
               seed=19, backward=True, bias_update=True),

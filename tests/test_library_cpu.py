@@ -68,5 +68,7 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert rc == 1
     rc = lib.moe_bias_update(None, 8, 16, 2, 0.001, None, None)
     assert rc == 1
+    rc = lib.moe_permute_fp8(None, None, None, None, None, 16, 128, 8, 2, None, None, None)
+    assert rc == 1
     code = ctypes.c_int(0)
     assert lib.moe_device_status(None, None, None) == 1
