@@ -28,7 +28,7 @@ METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 pe
 # DRAM bytes (read + write) of one step's grouped-GEMM launches from an ncu capture of the
 # current kernels (profiles/grouped_gemm_dram_C4_large.md); workloads without a capture
 # report null.
-MEASURED_GEMM_TRAFFIC = {"C4": 142.52e9}
+MEASURED_GEMM_TRAFFIC = {"C4": 105.13e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -220,16 +220,19 @@ def main():
     inp = make_inputs(cfg)
     dev = {k: v.cuda() for k, v in inp.items()}
     plan = MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)
+    # the end-to-end loop alternates two buffer sets; the second is made and warmed up here
+    plan_b = None if args.no_e2e else MoEPlan(MoEShape.from_config(cfg), "cuda",
+                                              backward=cfg.backward)
     b_work = dev["b"].clone()
     stream = torch.cuda.current_stream()
 
-    def step(x, dY):
-        plan.forward(x, dev["W_r"], b_work, dev["W_g"], dev["W_u"], dev["W_d"], dev.get("Ws_g"),
-                     dev.get("Ws_u"), dev.get("Ws_d"))
+    def step(x, dY, p=plan):
+        p.forward(x, dev["W_r"], b_work, dev["W_g"], dev["W_u"], dev["W_d"], dev.get("Ws_g"),
+                  dev.get("Ws_u"), dev.get("Ws_d"))
         if cfg.backward:
-            plan.backward(dY)
+            p.backward(dY)
             if cfg.bias_update:
-                plan.bias_update(b_work, cfg.gamma, cfg.bias_rule)
+                p.bias_update(b_work, cfg.gamma, cfg.bias_rule)
 
     def sync_all():
         torch.cuda.synchronize()
@@ -239,6 +242,8 @@ def main():
 
     for _ in range(args.warmup):
         step(dev["x"], dev.get("dY"))
+        if plan_b is not None:
+            step(dev["x"], dev.get("dY"), plan_b)
     ops.moe_clear_device_status()
     sync_all()
 
@@ -262,31 +267,16 @@ def main():
     ms_eager = timed(lambda: step(dev["x"], dev.get("dY")), args.steps)
     gemm_ms = sum(a.elapsed_time(b) for a, b in plan.gemm_events)
     plan.gemm_events = None
-    ms_graph = None
-    if not args.no_graph:
-        weights = {k: dev[k] for k in ("W_r", "W_g", "W_u", "W_d", "Ws_g", "Ws_u", "Ws_d") if k in dev}
-        graph = plan.capture_step(dev["x"], weights, dev.get("dY") if cfg.backward else None,
-                                  b_work, cfg.gamma, cfg.bias_rule, cfg.bias_update)
-        graph.replay()
-        ms_graph = timed(graph.replay, args.steps)
-    clocks = sampler.stop()
-    code, site = ops.moe_device_status()
-    if code != 0:
-        raise RuntimeError(f"device status {code} ({ops.status_string(code)}) at site {site}")
-    ms_eager, gemm_ms, ms_g = slowest_rank(
-        [ms_eager, gemm_ms, ms_graph if ms_graph is not None else 0.0], world)
-    ms_total = ms_g if ms_graph is not None else ms_eager
-    ms_step = ms_total / args.steps
-    value = job_tokens_per_s(world, cfg.T, ms_step)
 
     # ------------------------------------------------------------ end to end, host buffers
+    # (between the two device-resident passes, under the same clock sampling)
     e2e = None
     if not args.no_e2e:
         # Pipelined like a training loop: step i+1's inputs are uploaded on a copy stream
         # while step i computes, and step i's out/dx are read back while step i+1 computes.
         # Two sets of activation buffers (plans) alternate so a readback never races the
         # next step's writes. Every step's copies are inside the timed region.
-        plans = [plan, MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)]
+        plans = [plan, plan_b]
         hx = inp["x"].pin_memory()
         hdy = inp["dY"].pin_memory() if cfg.backward else None
         hout = [torch.empty_like(inp["x"]).pin_memory() for _ in range(2)]
@@ -320,12 +310,7 @@ def main():
                 stream.wait_event(uploaded[j])
                 stream.wait_event(read_back[j])  # slot j's previous outputs are on the host
                 p = plans[j]
-                p.forward(xd[j], dev["W_r"], b_work, dev["W_g"], dev["W_u"], dev["W_d"],
-                          dev.get("Ws_g"), dev.get("Ws_u"), dev.get("Ws_d"))
-                if cfg.backward:
-                    p.backward(dyd[j])
-                    if cfg.bias_update:
-                        p.bias_update(b_work, cfg.gamma, cfg.bias_rule)
+                step(xd[j], dyd[j] if cfg.backward else None, p)
                 freed[j].record(stream)
                 computed[j].record(stream)
                 down.wait_event(computed[j])
@@ -337,7 +322,7 @@ def main():
             stream.wait_event(read_back[0])
             stream.wait_event(read_back[1])
 
-        run_steps(max(4, args.warmup))  # the second buffer set warms up too
+        run_steps(args.warmup)
         sync_all()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -351,7 +336,24 @@ def main():
                "d2h_bytes_per_step": nbytes * (2 if cfg.backward else 1),
                "ms_per_step": ms_e2e,
                "note": "pinned host buffers; uploads and readbacks overlap adjacent steps"}
-        del plans
+        del plans, plan_b
+
+    ms_graph = None
+    if not args.no_graph:
+        weights = {k: dev[k] for k in ("W_r", "W_g", "W_u", "W_d", "Ws_g", "Ws_u", "Ws_d") if k in dev}
+        graph = plan.capture_step(dev["x"], weights, dev.get("dY") if cfg.backward else None,
+                                  b_work, cfg.gamma, cfg.bias_rule, cfg.bias_update)
+        graph.replay()
+        ms_graph = timed(graph.replay, args.steps)
+    clocks = sampler.stop()
+    code, site = ops.moe_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} ({ops.status_string(code)}) at site {site}")
+    ms_eager, gemm_ms, ms_g = slowest_rank(
+        [ms_eager, gemm_ms, ms_graph if ms_graph is not None else 0.0], world)
+    ms_total = ms_g if ms_graph is not None else ms_eager
+    ms_step = ms_total / args.steps
+    value = job_tokens_per_s(world, cfg.T, ms_step)
 
     # ------------------------------------------------------------------------- report
     if rank != 0:
