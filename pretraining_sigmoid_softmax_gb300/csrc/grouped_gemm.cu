@@ -120,17 +120,16 @@ struct Params {
     int M_out;  // weight gradients: rows of each expert's output
     int nprob;  // weight gradients: (a0,out0) and, if 2, (a1,out1)
     int kb_per_expert;  // B operand rows per expert (MN-major weights: K extent per expert)
+    // weight gradients: the outputs of problems 0 and 1 (token-major outputs leave through
+    // the output tensor maps instead)
     __nv_bfloat16* out0;
     __nv_bfloat16* out1;
-    __nv_bfloat16* out2;
-    const __nv_bfloat16* in0;  // SwiGLU backward: saved a
-    const __nv_bfloat16* in1;  // SwiGLU backward: saved u
     const float* sa;           // FP8: scale of each A row (indexed by the global row)
     const float* sb0;          // FP8: scale of each B row (output channel), first B operand
     const float* sb1;          // FP8: second B operand (W_u of G1)
     const float* row_scale;    // gate folded into the expert: G1 writes g*h, B2 forms g*dh
     float* gate_part;          // B2 with row_scale: per row, (dy W_d) . h per 64 columns
-    int ld_out;
+    int ld_out;                // B2: output columns; gate_part holds ld_out / 64 per row
     int* status;
     uint64_t wait_limit_ns;
 };
@@ -971,10 +970,6 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     Params P = base_params(row_offsets, rows, E);
     P.N = f;
     P.K0 = d;
-    P.out0 = reinterpret_cast<__nv_bfloat16*>(A);
-    P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
-    P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
-    P.ld_out = f;
     P.row_scale = row_gate;
     CUtensorMap moa[3], moy[3];
     if (!out_maps(moa, A, U, H, f, rows) || !out_maps(moy, Y, nullptr, nullptr, d, rows))
@@ -985,8 +980,6 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     Params Q = base_params(row_offsets, rows, E);
     Q.N = d;
     Q.K0 = f;
-    Q.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
-    Q.ld_out = d;
     if (d % 256 == 0) {  // CTA pair: each CTA stages 128 of the tile's 256 W_d rows
         if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
         rc = launch<CfgStoreKP>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st, moy);
@@ -1019,8 +1012,6 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
     int32_t* order = wc.take<int32_t>(E + 1);
     if (row_offsets && (!ws || !wc.ok())) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    const __nv_bfloat16* Ab = reinterpret_cast<const __nv_bfloat16*>(A);
-    const __nv_bfloat16* Ub = reinterpret_cast<const __nv_bfloat16*>(U);
     int rc;
 
     // B2: dH = dY W_d (W_d[e] is [d, f]: K = d rows, N = f contiguous), SwiGLU backward; the
@@ -1038,10 +1029,6 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.N = f;
         P.K0 = d;
         P.kb_per_expert = d;
-        P.out0 = reinterpret_cast<__nv_bfloat16*>(dA);
-        P.out1 = reinterpret_cast<__nv_bfloat16*>(dU);
-        P.in0 = Ab;
-        P.in1 = Ub;
         P.ld_out = f;
         P.row_scale = row_gate;
         P.gate_part = gate_part;
@@ -1066,8 +1053,6 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.K0 = f;
         P.K1 = f;
         P.kb_per_expert = f;
-        P.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
-        P.ld_out = d;
         CUtensorMap mox[3];
         if (!out_maps(mox, dX, nullptr, nullptr, d, rows)) return MOE_ERR_LAUNCH;
         if (d % 256 == 0)
@@ -1154,10 +1139,6 @@ extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int6
     Params P = base_params(row_offsets, rows, E);
     P.N = f;
     P.K0 = d;
-    P.out0 = reinterpret_cast<__nv_bfloat16*>(A);
-    P.out1 = reinterpret_cast<__nv_bfloat16*>(U);
-    P.out2 = reinterpret_cast<__nv_bfloat16*>(H);
-    P.ld_out = f;
     P.sa = sX;
     P.sb0 = sWg;
     P.sb1 = sWu;
@@ -1175,8 +1156,6 @@ extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int6
     Params Q = base_params(row_offsets, rows, E);
     Q.N = d;
     Q.K0 = f;
-    Q.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
-    Q.ld_out = d;
     Q.sa = sH;
     Q.sb0 = sWd;
     if (d % 256 == 0)
