@@ -98,6 +98,18 @@ int moe_clear_device_status(moe_stream_t stream);
 void moe_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * moe_check_bounded_wait - self-check of the failure path of the bounded device waits (no
+ * counterpart on the pages, which name failure detection only as monitoring: DCGM, NaN
+ * detection). Enqueues one kernel that waits, with the same bounded wait the grouped-GEMM
+ * kernels use, on an mbarrier that nothing arrives on, with no copy or tensor-core work in
+ * flight. The wait runs out after limit_ns nanoseconds (0 < limit_ns <= 1e9, else
+ * MOE_ERR_INVALID_ARG), records MOE_ERR_TIMEOUT with site 90 in the device status word and
+ * the kernel returns; the context stays usable. Clear the word with moe_clear_device_status
+ * afterwards.
+ */
+int moe_check_bounded_wait(uint64_t limit_ns, moe_stream_t stream);
+
+/*
  * moe_route - router forward (R1).
  * Definition: l[t,e] = sum_j x[t,j] * W_r[e,j] in fp32, each sum in a fixed order.
  *   MOE_MODE_SIGMOID: s = 1/(1+exp(-l)); choose the k largest s[e] + b[e] (lower e first

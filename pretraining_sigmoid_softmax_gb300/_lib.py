@@ -25,6 +25,7 @@ PROTOTYPES = {
     "moe_device_status": (_I, [_P, _P, _P]),
     "moe_clear_device_status": (_I, [_P]),
     "moe_set_wait_limit_ns": (None, [_U64]),
+    "moe_check_bounded_wait": (_I, [_U64, _P]),
     "moe_route": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),

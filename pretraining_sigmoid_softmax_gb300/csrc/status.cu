@@ -22,6 +22,23 @@ int g_supported[kMaxDevices] = {0};  // 0 unknown, 1 yes, 2 no
 std::mutex g_mu;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
+// Site recorded by the bounded-wait self-check.
+constexpr int kSiteWaitCheck = 90;
+
+// One mbarrier that nothing ever arrives on, waited on with the bounded wait every role of
+// the grouped-GEMM kernels uses. Nothing is in flight: the wait runs out after `limit_ns`,
+// records MOE_ERR_TIMEOUT and the kernel returns.
+__global__ void bounded_wait_check_kernel(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    moe::mbar_init(moe::smem_u32(&bar), 1);
+    moe::fence_mbar_init();
+    moe::mbar_wait_bounded(moe::smem_u32(&bar), 0u, &abort_flag, status, limit_ns,
+                           kSiteWaitCheck);
+}
+
 int current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
@@ -123,5 +140,14 @@ int moe_clear_device_status(moe_stream_t stream) {
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+
+int moe_check_bounded_wait(uint64_t limit_ns, moe_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
+    if (!moe::device_supported()) return MOE_ERR_UNSUPPORTED;
+    int* w = moe::device_status_word();
+    if (!w) return MOE_ERR_LAUNCH;
+    bounded_wait_check_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(w, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
 
 }  // extern "C"

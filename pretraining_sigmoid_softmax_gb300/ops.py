@@ -70,6 +70,12 @@ def moe_set_wait_limit_ns(ns: int):
     _lib.load().moe_set_wait_limit_ns(int(ns))
 
 
+def moe_check_bounded_wait(limit_ns: int, stream=None):
+    """One bounded wait that cannot complete: records MOE_ERR_TIMEOUT (site 90) and returns."""
+    _check(_lib.load().moe_check_bounded_wait(int(limit_ns), _stream(stream)),
+           "moe_check_bounded_wait")
+
+
 def moe_route(x, W_r, b, k, mode, z_coef, logits, topk_idx, topk_gate, topk_score, lse, z_loss,
               ws, stream=None):
     T, d = x.shape

@@ -163,6 +163,28 @@ def test_permute_reports_bad_index_without_touching_other_rows():
     assert ops.moe_device_status()[0] == 0
 
 
+def test_bounded_wait_that_runs_out_records_timeout_and_returns():
+    """Failure detection without a fault: a bounded wait on an mbarrier that nothing arrives
+    on runs out after its limit, records MOE_ERR_TIMEOUT (site 90) and the kernel returns;
+    the context stays usable (an expert GEMM right after gives the usual result)."""
+    import time
+    ops.moe_clear_device_status()
+    assert ops.moe_device_status()[0] == 0
+    t0 = time.perf_counter()
+    ops.moe_check_bounded_wait(5_000_000)  # 5 ms
+    code, site = ops.moe_device_status()
+    elapsed = time.perf_counter() - t0
+    assert (code, site) == (6, 90)
+    assert elapsed >= 0.005
+    ops.moe_clear_device_status()
+    assert ops.moe_device_status()[0] == 0
+    g = torch.Generator().manual_seed(90)
+    X, dY = randn_bf16((200, 256), g), randn_bf16((200, 256), g)
+    W_g, W_u, W_d = _weights(1, 256, 128, g)
+    B = _run_experts(X, dY, None, W_g, W_u, W_d)
+    _check_expert(B, 0, 0, 200, X, dY, W_g, W_u, W_d, "after a timeout")
+
+
 # --------------------------------------------------------------------- expert GEMMs
 
 def _expert_buffers(rows, d, f, E):

@@ -70,5 +70,8 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert rc == 1
     rc = lib.moe_permute_fp8(None, None, None, None, None, 16, 128, 8, 2, None, None, None)
     assert rc == 1
+    lib.moe_check_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+    assert lib.moe_check_bounded_wait(0, None) == 1  # a zero limit is rejected
+    assert lib.moe_check_bounded_wait(2_000_000_000, None) == 1  # so is one above a second
     code = ctypes.c_int(0)
     assert lib.moe_device_status(None, None, None) == 1
