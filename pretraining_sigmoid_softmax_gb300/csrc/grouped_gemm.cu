@@ -639,7 +639,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *S.tmem_slot;
     volatile int* abort_flag = S.abort_flag;
 
-    bool layout_ok = true;
+    // the padded layout: offsets start at 0, never decrease, every segment is a whole number
+    // of 128-row tiles and the last ends within the row capacity; anything else is reported
+    // and the launch does no work (the same decision in every CTA)
+    bool bad_offs = false;
+    if (P.row_offsets && tid < P.E) {
+        const int64_t lo = S.offs[tid], hi = S.offs[tid + 1];
+        bad_offs = hi < lo || (hi - lo) % BM != 0 || (tid == 0 && lo != 0);
+    }
+    bool layout_ok = !__syncthreads_or(bad_offs);
     if (P.row_offsets && S.offs[P.E] > P.rows) layout_ok = false;
     if (!layout_ok && tid == 0) record_error(P.status, MOE_ERR_BAD_INDEX, 20);
     const int64_t ntiles = layout_ok ? total_tiles<C>(P, S) : 0;

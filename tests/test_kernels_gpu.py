@@ -185,6 +185,29 @@ def test_bounded_wait_that_runs_out_records_timeout_and_returns():
     _check_expert(B, 0, 0, 200, X, dY, W_g, W_u, W_d, "after a timeout")
 
 
+@pytest.mark.parametrize("offsets", [[0, 256, 128, 384],   # a segment that ends before it starts
+                                     [0, 100, 228, 356],   # segments not whole 128-row tiles
+                                     [128, 256, 384, 512],  # a layout that does not start at 0
+                                     [0, 128, 256, 1024]])  # past the row capacity
+def test_expert_gemms_reject_a_malformed_layout(offsets):
+    """row_offsets that break the padded layout are reported (MOE_ERR_BAD_INDEX) by every
+    CTA's own check before any tile is touched: the outputs stay as they were."""
+    rows, d, f, E = 512, 256, 128, 3
+    g = torch.Generator().manual_seed(91)
+    X = dev(randn_bf16((rows, d), g))
+    W_g, W_u, W_d = (dev(w) for w in _weights(E, d, f, g))
+    B = _expert_buffers(rows, d, f, E)
+    ro = torch.tensor(offsets, dtype=torch.int64, device="cuda")
+    ops.moe_clear_device_status()
+    ops.moe_expert_fwd(X, ro, W_g, W_u, W_d, B["A"], B["U"], B["H"], B["Y"], _ws(rows, d, E, 1))
+    torch.cuda.synchronize()
+    code, site = ops.moe_device_status()
+    assert (code, site) == (5, 20)
+    for name in ("A", "U", "H", "Y"):
+        assert torch.isnan(B[name].float()).all(), name
+    ops.moe_clear_device_status()
+
+
 # --------------------------------------------------------------------- expert GEMMs
 
 def _expert_buffers(rows, d, f, E):
