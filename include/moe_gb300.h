@@ -194,6 +194,10 @@ int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, int64_t T, i
  *      output; a and u are not scaled. The down projection is linear, so this gives the
  *      combine's g * y without a second pass (moe_row_gates builds row_gate).
  * `rows` is the row capacity of X/A/U/H/Y; rows past it are never touched.
+ * A row_offsets array that breaks the padded layout (row_offsets[0] != 0, a decrease, a
+ * segment that is not a multiple of 128 rows, row_offsets[E] > rows) records
+ * MOE_ERR_BAD_INDEX (site 20) and the GEMMs write nothing; the same holds for
+ * moe_expert_bwd and moe_expert_fwd_fp8.
  */
 int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int E, int64_t rows, int d,
                    int f, const moe_bf16* W_g, const moe_bf16* W_u, const moe_bf16* W_d,
