@@ -137,6 +137,15 @@ def gpu_id_for(device_index: int) -> str:
         return vis.split(",")[device_index] if vis else str(device_index)
 
 
+def oracle_aux(cfg, T_s: int):
+    """Balancing-loss arguments of the oracle for a T_s-token sample: a sample shorter than
+    one sequence is taken as one sequence."""
+    if not cfg.has_aux:
+        return None
+    L = min(cfg.seq_len or T_s, T_s)
+    return (L if T_s % L == 0 else T_s, cfg.aux_switch, cfg.aux_seq)
+
+
 def oracle_pass_desc(cfg) -> str:
     """What one oracle step computes for this workload (as bench.py times it)."""
     parts = ["forward"]
@@ -144,7 +153,12 @@ def oracle_pass_desc(cfg) -> str:
         parts.append("backward")
     if cfg.bias_update:
         parts.append("bias update")
-    return "fp64 " + "+".join(parts)
+    desc = "fp64 " + "+".join(parts)
+    if cfg.precision == "fp8":
+        desc += ", FP8 (E4M3 rowwise) expert forward operands"
+    if cfg.has_aux:
+        desc += ", both balancing losses (the sample as one sequence when shorter than one)"
+    return desc
 
 
 def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
@@ -155,10 +169,12 @@ def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
     sub["x"] = inp["x"][:T_s]
     i64 = {k: O.to64(v) for k, v in sub.items() if k != "dY"}
     dY = O.to64(inp["dY"][:T_s]) if cfg.backward else None
+    aux = oracle_aux(cfg, T_s)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef)
+        fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, aux=aux,
+                              fp8=cfg.precision == "fp8")
         if cfg.backward:
             O.layer_backward(i64, fwd, dY)
         if cfg.bias_update:

@@ -1,9 +1,11 @@
-"""Host logic of the multi-GPU path (replicas, one process per GPU), on CPU with gloo.
+"""Host logic of the benchmark on CPU: the multi-GPU path (replicas, one process per GPU)
+with gloo, and the reference arm.
 
 The layer shards by tokens with no exchange inside the step; bench.py times each replica's
 steps, takes the slowest rank's time (all-reduce MAX) and reports all ranks' tokens over it.
 These tests run that aggregation on two gloo ranks and check the reference arm's rank
 handling; no GPU is needed."""
+import json
 import os
 import socket
 import subprocess
@@ -17,6 +19,8 @@ import torch.multiprocessing as mp
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 import bench  # noqa: E402
+from pretraining_sigmoid_softmax_gb300.configs import CONFIGS, MoEConfig  # noqa: E402
+from pretraining_sigmoid_softmax_gb300.inputs import make_inputs  # noqa: E402
 
 
 def _free_port() -> int:
@@ -61,3 +65,39 @@ def test_reference_arm_runs_on_rank_zero_only():
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_the_contract_line_on_rank_zero():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "C0", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["value"] > 0
+    assert line["config"] == bench.workload_desc(CONFIGS["C0"])
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert "forward" in cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("kw", [dict(precision="fp8", f_shared=64),
+                                dict(mode="softmax", z_coef=1e-3, aux_switch=1e-3, aux_seq=1e-3,
+                                     seq_len=4096, bias_update=False)])
+def test_cpu_baseline_times_the_workloads_own_layer(kw):
+    """The timed oracle runs the workload's own precision and losses (FP8 operands, the
+    balancing losses with a sample shorter than one sequence taken as one sequence)."""
+    base = dict(name="t", T=64, d=128, E=8, k=2, f=128, f_shared=0, mode="sigmoid", seed=1,
+                backward=True, bias_update=True)
+    cfg = MoEConfig(**{**base, **kw})
+    rate, cores, times = bench.cpu_oracle_rate(cfg, make_inputs(cfg), 32)
+    assert rate > 0 and cores >= 1 and len(times) == 1
+    desc = bench.oracle_pass_desc(cfg)
+    assert ("FP8" in desc) == (cfg.precision == "fp8")
+    assert ("balancing" in desc) == cfg.has_aux
