@@ -522,6 +522,37 @@ def test_rowwise_fp8_quantisation_invariants():
     assert np.all((rel <= 2.0 ** -4 + 1e-12) | (np.abs(X) < 2.0 ** -6 * sc[:, None]))
 
 
+def _e4m3_rows(rng, rows, cols):
+    """Rows exactly representable under rowwise E4M3 scaling: E4M3 values times a per-row
+    power of two, with one element at +-448 so that the row's scale is that power of two."""
+    mags = np.array([m * 2.0 ** e for e in range(-6, 9) for m in (1, 1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875)])
+    mags = mags[mags <= 448.0]
+    v = rng.choice(mags, size=(rows, cols)) * rng.choice([-1.0, 1.0], size=(rows, cols))
+    v[np.arange(rows), rng.integers(0, cols, rows)] = 448.0 * rng.choice([-1.0, 1.0], rows)
+    return v * 2.0 ** rng.integers(-14, -9, size=(rows, 1))
+
+
+def test_fp8_expert_reduces_to_the_exact_expert_on_representable_operands():
+    """When x and every weight row are exactly representable under rowwise scaling, the FP8
+    expert's a, u and h equal the exact expert's; only h's own quantisation before the down
+    projection moves y, by at most its rounding (2^-4 relative per element of h)."""
+    rng = np.random.default_rng(24)
+    d, f = 64, 48
+    x = _e4m3_rows(rng, 40, d)
+    Wg, Wu = _e4m3_rows(rng, f, d), _e4m3_rows(rng, f, d)
+    Wd = _e4m3_rows(rng, d, f)
+    q, sc = O.quantize_rows_fp8(x)
+    np.testing.assert_array_equal(q * sc[:, None], x)  # the construction is representable
+    a8, u8, h8, y8 = O.swiglu_expert_fp8(x, Wg, Wu, Wd)
+    a, u, h, y = O.swiglu_expert(x, Wg, Wu, Wd)
+    np.testing.assert_array_equal(a8, a)
+    np.testing.assert_array_equal(u8, u)
+    np.testing.assert_array_equal(h8, h)
+    assert not np.array_equal(y8, y)  # h itself is not representable: its codes move y
+    bound = (2.0 ** -4 * np.abs(h) + 2.0 ** -9 * np.abs(h).max(axis=1, keepdims=True) / 448) @ np.abs(Wd).T
+    assert np.all(np.abs(y8 - y) <= bound * (1 + 1e-12))
+
+
 def test_fp8_expert_stays_close_to_bf16_expert():
     """FP8 operands (3 mantissa bits, about 2% RMS rounding each) move an expert's output
     by several percent through the two GEMMs and the SwiGLU."""

@@ -242,6 +242,31 @@ def _quantize_rows_to_240(X):
     return O.e4m3_round((X32 / scale[:, None]).astype(np.float32)), scale.astype(np.float64)
 
 
+def _fp8_expert(rows, W_g, W_u, W_d, rnd=None, *, weights_by_column=False, x_by_column=False,
+                requantise_h=True):
+    """The FP8 expert restated with knobs that plant a mistake."""
+    deq = ORIG["fp8_dequant_rows"]
+    wq = (lambda W: deq(W.T).T) if weights_by_column else deq
+    xq = deq(rows.T).T if x_by_column else deq(rows)
+    a = xq @ wq(W_g).T
+    u = xq @ wq(W_u).T
+    h = O._r(rnd, ORIG["silu"](a) * u)
+    y = O._r(rnd, (deq(h) if requantise_h else h) @ wq(W_d).T)
+    return O._r(rnd, a), O._r(rnd, u), h, y
+
+
+def _fp8_weights_by_column(*a, **kw):
+    return _fp8_expert(*a, weights_by_column=True, **kw)
+
+
+def _fp8_x_by_column(*a, **kw):
+    return _fp8_expert(*a, x_by_column=True, **kw)
+
+
+def _fp8_h_not_requantised(*a, **kw):
+    return _fp8_expert(*a, requantise_h=False, **kw)
+
+
 def _near_tie_ignores_next_value(select_value, k, gap=1e-6):
     srt = -np.sort(-select_value, axis=1)[:, :k]
     if k < 2:
@@ -296,6 +321,9 @@ MUTANTS = {
     "E4M3 rounding truncates": ("e4m3_round", _e4m3_truncates),
     "bf16 rounding ties away from zero": ("bf16_round", _bf16_ties_away),
     "FP8 rows scaled to 240": ("quantize_rows_fp8", _quantize_rows_to_240),
+    "FP8 weights scaled per input column": ("swiglu_expert_fp8", _fp8_weights_by_column),
+    "FP8 activations scaled per feature": ("swiglu_expert_fp8", _fp8_x_by_column),
+    "FP8 h not re-quantised before the down projection": ("swiglu_expert_fp8", _fp8_h_not_requantised),
     "near-tie check ignores the (k+1)-th value": ("near_tie_tokens", _near_tie_ignores_next_value),
     "sampled forward ignores the gates": ("token_forward", _token_forward_ungated),
     "sampled backward omits the shared expert": ("token_backward", _token_backward_without_shared),
