@@ -116,6 +116,14 @@ def test_z_loss_closed_form_at_zero_logits():
     np.testing.assert_allclose(r["lse"], math.log(g["E"]), rtol=1e-15)
 
 
+def test_z_loss_is_the_mean_of_squares_not_the_square_of_the_mean():
+    """Worked by hand: logits (0, 0) give lse = ln 2 and (ln 3, 0) give lse = ln 4, so
+    mean(lse^2) = 2.5 ln^2 2, while the square of the mean would be 2.25 ln^2 2."""
+    r = O.route_softmax(np.array([[0.0, 0.0], [math.log(3.0), 0.0]]), 1, 1.0)
+    np.testing.assert_allclose(r["lse"], [math.log(2.0), math.log(4.0)], rtol=1e-15)
+    assert r["z_loss"] == pytest.approx(2.5 * math.log(2.0) ** 2, rel=1e-14)
+
+
 def test_softmax_gates_are_unrenormalised_probabilities():
     rng = np.random.default_rng(4)
     logits = rng.standard_normal((16, 6))
@@ -468,6 +476,20 @@ def test_aux_losses_balanced_closed_form():
         a = O.aux_losses(logits, idx, mode, 8, 1.0, 1.0)
         assert a["switch_unscaled"] == pytest.approx(1.0, abs=1e-15)
         assert a["seq_unscaled"] == pytest.approx(1.0, abs=1e-15)
+
+
+def test_sequence_loss_uses_each_sequences_own_counts():
+    """Worked by hand: two sequences of two tokens, E = 2, k = 1, softmax probabilities
+    (0.9, 0.1) on sequence 0, whose tokens both choose expert 0, and (0.1, 0.9) on sequence
+    1, whose tokens both choose expert 1. Per sequence f = (2, 0) resp. (0, 2) and P = the
+    sequence's probabilities, so sum_e f P = 1.8 on each: seq = 1.8. Batch-wide f = P =
+    (0.5, 0.5), so switch = 2 (0.25 + 0.25) = 1."""
+    l9 = math.log(9.0)
+    logits = np.array([[l9, 0.0], [l9, 0.0], [0.0, l9], [0.0, l9]])
+    idx = np.array([[0], [0], [1], [1]])
+    a = O.aux_losses(logits, idx, "softmax", 2, 1.0, 1.0)
+    assert a["seq_unscaled"] == pytest.approx(1.8, rel=1e-14)
+    assert a["switch_unscaled"] == pytest.approx(1.0, rel=1e-14)
 
 
 @pytest.mark.parametrize("mode", ["sigmoid", "softmax"])

@@ -121,6 +121,12 @@ def _route_softmax_z_of_mean_lse(logits, k, z_coef):
     return r
 
 
+def _z_loss_square_of_mean(logits, k, z_coef):
+    r = ORIG["route_softmax"](logits, k, z_coef)
+    r["z_loss"] = z_coef * float(np.mean(r["lse"])) ** 2
+    return r
+
+
 def _router_bwd(dg, rr, x, W_r, mode, z_coef, T_norm=None, dl_extra=None, *, couple=True,
                 zfac=2.0):
     """The router backward restated with two knobs that plant a mistake."""
@@ -215,6 +221,18 @@ def _aux_switch_without_E(logits, idx, mode, seq_len, switch_coef, seq_coef):
     return a
 
 
+def _aux_seq_from_batch_counts(logits, idx, mode, seq_len, switch_coef, seq_coef):
+    a = ORIG["aux_losses"](logits, idx, mode, seq_len, switch_coef, seq_coef)
+    T, E = logits.shape
+    B = T // seq_len
+    f_batch = E * a["f"]  # E c_e / (T k): the batch's counts in place of each sequence's
+    Ps = a["pi"].reshape(B, seq_len, E).mean(axis=1)
+    a["seq_unscaled"] = float(np.mean(np.sum(f_batch[None, :] * Ps, axis=1)))
+    a["seq"] = seq_coef * a["seq_unscaled"]
+    a["f_seq"] = np.broadcast_to(f_batch, (B, E)).copy()
+    return a
+
+
 def _aux_bwd_drops_sequence_term(logits, idx, mode, seq_len, switch_coef, seq_coef):
     return ORIG["aux_losses_backward"](logits, idx, mode, seq_len, switch_coef, 0.0)
 
@@ -305,6 +323,7 @@ MUTANTS = {
     "ties go to the higher index": ("_top_k_desc", _top_k_ties_to_higher_index),
     "softmax gates renormalised": ("route_softmax", _route_softmax_renormalised),
     "z-loss of mean lse instead of mean lse^2": ("route_softmax", _route_softmax_z_of_mean_lse),
+    "z-loss as the square of the mean lse": ("route_softmax", _z_loss_square_of_mean),
     "router backward drops the renormalisation term": ("router_backward", _router_bwd_without_renormalisation_term),
     "z-loss gradient missing its factor 2": ("router_backward", _router_bwd_z_gradient_missing_factor_two),
     "rows within an expert ordered by slot": ("dispatch", _dispatch_rows_by_slot),
@@ -318,6 +337,7 @@ MUTANTS = {
     "proportional update relative to the load": ("bias_update_proportional", _bias_update_proportional_over_load),
     "Switch loss without the factor E": ("aux_losses", _aux_switch_without_E),
     "balancing-loss gradient drops the sequence term": ("aux_losses_backward", _aux_bwd_drops_sequence_term),
+    "sequence loss from the batch-wide counts": ("aux_losses", _aux_seq_from_batch_counts),
     "E4M3 rounding truncates": ("e4m3_round", _e4m3_truncates),
     "bf16 rounding ties away from zero": ("bf16_round", _bf16_ties_away),
     "FP8 rows scaled to 240": ("quantize_rows_fp8", _quantize_rows_to_240),
