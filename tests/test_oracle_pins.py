@@ -374,6 +374,39 @@ def test_sampled_rows_equal_full_layer():
             np.testing.assert_allclose(ent["dWs_u"], [bwd["dWs_u"][0, 3]], rtol=1e-11)
 
 
+def test_fp8_sampled_rows_equal_full_layer():
+    """The per-token and per-entry evaluations used at large sizes agree with the whole
+    layer in FP8 mode too (quantised forward operands, bf16 backward on the stored a, u, h
+    and the unquantised x)."""
+    rng = np.random.default_rng(25)
+    inp = _tiny_inputs(rng, T=30, d=16, E=5, f=8, fs=4)
+    dY = rng.standard_normal((30, 16))
+    fwd = O.layer_forward(inp, "sigmoid", 2, fp8=True)
+    bwd = O.layer_backward(inp, fwd, dY)
+    plain = O.layer_forward(inp, "sigmoid", 2)
+    assert not np.allclose(fwd["out"], plain["out"], rtol=1e-3)  # FP8 really changes the layer
+    for t in (0, 11, 29):
+        o = O.token_forward(inp, t, fwd["idx"][t], fwd["gate"][t], fp8=True)
+        np.testing.assert_allclose(o, fwd["out"][t], rtol=1e-12, atol=1e-12)
+        tb = O.token_backward(inp, t, fwd["logits"][t], fwd["idx"][t], "sigmoid", 2, dY[t], 0.0,
+                              30, fp8=True)
+        np.testing.assert_allclose(tb["dx"], bwd["dx"][t], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(tb["dg"], bwd["dg"][t], rtol=1e-11, atol=1e-12)
+    for e in range(5):
+        rows = np.arange(fwd["offsets"][e], fwd["offsets"][e + 1])
+        toks = fwd["perm_token"][rows]
+        gates = fwd["gate"][toks, fwd["perm_slot"][rows]]
+        ent = O.expert_weight_grad_entries(inp, e, toks, gates, dY, [(0, 1), (9, 7)],
+                                           [(2, 5), (7, 0)], fp8=True)
+        np.testing.assert_allclose(ent["dW_d"], [bwd["dW_d"][e][0, 1], bwd["dW_d"][e][9, 7]], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(ent["dW_g"], [bwd["dW_g"][e][2, 5], bwd["dW_g"][e][7, 0]], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(ent["dW_u"], [bwd["dW_u"][e][2, 5], bwd["dW_u"][e][7, 0]], rtol=1e-11, atol=1e-13)
+    ent = O.shared_weight_grad_entries(inp, dY, [(3, 2)], [(1, 6)], fp8=True)
+    np.testing.assert_allclose(ent["dWs_d"], [bwd["dWs_d"][3, 2]], rtol=1e-11)
+    np.testing.assert_allclose(ent["dWs_g"], [bwd["dWs_g"][1, 6]], rtol=1e-11)
+    np.testing.assert_allclose(ent["dWs_u"], [bwd["dWs_u"][1, 6]], rtol=1e-11)
+
+
 # ----------------------------------------------------------------- bf16 storage precision
 
 def test_bf16_round_matches_library_conversion_including_ties():

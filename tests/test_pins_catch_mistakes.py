@@ -285,6 +285,10 @@ def _fp8_h_not_requantised(*a, **kw):
     return _fp8_expert(*a, requantise_h=False, **kw)
 
 
+def _gemm_operands_unquantised(X, Wg, Wu, fp8):
+    return X, Wg, Wu
+
+
 def _near_tie_ignores_next_value(select_value, k, gap=1e-6):
     srt = -np.sort(-select_value, axis=1)[:, :k]
     if k < 2:
@@ -348,6 +352,7 @@ MUTANTS = {
     "sampled forward ignores the gates": ("token_forward", _token_forward_ungated),
     "sampled backward omits the shared expert": ("token_backward", _token_backward_without_shared),
     "sampled weight gradients ignore the gates": ("expert_weight_grad_entries", _weight_grad_entries_ungated),
+    "sampled FP8 weight gradients from unquantised operands": ("_gemm_operands", _gemm_operands_unquantised),
     "replayed sigmoid gates not renormalised": ("_regate", _regate_unrenormalised),
 }
 
