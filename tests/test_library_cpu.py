@@ -75,3 +75,37 @@ def test_argument_checks_return_before_any_device_work(lib):
     assert lib.moe_check_bounded_wait(2_000_000_000, None) == 1  # so is one above a second
     code = ctypes.c_int(0)
     assert lib.moe_device_status(None, None, None) == 1
+
+
+@needs_nvcc
+def test_padded_capacity_holds_every_routing(lib):
+    """moe_padded_rows bounds the padded layout (each expert's segment rounded up to 128
+    rows) for any split of the T*k routed rows over E experts, including the worst split,
+    where E - 1 experts hold one row each and waste 127 padding rows apiece."""
+    import numpy as np
+    rng = np.random.default_rng(0)
+
+    def padded(counts):
+        return int(sum(-(-int(c) // 128) * 128 for c in counts))
+
+    for T, k, E in [(1, 1, 1), (7, 2, 4), (300, 3, 6), (4096, 8, 64), (65536, 8, 64), (1000, 32, 256)]:
+        cap = lib.moe_padded_rows(T, k, E)
+        assert cap % 128 == 0 and cap >= T * k
+        for _ in range(50):
+            assert padded(rng.multinomial(T * k, rng.dirichlet(np.ones(E) * 0.3))) <= cap
+        if T * k >= E:
+            worst = np.ones(E, dtype=np.int64)
+            worst[0] = T * k - (E - 1)
+            assert padded(worst) <= cap
+
+
+@needs_nvcc
+def test_workspace_grows_with_every_size(lib):
+    lib.moe_workspace_bytes.restype = ctypes.c_size_t
+    base = (4096, 1024, 32, 4)
+    w0 = lib.moe_workspace_bytes(*base)
+    assert w0 > 0
+    for i, bigger in enumerate([8192, 2048, 64, 8]):
+        args = list(base)
+        args[i] = bigger
+        assert lib.moe_workspace_bytes(*args) >= w0, args
