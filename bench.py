@@ -197,6 +197,20 @@ def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
     return T_s / statistics.median(times), cores, times
 
 
+def cpu_oracle_rate_one_core(config_name: str, T_s: int, steps: int = 1) -> float:
+    """The same oracle timing on one host core: a child process whose numerical libraries
+    are held to one thread. Returns tokens/s."""
+    code = ("import json, sys, torch; torch.set_num_threads(1); sys.path.insert(0, %r); "
+            "import bench; from pretraining_sigmoid_softmax_gb300.configs import CONFIGS; "
+            "from pretraining_sigmoid_softmax_gb300.inputs import make_inputs; "
+            "cfg = CONFIGS[%r]; r = bench.cpu_oracle_rate(cfg, make_inputs(cfg), %d, %d); "
+            "print(json.dumps(r[0]))" % (ROOT, config_name, T_s, steps))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=600, check=True)
+    return float(r.stdout.strip().splitlines()[-1])
+
+
 def run_reference(args, cfg):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -439,6 +453,8 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"first {T_s} tokens of the workload, all {cfg.E} "
                                           f"experts, {oracle_pass_desc(cfg)}"}
+        if args.config == "C0":  # the tiny workload is also timed on one core
+            line["cpu_baseline"]["one_core"] = cpu_oracle_rate_one_core("C0", T_s, steps=3)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

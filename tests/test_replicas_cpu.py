@@ -101,3 +101,15 @@ def test_cpu_baseline_times_the_workloads_own_layer(kw):
     desc = bench.oracle_pass_desc(cfg)
     assert ("FP8" in desc) == (cfg.precision == "fp8")
     assert ("balancing" in desc) == cfg.has_aux
+
+
+def test_one_core_oracle_timing_runs_in_a_single_threaded_child():
+    rate = bench.cpu_oracle_rate_one_core("C0", 32)
+    assert rate > 0
+
+
+def test_small_workloads_flush_l2_and_say_so():
+    for name, cfg in CONFIGS.items():
+        small = cfg.T * cfg.d * 2 < 128 * 2**20
+        assert bench.needs_l2_flush(cfg) == small, name
+        assert bench.workload_desc(cfg)["l2"].startswith("L2 flushed" if small else "inputs larger")
