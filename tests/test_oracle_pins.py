@@ -87,6 +87,12 @@ def test_sigmoid_selection_random_against_enumeration():
     v = 1.0 / (1.0 + np.exp(-logits)) + b
     for t in range(64):
         assert tuple(r["idx"][t]) == O.select_brute_force(v[t], k)
+    # invariants: k distinct experts, gates sum to 1 and are proportional to the chosen
+    # experts' own sigmoid scores (not to the biased selection values)
+    assert all(len(set(row)) == k for row in r["idx"].tolist())
+    np.testing.assert_allclose(r["gate"].sum(axis=1), 1.0, rtol=1e-15)
+    s = np.take_along_axis(1.0 / (1.0 + np.exp(-logits)), r["idx"], axis=1)
+    np.testing.assert_allclose(r["gate"] * s.sum(axis=1, keepdims=True), s, rtol=1e-14)
 
 
 def test_bias_steers_selection_but_not_gates():
