@@ -48,7 +48,7 @@ class MoEPlan:
     """Device buffers of one layer shape and the forward / backward call sequences."""
 
     # Shared-expert GEMM work per step (FLOPs, forward + backward) below which the shared
-    # expert runs on a side stream. Measured on GB300: the softmax-free small layer (T 8192,
+    # expert runs on a side stream. Measured on GB300: the small fine-grained layer (T 8192,
     # d 1024, shared 512: 0.08 TFLOP) 0.835 -> 0.746 ms per step with the overlap; the large
     # layer (T 65536, d 4096, shared 3072: 14.8 TFLOP) 51.3 -> 52.7 ms, as it runs at the
     # power cap, where concurrent kernels add interference and no energy budget.
