@@ -109,3 +109,32 @@ def test_workspace_grows_with_every_size(lib):
         args = list(base)
         args[i] = bigger
         assert lib.moe_workspace_bytes(*args) >= w0, args
+
+
+@needs_nvcc
+def test_degenerate_and_inconsistent_arguments_are_rejected_on_the_host(lib):
+    """Empty sizes, an unknown router mode, a router mode without its outputs, misaligned
+    pointers and a half-given gate-folding pair return MOE_ERR_INVALID_ARG (1) before any
+    device work (these checks come before the device check, so they hold without a GPU)."""
+    P = 4096  # a stand-in device address (never dereferenced on the host), 16-byte aligned
+    bad = P + 2  # not 16-byte aligned
+    ws = P
+    route = lambda x, b, T, mode, logits, lse, z: lib.moe_route(
+        x, P, b, T, 256, 8, 2, mode, 0.0, logits, P, P, P, lse, z, ws, 1 << 20, None)
+    assert route(P, P, 0, 0, P, P, P) == 1          # T = 0
+    assert route(P, P, 16, 7, P, P, P) == 1         # unknown mode
+    assert route(P, None, 16, 0, P, P, P) == 1      # sigmoid mode needs the bias
+    assert route(P, None, 16, 1, None, P, P) == 1   # softmax mode needs logits, lse, z-loss
+    assert route(bad, P, 16, 0, P, P, P) == 1       # misaligned x
+    assert lib.moe_permute(P, P, 0, 256, 8, 2, P, P, P, P, P, P, ws, 1 << 20, None) == 1
+    assert lib.moe_permute(P, bad, 16, 256, 8, 2, P, P, P, P, P, P, ws, 1 << 20, None) == 1
+    assert lib.moe_combine(P, P, P, None, 0, 256, 2, P, None) == 1
+    assert lib.moe_combine(bad, P, P, None, 16, 256, 2, P, None) == 1
+    fwd = lambda rows, E, ro, X: lib.moe_expert_fwd(X, ro, E, rows, 256, 128, P, P, P, P, P, P,
+                                                     P, None, ws, 1 << 20, None)
+    assert fwd(0, 1, None, P) == 1                  # no rows
+    assert fwd(16, 2, None, P) == 1                 # no layout for two experts
+    assert fwd(16, 1, None, bad) == 1               # misaligned operand
+    bwd = lambda rg, gp: lib.moe_expert_bwd(P, P, P, P, P, None, 1, 16, 256, 128, P, P, P, P, P, P,
+                                            P, P, P, rg, gp, ws, 1 << 20, None)
+    assert bwd(P, None) == 1 and bwd(None, P) == 1  # row gates and gate partials come together
