@@ -197,6 +197,31 @@ def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
     return T_s / statistics.median(times), cores, times
 
 
+def cpu_desc_from(cpuinfo: str, machine: str) -> str:
+    """The CPU model as a /proc/cpuinfo text names it (x86: model name; Arm: implementer and
+    part numbers), with the machine type."""
+    fields = {}
+    for line in cpuinfo.splitlines():
+        key, _, val = line.partition(":")
+        fields.setdefault(key.strip(), val.strip())
+    if fields.get("model name"):
+        return f"{fields['model name']} ({machine})"
+    if fields.get("CPU part"):
+        return f"{machine}, CPU implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return machine
+
+
+def host_cpu_desc() -> str:
+    """This host's CPU model; the machine type alone when /proc/cpuinfo cannot be read."""
+    import platform
+    machine = platform.machine() or "unknown"
+    try:
+        with open("/proc/cpuinfo") as fh:
+            return cpu_desc_from(fh.read(), machine)
+    except OSError:
+        return machine
+
+
 def cpu_oracle_rate_one_core(config_name: str, T_s: int, steps: int = 1) -> float:
     """The same oracle timing on one host core: a child process whose numerical libraries
     are held to one thread. Returns tokens/s."""
@@ -227,6 +252,7 @@ def run_reference(args, cfg):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_desc(cfg),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "cpu": host_cpu_desc(),
                              "sample": f"first {T_s} tokens of the workload per step, all "
                                        f"{cfg.E} experts, {oracle_pass_desc(cfg)}"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -450,7 +476,7 @@ def main():
         T_s = min(args.cpu_sample_tokens, cfg.T)
         rate, cores, _ = cpu_oracle_rate(cfg, inp, T_s)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu": host_cpu_desc(),
                                 "sample": f"first {T_s} tokens of the workload, all {cfg.E} "
                                           f"experts, {oracle_pass_desc(cfg)}"}
         if args.config == "C0":  # the tiny workload is also timed on one core

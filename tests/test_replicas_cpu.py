@@ -113,3 +113,12 @@ def test_small_workloads_flush_l2_and_say_so():
         small = cfg.T * cfg.d * 2 < 128 * 2**20
         assert bench.needs_l2_flush(cfg) == small, name
         assert bench.workload_desc(cfg)["l2"].startswith("L2 flushed" if small else "inputs larger")
+
+
+def test_host_cpu_description_reads_x86_and_arm_cpuinfo():
+    assert isinstance(bench.host_cpu_desc(), str) and bench.host_cpu_desc()
+    x86 = "processor\t: 0\nmodel name\t: Example CPU @ 2.0GHz\nflags\t: sse\n"
+    assert bench.cpu_desc_from(x86, "x86_64") == "Example CPU @ 2.0GHz (x86_64)"
+    arm = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n"
+    assert bench.cpu_desc_from(arm, "aarch64") == "aarch64, CPU implementer 0x41 part 0xd4f"
+    assert bench.cpu_desc_from("", "aarch64") == "aarch64"
