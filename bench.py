@@ -25,9 +25,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 peak"
-# DRAM bytes (read + write) of one step's grouped-GEMM launches from an ncu capture of the
-# current kernels (profiles/grouped_gemm_dram_C4_large.md); workloads without a capture
-# report null.
+# DRAM bytes (read + write) of one step's grouped-GEMM launches, summed from a stored ncu
+# capture of the current kernels at that workload (not measured by this run; the line says
+# so); workloads without a capture report null.
 MEASURED_GEMM_TRAFFIC = {"C4": 105.13e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -468,7 +468,11 @@ def main():
                          "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
                          "frac": gemm_tflops / peak_t, "peak_kind": peak_kind,
                          "traffic": MEASURED_GEMM_TRAFFIC.get(args.config),
-                         "traffic_unit": "bytes per step (all grouped-GEMM launches)"},
+                         "traffic_unit": "bytes per step (all grouped-GEMM launches)",
+                         "traffic_source": ("stored ncu capture (dram__bytes_read.sum + "
+                                            "dram__bytes_write.sum) of these kernels at this "
+                                            "workload, not measured in this run"
+                                            if args.config in MEASURED_GEMM_TRAFFIC else None)},
             "gpu_launches": plan.launches_per_step(cfg.backward, cfg.bias_update) * args.steps,
             "gpu_launches_note": "kernels per timed pass (the graph pass replays the same kernels)",
             "clocks": clocks, "e2e": e2e}

@@ -465,9 +465,17 @@ def router_backward(dg: np.ndarray, route_res: dict, x: np.ndarray, W_r: np.ndar
     return {"dlogits": dl, "dW_r": dl.T @ x, "dx_r": dl @ W_r}
 
 
-def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
+def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = None,
+                   dl_extra: np.ndarray | None = None, weight_grads: bool = True) -> dict:
     """Gradients of ``loss`` with respect to x, every weight and the router (stored in the
-    precision the forward used)."""
+    precision the forward used).
+
+    For a forward over a subset of a batch's tokens (each token's output and input gradient
+    depend only on its own routing, rows and upstream gradient): ``T_norm`` is the batch's
+    token count that the z-loss mean divides by, ``dl_extra`` the batch's balancing-loss
+    logit gradient rows of these tokens (it replaces the subset's own, whose counts would
+    be the subset's), and ``weight_grads=False`` skips the weight gradients, which only the
+    whole batch gives."""
     rnd = fwd.get("rnd")
     idx, gate, s2r = fwd["idx"], fwd["gate"], fwd["slot_to_row"]
     T, k = idx.shape
@@ -484,7 +492,9 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
     N, d = fwd["X_perm"].shape
     f = inp["W_g"].shape[1]
     dX_perm = np.zeros((N, d))
-    dW_g = np.zeros_like(inp["W_g"]); dW_u = np.zeros_like(inp["W_u"]); dW_d = np.zeros_like(inp["W_d"])
+    if weight_grads:
+        dW_g = np.zeros(inp["W_g"].shape); dW_u = np.zeros(inp["W_u"].shape)
+        dW_d = np.zeros(inp["W_d"].shape)
     dA = np.zeros((N, f)); dU = np.zeros((N, f))
     for e in range(E):
         lo, hi = int(offs[e]), int(offs[e + 1])
@@ -497,20 +507,23 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray) -> dict:
         if row_gate is not None:
             dg[tok[lo:hi], slot[lo:hi]] = g["dg_row"]
         dX_perm[lo:hi], dA[lo:hi], dU[lo:hi] = g["dX"], g["dA"], g["dU"]
-        dW_g[e], dW_u[e], dW_d[e] = g["dW_g"], g["dW_u"], g["dW_d"]
-    res = {"dY_perm": dY_perm, "dg": dg, "dA": dA, "dU": dU, "dX_perm": dX_perm,
-           "dW_g": dW_g, "dW_u": dW_u, "dW_d": dW_d}
+        if weight_grads:
+            dW_g[e], dW_u[e], dW_d[e] = g["dW_g"], g["dW_u"], g["dW_d"]
+    res = {"dY_perm": dY_perm, "dg": dg, "dA": dA, "dU": dU, "dX_perm": dX_perm}
+    if weight_grads:
+        res.update(dW_g=dW_g, dW_u=dW_u, dW_d=dW_d)
     if "shared" in fwd:
         sh = fwd["shared"]
         g = expert_backward(dY, inp["x"], sh["A"], sh["U"], sh["H"], inp["Ws_g"], inp["Ws_u"],
                             inp["Ws_d"], rnd)
-        res["dWs_d"], res["dWs_g"], res["dWs_u"] = g["dW_d"], g["dW_g"], g["dW_u"]
+        if weight_grads:
+            res["dWs_d"], res["dWs_g"], res["dWs_u"] = g["dW_d"], g["dW_g"], g["dW_u"]
         res["dx_shared"] = g["dX"]
-    dl_aux = None
-    if fwd.get("aux") is not None:
+    dl_aux = dl_extra
+    if dl_aux is None and fwd.get("aux") is not None:
         dl_aux = aux_losses_backward(fwd["logits"], idx, fwd["mode"], *fwd["aux"])
     rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"],
-                         dl_extra=dl_aux)
+                         T_norm=T_norm, dl_extra=dl_aux)
     res.update(rb)
     res["dx"] = input_gradient(dX_perm, s2r, res.get("dx_shared"), rb["dx_r"], rnd)
     return res
@@ -749,3 +762,42 @@ def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu,
         res["dWs_g"].append(float(_r(rnd, np.sum(_r(rnd, da) * X[:, i]))))
         res["dWs_u"].append(float(_r(rnd, np.sum(_r(rnd, du) * X[:, i]))))
     return res
+
+
+def expert_weight_grads(inp: dict, e: int, X: np.ndarray, gates: np.ndarray, dY_rows: np.ndarray,
+                        rnd=None, fp8: bool = False, fold_gate: bool = False) -> dict:
+    """The whole weight gradients dW_g[e], dW_u[e], dW_d[e] of one expert.
+
+    ``X`` holds the rows of the tokens routed to expert e in ascending token order, ``gates``
+    their gates for e and ``dY_rows`` their upstream gradients. Only these rows enter expert
+    e's weight gradients, so this is the whole layer's dW[e]: the combine's backward gives
+    each row g * dY (``fold_gate``: the row keeps dY and the gate sits inside the expert),
+    then the expert's own backward."""
+    expert = swiglu_expert_fp8 if fp8 else swiglu_expert
+    Wg, Wu, Wd = inp["W_g"][e], inp["W_u"][e], inp["W_d"][e]
+    if fold_gate:
+        a, u, h, _ = swiglu_expert(X, Wg, Wu, Wd, rnd, row_gate=gates)
+        g = expert_backward(dY_rows, X, a, u, h, Wg, Wu, Wd, rnd, row_gate=gates)
+    else:
+        a, u, h, _ = expert(X, Wg, Wu, Wd, rnd)
+        dy = _r(rnd, gates[:, None] * dY_rows)
+        g = expert_backward(dy, X, a, u, h, Wg, Wu, Wd, rnd)
+    return {"dW_g": g["dW_g"], "dW_u": g["dW_u"], "dW_d": g["dW_d"]}
+
+
+def shared_weight_grad_units(inp: dict, dY: np.ndarray, units, rnd=None,
+                             fp8: bool = False) -> dict:
+    """Whole weight rows of chosen hidden units j of the shared expert (every token, weight
+    1): dWs_g[j, :], dWs_u[j, :] (the units' input weights) and dWs_d[:, j] (their output
+    weights). The units' a, u and h over all tokens need only their own weight rows:
+    a = x W_g[units]^T, dh = dY W_d[:, units], then the SwiGLU derivative and the sums over
+    tokens."""
+    X = inp["x"]
+    units = np.asarray(list(units), dtype=np.int64)
+    Xo, Wgo, Wuo = _gemm_operands(X, inp["Ws_g"], inp["Ws_u"], fp8)
+    av, uv = Xo @ Wgo[units].T, Xo @ Wuo[units].T
+    a, u = _r(rnd, av), _r(rnd, uv)
+    h = _r(rnd, silu(av) * uv)  # from the unrounded a and u, as the forward stores it
+    da, du = swiglu_backward(dY @ inp["Ws_d"][:, units], a, u)
+    return {"dWs_g": _r(rnd, _r(rnd, da).T @ X), "dWs_u": _r(rnd, _r(rnd, du).T @ X),
+            "dWs_d": _r(rnd, dY.T @ h)}

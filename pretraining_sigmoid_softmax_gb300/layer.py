@@ -348,16 +348,28 @@ class MoEPlan:
 
 
 class _MoEFunction(torch.autograd.Function):
+    """One layer step as an autograd node over a plan's fixed buffers.
+
+    The plan keeps the forward's activations for the backward, so a later forward through
+    the same plan (the same token count) overwrites them: ``plan.generation`` counts the
+    forwards and the backward refuses a stale one."""
+
     @staticmethod
     def forward(ctx, x, W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d, plan):
         ctx.plan = plan
+        plan.generation += 1
+        ctx.generation = plan.generation
         out = plan.forward(x.contiguous(), W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d)
         return out.clone()
 
     @staticmethod
     def backward(ctx, dY):
         plan = ctx.plan
-        plan.backward(dY.contiguous())
+        if plan.generation != ctx.generation:
+            raise RuntimeError(
+                "MoELayer: another forward with the same token count ran after this one and "
+                "overwrote its saved activations; run each backward before the next forward")
+        plan.backward(dY.to(torch.bfloat16).contiguous())
         g = plan.grads()
         shared = plan.s.f_shared > 0
         return (g["dx"].clone(), g["dW_r"].clone(), None, g["dW_g"].clone(), g["dW_u"].clone(),
@@ -369,15 +381,29 @@ class _MoEFunction(torch.autograd.Function):
 class MoELayer(torch.nn.Module):
     """Fine-grained MoE layer module (bf16 experts, fp32 router and bias) on one GPU.
 
-    ``forward(x)`` with x [T, d] bf16; gradients flow to x and every weight; the bias is a
-    buffer updated by ``update_bias()`` after backward (it gets no gradient)."""
+    ``forward(x)`` takes x [T, d] bf16 and returns out [T, d] bf16; gradients flow to x and
+    every weight. The router's own losses (the z-loss in softmax mode, the balancing losses
+    when their coefficients are set) enter the training loss with weight 1: their gradient
+    is added in the layer's backward, and their values are read with ``z_loss()`` and
+    ``aux_loss()`` for logging. The bias is a buffer: it gets no gradient and moves only by
+    ``update_bias()``, called after backward with that step's expert counts.
+
+    One plan (set of device buffers) is kept per token count; each backward must run before
+    the next forward with the same token count."""
 
     def __init__(self, d, E, k, f, f_shared=0, mode="sigmoid", z_coef=0.0, gamma=1e-3,
-                 device="cuda"):
+                 device="cuda", bias_rule="sign", aux_switch=0.0, aux_seq=0.0, seq_len=0,
+                 precision="bf16"):
         super().__init__()
+        if mode not in ("sigmoid", "softmax") or bias_rule not in ("sign", "proportional") \
+                or precision not in ("bf16", "fp8"):
+            raise ValueError("mode is sigmoid or softmax, bias_rule sign or proportional, "
+                             "precision bf16 or fp8")
         self.d, self.E, self.k, self.f, self.f_shared = d, E, k, f, f_shared
         self.mode = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
-        self.z_coef, self.gamma = z_coef, gamma
+        self.z_coef, self.gamma, self.bias_rule = z_coef, gamma, bias_rule
+        self.aux_switch, self.aux_seq, self.seq_len = aux_switch, aux_seq, seq_len
+        self.fp8 = precision == "fp8"
         bf = dict(dtype=torch.bfloat16, device=device)
         self.W_r = torch.nn.Parameter(torch.randn(E, d, device=device) * d ** -0.5)
         self.register_buffer("b", torch.zeros(E, device=device))
@@ -395,11 +421,17 @@ class MoELayer(torch.nn.Module):
 
     def _plan(self, T):
         if T not in self._plans:
-            self._plans[T] = MoEPlan(MoEShape(T, self.d, self.E, self.k, self.f, self.f_shared,
-                                              self.mode, self.z_coef), self.W_g.device)
+            shape = MoEShape(T, self.d, self.E, self.k, self.f, self.f_shared, self.mode,
+                             self.z_coef, self.aux_switch, self.aux_seq, self.seq_len or T,
+                             self.fp8)
+            plan = MoEPlan(shape, self.W_g.device)
+            plan.generation = 0
+            self._plans[T] = plan
         return self._plans[T]
 
     def forward(self, x):
+        if x.dim() != 2 or x.shape[1] != self.d or x.dtype != torch.bfloat16:
+            raise ValueError(f"x must be [T, {self.d}] bf16, got {tuple(x.shape)} {x.dtype}")
         plan = self._plan(x.shape[0])
         self._last_plan = plan
         return _MoEFunction.apply(x, self.W_r, self.b, self.W_g, self.W_u, self.W_d, self.Ws_g,
@@ -408,7 +440,13 @@ class MoELayer(torch.nn.Module):
     @torch.no_grad()
     def update_bias(self):
         if self.mode == ops.MODE_SIGMOID and self._last_plan is not None:
-            self._last_plan.bias_update(self.b, self.gamma)
+            self._last_plan.bias_update(self.b, self.gamma, self.bias_rule)
 
     def z_loss(self):
+        """The last forward's router z-loss ([1] fp32 device tensor; softmax mode)."""
         return None if self._last_plan is None else self._last_plan.z_loss
+
+    def aux_loss(self):
+        """The last forward's balancing losses ([2] fp32: Switch-style, sequence-wise)."""
+        p = self._last_plan
+        return None if p is None or not p.s.has_aux else p.aux_loss

@@ -29,6 +29,9 @@ def h64(t):
 def assert_close(gpu, ref, name, atol=ATOL, rtol=RTOL, reduction=False):
     """|gpu - oracle| <= atol + rtol |oracle| elementwise.
 
+    Against the oracle's bf16-storage model this is the consistency check of the kernels'
+    arithmetic; parity with the plain definition is ``check_plain``.
+
     ``reduction=True`` marks sums over the token axis (weight and gate gradients): there one
     operand element that the fp32 GPU evaluation rounds to the neighbouring bf16 value
     (unavoidable: about 1 in 2000 elements of a bf16 activation) moves every sum it enters
@@ -46,6 +49,56 @@ def assert_close(gpu, ref, name, atol=ATOL, rtol=RTOL, reduction=False):
         raise AssertionError(
             f"{name}: {int(bad.sum())} of {bad.size} elements outside {atol} + {rtol}|ref|; "
             f"worst at {i}: gpu {g[i]!r} oracle {r[i]!r}; max abs err {err.max():.3e}")
+
+
+# Literal-tolerance report against the plain definition: per case and tensor, how many
+# elements fall outside |gpu - oracle| <= ATOL + RTOL |oracle| and by how much, beside the
+# same figures for the oracle's own bf16-storage model. Printed at the end of the session
+# (tests/conftest.py) and written as JSON to $MOE_PARITY_REPORT when that is set.
+REPORT = {"plain": [], "near_ties": []}
+
+
+def exceedances(got, want) -> dict:
+    """Elements outside the literal tolerance: count, worst excess over the bound and the
+    largest absolute error."""
+    g = h64(got) if not isinstance(got, np.ndarray) else got.astype(np.float64)
+    w = np.asarray(want, dtype=np.float64)
+    assert g.shape == w.shape, f"shape {g.shape} vs {w.shape}"
+    if w.size == 0:
+        return {"size": 0, "exceed": 0, "worst_excess": 0.0, "max_err": 0.0}
+    err = np.abs(g - w)
+    over = err - (ATOL + RTOL * np.abs(w))
+    return {"size": int(w.size), "exceed": int((over > 0).sum()),
+            "worst_excess": float(over.max()), "max_err": float(err.max())}
+
+
+def check_plain(case, name, gpu, plain, storage):
+    """Parity with the plain definition at the literal tolerance.
+
+    ``plain`` is the oracle's exact fp64 value and ``storage`` the oracle's value when the
+    tensors the workloads store in bf16 are rounded to bf16 (``rnd=bf16_round``). Elements
+    outside the tolerance are recorded, not hidden. Storing activations in bf16 alone moves
+    sums over thousands of tokens past the tolerance's absolute term, so the check is that the
+    GPU goes outside it no more often, and by no more, than bf16 storage itself does: its
+    count at most 1.5x the storage model's plus a few elements of chance (a sum within an
+    ulp of the bound falls either way), and its worst excess at most 1.5x the storage
+    model's plus a quarter of the absolute term."""
+    g = exceedances(gpu, plain)
+    s = exceedances(storage, plain)
+    REPORT["plain"].append({"case": case, "tensor": name, **g, "storage_exceed": s["exceed"],
+                            "storage_worst_excess": s["worst_excess"]})
+    allow = 1.5 * s["exceed"] + 3.0 * np.sqrt(s["exceed"]) + 1e-5 * g["size"] + 2
+    assert g["exceed"] <= allow, (
+        f"{case} {name}: {g['exceed']} of {g['size']} elements outside the literal tolerance "
+        f"(bf16 storage alone: {s['exceed']}); worst excess {g['worst_excess']:.3e}")
+    assert g["worst_excess"] <= 1.5 * max(s["worst_excess"], 0.0) + 0.25 * ATOL, (
+        f"{case} {name}: worst excess {g['worst_excess']:.3e} over the literal tolerance "
+        f"(bf16 storage alone: {s['worst_excess']:.3e})")
+    return g
+
+
+def record_near_ties(case, near, T):
+    REPORT["near_ties"].append({"case": case, "near_ties": int(near), "tokens": int(T)})
 
 
 def ulp_bf16(v):

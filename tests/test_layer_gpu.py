@@ -1,5 +1,13 @@
 """Whole-layer parity (forward, backward, bias update) of the CUDA path against the fp64
-oracle on the five workloads and on small ragged shapes, through the C ABI."""
+oracle on the workloads and on small ragged shapes, through the C ABI.
+
+Every value check has two parts. Parity proper compares the GPU with the plain definition
+(the oracle's exact fp64 layer, nothing rounded, its own fp64 router logits and the GPU's
+choice of experts) at the literal tolerance |gpu - oracle| <= 1e-2 + 1e-2 |oracle|, and
+reports the elements outside it per tensor (``check_plain``). A second check holds the
+kernels' arithmetic to the oracle's bf16-storage model (the tensors the workloads store in
+bf16 rounded where they are stored), which is tighter on everything but the sums over tokens.
+"""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +18,8 @@ from pretraining_sigmoid_softmax_gb300.configs import CONFIGS, MoEConfig
 from pretraining_sigmoid_softmax_gb300.inputs import make_inputs, make_upstream_gate_grad
 from pretraining_sigmoid_softmax_gb300.layer import MoEPlan, MoEShape
 
-from gpu_common import assert_close, gpu_rows, h64, padded_offsets, require_gpu
+from gpu_common import (assert_close, check_plain, gpu_rows, h64, padded_offsets,
+                        record_near_ties, require_gpu)
 
 pytestmark = pytest.mark.gpu
 RND = O.bf16_round
@@ -19,21 +28,6 @@ RND = O.bf16_round
 @pytest.fixture(autouse=True, scope="module")
 def _gpu():
     require_gpu()
-
-
-class Lazy:
-    """fp64 view of a host tensor converted slice by slice (whole-weight fp64 copies of the
-    large workloads would need tens of GB)."""
-
-    def __init__(self, t):
-        self.t = t
-        self.shape = tuple(t.shape)
-
-    def __getitem__(self, key):
-        return O.to64(self.t[key])
-
-
-WEIGHTS = ("W_g", "W_u", "W_d")  # converted to fp64 slice by slice
 
 
 def oracle_bias(cfg):
@@ -80,33 +74,58 @@ def check_routing(cfg, inp, plan):
     return idx, lg, D, rows, int(near.sum())
 
 
+def _aux(cfg):
+    return (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
+
+
+def _replayed_gates(cfg, lg, idx, b):
+    """Gates of the GPU's choice from the given logits."""
+    r = O.route(lg, cfg.mode, cfg.k, b, cfg.z_coef)
+    return O._regate(r, lg, idx, cfg.mode, b, cfg.z_coef)
+
+
 def full_parity(cfg, inp):
     plan, b_new = run_gpu(cfg, inp)
-    idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
+    idx, lg, D, rows, near = check_routing(cfg, inp, plan)
+    record_near_ties(cfg.name, near, cfg.T)
     i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
-    aux = (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
-    # the bf16 layer folds each slot's gate into its expert (stored h and y carry the gate)
+    aux = _aux(cfg)
     fp8 = cfg.precision == "fp8"
-    fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, logits=lg, idx=idx, rnd=RND, aux=aux,
-                          fp8=fp8, fold_gate=not fp8)
-    assert_close(plan.topk_gate, fwd["gate"], "gates", atol=1e-6, rtol=1e-5)
+    # gates of the GPU's fp32 logits: fp32-tight
+    assert_close(plan.topk_gate, _replayed_gates(cfg, lg, idx, i64["b"])["gate"], "gates",
+                 atol=1e-6, rtol=1e-5)
+    # the plain definition and the bf16-storage model (the bf16 layer folds each slot's gate
+    # into its expert: the stored h and y carry the gate)
+    P = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, aux=aux, fp8=fp8)
+    S = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, rnd=RND, aux=aux, fp8=fp8,
+                        fold_gate=not fp8)
+    case = cfg.name
+    assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], P["X_perm"], "X_perm", 0, 0)
+    check_plain(case, "logits", plan.logits, P["logits"], S["logits"])
+    check_plain(case, "gates", plan.topk_gate, P["gate"], S["gate"])
+    check_plain(case, "out", plan.out, P["out"], S["out"])
+    assert_close(plan.out, S["out"], "out")
     if aux is not None:
-        assert float(plan.aux_loss[0]) == pytest.approx(fwd["aux_switch"], rel=1e-5)
-        assert float(plan.aux_loss[1]) == pytest.approx(fwd["aux_seq"], rel=1e-5)
-    assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], fwd["X_perm"], "X_perm", 0, 0)
-    assert_close(plan.out, fwd["out"], "out")
+        assert float(plan.aux_loss[0]) == pytest.approx(P["aux_switch"], rel=1e-5)
+        assert float(plan.aux_loss[1]) == pytest.approx(P["aux_seq"], rel=1e-5)
     if cfg.mode == "softmax":
-        assert float(plan.z_loss[0]) == pytest.approx(fwd["z_loss"], rel=1e-4)
+        check_plain(case, "lse", plan.lse, P["lse"], S["lse"])
+        assert float(plan.z_loss[0]) == pytest.approx(P["z_loss"], rel=1e-4)
     if not cfg.backward:
         return
-    bwd = O.layer_backward(i64, fwd, O.to64(inp["dY"]))
-    assert_close(plan.dx, bwd["dx"], "dx")
-    for name in ("dW_g", "dW_u", "dW_d"):
-        assert_close(getattr(plan, name), bwd[name], name, reduction=True)
-    assert_close(plan.dW_r, bwd["dW_r"], "dW_r", reduction=True)
+    dY = O.to64(inp["dY"])
+    PB = O.layer_backward(i64, P, dY)
+    SB = O.layer_backward(i64, S, dY)
+    names = ["dx", "dg", "dlogits", "dW_r", "dW_g", "dW_u", "dW_d"]
     if cfg.f_shared:
-        for name in ("dWs_g", "dWs_u", "dWs_d"):
-            assert_close(getattr(plan, name), bwd[name], name, reduction=True)
+        names += ["dWs_g", "dWs_u", "dWs_d"]
+    for name in names:
+        got = getattr(plan, name)
+        check_plain(case, name, got, PB[name], SB[name])
+        if name == "dlogits":
+            assert_close(got, SB[name], name, atol=1e-5, rtol=1e-4)
+        else:
+            assert_close(got, SB[name], name, reduction=name != "dx")
     if cfg.bias_update:
         ref = oracle_bias(cfg)(D["counts"], inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), ref.view(np.uint32))
@@ -156,7 +175,7 @@ def test_single_expert_router_gets_zero_gradient():
     assert (plan.dW_r == 0).all()
 
 
-@pytest.mark.parametrize("name", ["C0", "C1"])
+@pytest.mark.parametrize("name", ["C0", "C1", "C2"])
 def test_workload_full_parity(name):
     cfg = CONFIGS[name]
     full_parity(cfg, make_inputs(cfg))
@@ -174,82 +193,91 @@ def test_layer_is_bitwise_repeatable():
         assert torch.equal(r1[k], v), k
 
 
-@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5", "C6", "C7"])
+SAMPLED_TOKENS = 2048
+SHARED_UNITS = 16
+
+
+@pytest.mark.parametrize("name", ["C3", "C4", "C5", "C6", "C7"])
 def test_workload_sampled_parity(name):
-    """Full-size workloads in the benchmark's launch configuration: routing, counts and
-    permutation in full; out and dx on sampled tokens; weight-gradient entries of sampled
-    experts (every empty expert must have exactly zero weight gradients)."""
+    """Full-size workloads in the benchmark's launch configuration, against a stratified
+    subset of the oracle: routing, counts and permutation in full; out, dx, the gate and
+    logit gradients on 2,048 fixed-seed tokens plus the first and last; the whole weight
+    gradients of the most-loaded expert and of the least-loaded live one (a handful of rows
+    in the skewed workload); exactly zero weight gradients for every empty expert; whole
+    weight rows of 16 shared-expert units."""
     cfg = CONFIGS[name]
     inp = make_inputs(cfg)
     plan, b_new = run_gpu(cfg, inp)
-    idx, lg, D, rows, _ = check_routing(cfg, inp, plan)
-    lazy = {k: (Lazy(v) if k in WEIGHTS or k == "x" else O.to64(v)) for k, v in inp.items()
-            if k != "dY"}
+    idx, lg, D, rows, near = check_routing(cfg, inp, plan)
+    record_near_ties(cfg.name, near, cfg.T)
+    case = cfg.name
+    fp8 = cfg.precision == "fp8"
+    W64 = {k: O.to64(v) for k, v in inp.items() if k not in ("x", "dY")}
+    x64, dY64 = O.to64(inp["x"]), O.to64(inp["dY"])
+    lg64 = O.router_logits(x64, W64["W_r"])
+    R = _replayed_gates(cfg, lg64, idx, W64["b"])
     rng = np.random.default_rng(cfg.seed)
-    toks = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, 14, replace=False)]))
-    ref = O.route(lg, cfg.mode, cfg.k, O.to64(inp["b"]), cfg.z_coef)
-    ref = O._regate(ref, lg, idx, cfg.mode, O.to64(inp["b"]), cfg.z_coef)
-    out = plan.out[torch.from_numpy(toks).cuda()]
-    dx = plan.dx[torch.from_numpy(toks).cuda()]
+    toks = np.unique(np.concatenate([[0, cfg.T - 1],
+                                     rng.choice(cfg.T, SAMPLED_TOKENS, replace=False)]))
+    tt = torch.from_numpy(toks).cuda()
     dl_aux = None
-    if cfg.has_aux:  # batch-wide losses: compared in full, their gradient feeds dx
-        a = O.aux_losses(lg, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
+    if cfg.has_aux:  # batch-wide losses: compared in full, their gradient rows feed dx
+        a = O.aux_losses(lg64, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
         assert float(plan.aux_loss[0]) == pytest.approx(a["switch"], rel=1e-5)
         assert float(plan.aux_loss[1]) == pytest.approx(a["seq"], rel=1e-5)
-        dl_aux = O.aux_losses_backward(lg, idx, cfg.mode, cfg.seq_len, cfg.aux_switch, cfg.aux_seq)
-    fp8 = cfg.precision == "fp8"
-    for j, t in enumerate(toks):
-        o = O.token_forward(lazy, int(t), idx[t], ref["gate"][t], rnd=RND, fp8=fp8,
-                            fold_gate=not fp8)
-        assert_close(out[j], o, f"out[{t}]")
-        tb = O.token_backward(lazy, int(t), lg[t], idx[t], cfg.mode, cfg.k,
-                              O.to64(inp["dY"][t]), cfg.z_coef, cfg.T, rnd=RND,
-                              dl_extra_t=None if dl_aux is None else dl_aux[t], fp8=fp8,
-                              fold_gate=not fp8)
-        assert_close(dx[j], tb["dx"], f"dx[{t}]")
+        dl_aux = O.aux_losses_backward(lg64, idx, cfg.mode, cfg.seq_len, cfg.aux_switch,
+                                       cfg.aux_seq)[toks]
+    # the layer over the sampled tokens: each token's out and dx depend only on its own
+    # routing; the z-loss mean and the balancing losses are the whole batch's
+    part = dict(W64, x=x64[toks])
+    P = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
+                        fp8=fp8)
+    S = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
+                        rnd=RND, fp8=fp8, fold_gate=not fp8)
+    check_plain(case, "gates", plan.topk_gate[tt], P["gate"], S["gate"])
+    check_plain(case, "out", plan.out[tt], P["out"], S["out"])
+    assert_close(plan.out[tt], S["out"], "out")
+    PB = O.layer_backward(part, P, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux, weight_grads=False)
+    SB = O.layer_backward(part, S, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux, weight_grads=False)
+    for nm in ("dx", "dg", "dlogits"):
+        got = getattr(plan, nm)[tt]
+        check_plain(case, nm, got, PB[nm], SB[nm])
+        if nm == "dlogits":
+            assert_close(got, SB[nm], nm, atol=1e-5, rtol=1e-4)
+        else:
+            assert_close(got, SB[nm], nm, reduction=nm == "dg")
+    # whole weight gradients of chosen experts
     counts = D["counts"]
     live = np.nonzero(counts)[0]
-    picks = {int(live[np.argmax(counts[live])]), int(live[np.argmin(counts[live])]),
-             int(rng.choice(live))}
-    dY64 = Lazy(inp["dY"])
-    for e in sorted(picks):
+    for e in sorted({int(live[np.argmax(counts[live])]), int(live[np.argmin(counts[live])])}):
         lo, hi = int(D["offsets"][e]), int(D["offsets"][e + 1])
         tok_e = D["perm_token"][lo:hi]
-        gates = ref["gate"][tok_e, D["perm_slot"][lo:hi]]
-        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f))) for _ in range(8)]
-        eg = [(int(rng.integers(cfg.f)), int(rng.integers(cfg.d))) for _ in range(8)]
-        want = O.expert_weight_grad_entries(
-            {"x": O.to64(inp["x"][torch.from_numpy(tok_e)]), "W_g": lazy["W_g"],
-             "W_u": lazy["W_u"], "W_d": lazy["W_d"]},
-            e, np.arange(hi - lo), gates, O.to64(inp["dY"][torch.from_numpy(tok_e)]), ed, eg,
-            rnd=RND, fp8=fp8, fold_gate=not fp8)
-        got_d = [float(plan.dW_d[e, i, j]) for (i, j) in ed]
-        got_g = [float(plan.dW_g[e, j, i]) for (j, i) in eg]
-        got_u = [float(plan.dW_u[e, j, i]) for (j, i) in eg]
-        assert_close(np.array(got_d), want["dW_d"], f"dW_d[{e}]", reduction=True)
-        assert_close(np.array(got_g), want["dW_g"], f"dW_g[{e}]", reduction=True)
-        assert_close(np.array(got_u), want["dW_u"], f"dW_u[{e}]", reduction=True)
+        gates = R["gate"][tok_e, D["perm_slot"][lo:hi]]
+        Pw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], fp8=fp8)
+        Sw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], rnd=RND, fp8=fp8,
+                                   fold_gate=not fp8)
+        for nm in ("dW_g", "dW_u", "dW_d"):
+            got = getattr(plan, nm)[e]
+            check_plain(case, f"{nm}[{e}]", got, Pw[nm], Sw[nm])
+            assert_close(got, Sw[nm], f"{nm}[{e}]", reduction=True)
     for e in np.nonzero(counts == 0)[0]:
-        for name in ("dW_g", "dW_u", "dW_d"):
-            assert (getattr(plan, name)[int(e)] == 0).all()
+        for nm in ("dW_g", "dW_u", "dW_d"):
+            assert (getattr(plan, nm)[int(e)] == 0).all()
     if cfg.zipf:
         assert (counts == 0).sum() >= 10
     if cfg.f_shared:
-        ed = [(int(rng.integers(cfg.d)), int(rng.integers(cfg.f_shared))) for _ in range(6)]
-        eg = [(int(rng.integers(cfg.f_shared)), int(rng.integers(cfg.d))) for _ in range(6)]
-        want = O.shared_weight_grad_entries({"x": O.to64(inp["x"]), "Ws_g": lazy["Ws_g"],
-                                             "Ws_u": lazy["Ws_u"], "Ws_d": lazy["Ws_d"]},
-                                            O.to64(inp["dY"]), ed, eg, rnd=RND, fp8=fp8)
-        assert_close(np.array([float(plan.dWs_d[i, j]) for (i, j) in ed]), want["dWs_d"], "dWs_d",
-                     reduction=True)
-        assert_close(np.array([float(plan.dWs_g[j, i]) for (j, i) in eg]), want["dWs_g"], "dWs_g",
-                     reduction=True)
-        assert_close(np.array([float(plan.dWs_u[j, i]) for (j, i) in eg]), want["dWs_u"], "dWs_u",
-                     reduction=True)
+        units = np.sort(rng.choice(cfg.f_shared, SHARED_UNITS, replace=False))
+        sh = {"x": x64, "Ws_g": W64["Ws_g"], "Ws_u": W64["Ws_u"], "Ws_d": W64["Ws_d"]}
+        Pu = O.shared_weight_grad_units(sh, dY64, units, fp8=fp8)
+        Su = O.shared_weight_grad_units(sh, dY64, units, rnd=RND, fp8=fp8)
+        ut = torch.from_numpy(units).cuda()
+        for nm, got in (("dWs_g", plan.dWs_g[ut]), ("dWs_u", plan.dWs_u[ut]),
+                        ("dWs_d", plan.dWs_d[:, ut])):
+            check_plain(case, nm, got, Pu[nm], Su[nm])
+            assert_close(got, Su[nm], nm, reduction=True)
     if cfg.bias_update:
         refb = oracle_bias(cfg)(counts, inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), refb.view(np.uint32))
-    del dY64
 
 
 def test_router_backward_at_full_size():
@@ -282,6 +310,7 @@ def test_router_backward_at_full_size():
     ref = O._regate(ref, lg, plan.topk_idx.cpu().numpy(), "sigmoid", O.to64(b), 0.0)
     rb = O.router_backward(O.to64(dg), ref, O.to64(x), O.to64(W_r), "sigmoid", 0.0)
     assert_close(plan.dlogits, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
+    assert_close(plan.dW_r, rb["dW_r"], "dW_r")  # the literal tolerance
     assert_close(plan.dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)
 
 

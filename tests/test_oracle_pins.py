@@ -413,6 +413,64 @@ def test_fp8_sampled_rows_equal_full_layer():
     np.testing.assert_allclose(ent["dWs_u"], [bwd["dWs_u"][1, 6]], rtol=1e-11)
 
 
+@pytest.mark.parametrize("mode, z, aux, fp8, fold, rnd", [
+    ("sigmoid", 0.0, None, False, False, None),
+    ("softmax", 0.05, None, False, False, None),
+    ("softmax", 0.05, (10, 0.3, 0.2), False, False, None),
+    ("sigmoid", 0.0, (10, 0.3, 0.2), False, True, "bf16"),
+    ("sigmoid", 0.0, None, True, False, "bf16"),
+])
+def test_token_subset_backward_equals_whole_layer(mode, z, aux, fp8, fold, rnd):
+    """The layer over a subset of a batch's tokens, with the batch's z-loss token count and
+    the batch's balancing-loss logit gradient rows passed in, gives the whole layer's out,
+    dx and dg rows of those tokens."""
+    rng = np.random.default_rng(41)
+    r = O.bf16_round if rnd else None
+    T = 30
+    inp = _tiny_inputs(rng, T=T, d=16, E=5, f=8, fs=4 if mode == "sigmoid" else 0)
+    dY = O.bf16_round(rng.standard_normal((T, 16)))
+    fwd = O.layer_forward(inp, mode, 2, z, rnd=r, aux=aux, fp8=fp8, fold_gate=fold)
+    bwd = O.layer_backward(inp, fwd, dY)
+    sub = np.array([0, 3, 4, 17, 29])
+    dl = None if aux is None else O.aux_losses_backward(fwd["logits"], fwd["idx"], mode, *aux)[sub]
+    part = dict(inp, x=inp["x"][sub])
+    f1 = O.layer_forward(part, mode, 2, z, logits=fwd["logits"][sub], idx=fwd["idx"][sub], rnd=r,
+                         fp8=fp8, fold_gate=fold)
+    b1 = O.layer_backward(part, f1, dY[sub], T_norm=T, dl_extra=dl, weight_grads=False)
+    np.testing.assert_allclose(f1["out"], fwd["out"][sub], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b1["dx"], bwd["dx"][sub], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(b1["dg"], bwd["dg"][sub], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(b1["dlogits"], bwd["dlogits"][sub], rtol=1e-11, atol=1e-13)
+    assert "dW_g" not in b1 and "dWs_g" not in b1
+
+
+@pytest.mark.parametrize("fp8, fold, rnd", [(False, False, None), (False, True, "bf16"),
+                                            (False, False, "bf16"), (True, False, "bf16")])
+def test_whole_expert_and_shared_unit_weight_grads_equal_whole_layer(fp8, fold, rnd):
+    """One expert's whole weight gradients from its own rows alone, and whole weight rows of
+    chosen shared-expert units, equal those of the whole layer."""
+    rng = np.random.default_rng(43)
+    r = O.bf16_round if rnd else None
+    T = 40
+    inp = _tiny_inputs(rng, T=T, d=16, E=5, f=8, fs=6)
+    dY = O.bf16_round(rng.standard_normal((T, 16)))
+    fwd = O.layer_forward(inp, "sigmoid", 2, rnd=r, fp8=fp8, fold_gate=fold)
+    bwd = O.layer_backward(inp, fwd, dY)
+    for e in range(5):
+        rows = np.arange(fwd["offsets"][e], fwd["offsets"][e + 1])
+        toks = fwd["perm_token"][rows]
+        gates = fwd["gate"][toks, fwd["perm_slot"][rows]]
+        w = O.expert_weight_grads(inp, e, inp["x"][toks], gates, dY[toks], rnd=r, fp8=fp8,
+                                  fold_gate=fold)
+        for name in ("dW_g", "dW_u", "dW_d"):
+            np.testing.assert_allclose(w[name], bwd[name][e], rtol=1e-11, atol=1e-13)
+    units = [0, 2, 5]
+    w = O.shared_weight_grad_units(inp, dY, units, rnd=r, fp8=fp8)
+    np.testing.assert_allclose(w["dWs_g"], bwd["dWs_g"][units], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(w["dWs_u"], bwd["dWs_u"][units], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(w["dWs_d"], bwd["dWs_d"][:, units], rtol=1e-11, atol=1e-13)
+
+
 # ----------------------------------------------------------------- bf16 storage precision
 
 def test_bf16_round_matches_library_conversion_including_ties():

@@ -315,6 +315,22 @@ def _regate_unrenormalised(r, logits, idx, mode, b, z_coef):
     return r
 
 
+def _expert_weight_grads_ungated(inp, e, X, gates, *a, **kw):
+    return ORIG["expert_weight_grads"](inp, e, X, np.ones_like(gates), *a, **kw)
+
+
+def _shared_units_dh_from_transposed_weight(inp, dY, units, rnd=None, fp8=False):
+    wd = inp["Ws_d"]
+    if wd.shape[0] != wd.shape[1]:
+        wd = np.resize(wd.T, wd.shape)
+    return ORIG["shared_weight_grad_units"](dict(inp, Ws_d=wd), dY, units, rnd, fp8)
+
+
+def _layer_backward_subset_ignores_batch_count(inp, fwd, dY, T_norm=None, dl_extra=None,
+                                               weight_grads=True):
+    return ORIG["layer_backward"](inp, fwd, dY, None, dl_extra, weight_grads)
+
+
 MUTANTS = {
     "silu with sigmoid(-z)": ("silu", _silu_wrong_sign),
     "sigmoid with the wrong sign": ("sigmoid", _sigmoid_wrong_sign),
@@ -354,6 +370,9 @@ MUTANTS = {
     "sampled weight gradients ignore the gates": ("expert_weight_grad_entries", _weight_grad_entries_ungated),
     "sampled FP8 weight gradients from unquantised operands": ("_gemm_operands", _gemm_operands_unquantised),
     "replayed sigmoid gates not renormalised": ("_regate", _regate_unrenormalised),
+    "whole expert weight gradients ignore the gates": ("expert_weight_grads", _expert_weight_grads_ungated),
+    "shared-unit gradients through the wrong output weights": ("shared_weight_grad_units", _shared_units_dh_from_transposed_weight),
+    "token-subset backward normalises the z-loss by the subset": ("layer_backward", _layer_backward_subset_ignores_batch_count),
 }
 
 
