@@ -79,14 +79,17 @@ def workload_desc(cfg):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples of SM clock, power and throttle reasons while the timed region
+    runs; ``mark(name)`` closes a phase, and the report gives each phase's medians too."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id: str):
         self.proc = None
+        self.phases = []  # (name, host start, host end)
+        self._t = time.time()
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(
@@ -94,6 +97,20 @@ class ClockSampler:
                  "-lms", "200", "-i", gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def mark(self, name: str):
+        """End the current phase (the caller has synchronised the device)."""
+        now = time.time()
+        self.phases.append((name, self._t, now))
+        self._t = now
+
+    @staticmethod
+    def _stamp(text: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -105,21 +122,33 @@ class ClockSampler:
         self.file.seek(0)
         rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
         os.unlink(self.file.name)
-        sm, mx, reasons = [], 0.0, set()
+        samples, mx, reasons = [], 0.0, set()  # (time, sm MHz, power W)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
-                sm.append(float(r[1]))
-                mx = max(mx, float(r[2]))
-                for name, v in zip(names, r[5:9]):
+                pw = float(r[4]) if r[4].strip() not in ("", "[N/A]") else float("nan")
+                samples.append((self._stamp(r[0]), float(r[2]), pw))
+                mx = max(mx, float(r[3]))
+                for name, v in zip(names, r[6:10]):
                     if v.strip().lower() == "active":
                         reasons.add(name)
             except (ValueError, IndexError):
                 continue
-        if not sm:
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(s[1] for s in samples), "sm_max_mhz": mx,
+               "reasons": sorted(reasons), "samples": len(samples)}
+        by_phase = {}
+        for name, t0, t1 in self.phases:
+            sel = [s for s in samples if s[0] is not None and t0 <= s[0] <= t1]
+            if sel:
+                pws = [s[2] for s in sel if s[2] == s[2]]
+                by_phase[name] = {"sm_mhz": statistics.median(s[1] for s in sel),
+                                  "power_w": statistics.median(pws) if pws else None,
+                                  "samples": len(sel)}
+        if by_phase:
+            out["by_phase"] = by_phase
+        return out
 
 
 def slowest_rank(times_ms, world: int, device: str = "cuda"):
@@ -349,6 +378,7 @@ def main():
     ms_eager = timed(lambda: step(dev["x"], dev.get("dY")), args.steps)
     gemm_ms = sum(a.elapsed_time(b) for a, b in plan.gemm_events)
     plan.gemm_events = None
+    sampler.mark("device_eager")
 
     # ------------------------------------------------------------ end to end, host buffers
     # (between the two device-resident passes, under the same clock sampling)
@@ -406,11 +436,13 @@ def main():
 
         run_steps(args.warmup)
         sync_all()
+        sampler.mark("e2e_warmup")
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         run_steps(args.steps)
         b.record(stream)
         sync_all()
+        sampler.mark("e2e")
         ms_e2e = slowest_rank([a.elapsed_time(b)], world)[0] / args.steps
         nbytes = cfg.T * cfg.d * 2
         e2e = {"value": job_tokens_per_s(world, cfg.T, ms_e2e), "unit": "tokens/s",
@@ -426,7 +458,10 @@ def main():
         graph = plan.capture_step(dev["x"], weights, dev.get("dY") if cfg.backward else None,
                                   b_work, cfg.gamma, cfg.bias_rule, cfg.bias_update)
         graph.replay()
+        torch.cuda.synchronize()
+        sampler.mark("graph_capture")
         ms_graph = timed(graph.replay, args.steps)
+        sampler.mark("device_graph")
     clocks = sampler.stop()
     code, site = ops.moe_device_status()
     if code != 0:

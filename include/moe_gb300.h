@@ -167,7 +167,9 @@ int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, in
  *   - Allocation: none. It calls no cudaMalloc, cudaFree or allocating library routine.
  *   - Set-up: the first call on each device (made with that device current) looks up the
  *     device address of the static array once; make that first call before any stream
- *     capture on that device.
+ *     capture on that device. The lookup is repeated only when the device's context has
+ *     changed since (e.g. after cudaDeviceReset), which makes the next call a first call
+ *     again.
  *   - Sharing: all calls on a device use the same array and it keeps the last call's
  *     contents (nothing in it needs to start at zero: every entry is written before it is
  *     read). Calls that overlap on the GPU (different streams, no ordering between them)

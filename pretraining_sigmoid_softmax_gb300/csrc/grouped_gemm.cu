@@ -58,10 +58,11 @@ enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
 // columns per chunk, kAuBufs chunks deep; the ring of operand stages gets what is left of
 // kSmemBudgetAu.
 constexpr int kAuCols = 16;
-constexpr int kAuBufs = 3;
+constexpr int kAuBufs = 2;
 constexpr int kSmemBudgetAu = 220 * 1024;
 // Token-major epilogues stage their outputs in shared memory, 16 columns x 32 rows per warp
-// and output, two buffers deep, and write them with TMA stores.
+// and output, and write them with TMA stores: two buffers deep, or one for the SwiGLU
+// backward, whose operand ring then keeps a fifth stage (what bounds it at K = 4096).
 constexpr int kOutCols = 16;
 
 template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
@@ -89,7 +90,8 @@ struct Cfg {
     static constexpr bool TS = !WGRAD;  // token-major outputs leave by TMA stores
     static constexpr int NOUT = EPI == kEpiSwigluFwd ? 3 : EPI == kEpiSwigluBwd ? 2 : 1;
     static constexpr int OUT_BUF_BYTES = NOUT * 32 * kOutCols * 2;  // one chunk, every output
-    static constexpr int OUT_BYTES = TS ? kEpiWarps * 2 * OUT_BUF_BYTES : 0;
+    static constexpr int OUT_DEPTH = AU ? 1 : 2;                     // staged chunks per warp
+    static constexpr int OUT_BYTES = TS ? kEpiWarps * OUT_DEPTH * OUT_BUF_BYTES : 0;
     static constexpr int BUDGET = (AU || TS ? kSmemBudgetAu : kSmemBudget) - AU_BYTES - OUT_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 6 ? 6 : (BUDGET / STAGE_BYTES);
     static constexpr int ACC_COLS = MMA_N;
@@ -429,8 +431,8 @@ __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const Ti
             for (int j = 0; j < kOutCols; ++j) v[0][j] = __uint_as_float(r[j]);
             if constexpr (C::FP8) fp8_scale<kOutCols>(v[0], v[0], P, row, ti, c, /*dual=*/false);
         }
-        uint8_t* buf = S.ob + ((size_t)slot * 2 + (n & 1)) * C::OUT_BUF_BYTES;
-        if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+        uint8_t* buf = S.ob + ((size_t)slot * C::OUT_DEPTH + n % C::OUT_DEPTH) * C::OUT_BUF_BYTES;
+        if (lane == 0) bulk_wait_read<C::OUT_DEPTH - 1>();  // the store that last read it is done
         __syncwarp();
 #pragma unroll
         for (int o = 0; o < C::NOUT; ++o)
@@ -549,8 +551,8 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
         if (lane == 0 && i + kAuBufs < nch)
             au_issue<C>(S, ma, mu, slot, n + kAuBufs, row0, ti.n0 + c + kAuBufs * kAuCols);
         if (store) {
-            uint8_t* ob = S.ob + ((size_t)slot * 2 + (n & 1)) * C::OUT_BUF_BYTES;
-            if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+            uint8_t* ob = S.ob + ((size_t)slot * C::OUT_DEPTH + n % C::OUT_DEPTH) * C::OUT_BUF_BYTES;
+            if (lane == 0) bulk_wait_read<C::OUT_DEPTH - 1>();  // the store that last read it is done
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < kAuCols / 8; ++j) {

@@ -9,6 +9,7 @@
 // These steps move bytes: every row copy is a warp-wide run of 16-byte vectors so each
 // memory instruction touches whole 512-byte spans. Counting uses integer atomics in shared
 // memory only (order-independent); every floating-point sum has a fixed order.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -638,23 +639,62 @@ constexpr int kNoallocMaxDevices = 64;
 // [0, kNoallocMaxInts): per-chunk counts; [kNoallocMaxInts, 2 kNoallocMaxInts): chunk bases.
 static __device__ __align__(256) int32_t g_permute_scratch[2 * kNoallocMaxInts];
 
-int32_t* g_permute_scratch_ptr[kNoallocMaxDevices] = {nullptr};
+// Per device: the context the address was looked up in (by its driver-assigned id, which
+// is never reused) and the address. A new context on the device (after cudaDeviceReset, or
+// a primary context released and created again) may place the array elsewhere, so the
+// address is looked up again whenever the current context's id differs.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    int32_t* ptr;
+};
+ScratchAddr g_permute_scratch_addr[kNoallocMaxDevices] = {};
 std::mutex g_permute_scratch_mu;
 
-// Device address of g_permute_scratch on the current device, looked up once per device.
-// In host code the symbol name is only a host-side handle, so the address must come from
-// the runtime before a kernel can be given it.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the current context, or 0 when the driver cannot give one (then the address is
+// looked up on every call).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_permute_scratch in the current device's context, looked up once per
+// context. In host code the symbol name is only a host-side handle, so the address must
+// come from the runtime before a kernel can be given it.
 int32_t* permute_scratch_on_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) return nullptr;
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lk(g_permute_scratch_mu);
-    if (!g_permute_scratch_ptr[dev]) {
+    ScratchAddr& a = g_permute_scratch_addr[dev];
+    if (!a.ptr || id == 0 || a.ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
             return nullptr;
-        g_permute_scratch_ptr[dev] = static_cast<int32_t*>(p);
+        a.ptr = static_cast<int32_t*>(p);
+        a.ctx_id = id;
     }
-    return g_permute_scratch_ptr[dev];
+    return a.ptr;
 }
 
 }  // namespace

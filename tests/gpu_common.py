@@ -8,6 +8,11 @@ from oracle import moe_oracle as O
 
 ATOL = 1e-2
 RTOL = 1e-2
+# Sums over tokens in the storage-model check: the fraction of elements allowed past the bound.
+# When the fp32 evaluation rounds one large operand (h of 8 to 16 has a bf16 ulp of 1/16) to
+# its other bf16 neighbour, every sum that operand enters moves by |other operand| x that
+# ulp, up to about 0.3, whatever the sum's own size: a column of dW_d, for example.
+SUM_FLIP_FRAC = 1e-6
 
 
 def require_gpu():
@@ -26,7 +31,8 @@ def h64(t):
     return O.to64(t)
 
 
-def assert_close(gpu, ref, name, atol=ATOL, rtol=RTOL, reduction=False):
+def assert_close(gpu, ref, name, atol=ATOL, rtol=RTOL, reduction=False, extra=None,
+                 allow_frac=0.0):
     """|gpu - oracle| <= atol + rtol |oracle| elementwise.
 
     Against the oracle's bf16-storage model this is the consistency check of the kernels'
@@ -36,19 +42,31 @@ def assert_close(gpu, ref, name, atol=ATOL, rtol=RTOL, reduction=False):
     operand element that the fp32 GPU evaluation rounds to the neighbouring bf16 value
     (unavoidable: about 1 in 2000 elements of a bf16 activation) moves every sum it enters
     by |other operand| x one bf16 ulp, independent of the sum's own value. The absolute
-    term is then taken relative to the tensor's RMS: atol * max(1, rms(oracle))."""
+    term is then taken relative to the tensor's RMS: atol * max(1, rms(oracle)).
+
+    ``extra`` adds an elementwise term to the bound (e.g. one bf16 ulp of each bf16 summand
+    of a sum over slots). ``allow_frac`` lets that fraction of the elements fall outside:
+    with FP8 operands a bf16 neighbour of h can round to the next E4M3 code, which moves a
+    whole output row by a code step."""
     g = h64(gpu) if not isinstance(gpu, np.ndarray) else gpu.astype(np.float64)
     r = np.asarray(ref, dtype=np.float64)
     if reduction and r.size:
         atol = atol * max(1.0, float(np.sqrt(np.mean(r * r))))
     assert g.shape == r.shape, f"{name}: shape {g.shape} vs {r.shape}"
     err = np.abs(g - r)
-    bad = err > atol + rtol * np.abs(r)
+    bound = atol + rtol * np.abs(r) + (0.0 if extra is None else extra)
+    bad = err > bound
+    if reduction:
+        allow_frac = max(allow_frac, SUM_FLIP_FRAC)
+    if bad.sum() <= allow_frac * bad.size:
+        return
     if bad.any():
-        i = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(r))), r.shape)
+        i = np.unravel_index(np.argmax(err - bound), r.shape)
+        where = [tuple(int(v) for v in w) for w in np.argwhere(bad)[:8]]
         raise AssertionError(
             f"{name}: {int(bad.sum())} of {bad.size} elements outside {atol} + {rtol}|ref|; "
-            f"worst at {i}: gpu {g[i]!r} oracle {r[i]!r}; max abs err {err.max():.3e}")
+            f"worst at {i}: gpu {g[i]!r} oracle {r[i]!r}; max abs err {err.max():.3e}; "
+            f"first outside at {where}")
 
 
 # Literal-tolerance report against the plain definition: per case and tensor, how many
@@ -117,6 +135,19 @@ def assert_gemm_exact(gpu, A, B, name):
         i = tuple(np.argwhere(bad)[0])
         raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} elements outside the "
                              f"bf16/fp32 bound; e.g. {i}: gpu {g[i]!r} exact {ex[i]!r}")
+
+
+def dx_summand_ulps(fwd, bwd):
+    """Per element of the layer's input gradient: one bf16 ulp of each of its bf16 summands
+    (the token's expert input-gradient rows and the shared expert's), by which a different
+    but correct rounding of each summand moves the sum."""
+    s2r = fwd["slot_to_row"]
+    b = np.zeros_like(bwd["dx"])
+    for i in range(s2r.shape[1]):
+        b += ulp_bf16(bwd["dX_perm"][s2r[:, i]])
+    if "dx_shared" in bwd:
+        b += ulp_bf16(bwd["dx_shared"])
+    return b
 
 
 def padded_offsets(counts, align=128):

@@ -18,8 +18,12 @@ from pretraining_sigmoid_softmax_gb300.configs import CONFIGS, MoEConfig
 from pretraining_sigmoid_softmax_gb300.inputs import make_inputs, make_upstream_gate_grad
 from pretraining_sigmoid_softmax_gb300.layer import MoEPlan, MoEShape
 
-from gpu_common import (assert_close, check_plain, gpu_rows, h64, padded_offsets,
-                        record_near_ties, require_gpu)
+from gpu_common import (assert_close, check_plain, dx_summand_ulps, gpu_rows, h64,
+                        padded_offsets, record_near_ties, require_gpu)
+
+# FP8 operands: the fraction of elements the storage-model check lets a bf16 neighbour of h
+# move past its bound by rounding to the next E4M3 code (every element of the affected rows)
+FP8_CODE_FLIPS = 1e-3
 
 pytestmark = pytest.mark.gpu
 RND = O.bf16_round
@@ -74,6 +78,15 @@ def check_routing(cfg, inp, plan):
     return idx, lg, D, rows, int(near.sum())
 
 
+def dlogits_atol(bwd):
+    """Absolute term of the storage check of the logit gradient. It is linear in the gate
+    gradient dg with coefficients of magnitude at most 1 (softmax: p_j (delta_j - p_i);
+    sigmoid: s (1 - s) (delta - g) / sum of the chosen s), so it inherits dg's absolute
+    error: twice dg's absolute term, 1e-2 max(1, rms(dg))."""
+    dg = np.asarray(bwd["dg"])
+    return 2.0 * 1e-2 * max(1.0, float(np.sqrt(np.mean(dg * dg)))) if dg.size else 1e-2
+
+
 def _aux(cfg):
     return (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
 
@@ -103,8 +116,9 @@ def full_parity(cfg, inp):
     assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], P["X_perm"], "X_perm", 0, 0)
     check_plain(case, "logits", plan.logits, P["logits"], S["logits"])
     check_plain(case, "gates", plan.topk_gate, P["gate"], S["gate"])
+    flips = FP8_CODE_FLIPS if fp8 else 0.0
     check_plain(case, "out", plan.out, P["out"], S["out"])
-    assert_close(plan.out, S["out"], "out")
+    assert_close(plan.out, S["out"], "out", allow_frac=flips)
     if aux is not None:
         assert float(plan.aux_loss[0]) == pytest.approx(P["aux_switch"], rel=1e-5)
         assert float(plan.aux_loss[1]) == pytest.approx(P["aux_seq"], rel=1e-5)
@@ -122,10 +136,12 @@ def full_parity(cfg, inp):
     for name in names:
         got = getattr(plan, name)
         check_plain(case, name, got, PB[name], SB[name])
-        if name == "dlogits":
-            assert_close(got, SB[name], name, atol=1e-5, rtol=1e-4)
-        else:
-            assert_close(got, SB[name], name, reduction=name != "dx")
+        if name == "dx":
+            assert_close(got, SB[name], name, extra=dx_summand_ulps(S, SB), allow_frac=flips)
+        elif name == "dlogits":
+            assert_close(got, SB[name], name, atol=dlogits_atol(SB), allow_frac=flips)
+        else:  # sums over tokens, or (dg) over the features of bf16 rows
+            assert_close(got, SB[name], name, reduction=True, allow_frac=flips)
     if cfg.bias_update:
         ref = oracle_bias(cfg)(D["counts"], inp["b"].numpy(), cfg.T, cfg.k, cfg.gamma)
         assert np.array_equal(b_new.cpu().numpy().view(np.uint32), ref.view(np.uint32))
@@ -234,18 +250,21 @@ def test_workload_sampled_parity(name):
                         fp8=fp8)
     S = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
                         rnd=RND, fp8=fp8, fold_gate=not fp8)
+    flips = FP8_CODE_FLIPS if fp8 else 0.0
     check_plain(case, "gates", plan.topk_gate[tt], P["gate"], S["gate"])
     check_plain(case, "out", plan.out[tt], P["out"], S["out"])
-    assert_close(plan.out[tt], S["out"], "out")
+    assert_close(plan.out[tt], S["out"], "out", allow_frac=flips)
     PB = O.layer_backward(part, P, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux, weight_grads=False)
     SB = O.layer_backward(part, S, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux, weight_grads=False)
     for nm in ("dx", "dg", "dlogits"):
         got = getattr(plan, nm)[tt]
         check_plain(case, nm, got, PB[nm], SB[nm])
-        if nm == "dlogits":
-            assert_close(got, SB[nm], nm, atol=1e-5, rtol=1e-4)
+        if nm == "dx":
+            assert_close(got, SB[nm], nm, extra=dx_summand_ulps(S, SB), allow_frac=flips)
+        elif nm == "dlogits":
+            assert_close(got, SB[nm], nm, atol=dlogits_atol(SB), allow_frac=flips)
         else:
-            assert_close(got, SB[nm], nm, reduction=nm == "dg")
+            assert_close(got, SB[nm], nm, reduction=True, allow_frac=flips)
     # whole weight gradients of chosen experts
     counts = D["counts"]
     live = np.nonzero(counts)[0]
