@@ -123,6 +123,30 @@ def fp8_dequant_rows(X: np.ndarray) -> np.ndarray:
     return q * sc[:, None]
 
 
+def fp8_dequant_cols(W: np.ndarray) -> np.ndarray:
+    """Columnwise FP8 quantisation: each column scaled by its own amax over the rows (the
+    rowwise quantisation of W^T), dequantised."""
+    return fp8_dequant_rows(np.asarray(W).T).T
+
+
+def fp8_dgrad_dh(dy: np.ndarray, W_d: np.ndarray) -> np.ndarray:
+    """The down projection's data gradient r = dy W_d with FP8 operands (reading of the
+    Apex-3 stack's fp8_rowwise precision for the backward): the rows of dy are scaled along
+    the contraction axis d (one scale per row), W_d [d, f] per output column j (one scale
+    per column, over d), and the products accumulate exactly."""
+    return fp8_dequant_rows(dy) @ fp8_dequant_cols(W_d)
+
+
+def fp8_dgrad_dx(da: np.ndarray, du: np.ndarray, W_g: np.ndarray, W_u: np.ndarray) -> np.ndarray:
+    """The expert's input gradient dX = da W_g + du W_u as one product over K = 2f with FP8
+    operands: each row of [da | du] gets one scale over its 2f elements, each column i of
+    [W_g; W_u] (2f x d) one scale over its 2f elements, and the products accumulate
+    exactly."""
+    AU = fp8_dequant_rows(np.concatenate([da, du], axis=1))
+    W = fp8_dequant_cols(np.concatenate([W_g, W_u], axis=0))
+    return AU @ W
+
+
 def sigmoid(z: np.ndarray) -> np.ndarray:
     return 1.0 / (1.0 + np.exp(-z))
 
@@ -312,7 +336,7 @@ def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
 def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                   logits: np.ndarray | None = None, idx: np.ndarray | None = None,
                   rnd=None, aux: tuple | None = None, fp8: bool = False,
-                  fold_gate: bool = False) -> dict:
+                  fold_gate: bool = False, fp8_dgrad: bool = False) -> dict:
     """Full forward of the layer from fp64 copies of the inputs.
 
     ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
@@ -320,7 +344,8 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
     the chosen experts (used so value checks do not cascade from a near-tie).
     ``fold_gate`` applies each slot's gate inside its expert (before the linear down
     projection) and combines without weights: the same value in exact arithmetic, and with
-    ``rnd`` the rounding of a layout that stores the gated h and y."""
+    ``rnd`` the rounding of a layout that stores the gated h and y. ``fp8_dgrad`` marks the
+    layer whose backward data-gradient products take FP8 operands (``layer_backward``)."""
     x = inp["x"]
     E = inp["W_r"].shape[0]
     if logits is None:
@@ -341,8 +366,11 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                                                                inp["Ws_d"], rnd)
     out = combine(ex["Y_perm"], np.ones_like(r["gate"]) if fold_gate else r["gate"],
                   disp["slot_to_row"], None if shared is None else shared[3], rnd)
+    if fp8_dgrad and fold_gate:
+        raise ValueError("the FP8 data gradients take the ungated rows; fold_gate is bf16 only")
     res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
-           "z_coef": z_coef, "rnd": rnd, "aux": aux, "row_gate": row_gate}
+           "z_coef": z_coef, "rnd": rnd, "aux": aux, "row_gate": row_gate,
+           "fp8_dgrad": fp8_dgrad}
     if aux is not None:  # (seq_len, switch_coef, seq_coef)
         a = aux_losses(logits, r["idx"], mode, *aux)
         res["aux_switch"], res["aux_seq"] = a["switch"], a["seq"]
@@ -412,7 +440,8 @@ def swiglu_backward(dh: np.ndarray, a: np.ndarray, u: np.ndarray):
 
 def expert_backward(dy: np.ndarray, x: np.ndarray, a: np.ndarray, u: np.ndarray,
                     h: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_d: np.ndarray,
-                    rnd=None, row_gate: np.ndarray | None = None) -> dict:
+                    rnd=None, row_gate: np.ndarray | None = None,
+                    fp8_dgrad: bool = False) -> dict:
     """Backward of one SwiGLU expert over its rows, given the upstream gradient of its
     output and the stored a, u, h of the forward:
     dh = dy W_d, (da, du) from the SwiGLU derivative, dx = da W_g + du W_u,
@@ -420,12 +449,17 @@ def expert_backward(dy: np.ndarray, x: np.ndarray, a: np.ndarray, u: np.ndarray,
 
     With ``row_gate`` (the gate folded into the expert, h stored gated): dy is the gradient
     of the gated output, r = dy W_d, dh = g * r, dW_d = dy^T h (h already carries g), and
-    the gate's gradient per row is dg = sum_j r_j silu(a_j) u_j (returned as "dg_row")."""
-    r = dy @ W_d
+    the gate's gradient per row is dg = sum_j r_j silu(a_j) u_j (returned as "dg_row").
+
+    ``fp8_dgrad``: the two data-gradient products (r and dx) take FP8 operands
+    (``fp8_dgrad_dh``, ``fp8_dgrad_dx``, the latter on the stored da and du); the weight
+    gradients stay products of the stored bf16 tensors."""
+    r = fp8_dgrad_dh(dy, W_d) if fp8_dgrad else dy @ W_d
     dh = r if row_gate is None else row_gate[:, None] * r
     da, du = swiglu_backward(dh, a, u)
     da, du = _r(rnd, da), _r(rnd, du)
-    res = {"dA": da, "dU": du, "dX": _r(rnd, da @ W_g + du @ W_u),
+    dx = fp8_dgrad_dx(da, du, W_g, W_u) if fp8_dgrad else da @ W_g + du @ W_u
+    res = {"dA": da, "dU": du, "dX": _r(rnd, dx),
            "dW_d": _r(rnd, dy.T @ h), "dW_g": _r(rnd, da.T @ x), "dW_u": _r(rnd, du.T @ x)}
     if row_gate is not None:
         res["dg_row"] = np.sum(r * silu(a) * u, axis=1)
@@ -477,6 +511,7 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = No
     be the subset's), and ``weight_grads=False`` skips the weight gradients, which only the
     whole batch gives."""
     rnd = fwd.get("rnd")
+    f8 = bool(fwd.get("fp8_dgrad"))
     idx, gate, s2r = fwd["idx"], fwd["gate"], fwd["slot_to_row"]
     T, k = idx.shape
     E = inp["W_r"].shape[0]
@@ -503,7 +538,8 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = No
         g = expert_backward(dY_perm[lo:hi], fwd["X_perm"][lo:hi], fwd["A"][lo:hi],
                             fwd["U"][lo:hi], fwd["H"][lo:hi], inp["W_g"][e], inp["W_u"][e],
                             inp["W_d"][e], rnd,
-                            row_gate=None if row_gate is None else row_gate[lo:hi])
+                            row_gate=None if row_gate is None else row_gate[lo:hi],
+                            fp8_dgrad=f8)
         if row_gate is not None:
             dg[tok[lo:hi], slot[lo:hi]] = g["dg_row"]
         dX_perm[lo:hi], dA[lo:hi], dU[lo:hi] = g["dX"], g["dA"], g["dU"]
@@ -515,7 +551,7 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = No
     if "shared" in fwd:
         sh = fwd["shared"]
         g = expert_backward(dY, inp["x"], sh["A"], sh["U"], sh["H"], inp["Ws_g"], inp["Ws_u"],
-                            inp["Ws_d"], rnd)
+                            inp["Ws_d"], rnd, fp8_dgrad=f8)
         if weight_grads:
             res["dWs_d"], res["dWs_g"], res["dWs_u"] = g["dW_d"], g["dW_g"], g["dW_u"]
         res["dx_shared"] = g["dX"]
@@ -765,7 +801,8 @@ def shared_weight_grad_entries(inp: dict, dY: np.ndarray, entries_d, entries_gu,
 
 
 def expert_weight_grads(inp: dict, e: int, X: np.ndarray, gates: np.ndarray, dY_rows: np.ndarray,
-                        rnd=None, fp8: bool = False, fold_gate: bool = False) -> dict:
+                        rnd=None, fp8: bool = False, fold_gate: bool = False,
+                        fp8_dgrad: bool = False) -> dict:
     """The whole weight gradients dW_g[e], dW_u[e], dW_d[e] of one expert.
 
     ``X`` holds the rows of the tokens routed to expert e in ascending token order, ``gates``
@@ -781,12 +818,12 @@ def expert_weight_grads(inp: dict, e: int, X: np.ndarray, gates: np.ndarray, dY_
     else:
         a, u, h, _ = expert(X, Wg, Wu, Wd, rnd)
         dy = _r(rnd, gates[:, None] * dY_rows)
-        g = expert_backward(dy, X, a, u, h, Wg, Wu, Wd, rnd)
+        g = expert_backward(dy, X, a, u, h, Wg, Wu, Wd, rnd, fp8_dgrad=fp8_dgrad)
     return {"dW_g": g["dW_g"], "dW_u": g["dW_u"], "dW_d": g["dW_d"]}
 
 
 def shared_weight_grad_units(inp: dict, dY: np.ndarray, units, rnd=None,
-                             fp8: bool = False) -> dict:
+                             fp8: bool = False, fp8_dgrad: bool = False) -> dict:
     """Whole weight rows of chosen hidden units j of the shared expert (every token, weight
     1): dWs_g[j, :], dWs_u[j, :] (the units' input weights) and dWs_d[:, j] (their output
     weights). The units' a, u and h over all tokens need only their own weight rows:
@@ -798,6 +835,10 @@ def shared_weight_grad_units(inp: dict, dY: np.ndarray, units, rnd=None,
     av, uv = Xo @ Wgo[units].T, Xo @ Wuo[units].T
     a, u = _r(rnd, av), _r(rnd, uv)
     h = _r(rnd, silu(av) * uv)  # from the unrounded a and u, as the forward stores it
-    da, du = swiglu_backward(dY @ inp["Ws_d"][:, units], a, u)
+    if fp8_dgrad:  # the units' columns of the FP8 product (column scales are per column)
+        dh = fp8_dequant_rows(dY) @ fp8_dequant_cols(inp["Ws_d"])[:, units]
+    else:
+        dh = dY @ inp["Ws_d"][:, units]
+    da, du = swiglu_backward(dh, a, u)
     return {"dWs_g": _r(rnd, _r(rnd, da).T @ X), "dWs_u": _r(rnd, _r(rnd, du).T @ X),
             "dWs_d": _r(rnd, dY.T @ h)}

@@ -413,14 +413,15 @@ def test_fp8_sampled_rows_equal_full_layer():
     np.testing.assert_allclose(ent["dWs_u"], [bwd["dWs_u"][1, 6]], rtol=1e-11)
 
 
-@pytest.mark.parametrize("mode, z, aux, fp8, fold, rnd", [
-    ("sigmoid", 0.0, None, False, False, None),
-    ("softmax", 0.05, None, False, False, None),
-    ("softmax", 0.05, (10, 0.3, 0.2), False, False, None),
-    ("sigmoid", 0.0, (10, 0.3, 0.2), False, True, "bf16"),
-    ("sigmoid", 0.0, None, True, False, "bf16"),
+@pytest.mark.parametrize("mode, z, aux, fp8, fold, rnd, f8d", [
+    ("sigmoid", 0.0, None, False, False, None, False),
+    ("softmax", 0.05, None, False, False, None, False),
+    ("softmax", 0.05, (10, 0.3, 0.2), False, False, None, False),
+    ("sigmoid", 0.0, (10, 0.3, 0.2), False, True, "bf16", False),
+    ("sigmoid", 0.0, None, True, False, "bf16", False),
+    ("softmax", 0.05, None, True, False, "bf16", True),
 ])
-def test_token_subset_backward_equals_whole_layer(mode, z, aux, fp8, fold, rnd):
+def test_token_subset_backward_equals_whole_layer(mode, z, aux, fp8, fold, rnd, f8d):
     """The layer over a subset of a batch's tokens, with the batch's z-loss token count and
     the batch's balancing-loss logit gradient rows passed in, gives the whole layer's out,
     dx and dg rows of those tokens."""
@@ -429,13 +430,14 @@ def test_token_subset_backward_equals_whole_layer(mode, z, aux, fp8, fold, rnd):
     T = 30
     inp = _tiny_inputs(rng, T=T, d=16, E=5, f=8, fs=4 if mode == "sigmoid" else 0)
     dY = O.bf16_round(rng.standard_normal((T, 16)))
-    fwd = O.layer_forward(inp, mode, 2, z, rnd=r, aux=aux, fp8=fp8, fold_gate=fold)
+    fwd = O.layer_forward(inp, mode, 2, z, rnd=r, aux=aux, fp8=fp8, fold_gate=fold,
+                          fp8_dgrad=f8d)
     bwd = O.layer_backward(inp, fwd, dY)
     sub = np.array([0, 3, 4, 17, 29])
     dl = None if aux is None else O.aux_losses_backward(fwd["logits"], fwd["idx"], mode, *aux)[sub]
     part = dict(inp, x=inp["x"][sub])
     f1 = O.layer_forward(part, mode, 2, z, logits=fwd["logits"][sub], idx=fwd["idx"][sub], rnd=r,
-                         fp8=fp8, fold_gate=fold)
+                         fp8=fp8, fold_gate=fold, fp8_dgrad=f8d)
     b1 = O.layer_backward(part, f1, dY[sub], T_norm=T, dl_extra=dl, weight_grads=False)
     np.testing.assert_allclose(f1["out"], fwd["out"][sub], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(b1["dx"], bwd["dx"][sub], rtol=1e-11, atol=1e-12)
@@ -444,9 +446,12 @@ def test_token_subset_backward_equals_whole_layer(mode, z, aux, fp8, fold, rnd):
     assert "dW_g" not in b1 and "dWs_g" not in b1
 
 
-@pytest.mark.parametrize("fp8, fold, rnd", [(False, False, None), (False, True, "bf16"),
-                                            (False, False, "bf16"), (True, False, "bf16")])
-def test_whole_expert_and_shared_unit_weight_grads_equal_whole_layer(fp8, fold, rnd):
+@pytest.mark.parametrize("fp8, fold, rnd, f8d", [(False, False, None, False),
+                                                 (False, True, "bf16", False),
+                                                 (False, False, "bf16", False),
+                                                 (True, False, "bf16", False),
+                                                 (True, False, "bf16", True)])
+def test_whole_expert_and_shared_unit_weight_grads_equal_whole_layer(fp8, fold, rnd, f8d):
     """One expert's whole weight gradients from its own rows alone, and whole weight rows of
     chosen shared-expert units, equal those of the whole layer."""
     rng = np.random.default_rng(43)
@@ -454,18 +459,18 @@ def test_whole_expert_and_shared_unit_weight_grads_equal_whole_layer(fp8, fold, 
     T = 40
     inp = _tiny_inputs(rng, T=T, d=16, E=5, f=8, fs=6)
     dY = O.bf16_round(rng.standard_normal((T, 16)))
-    fwd = O.layer_forward(inp, "sigmoid", 2, rnd=r, fp8=fp8, fold_gate=fold)
+    fwd = O.layer_forward(inp, "sigmoid", 2, rnd=r, fp8=fp8, fold_gate=fold, fp8_dgrad=f8d)
     bwd = O.layer_backward(inp, fwd, dY)
     for e in range(5):
         rows = np.arange(fwd["offsets"][e], fwd["offsets"][e + 1])
         toks = fwd["perm_token"][rows]
         gates = fwd["gate"][toks, fwd["perm_slot"][rows]]
         w = O.expert_weight_grads(inp, e, inp["x"][toks], gates, dY[toks], rnd=r, fp8=fp8,
-                                  fold_gate=fold)
+                                  fold_gate=fold, fp8_dgrad=f8d)
         for name in ("dW_g", "dW_u", "dW_d"):
             np.testing.assert_allclose(w[name], bwd[name][e], rtol=1e-11, atol=1e-13)
     units = [0, 2, 5]
-    w = O.shared_weight_grad_units(inp, dY, units, rnd=r, fp8=fp8)
+    w = O.shared_weight_grad_units(inp, dY, units, rnd=r, fp8=fp8, fp8_dgrad=f8d)
     np.testing.assert_allclose(w["dWs_g"], bwd["dWs_g"][units], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(w["dWs_u"], bwd["dWs_u"][units], rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(w["dWs_d"], bwd["dWs_d"][:, units], rtol=1e-11, atol=1e-13)
@@ -670,6 +675,90 @@ def test_fp8_expert_reduces_to_the_exact_expert_on_representable_operands():
     assert not np.array_equal(y8, y)  # h itself is not representable: its codes move y
     bound = (2.0 ** -4 * np.abs(h) + 2.0 ** -9 * np.abs(h).max(axis=1, keepdims=True) / 448) @ np.abs(Wd).T
     assert np.all(np.abs(y8 - y) <= bound * (1 + 1e-12))
+
+
+def test_fp8_data_gradients_are_exact_on_representable_operands():
+    """The FP8 data-gradient products reduce to the exact products when every operand row
+    (or column) is an E4M3 code times a scale that fp32 holds exactly.
+
+    dh = dy W_d: dy rows are 1.75 e_i (scale 2^-8, code 448); every row and column of W_d
+    holds +-1.75 among 0, +-0.25, +-0.5, +-1 (scale 2^-8 on either axis). dX = [da|du]
+    [W_g; W_u]: every da row holds 49/32 among 7/8, 7/16, 7/32 (joint scale 7/2048); du
+    rows hold 24 and 16 times 7/2048 (codes 24 and 16 under the joint scale, but 448 and
+    298.7 under a scale of their own); every column of W_g holds 1.75 and W_u only 0.75 and
+    0.5 (codes 192, 128 under the joint scale 2^-8, but 448 and 298.7 alone). So the joint
+    scales give the exact products and separate ones do not."""
+    rng = np.random.default_rng(51)
+    d, f, n = 8, 4, 3
+    vals = np.array([0.0, 0.25, -0.25, 0.5, -0.5, 1.0, -1.0])
+    W_d = rng.choice(vals, (d, f))
+    for i in range(d):
+        W_d[i, i % f] = 1.75 * (1 if i % 2 else -1)
+    for j in range(f):
+        W_d[j + 4, j] = -1.75  # every column too
+    dy = np.zeros((n, d))
+    dy[np.arange(n), [1, 4, 6]] = 1.75
+    np.testing.assert_array_equal(O.fp8_dgrad_dh(dy, W_d), dy @ W_d)
+    c = 7.0 / 2048
+    da = c * rng.choice([0.0, 256.0, -256.0, 128.0, 64.0], (n, f))
+    da[:, 0] = c * 448.0 * np.array([1, -1, 1])
+    du = c * rng.choice([16.0, -16.0], (n, f))
+    du[:, 1] = c * 24.0
+    W_g = rng.choice(vals, (f, d))
+    W_g[0, :] = 1.75
+    W_u = rng.choice([0.5, -0.5], (f, d))
+    W_u[2, :] = 0.75
+    np.testing.assert_array_equal(O.fp8_dgrad_dx(da, du, W_g, W_u), da @ W_g + du @ W_u)
+
+
+def test_fp8_data_gradient_scaling_axes():
+    """Scaling one row of the left operand, or one column of the right, by 4 scales that row
+    or column of the FP8 product by exactly 4 and leaves the rest bit for bit: the scales
+    run along the contraction axis of each operand (rows of dy and of [da|du]; columns of
+    W_d and of [W_g; W_u])."""
+    rng = np.random.default_rng(52)
+    n, d, f = 5, 16, 8
+    dy = O.bf16_round(rng.standard_normal((n, d)))
+    W_d = O.bf16_round(rng.standard_normal((d, f)))
+    base = O.fp8_dgrad_dh(dy, W_d)
+    dy2 = dy.copy(); dy2[2] *= 4
+    got = O.fp8_dgrad_dh(dy2, W_d)
+    np.testing.assert_array_equal(got[2], 4 * base[2])
+    np.testing.assert_array_equal(np.delete(got, 2, 0), np.delete(base, 2, 0))
+    W2 = W_d.copy(); W2[:, 5] *= 4
+    got = O.fp8_dgrad_dh(dy, W2)
+    np.testing.assert_array_equal(got[:, 5], 4 * base[:, 5])
+    np.testing.assert_array_equal(np.delete(got, 5, 1), np.delete(base, 5, 1))
+    da = O.bf16_round(rng.standard_normal((n, f)))
+    du = O.bf16_round(rng.standard_normal((n, f)))
+    W_g = O.bf16_round(rng.standard_normal((f, d)))
+    W_u = O.bf16_round(rng.standard_normal((f, d)))
+    base = O.fp8_dgrad_dx(da, du, W_g, W_u)
+    da2, du2 = da.copy(), du.copy(); da2[1] *= 4; du2[1] *= 4
+    got = O.fp8_dgrad_dx(da2, du2, W_g, W_u)
+    np.testing.assert_array_equal(got[1], 4 * base[1])
+    np.testing.assert_array_equal(np.delete(got, 1, 0), np.delete(base, 1, 0))
+    Wg2, Wu2 = W_g.copy(), W_u.copy(); Wg2[:, 3] *= 4; Wu2[:, 3] *= 4
+    got = O.fp8_dgrad_dx(da, du, Wg2, Wu2)
+    np.testing.assert_array_equal(got[:, 3], 4 * base[:, 3])
+    np.testing.assert_array_equal(np.delete(got, 3, 1), np.delete(base, 3, 1))
+
+
+def test_fp8_data_gradients_stay_close_to_the_bf16_backward():
+    """E4M3 keeps 4 significant bits: the FP8 data gradients move the expert's backward by a
+    few per cent of the gradient's scale, and leave the weight gradients' form alone."""
+    rng = np.random.default_rng(53)
+    inp = _tiny_inputs(rng, T=64, d=32, E=4, f=16, fs=8)
+    dY = O.bf16_round(rng.standard_normal((64, 32)))
+    f0 = O.layer_forward(inp, "sigmoid", 2, fp8=True)
+    f1 = O.layer_forward(inp, "sigmoid", 2, fp8=True, fp8_dgrad=True)
+    b0, b1 = O.layer_backward(inp, f0, dY), O.layer_backward(inp, f1, dY)
+    for name in ("dx", "dA", "dU", "dW_g", "dW_u", "dWs_g"):
+        rms = np.sqrt(np.mean(b0[name] ** 2))
+        err = np.sqrt(np.mean((b1[name] - b0[name]) ** 2))
+        assert 0 < err < 0.1 * rms, name
+    np.testing.assert_array_equal(b1["dW_d"], b0["dW_d"])  # dy and h do not change
+    np.testing.assert_array_equal(b1["dWs_d"], b0["dWs_d"])
 
 
 def test_fp8_expert_stays_close_to_bf16_expert():

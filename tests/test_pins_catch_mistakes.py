@@ -319,16 +319,33 @@ def _expert_weight_grads_ungated(inp, e, X, gates, *a, **kw):
     return ORIG["expert_weight_grads"](inp, e, X, np.ones_like(gates), *a, **kw)
 
 
-def _shared_units_dh_from_transposed_weight(inp, dY, units, rnd=None, fp8=False):
+def _shared_units_dh_from_transposed_weight(inp, dY, units, rnd=None, fp8=False, fp8_dgrad=False):
     wd = inp["Ws_d"]
     if wd.shape[0] != wd.shape[1]:
         wd = np.resize(wd.T, wd.shape)
-    return ORIG["shared_weight_grad_units"](dict(inp, Ws_d=wd), dY, units, rnd, fp8)
+    return ORIG["shared_weight_grad_units"](dict(inp, Ws_d=wd), dY, units, rnd, fp8, fp8_dgrad)
 
 
 def _layer_backward_subset_ignores_batch_count(inp, fwd, dY, T_norm=None, dl_extra=None,
                                                weight_grads=True):
     return ORIG["layer_backward"](inp, fwd, dY, None, dl_extra, weight_grads)
+
+
+def _dgrad_dh_weights_by_row(dy, W_d):
+    return O.fp8_dequant_rows(dy) @ O.fp8_dequant_rows(W_d)
+
+
+def _dgrad_dh_dy_by_column(dy, W_d):
+    return O.fp8_dequant_cols(dy) @ O.fp8_dequant_cols(W_d)
+
+
+def _dgrad_dx_separate_scales(da, du, W_g, W_u):
+    return (O.fp8_dequant_rows(da) @ O.fp8_dequant_cols(W_g) +
+            O.fp8_dequant_rows(du) @ O.fp8_dequant_cols(W_u))
+
+
+def _expert_bwd_fp8_dgrad_ignored(*a, fp8_dgrad=False, **kw):
+    return ORIG["expert_backward"](*a, **kw)
 
 
 MUTANTS = {
@@ -373,6 +390,10 @@ MUTANTS = {
     "whole expert weight gradients ignore the gates": ("expert_weight_grads", _expert_weight_grads_ungated),
     "shared-unit gradients through the wrong output weights": ("shared_weight_grad_units", _shared_units_dh_from_transposed_weight),
     "token-subset backward normalises the z-loss by the subset": ("layer_backward", _layer_backward_subset_ignores_batch_count),
+    "FP8 dgrad: W_d scaled per row instead of per column": ("fp8_dgrad_dh", _dgrad_dh_weights_by_row),
+    "FP8 dgrad: dy scaled per column instead of per row": ("fp8_dgrad_dh", _dgrad_dh_dy_by_column),
+    "FP8 dgrad: da and du scaled separately": ("fp8_dgrad_dx", _dgrad_dx_separate_scales),
+    "FP8 dgrad switch ignored by the expert backward": ("expert_backward", _expert_bwd_fp8_dgrad_ignored),
 }
 
 
