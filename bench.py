@@ -195,8 +195,10 @@ def oracle_pass_desc(cfg) -> str:
     if cfg.bias_update:
         parts.append("bias update")
     desc = "fp64 " + "+".join(parts)
-    if cfg.precision == "fp8":
+    if cfg.fp8:
         desc += ", FP8 (E4M3 rowwise) expert forward operands"
+    if cfg.fp8_dgrad:
+        desc += " and data-gradient operands"
     if cfg.has_aux:
         desc += ", both balancing losses (the sample as one sequence when shorter than one)"
     return desc
@@ -215,7 +217,7 @@ def cpu_oracle_rate(cfg, inp, T_s: int, steps: int = 1):
     for _ in range(steps):
         t0 = time.perf_counter()
         fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, aux=aux,
-                              fp8=cfg.precision == "fp8")
+                              fp8=cfg.fp8, fp8_dgrad=cfg.fp8_dgrad)
         if cfg.backward:
             O.layer_backward(i64, fwd, dY)
         if cfg.bias_update:
@@ -483,13 +485,17 @@ def main():
     gemm_tflops = gemm_flops / (gemm_ms / args.steps / 1e3) / 1e12
     peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
     peak_kind = f"{kind} bf16 sustained"
-    if cfg.precision == "fp8":
-        # forward GEMMs on E4M3 (a third of the FLOPs with backward) have twice the dense
-        # bf16 rate (4.5 vs 2.25 PFLOP/s nominal): the peak of the mix is the FLOP-weighted
-        # harmonic combination of the measured bf16 peak and twice it
-        f_fwd = gemm_flops / (3.0 if cfg.backward else 1.0)
-        peak_t = gemm_flops / (f_fwd / (2.0 * peak_t) + (gemm_flops - f_fwd) / peak_t)
-        peak_kind = f"{kind} bf16 sustained; fp8 forward at 2x (nominal ratio)"
+    if cfg.fp8:
+        # GEMMs on E4M3 have twice the dense bf16 rate (4.5 vs 2.25 PFLOP/s nominal): the
+        # forward GEMMs are a third of the FLOPs with backward, and the data-gradient GEMMs
+        # (fp8_dgrad) another third; the peak of the mix is the FLOP-weighted harmonic
+        # combination of the measured bf16 peak and twice it
+        f_fp8 = gemm_flops / (3.0 if cfg.backward else 1.0)
+        if cfg.fp8_dgrad and cfg.backward:
+            f_fp8 *= 2.0
+        peak_t = gemm_flops / (f_fp8 / (2.0 * peak_t) + (gemm_flops - f_fp8) / peak_t)
+        peak_kind = (f"{kind} bf16 sustained; fp8 forward"
+                     f"{' and data-gradient' if cfg.fp8_dgrad else ''} GEMMs at 2x (nominal ratio)")
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",

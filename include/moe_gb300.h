@@ -256,6 +256,63 @@ int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int64_t* row_of
                        moe_stream_t stream);
 
 /*
+ * moe_quantize_rows2_fp8 - moe_quantize_rows_fp8 of the concatenated rows [X0 | X1]: one
+ * scale per row over both halves, codes 2 cols bytes per row (X0's in the first half).
+ * Used for the expert input gradient's operand [dA | dU] of moe_expert_bwd_fp8, one product
+ * over K = 2f whose row scale must cover both halves.
+ * In : X0, X1 [rows, cols] bf16; rows_limit as in moe_quantize_rows_fp8.
+ * Out: Q [rows, 2 cols] E4M3 codes; scale [rows] fp32. cols % 128 == 0.
+ */
+int moe_quantize_rows2_fp8(const moe_bf16* X0, const moe_bf16* X1, const int64_t* rows_limit,
+                           int64_t rows, int cols, uint8_t* Q, float* scale, moe_stream_t stream);
+
+/*
+ * moe_quantize_cols_fp8 - columnwise FP8 (E4M3) quantisation of a weight operand whose
+ * contraction runs over its rows, written transposed so the GEMM reads it K-major.
+ * Reading (Apex-3 "fp8_rowwise" precision carried to the backward, as for
+ * moe_expert_bwd_fp8): each column n of each of the E matrices gets scale = fp32(amax/448)
+ * over its K values (1 for an all-zero column), codes E4M3(fp32(x / scale)) as in
+ * moe_quantize_rows_fp8, so Qt[e][n][k] is the code of X[e][k][n].
+ * In : X0 [E, K0, N] bf16; X1 [E, K0, N] bf16 or NULL: with X1 the matrices are the stacks
+ *      [X0[e]; X1[e]] of K = 2 K0 rows under one scale per column.
+ * Out: Qt [E, N, K] codes; scale [E N] fp32. K0 % 64 == 0, N % 64 == 0.
+ * W_d [E, d, f] -> (X0 = W_d, K0 = d, N = f): Wdq [E, f, d]; W_g, W_u [E, f, d] ->
+ * (X0 = W_g, X1 = W_u, K0 = f, N = d): Wguq [E, d, 2f].
+ */
+int moe_quantize_cols_fp8(const moe_bf16* X0, const moe_bf16* X1, int E, int K0, int N,
+                          uint8_t* Qt, float* scale, moe_stream_t stream);
+
+/*
+ * moe_expert_bwd_fp8 - moe_expert_bwd with the two data-gradient GEMMs on E4M3 operands
+ * (tcgen05 kind::f8f6f4, fp32 accumulation, scales applied in the epilogues); the weight
+ * gradients stay bf16 GEMMs of the stored bf16 tensors.
+ * Reading of the Apex-3 stack's fp8_rowwise precision ("The whole stack, in the open", "Run
+ * it yourself") for the backward, whose form the pages do not give: each data-gradient
+ * operand is scaled along the contraction axis, one scale per row of the left operand and
+ * per column of the right one:
+ *   r = dYq W_d: dy rows (moe_quantize_rows_fp8 of the expert-major upstream gradient) and
+ *       W_d columns (Wdq, sWd: moe_quantize_cols_fp8 of W_d); then the SwiGLU backward on
+ *       the stored bf16 a and u gives dA, dU (bf16);
+ *   dX = [dA | dU] [W_g; W_u] as one product over K = 2f: the rows of [dA | dU]
+ *       (moe_quantize_rows2_fp8, done here into AUq, sAU) and the columns of [W_g; W_u]
+ *       (Wguq, sWgu: moe_quantize_cols_fp8 of W_g over W_u);
+ *   dW_d = sum dY^T H, dW_g = sum dA^T X, dW_u = sum dU^T X as in moe_expert_bwd.
+ * In : dYq [rows, d] codes, sdY [rows]; dY [rows, d] bf16 (the same gradient, for dW_d);
+ *      X, A, U, H, row_offsets, E, rows, d, f as in moe_expert_bwd; Wdq [E, f, d], sWd [E f];
+ *      Wguq [E, d, 2f], sWgu [E d].
+ * Out: dX [rows, d], dA, dU [rows, f] bf16; AUq [rows, 2f] codes and sAU [rows] (the
+ *      quantised [dA | dU]); dW_g, dW_u [E, f, d], dW_d [E, d, f] bf16.
+ * The gate is not folded here (the FP8 layer combines with its gates); dY is g * dY[t].
+ */
+int moe_expert_bwd_fp8(const uint8_t* dYq, const float* sdY, const moe_bf16* dY,
+                       const moe_bf16* X, const moe_bf16* A, const moe_bf16* U,
+                       const moe_bf16* H, const int64_t* row_offsets, int E, int64_t rows, int d,
+                       int f, const uint8_t* Wdq, const float* sWd, const uint8_t* Wguq,
+                       const float* sWgu, moe_bf16* dX, moe_bf16* dA, moe_bf16* dU, uint8_t* AUq,
+                       float* sAU, moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_combine - gate-weighted sum of the expert outputs (C1).
  * Definition: out[t] = sum_{i<k} topk_gate[t,i] * Y_perm[slot_to_row[t,i]] + Y_shared[t],
  * summed in fp32 in slot order, shared term last, one bf16 rounding. Source: section 2.5

@@ -33,7 +33,17 @@ class MoEConfig:
     aux_switch: float = 0.0  # Switch-style load-balancing loss coefficient (0 = off)
     aux_seq: float = 0.0     # sequence-wise load-balancing loss coefficient (0 = off)
     seq_len: int = 0         # tokens per sequence for the sequence-wise loss
-    precision: str = "bf16"  # expert forward GEMM operands: "bf16" or "fp8" (E4M3 rowwise)
+    # expert GEMM operands: "bf16"; "fp8" (E4M3 rowwise forward GEMMs); "fp8_dgrad" (also the
+    # backward's data-gradient GEMMs on E4M3; weight gradients stay bf16)
+    precision: str = "bf16"
+
+    @property
+    def fp8(self) -> bool:
+        return self.precision in ("fp8", "fp8_dgrad")
+
+    @property
+    def fp8_dgrad(self) -> bool:
+        return self.precision == "fp8_dgrad"
 
     @property
     def has_aux(self) -> bool:
@@ -94,4 +104,9 @@ C6 = C4.with_(name="large_T65536_d4096_E64_k8_f1536_shared3072_auxlosses", aux_s
 # stack's fp8_rowwise precision); the backward stays bf16.
 C7 = C4.with_(name="large_T65536_d4096_E64_k8_f1536_shared3072_fp8fwd", precision="fp8")
 
-CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5, "C6": C6, "C7": C7}
+# The large layer with the data-gradient GEMMs of the backward on E4M3 operands as well (the
+# same fp8_rowwise precision carried to the backward; weight gradients stay bf16).
+C8 = C4.with_(name="large_T65536_d4096_E64_k8_f1536_shared3072_fp8dgrad", precision="fp8_dgrad")
+
+CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C3": C3, "C4": C4, "C5": C5, "C6": C6, "C7": C7,
+           "C8": C8}

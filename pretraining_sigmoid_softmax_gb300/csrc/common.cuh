@@ -24,7 +24,8 @@ bool device_supported();
 
 // Rowwise E4M3 quantisation of rows [0, min(rows, *limit)) of X (limit may be null); see fp8.cu.
 int launch_quantize_rows_fp8(const __nv_bfloat16* X, const int64_t* limit, int64_t rows, int cols,
-                             uint8_t* Q, float* S, cudaStream_t st);
+                             uint8_t* Q, float* S, cudaStream_t st,
+                             const __nv_bfloat16* X1 = nullptr);
 
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;

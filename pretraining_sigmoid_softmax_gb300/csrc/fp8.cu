@@ -18,51 +18,158 @@ namespace {
 
 constexpr int kQWarps = 8;
 
+// scale = RN(amax / 448) (1 for a zero amax) and its correctly rounded reciprocal.
+struct Fp8Scale {
+    float s, rs;
+    __device__ __forceinline__ explicit Fp8Scale(float amax) {
+        s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        rs = __frcp_rn(s);
+    }
+    __device__ __forceinline__ static Fp8Scale of(float scale) {  // a scale formed before
+        Fp8Scale f(0.f);
+        f.s = scale;
+        f.rs = __frcp_rn(scale);
+        return f;
+    }
+    __device__ __forceinline__ float quot(float x) const {  // RN(x / s)
+        const float q0 = __fmul_rn(x, rs);
+        const float e = __fmaf_rn(-q0, s, x);
+        return __fmaf_rn(e, rs, q0);
+    }
+};
+
+__device__ __forceinline__ float amax8(const uint4 v, float m) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+    return m;
+}
+
+// Eight bf16 values -> eight E4M3 codes.
+__device__ __forceinline__ uint2 codes8(const uint4 v, const Fp8Scale& sc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t packed[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const __nv_fp8x2_storage_t p0 = __nv_cvt_float2_to_fp8x2(
+            make_float2(sc.quot(bf16_lo(w[2 * h])), sc.quot(bf16_hi(w[2 * h]))), __NV_SATFINITE,
+            __NV_E4M3);
+        const __nv_fp8x2_storage_t p1 = __nv_cvt_float2_to_fp8x2(
+            make_float2(sc.quot(bf16_lo(w[2 * h + 1])), sc.quot(bf16_hi(w[2 * h + 1]))),
+            __NV_SATFINITE, __NV_E4M3);
+        packed[h] = (uint32_t)p0 | ((uint32_t)p1 << 16);
+    }
+    return make_uint2(packed[0], packed[1]);
+}
+
+// One warp per row. With X1, the row is the concatenation [X0 row | X1 row] (each `cols`
+// wide) under one scale, and its codes fill 2 cols bytes of Q.
 __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_fp8_kernel(
-    const __nv_bfloat16* __restrict__ X, const int64_t* __restrict__ limit, int64_t rows, int cols,
-    uint8_t* __restrict__ Q, float* __restrict__ S) {
+    const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ X1,
+    const int64_t* __restrict__ limit, int64_t rows, int cols, uint8_t* __restrict__ Q,
+    float* __restrict__ S) {
     const int lane = threadIdx.x % 32;
     const int64_t nwarps = (int64_t)gridDim.x * kQWarps;
     int64_t n = rows;
     if (limit) n = min(n, *limit);
     const int nvec = cols / 8;
+    const int64_t qcols = X1 ? 2 * (int64_t)cols : cols;
     for (int64_t r = (int64_t)blockIdx.x * kQWarps + threadIdx.x / 32; r < n; r += nwarps) {
         const uint4* src = reinterpret_cast<const uint4*>(X + r * cols);
+        const uint4* src1 = X1 ? reinterpret_cast<const uint4*>(X1 + r * cols) : nullptr;
         float m = 0.f;
         for (int c = lane; c < nvec; c += 32) {
-            const uint4 v = src[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+            m = amax8(src[c], m);
+            if (src1) m = amax8(src1[c], m);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float s = m > 0.f ? __fdiv_rn(m, 448.f) : 1.f;
-        const float rs = __frcp_rn(s);
-        auto quot = [s, rs](float x) {  // RN(x / s)
-            const float q0 = __fmul_rn(x, rs);
-            const float e = __fmaf_rn(-q0, s, x);
-            return __fmaf_rn(e, rs, q0);
-        };
-        uint2* dst = reinterpret_cast<uint2*>(Q + r * cols);
+        const Fp8Scale sc(m);
+        uint2* dst = reinterpret_cast<uint2*>(Q + r * qcols);
         for (int c = lane; c < nvec; c += 32) {
-            const uint4 v = src[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t packed[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const __nv_fp8x2_storage_t p0 = __nv_cvt_float2_to_fp8x2(
-                    make_float2(quot(bf16_lo(w[2 * h])), quot(bf16_hi(w[2 * h]))),
-                    __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8x2_storage_t p1 = __nv_cvt_float2_to_fp8x2(
-                    make_float2(quot(bf16_lo(w[2 * h + 1])), quot(bf16_hi(w[2 * h + 1]))),
-                    __NV_SATFINITE, __NV_E4M3);
-                packed[h] = (uint32_t)p0 | ((uint32_t)p1 << 16);
-            }
-            dst[c] = make_uint2(packed[0], packed[1]);
+            dst[c] = codes8(src[c], sc);
+            if (src1) dst[nvec + c] = codes8(src1[c], sc);
         }
-        if (lane == 0) S[r] = s;
+        if (lane == 0) S[r] = sc.s;
     }
+}
+
+// ------------------------------------------------ columnwise scales, transposed codes
+// X is E matrices of K x N bf16 (row-major), or, with X1, the K = 2 K0 stack of X0 over X1
+// (both E x K0 x N). Column n of matrix e gets scale RN(amax / 448) over its K values, and
+// its codes are written transposed, Qt[e][n][0..K), so that a GEMM contracting over K
+// reads them K-major.
+constexpr int kColThreads = 256;
+
+__global__ void __launch_bounds__(kColThreads) col_amax_kernel(
+    const __nv_bfloat16* __restrict__ X0, const __nv_bfloat16* __restrict__ X1, int K0, int N,
+    float* __restrict__ S) {
+    const int e = blockIdx.y;
+    const int n = blockIdx.x * kColThreads + threadIdx.x;
+    if (n >= N) return;
+    float m = 0.f;
+    for (int part = 0; part < (X1 ? 2 : 1); ++part) {
+        const __nv_bfloat16* src = (part ? X1 : X0) + (int64_t)e * K0 * N + n;
+        int k = 0;
+        for (; k + 4 <= K0; k += 4) {  // four independent loads in flight
+            const float a = fabsf(__bfloat162float(src[(int64_t)k * N]));
+            const float b = fabsf(__bfloat162float(src[(int64_t)(k + 1) * N]));
+            const float c = fabsf(__bfloat162float(src[(int64_t)(k + 2) * N]));
+            const float d = fabsf(__bfloat162float(src[(int64_t)(k + 3) * N]));
+            m = fmaxf(m, fmaxf(fmaxf(a, b), fmaxf(c, d)));
+        }
+        for (; k < K0; ++k) m = fmaxf(m, fabsf(__bfloat162float(src[(int64_t)k * N])));
+    }
+    S[(int64_t)e * N + n] = Fp8Scale(m).s;
+}
+
+// Tiles of 64 K-rows x 64 columns: read as bf16 rows, written as 64 code rows of 64 bytes.
+constexpr int kColTile = 64;
+
+__global__ void __launch_bounds__(kColThreads) col_quantize_kernel(
+    const __nv_bfloat16* __restrict__ X0, const __nv_bfloat16* __restrict__ X1, int K0, int N,
+    const float* __restrict__ S, uint8_t* __restrict__ Qt) {
+    __shared__ float tile[kColTile][kColTile + 1];
+    const int e = blockIdx.z;
+    const int n0 = blockIdx.x * kColTile;
+    const int k0 = blockIdx.y * kColTile;  // over K = K0 or 2 K0
+    const int K = X1 ? 2 * K0 : K0;
+    const int tid = threadIdx.x;
+    // load: 64 rows x 64 bf16 (8 vectors of 8 per row); 512 vectors, two per thread
+    for (int i = tid; i < kColTile * (kColTile / 8); i += kColThreads) {
+        const int r = i / (kColTile / 8), c8 = i % (kColTile / 8);
+        const int k = k0 + r;
+        const __nv_bfloat16* src = (k < K0 ? X0 + (int64_t)e * K0 * N + (int64_t)k * N
+                                           : X1 + (int64_t)e * K0 * N + (int64_t)(k - K0) * N) +
+                                   n0 + 8 * c8;
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            tile[r][8 * c8 + 2 * q] = bf16_lo(w[q]);
+            tile[r][8 * c8 + 2 * q + 1] = bf16_hi(w[q]);
+        }
+    }
+    __syncthreads();
+    // store: code row n (64 K values) in four 16-byte pieces, one per thread
+    const int nl = tid / 4, piece = tid % 4;
+    const Fp8Scale cs = Fp8Scale::of(S[(int64_t)e * N + n0 + nl]);
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kk = 16 * piece + 4 * q + 2 * h;
+            const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(
+                make_float2(cs.quot(tile[kk][nl]), cs.quot(tile[kk + 1][nl])), __NV_SATFINITE,
+                __NV_E4M3);
+            word |= (uint32_t)p << (16 * h);
+        }
+        out[q] = word;
+    }
+    uint8_t* dst = Qt + ((int64_t)e * N + n0 + nl) * K + k0 + 16 * piece;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // Rowwise codes are a function of the row alone, so the codes of a token's k expert-major
@@ -122,12 +229,23 @@ __global__ void __launch_bounds__(256) pad_rows_fp8_kernel(const int64_t* __rest
 }  // namespace
 
 int launch_quantize_rows_fp8(const __nv_bfloat16* X, const int64_t* limit, int64_t rows, int cols,
-                             uint8_t* Q, float* S, cudaStream_t st) {
+                             uint8_t* Q, float* S, cudaStream_t st, const __nv_bfloat16* X1) {
     int64_t blocks = cdiv(rows, kQWarps);
     const int64_t cap = (int64_t)sm_count() * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    quantize_rows_fp8_kernel<<<(unsigned)blocks, kQWarps * 32, 0, st>>>(X, limit, rows, cols, Q, S);
+    quantize_rows_fp8_kernel<<<(unsigned)blocks, kQWarps * 32, 0, st>>>(X, X1, limit, rows, cols,
+                                                                       Q, S);
+    return launch_status();
+}
+
+int launch_quantize_cols_fp8(const __nv_bfloat16* X0, const __nv_bfloat16* X1, int E, int K0,
+                             int N, uint8_t* Qt, float* S, cudaStream_t st) {
+    col_amax_kernel<<<dim3((unsigned)cdiv(N, kColThreads), (unsigned)E), kColThreads, 0, st>>>(
+        X0, X1, K0, N, S);
+    const int K = X1 ? 2 * K0 : K0;
+    col_quantize_kernel<<<dim3((unsigned)(N / kColTile), (unsigned)(K / kColTile), (unsigned)E),
+                          kColThreads, 0, st>>>(X0, X1, K0, N, S, Qt);
     return launch_status();
 }
 
@@ -143,7 +261,32 @@ extern "C" int moe_quantize_rows_fp8(const moe_bf16* X, const int64_t* rows_limi
     if (!aligned16(X) || !aligned16(Q)) return MOE_ERR_INVALID_ARG;
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     return launch_quantize_rows_fp8(reinterpret_cast<const __nv_bfloat16*>(X), rows_limit, rows,
-                                    cols, Q, scale, (cudaStream_t)stream);
+                                    cols, Q, scale, (cudaStream_t)stream, nullptr);
+}
+
+extern "C" int moe_quantize_rows2_fp8(const moe_bf16* X0, const moe_bf16* X1,
+                                      const int64_t* rows_limit, int64_t rows, int cols,
+                                      uint8_t* Q, float* scale, moe_stream_t stream) {
+    if (!X0 || !X1 || !Q || !scale) return MOE_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+    if (cols % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(X0) || !aligned16(X1) || !aligned16(Q)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    return launch_quantize_rows_fp8(reinterpret_cast<const __nv_bfloat16*>(X0), rows_limit, rows,
+                                    cols, Q, scale, (cudaStream_t)stream,
+                                    reinterpret_cast<const __nv_bfloat16*>(X1));
+}
+
+extern "C" int moe_quantize_cols_fp8(const moe_bf16* X0, const moe_bf16* X1, int E, int K0, int N,
+                                     uint8_t* Qt, float* scale, moe_stream_t stream) {
+    if (!X0 || !Qt || !scale) return MOE_ERR_INVALID_ARG;
+    if (E <= 0 || K0 <= 0 || N <= 0) return MOE_ERR_INVALID_ARG;
+    if (K0 % 64 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(X0) || (X1 && !aligned16(X1)) || !aligned16(Qt)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    return launch_quantize_cols_fp8(reinterpret_cast<const __nv_bfloat16*>(X0),
+                                    reinterpret_cast<const __nv_bfloat16*>(X1), E, K0, N, Qt,
+                                    scale, (cudaStream_t)stream);
 }
 
 extern "C" int moe_permute_fp8(const uint8_t* xq, const float* sx, const int32_t* slot_to_row,

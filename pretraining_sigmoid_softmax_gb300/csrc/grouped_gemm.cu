@@ -523,6 +523,12 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
         if (store) {  // lanes past an unpadded layout's end see zero-filled a, u and acc
             const uint8_t* abuf = S.au + ((size_t)slot * kAuBufs + b) * C::AU_BUF_BYTES;
             const uint8_t* ubuf = abuf + C::AU_BUF_BYTES / 2;
+            float accf[kAuCols];
+#pragma unroll
+            for (int j = 0; j < kAuCols; ++j) accf[j] = __uint_as_float(acc[j]);
+            // FP8 operands: the dequantised r = (dy codes) (W_d codes) * scale(row) * scale(col)
+            if constexpr (C::FP8)
+                fp8_scale<kAuCols>(accf, accf, P, ok_row ? row : ti.row_end - 1, ti, c, false);
 #pragma unroll
             for (int j = 0; j < kAuCols / 8; ++j) {
                 const uint4 a4 = *reinterpret_cast<const uint4*>(abuf + au_offset(lane, j));
@@ -533,7 +539,7 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
                 for (int h = 0; h < 8; ++h) {
                     const float a = (h & 1) ? bf16_hi(aw[h >> 1]) : bf16_lo(aw[h >> 1]);
                     const float u = (h & 1) ? bf16_hi(uw[h >> 1]) : bf16_lo(uw[h >> 1]);
-                    const float acc_h = __uint_as_float(acc[8 * j + h]);
+                    const float acc_h = accf[8 * j + h];
                     const float sa = 1.0f / (1.0f + __expf(-a));
                     if (P.gate_part) gpart = fmaf(acc_h, a * sa * u, gpart);
                     const float dh = acc_h * g;
@@ -917,6 +923,9 @@ using CfgWgradP = Cfg<256, true, true, false, kEpiStore, false, true, true>;
 using CfgG1P8 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false, true, true>;
 using CfgStoreKP8 = Cfg<256, false, false, false, kEpiStore, false, false, true, true>;
 using CfgStoreK8 = Cfg<128, false, false, false, kEpiStore, false, false, false, true>;
+// E4M3 data gradients (B2 on the upstream gradient's codes and W_d's transposed column codes)
+using CfgSwigluBwdP8 = Cfg<256, false, false, false, kEpiSwigluBwd, false, false, true, true>;
+using CfgSwigluBwd8 = Cfg<128, false, false, false, kEpiSwigluBwd, false, false, false, true>;
 
 Params base_params(const int64_t* row_offsets, int64_t rows, int E) {
     Params P{};
@@ -1000,6 +1009,11 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     return rc;
 }
 
+static int weight_grads(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* H,
+                        const moe_bf16* dA, const moe_bf16* dU, const int64_t* row_offsets, int E,
+                        int64_t rows, int d, int f, int32_t* order, moe_bf16* dW_g, moe_bf16* dW_u,
+                        moe_bf16* dW_d, cudaStream_t st);
+
 extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
                               const moe_bf16* U, const moe_bf16* H, const int64_t* row_offsets,
                               int E, int64_t rows, int d, int f, const moe_bf16* W_g,
@@ -1071,6 +1085,16 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
             rc = launch<CfgDgrad2<128>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 128), st, mox);
         if (rc != MOE_OK) return rc;
     }
+    return weight_grads(dY, X, H, dA, dU, row_offsets, E, rows, d, f, order, dW_g, dW_u, dW_d, st);
+}
+
+// B3 and B5, the weight gradients, from bf16 operands (shared by both expert backward
+// entry points): experts scheduled longest first.
+static int weight_grads(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* H,
+                        const moe_bf16* dA, const moe_bf16* dU, const int64_t* row_offsets, int E,
+                        int64_t rows, int d, int f, int32_t* order, moe_bf16* dW_g, moe_bf16* dW_u,
+                        moe_bf16* dW_d, cudaStream_t st) {
+    int rc;
     if (row_offsets) {
         expert_order_kernel<<<1, kMaxExperts, 0, st>>>(row_offsets, E, order);
         if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
@@ -1116,6 +1140,84 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
             rc = launch<CfgWgrad<128>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 128), st);
     }
     return rc;
+}
+
+extern "C" int moe_expert_bwd_fp8(const uint8_t* dYq, const float* sdY, const moe_bf16* dY,
+                                  const moe_bf16* X, const moe_bf16* A, const moe_bf16* U,
+                                  const moe_bf16* H, const int64_t* row_offsets, int E,
+                                  int64_t rows, int d, int f, const uint8_t* Wdq, const float* sWd,
+                                  const uint8_t* Wguq, const float* sWgu, moe_bf16* dX,
+                                  moe_bf16* dA, moe_bf16* dU, uint8_t* AUq, float* sAU,
+                                  moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+    if (!dYq || !sdY || !dY || !X || !A || !U || !H || !Wdq || !sWd || !Wguq || !sWgu || !dX ||
+        !dA || !dU || !AUq || !sAU || !dW_g || !dW_u || !dW_d)
+        return MOE_ERR_INVALID_ARG;
+    if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
+    const void* ptrs[14] = {dYq, dY, X, A, U, H, Wdq, Wguq, dX, dA, dU, AUq, dW_g, dW_u};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dW_d) || !aligned16(sWd) || !aligned16(sWgu)) return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    if (!device_status_word()) return MOE_ERR_LAUNCH;
+    WsCarver wc(ws, ws_bytes);
+    int32_t* order = wc.take<int32_t>(E + 1);
+    if (row_offsets && (!ws || !wc.ok())) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc;
+    // B2 on E4M3: r = (dy codes)(W_d column codes, transposed: [E f, d], K-major) times the
+    // row and column scales, then the SwiGLU backward on the staged bf16 a and u
+    {
+        constexpr CUtensorMapSwizzle kAuSwz = kAuCols == 32   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : kAuCols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                              : CU_TENSOR_MAP_SWIZZLE_NONE;
+        CUtensorMap mdy, mwd, msa, msu;
+        if (!make_map(&mdy, dYq, d, rows, 128, 128, true) ||
+            !make_map(&mwd, Wdq, d, (uint64_t)E * f, 128, 128, true) ||
+            !make_map(&msa, A, f, rows, kAuCols, 32, false, kAuSwz) ||
+            !make_map(&msu, U, f, rows, kAuCols, 32, false, kAuSwz))
+            return MOE_ERR_LAUNCH;
+        Params P = base_params(row_offsets, rows, E);
+        P.N = f;
+        P.K0 = d;
+        P.ld_out = f;
+        P.sa = sdY;
+        P.sb0 = sWd;
+        CUtensorMap mod[3];
+        if (!out_maps(mod, dA, dU, nullptr, f, rows)) return MOE_ERR_LAUNCH;
+        if (f % 256 == 0)
+            rc = launch<CfgSwigluBwdP8>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st, mod);
+        else
+            rc = launch<CfgSwigluBwd8>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 128), st, mod);
+        if (rc != MOE_OK) return rc;
+    }
+    // [dA | dU] rows -> E4M3 codes under one scale per row (2 f bytes per row)
+    rc = launch_quantize_rows_fp8(reinterpret_cast<const __nv_bfloat16*>(dA),
+                                  row_offsets ? row_offsets + E : nullptr, rows, f, AUq, sAU, st,
+                                  reinterpret_cast<const __nv_bfloat16*>(dU));
+    if (rc != MOE_OK) return rc;
+    // B4 on E4M3: dX = [dA | dU] codes ([rows, 2f]) x ([W_g; W_u] column codes, transposed:
+    // [E d, 2f], K-major), one product over K = 2f, times the row and column scales
+    {
+        CUtensorMap mau, mwgu;
+        if (!make_map(&mau, AUq, 2 * (uint64_t)f, rows, 128, 128, true) ||
+            !make_map(&mwgu, Wguq, 2 * (uint64_t)f, (uint64_t)E * d, 128, 128, true))
+            return MOE_ERR_LAUNCH;
+        Params P = base_params(row_offsets, rows, E);
+        P.N = d;
+        P.K0 = 2 * f;
+        P.sa = sAU;
+        P.sb0 = sWgu;
+        CUtensorMap mox[3];
+        if (!out_maps(mox, dX, nullptr, nullptr, d, rows)) return MOE_ERR_LAUNCH;
+        if (d % 256 == 0)
+            rc = launch<CfgStoreKP8>(mau, mau, mwgu, mwgu, P, token_tiles_max(rows, d, 256), st, mox);
+        else
+            rc = launch<CfgStoreK8>(mau, mau, mwgu, mwgu, P, token_tiles_max(rows, d, 128), st, mox);
+        if (rc != MOE_OK) return rc;
+    }
+    return weight_grads(dY, X, H, dA, dU, row_offsets, E, rows, d, f, order, dW_g, dW_u, dW_d, st);
 }
 
 extern "C" int moe_expert_fwd_fp8(const uint8_t* Xq, const float* sX, const int64_t* row_offsets,

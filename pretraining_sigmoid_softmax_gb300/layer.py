@@ -28,7 +28,8 @@ class MoEShape:
     aux_switch: float = 0.0
     aux_seq: float = 0.0
     seq_len: int = 0
-    fp8: bool = False
+    fp8: bool = False        # expert forward GEMMs on E4M3 operands
+    fp8_dgrad: bool = False  # and the expert backward's data-gradient GEMMs too
 
     @property
     def has_aux(self) -> bool:
@@ -37,7 +38,8 @@ class MoEShape:
     @classmethod
     def from_config(cls, cfg) -> "MoEShape":
         return cls(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_shared, cfg.mode_id, cfg.z_coef,
-                   cfg.aux_switch, cfg.aux_seq, cfg.seq_len or cfg.T, cfg.precision == "fp8")
+                   cfg.aux_switch, cfg.aux_seq, cfg.seq_len or cfg.T,
+                   cfg.precision in ("fp8", "fp8_dgrad"), cfg.precision == "fp8_dgrad")
 
 
 def _empty(shape, dtype, dev):
@@ -117,6 +119,18 @@ class MoEPlan:
             self.aux_loss = torch.zeros((2,), dtype=f32, device=dev)
             self.aux_f = _empty((E + (T // s.seq_len) * E,), f32, dev)
         self.has_backward = backward
+        if backward and s.fp8_dgrad:  # E4M3 operands of the data-gradient GEMMs
+            u8 = torch.uint8
+            self.dYq, self.sdY = _empty((R, d), u8, dev), _empty((R,), f32, dev)
+            self.AUq, self.sAU = _empty((R, 2 * f), u8, dev), _empty((R,), f32, dev)
+            self.Wdq_t, self.sWd_t = _empty((E, f, d), u8, dev), _empty((E * f,), f32, dev)
+            self.Wguq_t, self.sWgu_t = _empty((E, d, 2 * f), u8, dev), _empty((E * d,), f32, dev)
+            if fs:
+                self.dYsq, self.sdYs = _empty((T, d), u8, dev), _empty((T,), f32, dev)
+                self.AUsq, self.sAUs = _empty((T, 2 * fs), u8, dev), _empty((T,), f32, dev)
+                self.Wsdq_t, self.sWsd_t = _empty((1, fs, d), u8, dev), _empty((fs,), f32, dev)
+                self.Wsguq_t, self.sWsgu_t = (_empty((1, d, 2 * fs), u8, dev),
+                                              _empty((d,), f32, dev))
         if backward:
             if s.has_aux:
                 self.dlogits_aux = _empty((T, E), f32, dev)
@@ -178,7 +192,10 @@ class MoEPlan:
         if backward:
             n += 2                                          # combine backward + padding rows
             n += 1 if not s.fp8 else 0                      # gate gradient from its partials
-            n += 5 + (4 if s.f_shared else 0)               # expert backward (+ expert order)
+            if s.fp8_dgrad:  # quantise dY rows, W_d and W_g/W_u columns (2 each), B2,
+                n += 11 + (10 if s.f_shared else 0)         # [dA|dU] rows, B4, order, B3, B5
+            else:
+                n += 5 + (4 if s.f_shared else 0)           # expert backward (+ expert order)
             n += 3                                          # router backward
             if (s.mode == ops.MODE_SOFTMAX or s.has_aux) and s.E <= 128:
                 n += 3                                      # router dx: two splits + GEMM
@@ -273,9 +290,19 @@ class MoEPlan:
         else:
             ops.moe_combine_bwd(dY, self.Y_perm, self.topk_gate, self.slot_to_row,
                                 self.row_offsets, self.perm_token, self.dY_perm, self.dg, stream)
-            self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
-                       self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
-                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
+            if s.fp8_dgrad:
+                ops.moe_quantize_rows_fp8(self.dY_perm, self.row_offsets[s.E:], self.dYq, self.sdY,
+                                          stream)
+                ops.moe_quantize_cols_fp8(W_d, None, self.Wdq_t, self.sWd_t, stream)
+                ops.moe_quantize_cols_fp8(W_g, W_u, self.Wguq_t, self.sWgu_t, stream)
+                self._gemm(ops.moe_expert_bwd_fp8, self.dYq, self.sdY, self.dY_perm, self.X_perm,
+                           self.A, self.U, self.H, self.row_offsets, self.Wdq_t, self.sWd_t,
+                           self.Wguq_t, self.sWgu_t, self.dX_perm, self.dA, self.dU, self.AUq,
+                           self.sAU, self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
+            else:
+                self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
+                           self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
+                           self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
         dxs = None
         extra = None
         if s.has_aux:
@@ -302,6 +329,15 @@ class MoEPlan:
         return self.dx
 
     def _shared_backward(self, dY, x, Ws_g, Ws_u, Ws_d, st):
+        if self.s.fp8_dgrad:
+            ops.moe_quantize_rows_fp8(dY, None, self.dYsq, self.sdYs, st)
+            ops.moe_quantize_cols_fp8(Ws_d[None], None, self.Wsdq_t, self.sWsd_t, st)
+            ops.moe_quantize_cols_fp8(Ws_g[None], Ws_u[None], self.Wsguq_t, self.sWsgu_t, st)
+            self._gemm(ops.moe_expert_bwd_fp8, self.dYsq, self.sdYs, dY, x, self.As, self.Us,
+                       self.Hs, None, self.Wsdq_t, self.sWsd_t, self.Wsguq_t, self.sWsgu_t,
+                       self.dxs, self.dAs, self.dUs, self.AUsq, self.sAUs, self.dWs_g[None],
+                       self.dWs_u[None], self.dWs_d[None], self.ws_side, stream=st)
+            return
         self._gemm(ops.moe_expert_bwd, dY, x, self.As, self.Us, self.Hs, None, Ws_g[None],
                    Ws_u[None], Ws_d[None], self.dxs, self.dAs, self.dUs, self.dWs_g[None],
                    self.dWs_u[None], self.dWs_d[None], self.ws_side, stream=st)
@@ -396,14 +432,15 @@ class MoELayer(torch.nn.Module):
                  precision="bf16"):
         super().__init__()
         if mode not in ("sigmoid", "softmax") or bias_rule not in ("sign", "proportional") \
-                or precision not in ("bf16", "fp8"):
+                or precision not in ("bf16", "fp8", "fp8_dgrad"):
             raise ValueError("mode is sigmoid or softmax, bias_rule sign or proportional, "
-                             "precision bf16 or fp8")
+                             "precision bf16, fp8 or fp8_dgrad")
         self.d, self.E, self.k, self.f, self.f_shared = d, E, k, f, f_shared
         self.mode = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
         self.z_coef, self.gamma, self.bias_rule = z_coef, gamma, bias_rule
         self.aux_switch, self.aux_seq, self.seq_len = aux_switch, aux_seq, seq_len
-        self.fp8 = precision == "fp8"
+        self.fp8 = precision in ("fp8", "fp8_dgrad")
+        self.fp8_dgrad = precision == "fp8_dgrad"
         bf = dict(dtype=torch.bfloat16, device=device)
         self.W_r = torch.nn.Parameter(torch.randn(E, d, device=device) * d ** -0.5)
         self.register_buffer("b", torch.zeros(E, device=device))
@@ -423,7 +460,7 @@ class MoELayer(torch.nn.Module):
         if T not in self._plans:
             shape = MoEShape(T, self.d, self.E, self.k, self.f, self.f_shared, self.mode,
                              self.z_coef, self.aux_switch, self.aux_seq, self.seq_len or T,
-                             self.fp8)
+                             self.fp8, self.fp8_dgrad)
             plan = MoEPlan(shape, self.W_g.device)
             plan.generation = 0
             self._plans[T] = plan

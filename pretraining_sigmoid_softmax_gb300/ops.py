@@ -153,6 +153,25 @@ def moe_expert_fwd_fp8(Xq, sX, row_offsets, Wgq, sWg, Wuq, sWu, Wdq, sWd, A, U, 
            "moe_expert_fwd_fp8")
 
 
+def moe_quantize_rows2_fp8(X0, X1, rows_limit, Q, scale, stream=None):
+    """E4M3 codes of the rows [X0 | X1] under one scale per row: Q is [rows, 2 cols]."""
+    rows, cols = X0.shape
+    _contig(X0, X1, Q, scale)
+    _check(_lib.load().moe_quantize_rows2_fp8(_p(X0), _p(X1), _p(rows_limit), rows, cols, _p(Q),
+                                              _p(scale), _stream(stream)),
+           "moe_quantize_rows2_fp8")
+
+
+def moe_quantize_cols_fp8(X0, X1, Qt, scale, stream=None):
+    """Columnwise E4M3 codes of E matrices [K0, N] (X0, or the stack of X0 over X1), written
+    transposed: Qt [E, N, K] with K = K0 or 2 K0; scale [E N]."""
+    X0v = X0.reshape(-1, X0.shape[-2], X0.shape[-1])
+    E, K0, N = X0v.shape
+    _contig(X0, X1, Qt, scale)
+    _check(_lib.load().moe_quantize_cols_fp8(_p(X0), _p(X1), E, K0, N, _p(Qt), _p(scale),
+                                             _stream(stream)), "moe_quantize_cols_fp8")
+
+
 def moe_combine(Y_perm, topk_gate, slot_to_row, Y_shared, out, stream=None):
     """topk_gate None: the rows of Y_perm already carry their gates."""
     T, k = slot_to_row.shape
@@ -200,6 +219,21 @@ def moe_expert_bwd(dY, X, A, U, H, row_offsets, W_g, W_u, W_d, dX, dA, dU, dW_g,
                                       _p(dW_g), _p(dW_u), _p(dW_d), _p(row_gate), _p(gate_part),
                                       _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "moe_expert_bwd")
+
+
+def moe_expert_bwd_fp8(dYq, sdY, dY, X, A, U, H, row_offsets, Wdq, sWd, Wguq, sWgu, dX, dA, dU,
+                       AUq, sAU, dW_g, dW_u, dW_d, ws, stream=None):
+    """Wdq [E, f, d] and Wguq [E, d, 2f]: moe_quantize_cols_fp8 of W_d and of W_g over W_u."""
+    rows, d = X.shape
+    E, f, _ = Wdq.shape
+    _contig(dYq, sdY, dY, X, A, U, H, Wdq, sWd, Wguq, sWgu, dX, dA, dU, AUq, sAU, dW_g, dW_u,
+            dW_d, ws)
+    _check(_lib.load().moe_expert_bwd_fp8(_p(dYq), _p(sdY), _p(dY), _p(X), _p(A), _p(U), _p(H),
+                                          _p(row_offsets), E, rows, d, f, _p(Wdq), _p(sWd),
+                                          _p(Wguq), _p(sWgu), _p(dX), _p(dA), _p(dU), _p(AUq),
+                                          _p(sAU), _p(dW_g), _p(dW_u), _p(dW_d), _p(ws),
+                                          0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_expert_bwd_fp8")
 
 
 def moe_row_gates(topk_gate, slot_to_row, row_gate, stream=None):

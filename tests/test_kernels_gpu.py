@@ -718,3 +718,100 @@ def test_fp8_expert_forward_matches_oracle(counts, d, f):
         # tensor-core result of the oracle's own E4M3 operands, dequantised in the epilogue
         xq = O.fp8_dequant_rows(h64(X[lo:hi]))
         assert_gemm_exact(A[lo:hi], xq, O.fp8_dequant_rows(h64(W_g[e])).T, f"fp8 A exact e{e}")
+
+
+# ------------------------------------------------------ FP8 data gradients (backward)
+
+def test_fp8_columnwise_and_joint_row_codes_are_bit_exact():
+    """moe_quantize_cols_fp8 (one scale per column over the rows, codes transposed), also
+    over the stack of two matrices, and moe_quantize_rows2_fp8 (one scale per row over two
+    halves) give the oracle's codes and scales bit for bit."""
+    g = torch.Generator().manual_seed(71)
+    E, K0, N = 3, 192, 320
+    X0 = randn_bf16((E, K0, N), g) * torch.rand(1, 1, N, generator=g).mul(40).to(torch.bfloat16)
+    X1 = randn_bf16((E, K0, N), g) * 0.25
+    X0[1, :, 7] = 0  # an all-zero column: scale 1
+    for X1v, K in ((None, K0), (X1, 2 * K0)):
+        Qt = torch.full((E, N, K), 0x7F, dtype=torch.uint8, device="cuda")
+        S = torch.empty(E * N, device="cuda")
+        ops.moe_quantize_cols_fp8(dev(X0), None if X1v is None else dev(X1v), Qt, S)
+        torch.cuda.synchronize()
+        for e in range(E):
+            M = h64(X0[e]) if X1v is None else np.concatenate([h64(X0[e]), h64(X1v[e])], axis=0)
+            q_ref, s_ref = O.quantize_rows_fp8(M.T)  # columns of M as rows
+            assert np.array_equal(S[e * N:(e + 1) * N].cpu().numpy().view(np.uint32),
+                                  s_ref.astype(np.float32).view(np.uint32))
+            assert np.array_equal(_e4m3_values(Qt[e]), q_ref)
+    rows, cols = 300, 256
+    A = randn_bf16((rows, cols), g) * torch.rand(rows, 1, generator=g).mul(8).to(torch.bfloat16)
+    B = randn_bf16((rows, cols), g) * 0.1
+    B[5] = 30.0  # this row's amax comes from the second half
+    Q = torch.full((rows, 2 * cols), 0x7F, dtype=torch.uint8, device="cuda")
+    S = torch.empty(rows, device="cuda")
+    lim = torch.tensor([280], dtype=torch.int64, device="cuda")
+    ops.moe_quantize_rows2_fp8(dev(A), dev(B), lim, Q, S)
+    torch.cuda.synchronize()
+    q_ref, s_ref = O.quantize_rows_fp8(np.concatenate([h64(A), h64(B)], axis=1))
+    assert np.array_equal(S[:280].cpu().numpy().view(np.uint32),
+                          s_ref[:280].astype(np.float32).view(np.uint32))
+    assert np.array_equal(_e4m3_values(Q[:280]), q_ref[:280])
+    assert (Q[280:] == 0x7F).all()
+
+
+@pytest.mark.parametrize("counts,d,f", [(None, 512, 256), ([300, 0, 129, 1, 513], 512, 256),
+                                        ([130, 5, 0], 384, 128)])
+def test_fp8_expert_backward_matches_oracle(counts, d, f):
+    """moe_expert_bwd_fp8 on caller-made saved activations: dA and dU against the oracle's FP8
+    data gradient; dX as the exact tensor-core product of the oracle's own codes of the GPU's
+    [dA | dU] and of [W_g; W_u]; the bf16 weight gradients as before; empty experts zero."""
+    g = torch.Generator().manual_seed(73 + d)
+    if counts is None:
+        E, ro, rows, segs = 1, None, 600, [(0, 600)]
+    else:
+        E = len(counts)
+        ro = padded_offsets(counts)
+        rows = int(ro[-1]) + 128
+        segs = [(int(ro[e]), int(ro[e]) + counts[e]) for e in range(E)]
+    z = dict(dtype=torch.bfloat16)
+    X, dY = torch.zeros(rows, d, **z), torch.zeros(rows, d, **z)
+    A, U, H = (torch.zeros(rows, f, **z) for _ in range(3))
+    for lo, hi in segs:
+        for t, std in ((X, 1.0), (dY, 0.3), (A, 1.0), (U, 1.0), (H, 0.5)):
+            t[lo:hi] = randn_bf16((hi - lo, t.shape[1]), g, std)
+    W_g, W_u, W_d = _weights(E, d, f, g)
+    ro_d = None if ro is None else dev(torch.from_numpy(ro))
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    dYq, sdY = torch.empty(rows, d, **u8), torch.empty(rows, device="cuda")
+    ops.moe_quantize_rows_fp8(dev(dY), None if ro_d is None else ro_d[E:], dYq, sdY)
+    Wdq, sWd = torch.empty(E, f, d, **u8), torch.empty(E * f, device="cuda")
+    Wguq, sWgu = torch.empty(E, d, 2 * f, **u8), torch.empty(E * d, device="cuda")
+    ops.moe_quantize_cols_fp8(dev(W_d), None, Wdq, sWd)
+    ops.moe_quantize_cols_fp8(dev(W_g), dev(W_u), Wguq, sWgu)
+    B = _expert_buffers(rows, d, f, E)
+    AUq, sAU = torch.empty(rows, 2 * f, **u8), torch.empty(rows, device="cuda")
+    ops.moe_expert_bwd_fp8(dYq, sdY, dev(dY), dev(X), dev(A), dev(U), dev(H), ro_d, Wdq, sWd,
+                           Wguq, sWgu, B["dX"], B["dA"], B["dU"], AUq, sAU, B["dW_g"], B["dW_u"],
+                           B["dW_d"], _ws(rows, d, E, 1))
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    for e, (lo, hi) in enumerate(segs):
+        if hi == lo:
+            for nm in ("dW_g", "dW_u", "dW_d"):
+                assert (B[nm][e] == 0).all(), nm
+            continue
+        x, dy, a, u, h = (h64(t[lo:hi]) for t in (X, dY, A, U, H))
+        wg, wu, wd = h64(W_g[e]), h64(W_u[e]), h64(W_d[e])
+        r = O.fp8_dgrad_dh(dy, wd)
+        da, du = O.swiglu_backward(r, a, u)
+        assert_close(B["dA"][lo:hi], O.bf16_round(da), f"fp8 dA e{e}")
+        assert_close(B["dU"][lo:hi], O.bf16_round(du), f"fp8 dU e{e}")
+        # dX: the exact product of the codes of the GPU's own bf16 dA, dU and of the weights
+        dag, dug = h64(B["dA"][lo:hi]), h64(B["dU"][lo:hi])
+        AU = O.fp8_dequant_rows(np.concatenate([dag, dug], axis=1))
+        Wgu = O.fp8_dequant_cols(np.concatenate([wg, wu], axis=0))
+        assert_gemm_exact(B["dX"][lo:hi], AU, Wgu, f"fp8 dX exact e{e}")
+        ref = O.expert_backward(dy, x, a, u, h, wg, wu, wd, O.bf16_round, fp8_dgrad=True)
+        assert_close(B["dX"][lo:hi], ref["dX"], f"fp8 dX e{e}")
+        assert_gemm_exact(B["dW_d"][e], dy.T, h, f"dW_d exact e{e}")
+        assert_gemm_exact(B["dW_g"][e], dag.T, x, f"dW_g exact e{e}")
+        assert_gemm_exact(B["dW_u"][e], dug.T, x, f"dW_u exact e{e}")

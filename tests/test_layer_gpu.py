@@ -103,15 +103,16 @@ def full_parity(cfg, inp):
     record_near_ties(cfg.name, near, cfg.T)
     i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
     aux = _aux(cfg)
-    fp8 = cfg.precision == "fp8"
+    fp8, f8d = cfg.fp8, cfg.fp8_dgrad
     # gates of the GPU's fp32 logits: fp32-tight
     assert_close(plan.topk_gate, _replayed_gates(cfg, lg, idx, i64["b"])["gate"], "gates",
                  atol=1e-6, rtol=1e-5)
     # the plain definition and the bf16-storage model (the bf16 layer folds each slot's gate
     # into its expert: the stored h and y carry the gate)
-    P = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, aux=aux, fp8=fp8)
+    P = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, aux=aux, fp8=fp8,
+                        fp8_dgrad=f8d)
     S = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, rnd=RND, aux=aux, fp8=fp8,
-                        fold_gate=not fp8)
+                        fold_gate=not fp8, fp8_dgrad=f8d)
     case = cfg.name
     assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], P["X_perm"], "X_perm", 0, 0)
     check_plain(case, "logits", plan.logits, P["logits"], S["logits"])
@@ -169,6 +170,11 @@ SMALL = [
     MoEConfig("fp8_forward_softmax_ragged", T=777, d=256, E=5, k=2, f=128, f_shared=0,
               mode="softmax", seed=21, backward=True, bias_update=False, z_coef=1e-3,
               precision="fp8"),
+    MoEConfig("fp8_dgrad_shared", T=1024, d=512, E=8, k=2, f=256, f_shared=256,
+              mode="sigmoid", seed=24, backward=True, bias_update=True, precision="fp8_dgrad"),
+    MoEConfig("fp8_dgrad_softmax_ragged", T=777, d=384, E=5, k=2, f=128, f_shared=0,
+              mode="softmax", seed=25, backward=True, bias_update=False, z_coef=1e-3,
+              precision="fp8_dgrad"),
     # fewer tokens than one tile row block: 7-row tensors behind 32- and 128-row boxes
     MoEConfig("sub_tile_T7", T=7, d=128, E=4, k=2, f=128, f_shared=128, mode="sigmoid",
               seed=19, backward=True, bias_update=True),
@@ -213,7 +219,7 @@ SAMPLED_TOKENS = 2048
 SHARED_UNITS = 16
 
 
-@pytest.mark.parametrize("name", ["C3", "C4", "C5", "C6", "C7"])
+@pytest.mark.parametrize("name", ["C3", "C4", "C5", "C6", "C7", "C8"])
 def test_workload_sampled_parity(name):
     """Full-size workloads in the benchmark's launch configuration, against a stratified
     subset of the oracle: routing, counts and permutation in full; out, dx, the gate and
@@ -227,7 +233,7 @@ def test_workload_sampled_parity(name):
     idx, lg, D, rows, near = check_routing(cfg, inp, plan)
     record_near_ties(cfg.name, near, cfg.T)
     case = cfg.name
-    fp8 = cfg.precision == "fp8"
+    fp8, f8d = cfg.fp8, cfg.fp8_dgrad
     W64 = {k: O.to64(v) for k, v in inp.items() if k not in ("x", "dY")}
     x64, dY64 = O.to64(inp["x"]), O.to64(inp["dY"])
     lg64 = O.router_logits(x64, W64["W_r"])
@@ -247,9 +253,9 @@ def test_workload_sampled_parity(name):
     # routing; the z-loss mean and the balancing losses are the whole batch's
     part = dict(W64, x=x64[toks])
     P = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
-                        fp8=fp8)
+                        fp8=fp8, fp8_dgrad=f8d)
     S = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
-                        rnd=RND, fp8=fp8, fold_gate=not fp8)
+                        rnd=RND, fp8=fp8, fold_gate=not fp8, fp8_dgrad=f8d)
     flips = FP8_CODE_FLIPS if fp8 else 0.0
     check_plain(case, "gates", plan.topk_gate[tt], P["gate"], S["gate"])
     check_plain(case, "out", plan.out[tt], P["out"], S["out"])
@@ -272,9 +278,10 @@ def test_workload_sampled_parity(name):
         lo, hi = int(D["offsets"][e]), int(D["offsets"][e + 1])
         tok_e = D["perm_token"][lo:hi]
         gates = R["gate"][tok_e, D["perm_slot"][lo:hi]]
-        Pw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], fp8=fp8)
+        Pw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], fp8=fp8,
+                                   fp8_dgrad=f8d)
         Sw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], rnd=RND, fp8=fp8,
-                                   fold_gate=not fp8)
+                                   fold_gate=not fp8, fp8_dgrad=f8d)
         for nm in ("dW_g", "dW_u", "dW_d"):
             got = getattr(plan, nm)[e]
             check_plain(case, f"{nm}[{e}]", got, Pw[nm], Sw[nm])
@@ -287,8 +294,8 @@ def test_workload_sampled_parity(name):
     if cfg.f_shared:
         units = np.sort(rng.choice(cfg.f_shared, SHARED_UNITS, replace=False))
         sh = {"x": x64, "Ws_g": W64["Ws_g"], "Ws_u": W64["Ws_u"], "Ws_d": W64["Ws_d"]}
-        Pu = O.shared_weight_grad_units(sh, dY64, units, fp8=fp8)
-        Su = O.shared_weight_grad_units(sh, dY64, units, rnd=RND, fp8=fp8)
+        Pu = O.shared_weight_grad_units(sh, dY64, units, fp8=fp8, fp8_dgrad=f8d)
+        Su = O.shared_weight_grad_units(sh, dY64, units, rnd=RND, fp8=fp8, fp8_dgrad=f8d)
         ut = torch.from_numpy(units).cuda()
         for nm, got in (("dWs_g", plan.dWs_g[ut]), ("dWs_u", plan.dWs_u[ut]),
                         ("dWs_d", plan.dWs_d[:, ut])):

@@ -99,7 +99,7 @@ def test_cpu_baseline_times_the_workloads_own_layer(kw):
     rate, cores, times = bench.cpu_oracle_rate(cfg, make_inputs(cfg), 32)
     assert rate > 0 and cores >= 1 and len(times) == 1
     desc = bench.oracle_pass_desc(cfg)
-    assert ("FP8" in desc) == (cfg.precision == "fp8")
+    assert ("FP8" in desc) == cfg.fp8
     assert ("balancing" in desc) == cfg.has_aux
 
 
