@@ -366,6 +366,21 @@ int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm, const float* top
                     moe_bf16* dY_perm, float* dg, moe_stream_t stream);
 
 /*
+ * moe_combine_bwd_fp8 - moe_combine_bwd (with gates and the gate gradient) that also writes
+ * the E4M3 codes of every dY_perm row it stores, for moe_expert_bwd_fp8: dYq and sdY equal
+ * moe_quantize_rows_fp8 of dY_perm bit for bit (padding rows: zero codes, scale 1), without
+ * a second pass over dY_perm. A row is bf16(g * dY[t]) with g >= 0, a monotone function of
+ * dY[t], so its amax is bf16(g * amax|dY[t]|) and its scale is known before it is written.
+ * In / Out as moe_combine_bwd (Y_perm, topk_gate and dg required), plus dYq [padded rows, d]
+ * codes and sdY [padded rows] fp32.
+ */
+int moe_combine_bwd_fp8(const moe_bf16* dY, const moe_bf16* Y_perm, const float* topk_gate,
+                        const int32_t* slot_to_row, const int64_t* row_offsets,
+                        const int32_t* perm_token, int64_t T, int d, int E, int k,
+                        moe_bf16* dY_perm, float* dg, uint8_t* dYq, float* sdY,
+                        moe_stream_t stream);
+
+/*
  * moe_expert_bwd - backward of moe_expert_fwd (B2-B5) on tcgen05 tensor cores.
  * Definition, per row p of expert e, with dy = dY[p]:
  *   dh = dy W_d[e]; da = dh * u * s(a) * (1 + a (1 - s(a))); du = dh * silu(a);

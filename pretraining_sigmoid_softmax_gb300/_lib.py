@@ -43,6 +43,7 @@ PROTOTYPES = {
     "moe_bias_update": (_I, [_P, _I, _I64, _I, _F, _P, _P]),
     "moe_bias_update_proportional": (_I, [_P, _I, _I64, _I, _F, _P, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P]),
+    "moe_combine_bwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                             _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_row_gates": (_I, [_P, _P, _I64, _I, _I64, _P, _P]),

@@ -26,6 +26,9 @@ bool device_supported();
 int launch_quantize_rows_fp8(const __nv_bfloat16* X, const int64_t* limit, int64_t rows, int cols,
                              uint8_t* Q, float* S, cudaStream_t st,
                              const __nv_bfloat16* X1 = nullptr);
+// Padding rows of the expert-major layout (perm_token < 0) get zero codes and scale 1.
+int launch_pad_rows_fp8(const int64_t* row_offsets, const int32_t* perm_token, int d, int E,
+                        uint8_t* Xq, float* sX, cudaStream_t st);
 
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;

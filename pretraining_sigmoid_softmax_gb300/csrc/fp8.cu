@@ -11,56 +11,13 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "fp8.cuh"
 #include "sizes.h"
 
 namespace moe {
 namespace {
 
 constexpr int kQWarps = 8;
-
-// scale = RN(amax / 448) (1 for a zero amax) and its correctly rounded reciprocal.
-struct Fp8Scale {
-    float s, rs;
-    __device__ __forceinline__ explicit Fp8Scale(float amax) {
-        s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-        rs = __frcp_rn(s);
-    }
-    __device__ __forceinline__ static Fp8Scale of(float scale) {  // a scale formed before
-        Fp8Scale f(0.f);
-        f.s = scale;
-        f.rs = __frcp_rn(scale);
-        return f;
-    }
-    __device__ __forceinline__ float quot(float x) const {  // RN(x / s)
-        const float q0 = __fmul_rn(x, rs);
-        const float e = __fmaf_rn(-q0, s, x);
-        return __fmaf_rn(e, rs, q0);
-    }
-};
-
-__device__ __forceinline__ float amax8(const uint4 v, float m) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
-    return m;
-}
-
-// Eight bf16 values -> eight E4M3 codes.
-__device__ __forceinline__ uint2 codes8(const uint4 v, const Fp8Scale& sc) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t packed[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const __nv_fp8x2_storage_t p0 = __nv_cvt_float2_to_fp8x2(
-            make_float2(sc.quot(bf16_lo(w[2 * h])), sc.quot(bf16_hi(w[2 * h]))), __NV_SATFINITE,
-            __NV_E4M3);
-        const __nv_fp8x2_storage_t p1 = __nv_cvt_float2_to_fp8x2(
-            make_float2(sc.quot(bf16_lo(w[2 * h + 1])), sc.quot(bf16_hi(w[2 * h + 1]))),
-            __NV_SATFINITE, __NV_E4M3);
-        packed[h] = (uint32_t)p0 | ((uint32_t)p1 << 16);
-    }
-    return make_uint2(packed[0], packed[1]);
-}
 
 // One warp per row. With X1, the row is the concatenation [X0 row | X1 row] (each `cols`
 // wide) under one scale, and its codes fill 2 cols bytes of Q.
@@ -101,26 +58,54 @@ __global__ void __launch_bounds__(kQWarps * 32) quantize_rows_fp8_kernel(
 // reads them K-major.
 constexpr int kColThreads = 256;
 
-__global__ void __launch_bounds__(kColThreads) col_amax_kernel(
+// Column amax: thread = 8 adjacent columns (16-byte loads), block = kAmaxThreads threads x
+// kAmaxRows rows, so that even one small matrix fills the GPU. Block maxima meet by an
+// integer atomic max on the bits of non-negative floats, which order as the floats do (a
+// maximum does not depend on the order of its arguments). `bits` starts at zero.
+constexpr int kAmaxThreads = 128;
+constexpr int kAmaxRows = 256;
+
+__global__ void __launch_bounds__(kAmaxThreads) col_amax_kernel(
     const __nv_bfloat16* __restrict__ X0, const __nv_bfloat16* __restrict__ X1, int K0, int N,
-    float* __restrict__ S) {
+    unsigned int* __restrict__ bits) {
     const int e = blockIdx.y;
-    const int n = blockIdx.x * kColThreads + threadIdx.x;
-    if (n >= N) return;
-    float m = 0.f;
-    for (int part = 0; part < (X1 ? 2 : 1); ++part) {
-        const __nv_bfloat16* src = (part ? X1 : X0) + (int64_t)e * K0 * N + n;
-        int k = 0;
-        for (; k + 4 <= K0; k += 4) {  // four independent loads in flight
-            const float a = fabsf(__bfloat162float(src[(int64_t)k * N]));
-            const float b = fabsf(__bfloat162float(src[(int64_t)(k + 1) * N]));
-            const float c = fabsf(__bfloat162float(src[(int64_t)(k + 2) * N]));
-            const float d = fabsf(__bfloat162float(src[(int64_t)(k + 3) * N]));
-            m = fmaxf(m, fmaxf(fmaxf(a, b), fmaxf(c, d)));
+    const int K = X1 ? 2 * K0 : K0;
+    const int c = (blockIdx.x * kAmaxThreads + threadIdx.x) * 8;
+    if (c >= N) return;
+    const int r0 = blockIdx.z * kAmaxRows;
+    const int r1 = min(K, r0 + kAmaxRows);
+    auto row = [&](int r) {
+        return reinterpret_cast<const uint4*>(
+            (r < K0 ? X0 + ((int64_t)e * K0 + r) * N : X1 + ((int64_t)e * K0 + (r - K0)) * N) + c);
+    };
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = 0.f;
+    auto fold = [&](const uint4 v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            m[2 * q] = fmaxf(m[2 * q], fabsf(bf16_lo(w[q])));
+            m[2 * q + 1] = fmaxf(m[2 * q + 1], fabsf(bf16_hi(w[q])));
         }
-        for (; k < K0; ++k) m = fmaxf(m, fabsf(__bfloat162float(src[(int64_t)k * N])));
+    };
+    int r = r0;
+    for (; r + 4 <= r1; r += 4) {  // four rows in flight
+        const uint4 v0 = *row(r), v1 = *row(r + 1), v2 = *row(r + 2), v3 = *row(r + 3);
+        fold(v0);
+        fold(v1);
+        fold(v2);
+        fold(v3);
     }
-    S[(int64_t)e * N + n] = Fp8Scale(m).s;
+    for (; r < r1; ++r) fold(*row(r));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) atomicMax(bits + (int64_t)e * N + c + j, __float_as_uint(m[j]));
+}
+
+// amax (as bits) -> scale, in place.
+__global__ void col_scale_kernel(float* __restrict__ S, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) S[i] = Fp8Scale(S[i]).s;
 }
 
 // Tiles of 64 K-rows x 64 columns: read as bf16 rows, written as 64 code rows of 64 bytes.
@@ -239,11 +224,20 @@ int launch_quantize_rows_fp8(const __nv_bfloat16* X, const int64_t* limit, int64
     return launch_status();
 }
 
+int launch_pad_rows_fp8(const int64_t* row_offsets, const int32_t* perm_token, int d, int E,
+                        uint8_t* Xq, float* sX, cudaStream_t st) {
+    pad_rows_fp8_kernel<<<dim3(E, kPadSplitFp8), 256, 0, st>>>(row_offsets, perm_token, d, Xq, sX);
+    return launch_status();
+}
+
 int launch_quantize_cols_fp8(const __nv_bfloat16* X0, const __nv_bfloat16* X1, int E, int K0,
                              int N, uint8_t* Qt, float* S, cudaStream_t st) {
-    col_amax_kernel<<<dim3((unsigned)cdiv(N, kColThreads), (unsigned)E), kColThreads, 0, st>>>(
-        X0, X1, K0, N, S);
     const int K = X1 ? 2 * K0 : K0;
+    if (cudaMemsetAsync(S, 0, sizeof(float) * (size_t)E * N, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+    col_amax_kernel<<<dim3((unsigned)cdiv(N, 8 * kAmaxThreads), (unsigned)E,
+                           (unsigned)cdiv(K, kAmaxRows)),
+                      kAmaxThreads, 0, st>>>(X0, X1, K0, N, reinterpret_cast<unsigned int*>(S));
+    col_scale_kernel<<<(unsigned)cdiv((int64_t)E * N, 256), 256, 0, st>>>(S, (int64_t)E * N);
     col_quantize_kernel<<<dim3((unsigned)(N / kColTile), (unsigned)(K / kColTile), (unsigned)E),
                           kColThreads, 0, st>>>(X0, X1, K0, N, S, Qt);
     return launch_status();

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "fp8.cuh"
 #include "sizes.h"
 
 namespace moe {
@@ -271,11 +272,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 
 // dY_perm[row(t,i)] = bf16(g[t,i] * dY[t]); dg[t,i] = <dY[t], Y_perm[row(t,i)]>. Without
 // gates the rows are plain copies of dY[t]; without Y_perm no dg is formed.
-template <int KMAX>
+// CODES: also the E4M3 codes and scale of every written row, equal to what
+// moe_quantize_rows_fp8 of dY_perm gives: each row is bf16(g dY[t]), a monotone function of
+// dY[t] for g >= 0, so its amax is bf16(g amax|dY[t]|), known before the row is written.
+template <int KMAX, bool CODES = false>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ Y_perm,
     const float* __restrict__ gate, const int32_t* __restrict__ slot_to_row, int64_t T, int d,
-    int k, __nv_bfloat16* __restrict__ dY_perm, float* __restrict__ dg) {
+    int k, __nv_bfloat16* __restrict__ dY_perm, float* __restrict__ dg,
+    uint8_t* __restrict__ dYq = nullptr, float* __restrict__ sdY = nullptr) {
     const int lane = threadIdx.x % 32;
     const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
     if (t >= T) return;
@@ -284,6 +289,20 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
     if (lane < k) {
         my_row = slot_to_row[t * k + lane];
         my_g = gate ? gate[t * k + lane] : 1.0f;
+    }
+    float sc_s[CODES ? KMAX : 1], sc_rs[CODES ? KMAX : 1];  // each slot row's scale
+    if constexpr (CODES) {
+        float m = 0.f;
+        for (int c = lane; c < d / 8; c += 32) m = amax8(reinterpret_cast<const uint4*>(dY + t * d)[c], m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const Fp8Scale sc(__bfloat162float(__float2bfloat16_rn(my_g * m)));
+        if (lane < k && my_row >= 0) sdY[my_row] = sc.s;
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+            sc_s[i] = __shfl_sync(0xffffffffu, sc.s, i);
+            sc_rs[i] = __shfl_sync(0xffffffffu, sc.rs, i);
+        }
     }
     float dot[KMAX];
 #pragma unroll
@@ -322,6 +341,13 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
 #pragma unroll
                     for (int q = 0; q < 8; ++q) o[q] = g * dyf[q];
                     reinterpret_cast<uint4*>(dY_perm + (int64_t)row * d)[c] = pack8(o);
+                    if constexpr (CODES) {  // the codes of the bf16 values just stored
+                        Fp8Scale sc = Fp8Scale::of(sc_s[i]);
+                        sc.rs = sc_rs[i];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) o[q] = __bfloat162float(__float2bfloat16_rn(o[q]));
+                        reinterpret_cast<uint2*>(dYq + (int64_t)row * d)[c] = codes8f(o, sc);
+                    }
                 }
             }
         }
@@ -574,6 +600,35 @@ extern "C" int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm,
     else if (k <= 16) combine_bwd_kernel<16><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
     else combine_bwd_kernel<32><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
     zero_pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    return launch_status();
+}
+
+extern "C" int moe_combine_bwd_fp8(const moe_bf16* dY, const moe_bf16* Y_perm,
+                                   const float* topk_gate, const int32_t* slot_to_row,
+                                   const int64_t* row_offsets, const int32_t* perm_token,
+                                   int64_t T, int d, int E, int k, moe_bf16* dY_perm, float* dg,
+                                   uint8_t* dYq, float* sdY, moe_stream_t stream) {
+    if (!dY || !Y_perm || !topk_gate || !slot_to_row || !row_offsets || !perm_token ||
+        !dY_perm || !dg || !dYq || !sdY)
+        return MOE_ERR_INVALID_ARG;
+    if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(dY) || !aligned16(Y_perm) || !aligned16(dY_perm) || !aligned16(dYq))
+        return MOE_ERR_INVALID_ARG;
+    if (!device_supported()) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const __nv_bfloat16* dYb = reinterpret_cast<const __nv_bfloat16*>(dY);
+    const __nv_bfloat16* Yb = reinterpret_cast<const __nv_bfloat16*>(Y_perm);
+    __nv_bfloat16* dYp = reinterpret_cast<__nv_bfloat16*>(dY_perm);
+    const unsigned g = warp_grid(T);
+    if (k <= 2) combine_bwd_kernel<2, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
+    else if (k <= 4) combine_bwd_kernel<4, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
+    else if (k <= 8) combine_bwd_kernel<8, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
+    else if (k <= 16) combine_bwd_kernel<16, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
+    else combine_bwd_kernel<32, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
+    zero_pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    if (launch_pad_rows_fp8(row_offsets, perm_token, d, E, dYq, sdY, st) != MOE_OK)
+        return MOE_ERR_LAUNCH;
     return launch_status();
 }
 

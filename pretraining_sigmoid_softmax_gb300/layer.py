@@ -192,8 +192,9 @@ class MoEPlan:
         if backward:
             n += 2                                          # combine backward + padding rows
             n += 1 if not s.fp8 else 0                      # gate gradient from its partials
-            if s.fp8_dgrad:  # quantise dY rows, W_d and W_g/W_u columns (2 each), B2,
-                n += 11 + (10 if s.f_shared else 0)         # [dA|dU] rows, B4, order, B3, B5
+            if s.fp8_dgrad:  # pad the dY codes, W_d and W_g/W_u columns (3 each), B2,
+                n += 13 + (12 if s.f_shared else 0)         # [dA|dU] rows, B4, order, B3, B5
+                                                            # (shared: quantise dY rows)
             else:
                 n += 5 + (4 if s.f_shared else 0)           # expert backward (+ expert order)
             n += 3                                          # router backward
@@ -287,22 +288,22 @@ class MoEPlan:
                        self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
                        row_gate=self.row_gate, gate_part=self.gate_part)
             ops.moe_gate_grad(self.gate_part, self.slot_to_row, s.f, self.dg, stream)
+        elif s.fp8_dgrad:  # the combine backward also writes the codes of the rows it stores
+            ops.moe_combine_bwd_fp8(dY, self.Y_perm, self.topk_gate, self.slot_to_row,
+                                    self.row_offsets, self.perm_token, self.dY_perm, self.dg,
+                                    self.dYq, self.sdY, stream)
+            ops.moe_quantize_cols_fp8(W_d, None, self.Wdq_t, self.sWd_t, stream)
+            ops.moe_quantize_cols_fp8(W_g, W_u, self.Wguq_t, self.sWgu_t, stream)
+            self._gemm(ops.moe_expert_bwd_fp8, self.dYq, self.sdY, self.dY_perm, self.X_perm,
+                       self.A, self.U, self.H, self.row_offsets, self.Wdq_t, self.sWd_t,
+                       self.Wguq_t, self.sWgu_t, self.dX_perm, self.dA, self.dU, self.AUq,
+                       self.sAU, self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
         else:
             ops.moe_combine_bwd(dY, self.Y_perm, self.topk_gate, self.slot_to_row,
                                 self.row_offsets, self.perm_token, self.dY_perm, self.dg, stream)
-            if s.fp8_dgrad:
-                ops.moe_quantize_rows_fp8(self.dY_perm, self.row_offsets[s.E:], self.dYq, self.sdY,
-                                          stream)
-                ops.moe_quantize_cols_fp8(W_d, None, self.Wdq_t, self.sWd_t, stream)
-                ops.moe_quantize_cols_fp8(W_g, W_u, self.Wguq_t, self.sWgu_t, stream)
-                self._gemm(ops.moe_expert_bwd_fp8, self.dYq, self.sdY, self.dY_perm, self.X_perm,
-                           self.A, self.U, self.H, self.row_offsets, self.Wdq_t, self.sWd_t,
-                           self.Wguq_t, self.sWgu_t, self.dX_perm, self.dA, self.dU, self.AUq,
-                           self.sAU, self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
-            else:
-                self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
-                           self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
-                           self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
+            self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
+                       self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
+                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
         dxs = None
         extra = None
         if s.has_aux:

@@ -236,6 +236,19 @@ def moe_expert_bwd_fp8(dYq, sdY, dY, X, A, U, H, row_offsets, Wdq, sWd, Wguq, sW
            "moe_expert_bwd_fp8")
 
 
+def moe_combine_bwd_fp8(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm,
+                        dg, dYq, sdY, stream=None):
+    """moe_combine_bwd plus the E4M3 codes and scales of the dY_perm rows."""
+    T, k = slot_to_row.shape
+    d = dY.shape[1]
+    E = row_offsets.shape[0] - 1
+    _contig(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token, dY_perm, dg, dYq, sdY)
+    _check(_lib.load().moe_combine_bwd_fp8(_p(dY), _p(Y_perm), _p(topk_gate), _p(slot_to_row),
+                                           _p(row_offsets), _p(perm_token), T, d, E, k,
+                                           _p(dY_perm), _p(dg), _p(dYq), _p(sdY),
+                                           _stream(stream)), "moe_combine_bwd_fp8")
+
+
 def moe_row_gates(topk_gate, slot_to_row, row_gate, stream=None):
     T, k = topk_gate.shape
     _contig(topk_gate, slot_to_row, row_gate)

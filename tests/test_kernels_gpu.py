@@ -815,3 +815,36 @@ def test_fp8_expert_backward_matches_oracle(counts, d, f):
         assert_gemm_exact(B["dW_d"][e], dy.T, h, f"dW_d exact e{e}")
         assert_gemm_exact(B["dW_g"][e], dag.T, x, f"dW_g exact e{e}")
         assert_gemm_exact(B["dW_u"][e], dug.T, x, f"dW_u exact e{e}")
+
+
+def test_combine_backward_with_fp8_codes():
+    """moe_combine_bwd_fp8 gives moe_combine_bwd's dY_perm and dg bit for bit, and the codes
+    and scales of moe_quantize_rows_fp8 of that dY_perm (padding rows: zero codes, scale 1),
+    including a token whose gradient row is zero and a gate of zero."""
+    g = torch.Generator().manual_seed(75)
+    T, d, E, k = 900, 384, 12, 4
+    idx = _random_choice(T, E, k, g, skew=True)
+    P = _permute(idx, randn_bf16((T, d), g), E)
+    R = P["X_perm"].shape[0]
+    Y_perm = randn_bf16((R, d), g)
+    gate = torch.rand(T, k, generator=g)
+    gate[3, 1] = 0.0
+    dY = randn_bf16((T, d), g) * torch.rand(T, 1, generator=g).mul(20).to(torch.bfloat16)
+    dY[5] = 0
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    a_dYp, b_dYp = torch.full((R, d), float("nan"), **bf), torch.full((R, d), float("nan"), **bf)
+    a_dg, b_dg = torch.empty(T, k, device="cuda"), torch.empty(T, k, device="cuda")
+    ops.moe_combine_bwd(dev(dY), dev(Y_perm), dev(gate), P["slot_to_row"], P["row_offsets"],
+                        P["perm_token"], a_dYp, a_dg)
+    q = torch.full((R, d), 0x7F, dtype=torch.uint8, device="cuda")
+    sq = torch.full((R,), float("nan"), device="cuda")
+    ops.moe_combine_bwd_fp8(dev(dY), dev(Y_perm), dev(gate), P["slot_to_row"], P["row_offsets"],
+                            P["perm_token"], b_dYp, b_dg, q, sq)
+    n = int(P["row_offsets"][-1])
+    q_ref = torch.empty(R, d, dtype=torch.uint8, device="cuda")
+    s_ref = torch.empty(R, device="cuda")
+    ops.moe_quantize_rows_fp8(a_dYp, P["row_offsets"][E:], q_ref, s_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(a_dYp[:n], b_dYp[:n]) and torch.equal(a_dg, b_dg)
+    assert torch.equal(q[:n], q_ref[:n])
+    assert torch.equal(sq[:n], s_ref[:n])
