@@ -8,6 +8,8 @@ reports the elements outside it per tensor (``check_plain``). A second check hol
 kernels' arithmetic to the oracle's bf16-storage model (the tensors the workloads store in
 bf16 rounded where they are stored), which is tighter on everything but the sums over tokens.
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -87,6 +89,14 @@ def dlogits_atol(bwd):
     return 2.0 * 1e-2 * max(1.0, float(np.sqrt(np.mean(dg * dg)))) if dg.size else 1e-2
 
 
+def both(plain, storage):
+    """The plain-definition and bf16-storage oracle evaluations side by side in two threads
+    (numpy's elementwise work releases the GIL); returns their results in that order."""
+    with ThreadPoolExecutor(2) as ex:
+        a, b = ex.submit(plain), ex.submit(storage)
+        return a.result(), b.result()
+
+
 def _aux(cfg):
     return (cfg.seq_len or cfg.T, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
 
@@ -109,10 +119,14 @@ def full_parity(cfg, inp):
                  atol=1e-6, rtol=1e-5)
     # the plain definition and the bf16-storage model (the bf16 layer folds each slot's gate
     # into its expert: the stored h and y carry the gate)
-    P = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, aux=aux, fp8=fp8,
-                        fp8_dgrad=f8d)
-    S = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, rnd=RND, aux=aux, fp8=fp8,
-                        fold_gate=not fp8, fp8_dgrad=f8d)
+    dY = O.to64(inp["dY"]) if cfg.backward else None
+
+    def run(**kw):
+        fwd = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, aux=aux, fp8=fp8,
+                              fp8_dgrad=f8d, **kw)
+        return fwd, (O.layer_backward(i64, fwd, dY) if cfg.backward else None)
+
+    (P, PB), (S, SB) = both(lambda: run(), lambda: run(rnd=RND, fold_gate=not fp8))
     case = cfg.name
     assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], P["X_perm"], "X_perm", 0, 0)
     check_plain(case, "logits", plan.logits, P["logits"], S["logits"])
@@ -128,9 +142,6 @@ def full_parity(cfg, inp):
         assert float(plan.z_loss[0]) == pytest.approx(P["z_loss"], rel=1e-4)
     if not cfg.backward:
         return
-    dY = O.to64(inp["dY"])
-    PB = O.layer_backward(i64, P, dY)
-    SB = O.layer_backward(i64, S, dY)
     names = ["dx", "dg", "dlogits", "dW_r", "dW_g", "dW_u", "dW_d"]
     if cfg.f_shared:
         names += ["dWs_g", "dWs_u", "dWs_d"]
@@ -252,16 +263,18 @@ def test_workload_sampled_parity(name):
     # the layer over the sampled tokens: each token's out and dx depend only on its own
     # routing; the z-loss mean and the balancing losses are the whole batch's
     part = dict(W64, x=x64[toks])
-    P = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
-                        fp8=fp8, fp8_dgrad=f8d)
-    S = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
-                        rnd=RND, fp8=fp8, fold_gate=not fp8, fp8_dgrad=f8d)
+
+    def run(**kw):
+        fwd = O.layer_forward(part, cfg.mode, cfg.k, cfg.z_coef, logits=lg64[toks], idx=idx[toks],
+                              fp8=fp8, fp8_dgrad=f8d, **kw)
+        return fwd, O.layer_backward(part, fwd, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux,
+                                     weight_grads=False)
+
+    (P, PB), (S, SB) = both(lambda: run(), lambda: run(rnd=RND, fold_gate=not fp8))
     flips = FP8_CODE_FLIPS if fp8 else 0.0
     check_plain(case, "gates", plan.topk_gate[tt], P["gate"], S["gate"])
     check_plain(case, "out", plan.out[tt], P["out"], S["out"])
     assert_close(plan.out[tt], S["out"], "out", allow_frac=flips)
-    PB = O.layer_backward(part, P, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux, weight_grads=False)
-    SB = O.layer_backward(part, S, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux, weight_grads=False)
     for nm in ("dx", "dg", "dlogits"):
         got = getattr(plan, nm)[tt]
         check_plain(case, nm, got, PB[nm], SB[nm])
@@ -278,10 +291,11 @@ def test_workload_sampled_parity(name):
         lo, hi = int(D["offsets"][e]), int(D["offsets"][e + 1])
         tok_e = D["perm_token"][lo:hi]
         gates = R["gate"][tok_e, D["perm_slot"][lo:hi]]
-        Pw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], fp8=fp8,
-                                   fp8_dgrad=f8d)
-        Sw = O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], rnd=RND, fp8=fp8,
-                                   fold_gate=not fp8, fp8_dgrad=f8d)
+        Pw, Sw = both(
+            lambda: O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], fp8=fp8,
+                                          fp8_dgrad=f8d),
+            lambda: O.expert_weight_grads(W64, e, x64[tok_e], gates, dY64[tok_e], rnd=RND,
+                                          fp8=fp8, fold_gate=not fp8, fp8_dgrad=f8d))
         for nm in ("dW_g", "dW_u", "dW_d"):
             got = getattr(plan, nm)[e]
             check_plain(case, f"{nm}[{e}]", got, Pw[nm], Sw[nm])
@@ -294,8 +308,9 @@ def test_workload_sampled_parity(name):
     if cfg.f_shared:
         units = np.sort(rng.choice(cfg.f_shared, SHARED_UNITS, replace=False))
         sh = {"x": x64, "Ws_g": W64["Ws_g"], "Ws_u": W64["Ws_u"], "Ws_d": W64["Ws_d"]}
-        Pu = O.shared_weight_grad_units(sh, dY64, units, fp8=fp8, fp8_dgrad=f8d)
-        Su = O.shared_weight_grad_units(sh, dY64, units, rnd=RND, fp8=fp8, fp8_dgrad=f8d)
+        Pu, Su = both(
+            lambda: O.shared_weight_grad_units(sh, dY64, units, fp8=fp8, fp8_dgrad=f8d),
+            lambda: O.shared_weight_grad_units(sh, dY64, units, rnd=RND, fp8=fp8, fp8_dgrad=f8d))
         ut = torch.from_numpy(units).cuda()
         for nm, got in (("dWs_g", plan.dWs_g[ut]), ("dWs_u", plan.dWs_u[ut]),
                         ("dWs_d", plan.dWs_d[:, ut])):
