@@ -28,7 +28,10 @@ METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 pe
 # DRAM bytes (read + write) of one step's grouped-GEMM launches, summed from a stored ncu
 # capture of the current kernels at that workload (not measured by this run; the line says
 # so); workloads without a capture report null.
-MEASURED_GEMM_TRAFFIC = {"C4": 105.13e9}
+MEASURED_GEMM_TRAFFIC = {"C4": 109.52e9}
+# Datasheet dense peaks of a GB300 (not from the source pages), reported beside the measured
+# ones: bf16 2250 TFLOP/s (fp8 twice that), HBM3e about 8 TB/s.
+NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -485,6 +488,7 @@ def main():
     gemm_tflops = gemm_flops / (gemm_ms / args.steps / 1e3) / 1e12
     peak_t = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
     peak_kind = f"{kind} bf16 sustained"
+    peak_nominal = NOMINAL_BF16_TFLOPS
     if cfg.fp8:
         # GEMMs on E4M3 have twice the dense bf16 rate (4.5 vs 2.25 PFLOP/s nominal): the
         # forward GEMMs are a third of the FLOPs with backward, and the data-gradient GEMMs
@@ -494,6 +498,8 @@ def main():
         if cfg.fp8_dgrad and cfg.backward:
             f_fp8 *= 2.0
         peak_t = gemm_flops / (f_fp8 / (2.0 * peak_t) + (gemm_flops - f_fp8) / peak_t)
+        peak_nominal = gemm_flops / (f_fp8 / (2.0 * peak_nominal) +
+                                     (gemm_flops - f_fp8) / peak_nominal)
         peak_kind = (f"{kind} bf16 sustained; fp8 forward"
                      f"{' and data-gradient' if cfg.fp8_dgrad else ''} GEMMs at 2x (nominal ratio)")
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -508,6 +514,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (all GEMM launches)",
                          "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
                          "frac": gemm_tflops / peak_t, "peak_kind": peak_kind,
+                         "peak_nominal": peak_nominal, "frac_of_nominal": gemm_tflops / peak_nominal,
                          "traffic": MEASURED_GEMM_TRAFFIC.get(args.config),
                          "traffic_unit": "bytes per step (all grouped-GEMM launches)",
                          "traffic_source": ("stored ncu capture (dram__bytes_read.sum + "
@@ -517,6 +524,9 @@ def main():
             "gpu_launches": plan.launches_per_step(cfg.backward, cfg.bias_update) * args.steps,
             "gpu_launches_note": "kernels per timed pass (the graph pass replays the same kernels)",
             "clocks": clocks, "e2e": e2e}
+    if clocks and clocks.get("sm_mhz"):
+        # step time x median SM clock under load: comparable between runs at other clocks
+        line["clock_normalised_ms_ghz"] = ms_step * clocks["sm_mhz"] / 1e3
     if world == 1 and not args.no_cpu_baseline:
         T_s = min(args.cpu_sample_tokens, cfg.T)
         rate, cores, _ = cpu_oracle_rate(cfg, inp, T_s)
