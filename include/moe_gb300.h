@@ -275,7 +275,7 @@ int moe_quantize_rows2_fp8(const moe_bf16* X0, const moe_bf16* X1, const int64_t
  * moe_quantize_rows_fp8, so Qt[e][n][k] is the code of X[e][k][n].
  * In : X0 [E, K0, N] bf16; X1 [E, K0, N] bf16 or NULL: with X1 the matrices are the stacks
  *      [X0[e]; X1[e]] of K = 2 K0 rows under one scale per column.
- * Out: Qt [E, N, K] codes; scale [E N] fp32. K0 % 64 == 0, N % 64 == 0.
+ * Out: Qt [E, N, K] codes; scale [E N] fp32. K0 % 128 == 0, N % 64 == 0.
  * W_d [E, d, f] -> (X0 = W_d, K0 = d, N = f): Wdq [E, f, d]; W_g, W_u [E, f, d] ->
  * (X0 = W_g, X1 = W_u, K0 = f, N = d): Wguq [E, d, 2f].
  */

@@ -63,7 +63,7 @@ constexpr int kColThreads = 256;
 // integer atomic max on the bits of non-negative floats, which order as the floats do (a
 // maximum does not depend on the order of its arguments). `bits` starts at zero.
 constexpr int kAmaxThreads = 128;
-constexpr int kAmaxRows = 256;
+constexpr int kAmaxRows = 128;
 
 __global__ void __launch_bounds__(kAmaxThreads) col_amax_kernel(
     const __nv_bfloat16* __restrict__ X0, const __nv_bfloat16* __restrict__ X1, int K0, int N,
@@ -108,21 +108,23 @@ __global__ void col_scale_kernel(float* __restrict__ S, int64_t n) {
     if (i < n) S[i] = Fp8Scale(S[i]).s;
 }
 
-// Tiles of 64 K-rows x 64 columns: read as bf16 rows, written as 64 code rows of 64 bytes.
-constexpr int kColTile = 64;
+// Tiles of 128 K-rows x 64 columns: read as 128 bf16 row pieces of 128 bytes, written as 64
+// code rows of 128 bytes (whole lines).
+constexpr int kColTileK = 128;
+constexpr int kColTileN = 64;
 
 __global__ void __launch_bounds__(kColThreads) col_quantize_kernel(
     const __nv_bfloat16* __restrict__ X0, const __nv_bfloat16* __restrict__ X1, int K0, int N,
     const float* __restrict__ S, uint8_t* __restrict__ Qt) {
-    __shared__ float tile[kColTile][kColTile + 1];
+    __shared__ float tile[kColTileK][kColTileN + 1];
     const int e = blockIdx.z;
-    const int n0 = blockIdx.x * kColTile;
-    const int k0 = blockIdx.y * kColTile;  // over K = K0 or 2 K0
+    const int n0 = blockIdx.x * kColTileN;
+    const int k0 = blockIdx.y * kColTileK;  // over K = K0 or 2 K0
     const int K = X1 ? 2 * K0 : K0;
     const int tid = threadIdx.x;
-    // load: 64 rows x 64 bf16 (8 vectors of 8 per row); 512 vectors, two per thread
-    for (int i = tid; i < kColTile * (kColTile / 8); i += kColThreads) {
-        const int r = i / (kColTile / 8), c8 = i % (kColTile / 8);
+    // load: 128 rows x 64 bf16 (8 vectors of 8 per row); 1024 vectors, four per thread
+    for (int i = tid; i < kColTileK * (kColTileN / 8); i += kColThreads) {
+        const int r = i / (kColTileN / 8), c8 = i % (kColTileN / 8);
         const int k = k0 + r;
         const __nv_bfloat16* src = (k < K0 ? X0 + (int64_t)e * K0 * N + (int64_t)k * N
                                            : X1 + (int64_t)e * K0 * N + (int64_t)(k - K0) * N) +
@@ -136,25 +138,27 @@ __global__ void __launch_bounds__(kColThreads) col_quantize_kernel(
         }
     }
     __syncthreads();
-    // store: code row n (64 K values) in four 16-byte pieces, one per thread
-    const int nl = tid / 4, piece = tid % 4;
-    const Fp8Scale cs = Fp8Scale::of(S[(int64_t)e * N + n0 + nl]);
-    uint32_t out[4];
+    // store: code row n (128 K values) in eight 16-byte pieces; 512 pieces, two per thread
+    for (int i = tid; i < kColTileN * 8; i += kColThreads) {
+        const int nl = i / 8, piece = i % 8;
+        const Fp8Scale cs = Fp8Scale::of(S[(int64_t)e * N + n0 + nl]);
+        uint32_t out[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
+        for (int q = 0; q < 4; ++q) {
+            uint32_t word = 0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int kk = 16 * piece + 4 * q + 2 * h;
-            const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(
-                make_float2(cs.quot(tile[kk][nl]), cs.quot(tile[kk + 1][nl])), __NV_SATFINITE,
-                __NV_E4M3);
-            word |= (uint32_t)p << (16 * h);
+            for (int h = 0; h < 2; ++h) {
+                const int kk = 16 * piece + 4 * q + 2 * h;
+                const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(
+                    make_float2(cs.quot(tile[kk][nl]), cs.quot(tile[kk + 1][nl])), __NV_SATFINITE,
+                    __NV_E4M3);
+                word |= (uint32_t)p << (16 * h);
+            }
+            out[q] = word;
         }
-        out[q] = word;
+        uint8_t* dst = Qt + ((int64_t)e * N + n0 + nl) * K + k0 + 16 * piece;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
     }
-    uint8_t* dst = Qt + ((int64_t)e * N + n0 + nl) * K + k0 + 16 * piece;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // Rowwise codes are a function of the row alone, so the codes of a token's k expert-major
@@ -238,7 +242,7 @@ int launch_quantize_cols_fp8(const __nv_bfloat16* X0, const __nv_bfloat16* X1, i
                            (unsigned)cdiv(K, kAmaxRows)),
                       kAmaxThreads, 0, st>>>(X0, X1, K0, N, reinterpret_cast<unsigned int*>(S));
     col_scale_kernel<<<(unsigned)cdiv((int64_t)E * N, 256), 256, 0, st>>>(S, (int64_t)E * N);
-    col_quantize_kernel<<<dim3((unsigned)(N / kColTile), (unsigned)(K / kColTile), (unsigned)E),
+    col_quantize_kernel<<<dim3((unsigned)(N / kColTileN), (unsigned)(K / kColTileK), (unsigned)E),
                           kColThreads, 0, st>>>(X0, X1, K0, N, S, Qt);
     return launch_status();
 }
@@ -275,7 +279,7 @@ extern "C" int moe_quantize_cols_fp8(const moe_bf16* X0, const moe_bf16* X1, int
                                      uint8_t* Qt, float* scale, moe_stream_t stream) {
     if (!X0 || !Qt || !scale) return MOE_ERR_INVALID_ARG;
     if (E <= 0 || K0 <= 0 || N <= 0) return MOE_ERR_INVALID_ARG;
-    if (K0 % 64 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (K0 % 128 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(X0) || (X1 && !aligned16(X1)) || !aligned16(Qt)) return MOE_ERR_INVALID_ARG;
     if (!device_supported()) return MOE_ERR_UNSUPPORTED;
     return launch_quantize_cols_fp8(reinterpret_cast<const __nv_bfloat16*>(X0),

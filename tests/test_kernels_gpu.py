@@ -727,7 +727,7 @@ def test_fp8_columnwise_and_joint_row_codes_are_bit_exact():
     over the stack of two matrices, and moe_quantize_rows2_fp8 (one scale per row over two
     halves) give the oracle's codes and scales bit for bit."""
     g = torch.Generator().manual_seed(71)
-    E, K0, N = 3, 192, 320
+    E, K0, N = 3, 256, 320
     X0 = randn_bf16((E, K0, N), g) * torch.rand(1, 1, N, generator=g).mul(40).to(torch.bfloat16)
     X1 = randn_bf16((E, K0, N), g) * 0.25
     X0[1, :, 7] = 0  # an all-zero column: scale 1
