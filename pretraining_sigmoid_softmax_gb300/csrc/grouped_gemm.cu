@@ -13,7 +13,8 @@
 //   B5  dW_g[e] = dA_e^T X_e, dW_u[e] = dU_e^T X_e
 // Row tiles are 128 rows of the expert-major layout, whose segments are padded to 128
 // rows, so every tile belongs to one expert and is found from row_offsets on the device
-// (no host synchronisation). Roles per CTA (384 threads, one CTA per SM):
+// (no host synchronisation). Roles per CTA (384 threads, or 640 with sixteen epilogue warps,
+// one CTA per SM):
 //   warp 0  TMA producer (one thread): operand tiles into a ring of shared-memory stages;
 //   warp 1  MMA issuer (one thread): tcgen05.mma 128 x N x 16 steps into a TMEM accumulator;
 //   warp 2  allocates / frees tensor memory (two accumulators, double-buffered);
@@ -22,7 +23,9 @@
 //            fused elementwise step, bf16 outputs. Token-major outputs (G1, G2, B2, B4) are
 //            packed into swizzled shared-memory boxes and written by TMA stores; B2 reads
 //            its saved a and u through TMA-staged boxes; weight gradients store per thread.
-//            Two warps per quadrant double the loads and stores in flight.
+//            Two warps per quadrant double the loads and stores in flight; GEMMs with a
+//            reduction of at most 1024 (G1) or 512 (G2) take four per quadrant (warps 4-19), as their main
+//            loop is shorter than eight warps' epilogue of the previous tile.
 // Pair mode (a cluster of two CTAs on two SMs): the leading CTA issues
 // tcgen05.mma.cta_group::2 over a 256-row tile; each CTA stages its own 128 rows of A and
 // half of the tile's B columns, so per SM the shared-memory operand traffic and the TMA
@@ -49,8 +52,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;        // bf16 K elements per stage (128 bytes per row)
 constexpr int BK_FP8 = 128;   // E4M3 K elements per stage (also 128 bytes per row)
-constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each taking half the columns
-constexpr int kThreads = 128 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 8;  // default: two per TMEM lane quadrant, each half the columns
 constexpr int kSmemBudget = 200 * 1024;
 
 enum Epi : int { kEpiSwigluFwd = 0, kEpiStore = 1, kEpiSwigluBwd = 2 };
@@ -66,8 +68,13 @@ constexpr int kSmemBudgetAu = 220 * 1024;
 constexpr int kOutCols = 16;
 
 template <int BN_, bool A_MN_, bool B_MN_, bool DUAL_, int EPI_, bool TWO_K_, bool WGRAD_,
-          bool PAIR_ = false, bool FP8_ = false>
+          bool PAIR_ = false, bool FP8_ = false, int OC_ = kOutCols, int EW_ = kEpiWarps>
 struct Cfg {
+    // epilogue warps: 8 (two per TMEM lane quadrant), or 16 for GEMMs whose reduction is so
+    // short that the epilogue, not the tensor cores, sets the pace (at most 96 registers)
+    static constexpr int EW = EW_;
+    static constexpr int THREADS = 128 + 32 * EW;
+    static_assert(EW == 8 || EW == 16, "epilogue warps");
     static constexpr bool FP8 = FP8_;        // E4M3 operands with row / column scales
     static constexpr int KB = FP8 ? BK_FP8 : BK;  // K elements per stage
     static constexpr int BN = BN_;           // output columns per tile (per B matrix if DUAL)
@@ -86,12 +93,17 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // this CTA's bytes per K block
     static constexpr bool AU = EPI == kEpiSwigluBwd;
     static constexpr int AU_BUF_BYTES = 2 * 32 * kAuCols * 2;  // a and u: 32 rows x kAuCols
-    static constexpr int AU_BYTES = AU ? kEpiWarps * kAuBufs * AU_BUF_BYTES : 0;
+    static constexpr int AU_BYTES = AU ? EW * kAuBufs * AU_BUF_BYTES : 0;
     static constexpr bool TS = !WGRAD;  // token-major outputs leave by TMA stores
     static constexpr int NOUT = EPI == kEpiSwigluFwd ? 3 : EPI == kEpiSwigluBwd ? 2 : 1;
-    static constexpr int OUT_BUF_BYTES = NOUT * 32 * kOutCols * 2;  // one chunk, every output
-    static constexpr int OUT_DEPTH = AU ? 1 : 2;                     // staged chunks per warp
-    static constexpr int OUT_BYTES = TS ? kEpiWarps * OUT_DEPTH * OUT_BUF_BYTES : 0;
+    // output columns per staged chunk: 16, or 32 (single-output epilogues of short-K GEMMs,
+    // where the per-chunk fence and store issue dominate) at the same shared-memory size
+    static constexpr int OCOLS = OC_;
+    static_assert(OCOLS == 16 || (OCOLS == 32 && NOUT == 1 && !AU), "output chunk width");
+    static constexpr int OUT_BOX_BYTES = 32 * OCOLS * 2;             // one output, one chunk
+    static constexpr int OUT_BUF_BYTES = NOUT * OUT_BOX_BYTES;       // one chunk, every output
+    static constexpr int OUT_DEPTH = (AU || OCOLS == 32 || EW == 16) ? 1 : 2;  // chunks per warp
+    static constexpr int OUT_BYTES = TS ? EW * OUT_DEPTH * OUT_BUF_BYTES : 0;
     static constexpr int BUDGET = (AU || TS ? kSmemBudgetAu : kSmemBudget) - AU_BYTES - OUT_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 6 ? 6 : (BUDGET / STAGE_BYTES);
     static constexpr int ACC_COLS = MMA_N;
@@ -108,7 +120,8 @@ struct Cfg {
                                          sizeof(int32_t) * (kMaxExperts + 1);
     static constexpr size_t SMEM_BYTES =
         1024 + (size_t)STAGES * STAGE_BYTES + AU_BYTES + OUT_BYTES + MISC_BYTES;
-    static_assert((2 * STAGES + 4 + kEpiWarps * kAuBufs) * 8 + 8 <= 512, "barrier block");
+    static_assert((2 * STAGES + 4 + EW * kAuBufs) * 8 + 8 <= 512, "barrier block");
+    static_assert(!AU || EW == 8, "the SwiGLU-backward epilogue keeps eight warps");
 };
 
 struct Params {
@@ -158,9 +171,9 @@ struct SmemLayout {
     int64_t* offs;     // E + 1
     int32_t* order;    // E
     int32_t* ptp;      // E + 1: exclusive prefix of pair tiles per expert (pair, token-major)
-    uint8_t* au;       // SwiGLU backward: kEpiWarps x kAuBufs staged (a | u) chunks
-    uint64_t* au_full; // kEpiWarps x kAuBufs
-    uint8_t* ob;       // TMA-store epilogues: kEpiWarps x 2 staged output chunks
+    uint8_t* au;       // SwiGLU backward: EW x kAuBufs staged (a | u) chunks
+    uint64_t* au_full; // EW x kAuBufs
+    uint8_t* ob;       // TMA-store epilogues: EW x OUT_DEPTH staged output chunks
 };
 
 template <class C>
@@ -177,7 +190,7 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
     s.tfull = s.empty + C::STAGES;
     s.tempty = s.tfull + 2;
     s.au_full = s.tempty + 2;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.au_full + (C::AU ? kEpiWarps * kAuBufs : 0));
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.au_full + (C::AU ? C::EW * kAuBufs : 0));
     s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
     s.offs = reinterpret_cast<int64_t*>(misc + 512);
     s.order = reinterpret_cast<int32_t*>(s.offs + kMaxExperts + 1);
@@ -392,6 +405,16 @@ __device__ __forceinline__ void epilogue_wgrad(const TileInfo& ti, uint32_t t_ac
 
 // Byte offset of 16-byte piece j of row r in a 32-byte-swizzled box of 32-byte rows.
 __device__ __forceinline__ int sw32_offset(int r, int j) { return r * 32 + ((j ^ ((r >> 2) & 1)) << 4); }
+// ... and in a 64-byte-swizzled box of 64-byte rows (32 bf16 columns).
+__device__ __forceinline__ int sw64_offset(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
+
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_ld32(taddr, r);
+    else if constexpr (W == 16) tmem_ld16(taddr, r);
+    else tmem_ld8(taddr, r);
+}
+
 
 template <class C>
 __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const TileInfo& ti,
@@ -399,37 +422,37 @@ __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const Ti
                                                    int c_lo, int ncols, const Params& P,
                                                    const CUtensorMap* mo0, const CUtensorMap* mo1,
                                                    const CUtensorMap* mo2, uint32_t& n) {
-    static_assert(kOutCols == 16, "chunk layout");
+    constexpr int W = C::OCOLS;
     if (ti.m0 >= ti.row_end) return;  // warp-uniform: the whole half is past the segment
     const int64_t row0 = ti.m0 + 32 * q;
     // rows past row_end (the tail of an unpadded layout) are clipped by the store; their FP8
     // row scale is read from the last row instead
     const int64_t row = row0 + lane < ti.row_end ? row0 + lane : ti.row_end - 1;
-    for (int i = 0; i < ncols / kOutCols; ++i, ++n) {
-        const int c = c_lo + i * kOutCols;
-        float v[C::NOUT][kOutCols];
+    for (int i = 0; i < ncols / W; ++i, ++n) {
+        const int c = c_lo + i * W;
+        float v[C::NOUT][W];
         if constexpr (C::EPI == kEpiSwigluFwd) {
-            uint32_t g[kOutCols], u[kOutCols];
-            tmem_ld16(t_acc + c, g);
-            tmem_ld16(t_acc + C::BN + c, u);
+            uint32_t g[W], u[W];
+            tmem_ld_cols<W>(t_acc + c, g);
+            tmem_ld_cols<W>(t_acc + C::BN + c, u);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < kOutCols; ++j) {
+            for (int j = 0; j < W; ++j) {
                 v[0][j] = __uint_as_float(g[j]);
                 v[1][j] = __uint_as_float(u[j]);
             }
-            if constexpr (C::FP8) fp8_scale<kOutCols>(v[0], v[1], P, row, ti, c);
+            if constexpr (C::FP8) fp8_scale<W>(v[0], v[1], P, row, ti, c);
             const float rg = P.row_scale ? __ldg(P.row_scale + row) : 1.0f;
 #pragma unroll
-            for (int j = 0; j < kOutCols; ++j)
+            for (int j = 0; j < W; ++j)
                 v[2][j] = v[0][j] / (1.0f + __expf(-v[0][j])) * v[1][j] * rg;
         } else {
-            uint32_t r[kOutCols];
-            tmem_ld16(t_acc + c, r);
+            uint32_t r[W];
+            tmem_ld_cols<W>(t_acc + c, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < kOutCols; ++j) v[0][j] = __uint_as_float(r[j]);
-            if constexpr (C::FP8) fp8_scale<kOutCols>(v[0], v[0], P, row, ti, c, /*dual=*/false);
+            for (int j = 0; j < W; ++j) v[0][j] = __uint_as_float(r[j]);
+            if constexpr (C::FP8) fp8_scale<W>(v[0], v[0], P, row, ti, c, /*dual=*/false);
         }
         uint8_t* buf = S.ob + ((size_t)slot * C::OUT_DEPTH + n % C::OUT_DEPTH) * C::OUT_BUF_BYTES;
         if (lane == 0) bulk_wait_read<C::OUT_DEPTH - 1>();  // the store that last read it is done
@@ -437,15 +460,17 @@ __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const Ti
 #pragma unroll
         for (int o = 0; o < C::NOUT; ++o)
 #pragma unroll
-            for (int j = 0; j < kOutCols / 8; ++j)
-                *reinterpret_cast<uint4*>(buf + o * 1024 + sw32_offset(lane, j)) = pack_chunk8(v[o] + 8 * j);
+            for (int j = 0; j < W / 8; ++j)
+                *reinterpret_cast<uint4*>(buf + o * C::OUT_BOX_BYTES +
+                                          (W == 32 ? sw64_offset(lane, j) : sw32_offset(lane, j))) =
+                    pack_chunk8(v[o] + 8 * j);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
             const CUtensorMap* mo[3] = {mo0, mo1, mo2};
 #pragma unroll
             for (int o = 0; o < C::NOUT; ++o)
-                tma_store_2d(mo[o], smem_u32(buf + o * 1024), ti.n0 + c, (int32_t)row0);
+                tma_store_2d(mo[o], smem_u32(buf + o * C::OUT_BOX_BYTES), ti.n0 + c, (int32_t)row0);
             bulk_commit();
         }
     }
@@ -478,13 +503,6 @@ __device__ __forceinline__ void au_issue(const SmemLayout& S, const CUtensorMap*
     mbar_arrive_expect_tx_relaxed(bar, C::AU_BUF_BYTES);
     tma_load_2d(dst, ma, bar, col, (int32_t)row0);
     tma_load_2d(dst + C::AU_BUF_BYTES / 2, mu, bar, col, (int32_t)row0);
-}
-
-template <int W>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
-    if constexpr (W == 32) tmem_ld32(taddr, r);
-    else if constexpr (W == 16) tmem_ld16(taddr, r);
-    else tmem_ld8(taddr, r);
 }
 
 // One tile of this warp's columns [c_lo, c_lo + ncols). `n` counts the warp's chunks over the
@@ -578,7 +596,7 @@ __device__ __forceinline__ bool swiglu_bwd_staged(const SmemLayout& S, const Til
 }
 
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap ma0,
                         const __grid_constant__ CUtensorMap ma1,
                         const __grid_constant__ CUtensorMap mb0,
@@ -602,17 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&S.tfull[b]), 1);
-            mbar_init(smem_u32(&S.tempty[b]), C::PAIR ? 2 * kEpiWarps : kEpiWarps);
+            mbar_init(smem_u32(&S.tempty[b]), C::PAIR ? 2 * C::EW : C::EW);
         }
         if constexpr (C::AU)
-            for (int b = 0; b < kEpiWarps * kAuBufs; ++b) mbar_init(smem_u32(&S.au_full[b]), 1);
+            for (int b = 0; b < C::EW * kAuBufs; ++b) mbar_init(smem_u32(&S.au_full[b]), 1);
         *S.abort_flag = 0;
         fence_mbar_init();
     }
     if (P.row_offsets)
-        for (int i = tid; i <= P.E; i += kThreads) S.offs[i] = P.row_offsets[i];
+        for (int i = tid; i <= P.E; i += C::THREADS) S.offs[i] = P.row_offsets[i];
     if (C::WGRAD)
-        for (int i = tid; i < P.E; i += kThreads) S.order[i] = P.expert_order ? P.expert_order[i] : i;
+        for (int i = tid; i < P.E; i += C::THREADS) S.order[i] = P.expert_order ? P.expert_order[i] : i;
     if (warp == 2) {
         if constexpr (C::PAIR) {
             tmem_alloc_pair(smem_u32(S.tmem_slot), C::TMEM_COLS);
@@ -746,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp % 4;  // TMEM lanes 32q .. 32q+31 (a warp's rank in its warpgroup)
         const int row_in_tile = 32 * q + lane;
-        constexpr int kCols = C::BN / (kEpiWarps / 4);  // columns per epilogue warp
+        constexpr int kCols = C::BN / (C::EW / 4);  // columns per epilogue warp
         static_assert(kCols % 32 == 0, "epilogue column split");
         const int c_lo = ((warp - 4) / 4) * kCols;
         const int slot = warp - 4;
@@ -852,13 +870,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor maps for the TMA-store epilogue: boxes of kOutCols x 32 rows over [rows, ld] bf16.
+// Tensor maps for the TMA-store epilogue: boxes of `cols` (16 or 32) x 32 rows over [rows, ld]
+// bf16, swizzled as the epilogue lays them out (32- or 64-byte rows).
 bool out_maps(CUtensorMap (&mo)[3], const void* o0, const void* o1, const void* o2, uint64_t ld,
-              uint64_t rows) {
+              uint64_t rows, int cols = kOutCols) {
     const void* o[3] = {o0, o1 ? o1 : o0, o2 ? o2 : o0};
+    const CUtensorMapSwizzle swz = cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     for (int i = 0; i < 3; ++i)
-        if (!make_map(&mo[i], o[i], ld, rows, kOutCols, 32, false, CU_TENSOR_MAP_SWIZZLE_32B))
-            return false;
+        if (!make_map(&mo[i], o[i], ld, rows, (uint32_t)cols, 32, false, swz)) return false;
     return true;
 }
 
@@ -883,7 +902,7 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(C::THREADS);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = st;
         cfg.attrs = attr;
@@ -903,7 +922,7 @@ int launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
         int64_t grid = sm_count();
         if (max_tiles < grid) grid = max_tiles;
         if (grid < 1) grid = 1;
-        kern<<<(unsigned)grid, kThreads, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, o0, o1, o2, P);
+        kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(a0, a1, b0, b1, o0, o1, o2, P);
         return launch_status();
     }
 }
@@ -913,10 +932,20 @@ using CfgG1 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false>;
 using CfgG1P = Cfg<128, false, false, true, kEpiSwigluFwd, false, false, true>;
 template <int BN> using CfgStoreK = Cfg<BN, false, false, false, kEpiStore, false, false>;
 using CfgStoreKP = Cfg<256, false, false, false, kEpiStore, false, false, true>;
+// short reductions: sixteen epilogue warps (and 32-column chunks for one output)
+using CfgG1P16 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false, true, false, 16, 16>;
+using CfgStoreKP32 = Cfg<256, false, false, false, kEpiStore, false, false, true, false, 32, 16>;
 template <int BN> using CfgSwigluBwd = Cfg<BN, false, true, false, kEpiSwigluBwd, false, false>;
 using CfgSwigluBwdP = Cfg<256, false, true, false, kEpiSwigluBwd, false, false, true>;
 template <int BN> using CfgDgrad2 = Cfg<BN, false, true, false, kEpiStore, true, false>;
 using CfgDgrad2P = Cfg<256, false, true, false, kEpiStore, true, false, true>;
+// Reductions this short (K elements) finish their main loop well before eight epilogue warps
+// have stored the tile, so those GEMMs take sixteen: G1 (three outputs) up to K = 1024, G2
+// (one output, 32-column chunks) up to K = 512. Measured on one box, the small fine-grained
+// layer's forward went from 0.156 to 0.137 ms; at K = 768-1024 sixteen warps for G2 (which
+// cost an operand stage) were 3% slower, and B4 at K = 512 gained nothing.
+constexpr int kShortK = 1024;
+constexpr int kShortKOneOut = 512;
 template <int BN> using CfgWgrad = Cfg<BN, true, true, false, kEpiStore, false, true>;
 using CfgWgradP = Cfg<256, true, true, false, kEpiStore, false, true, true>;
 // E4M3 forward GEMMs (rowwise scales)
@@ -993,7 +1022,9 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     CUtensorMap moa[3], moy[3];
     if (!out_maps(moa, A, U, H, f, rows) || !out_maps(moy, Y, nullptr, nullptr, d, rows))
         return MOE_ERR_LAUNCH;
-    int rc = launch<CfgG1P>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st, moa);
+    int rc = d <= kShortK
+                 ? launch<CfgG1P16>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st, moa)
+                 : launch<CfgG1P>(mx, mx, mwg, mwu, P, token_tiles_max(rows, f, 128), st, moa);
     if (rc != MOE_OK) return rc;
     // G2: y = h W_d^T
     Params Q = base_params(row_offsets, rows, E);
@@ -1001,7 +1032,13 @@ extern "C" int moe_expert_fwd(const moe_bf16* X, const int64_t* row_offsets, int
     Q.K0 = f;
     if (d % 256 == 0) {  // CTA pair: each CTA stages 128 of the tile's 256 W_d rows
         if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
-        rc = launch<CfgStoreKP>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st, moy);
+        if (f <= kShortKOneOut) {
+            CUtensorMap moy32[3];
+            if (!out_maps(moy32, Y, nullptr, nullptr, d, rows, 32)) return MOE_ERR_LAUNCH;
+            rc = launch<CfgStoreKP32>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st, moy32);
+        } else {
+            rc = launch<CfgStoreKP>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 256), st, moy);
+        }
     } else {
         if (!make_map(&mwd, W_d, f, (uint64_t)E * d, 64, 128)) return MOE_ERR_LAUNCH;
         rc = launch<CfgStoreK<128>>(mh, mh, mwd, mwd, Q, token_tiles_max(rows, d, 128), st, moy);
