@@ -121,7 +121,7 @@ struct Cfg {
     static constexpr size_t SMEM_BYTES =
         1024 + (size_t)STAGES * STAGE_BYTES + AU_BYTES + OUT_BYTES + MISC_BYTES;
     static_assert((2 * STAGES + 4 + EW * kAuBufs) * 8 + 8 <= 512, "barrier block");
-    static_assert(!AU || EW == 8, "the SwiGLU-backward epilogue keeps eight warps");
+
 };
 
 struct Params {
@@ -937,6 +937,7 @@ using CfgG1P16 = Cfg<128, false, false, true, kEpiSwigluFwd, false, false, true,
 using CfgStoreKP32 = Cfg<256, false, false, false, kEpiStore, false, false, true, false, 32, 16>;
 template <int BN> using CfgSwigluBwd = Cfg<BN, false, true, false, kEpiSwigluBwd, false, false>;
 using CfgSwigluBwdP = Cfg<256, false, true, false, kEpiSwigluBwd, false, false, true>;
+using CfgSwigluBwdP16 = Cfg<256, false, true, false, kEpiSwigluBwd, false, false, true, false, 16, 16>;
 template <int BN> using CfgDgrad2 = Cfg<BN, false, true, false, kEpiStore, true, false>;
 using CfgDgrad2P = Cfg<256, false, true, false, kEpiStore, true, false, true>;
 // Reductions this short (K elements) finish their main loop well before eight epilogue warps
@@ -946,6 +947,7 @@ using CfgDgrad2P = Cfg<256, false, true, false, kEpiStore, true, false, true>;
 // cost an operand stage) were 3% slower, and B4 at K = 512 gained nothing.
 constexpr int kShortK = 1024;
 constexpr int kShortKOneOut = 512;
+constexpr int kShortKB2 = 1024;
 template <int BN> using CfgWgrad = Cfg<BN, true, true, false, kEpiStore, false, true>;
 using CfgWgradP = Cfg<256, true, true, false, kEpiStore, false, true, true>;
 // E4M3 forward GEMMs (rowwise scales)
@@ -1095,7 +1097,9 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.gate_part = gate_part;
         CUtensorMap mod[3];
         if (!out_maps(mod, dA, dU, nullptr, f, rows)) return MOE_ERR_LAUNCH;
-        if (f % 256 == 0)
+        if (f % 256 == 0 && d <= kShortKB2)
+            rc = launch<CfgSwigluBwdP16>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st, mod);
+        else if (f % 256 == 0)
             rc = launch<CfgSwigluBwdP>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 256), st, mod);
         else
             rc = launch<CfgSwigluBwd<128>>(mdy, msa, mwd, msu, P, token_tiles_max(rows, f, 128), st,
