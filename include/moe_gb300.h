@@ -143,12 +143,15 @@ int moe_route(const moe_bf16* x, const float* W_r, const float* b, int64_t T, in
  *      layout, multiples of 128); perm_token [moe_padded_rows] int32 (token of each row,
  *      -1 for padding rows); slot_to_row [T,k] int32 (row of slot (t,i));
  *      X_perm [moe_padded_rows, d] bf16 (x rows in the permuted layout, padding rows 0).
+ * Optional (both or neither, else MOE_ERR_INVALID_ARG): topk_gate [T,k] fp32 in, row_gate
+ *      [moe_padded_rows] fp32 out: the gate of each row's slot, 0 on padding rows (what
+ *      moe_row_gates writes, for the gate folded into the experts), formed in the same pass.
  * An out-of-range index records MOE_ERR_BAD_INDEX; that slot is dropped.
  */
 int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, int E, int k,
                 int32_t* counts, int64_t* offsets, int64_t* row_offsets, int32_t* perm_token,
-                int32_t* slot_to_row, moe_bf16* X_perm, void* ws, size_t ws_bytes,
-                moe_stream_t stream);
+                int32_t* slot_to_row, moe_bf16* X_perm, const float* topk_gate,
+                float* row_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_permute_noalloc - moe_permute for callers that cannot allocate device memory.
@@ -157,11 +160,11 @@ int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, in
  * fixed-signature callback that is handed tensors but no allocator, or a process whose
  * device memory is owned entirely by another allocator. They cannot provide the `ws`
  * scratch that moe_permute needs and cannot call cudaMalloc to make one.
- * This variant takes the same arguments as moe_permute minus `ws`/`ws_bytes` and gives
- * the same results. Its scratch (two ceil(T/1024) x E int32 tables of per-chunk expert
+ * This variant takes the same arguments as moe_permute minus `topk_gate`/`row_gate` and
+ * `ws`/`ws_bytes`, and gives the same results. Its scratch (two ceil(T/256) x E int32 tables of per-chunk expert
  * counts) lives in a static device array of MOE_PERMUTE_NOALLOC_MAX_INTS int32 per table
- * (2 MiB in total), which every GPU that loads the library holds until the process exits.
- *   - Limit: ceil(T / 1024) * E <= MOE_PERMUTE_NOALLOC_MAX_INTS (T up to 4,194,304 tokens
+ * (8 MiB in total), which every GPU that loads the library holds until the process exits.
+ *   - Limit: ceil(T / 256) * E <= MOE_PERMUTE_NOALLOC_MAX_INTS (T up to 4,194,304 tokens
  *     with E = 64, 1,048,576 with E = 256); larger sizes return MOE_ERR_TOO_LARGE before
  *     any device work.
  *   - Allocation: none. It calls no cudaMalloc, cudaFree or allocating library routine.
@@ -175,7 +178,7 @@ int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, in
  *     read). Calls that overlap on the GPU (different streams, no ordering between them)
  *     race on the array and give wrong results; order them on one stream.
  */
-#define MOE_PERMUTE_NOALLOC_MAX_INTS 262144
+#define MOE_PERMUTE_NOALLOC_MAX_INTS 1048576
 int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, int E,
                         int k, int32_t* counts, int64_t* offsets, int64_t* row_offsets,
                         int32_t* perm_token, int32_t* slot_to_row, moe_bf16* X_perm,

@@ -27,7 +27,7 @@ PROTOTYPES = {
     "moe_set_wait_limit_ns": (None, [_U64]),
     "moe_check_bounded_wait": (_I, [_U64, _P]),
     "moe_route": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_permute": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_fwd": (_I, [_P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                             _P]),

@@ -21,8 +21,10 @@
 namespace moe {
 namespace {
 
-constexpr int kHistThreads = 256;
+constexpr int kHistThreads = kHistTokensPerCta;     // one token per thread
 constexpr int kScatterThreads = kHistTokensPerCta;  // one token per thread
+constexpr int kScatterWarps = kScatterThreads / 32;
+constexpr int kScanThreads = 1024;                  // one warp per expert at a time
 constexpr int kWarpsPerCta = 8;                     // warp-per-token kernels
 
 // Expert of slot (t, i), or -1 when the index is out of range or repeats an earlier slot
@@ -36,6 +38,8 @@ __device__ __forceinline__ int valid_expert(const int32_t* __restrict__ idx, int
     return e;
 }
 
+// Per chunk of kHistTokensPerCta tokens, the number of slots of each expert, stored expert
+// major: block_counts[e * nblocks + chunk].
 __global__ void __launch_bounds__(kHistThreads) hist_kernel(const int32_t* __restrict__ idx,
                                                             int64_t T, int E, int k,
                                                             int32_t* __restrict__ block_counts,
@@ -43,10 +47,8 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(const int32_t* __res
     __shared__ int cnt[kMaxExperts];
     for (int e = threadIdx.x; e < E; e += kHistThreads) cnt[e] = 0;
     __syncthreads();
-    const int64_t t0 = (int64_t)blockIdx.x * kHistTokensPerCta;
-    for (int q = threadIdx.x; q < kHistTokensPerCta; q += kHistThreads) {
-        const int64_t t = t0 + q;
-        if (t >= T) break;
+    const int64_t t = (int64_t)blockIdx.x * kHistTokensPerCta + threadIdx.x;
+    if (t < T) {
         for (int i = 0; i < k; ++i) {
             const int e = valid_expert(idx, t, k, i, E);
             if (e >= 0) atomicAdd(&cnt[e], 1);
@@ -55,40 +57,46 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(const int32_t* __res
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kHistThreads)
-        block_counts[(int64_t)blockIdx.x * E + e] = cnt[e];
+        block_counts[(int64_t)e * gridDim.x + blockIdx.x] = cnt[e];
 }
 
-// One CTA: per-expert running sums over the chunks (block bases), counts, the unpadded
-// offsets and the 128-row padded segment offsets.
-__global__ void __launch_bounds__(kMaxExperts) scan_kernel(
+// One CTA: per expert, the running sums over the chunks (block bases), then the counts, the
+// unpadded offsets and the 128-row padded segment offsets. Warp w takes experts w, w + 32,
+// ...; for an expert its lanes own consecutive runs of chunks: each sums its run, an
+// exclusive warp scan of those sums gives each run's base, and a second pass writes the
+// chunk bases. Integer sums: the result does not depend on the grouping.
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(
     const int32_t* __restrict__ block_counts, int64_t nblocks, int E,
     int32_t* __restrict__ block_base, int32_t* __restrict__ counts, int64_t* __restrict__ offsets,
     int64_t* __restrict__ row_offsets) {
     __shared__ int32_t c_sh[kMaxExperts];
-    const int e = threadIdx.x;
-    if (e < E) {
-        int32_t run = 0;
-        int64_t b = 0;
-        for (; b + 4 <= nblocks; b += 4) {  // four independent loads in flight
-            const int32_t v0 = block_counts[(b + 0) * E + e];
-            const int32_t v1 = block_counts[(b + 1) * E + e];
-            const int32_t v2 = block_counts[(b + 2) * E + e];
-            const int32_t v3 = block_counts[(b + 3) * E + e];
-            block_base[(b + 0) * E + e] = run;
-            block_base[(b + 1) * E + e] = run + v0;
-            block_base[(b + 2) * E + e] = run + v0 + v1;
-            block_base[(b + 3) * E + e] = run + v0 + v1 + v2;
-            run += v0 + v1 + v2 + v3;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t per = (nblocks + 31) / 32;
+    const int64_t b_lo = lane * per < nblocks ? lane * per : nblocks;
+    const int64_t b_hi = b_lo + per < nblocks ? b_lo + per : nblocks;
+    for (int e = warp; e < E; e += kScanThreads / 32) {
+        const int32_t* src = block_counts + (int64_t)e * nblocks;
+        int32_t* dst = block_base + (int64_t)e * nblocks;
+        int32_t sum = 0;
+        int64_t b = b_lo;
+        for (; b + 4 <= b_hi; b += 4) sum += (src[b] + src[b + 1]) + (src[b + 2] + src[b + 3]);
+        for (; b < b_hi; ++b) sum += src[b];
+        int32_t incl = sum;  // inclusive scan of the lanes' run sums
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        for (; b < nblocks; ++b) {
-            const int32_t v = block_counts[b * E + e];
-            block_base[b * E + e] = run;
+        int32_t run = incl - sum;
+        for (b = b_lo; b < b_hi; ++b) {
+            const int32_t v = src[b];
+            dst[b] = run;
             run += v;
         }
-        counts[e] = run;
-        c_sh[e] = run;
+        if (lane == 31) c_sh[e] = incl;
     }
     __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kScanThreads) counts[e] = c_sh[e];
     if (threadIdx.x == 0) {
         int64_t o = 0, ro = 0;
         for (int j = 0; j < E; ++j) {
@@ -106,53 +114,68 @@ __global__ void __launch_bounds__(kMaxExperts) scan_kernel(
 // strided share of the expert's padding rows.
 constexpr int kPadSplit = 16;
 
-// Padding rows of each expert segment: perm_token = -1 and (optionally) a zero row.
-__global__ void __launch_bounds__(256) pad_rows_kernel(const int64_t* __restrict__ row_offsets,
-                                                       const int32_t* __restrict__ counts,
-                                                       int d, int32_t* __restrict__ perm_token,
-                                                       __nv_bfloat16* __restrict__ buf) {
-    const int e = blockIdx.x;
+// Padding rows of expert e's segment, share `split` of kPadSplit: perm_token = -1, a zero row
+// of buf and (optionally) a zero row gate.
+__device__ __forceinline__ void pad_rows_share(const int64_t* __restrict__ row_offsets,
+                                               const int32_t* __restrict__ counts, int d,
+                                               int32_t* __restrict__ perm_token,
+                                               __nv_bfloat16* __restrict__ buf,
+                                               float* __restrict__ row_gate, int e, int split) {
     const int64_t lo = row_offsets[e] + counts[e], hi = row_offsets[e + 1];
     const int vec_per_row = d / 8;
-    for (int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
-         i += (int64_t)gridDim.y * blockDim.x) {
+    for (int64_t i = (int64_t)split * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
+         i += (int64_t)kPadSplit * blockDim.x) {
         const int64_t r = lo + i / vec_per_row;
         const int c = (int)(i % vec_per_row);
         reinterpret_cast<uint4*>(buf + r * d)[c] = make_uint4(0, 0, 0, 0);
-        if (c == 0 && perm_token) perm_token[r] = -1;
+        if (c == 0) {
+            if (perm_token) perm_token[r] = -1;
+            if (row_gate) row_gate[r] = 0.f;
+        }
     }
 }
 
-// Zero the padding rows of each segment, found as the trailing rows with perm_token < 0.
-__global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int64_t* __restrict__ row_offsets,
-                                                            const int32_t* __restrict__ perm_token,
-                                                            int d, __nv_bfloat16* __restrict__ buf) {
-    const int e = blockIdx.x;
+// Zero the padding rows of expert e's segment, found as the trailing rows with perm_token < 0
+// (share `split` of kPadSplit).
+__device__ __forceinline__ void zero_pad_rows_share(const int64_t* __restrict__ row_offsets,
+                                                    const int32_t* __restrict__ perm_token, int d,
+                                                    __nv_bfloat16* __restrict__ buf, int e,
+                                                    int split) {
     const int64_t hi = row_offsets[e + 1];
     int64_t lo = row_offsets[e];
     if (hi - lo > MOE_ROW_ALIGN - 1) lo = hi - (MOE_ROW_ALIGN - 1);
     const int vec_per_row = d / 8;
-    for (int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
-         i += (int64_t)gridDim.y * blockDim.x) {
+    for (int64_t i = (int64_t)split * blockDim.x + threadIdx.x; i < (hi - lo) * vec_per_row;
+         i += (int64_t)kPadSplit * blockDim.x) {
         const int64_t r = lo + i / vec_per_row;
         if (perm_token[r] < 0)
             reinterpret_cast<uint4*>(buf + r * d)[i % vec_per_row] = make_uint4(0, 0, 0, 0);
     }
 }
 
-// Stable ranks: within a chunk of 1024 tokens, warp w owns tokens [32 w, 32 w + 32).
-// Row of (t, i) = row_offsets[e] + chunk base of e + warp base of e + rank within warp.
+// Stable ranks: within a chunk of kHistTokensPerCta tokens, warp w owns tokens [32 w, 32 w +
+// 32). Row of (t, i) = row_offsets[e] + chunk base of e + warp base of e + rank within warp.
+// Blocks past the nblocks chunks pad the segments instead (kPadSplit per expert: perm_token
+// -1, zero rows of X_perm and of the row gates). With row_gate, each slot's gate is copied to
+// its row as well (the gate folded into the expert).
 __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
-    const int32_t* __restrict__ idx, int64_t T, int E, int k,
+    const int32_t* __restrict__ idx, int64_t T, int E, int k, int64_t nblocks,
     const int32_t* __restrict__ block_base, const int64_t* __restrict__ row_offsets,
-    int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_to_row) {
-    extern __shared__ int32_t sc_smem[];
-    int32_t* wcnt = sc_smem;                                                       // [32][E]
-    uint32_t* wmask = reinterpret_cast<uint32_t*>(sc_smem + 32 * E);              // [32][E]
+    const int32_t* __restrict__ counts, int d, int32_t* __restrict__ perm_token,
+    int32_t* __restrict__ slot_to_row, __nv_bfloat16* __restrict__ X_perm,
+    const float* __restrict__ gate, float* __restrict__ row_gate) {
+    if (blockIdx.x >= nblocks) {  // block-uniform: no barrier below is reached
+        const int p = (int)(blockIdx.x - nblocks);
+        pad_rows_share(row_offsets, counts, d, perm_token, X_perm, row_gate, p / kPadSplit,
+                       p % kPadSplit);
+        return;
+    }
+    __shared__ int32_t wcnt[kScatterWarps][kMaxExperts];
+    __shared__ uint32_t wmask[kScatterWarps][kMaxExperts];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    for (int i = tid; i < 32 * E; i += kScatterThreads) {
-        wcnt[i] = 0;
-        wmask[i] = 0u;
+    for (int i = tid; i < kScatterWarps * kMaxExperts; i += kScatterThreads) {
+        (&wcnt[0][0])[i] = 0;
+        (&wmask[0][0])[i] = 0u;
     }
     __syncthreads();
     const int64_t t = (int64_t)blockIdx.x * kHistTokensPerCta + tid;
@@ -161,16 +184,17 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
         for (int i = 0; i < k; ++i) {
             const int e = valid_expert(idx, t, k, i, E);
             if (e >= 0) {
-                atomicAdd(&wcnt[warp * E + e], 1);
-                atomicOr(&wmask[warp * E + e], 1u << lane);
+                atomicAdd(&wcnt[warp][e], 1);
+                atomicOr(&wmask[warp][e], 1u << lane);
             }
         }
     __syncthreads();
-    if (tid < E) {  // exclusive scan over warps, per expert
+    for (int e = tid; e < E; e += kScatterThreads) {  // exclusive scan over warps, per expert
         int32_t run = 0;
-        for (int w = 0; w < 32; ++w) {
-            const int32_t c = wcnt[w * E + tid];
-            wcnt[w * E + tid] = run;
+#pragma unroll
+        for (int w = 0; w < kScatterWarps; ++w) {
+            const int32_t c = wcnt[w][e];
+            wcnt[w][e] = run;
             run += c;
         }
     }
@@ -181,10 +205,11 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
         const int e = valid_expert(idx, t, k, i, E);
         int32_t row = -1;
         if (e >= 0) {
-            const int rank = __popc(wmask[warp * E + e] & lt_mask);
-            row = (int32_t)(row_offsets[e] + block_base[(int64_t)blockIdx.x * E + e] +
-                            wcnt[warp * E + e] + rank);
+            const int rank = __popc(wmask[warp][e] & lt_mask);
+            row = (int32_t)(row_offsets[e] + block_base[(int64_t)e * nblocks + blockIdx.x] +
+                            wcnt[warp][e] + rank);
             perm_token[row] = (int32_t)t;
+            if (row_gate) row_gate[row] = gate[t * k + i];
         }
         slot_to_row[t * k + i] = row;
     }
@@ -279,8 +304,14 @@ template <int KMAX, bool CODES = false>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ Y_perm,
     const float* __restrict__ gate, const int32_t* __restrict__ slot_to_row, int64_t T, int d,
-    int k, __nv_bfloat16* __restrict__ dY_perm, float* __restrict__ dg,
+    int k, __nv_bfloat16* __restrict__ dY_perm, float* __restrict__ dg, int64_t tok_blocks,
+    const int64_t* __restrict__ row_offsets, const int32_t* __restrict__ perm_token,
     uint8_t* __restrict__ dYq = nullptr, float* __restrict__ sdY = nullptr) {
+    if (blockIdx.x >= tok_blocks) {  // the segments' padding rows of dY_perm, kPadSplit per expert
+        const int p = (int)(blockIdx.x - tok_blocks);
+        zero_pad_rows_share(row_offsets, perm_token, d, dY_perm, p / kPadSplit, p % kPadSplit);
+        return;
+    }
     const int lane = threadIdx.x % 32;
     const int64_t t = (int64_t)blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
     if (t >= T) return;
@@ -510,10 +541,12 @@ using namespace moe;
 extern "C" int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T, int d, int E,
                            int k, int32_t* counts, int64_t* offsets, int64_t* row_offsets,
                            int32_t* perm_token, int32_t* slot_to_row, moe_bf16* X_perm,
-                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+                           const float* topk_gate, float* row_gate, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
     if (!topk_idx || !x || !counts || !offsets || !row_offsets || !perm_token || !slot_to_row ||
         !X_perm)
         return MOE_ERR_INVALID_ARG;
+    if ((topk_gate == nullptr) != (row_gate == nullptr)) return MOE_ERR_INVALID_ARG;
     if (!shape_ok(T, d, E, k)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || k > E || k > 32 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(X_perm)) return MOE_ERR_INVALID_ARG;
@@ -527,16 +560,10 @@ extern "C" int moe_permute(const int32_t* topk_idx, const moe_bf16* x, int64_t T
     if (!ws || !wc.ok()) return MOE_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     hist_kernel<<<(unsigned)nb, kHistThreads, 0, st>>>(topk_idx, T, E, k, bcounts, status);
-    scan_kernel<<<1, kMaxExperts, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
-    pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, counts, d, perm_token,
-                                       reinterpret_cast<__nv_bfloat16*>(X_perm));
-    const size_t sc_smem = sizeof(int32_t) * 64 * E;
-    if (cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sc_smem) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    scatter_kernel<<<(unsigned)nb, kScatterThreads, sc_smem, st>>>(topk_idx, T, E, k, bbase,
-                                                                   row_offsets, perm_token,
-                                                                   slot_to_row);
+    scan_kernel<<<1, kScanThreads, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
+    scatter_kernel<<<(unsigned)(nb + (int64_t)E * kPadSplit), kScatterThreads, 0, st>>>(
+        topk_idx, T, E, k, nb, bbase, row_offsets, counts, d, perm_token, slot_to_row,
+        reinterpret_cast<__nv_bfloat16*>(X_perm), topk_gate, row_gate);
     gather_kernel<<<warp_grid(T), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x),
                                                 slot_to_row, T, d, k,
                                                 reinterpret_cast<__nv_bfloat16*>(X_perm));
@@ -594,12 +621,13 @@ extern "C" int moe_combine_bwd(const moe_bf16* dY, const moe_bf16* Y_perm,
     const __nv_bfloat16* dYb = reinterpret_cast<const __nv_bfloat16*>(dY);
     const __nv_bfloat16* Yb = reinterpret_cast<const __nv_bfloat16*>(Y_perm);
     __nv_bfloat16* dYp = reinterpret_cast<__nv_bfloat16*>(dY_perm);
-    if (k <= 2) combine_bwd_kernel<2><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
-    else if (k <= 4) combine_bwd_kernel<4><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
-    else if (k <= 8) combine_bwd_kernel<8><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
-    else if (k <= 16) combine_bwd_kernel<16><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
-    else combine_bwd_kernel<32><<<warp_grid(T), 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg);
-    zero_pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    const int64_t tb = warp_grid(T);  // token blocks; then kPadSplit padding blocks per expert
+    const unsigned g = (unsigned)(tb + (int64_t)E * kPadSplit);
+    if (k <= 2) combine_bwd_kernel<2><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token);
+    else if (k <= 4) combine_bwd_kernel<4><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token);
+    else if (k <= 8) combine_bwd_kernel<8><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token);
+    else if (k <= 16) combine_bwd_kernel<16><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token);
+    else combine_bwd_kernel<32><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token);
     return launch_status();
 }
 
@@ -620,13 +648,13 @@ extern "C" int moe_combine_bwd_fp8(const moe_bf16* dY, const moe_bf16* Y_perm,
     const __nv_bfloat16* dYb = reinterpret_cast<const __nv_bfloat16*>(dY);
     const __nv_bfloat16* Yb = reinterpret_cast<const __nv_bfloat16*>(Y_perm);
     __nv_bfloat16* dYp = reinterpret_cast<__nv_bfloat16*>(dY_perm);
-    const unsigned g = warp_grid(T);
-    if (k <= 2) combine_bwd_kernel<2, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
-    else if (k <= 4) combine_bwd_kernel<4, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
-    else if (k <= 8) combine_bwd_kernel<8, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
-    else if (k <= 16) combine_bwd_kernel<16, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
-    else combine_bwd_kernel<32, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, dYq, sdY);
-    zero_pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, perm_token, d, dYp);
+    const int64_t tb = warp_grid(T);  // token blocks; then kPadSplit padding blocks per expert
+    const unsigned g = (unsigned)(tb + (int64_t)E * kPadSplit);
+    if (k <= 2) combine_bwd_kernel<2, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token, dYq, sdY);
+    else if (k <= 4) combine_bwd_kernel<4, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token, dYq, sdY);
+    else if (k <= 8) combine_bwd_kernel<8, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token, dYq, sdY);
+    else if (k <= 16) combine_bwd_kernel<16, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token, dYq, sdY);
+    else combine_bwd_kernel<32, true><<<g, 256, 0, st>>>(dYb, Yb, topk_gate, slot_to_row, T, d, k, dYp, dg, tb, row_offsets, perm_token, dYq, sdY);
     if (launch_pad_rows_fp8(row_offsets, perm_token, d, E, dYq, sdY, st) != MOE_OK)
         return MOE_ERR_LAUNCH;
     return launch_status();
@@ -776,16 +804,10 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, i
     int32_t* bbase = scratch + kNoallocMaxInts;
     cudaStream_t st = (cudaStream_t)stream;
     hist_kernel<<<(unsigned)nb, kHistThreads, 0, st>>>(topk_idx, T, E, k, bcounts, status);
-    scan_kernel<<<1, kMaxExperts, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
-    pad_rows_kernel<<<dim3(E, kPadSplit), 256, 0, st>>>(row_offsets, counts, d, perm_token,
-                                       reinterpret_cast<__nv_bfloat16*>(X_perm));
-    const size_t sc_smem = sizeof(int32_t) * 64 * E;
-    if (cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sc_smem) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    scatter_kernel<<<(unsigned)nb, kScatterThreads, sc_smem, st>>>(topk_idx, T, E, k, bbase,
-                                                                   row_offsets, perm_token,
-                                                                   slot_to_row);
+    scan_kernel<<<1, kScanThreads, 0, st>>>(bcounts, nb, E, bbase, counts, offsets, row_offsets);
+    scatter_kernel<<<(unsigned)(nb + (int64_t)E * kPadSplit), kScatterThreads, 0, st>>>(
+        topk_idx, T, E, k, nb, bbase, row_offsets, counts, d, perm_token, slot_to_row,
+        reinterpret_cast<__nv_bfloat16*>(X_perm), nullptr, nullptr);
     gather_kernel<<<warp_grid(T), 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x),
                                                 slot_to_row, T, d, k,
                                                 reinterpret_cast<__nv_bfloat16*>(X_perm));

@@ -7,7 +7,7 @@
 namespace moe {
 
 constexpr int kRouteTokensPerCta = 64;     // router forward: tokens per CTA
-constexpr int kHistTokensPerCta = 1024;    // permute: tokens per histogram chunk
+constexpr int kHistTokensPerCta = 256;     // permute: tokens per histogram chunk
 constexpr int kRouteBwdTokensPerSplit = 2048;  // router backward: tokens per dW_r split
 constexpr int kMaxExperts = 256;
 

@@ -182,15 +182,15 @@ class MoEPlan:
         n += 1 if s.mode == ops.MODE_SOFTMAX else 0         # logits) (+ z-loss reduction)
         if s.has_aux:
             n += 2 + (1 if backward else 0)                 # balancing losses (+ gradient)
-        n += 5                                              # permute
-        n += 1 if not s.fp8 else 0                          # row gates (folded gates)
+        n += 4                                              # permute (the padding rows and
+                                                            # folded row gates in the scatter)
         if s.fp8:  # quantise x, W_g, W_u, W_d; expert-major codes (2); G1, quantise H, G2
             n += 9 + (6 if s.f_shared else 0)               # (shared: its weights, G1, H, G2)
         else:
             n += 2 + (2 if s.f_shared else 0)               # expert forward (G1, G2)
         n += 1                                              # combine
         if backward:
-            n += 2                                          # combine backward + padding rows
+            n += 1                                          # combine backward (+ padding rows)
             n += 1 if not s.fp8 else 0                      # gate gradient from its partials
             if s.fp8_dgrad:  # pad the dY codes, W_d and W_g/W_u columns (3 each), B2,
                 n += 13 + (12 if s.f_shared else 0)         # [dA|dU] rows, B4, order, B3, B5
@@ -224,12 +224,13 @@ class MoEPlan:
         if s.has_aux:
             ops.moe_aux_loss(self.logits, self.topk_idx, s.mode, s.seq_len, s.aux_switch,
                              s.aux_seq, self.aux_loss, self.aux_f, self.ws, stream)
-        ops.moe_permute(self.topk_idx, x, s.E, self.counts, self.offsets, self.row_offsets,
-                        self.perm_token, self.slot_to_row, self.X_perm, self.ws, stream)
         # the combine's gate weights move before the (linear) down projection: the routed
-        # experts emit g * y directly, and the combine adds rows without weights
-        if self.fold_gate:
-            ops.moe_row_gates(self.topk_gate, self.slot_to_row, self.row_gate, stream)
+        # experts emit g * y directly, and the combine adds rows without weights; the
+        # dispatch copies each slot's gate to its row as it places the row
+        ops.moe_permute(self.topk_idx, x, s.E, self.counts, self.offsets, self.row_offsets,
+                        self.perm_token, self.slot_to_row, self.X_perm, self.ws, stream,
+                        topk_gate=self.topk_gate if self.fold_gate else None,
+                        row_gate=self.row_gate)
         ys = None
         if s.fp8:
             q = ops.moe_quantize_rows_fp8

@@ -87,13 +87,16 @@ def moe_route(x, W_r, b, k, mode, z_coef, logits, topk_idx, topk_gate, topk_scor
 
 
 def moe_permute(topk_idx, x, E, counts, offsets, row_offsets, perm_token, slot_to_row, X_perm,
-                ws, stream=None):
+                ws, stream=None, topk_gate=None, row_gate=None):
     T, k = topk_idx.shape
     d = x.shape[1]
     _contig(topk_idx, x, counts, offsets, row_offsets, perm_token, slot_to_row, X_perm, ws)
+    if row_gate is not None:
+        _contig(topk_gate, row_gate)
     _check(_lib.load().moe_permute(_p(topk_idx), _p(x), T, d, E, k, _p(counts), _p(offsets),
                                    _p(row_offsets), _p(perm_token), _p(slot_to_row), _p(X_perm),
-                                   _p(ws), ws.numel(), _stream(stream)), "moe_permute")
+                                   _p(topk_gate), _p(row_gate), _p(ws), ws.numel(),
+                                   _stream(stream)), "moe_permute")
 
 
 def moe_permute_noalloc(topk_idx, x, E, counts, offsets, row_offsets, perm_token, slot_to_row,

@@ -85,6 +85,39 @@ def test_route_matches_oracle(T, d, E, k, mode):
         assert float(r["z"][0]) == pytest.approx(ref["z_loss"], rel=1e-4)
 
 
+@pytest.mark.parametrize("T,d,E,k,mode", [(1000, 256, 64, 8, "sigmoid"), (500, 128, 64, 5, "sigmoid"),
+                                         (777, 256, 32, 5, "softmax"), (400, 128, 24, 3, "sigmoid"),
+                                         (300, 128, 128, 7, "sigmoid")])
+def test_route_breaks_exact_ties_by_lower_index(T, d, E, k, mode):
+    """Experts 2j and 2j + 1 have identical router rows (and biases), so every selection value
+    has an exact twin: the choice must take the lower index first, as the definition's order
+    (larger value, then lower index) says, and otherwise agree with the oracle on the GPU's
+    own logits wherever the distinct values are not near a tie."""
+    g = torch.Generator().manual_seed(T + 31 * E + k)
+    x = randn_bf16((T, d), g)
+    half = torch.randn((E + 1) // 2, d, generator=g) * d ** -0.5
+    W_r = half.repeat_interleave(2, dim=0)[:E].contiguous()
+    bh = torch.rand((E + 1) // 2, generator=g) * 0.1 - 0.05
+    b = bh.repeat_interleave(2)[:E].contiguous()
+    m = ops.MODE_SIGMOID if mode == "sigmoid" else ops.MODE_SOFTMAX
+    r = _route(x, W_r, b, k, m, 0.0)
+    lg = r["logits"].cpu()
+    assert torch.equal(lg[:, 0:E - 1:2], lg[:, 1:E:2]), "twin experts' logits differ"
+    ref = O.route(h64(lg), mode, k, h64(b), 0.0)
+    if mode == "sigmoid":  # fp32 against fp64 selection values: skip near ties between pairs
+        near = O.near_tie_tokens(ref["select_value"][:, 0::2], (k + 1) // 2)
+    else:
+        near = np.zeros(T, bool)
+    assert near.mean() < 0.02
+    idx = r["idx"].cpu().numpy()
+    assert (idx[~near] == ref["idx"][~near]).all(), "choice differs from the oracle's order"
+    for t in range(T):  # an upper twin is never taken before its lower twin
+        pos = {e: i for i, e in enumerate(idx[t].tolist())}
+        for e, i in pos.items():
+            if e % 2 == 1:
+                assert e - 1 in pos and pos[e - 1] < i, (t, idx[t])
+
+
 def test_route_is_bitwise_repeatable():
     g = torch.Generator().manual_seed(5)
     x = randn_bf16((2000, 512), g)
@@ -107,7 +140,7 @@ def _random_choice(T, E, k, gen, skew=False):
     return idx.to(torch.int32)
 
 
-def _permute(idx, x, E):
+def _permute(idx, x, E, gate=None):
     T, k = idx.shape
     d = x.shape[1]
     R = ops.moe_padded_rows(T, k, E)
@@ -117,8 +150,11 @@ def _permute(idx, x, E):
                perm_token=torch.full((R,), -7, dtype=torch.int32, device="cuda"),
                slot_to_row=torch.empty(T, k, dtype=torch.int32, device="cuda"),
                X_perm=torch.full((R, d), float("nan"), dtype=torch.bfloat16, device="cuda"))
+    if gate is not None:
+        out["row_gate"] = torch.full((R,), float("nan"), device="cuda")
     ops.moe_permute(dev(idx), dev(x), E, out["counts"], out["offsets"], out["row_offsets"],
-                    out["perm_token"], out["slot_to_row"], out["X_perm"], _ws(T, d, E, k))
+                    out["perm_token"], out["slot_to_row"], out["X_perm"], _ws(T, d, E, k),
+                    topk_gate=None if gate is None else dev(gate), row_gate=out.get("row_gate"))
     torch.cuda.synchronize()
     return out
 
@@ -130,7 +166,8 @@ def test_permute_is_bit_exact(T, d, E, k, skew):
     g = torch.Generator().manual_seed(T + E)
     idx = _random_choice(T, E, k, g, skew)
     x = randn_bf16((T, d), g)
-    r = _permute(idx, x, E)
+    gate = torch.rand(T, k, generator=g)
+    r = _permute(idx, x, E, gate)
     D = O.dispatch(idx.numpy().astype(np.int64), E)
     counts = r["counts"].cpu().numpy()
     assert (counts == D["counts"]).all()
@@ -147,6 +184,11 @@ def test_permute_is_bit_exact(T, d, E, k, skew):
     pad = np.setdiff1d(np.arange(int(ro[-1])), rows)
     assert (pt[pad] == -1).all()
     assert (Xp[torch.from_numpy(pad)] == 0).all()
+    # the gate of each row's slot, copied in the same pass; zero on padding rows
+    rg = r["row_gate"].cpu().numpy()
+    want = gate.numpy()[D["perm_token"], D["perm_slot"]]
+    assert np.array_equal(rg[rows].view(np.uint32), want.astype(np.float32).view(np.uint32))
+    assert (rg[pad] == 0).all()
 
 
 def test_permute_reports_bad_index_without_touching_other_rows():

@@ -61,7 +61,8 @@ def test_argument_checks_return_before_any_device_work(lib):
     rc = lib.moe_route(None, None, None, 16, 128, 8, 2, 0, 0.0, None, None, None, None, None,
                        None, None, 0, None)
     assert rc == 1
-    rc = lib.moe_permute(None, None, 16, 128, 8, 2, None, None, None, None, None, None, None, 0, None)
+    rc = lib.moe_permute(None, None, 16, 128, 8, 2, None, None, None, None, None, None, None, None,
+                         None, 0, None)
     assert rc == 1
     rc = lib.moe_expert_fwd(None, None, 1, 16, 128, 128, None, None, None, None, None, None, None,
                             None, None, 0, None)
@@ -126,8 +127,11 @@ def test_degenerate_and_inconsistent_arguments_are_rejected_on_the_host(lib):
     assert route(P, None, 16, 0, P, P, P) == 1      # sigmoid mode needs the bias
     assert route(P, None, 16, 1, None, P, P) == 1   # softmax mode needs logits, lse, z-loss
     assert route(bad, P, 16, 0, P, P, P) == 1       # misaligned x
-    assert lib.moe_permute(P, P, 0, 256, 8, 2, P, P, P, P, P, P, ws, 1 << 20, None) == 1
-    assert lib.moe_permute(P, bad, 16, 256, 8, 2, P, P, P, P, P, P, ws, 1 << 20, None) == 1
+    assert lib.moe_permute(P, P, 0, 256, 8, 2, P, P, P, P, P, P, None, None, ws, 1 << 20, None) == 1
+    assert lib.moe_permute(P, bad, 16, 256, 8, 2, P, P, P, P, P, P, None, None, ws, 1 << 20,
+                           None) == 1
+    assert lib.moe_permute(P, P, 16, 256, 8, 2, P, P, P, P, P, P, P, None, ws, 1 << 20,
+                           None) == 1   # the row gates need both pointers
     assert lib.moe_combine(P, P, P, None, 0, 256, 2, P, None) == 1
     assert lib.moe_combine(bad, P, P, None, 16, 256, 2, P, None) == 1
     fwd = lambda rows, E, ro, X: lib.moe_expert_fwd(X, ro, E, rows, 256, 128, P, P, P, P, P, P,

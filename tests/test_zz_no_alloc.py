@@ -69,7 +69,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     from pretraining_sigmoid_softmax_gb300 import _lib
     lib = _lib.load()
     E, k, d = 256, 8, 128
-    T = 1024 * (262144 // E + 1)  # one chunk of counts more than the static array holds
+    T = 256 * (1048576 // E + 1)  # one chunk of counts more than the static array holds
     small = torch.zeros(16, dtype=torch.int32, device="cuda")
     rc = lib.moe_permute_noalloc(small.data_ptr(), small.data_ptr(), T, d, E, k,
                                  small.data_ptr(), small.data_ptr(), small.data_ptr(),
