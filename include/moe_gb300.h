@@ -197,7 +197,7 @@ int moe_permute_noalloc(const int32_t* topk_idx, const moe_bf16* x, int64_t T, i
  * row_gate [rows] fp32 or NULL: with it the row's gate is folded into the expert, h is
  *      written as row_gate[p] * silu(a) * u (one bf16 rounding) and y is therefore the gated
  *      output; a and u are not scaled. The down projection is linear, so this gives the
- *      combine's g * y without a second pass (moe_row_gates builds row_gate).
+ *      combine's g * y without a second pass (moe_permute or moe_row_gates builds row_gate).
  * `rows` is the row capacity of X/A/U/H/Y; rows past it are never touched.
  * A row_offsets array that breaks the padded layout (row_offsets[0] != 0, a decrease, a
  * segment that is not a multiple of 128 rows, row_offsets[E] > rows) records
@@ -416,6 +416,9 @@ int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
  * Definition: row_gate[slot_to_row[t,i]] = topk_gate[t,i]; every other row (padding) 0.
  * In : topk_gate [T,k] fp32; slot_to_row [T,k] int32 (from moe_permute); rows = the layout's
  *      row capacity (moe_padded_rows).  Out: row_gate [rows] fp32.
+ * moe_permute forms the same table in its own pass when given topk_gate and row_gate (rows
+ * past the padded layout's end are then left as they were); this call serves callers that
+ * permute without them.
  */
 int moe_row_gates(const float* topk_gate, const int32_t* slot_to_row, int64_t T, int k,
                   int64_t rows, float* row_gate, moe_stream_t stream);

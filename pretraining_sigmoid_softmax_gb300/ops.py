@@ -113,7 +113,7 @@ def moe_permute_noalloc(topk_idx, x, E, counts, offsets, row_offsets, perm_token
 
 
 def moe_expert_fwd(X, row_offsets, W_g, W_u, W_d, A, U, H, Y, ws, stream=None, row_gate=None):
-    """row_gate [rows] fp32 (from moe_row_gates) folds each row's gate into h and y."""
+    """row_gate [rows] fp32 (from moe_permute or moe_row_gates) folds each row's gate into h and y."""
     rows, d = X.shape
     E, f, _ = W_g.shape
     _contig(X, W_g, W_u, W_d, A, U, H, Y, ws, row_gate)
