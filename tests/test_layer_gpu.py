@@ -374,3 +374,49 @@ def test_cuda_graph_replay_matches_eager_step():
     for k, v in plan.grads().items():
         assert torch.equal(v, p_eager.grads()[k]), k
     assert torch.equal(b, b_eager)
+
+
+LAUNCH_CASES = [CONFIGS["C1"], CONFIGS["C2"]] + [
+    c for c in SMALL if c.name in ("aux_losses_sigmoid", "aux_losses_softmax", "fp8_forward_shared",
+                                   "fp8_dgrad_shared", "widest_router_E256", "one_expert_top1")]
+
+
+@pytest.mark.parametrize("cfg", LAUNCH_CASES, ids=lambda c: c.name)
+def test_launch_count_matches_the_plan(cfg):
+    """The bench's gpu_launches is launches_per_step times the steps: count the library's
+    kernels that one step actually runs (CUDA activity of the profiler, kernels of the moe
+    namespace; the profiler's own and torch's kernels are not the library's)."""
+    from torch.autograd import DeviceType
+    from torch.profiler import ProfilerActivity, profile
+    inp = make_inputs(cfg)
+    d = {k: v.cuda() for k, v in inp.items()}
+    plan = MoEPlan(MoEShape.from_config(cfg), "cuda", backward=cfg.backward)
+    b = d["b"].clone()
+
+    def step():
+        plan.forward(d["x"], d["W_r"], b, d["W_g"], d["W_u"], d["W_d"], d.get("Ws_g"),
+                     d.get("Ws_u"), d.get("Ws_d"))
+        if cfg.backward:
+            plan.backward(d["dY"])
+            if cfg.bias_update:
+                plan.bias_update(b, cfg.gamma, cfg.bias_rule)
+
+    step()  # every kernel loaded before the counted step
+    torch.cuda.synchronize()
+    kernels = []
+    for _ in range(2):  # the profiler's first session in a process may record no activity
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step()
+            torch.cuda.synchronize()
+        kernels = [e.name for e in prof.events() if e.device_type == DeviceType.CUDA]
+        if kernels:
+            break
+    if not kernels:
+        pytest.skip("the profiler recorded no CUDA activity on this machine")
+    ours = [n for n in kernels if "moe::" in n]
+    want = plan.launches_per_step(cfg.backward, cfg.bias_update)
+    counts = {}
+    for n in ours:
+        key = n.split("(")[0].replace("(anonymous namespace)::", "")
+        counts[key] = counts.get(key, 0) + 1
+    assert len(ours) == want, (len(ours), want, counts)
