@@ -336,7 +336,8 @@ def combine(Y_perm: np.ndarray, gate: np.ndarray, slot_to_row: np.ndarray,
 def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                   logits: np.ndarray | None = None, idx: np.ndarray | None = None,
                   rnd=None, aux: tuple | None = None, fp8: bool = False,
-                  fold_gate: bool = False, fp8_dgrad: bool = False) -> dict:
+                  fold_gate: bool = False, fp8_dgrad: bool = False,
+                  router_rows: bool = False) -> dict:
     """Full forward of the layer from fp64 copies of the inputs.
 
     ``logits`` replaces the fp64 router logits (used to replay the GPU's fp32 logits, so
@@ -345,7 +346,11 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
     ``fold_gate`` applies each slot's gate inside its expert (before the linear down
     projection) and combines without weights: the same value in exact arithmetic, and with
     ``rnd`` the rounding of a layout that stores the gated h and y. ``fp8_dgrad`` marks the
-    layer whose backward data-gradient products take FP8 operands (``layer_backward``)."""
+    layer whose backward data-gradient products take FP8 operands (``layer_backward``).
+    ``router_rows`` marks a backward that adds the router's input-gradient term to each
+    slot's expert row before that row is stored (``layer_backward``): sigmoid routing
+    without balancing losses only, where the logit gradient of a token is nonzero only at
+    its chosen experts."""
     x = inp["x"]
     E = inp["W_r"].shape[0]
     if logits is None:
@@ -368,9 +373,11 @@ def layer_forward(inp: dict, mode: str, k: int, z_coef: float = 0.0,
                   disp["slot_to_row"], None if shared is None else shared[3], rnd)
     if fp8_dgrad and fold_gate:
         raise ValueError("the FP8 data gradients take the ungated rows; fold_gate is bf16 only")
+    if router_rows and (mode != SIGMOID or aux is not None):
+        raise ValueError("the router term fits the expert rows only for sparse logit gradients")
     res = {**r, **disp, **ex, "X_perm": x_perm, "out": out, "mode": mode, "k": k,
            "z_coef": z_coef, "rnd": rnd, "aux": aux, "row_gate": row_gate,
-           "fp8_dgrad": fp8_dgrad}
+           "fp8_dgrad": fp8_dgrad, "router_rows": router_rows}
     if aux is not None:  # (seq_len, switch_coef, seq_coef)
         a = aux_losses(logits, r["idx"], mode, *aux)
         res["aux_switch"], res["aux_seq"] = a["switch"], a["seq"]
@@ -459,7 +466,7 @@ def expert_backward(dy: np.ndarray, x: np.ndarray, a: np.ndarray, u: np.ndarray,
     da, du = swiglu_backward(dh, a, u)
     da, du = _r(rnd, da), _r(rnd, du)
     dx = fp8_dgrad_dx(da, du, W_g, W_u) if fp8_dgrad else da @ W_g + du @ W_u
-    res = {"dA": da, "dU": du, "dX": _r(rnd, dx),
+    res = {"dA": da, "dU": du, "dX": _r(rnd, dx), "dX_exact": dx,
            "dW_d": _r(rnd, dy.T @ h), "dW_g": _r(rnd, da.T @ x), "dW_u": _r(rnd, du.T @ x)}
     if row_gate is not None:
         res["dg_row"] = np.sum(r * silu(a) * u, axis=1)
@@ -531,6 +538,8 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = No
         dW_g = np.zeros(inp["W_g"].shape); dW_u = np.zeros(inp["W_u"].shape)
         dW_d = np.zeros(inp["W_d"].shape)
     dA = np.zeros((N, f)); dU = np.zeros((N, f))
+    rows_term = bool(fwd.get("router_rows"))
+    dX_exact = np.zeros((N, d)) if rows_term else None
     for e in range(E):
         lo, hi = int(offs[e]), int(offs[e + 1])
         if hi == lo:
@@ -543,6 +552,8 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = No
         if row_gate is not None:
             dg[tok[lo:hi], slot[lo:hi]] = g["dg_row"]
         dX_perm[lo:hi], dA[lo:hi], dU[lo:hi] = g["dX"], g["dA"], g["dU"]
+        if rows_term:
+            dX_exact[lo:hi] = g["dX_exact"]
         if weight_grads:
             dW_g[e], dW_u[e], dW_d[e] = g["dW_g"], g["dW_u"], g["dW_d"]
     res = {"dY_perm": dY_perm, "dg": dg, "dA": dA, "dU": dU, "dX_perm": dX_perm}
@@ -561,8 +572,27 @@ def layer_backward(inp: dict, fwd: dict, dY: np.ndarray, T_norm: int | None = No
     rb = router_backward(dg, fwd, inp["x"], inp["W_r"], fwd["mode"], fwd["z_coef"],
                          T_norm=T_norm, dl_extra=dl_aux)
     res.update(rb)
-    res["dx"] = input_gradient(dX_perm, s2r, res.get("dx_shared"), rb["dx_r"], rnd)
+    if rows_term:
+        # each chosen slot's row carries its token's router term dl[t, e] W_r[e] before the
+        # row is stored; the token sum then has no separate router summand (the same value
+        # in exact arithmetic: the logit gradient is zero off the chosen experts)
+        terms = slot_router_terms(rb["dlogits"], idx, inp["W_r"])
+        for i in range(k):
+            rws = s2r[:, i]
+            dX_perm[rws] = _r(rnd, dX_exact[rws] + terms[:, i])
+        res["dX_perm"] = dX_perm
+        res["dx"] = input_gradient(dX_perm, s2r, res.get("dx_shared"), None, rnd)
+    else:
+        res["dx"] = input_gradient(dX_perm, s2r, res.get("dx_shared"), rb["dx_r"], rnd)
     return res
+
+
+def slot_router_terms(dlogits: np.ndarray, idx: np.ndarray, W_r: np.ndarray) -> np.ndarray:
+    """[T, k, d]: each chosen slot's share of the router's input gradient dl W_r, i.e.
+    dl[t, idx[t, i]] W_r[idx[t, i]]. Their sum over the slots is dl W_r whenever dl is zero
+    off the chosen experts."""
+    T, k = idx.shape
+    return dlogits[np.arange(T)[:, None], idx][:, :, None] * W_r[idx]
 
 
 def combine_backward(dY, Y_perm, gate, slot_to_row, perm_token, perm_slot, rnd=None):

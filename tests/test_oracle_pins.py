@@ -313,6 +313,41 @@ def test_backward_matches_central_finite_differences(mode, aux):
         assert np.abs(ana - num).max() / scale < 1e-6, p
 
 
+@pytest.mark.parametrize("fs", [0, 4])
+def test_router_term_in_the_expert_rows_is_the_same_layer(fs):
+    """Sigmoid routing without balancing losses: a token's logit gradient is zero off its
+    chosen experts, so adding dl[t, e] W_r[e] to the expert row of each chosen slot (t, e),
+    instead of forming dl W_r as a separate summand, gives the same input gradient in exact
+    arithmetic, and with bf16 storage the same up to the rounding of the rows; every other
+    gradient is untouched. The option is refused where the logit gradient is dense."""
+    rng = np.random.default_rng(37)
+    inp = _tiny_inputs(rng, T=40, d=8, E=6, f=6, fs=fs)
+    dY = rng.standard_normal((40, 8))
+    f0 = O.layer_forward(inp, "sigmoid", 3)
+    f1 = O.layer_forward(inp, "sigmoid", 3, router_rows=True)
+    b0, b1 = O.layer_backward(inp, f0, dY), O.layer_backward(inp, f1, dY)
+    np.testing.assert_allclose(b1["dx"], b0["dx"], rtol=1e-12, atol=1e-13)
+    for name in ("dg", "dlogits", "dW_r", "dW_g", "dW_u", "dW_d"):
+        np.testing.assert_array_equal(b1[name], b0[name], err_msg=name)
+    # the rows really carry the term: their difference is the router term of their slots
+    s2r, idx = f1["slot_to_row"], f1["idx"]
+    for i in range(3):
+        diff = b1["dX_perm"][s2r[:, i]] - b0["dX_perm"][s2r[:, i]]
+        want = b0["dlogits"][np.arange(40), idx[:, i]][:, None] * inp["W_r"][idx[:, i]]
+        np.testing.assert_allclose(diff, want, rtol=1e-10, atol=1e-13)
+    assert np.abs(b0["dx_r"]).max() > 1e-3  # the term is not negligible here
+    # with bf16 storage: within the rounding of k + 1 rows of the token sum
+    s0 = O.layer_forward(inp, "sigmoid", 3, rnd=O.bf16_round, fold_gate=True)
+    s1 = O.layer_forward(inp, "sigmoid", 3, rnd=O.bf16_round, fold_gate=True, router_rows=True)
+    c0, c1 = O.layer_backward(inp, s0, dY), O.layer_backward(inp, s1, dY)
+    bound = 6 * 2.0 ** -8 * (np.abs(b0["dx"]) + 3 * np.abs(b0["dX_perm"]).max())
+    assert (np.abs(c1["dx"] - c0["dx"]) <= bound).all()
+    with pytest.raises(ValueError):
+        O.layer_forward(inp, "softmax", 3, router_rows=True)
+    with pytest.raises(ValueError):
+        O.layer_forward(inp, "sigmoid", 3, aux=(20, 0.01, 0.01), router_rows=True)
+
+
 @pytest.mark.parametrize("mode,fs,aux", [("sigmoid", 0, None), ("sigmoid", 4, (5, 0.2, 0.3)),
                                          ("softmax", 0, None)])
 def test_gate_folded_into_experts_is_the_same_layer(mode, fs, aux):

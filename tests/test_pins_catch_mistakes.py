@@ -348,8 +348,13 @@ def _expert_bwd_fp8_dgrad_ignored(*a, fp8_dgrad=False, **kw):
     return ORIG["expert_backward"](*a, **kw)
 
 
+def _slot_router_terms_without_dlogits(dlogits, idx, W_r):
+    return W_r[idx] * 0.1
+
+
 MUTANTS = {
     "silu with sigmoid(-z)": ("silu", _silu_wrong_sign),
+    "router term in the rows without the logit gradient": ("slot_router_terms", _slot_router_terms_without_dlogits),
     "sigmoid with the wrong sign": ("sigmoid", _sigmoid_wrong_sign),
     "SwiGLU backward drops silu's product-rule term": ("swiglu_backward", _swiglu_bwd_drops_sigmoid_derivative),
     "SwiGLU backward du misses the factor a": ("swiglu_backward", _swiglu_bwd_du_without_a),
