@@ -401,13 +401,29 @@ int moe_combine_bwd_fp8(const moe_bf16* dY, const moe_bf16* Y_perm, const float*
  *      needs no change) and gate_part[p, j] = sum over columns 64j .. 64j+63 of
  *      r * silu(a) * u, in column order (h recomputed in fp32 from a and u): the gate's
  *      gradient in f/64 partial sums. gate_part is [rows, f/64] fp32.
+ * parts: which products to run, any union of MOE_BWD_DH (dh and dA, dU; with the gate
+ *      folded, gate_part), MOE_BWD_DX (dX, from dA and dU) and MOE_BWD_W (the weight
+ *      gradients, from dY, X, H, dA, dU); MOE_BWD_ALL for the whole backward. A caller that
+ *      needs the gate's gradient before dX (to form the router term below) runs MOE_BWD_DH
+ *      first and the rest after, on the same stream. Other values: MOE_ERR_INVALID_ARG.
+ * Router term in the rows (dl_rows and W_r both given, else both NULL; routed layout only):
+ *      dX[p] += dl_rows[p] * W_r[e] for each row p of expert e, in fp32 before the row is
+ *      rounded, where dl_rows [rows] fp32 holds the logit gradient of each row's slot
+ *      (moe_route_bwd writes it) and W_r [E, d] fp32 is the router weight (16-byte
+ *      aligned). With sigmoid routing and no balancing losses this is the whole router
+ *      input gradient, so moe_permute_bwd then takes neither dlogits nor dx_router.
  */
+#define MOE_BWD_DH 1
+#define MOE_BWD_DX 2
+#define MOE_BWD_W 4
+#define MOE_BWD_ALL 7
 int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* A,
                    const moe_bf16* U, const moe_bf16* H, const int64_t* row_offsets, int E,
                    int64_t rows, int d, int f, const moe_bf16* W_g, const moe_bf16* W_u,
                    const moe_bf16* W_d, moe_bf16* dX, moe_bf16* dA, moe_bf16* dU,
                    moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, const float* row_gate,
-                   float* gate_part, void* ws, size_t ws_bytes, moe_stream_t stream);
+                   float* gate_part, int parts, const float* dl_rows, const float* W_r,
+                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_row_gates - each slot's gate at its row of the expert-major layout, for folding the
@@ -444,12 +460,18 @@ int moe_gate_grad(const float* gate_part, const int32_t* slot_to_row, int64_t T,
  *      NULL: a further logit gradient (the balancing losses') added before dW_r is formed.
  * Out: dlogits [T,E] fp32 (consumed by moe_permute_bwd for the router's dx term);
  *      dW_r [E,d] fp32.
+ * Optional (both or neither; MOE_MODE_SIGMOID without dlogits_extra, where a token's logit
+ *      gradient is zero off its chosen experts; else MOE_ERR_INVALID_ARG): slot_to_row
+ *      [T,k] int32 in, dl_rows [rows] fp32 out: dl_rows[slot_to_row[t,i]] =
+ *      dlogits[t, topk_idx[t,i]], for moe_expert_bwd's router term in the rows. Other
+ *      entries of dl_rows are left as they were.
  */
 int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* topk_idx,
                   const float* topk_gate, const float* topk_score, const float* logits,
                   const float* lse, const float* dlogits_extra, int64_t T, int d, int E, int k,
-                  int mode, float z_coef, float* dlogits, float* dW_r, void* ws,
-                  size_t ws_bytes, moe_stream_t stream);
+                  int mode, float z_coef, float* dlogits, float* dW_r,
+                  const int32_t* slot_to_row, float* dl_rows, void* ws, size_t ws_bytes,
+                  moe_stream_t stream);
 
 /*
  * moe_aux_loss - load-balancing losses of the router (forward).

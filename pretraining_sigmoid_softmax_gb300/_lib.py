@@ -45,11 +45,11 @@ PROTOTYPES = {
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P]),
     "moe_combine_bwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P,
-                            _P, _P, _P, _P, _P, _SZ, _P]),
+                            _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "moe_row_gates": (_I, [_P, _P, _I64, _I, _I64, _P, _P]),
     "moe_gate_grad": (_I, [_P, _P, _I64, _I, _I, _P, _P]),
     "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _F, _P, _P, _P,
-                           _SZ, _P]),
+                           _P, _P, _SZ, _P]),
     "moe_aux_loss": (_I, [_P, _P, _I64, _I, _I, _I, _I64, _F, _F, _P, _P, _P, _SZ, _P]),
     "moe_aux_loss_bwd": (_I, [_P, _P, _I64, _I, _I, _I64, _F, _F, _P, _P]),
     "moe_permute_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P]),

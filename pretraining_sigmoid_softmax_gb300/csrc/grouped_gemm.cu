@@ -145,6 +145,10 @@ struct Params {
     const float* row_scale;    // gate folded into the expert: G1 writes g*h, B2 forms g*dh
     float* gate_part;          // B2 with row_scale: per row, (dy W_d) . h per 64 columns
     int ld_out;                // B2: output columns; gate_part holds ld_out / 64 per row
+    // B4 with the router's input-gradient term in the rows: row += r1_row[row] * r1_col[e][col]
+    // (the slot's logit gradient times its expert's router row, both fp32)
+    const float* r1_row;
+    const float* r1_col;
     int* status;
     uint64_t wait_limit_ns;
 };
@@ -453,6 +457,21 @@ __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const Ti
 #pragma unroll
             for (int j = 0; j < W; ++j) v[0][j] = __uint_as_float(r[j]);
             if constexpr (C::FP8) fp8_scale<W>(v[0], v[0], P, row, ti, c, /*dual=*/false);
+            if constexpr (C::TWO_K && !C::FP8) {
+                if (P.r1_row) {  // the slot's router term, one fp32 FMA per element
+                    const float g = __ldg(P.r1_row + row);
+                    const float4* w = reinterpret_cast<const float4*>(
+                        P.r1_col + (int64_t)ti.e * P.N + ti.n0 + c);
+#pragma unroll
+                    for (int j = 0; j < W / 4; ++j) {
+                        const float4 w4 = __ldg(w + j);
+                        v[0][4 * j] = fmaf(g, w4.x, v[0][4 * j]);
+                        v[0][4 * j + 1] = fmaf(g, w4.y, v[0][4 * j + 1]);
+                        v[0][4 * j + 2] = fmaf(g, w4.z, v[0][4 * j + 2]);
+                        v[0][4 * j + 3] = fmaf(g, w4.w, v[0][4 * j + 3]);
+                    }
+                }
+            }
         }
         uint8_t* buf = S.ob + ((size_t)slot * C::OUT_DEPTH + n % C::OUT_DEPTH) * C::OUT_BUF_BYTES;
         if (lane == 0) bulk_wait_read<C::OUT_DEPTH - 1>();  // the store that last read it is done
@@ -1058,12 +1077,16 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
                               int E, int64_t rows, int d, int f, const moe_bf16* W_g,
                               const moe_bf16* W_u, const moe_bf16* W_d, moe_bf16* dX,
                               moe_bf16* dA, moe_bf16* dU, moe_bf16* dW_g, moe_bf16* dW_u,
-                              moe_bf16* dW_d, const float* row_gate, float* gate_part, void* ws,
-                              size_t ws_bytes, moe_stream_t stream) {
+                              moe_bf16* dW_d, const float* row_gate, float* gate_part, int parts,
+                              const float* dl_rows, const float* W_r, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
     if (!dY || !X || !A || !U || !H || !W_g || !W_u || !W_d || !dX || !dA || !dU || !dW_g ||
         !dW_u || !dW_d)
         return MOE_ERR_INVALID_ARG;
     if ((row_gate == nullptr) != (gate_part == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (parts <= 0 || parts > MOE_BWD_ALL) return MOE_ERR_INVALID_ARG;
+    if ((dl_rows == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (W_r && (!row_offsets || !aligned16(W_r))) return MOE_ERR_INVALID_ARG;
     if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
     const void* ptrs[14] = {dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d};
@@ -1079,7 +1102,7 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
 
     // B2: dH = dY W_d (W_d[e] is [d, f]: K = d rows, N = f contiguous), SwiGLU backward; the
     // saved a and u are staged by TMA (their maps ride in the second A and B slots)
-    {
+    if (parts & MOE_BWD_DH) {
         constexpr CUtensorMapSwizzle kAuSwz = kAuCols == 32   ? CU_TENSOR_MAP_SWIZZLE_64B
                                               : kAuCols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
                                                               : CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -1106,8 +1129,9 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
                                            mod);
         if (rc != MOE_OK) return rc;
     }
-    // B4: dX = dA W_g + dU W_u (W_g[e] is [f, d]: K = f rows, N = d contiguous)
-    {
+    // B4: dX = dA W_g + dU W_u (W_g[e] is [f, d]: K = f rows, N = d contiguous), plus each
+    // row's router term when given
+    if (parts & MOE_BWD_DX) {
         CUtensorMap mda, mdu, mwg, mwu;
         if (!make_map(&mda, dA, f, rows, 64, 128) || !make_map(&mdu, dU, f, rows, 64, 128) ||
             !make_map(&mwg, W_g, d, (uint64_t)E * f, 64, 64) ||
@@ -1118,6 +1142,8 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
         P.K0 = f;
         P.K1 = f;
         P.kb_per_expert = f;
+        P.r1_row = dl_rows;
+        P.r1_col = W_r;
         CUtensorMap mox[3];
         if (!out_maps(mox, dX, nullptr, nullptr, d, rows)) return MOE_ERR_LAUNCH;
         if (d % 256 == 0)
@@ -1126,6 +1152,7 @@ extern "C" int moe_expert_bwd(const moe_bf16* dY, const moe_bf16* X, const moe_b
             rc = launch<CfgDgrad2<128>>(mda, mdu, mwg, mwu, P, token_tiles_max(rows, d, 128), st, mox);
         if (rc != MOE_OK) return rc;
     }
+    if (!(parts & MOE_BWD_W)) return MOE_OK;
     return weight_grads(dY, X, H, dA, dU, row_offsets, E, rows, d, f, order, dW_g, dW_u, dW_d, st);
 }
 

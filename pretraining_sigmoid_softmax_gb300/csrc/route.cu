@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
     const float* __restrict__ topk_gate, const float* __restrict__ topk_score,
     const float* __restrict__ logits, const float* __restrict__ lse,
     const float* __restrict__ extra, int64_t T, int E, int k, int mode, float z_scale,
-    float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dl3, int np, int64_t pstride) {
+    float* __restrict__ dlogits, __nv_bfloat16* __restrict__ dl3, int np, int64_t pstride,
+    const int32_t* __restrict__ slot_to_row, float* __restrict__ dl_rows) {
     const int lane = threadIdx.x % 32;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (t >= T) return;
@@ -293,6 +294,10 @@ __global__ void __launch_bounds__(256) route_bwd_dlogits_kernel(
     const int ecount = dl3 ? np : E;
     const float ds = (my_dg - gdg) / S;
     const float vs = ds * my_s * (1.f - my_s);
+    if (dl_rows && lane < k) {  // sigmoid mode, no extra term: the slot's own logit gradient
+        const int32_t r = slot_to_row[t * k + lane];
+        if (r >= 0) dl_rows[r] = vs;
+    }
     const float l_se = mode == MOE_MODE_SIGMOID ? 0.f : lse[t];
     for (int e0 = 0; e0 < ecount; e0 += 32) {  // warp-uniform trip count
         const int e = e0 + lane;
@@ -625,10 +630,12 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
                              const float* topk_gate, const float* topk_score,
                              const float* logits, const float* lse, const float* dlogits_extra,
                              int64_t T, int d, int E, int k, int mode, float z_coef,
-                             float* dlogits, float* dW_r, void* ws, size_t ws_bytes,
-                             moe_stream_t stream) {
+                             float* dlogits, float* dW_r, const int32_t* slot_to_row,
+                             float* dl_rows, void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (!dg || !x || !topk_idx || !topk_gate || !topk_score || !dlogits || !dW_r)
         return MOE_ERR_INVALID_ARG;
+    if ((slot_to_row == nullptr) != (dl_rows == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (dl_rows && (mode != MOE_MODE_SIGMOID || dlogits_extra)) return MOE_ERR_INVALID_ARG;
     if (T <= 0 || d <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
     if (mode != MOE_MODE_SIGMOID && mode != MOE_MODE_SOFTMAX) return MOE_ERR_INVALID_ARG;
     if (mode == MOE_MODE_SOFTMAX && (!logits || !lse)) return MOE_ERR_INVALID_ARG;
@@ -649,7 +656,7 @@ extern "C" int moe_route_bwd(const float* dg, const moe_bf16* x, const int32_t* 
     const float z_scale = 2.0f * z_coef / (float)T;
     route_bwd_dlogits_kernel<<<(unsigned)cdiv(T, 8), 256, 0, st>>>(
         dg, topk_idx, topk_gate, topk_score, logits, lse, dlogits_extra, T, E, k, mode, z_scale,
-        dlogits, dl3, np, pstride);
+        dlogits, dl3, np, pstride, slot_to_row, dl_rows);
     if (launch_status() != MOE_OK) return MOE_ERR_LAUNCH;
     if (np) {
         int rc = launch_route_dwr_tc(reinterpret_cast<const __nv_bfloat16*>(x), dl3, pstride, T,

@@ -55,6 +55,7 @@ class MoEPlan:
     # layer (T 65536, d 4096, shared 3072: 14.8 TFLOP) 51.3 -> 52.7 ms, as it runs at the
     # power cap, where concurrent kernels add interference and no energy budget.
     OVERLAP_SHARED_MAX_FLOPS = 1e12
+    ROUTER_ROWS_MIN_FF = 768
 
     def __init__(self, shape: MoEShape, device="cuda", backward: bool = True,
                  overlap_shared: bool | None = None):
@@ -119,6 +120,7 @@ class MoEPlan:
             self.aux_loss = torch.zeros((2,), dtype=f32, device=dev)
             self.aux_f = _empty((E + (T // s.seq_len) * E,), f32, dev)
         self.has_backward = backward
+        self.router_rows, self.dl_rows = False, None
         if backward and s.fp8_dgrad:  # E4M3 operands of the data-gradient GEMMs
             u8 = torch.uint8
             self.dYq, self.sdY = _empty((R, d), u8, dev), _empty((R,), f32, dev)
@@ -148,6 +150,17 @@ class MoEPlan:
             # dense logit gradients (softmax router, balancing losses): the router's input-
             # gradient term runs on the tensor cores instead of in the dx kernel's row loop
             self.router_dx_tc = (s.mode == ops.MODE_SOFTMAX or s.has_aux) and E <= 128
+            # sigmoid routing without balancing losses: a token's logit gradient is zero off
+            # its chosen experts, so its router input-gradient term dl[t, e] W_r[e] joins
+            # each chosen slot's dX row in the data-gradient GEMM's epilogue, and the token
+            # sum reads no fp32 W_r rows (large layer: 1.05 -> 0.80 ms for the token sum).
+            # That GEMM's reduction is K = 2 d_ff; below ROUTER_ROWS_MIN_FF its epilogue sets
+            # its pace and the term costs more there than it saves (small fine-grained
+            # layer, d_ff 256: 0.675 -> 0.681 ms per step), so short experts keep the term
+            # in the token sum.
+            self.router_rows = (self.fold_gate and s.mode == ops.MODE_SIGMOID
+                                and not s.has_aux and s.f >= self.ROUTER_ROWS_MIN_FF)
+            self.dl_rows = torch.zeros((R,), dtype=f32, device=dev) if self.router_rows else None
             self.dx_r = _empty((T, d), f32, dev) if self.router_dx_tc else None
             self.dW_r = _empty((E, d), f32, dev)
             self.dx = _empty((T, d), bf, dev)
@@ -284,10 +297,13 @@ class MoEPlan:
             # the expert backward applies each row's gate and sums the gate's gradient in parts
             ops.moe_combine_bwd(dY, None, None, self.slot_to_row, self.row_offsets,
                                 self.perm_token, self.dY_perm, None, stream)
+            # with the router term in the rows, dX and the weight gradients wait for the
+            # logit gradient (below); the gate's gradient comes from the dh pass alone
             self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
                        self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
                        self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
-                       row_gate=self.row_gate, gate_part=self.gate_part)
+                       row_gate=self.row_gate, gate_part=self.gate_part,
+                       parts=ops.BWD_DH if self.router_rows else ops.BWD_ALL)
             ops.moe_gate_grad(self.gate_part, self.slot_to_row, s.f, self.dg, stream)
         elif s.fp8_dgrad:  # the combine backward also writes the codes of the rows it stores
             ops.moe_combine_bwd_fp8(dY, self.Y_perm, self.topk_gate, self.slot_to_row,
@@ -311,10 +327,17 @@ class MoEPlan:
             ops.moe_aux_loss_bwd(self.logits, self.aux_f, s.mode, s.seq_len, s.aux_switch,
                                  s.aux_seq, self.dlogits_aux, stream)
             extra = self.dlogits_aux
+        rows = self.router_rows
         ops.moe_route_bwd(self.dg, x, self.topk_idx, self.topk_gate, self.topk_score,
                           self.logits if softmax else None, self.lse if softmax else None, s.E,
                           s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream,
-                          dlogits_extra=extra)
+                          dlogits_extra=extra, slot_to_row=self.slot_to_row if rows else None,
+                          dl_rows=self.dl_rows)
+        if rows:
+            self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
+                       self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
+                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
+                       parts=ops.BWD_DX | ops.BWD_W, dl_rows=self.dl_rows, W_r=W_r)
         if s.f_shared:
             if self.overlap:  # join
                 main.wait_stream(self.side)
@@ -325,6 +348,8 @@ class MoEPlan:
             ops.moe_router_dx(self.dlogits, W_r, self.dx_r, self.ws, stream)
             ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, None, None, self.dx, stream,
                                 dx_router=self.dx_r)
+        elif rows:  # the router term is already in the rows
+            ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, None, None, self.dx, stream)
         else:
             ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx,
                                 stream)

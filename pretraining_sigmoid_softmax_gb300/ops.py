@@ -211,16 +211,24 @@ def moe_combine_bwd(dY, Y_perm, topk_gate, slot_to_row, row_offsets, perm_token,
                                        _p(dg), _stream(stream)), "moe_combine_bwd")
 
 
+BWD_DH, BWD_DX, BWD_W, BWD_ALL = 1, 2, 4, 7  # moe_expert_bwd's parts
+
+
 def moe_expert_bwd(dY, X, A, U, H, row_offsets, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws,
-                   stream=None, row_gate=None, gate_part=None):
-    """row_gate with gate_part [rows, f/64] fp32: the gate-folded backward (see the header)."""
+                   stream=None, row_gate=None, gate_part=None, parts=BWD_ALL, dl_rows=None,
+                   W_r=None):
+    """row_gate with gate_part [rows, f/64] fp32: the gate-folded backward; parts: which
+    products run; dl_rows [rows] with W_r [E, d] fp32: the router term in dX's rows (see the
+    header)."""
     rows, d = X.shape
     E, f, _ = W_g.shape
-    _contig(dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws, row_gate, gate_part)
+    _contig(dY, X, A, U, H, W_g, W_u, W_d, dX, dA, dU, dW_g, dW_u, dW_d, ws, row_gate, gate_part,
+            dl_rows, W_r)
     _check(_lib.load().moe_expert_bwd(_p(dY), _p(X), _p(A), _p(U), _p(H), _p(row_offsets), E, rows,
                                       d, f, _p(W_g), _p(W_u), _p(W_d), _p(dX), _p(dA), _p(dU),
                                       _p(dW_g), _p(dW_u), _p(dW_d), _p(row_gate), _p(gate_part),
-                                      _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+                                      int(parts), _p(dl_rows), _p(W_r), _p(ws),
+                                      0 if ws is None else ws.numel(), _stream(stream)),
            "moe_expert_bwd")
 
 
@@ -267,14 +275,16 @@ def moe_gate_grad(gate_part, slot_to_row, f, dg, stream=None):
 
 
 def moe_route_bwd(dg, x, topk_idx, topk_gate, topk_score, logits, lse, E, mode, z_coef, dlogits,
-                  dW_r, ws, stream=None, dlogits_extra=None):
+                  dW_r, ws, stream=None, dlogits_extra=None, slot_to_row=None, dl_rows=None):
+    """slot_to_row with dl_rows [rows] fp32: each slot's logit gradient at its row as well."""
     T, k = topk_idx.shape
     d = x.shape[1]
-    _contig(dg, x, topk_idx, topk_gate, topk_score, logits, lse, dlogits, dW_r, ws, dlogits_extra)
+    _contig(dg, x, topk_idx, topk_gate, topk_score, logits, lse, dlogits, dW_r, ws, dlogits_extra,
+            slot_to_row, dl_rows)
     _check(_lib.load().moe_route_bwd(_p(dg), _p(x), _p(topk_idx), _p(topk_gate), _p(topk_score),
                                      _p(logits), _p(lse), _p(dlogits_extra), T, d, E, k, mode,
-                                     float(z_coef), _p(dlogits), _p(dW_r), _p(ws), ws.numel(),
-                                     _stream(stream)),
+                                     float(z_coef), _p(dlogits), _p(dW_r), _p(slot_to_row),
+                                     _p(dl_rows), _p(ws), ws.numel(), _stream(stream)),
            "moe_route_bwd")
 
 

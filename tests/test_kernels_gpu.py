@@ -351,6 +351,53 @@ def test_routed_expert_gemms(counts, d, f):
             assert (B[name][lo + c:int(ro[e + 1])].float() == 0).all(), f"{name} padding {e}"
 
 
+@pytest.mark.parametrize("counts,d,f", [([130, 0, 5, 256, 1], 256, 128), ([300, 129], 384, 256)])
+def test_router_term_in_the_dx_rows(counts, d, f):
+    """moe_expert_bwd in two calls (dh first, then dX and the weight gradients) with the
+    router term: each row's dX gains dl_rows[p] * W_r[e] before it is rounded; dA, dU and
+    the weight gradients are bit for bit those of the single call without the term."""
+    E = len(counts)
+    g = torch.Generator().manual_seed(sum(counts) + 3 * d)
+    ro = padded_offsets(counts)
+    rows = int(ro[-1]) + 128
+    X = torch.zeros(rows, d, dtype=torch.bfloat16)
+    dY = torch.zeros(rows, d, dtype=torch.bfloat16)
+    for e in range(E):
+        X[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g)
+        dY[ro[e]:ro[e] + counts[e]] = randn_bf16((counts[e], d), g, 0.25)
+    W_g, W_u, W_d = _weights(E, d, f, g)
+    W_r = torch.randn(E, d, generator=g) * d ** -0.5
+    dl = torch.randn(rows, generator=g) * 0.3
+    B0 = _run_experts(X, dY, ro, W_g, W_u, W_d)  # the single call, no term
+    B1 = _expert_buffers(rows, d, f, E)
+    ws = _ws(rows, d, E, 1)
+    rod = dev(torch.from_numpy(ro))
+    for k in ("A", "U", "H"):
+        B1[k].copy_(B0[k])
+    args = (dev(dY), dev(X), B1["A"], B1["U"], B1["H"], rod, dev(W_g), dev(W_u), dev(W_d),
+            B1["dX"], B1["dA"], B1["dU"], B1["dW_g"], B1["dW_u"], B1["dW_d"], ws)
+    ops.moe_expert_bwd(*args, parts=ops.BWD_DH)
+    ops.moe_expert_bwd(*args, parts=ops.BWD_DX | ops.BWD_W, dl_rows=dev(dl), W_r=dev(W_r))
+    torch.cuda.synchronize()
+    assert ops.moe_device_status()[0] == 0
+    for name in ("dA", "dU", "dW_g", "dW_u", "dW_d"):  # bits (rows past the layout hold NaN)
+        assert torch.equal(B1[name].view(torch.int16), B0[name].view(torch.int16)), name
+    rnd = O.bf16_round
+    for e in range(E):
+        lo, c = int(ro[e]), counts[e]
+        if c == 0:
+            continue
+        hi = lo + c
+        x = h64(X[lo:hi])
+        a, u, h, y = O.swiglu_expert(x, h64(W_g[e]), h64(W_u[e]), h64(W_d[e]), rnd)
+        gr = O.expert_backward(h64(dY[lo:hi]), x, a, u, h, h64(W_g[e]), h64(W_u[e]),
+                               h64(W_d[e]), rnd)
+        term = h64(dl[lo:hi])[:, None] * h64(W_r[e])[None, :]
+        assert_close(B1["dX"][lo:hi], rnd(gr["dX_exact"] + term), f"expert {e} dX with term")
+        # the term really moved the rows
+        assert not torch.equal(B1["dX"][lo:hi], B0["dX"][lo:hi])
+
+
 # -------------------------------------------------- gate folded into the experts
 
 @pytest.mark.parametrize("counts,d,f", [([130, 0, 5, 256, 1], 256, 256), ([77, 300, 0], 384, 128)])
@@ -549,6 +596,21 @@ def test_router_backward(mode, T, d, E, k):
     rb = O.router_backward(h64(dg), ref, h64(x), h64(W_r), mode, z)
     assert_close(dl, rb["dlogits"], "dlogits", atol=1e-5, rtol=1e-4)
     assert_close(dW_r, rb["dW_r"], "dW_r", atol=1e-3, rtol=1e-3, reduction=True)
+    if mode == "sigmoid":  # each slot's logit gradient at its row as well, the same bits
+        s2r = torch.randperm(T * k, generator=g).to(torch.int32).reshape(T, k) + 3
+        s2r[0, 0] = -1  # a dropped slot writes nothing
+        rows = torch.full((T * k + 3,), float("nan"), device="cuda")
+        dl2 = torch.empty(T, E, device="cuda")
+        ops.moe_route_bwd(dev(dg), dev(x), r["idx"], r["gate"], r["score"], None, None, E, m, z,
+                          dl2, dW_r, _ws(T, d, E, k), slot_to_row=dev(s2r), dl_rows=rows)
+        torch.cuda.synchronize()
+        assert torch.equal(dl2, dl)
+        idx = r["idx"].cpu().long()
+        want = dl.cpu().gather(1, idx)
+        got = rows.cpu()[s2r.long().clamp(min=0)]
+        live = s2r >= 0
+        assert torch.equal(got[live], want[live])
+        assert torch.isnan(rows.cpu()[:3]).all()  # rows that no slot maps to are left alone
 
 
 def test_bias_update_is_bit_exact():

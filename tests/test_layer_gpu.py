@@ -126,7 +126,10 @@ def full_parity(cfg, inp):
                               fp8_dgrad=f8d, **kw)
         return fwd, (O.layer_backward(i64, fwd, dY) if cfg.backward else None)
 
-    (P, PB), (S, SB) = both(lambda: run(), lambda: run(rnd=RND, fold_gate=not fp8))
+    # the storage model: bf16 rows, the gate folded into the bf16 layer's experts, and the
+    # router's input-gradient term in the rows where the plan puts it there
+    (P, PB), (S, SB) = both(lambda: run(), lambda: run(rnd=RND, fold_gate=not fp8,
+                                                       router_rows=plan.router_rows))
     case = cfg.name
     assert_close(plan.X_perm[torch.from_numpy(rows).cuda()], P["X_perm"], "X_perm", 0, 0)
     check_plain(case, "logits", plan.logits, P["logits"], S["logits"])
@@ -189,6 +192,10 @@ SMALL = [
     # fewer tokens than one tile row block: 7-row tensors behind 32- and 128-row boxes
     MoEConfig("sub_tile_T7", T=7, d=128, E=4, k=2, f=128, f_shared=128, mode="sigmoid",
               seed=19, backward=True, bias_update=True),
+    # experts long enough (d_ff 768) for the router's input-gradient term to ride in their
+    # dX rows
+    MoEConfig("router_term_in_rows", T=400, d=256, E=5, k=2, f=768, f_shared=256,
+              mode="sigmoid", seed=26, backward=True, bias_update=True),
     # the widest router (SIMT logits and W_r gradient), most experts with 0-3 rows
     MoEConfig("widest_router_E256", T=300, d=256, E=256, k=8, f=128, f_shared=0,
               mode="softmax", seed=20, backward=True, bias_update=False, z_coef=1e-3),
@@ -270,7 +277,10 @@ def test_workload_sampled_parity(name):
         return fwd, O.layer_backward(part, fwd, dY64[toks], T_norm=cfg.T, dl_extra=dl_aux,
                                      weight_grads=False)
 
-    (P, PB), (S, SB) = both(lambda: run(), lambda: run(rnd=RND, fold_gate=not fp8))
+    # the storage model: bf16 rows, the gate folded into the bf16 layer's experts, and the
+    # router's input-gradient term in the rows where the plan puts it there
+    (P, PB), (S, SB) = both(lambda: run(), lambda: run(rnd=RND, fold_gate=not fp8,
+                                                       router_rows=plan.router_rows))
     flips = FP8_CODE_FLIPS if fp8 else 0.0
     check_plain(case, "gates", plan.topk_gate[tt], P["gate"], S["gate"])
     check_plain(case, "out", plan.out[tt], P["out"], S["out"])
@@ -378,7 +388,8 @@ def test_cuda_graph_replay_matches_eager_step():
 
 LAUNCH_CASES = [CONFIGS["C1"], CONFIGS["C2"]] + [
     c for c in SMALL if c.name in ("aux_losses_sigmoid", "aux_losses_softmax", "fp8_forward_shared",
-                                   "fp8_dgrad_shared", "widest_router_E256", "one_expert_top1")]
+                                   "fp8_dgrad_shared", "widest_router_E256", "one_expert_top1",
+                                   "router_term_in_rows")]
 
 
 @pytest.mark.parametrize("cfg", LAUNCH_CASES, ids=lambda c: c.name)

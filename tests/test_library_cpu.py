@@ -139,6 +139,17 @@ def test_degenerate_and_inconsistent_arguments_are_rejected_on_the_host(lib):
     assert fwd(0, 1, None, P) == 1                  # no rows
     assert fwd(16, 2, None, P) == 1                 # no layout for two experts
     assert fwd(16, 1, None, bad) == 1               # misaligned operand
-    bwd = lambda rg, gp: lib.moe_expert_bwd(P, P, P, P, P, None, 1, 16, 256, 128, P, P, P, P, P, P,
-                                            P, P, P, rg, gp, ws, 1 << 20, None)
+    bwd = lambda rg, gp, parts=7, dl=None, wr=None, ro=None: lib.moe_expert_bwd(
+        P, P, P, P, P, ro, 1, 16, 256, 128, P, P, P, P, P, P, P, P, P, rg, gp, parts, dl, wr, ws,
+        1 << 20, None)
     assert bwd(P, None) == 1 and bwd(None, P) == 1  # row gates and gate partials come together
+    assert bwd(None, None, parts=0) == 1 and bwd(None, None, parts=8) == 1  # unknown parts
+    assert bwd(None, None, dl=P) == 1 and bwd(None, None, wr=P) == 1  # router term: both or neither
+    assert bwd(None, None, dl=P, wr=P) == 1         # the router term needs the routed layout
+    assert bwd(None, None, dl=P, wr=bad, ro=P) == 1  # misaligned router weight
+    rbwd = lambda mode, extra, s2r, dl: lib.moe_route_bwd(P, P, P, P, P, P, P, extra, 16, 256, 8,
+                                                          2, mode, 0.0, P, P, s2r, dl, ws, 1 << 20,
+                                                          None)
+    assert rbwd(0, None, P, None) == 1 and rbwd(0, None, None, P) == 1  # rows: both or neither
+    assert rbwd(1, None, P, P) == 1                 # softmax: the logit gradient is dense
+    assert rbwd(0, P, P, P) == 1                    # an extra (dense) logit gradient

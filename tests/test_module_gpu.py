@@ -55,7 +55,7 @@ def test_module_backward_matches_the_plain_definition(cfg):
     aux = (cfg.seq_len, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
     P = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, aux=aux)
     S = O.layer_forward(i64, cfg.mode, cfg.k, cfg.z_coef, idx=idx, rnd=O.bf16_round, aux=aux,
-                        fold_gate=True)
+                        fold_gate=True, router_rows=plan.router_rows)
     dY64 = O.to64(inp["dY"])
     PB, SB = O.layer_backward(i64, P, dY64), O.layer_backward(i64, S, dY64)
     case = "module " + cfg.name
