@@ -1179,11 +1179,12 @@ static int weight_grads(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* H
         P.M_out = d;
         P.nprob = 1;
         P.out0 = reinterpret_cast<__nv_bfloat16*>(dW_d);
-        if (d % 256 == 0 && f % 256 == 0)
-            rc = launch<CfgWgradP>(mdy, mdy, mh, mh, P, (int64_t)E * (d / 256) * (f / 256), st);
-        else if (f % 256 == 0)
+        const int64_t pair_tiles = (int64_t)E * (d / 256) * (f / 256);
+        if (d % 256 == 0 && f % 256 == 0 && 2 * pair_tiles >= sm_count())
+            rc = launch<CfgWgradP>(mdy, mdy, mh, mh, P, pair_tiles, st);
+        else if (f % 256 == 0 && !(d % 256 == 0 && 2 * pair_tiles < sm_count()))
             rc = launch<CfgWgrad<256>>(mdy, mdy, mh, mh, P, (int64_t)E * (d / BM) * (f / 256), st);
-        else
+        else  // also when there are few pair tiles: 128-wide tiles on 4x the SMs
             rc = launch<CfgWgrad<128>>(mdy, mdy, mh, mh, P, (int64_t)E * (d / BM) * (f / 128), st);
         if (rc != MOE_OK) return rc;
     }
@@ -1200,8 +1201,11 @@ static int weight_grads(const moe_bf16* dY, const moe_bf16* X, const moe_bf16* H
         P.nprob = 2;
         P.out0 = reinterpret_cast<__nv_bfloat16*>(dW_g);
         P.out1 = reinterpret_cast<__nv_bfloat16*>(dW_u);
-        if (d % 256 == 0 && f % 256 == 0)
-            rc = launch<CfgWgradP>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / 256) * (d / 256), st);
+        const int64_t pair_tiles = (int64_t)E * 2 * (f / 256) * (d / 256);
+        if (d % 256 == 0 && f % 256 == 0 && 2 * pair_tiles >= sm_count())
+            rc = launch<CfgWgradP>(mda, mdu, mxx, mxx, P, pair_tiles, st);
+        else if (d % 256 == 0 && f % 256 == 0)  // few pair tiles: 128-wide tiles on 4x the SMs
+            rc = launch<CfgWgrad<128>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 128), st);
         else if (d % 256 == 0)
             rc = launch<CfgWgrad<256>>(mda, mdu, mxx, mxx, P, (int64_t)E * 2 * (f / BM) * (d / 256), st);
         else
