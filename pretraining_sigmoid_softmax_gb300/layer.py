@@ -158,7 +158,7 @@ class MoEPlan:
             # its pace and the term costs more there than it saves (small fine-grained
             # layer, d_ff 256: 0.675 -> 0.681 ms per step), so short experts keep the term
             # in the token sum.
-            self.router_rows = (self.fold_gate and s.mode == ops.MODE_SIGMOID
+            self.router_rows = (not s.fp8_dgrad and s.mode == ops.MODE_SIGMOID
                                 and not s.has_aux and s.f >= self.ROUTER_ROWS_MIN_FF)
             self.dl_rows = torch.zeros((R,), dtype=f32, device=dev) if self.router_rows else None
             self.dx_r = _empty((T, d), f32, dev) if self.router_dx_tc else None
@@ -320,7 +320,8 @@ class MoEPlan:
                                 self.row_offsets, self.perm_token, self.dY_perm, self.dg, stream)
             self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
                        self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
-                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
+                       self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
+                       parts=ops.BWD_DH if self.router_rows else ops.BWD_ALL)
         dxs = None
         extra = None
         if s.has_aux:
