@@ -306,14 +306,17 @@ int moe_quantize_cols_fp8(const moe_bf16* X0, const moe_bf16* X1, int E, int K0,
  * Out: dX [rows, d], dA, dU [rows, f] bf16; AUq [rows, 2f] codes and sAU [rows] (the
  *      quantised [dA | dU]); dW_g, dW_u [E, f, d], dW_d [E, d, f] bf16.
  * The gate is not folded here (the FP8 layer combines with its gates); dY is g * dY[t].
+ * dl_rows and W_r (both or neither; routed layout only): the router term added to dX's rows
+ *      as in moe_expert_bwd, after the rows' scales are applied and before the rounding.
  */
 int moe_expert_bwd_fp8(const uint8_t* dYq, const float* sdY, const moe_bf16* dY,
                        const moe_bf16* X, const moe_bf16* A, const moe_bf16* U,
                        const moe_bf16* H, const int64_t* row_offsets, int E, int64_t rows, int d,
                        int f, const uint8_t* Wdq, const float* sWd, const uint8_t* Wguq,
                        const float* sWgu, moe_bf16* dX, moe_bf16* dA, moe_bf16* dU, uint8_t* AUq,
-                       float* sAU, moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, void* ws,
-                       size_t ws_bytes, moe_stream_t stream);
+                       float* sAU, moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d,
+                       const float* dl_rows, const float* W_r, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /*
  * moe_combine - gate-weighted sum of the expert outputs (C1).

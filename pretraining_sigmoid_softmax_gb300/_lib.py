@@ -38,7 +38,7 @@ PROTOTYPES = {
     "moe_quantize_rows2_fp8": (_I, [_P, _P, _P, _I64, _I, _P, _P, _P]),
     "moe_quantize_cols_fp8": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_expert_bwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I64, _I, _I, _P, _P, _P, _P,
-                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I64, _I, _I, _P, _P]),
     "moe_bias_update": (_I, [_P, _I, _I64, _I, _F, _P, _P]),
     "moe_bias_update_proportional": (_I, [_P, _I, _I64, _I, _F, _P, _P]),

@@ -457,7 +457,7 @@ __device__ __forceinline__ void epilogue_tma_store(const SmemLayout& S, const Ti
 #pragma unroll
             for (int j = 0; j < W; ++j) v[0][j] = __uint_as_float(r[j]);
             if constexpr (C::FP8) fp8_scale<W>(v[0], v[0], P, row, ti, c, /*dual=*/false);
-            if constexpr (C::TWO_K && !C::FP8) {
+            if constexpr (C::EPI == kEpiStore && !C::WGRAD) {
                 if (P.r1_row) {  // the slot's router term, one fp32 FMA per element
                     const float g = __ldg(P.r1_row + row);
                     const float4* w = reinterpret_cast<const float4*>(
@@ -1220,11 +1220,14 @@ extern "C" int moe_expert_bwd_fp8(const uint8_t* dYq, const float* sdY, const mo
                                   int64_t rows, int d, int f, const uint8_t* Wdq, const float* sWd,
                                   const uint8_t* Wguq, const float* sWgu, moe_bf16* dX,
                                   moe_bf16* dA, moe_bf16* dU, uint8_t* AUq, float* sAU,
-                                  moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d, void* ws,
+                                  moe_bf16* dW_g, moe_bf16* dW_u, moe_bf16* dW_d,
+                                  const float* dl_rows, const float* W_r, void* ws,
                                   size_t ws_bytes, moe_stream_t stream) {
     if (!dYq || !sdY || !dY || !X || !A || !U || !H || !Wdq || !sWd || !Wguq || !sWgu || !dX ||
         !dA || !dU || !AUq || !sAU || !dW_g || !dW_u || !dW_d)
         return MOE_ERR_INVALID_ARG;
+    if ((dl_rows == nullptr) != (W_r == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (W_r && (!row_offsets || !aligned16(W_r))) return MOE_ERR_INVALID_ARG;
     if (E <= 0 || rows <= 0 || (!row_offsets && E != 1)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxExperts || !gemm_shape_ok(d, f)) return MOE_ERR_UNSUPPORTED;
     const void* ptrs[14] = {dYq, dY, X, A, U, H, Wdq, Wguq, dX, dA, dU, AUq, dW_g, dW_u};
@@ -1281,6 +1284,8 @@ extern "C" int moe_expert_bwd_fp8(const uint8_t* dYq, const float* sdY, const mo
         P.K0 = 2 * f;
         P.sa = sAU;
         P.sb0 = sWgu;
+        P.r1_row = dl_rows;
+        P.r1_col = W_r;
         CUtensorMap mox[3];
         if (!out_maps(mox, dX, nullptr, nullptr, d, rows)) return MOE_ERR_LAUNCH;
         if (d % 256 == 0)

@@ -158,8 +158,8 @@ class MoEPlan:
             # its pace and the term costs more there than it saves (small fine-grained
             # layer, d_ff 256: 0.675 -> 0.681 ms per step), so short experts keep the term
             # in the token sum.
-            self.router_rows = (not s.fp8_dgrad and s.mode == ops.MODE_SIGMOID
-                                and not s.has_aux and s.f >= self.ROUTER_ROWS_MIN_FF)
+            self.router_rows = (s.mode == ops.MODE_SIGMOID and not s.has_aux
+                                and s.f >= self.ROUTER_ROWS_MIN_FF)
             self.dl_rows = torch.zeros((R,), dtype=f32, device=dev) if self.router_rows else None
             self.dx_r = _empty((T, d), f32, dev) if self.router_dx_tc else None
             self.dW_r = _empty((E, d), f32, dev)
@@ -311,10 +311,13 @@ class MoEPlan:
                                     self.dYq, self.sdY, stream)
             ops.moe_quantize_cols_fp8(W_d, None, self.Wdq_t, self.sWd_t, stream)
             ops.moe_quantize_cols_fp8(W_g, W_u, self.Wguq_t, self.sWgu_t, stream)
+            if self.router_rows:  # the gate gradient is known: the logit gradient first
+                self._route_bwd(x, None, stream)
             self._gemm(ops.moe_expert_bwd_fp8, self.dYq, self.sdY, self.dY_perm, self.X_perm,
                        self.A, self.U, self.H, self.row_offsets, self.Wdq_t, self.sWd_t,
                        self.Wguq_t, self.sWgu_t, self.dX_perm, self.dA, self.dU, self.AUq,
-                       self.sAU, self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream)
+                       self.sAU, self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
+                       dl_rows=self.dl_rows, W_r=W_r if self.router_rows else None)
         else:
             ops.moe_combine_bwd(dY, self.Y_perm, self.topk_gate, self.slot_to_row,
                                 self.row_offsets, self.perm_token, self.dY_perm, self.dg, stream)
@@ -329,12 +332,9 @@ class MoEPlan:
                                  s.aux_seq, self.dlogits_aux, stream)
             extra = self.dlogits_aux
         rows = self.router_rows
-        ops.moe_route_bwd(self.dg, x, self.topk_idx, self.topk_gate, self.topk_score,
-                          self.logits if softmax else None, self.lse if softmax else None, s.E,
-                          s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream,
-                          dlogits_extra=extra, slot_to_row=self.slot_to_row if rows else None,
-                          dl_rows=self.dl_rows)
-        if rows:
+        if not (rows and s.fp8_dgrad):  # (the FP8 path formed the logit gradient above)
+            self._route_bwd(x, extra, stream)
+        if rows and not s.fp8_dgrad:
             self._gemm(ops.moe_expert_bwd, self.dY_perm, self.X_perm, self.A, self.U, self.H,
                        self.row_offsets, W_g, W_u, W_d, self.dX_perm, self.dA, self.dU,
                        self.dW_g, self.dW_u, self.dW_d, self.ws, stream=stream,
@@ -355,6 +355,16 @@ class MoEPlan:
             ops.moe_permute_bwd(self.dX_perm, self.slot_to_row, dxs, self.dlogits, W_r, self.dx,
                                 stream)
         return self.dx
+
+    def _route_bwd(self, x, extra, stream):
+        s = self.s
+        softmax = s.mode == ops.MODE_SOFTMAX
+        rows = self.router_rows
+        ops.moe_route_bwd(self.dg, x, self.topk_idx, self.topk_gate, self.topk_score,
+                          self.logits if softmax else None, self.lse if softmax else None, s.E,
+                          s.mode, s.z_coef, self.dlogits, self.dW_r, self.ws, stream,
+                          dlogits_extra=extra, slot_to_row=self.slot_to_row if rows else None,
+                          dl_rows=self.dl_rows)
 
     def _shared_backward(self, dY, x, Ws_g, Ws_u, Ws_d, st):
         if self.s.fp8_dgrad:

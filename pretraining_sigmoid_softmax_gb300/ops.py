@@ -233,17 +233,19 @@ def moe_expert_bwd(dY, X, A, U, H, row_offsets, W_g, W_u, W_d, dX, dA, dU, dW_g,
 
 
 def moe_expert_bwd_fp8(dYq, sdY, dY, X, A, U, H, row_offsets, Wdq, sWd, Wguq, sWgu, dX, dA, dU,
-                       AUq, sAU, dW_g, dW_u, dW_d, ws, stream=None):
-    """Wdq [E, f, d] and Wguq [E, d, 2f]: moe_quantize_cols_fp8 of W_d and of W_g over W_u."""
+                       AUq, sAU, dW_g, dW_u, dW_d, ws, stream=None, dl_rows=None, W_r=None):
+    """Wdq [E, f, d] and Wguq [E, d, 2f]: moe_quantize_cols_fp8 of W_d and of W_g over W_u;
+    dl_rows with W_r: the router term in dX's rows (see the header)."""
     rows, d = X.shape
     E, f, _ = Wdq.shape
     _contig(dYq, sdY, dY, X, A, U, H, Wdq, sWd, Wguq, sWgu, dX, dA, dU, AUq, sAU, dW_g, dW_u,
-            dW_d, ws)
+            dW_d, ws, dl_rows, W_r)
     _check(_lib.load().moe_expert_bwd_fp8(_p(dYq), _p(sdY), _p(dY), _p(X), _p(A), _p(U), _p(H),
                                           _p(row_offsets), E, rows, d, f, _p(Wdq), _p(sWd),
                                           _p(Wguq), _p(sWgu), _p(dX), _p(dA), _p(dU), _p(AUq),
-                                          _p(sAU), _p(dW_g), _p(dW_u), _p(dW_d), _p(ws),
-                                          0 if ws is None else ws.numel(), _stream(stream)),
+                                          _p(sAU), _p(dW_g), _p(dW_u), _p(dW_d), _p(dl_rows),
+                                          _p(W_r), _p(ws), 0 if ws is None else ws.numel(),
+                                          _stream(stream)),
            "moe_expert_bwd_fp8")
 
 

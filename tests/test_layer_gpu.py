@@ -196,6 +196,8 @@ SMALL = [
     # dX rows
     MoEConfig("router_term_in_rows", T=400, d=256, E=5, k=2, f=768, f_shared=256,
               mode="sigmoid", seed=26, backward=True, bias_update=True),
+    MoEConfig("fp8_dgrad_router_term_in_rows", T=400, d=256, E=4, k=2, f=768, f_shared=256,
+              mode="sigmoid", seed=27, backward=True, bias_update=True, precision="fp8_dgrad"),
     # the widest router (SIMT logits and W_r gradient), most experts with 0-3 rows
     MoEConfig("widest_router_E256", T=300, d=256, E=256, k=8, f=128, f_shared=0,
               mode="softmax", seed=20, backward=True, bias_update=False, z_coef=1e-3),
@@ -389,7 +391,7 @@ def test_cuda_graph_replay_matches_eager_step():
 LAUNCH_CASES = [CONFIGS["C1"], CONFIGS["C2"]] + [
     c for c in SMALL if c.name in ("aux_losses_sigmoid", "aux_losses_softmax", "fp8_forward_shared",
                                    "fp8_dgrad_shared", "widest_router_E256", "one_expert_top1",
-                                   "router_term_in_rows")]
+                                   "router_term_in_rows", "fp8_dgrad_router_term_in_rows")]
 
 
 @pytest.mark.parametrize("cfg", LAUNCH_CASES, ids=lambda c: c.name)
