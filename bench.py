@@ -277,7 +277,7 @@ def run_reference(args, cfg):
     from pretraining_sigmoid_softmax_gb300.inputs import make_inputs
     inp = make_inputs(cfg)
     T_s = max(8, min(args.cpu_sample_tokens // 4, cfg.T))
-    rate, cores, times = cpu_oracle_rate(cfg, inp, T_s, steps=args.warmup + args.steps)
+    _, cores, times = cpu_oracle_rate(cfg, inp, T_s, steps=args.warmup + args.steps)
     timed = times[args.warmup:] or times
     ms = 1e3 * sum(timed) / len(timed)
     value = T_s / (ms / 1e3)

@@ -591,7 +591,7 @@ def slot_router_terms(dlogits: np.ndarray, idx: np.ndarray, W_r: np.ndarray) -> 
     """[T, k, d]: each chosen slot's share of the router's input gradient dl W_r, i.e.
     dl[t, idx[t, i]] W_r[idx[t, i]]. Their sum over the slots is dl W_r whenever dl is zero
     off the chosen experts."""
-    T, k = idx.shape
+    T = idx.shape[0]
     return dlogits[np.arange(T)[:, None], idx][:, :, None] * W_r[idx]
 
 

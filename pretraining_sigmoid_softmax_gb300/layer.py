@@ -287,7 +287,6 @@ class MoEPlan:
         s = self.s
         x = self.x
         W_r, b, W_g, W_u, W_d, Ws_g, Ws_u, Ws_d = self.W
-        softmax = s.mode == ops.MODE_SOFTMAX
         main = stream if stream is not None else torch.cuda.current_stream()
         if s.f_shared and self.overlap:  # fork: the shared expert's backward on the side stream
             self.side.wait_stream(main)
