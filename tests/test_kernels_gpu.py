@@ -161,7 +161,9 @@ def _permute(idx, x, E, gate=None):
 
 @pytest.mark.parametrize("T,d,E,k,skew", [(1000, 128, 8, 2, False), (3000, 256, 64, 8, True),
                                           (2049, 128, 256, 32, False), (5, 128, 16, 4, True),
-                                          (1, 128, 1, 1, False)])
+                                          (1, 128, 1, 1, False),
+                                          # 157 chunks of 256 tokens: runs of 4 or 5 per lane
+                                          (40100, 128, 64, 8, True)])
 def test_permute_is_bit_exact(T, d, E, k, skew):
     g = torch.Generator().manual_seed(T + E)
     idx = _random_choice(T, E, k, g, skew)
