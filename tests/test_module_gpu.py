@@ -20,6 +20,9 @@ SOFTMAX_ZLOSS = MoEConfig("module_softmax_zloss", T=1000, d=384, E=16, k=4, f=25
 SIGMOID_AUX = MoEConfig("module_sigmoid_aux_shared", T=1024, d=256, E=16, k=4, f=256,
                         f_shared=128, mode="sigmoid", seed=23, backward=True, bias_update=True,
                         aux_switch=1e-2, aux_seq=2e-2, seq_len=256)
+# experts long enough (d_ff 768) for the router's input-gradient term to ride in the dX rows
+SIGMOID_ROWS = MoEConfig("module_sigmoid_router_rows", T=512, d=256, E=4, k=2, f=768,
+                         f_shared=256, mode="sigmoid", seed=28, backward=True, bias_update=True)
 
 
 @pytest.fixture(autouse=True, scope="module")
@@ -38,7 +41,7 @@ def _module(cfg, inp):
     return layer
 
 
-@pytest.mark.parametrize("cfg", [CONFIGS["C1"], SOFTMAX_ZLOSS, SIGMOID_AUX],
+@pytest.mark.parametrize("cfg", [CONFIGS["C1"], SOFTMAX_ZLOSS, SIGMOID_AUX, SIGMOID_ROWS],
                          ids=lambda c: c.name)
 def test_module_backward_matches_the_plain_definition(cfg):
     inp = make_inputs(cfg)
@@ -50,6 +53,7 @@ def test_module_backward_matches_the_plain_definition(cfg):
     loss.backward()
     torch.cuda.synchronize()
     plan = layer._last_plan
+    assert plan.router_rows == (cfg.name == SIGMOID_ROWS.name)
     idx = plan.topk_idx.cpu().numpy().astype(np.int64)
     i64 = {k: O.to64(v) for k, v in inp.items() if k != "dY"}
     aux = (cfg.seq_len, cfg.aux_switch, cfg.aux_seq) if cfg.has_aux else None
