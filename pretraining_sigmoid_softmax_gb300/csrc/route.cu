@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) route_fwd_kernel(
             float v = -INFINITY;
             if (e < E) {
                 const float l = lg[r][e];
-                v = (mode == MOE_MODE_SIGMOID) ? sigmoid_f(l) + bias[e] : l;
+                v = (mode == MOE_MODE_SIGMOID) ? route_select_sigmoid(l) + bias[e] : l;
                 if (v != v) v = -INFINITY;  // a NaN never wins
             }
             val[j] = v;

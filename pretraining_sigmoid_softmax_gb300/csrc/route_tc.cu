@@ -20,9 +20,11 @@
 // back to back: a 3 epad-row operand) into a ring of stages; warp 1 issues one tcgen05.mma
 // (M = 128, N = 3 epad, K = 16; two of half the width when 3 epad > 256) per K step, which
 // leaves the three partial logits side by side in TMEM. Warps 4-7 each own 32 tokens (one
-// TMEM lane per token): a first pass adds the partials, writes the logits and parks logits
-// and selection values back in TMEM (tcgen05.st); then k passes each pick the best expert not
-// yet taken, in the order "larger value, then lower index" - the definition's total order.
+// TMEM lane per token): a first pass adds the partials and writes the logits. Sigmoid routing
+// with k <= 8 (its own kernel instance) pushes each expert into an insertion network as it
+// goes and is done after that pass; otherwise the pass parks logits and selection values back
+// in TMEM (tcgen05.st) and k passes each pick the best expert not yet taken. Both follow the
+// order "larger value, then lower index" - the definition's total order.
 //
 // dW_r kernel: the transposed product dW_r^T[j][e] = sum_t x[t][j] dlogits[t][e], as
 // 128-column tiles of d (M) by np experts (N), K running over tokens. The token axis is
@@ -189,20 +191,20 @@ struct LogitCfg {
     static_assert(STAGES >= 2, "pipeline depth");
 };
 
-// One token's choice from its three partial logits in TMEM (columns [0, EPAD), [EPAD,
-// 2 EPAD), [2 EPAD, 3 EPAD) of its lane). A first pass adds the partials, writes the logits,
-// and parks each logit and selection value (sigmoid + bias, or the logit) back in TMEM; the
-// k choice passes then read those. Executed by all 32 lanes of the warp together
-// (tcgen05.ld/st are warp-collective); `live` masks the stores of rows past the last token.
-template <int EPAD>
-__device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool live,
-                                                 const LogitParams& P, const float* sbias) {
+// Widest choice made by the insertion network (RouteTopK) in one pass.
+constexpr int kNetK = 8;
+
+// The first pass over one token's three partial logits in TMEM (columns [0, EPAD), [EPAD,
+// 2 EPAD), [2 EPAD, 3 EPAD) of its lane), 32 experts at a time: adds the partials into the
+// logit l, forms the selection value (sigmoid(l) + b, or l; a NaN never wins), calls
+// f(e, l, value) for every expert e < E in increasing order, and writes the logits row.
+// Executed by all 32 lanes of the warp together (tcgen05.ld is warp-collective); `live`
+// masks the stores of rows past the last token.
+template <int EPAD, typename F>
+__device__ __forceinline__ void route_first_pass(uint32_t t_acc, int64_t t, bool live, bool sig,
+                                                 const LogitParams& P, const float* sbias, F&& f) {
     constexpr int NCH = EPAD / 32;
-    const int E = P.E, k = P.k;
-    const bool sig = P.mode == MOE_MODE_SIGMOID;
-    const uint32_t t_l = t_acc;          // logits (over the first partial)
-    const uint32_t t_v = t_acc + EPAD;   // selection values (over the second)
-    float mx = -INFINITY, sum = 0.f;
+    const int E = P.E;
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
         uint32_t p0[32], p1[32], p2[32];
@@ -215,9 +217,8 @@ __device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool
         for (int j = 0; j < 32; ++j) {
             const int e = 32 * c + j;
             const float l = (__uint_as_float(p0[j]) + __uint_as_float(p1[j])) + __uint_as_float(p2[j]);
-            float val = sig ? route_sigmoid(l) + sbias[e] : l;
-            if (val != val) val = -INFINITY;  // a NaN never wins
-            if (!sig && e < E) mx = fmaxf(mx, l);
+            float val = sig ? route_select_sigmoid(l) + sbias[e] : l;
+            if (val != val) val = -INFINITY;
             lv[j] = __float_as_uint(l);
             vv[j] = __float_as_uint(val);
         }
@@ -236,9 +237,68 @@ __device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool
                     if (32 * c + j < E) row[32 * c + j] = __uint_as_float(lv[j]);
             }
         }
+        f(c, lv, vv);
+    }
+}
+
+// Sigmoid routing with k <= kNetK: one pass pushes each expert, in index order, into a
+// kNetK-slot insertion network, which leaves the k best in the choice's order ("larger
+// value, then lower index"); scores are the sigmoids of their logits, gates the scores over
+// their sum.
+template <int EPAD>
+__device__ __forceinline__ void route_epilogue_net(uint32_t t_acc, int64_t t, bool live,
+                                                   const LogitParams& P, const float* sbias) {
+    const int E = P.E, k = P.k;
+    RouteTopK<kNetK> top;
+    top.init();
+    route_first_pass<EPAD>(t_acc, t, live, true, P, sbias, [&](int c, const uint32_t (&lv)[32], const uint32_t (&vv)[32]) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (32 * c + j < E) top.push(route_key(__uint_as_float(vv[j])), 32 * c + j, __uint_as_float(lv[j]));
+    });
+    if (!live) return;
+    int32_t* oi = P.topk_idx + t * k;
+    float* os = P.topk_score + t * k;
+    float* og = P.topk_gate + t * k;
+    float sc[kNetK];
+    float ssum = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNetK; ++i) {
+        sc[i] = 0.f;
+        if (i < k) {
+            sc[i] = route_sigmoid(top.l[i]);
+            ssum += sc[i];
+            oi[i] = top.e[i];
+            os[i] = sc[i];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kNetK; ++i)
+        if (i < k) og[i] = sc[i] / ssum;
+}
+
+// Every other router (softmax, or k > kNetK): the first pass parks each logit and selection
+// value back in TMEM (tcgen05.st), then k passes each pick the best expert not yet taken, in
+// the order "larger value, then lower index" - the definition's total order. Softmax also
+// forms the normaliser over all experts and returns lse^2 for the z-loss.
+template <int EPAD>
+__device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool live,
+                                                 const LogitParams& P, const float* sbias) {
+    constexpr int NCH = EPAD / 32;
+    const int E = P.E, k = P.k;
+    const bool sig = P.mode == MOE_MODE_SIGMOID;
+    const uint32_t t_l = t_acc;          // logits (over the first partial)
+    const uint32_t t_v = t_acc + EPAD;   // selection values (over the second)
+    float mx = -INFINITY, sum = 0.f;
+    route_first_pass<EPAD>(t_acc, t, live, sig, P, sbias, [&](int c, uint32_t (&lv)[32], uint32_t (&vv)[32]) {
+        if (!sig) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (32 * c + j < E) mx = fmaxf(mx, __uint_as_float(lv[j]));
+        }
         tmem_st32(t_l + 32 * c, lv);
         tmem_st32(t_v + 32 * c, vv);
-    }
+    });
     tmem_st_wait();
     if (!sig) {  // softmax normaliser over all experts
 #pragma unroll
@@ -299,7 +359,7 @@ __device__ __forceinline__ double route_epilogue(uint32_t t_acc, int64_t t, bool
     return live ? (double)l_se * (double)l_se : 0.0;
 }
 
-template <int EPAD>
+template <int EPAD, bool NET>
 __global__ void __launch_bounds__(kTcThreads, 1)
     route_logits_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw,
                            const LogitParams P) {
@@ -397,7 +457,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint32_t t_acc = tmem_base + buf * C::NTOT + ((uint32_t)(32 * q) << 16);
             const int64_t t = tile * 128 + 32 * q + lane;
-            double z = route_epilogue<EPAD>(t_acc, t, t < P.T, P, sbias);
+            double z = 0.0;
+            if constexpr (NET)
+                route_epilogue_net<EPAD>(t_acc, t, t < P.T, P, sbias);
+            else
+                z = route_epilogue<EPAD>(t_acc, t, t < P.T, P, sbias);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&R.tempty[buf]));
@@ -415,7 +479,8 @@ template <int EPAD>
 int launch_logits(const CUtensorMap& mx, const CUtensorMap& mw, const LogitParams& P, cudaStream_t st) {
     using C = LogitCfg<EPAD>;
     static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
-    auto kern = route_logits_tc_kernel<EPAD>;
+    const bool net = P.mode == MOE_MODE_SIGMOID && P.k <= kNetK;
+    auto kern = net ? route_logits_tc_kernel<EPAD, true> : route_logits_tc_kernel<EPAD, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES) !=
         cudaSuccess)
         return MOE_ERR_LAUNCH;

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -15,6 +16,61 @@ __device__ __forceinline__ bool route_better(float v1, int e1, float v2, int e2)
 }
 
 __device__ __forceinline__ float route_sigmoid(float l) { return 1.0f / (1.0f + expf(-l)); }
+
+// The sigmoid inside the selection value sigmoid(l) + b, which only orders experts: the
+// exponential and reciprocal by the hardware approximations (__expf, __fdividef) instead of
+// the correctly rounded expf and division. Over all l its absolute error stays within a few
+// 1e-7 (the relative error of __expf grows with |l|, but sigmoid's slope e^-|l| shrinks
+// faster), so it can reorder only experts whose values lie that close; the scores and gates
+// of the chosen experts use route_sigmoid. For l < -88, __expf(-l) is +inf and the value 0.
+__device__ __forceinline__ float route_select_sigmoid(float l) {
+    return __fdividef(1.0f, 1.0f + __expf(-l));
+}
+
+// Order-preserving integer key of a selection value: for non-NaN a and b, a > b exactly when
+// route_key(a) > route_key(b) as signed integers, and a == b exactly when the keys are equal
+// (-0 is folded into +0 first, as the float order has them equal). Positive floats keep their
+// bits; for negative ones the magnitude bits are flipped, so a larger magnitude sorts lower.
+// No non-NaN value has the key INT_MIN, which marks an empty slot.
+__device__ __forceinline__ int route_key(float v) {
+    const int b = __float_as_int(v + 0.0f);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
+
+// The K best experts among those pushed so far, best first, in the choice's order. Experts
+// must be pushed in increasing index order: a later expert then displaces an earlier one only
+// with a strictly larger value, so equal values keep the lower index ahead, and an empty slot
+// (key INT_MIN) loses to every expert. A push compares the new key with all K slots at once
+// and shifts the slots below its place down by one (an insertion network: branch-free, a
+// fixed number of compares and selects). Each slot also carries the expert's logit.
+template <int K>
+struct RouteTopK {
+    int key[K];
+    int e[K];
+    float l[K];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            key[j] = INT_MIN;
+            e[j] = 0;
+            l[j] = 0.f;
+        }
+    }
+    __device__ __forceinline__ void push(int ck, int ce, float cl) {
+        bool b[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) b[j] = ck > key[j];  // true from the new expert's place down
+#pragma unroll
+        for (int j = K - 1; j > 0; --j) {
+            key[j] = b[j] ? (b[j - 1] ? key[j - 1] : ck) : key[j];
+            e[j] = b[j] ? (b[j - 1] ? e[j - 1] : ce) : e[j];
+            l[j] = b[j] ? (b[j - 1] ? l[j - 1] : cl) : l[j];
+        }
+        key[0] = b[0] ? ck : key[0];
+        e[0] = b[0] ? ce : e[0];
+        l[0] = b[0] ? cl : l[0];
+    }
+};
 
 // Three bf16 pieces of an fp32 value: p0 = bf16(v), p1 = bf16(v - p0), p2 = bf16(v - p0 - p1).
 // Both differences are exact in fp32 (Sterbenz: each piece is within a factor 2 of what it

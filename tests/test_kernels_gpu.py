@@ -49,6 +49,8 @@ ROUTE_CASES = [
     (64, 128, 1, 1, "sigmoid"),
     (200, 128, 5, 5, "softmax"),
     (65, 128, 200, 3, "sigmoid"),
+    (400, 256, 64, 12, "sigmoid"),   # tensor-core kernel, choice wider than the network
+    (333, 128, 40, 7, "sigmoid"),    # network over a ragged expert tile
 ]
 
 
@@ -87,7 +89,7 @@ def test_route_matches_oracle(T, d, E, k, mode):
 
 @pytest.mark.parametrize("T,d,E,k,mode", [(1000, 256, 64, 8, "sigmoid"), (500, 128, 64, 5, "sigmoid"),
                                          (777, 256, 32, 5, "softmax"), (400, 128, 24, 3, "sigmoid"),
-                                         (300, 128, 128, 7, "sigmoid")])
+                                         (300, 128, 128, 7, "sigmoid"), (400, 128, 64, 11, "sigmoid")])
 def test_route_breaks_exact_ties_by_lower_index(T, d, E, k, mode):
     """Experts 2j and 2j + 1 have identical router rows (and biases), so every selection value
     has an exact twin: the choice must take the lower index first, as the definition's order
@@ -116,6 +118,30 @@ def test_route_breaks_exact_ties_by_lower_index(T, d, E, k, mode):
         for e, i in pos.items():
             if e % 2 == 1:
                 assert e - 1 in pos and pos[e - 1] < i, (t, idx[t])
+
+
+@pytest.mark.parametrize("E,k", [(64, 8), (128, 8), (64, 12)])
+def test_route_saturated_logits(E, k):
+    """Logits far outside sigmoid's working range (|l| up to a few hundred): the sigmoid
+    saturates at 0 and 1 in fp32, so the bias decides among the saturated experts. The
+    choice must match the oracle's on the GPU's own logits wherever the values are not near
+    a tie, and the scores the fp32 sigmoid of those logits. The biases are evenly spaced (in
+    shuffled order), so experts saturated at the same end never tie on the bias."""
+    g = torch.Generator().manual_seed(E + k)
+    T, d = 700, 256
+    x = randn_bf16((T, d), g)
+    W_r = torch.randn(E, d, generator=g) * (60.0 * d ** -0.5)
+    b = (torch.arange(E, dtype=torch.float32) * (0.1 / E) - 0.05)[torch.randperm(E, generator=g)]
+    r = _route(x, W_r, b, k, ops.MODE_SIGMOID, 0.0)
+    lg = h64(r["logits"])
+    assert np.abs(lg).max() > 100.0
+    ref = O.route(lg, "sigmoid", k, h64(b), 0.0)
+    near = O.near_tie_tokens(ref["select_value"], k)
+    assert near.mean() < 0.01
+    idx = r["idx"].cpu().numpy()
+    assert (idx[~near] == ref["idx"][~near]).all(), "expert choice differs from the oracle"
+    np.testing.assert_allclose(h64(r["score"])[~near], ref["score"][~near], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(h64(r["gate"])[~near], ref["gate"][~near], rtol=1e-5, atol=1e-6)
 
 
 def test_route_is_bitwise_repeatable():
