@@ -28,7 +28,7 @@ METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOP/s as % of GB300 BF16 pe
 # DRAM bytes (read + write) of one step's grouped-GEMM launches, summed from a stored ncu
 # capture of the current kernels at that workload (not measured by this run; the line says
 # so); workloads without a capture report null.
-MEASURED_GEMM_TRAFFIC = {"C4": 109.52e9}
+MEASURED_GEMM_TRAFFIC = {"C4": 144.04e9}
 # Datasheet dense peaks of a GB300 (not from the source pages), reported beside the measured
 # ones: bf16 2250 TFLOP/s (fp8 twice that), HBM3e about 8 TB/s.
 NOMINAL_BF16_TFLOPS = 2250.0
