@@ -51,6 +51,11 @@ ROUTE_CASES = [
     (65, 128, 200, 3, "sigmoid"),
     (400, 256, 64, 12, "sigmoid"),   # tensor-core kernel, choice wider than the network
     (333, 128, 40, 7, "sigmoid"),    # network over a ragged expert tile
+    # larger layers: more tiles than CTAs in some, long reductions over d in all
+    (8192, 1024, 64, 8, "sigmoid"),
+    (2000, 2048, 32, 4, "softmax"),
+    (20000, 1024, 128, 8, "sigmoid"),  # a ragged last wave of tiles
+    (4000, 1024, 64, 12, "sigmoid"),
 ]
 
 
@@ -89,7 +94,8 @@ def test_route_matches_oracle(T, d, E, k, mode):
 
 @pytest.mark.parametrize("T,d,E,k,mode", [(1000, 256, 64, 8, "sigmoid"), (500, 128, 64, 5, "sigmoid"),
                                          (777, 256, 32, 5, "softmax"), (400, 128, 24, 3, "sigmoid"),
-                                         (300, 128, 128, 7, "sigmoid"), (400, 128, 64, 11, "sigmoid")])
+                                         (300, 128, 128, 7, "sigmoid"), (400, 128, 64, 11, "sigmoid"),
+                                         (3000, 1024, 64, 8, "sigmoid")])
 def test_route_breaks_exact_ties_by_lower_index(T, d, E, k, mode):
     """Experts 2j and 2j + 1 have identical router rows (and biases), so every selection value
     has an exact twin: the choice must take the lower index first, as the definition's order
@@ -144,10 +150,11 @@ def test_route_saturated_logits(E, k):
     np.testing.assert_allclose(h64(r["gate"])[~near], ref["gate"][~near], rtol=1e-5, atol=1e-6)
 
 
-def test_route_is_bitwise_repeatable():
+@pytest.mark.parametrize("T,d", [(2000, 512), (8192, 1024), (20000, 1024)])
+def test_route_is_bitwise_repeatable(T, d):
     g = torch.Generator().manual_seed(5)
-    x = randn_bf16((2000, 512), g)
-    W_r = torch.randn(64, 512, generator=g) * 512 ** -0.5
+    x = randn_bf16((T, d), g)
+    W_r = torch.randn(64, d, generator=g) * d ** -0.5
     b = torch.rand(64, generator=g) * 0.1 - 0.05
     r1 = _route(x, W_r, b, 8, ops.MODE_SIGMOID, 0.0)
     r2 = _route(x, W_r, b, 8, ops.MODE_SIGMOID, 0.0)
