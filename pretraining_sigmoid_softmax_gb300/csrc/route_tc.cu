@@ -241,21 +241,39 @@ __device__ __forceinline__ void route_first_pass(uint32_t t_acc, int64_t t, bool
     }
 }
 
-// Sigmoid routing with k <= kNetK: one pass pushes each expert, in index order, into a
-// kNetK-slot insertion network, which leaves the k best in the choice's order ("larger
-// value, then lower index"); scores are the sigmoids of their logits, gates the scores over
-// their sum.
+// Sigmoid routing with k <= kNetK: the first pass parks each expert's logit and selection key
+// in TMEM (over the consumed accumulator); a rolled loop then reads them back eight experts
+// at a time and pushes each, in index order, into a kNetK-slot insertion network, which
+// leaves the k best in the choice's order ("larger value, then lower index"). Scores are the
+// sigmoids of their logits, gates the scores over their sum. The loop is kept rolled so the
+// epilogue's code stays small: fully unrolled over 64 or 128 experts it is tens of KB of
+// straight-line code per tile, which competes with the producer's and MMA issuer's loops for
+// the instruction cache.
 template <int EPAD>
 __device__ __forceinline__ void route_epilogue_net(uint32_t t_acc, int64_t t, bool live,
                                                    const LogitParams& P, const float* sbias) {
     const int E = P.E, k = P.k;
+    const uint32_t t_l = t_acc;         // logits (over the first partial)
+    const uint32_t t_v = t_acc + EPAD;  // selection keys (over the second)
+    route_first_pass<EPAD>(t_acc, t, live, true, P, sbias, [&](int c, uint32_t (&lv)[32], uint32_t (&vv)[32]) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vv[j] = (uint32_t)route_key(__uint_as_float(vv[j]));
+        tmem_st32(t_l + 32 * c, lv);
+        tmem_st32(t_v + 32 * c, vv);
+    });
+    tmem_st_wait();
     RouteTopK<kNetK> top;
     top.init();
-    route_first_pass<EPAD>(t_acc, t, live, true, P, sbias, [&](int c, const uint32_t (&lv)[32], const uint32_t (&vv)[32]) {
+#pragma unroll 1
+    for (int e0 = 0; e0 < E; e0 += 8) {
+        uint32_t kv[8], lv[8];
+        tmem_ld8(t_v + e0, kv);
+        tmem_ld8(t_l + e0, lv);
+        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (32 * c + j < E) top.push(route_key(__uint_as_float(vv[j])), 32 * c + j, __uint_as_float(lv[j]));
-    });
+        for (int j = 0; j < 8; ++j)
+            if (e0 + j < E) top.push((int)kv[j], e0 + j, __uint_as_float(lv[j]));
+    }
     if (!live) return;
     int32_t* oi = P.topk_idx + t * k;
     float* os = P.topk_score + t * k;
