@@ -20,11 +20,11 @@
 // back to back: a 3 epad-row operand) into a ring of stages; warp 1 issues one tcgen05.mma
 // (M = 128, N = 3 epad, K = 16; two of half the width when 3 epad > 256) per K step, which
 // leaves the three partial logits side by side in TMEM. Warps 4-7 each own 32 tokens (one
-// TMEM lane per token): a first pass adds the partials and writes the logits. Sigmoid routing
-// with k <= 8 (its own kernel instance) pushes each expert into an insertion network as it
-// goes and is done after that pass; otherwise the pass parks logits and selection values back
-// in TMEM (tcgen05.st) and k passes each pick the best expert not yet taken. Both follow the
-// order "larger value, then lower index" - the definition's total order.
+// TMEM lane per token): a first pass adds the partials, writes the logits and parks each
+// logit and selection value (or key) back in TMEM (tcgen05.st). Sigmoid routing with k <= 8
+// (its own kernel instance) then reads them back eight experts at a time into an insertion
+// network; otherwise k passes each pick the best expert not yet taken. Both follow the order
+// "larger value, then lower index" - the definition's total order.
 //
 // dW_r kernel: the transposed product dW_r^T[j][e] = sum_t x[t][j] dlogits[t][e], as
 // 128-column tiles of d (M) by np experts (N), K running over tokens. The token axis is
